@@ -1,0 +1,447 @@
+"""Benchmark of the fused row reductions on one GB300 (or N weak-scaled replicas).
+
+One step = one pass of the whole hot path over one batch of synthetic input,
+every input already resident in HBM:
+  1. LayerNorm forward,  fp32, 4096 x 768  (x = N(0,1) + U(-10,10) per row)
+  2. causal attention-score softmax, bf16, 65536 x 512 (scores ~ N(0, 4^2), key > query = -inf)
+  3. LayerNorm backward, fp32, 4096 x 768 (+ the fixed-order dgamma / dbeta pass)
+  4. LM-head softmax cross-entropy fwd+bwd, bf16, 16384 x 50304 (logits ~ N(0, 3^2),
+     5% labels = -100), per-row fp32 loss, dlogits written in place
+The metric is achieved HBM bandwidth: algorithmic (minimum) bytes of the step
+divided by its device time.  The 3.3 GB cross-entropy pass streams far more
+than the 129 MB L2 through the chip every step, so each step starts with a
+cold L2 for its inputs.
+
+Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle
+(the reference implementation of the same arithmetic) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from row_reduction_pass_gb300 import synth  # noqa: E402
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) for softmax-xent & LayerNorm fwd+bwd"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("hot-path step: LN fwd+bwd fp32 4096x768 + causal softmax fwd bf16 65536x512 + "
+            "softmax-xent fwd+bwd bf16 16384x50304 (in place, 5% ignored)")
+
+
+# ------------------------------------------------------------ byte counts ----
+
+def ln_bytes(rows, cols, e):
+    fwd = 2 * rows * cols * e + 2 * cols * e + 8 * rows          # x, y, gamma, beta, mean, rstd
+    bwd = 3 * rows * cols * e + 3 * cols * e + 8 * rows          # dy, x, dx, gamma, dg, db, mean, rstd
+    return fwd, bwd
+
+
+def softmax_bytes(rows, cols, e):
+    return 2 * rows * cols * e
+
+
+def xent_bytes(rows, cols, e, n_ignored):
+    """Minimum traffic: ignored rows are only written (zeros), others read + written."""
+    return (2 * (rows - n_ignored) + n_ignored) * cols * e + 8 * rows
+
+
+# ----------------------------------------------------------------- clocks ----
+
+_REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+                0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+                0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,"
+                 "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 3:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                bits = int(parts[2], 16) if parts[2].startswith("0x") else int(parts[2])
+            except ValueError:
+                continue
+            for b, name in _REASON_BITS.items():
+                if bits & b and name != "gpu_idle":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ peaks ----
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                d = json.load(f)
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_gb_s"):
+                if k in d and d[k]:
+                    return float(d[k]), "measured"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "row_reduction_pass_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(key: str):
+    """DRAM bytes per launch of `key` from profiles/traffic.txt, if taken on the
+    current kernel sources (a line: key bytes source-hash)."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    cur = kernel_source_hash()
+    with open(p) as f:
+        for ln in f:
+            parts = ln.split()
+            if len(parts) >= 3 and parts[0] == key and parts[2] == cur:
+                return float(parts[1])
+    return None
+
+
+# ------------------------------------------------------------- the workload --
+
+def make_inputs(scale_rows: float = 1.0):
+    """Host arrays of the step's four workloads (rows scaled for samples)."""
+    ln = synth.make("ln_f32_4096x768", rows=max(1, int(4096 * scale_rows)))
+    sm = synth.make("softmax_bf16_causal_65536x512")
+    if scale_rows < 1.0:
+        sm["x"] = sm["x"][:max(1, int(65536 * scale_rows))]
+    xe = synth.make("xent_bf16_16384x50304", rows=max(1, int(16384 * scale_rows)))
+    return ln, sm, xe
+
+
+def step_bytes(ln, sm, xe):
+    r, c = ln["x"].shape
+    lf, lb = ln_bytes(r, c, 4)
+    sb = softmax_bytes(*sm["x"].shape, 2)
+    n_ign = int((xe["labels"] == synth.IGNORE_INDEX).sum())
+    xb = xent_bytes(*xe["logits"].shape, 2, n_ign)
+    return {"ln_fwd": lf, "softmax": sb, "ln_bwd": lb, "xent": xb}
+
+
+def run_ours(args, rank, world):
+    import torch
+    import row_reduction_pass_gb300 as rr
+
+    torch.cuda.set_device(rank % max(1, torch.cuda.device_count()))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    rr.load_library()
+    ln, sm, xe = make_inputs()
+    nbytes = step_bytes(ln, sm, xe)
+    total_bytes = sum(nbytes.values())
+
+    def bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+
+    # pinned host copies (for the end-to-end leg) and device-resident inputs
+    h = {
+        "ln_x": torch.from_numpy(ln["x"]).pin_memory(),
+        "ln_g": torch.from_numpy(ln["gamma"]).pin_memory(),
+        "ln_b": torch.from_numpy(ln["beta"]).pin_memory(),
+        "ln_dy": torch.from_numpy(ln["dy"]).pin_memory(),
+        "sm_x": bf16(sm["x"]).pin_memory(),
+        "xe_x": bf16(xe["logits"]).pin_memory(),
+        "xe_l": torch.from_numpy(xe["labels"]).pin_memory(),
+    }
+    d = {k: v.to(dev) for k, v in h.items()}
+    R, C = ln["x"].shape
+    o = {
+        "ln_y": torch.empty_like(d["ln_x"]), "ln_mean": torch.empty(R, device=dev),
+        "ln_rstd": torch.empty(R, device=dev), "ln_dx": torch.empty_like(d["ln_x"]),
+        "ln_dg": torch.empty_like(d["ln_g"]), "ln_db": torch.empty_like(d["ln_g"]),
+        "sm_y": torch.empty_like(d["sm_x"]),
+        "xe_loss": torch.empty(xe["logits"].shape[0], device=dev),
+    }
+    ws = torch.empty(rr.rr_layernorm_bwd_workspace_size(R, C, torch.float32), dtype=torch.uint8,
+                     device=dev)
+    eps = ln["eps"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        rr.rr_layernorm_fwd(d["ln_x"], d["ln_g"], d["ln_b"], o["ln_y"], o["ln_mean"],
+                            o["ln_rstd"], eps=eps)
+        if ev is not None:
+            ev[1].record()
+        rr.rr_softmax_fwd(d["sm_x"], o["sm_y"])
+        if ev is not None:
+            ev[2].record()
+        rr.rr_layernorm_bwd(d["ln_dy"], d["ln_x"], o["ln_mean"], o["ln_rstd"], d["ln_g"],
+                            o["ln_dx"], o["ln_dg"], o["ln_db"], ws)
+        if ev is not None:
+            ev[3].record()
+        rr.rr_softmax_xent_fwd_bwd(d["xe_x"], d["xe_l"], o["xe_loss"], d["xe_x"])  # in place
+        if ev is not None:
+            ev[4].record()
+
+    launches_per_step = 5  # LN fwd, softmax, LN bwd rows + column pass, xent
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_start.record()
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ms = t_start.elapsed_time(t_end)
+    per = {k: [] for k in ("ln_fwd", "softmax", "ln_bwd", "xent")}
+    for e in evs:
+        per["ln_fwd"].append(e[0].elapsed_time(e[1]))
+        per["softmax"].append(e[1].elapsed_time(e[2]))
+        per["ln_bwd"].append(e[2].elapsed_time(e[3]))
+        per["xent"].append(e[3].elapsed_time(e[4]))
+    err = rr.rr.rr_read_device_error(torch.cuda.current_device())
+
+    # end to end through the public API with host buffers: H2D of every input,
+    # the step, D2H of the per-row loss and of dgamma / dbeta.
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    loss_h = torch.empty_like(o["xe_loss"], device="cpu").pin_memory()
+    dg_h = torch.empty_like(o["ln_dg"], device="cpu").pin_memory()
+    db_h = torch.empty_like(o["ln_db"], device="cpu").pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = sum(v.numel() * v.element_size() for v in (loss_h, dg_h, db_h))
+
+    def e2e_step():
+        for k, v in h.items():
+            d[k].copy_(v, non_blocking=True)
+        step()
+        loss_h.copy_(o["xe_loss"], non_blocking=True)
+        dg_h.copy_(o["ln_dg"], non_blocking=True)
+        db_h.copy_(o["ln_db"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record()
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+
+    # max over ranks
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    ms_step = ms / args.steps
+    peak, peak_src = hbm_peak()
+    value = world * total_bytes / (ms_step * 1e-3) / 1e9
+    x_ms = statistics.mean(per["xent"])
+    x_gbs = nbytes["xent"] / (x_ms * 1e-3) / 1e9
+    kernels = {}
+    for k in per:
+        t = statistics.median(per[k])
+        kernels[k] = {"ms_median": round(t, 5), "bytes": nbytes[k],
+                      "gbs": round(nbytes[k] / (t * 1e-3) / 1e9, 1),
+                      "frac_of_peak": round(nbytes[k] / (t * 1e-3) / 1e9 / peak, 4)}
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16+f32 I/O, f32 accumulate",
+        "data": "synthetic (seeded numpy PCG64, recipes in row_reduction_pass_gb300/synth.py)",
+        "config": {"workload": WORKLOAD, "bytes_per_step": total_bytes,
+                   "l2": "inputs larger than L2: the 3.3 GB xent pass streams through the "
+                         "129 MB L2 every step", "frac_of_peak": round(value / world / peak, 4),
+                   "parallelism": f"replicas x{world} (rows are independent; no collective)"},
+        "kernels": kernels,
+        "roofline": {"bound": "hbm", "achieved": round(x_gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(x_gbs / peak, 4),
+                     "traffic": recorded_traffic("xent_bf16_16384x50304"),
+                     "kernel": "row_kernel<OpSoftmaxXent bf16 chunks, staged> (xent 16384x50304)",
+                     "peak_source": peak_src},
+        "clocks": clk.summary(),
+        "e2e": {"value": round(world * total_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "device_error_word": err,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return out
+
+
+# ------------------------------------------------------- CPU oracle timing --
+
+def _oracle_sample(frac):
+    """Run the oracle over `frac` of every workload of the step; returns
+    (algorithmic bytes of the sample, seconds)."""
+    import oracle
+    ln, sm, xe = make_inputs(scale_rows=frac)
+    nb = sum(step_bytes(ln, sm, xe).values())
+    t0 = time.perf_counter()
+    _, mean, rstd = oracle.ln_fwd(ln["x"], ln["gamma"], ln["beta"], ln["eps"])
+    oracle.softmax(sm["x"])
+    oracle.ln_bwd(ln["dy"], ln["x"], mean, rstd, ln["gamma"])
+    oracle.xent(xe["logits"], xe["labels"])
+    return nb, time.perf_counter() - t0
+
+
+def cpu_baseline(seconds: float):
+    frac = 1 / 512
+    nb, t = _oracle_sample(frac)
+    if t < seconds / 4:
+        frac = min(1.0, frac * seconds / max(t, 1e-3) / 2)
+        nb, t = _oracle_sample(frac)
+    return {"value": round(nb / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"float64 C oracle, single thread, on {frac:.4%} of the rows of every "
+                      f"workload of the step ({nb / 1e6:.1f} MB algorithmic) in {t:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    # per-step sample sized so warmup + steps finish within ~2 minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    frac = 1 / 2048
+    nb, t = _oracle_sample(frac)
+    frac = max(1 / 65536, min(1.0, frac * budget / max(t, 1e-4)))
+    import oracle  # noqa: F401
+    ln, sm, xe = make_inputs(scale_rows=frac)
+    nb = sum(step_bytes(ln, sm, xe).values())
+    import oracle as orc
+    for _ in range(args.warmup):
+        _, m, r = orc.ln_fwd(ln["x"], ln["gamma"], ln["beta"], ln["eps"])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _, m, r = orc.ln_fwd(ln["x"], ln["gamma"], ln["beta"], ln["eps"])
+        orc.softmax(sm["x"])
+        orc.ln_bwd(ln["dy"], ln["x"], m, r, ln["gamma"])
+        orc.xent(xe["logits"], xe["labels"])
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = nb * args.steps / tot / 1e9
+    sample = (f"float64 C oracle, single thread, {frac:.5%} of the rows of every workload "
+              f"per step ({nb / 1e6:.2f} MB algorithmic per step)")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic (same seeded generators, row sample)",
+            "config": {"workload": WORKLOAD, "sample_fraction": frac},
+            "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    out = run_ours(args, rank, world)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

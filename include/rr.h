@@ -1,0 +1,148 @@
+/*
+ * rr.h -- C ABI of librr.so: single-pass fused row reductions for GB300 (sm_103a).
+ *
+ * Operations (definitions from "Engineering a CUDA Machine Learning Framework
+ * from Scratch", sec. 3.1 "Online FlashSoftmax", sec. 3.2 "Welford
+ * Single-Pass Normalization", sec. 2.1 (loss gradients fused into registers)
+ * and sec. 2.2 (pre-derived analytic backward); cross-entropy as in the
+ * "gpu-ml-learning" README, Module 3):
+ *   rr_softmax_fwd           y = softmax(x) per row
+ *   rr_softmax_xent_fwd_bwd  per-row cross-entropy loss and dlogits = softmax - onehot
+ *   rr_layernorm_fwd         y = (x - mean) * rstd * gamma + beta, saving mean / rstd
+ *   rr_layernorm_bwd         dx, dgamma, dbeta from the saved mean / rstd
+ *
+ * Common conventions
+ *   - Every tensor is dense, row-major [rows x cols] with row stride = cols
+ *     (per-column vectors are [cols], per-row vectors are [rows]).
+ *   - Every pointer is a DEVICE pointer on the current CUDA device, allocated
+ *     and owned by the caller; the library allocates nothing and keeps no state
+ *     beyond a per-device cache of attributes.  Any alignment is accepted;
+ *     16-byte aligned bases and rows whose byte length is a multiple of 16 take
+ *     the vectorised path.
+ *   - `dtype` (RR_F32 or RR_BF16) is the storage type of x, y, logits, dlogits,
+ *     gamma, beta, dy, dx, dgamma and dbeta.  mean, rstd and loss are always
+ *     float32 and labels int32.  Arithmetic is float32 on the GPU.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).
+ *     Argument errors are returned synchronously and nothing is launched;
+ *     launch errors are returned as RR_ERR_CUDA (detail string from
+ *     rr_last_error_detail()); faults during execution surface at the caller's
+ *     next synchronisation.  No C++ exception crosses this ABI.
+ *   - rows == 0 is a no-op returning RR_OK.  cols must be >= 1.
+ *   - Waits inside the kernels are bounded; a wait that gives up records
+ *     RR_ERR_DEVICE_TIMEOUT in a per-device error word read by
+ *     rr_read_device_error(), and the kernel returns instead of hanging.
+ */
+#ifndef RR_H
+#define RR_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { RR_F32 = 0, RR_BF16 = 1 } rr_dtype;
+
+typedef enum {
+    RR_OK = 0,
+    RR_ERR_INVALID_ARG = 1,         /* null pointer, negative size, cols == 0, bad eps */
+    RR_ERR_UNSUPPORTED_DTYPE = 2,
+    RR_ERR_ALIASING = 3,            /* partial overlap of an input and an output */
+    RR_ERR_WORKSPACE_TOO_SMALL = 4,
+    RR_ERR_CUDA = 5,                /* a CUDA runtime call failed */
+    RR_ERR_DEVICE_TIMEOUT = 6       /* a bounded device-side wait gave up */
+} rr_status;
+
+/* Static, human-readable name of a status. */
+const char *rr_status_string(rr_status status);
+
+/* Detail of the last error returned on the calling host thread ("" if none). */
+const char *rr_last_error_detail(void);
+
+/*
+ * Softmax forward ("Online FlashSoftmax", sec. 3.1): for each row,
+ *   y_j = exp(x_j - m) / d,  m = max_j x_j,  d = sum_j exp(x_j - m),
+ * with (m, d) computed in one pass over global memory by the online
+ * normaliser and merged across threads with its pairwise rule.
+ *   x, y : [rows x cols] dtype.  y == x (in place) is allowed; any other
+ *          overlap returns RR_ERR_ALIASING.
+ * A row whose maximum is -inf (fully masked) produces y = 0.
+ */
+rr_status rr_softmax_fwd(const void *x, void *y, int64_t rows, int64_t cols,
+                         rr_dtype dtype, cudaStream_t stream);
+
+/*
+ * Fused softmax cross-entropy, forward and backward in one pass (sec. 2.1
+ * and sec. 3.1; cross-entropy as in Module 3 of "gpu-ml-learning"):
+ *   loss_r      = m + log d - logits[r, label_r]           (float32, [rows])
+ *   dlogits_r,j = softmax(logits_r)_j - [j == label_r]     ([rows x cols] dtype)
+ *   logits  : [rows x cols] dtype.   labels : [rows] int32.
+ *   dlogits : may equal logits (written in place); other overlap is an error.
+ *   ignore_index : a row whose label equals it gets loss 0 and dlogits 0 and
+ *           its logits are not read (PyTorch's default is -100).
+ *   bad_label_count : nullable device int32; each row whose label is outside
+ *           [0, cols) and is not ignore_index adds 1.  Such a row gets loss NaN
+ *           and dlogits equal to the plain softmax.  There is no trap.
+ * A fully masked row (max = -inf) gets loss 0 and dlogits 0.
+ * dlogits is not divided by the number of rows (loss is per row).
+ */
+rr_status rr_softmax_xent_fwd_bwd(const void *logits, const int32_t *labels,
+                                  float *loss, void *dlogits, int64_t rows,
+                                  int64_t cols, int32_t ignore_index,
+                                  int32_t *bad_label_count, rr_dtype dtype,
+                                  cudaStream_t stream);
+
+/*
+ * LayerNorm forward ("Welford Single-Pass Normalization", sec. 3.2): per row,
+ *   mean = (1/C) sum_j x_j,  var = (1/C) sum_j (x_j - mean)^2 (biased),
+ *   rstd = 1 / sqrt(var + eps),  y_j = (x_j - mean) * rstd * gamma_j + beta_j,
+ * the moments computed in one pass over global memory and merged across
+ * threads with the Chan/Welford pairwise update.
+ *   x, y : [rows x cols] dtype (y == x allowed).  gamma, beta : [cols] dtype.
+ *   mean, rstd : [rows] float32 outputs, saved for rr_layernorm_bwd.
+ *   eps : >= 0 and finite.
+ * A row holding a non-finite value is masked: y = 0, mean = 0, rstd = 0.
+ */
+rr_status rr_layernorm_fwd(const void *x, const void *gamma, const void *beta,
+                           void *y, float *mean, float *rstd, int64_t rows,
+                           int64_t cols, float eps, rr_dtype dtype,
+                           cudaStream_t stream);
+
+/* Bytes of device workspace rr_layernorm_bwd needs for (rows, cols, dtype);
+ * 0 if the arguments are invalid.  Depends on the current device. */
+size_t rr_layernorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtype);
+
+/*
+ * LayerNorm backward (analytic derivative, sec. 2.2): with
+ * xhat = (x - mean) * rstd and g = dy * gamma,
+ *   dx_j     = rstd * (g_j - mean_j(g) - xhat_j * mean_j(g * xhat)),
+ *   dgamma_j = sum_r dy_rj * xhat_rj,   dbeta_j = sum_r dy_rj.
+ *   dy, x, dx : [rows x cols] dtype (dx may equal dy).  gamma, dgamma, dbeta :
+ *   [cols] dtype.  mean, rstd : [rows] float32 from rr_layernorm_fwd.
+ *   workspace : device scratch of workspace_bytes >= the size query's answer
+ *   (16-byte aligned), owned by the caller; its contents on entry are ignored.
+ * A row with rstd == 0 (masked by the forward) gets dx = 0 and adds nothing to
+ * dgamma / dbeta.  dgamma / dbeta are summed over rows in a fixed order, so the
+ * result is deterministic for a given device and shape.
+ */
+rr_status rr_layernorm_bwd(const void *dy, const void *x, const float *mean,
+                           const float *rstd, const void *gamma, void *dx,
+                           void *dgamma, void *dbeta, void *workspace,
+                           size_t workspace_bytes, int64_t rows, int64_t cols,
+                           rr_dtype dtype, cudaStream_t stream);
+
+/*
+ * Reads (and if `reset` is non-zero clears) the error word of `device` that
+ * the kernels set when a bounded wait gives up.  *value receives 0 or an
+ * rr_status such as RR_ERR_DEVICE_TIMEOUT.  Synchronous: it waits for the
+ * device's outstanding work.
+ */
+rr_status rr_read_device_error(int device, int *value, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RR_H */

@@ -1,0 +1,519 @@
+// rr_api.cu -- the C ABI of librr.so: argument checks, per-device attribute
+// cache, choice of kernel variant, and launches on the caller's stream.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "../../include/rr.h"
+#include "rr_kernels.h"
+#include "rr_ops.cuh"
+
+namespace {
+
+using rr::KernelSet;
+
+thread_local std::string g_detail;
+
+rr_status fail(rr_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_detail = buf;
+  return s;
+}
+
+rr_status ok() {
+  g_detail.clear();
+  return RR_OK;
+}
+
+// Error word written by bounded device-side waits that give up.
+__device__ int g_rr_device_error;
+
+struct DevInfo {
+  bool init = false;
+  int sms = 0;
+  int smem_optin = 0;
+  int* err = nullptr;
+  std::map<const void*, int> smem_set;                   // kernel -> max dyn smem set
+  std::map<std::pair<const void*, long long>, int> occ;  // (kernel, T<<32|smem) -> blocks/SM
+  std::map<std::pair<const void*, long long>, int> ncl;  // (kernel, K<<32|smem) -> clusters
+};
+
+constexpr int kMaxDev = 64;
+std::mutex g_mu;
+DevInfo g_dev[kMaxDev];
+
+rr_status device_info(DevInfo** out) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return fail(RR_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (d < 0 || d >= kMaxDev) return fail(RR_ERR_CUDA, "device index %d out of range", d);
+  DevInfo& di = g_dev[d];
+  if (!di.init) {
+    if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, d)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d)) !=
+            cudaSuccess ||
+        (e = cudaGetSymbolAddress(reinterpret_cast<void**>(&di.err), g_rr_device_error)) !=
+            cudaSuccess)
+      return fail(RR_ERR_CUDA, "device attributes: %s", cudaGetErrorString(e));
+    di.init = true;
+  }
+  *out = &di;
+  return RR_OK;
+}
+
+rr_status set_smem(DevInfo* di, const void* fn, size_t smem) {
+  int& cur = di->smem_set[fn];
+  if ((int)smem > cur) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+      return fail(RR_ERR_CUDA, "cudaFuncSetAttribute(%zu B smem): %s", smem, cudaGetErrorString(e));
+    cur = (int)smem;
+  }
+  return RR_OK;
+}
+
+enum OpKind { kSoftmax = 0, kLnFwd = 1, kLnBwd = 2 };
+
+const KernelSet& kernels(OpKind op, rr_dtype dt) {
+  static KernelSet sets[3][2] = {
+      {rr::softmax_kernels_f32(), rr::softmax_kernels_bf16()},
+      {rr::lnfwd_kernels_f32(), rr::lnfwd_kernels_bf16()},
+      {rr::lnbwd_kernels_f32(), rr::lnbwd_kernels_bf16()},
+  };
+  return sets[op][dt];
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+struct Plan {
+  bool staged = false;
+  int mode = 0;  // 0: 16-byte chunks, 1: elements
+  int G = 0, T = 0, K = 1;
+  const void* fn = nullptr;
+  int64_t grid = 0;
+  size_t smem = 0;
+  int64_t partials = 0;  // LayerNorm backward: rows of column partials
+  rr::Geo geo{};
+};
+
+// Chooses the kernel variant and launch shape for (op, dtype, mode, rows, cols)
+// on the current device.  head_free: every row starts 16-byte aligned, so a
+// row needs no extra chunk for a ragged head.  Deterministic for a given device, so the workspace
+// size query and the launch agree.
+rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t rows, int64_t cols,
+                    Plan* pl) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo* di = nullptr;
+  rr_status st = device_info(&di);
+  if (st != RR_OK) return st;
+  const KernelSet& ks = kernels(op, dt);
+  const int E = dt == RR_BF16 ? 2 : 4;
+  const int V = 16 / E;
+  const int NT = op == kLnBwd ? 2 : 1;
+  const int sb = ks.stats_bytes;
+  pl->mode = mode;
+  pl->geo.rows = rows;
+  pl->geo.cols = cols;
+
+  // Direct variants: the smallest row group whose threads hold the row.
+  const int64_t units = mode == 0 ? cdiv(cols * E + (head_free ? 0 : 15), 16) : cols;
+  int gi = -1;
+  for (int i = 0; i < rr::kNumDirectG; ++i)
+    if (cdiv(units, (int64_t)1 << i) <= ks.nq_direct[mode]) {
+      gi = i;
+      break;
+    }
+  if (gi >= 0) {
+    const int G = 1 << gi;
+    const int T = ks.maxt_direct;
+    const int ngroups = T / G;
+    size_t red = (size_t)((G > 32 ? ngroups * 64 : 0) + 2) * sb;
+    size_t col = (op == kLnBwd && ngroups > 1) ? (size_t)ngroups * 2 * cols * 4 : 0;
+    size_t smem = round_up((int64_t)red, 16) + col;
+    if ((int64_t)smem <= di->smem_optin) {
+      const void* fn = ks.direct[mode][gi];
+      if ((st = set_smem(di, fn, smem)) != RR_OK) return st;
+      int& occ = di->occ[{fn, ((long long)T << 32) | (long long)smem}];
+      if (occ == 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, T, smem);
+        if (e != cudaSuccess || occ <= 0)
+          return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+      }
+      int64_t per_sm = op == kLnBwd ? (occ < 2 ? occ : 2) : occ;
+      int64_t grid = cdiv(rows, ngroups);
+      if (grid > (int64_t)di->sms * per_sm) grid = (int64_t)di->sms * per_sm;
+      pl->staged = false;
+      pl->G = G;
+      pl->T = T;
+      pl->K = 1;
+      pl->fn = fn;
+      pl->grid = grid;
+      pl->smem = smem;
+      pl->partials = grid;
+      pl->geo.slice = cols;
+      pl->geo.nbuf = 0;
+      pl->geo.buf_bytes = 0;
+      pl->geo.red_off = 0;
+      pl->geo.col_off = (int32_t)round_up((int64_t)red, 16);
+      return RR_OK;
+    }
+  }
+
+  // Staged variants: one row (slice) per CTA, K-CTA clusters for long rows.
+  const int T = ks.maxt_staged;
+  const int nq = ks.nq_staged[mode];
+  int K = 0;
+  int64_t slice = 0;
+  for (int k = 1; k <= 8; k *= 2) {
+    const int64_t sl = round_up(cdiv(cols, k), V);
+    if (k > 1 && (k - 1) * sl >= cols) break;
+    const int64_t su = mode == 0 ? cdiv(sl * E + (head_free ? 0 : 15), 16) : sl;
+    if (cdiv(su, T) <= nq) {
+      K = k;
+      slice = sl;
+      break;
+    }
+  }
+  if (K == 0)
+    return fail(RR_ERR_INVALID_ARG, "cols=%lld is beyond the supported row length for this operation",
+                (long long)cols);
+  const int64_t buf_bytes = round_up(slice * E + 32, 128);
+  const int64_t fixed = 2 * 8 + 16 + (int64_t)(64 + 2) * sb;
+  int nbuf = 2;
+  if (nbuf * NT * buf_bytes + fixed > di->smem_optin) nbuf = 1;
+  if (nbuf * NT * buf_bytes + fixed > di->smem_optin)
+    return fail(RR_ERR_INVALID_ARG, "row slice of %lld bytes does not fit shared memory",
+                (long long)(slice * E));
+  const int64_t red_off = round_up(nbuf * NT * buf_bytes + nbuf * 8, 16);
+  const size_t smem = (size_t)(red_off + (int64_t)(64 + 2) * sb);
+  const void* fn = ks.staged[mode];
+  if ((st = set_smem(di, fn, smem)) != RR_OK) return st;
+  int64_t grid;
+  if (K == 1) {
+    int& occ = di->occ[{fn, ((long long)T << 32) | (long long)smem}];
+    if (occ == 0) {
+      cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, T, smem);
+      if (e != cudaSuccess || occ <= 0)
+        return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+    }
+    grid = rows < (int64_t)di->sms * occ ? rows : (int64_t)di->sms * occ;
+  } else {
+    int& ncl = di->ncl[{fn, ((long long)K << 32) | (long long)smem}];
+    if (ncl == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = K;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3((unsigned)(K * di->sms));
+      cfg.blockDim = dim3((unsigned)T);
+      cfg.dynamicSmemBytes = smem;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg);
+      if (e != cudaSuccess || ncl <= 0)
+        return fail(RR_ERR_CUDA, "cluster occupancy query (K=%d): %s", K, cudaGetErrorString(e));
+    }
+    grid = (int64_t)K * (rows < ncl ? rows : ncl);
+  }
+  pl->staged = true;
+  pl->G = T;
+  pl->T = T;
+  pl->K = K;
+  pl->fn = fn;
+  pl->grid = grid;
+  pl->smem = smem;
+  pl->partials = grid / K;
+  pl->geo.slice = slice;
+  pl->geo.nbuf = nbuf;
+  pl->geo.buf_bytes = (int32_t)buf_bytes;
+  pl->geo.red_off = (int32_t)red_off;
+  pl->geo.col_off = (int32_t)smem;
+  return RR_OK;
+}
+
+// Plans in chunk mode when allowed, falling back to element mode (which holds
+// longer rows per CTA) when the row does not fit the chunk-mode variants.
+rr_status plan_any(OpKind op, rr_dtype dt, bool chunk_ok, bool head_free, int64_t rows,
+                   int64_t cols, Plan* pl) {
+  if (chunk_ok) {
+    rr_status st = make_plan(op, dt, 0, head_free, rows, cols, pl);
+    if (st != RR_ERR_INVALID_ARG) return st;
+  }
+  return make_plan(op, dt, 1, false, rows, cols, pl);
+}
+
+template <class P>
+rr_status launch(const Plan& pl, const P& params, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)pl.grid);
+  cfg.blockDim = dim3((unsigned)pl.T);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = stream;
+  cfg.numAttrs = 0;
+  if (pl.K > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pl.K;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  P pcopy = params;
+  rr::Geo g = pl.geo;
+  void* args[] = {&pcopy, &g};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, pl.fn, args);
+  if (e != cudaSuccess)
+    return fail(RR_ERR_CUDA, "launch (grid %lld, block %d, smem %zu, cluster %d): %s",
+                (long long)pl.grid, pl.T, pl.smem, pl.K, cudaGetErrorString(e));
+  return RR_OK;
+}
+
+// ------------------------------------------------------------- checks ----
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return na && nb && pa < pb + nb && pb < pa + na;
+}
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+rr_status check_shape(int64_t rows, int64_t cols, rr_dtype dt) {
+  if (dt != RR_F32 && dt != RR_BF16) return fail(RR_ERR_UNSUPPORTED_DTYPE, "dtype %d", (int)dt);
+  if (rows < 0) return fail(RR_ERR_INVALID_ARG, "rows=%lld < 0", (long long)rows);
+  if (cols < 1) return fail(RR_ERR_INVALID_ARG, "cols=%lld < 1", (long long)cols);
+  if (cols > ((int64_t)1 << 31) || (rows > 0 && cols > (((int64_t)1 << 60) / rows)))
+    return fail(RR_ERR_INVALID_ARG, "rows*cols too large");
+  return RR_OK;
+}
+
+int* device_error_word() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo* di = nullptr;
+  if (device_info(&di) != RR_OK) return nullptr;
+  return di->err;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rr_status_string(rr_status s) {
+  switch (s) {
+    case RR_OK: return "RR_OK";
+    case RR_ERR_INVALID_ARG: return "RR_ERR_INVALID_ARG";
+    case RR_ERR_UNSUPPORTED_DTYPE: return "RR_ERR_UNSUPPORTED_DTYPE";
+    case RR_ERR_ALIASING: return "RR_ERR_ALIASING";
+    case RR_ERR_WORKSPACE_TOO_SMALL: return "RR_ERR_WORKSPACE_TOO_SMALL";
+    case RR_ERR_CUDA: return "RR_ERR_CUDA";
+    case RR_ERR_DEVICE_TIMEOUT: return "RR_ERR_DEVICE_TIMEOUT";
+  }
+  return "RR_UNKNOWN_STATUS";
+}
+
+const char* rr_last_error_detail(void) { return g_detail.c_str(); }
+
+rr_status rr_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, rr_dtype dtype,
+                         cudaStream_t stream) {
+  rr_status st = check_shape(rows, cols, dtype);
+  if (st != RR_OK) return st;
+  if (rows == 0) return ok();
+  if (!x || !y) return fail(RR_ERR_INVALID_ARG, "null pointer");
+  const size_t E = dtype == RR_BF16 ? 2 : 4;
+  if (!aligned(x, E) || !aligned(y, E)) return fail(RR_ERR_INVALID_ARG, "misaligned element pointer");
+  const size_t n = (size_t)rows * cols * E;
+  if (x != y && overlaps(x, n, y, n)) return fail(RR_ERR_ALIASING, "x and y partially overlap");
+  const bool same = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(y) & 15);
+  const bool head_free = same && aligned(x, 16) && (cols * E) % 16 == 0;
+  Plan pl;
+  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
+  int* err = device_error_word();
+  if (!err) return RR_ERR_CUDA;
+  rr::SoftmaxParams p{static_cast<const char*>(x), static_cast<char*>(y), nullptr, nullptr, nullptr,
+                      err, cols, 0};
+  if ((st = launch(pl, p, stream)) != RR_OK) return st;
+  return ok();
+}
+
+rr_status rr_softmax_xent_fwd_bwd(const void* logits, const int32_t* labels, float* loss,
+                                  void* dlogits, int64_t rows, int64_t cols, int32_t ignore_index,
+                                  int32_t* bad_label_count, rr_dtype dtype, cudaStream_t stream) {
+  rr_status st = check_shape(rows, cols, dtype);
+  if (st != RR_OK) return st;
+  if (rows == 0) return ok();
+  if (!logits || !labels || !loss || !dlogits) return fail(RR_ERR_INVALID_ARG, "null pointer");
+  const size_t E = dtype == RR_BF16 ? 2 : 4;
+  if (!aligned(logits, E) || !aligned(dlogits, E) || !aligned(labels, 4) || !aligned(loss, 4) ||
+      (bad_label_count && !aligned(bad_label_count, 4)))
+    return fail(RR_ERR_INVALID_ARG, "misaligned pointer");
+  const size_t n = (size_t)rows * cols * E, nr = (size_t)rows * 4;
+  if (logits != dlogits && overlaps(logits, n, dlogits, n))
+    return fail(RR_ERR_ALIASING, "logits and dlogits partially overlap");
+  if (overlaps(loss, nr, logits, n) || overlaps(loss, nr, dlogits, n) || overlaps(loss, nr, labels, nr) ||
+      overlaps(labels, nr, dlogits, n))
+    return fail(RR_ERR_ALIASING, "loss / labels overlap another tensor");
+  if (bad_label_count && (overlaps(bad_label_count, 4, logits, n) || overlaps(bad_label_count, 4, dlogits, n) ||
+                          overlaps(bad_label_count, 4, loss, nr) || overlaps(bad_label_count, 4, labels, nr)))
+    return fail(RR_ERR_ALIASING, "bad_label_count overlaps another tensor");
+  const bool same =
+      (reinterpret_cast<uintptr_t>(logits) & 15) == (reinterpret_cast<uintptr_t>(dlogits) & 15);
+  const bool head_free = same && aligned(logits, 16) && (cols * E) % 16 == 0;
+  Plan pl;
+  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
+  int* err = device_error_word();
+  if (!err) return RR_ERR_CUDA;
+  rr::SoftmaxParams p{static_cast<const char*>(logits), static_cast<char*>(dlogits), labels, loss,
+                      bad_label_count, err, cols, ignore_index};
+  if ((st = launch(pl, p, stream)) != RR_OK) return st;
+  return ok();
+}
+
+rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean,
+                           float* rstd, int64_t rows, int64_t cols, float eps, rr_dtype dtype,
+                           cudaStream_t stream) {
+  rr_status st = check_shape(rows, cols, dtype);
+  if (st != RR_OK) return st;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(RR_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (rows == 0) return ok();
+  if (!x || !gamma || !beta || !y || !mean || !rstd) return fail(RR_ERR_INVALID_ARG, "null pointer");
+  const size_t E = dtype == RR_BF16 ? 2 : 4;
+  if (!aligned(x, E) || !aligned(y, E) || !aligned(gamma, E) || !aligned(beta, E) || !aligned(mean, 4) ||
+      !aligned(rstd, 4))
+    return fail(RR_ERR_INVALID_ARG, "misaligned pointer");
+  const size_t n = (size_t)rows * cols * E, nc = (size_t)cols * E, nr = (size_t)rows * 4;
+  if (x != y && overlaps(x, n, y, n)) return fail(RR_ERR_ALIASING, "x and y partially overlap");
+  if (overlaps(y, n, gamma, nc) || overlaps(y, n, beta, nc) || overlaps(mean, nr, rstd, nr) ||
+      overlaps(mean, nr, x, n) || overlaps(mean, nr, y, n) || overlaps(rstd, nr, x, n) ||
+      overlaps(rstd, nr, y, n) || overlaps(mean, nr, gamma, nc) || overlaps(mean, nr, beta, nc) ||
+      overlaps(rstd, nr, gamma, nc) || overlaps(rstd, nr, beta, nc))
+    return fail(RR_ERR_ALIASING, "outputs overlap inputs");
+  const bool al = (cols * E) % 16 == 0 && aligned(x, 16) && aligned(y, 16) && aligned(gamma, 16) &&
+                  aligned(beta, 16);
+  Plan pl;
+  if ((st = plan_any(kLnFwd, dtype, al, true, rows, cols, &pl)) != RR_OK) return st;
+  int* err = device_error_word();
+  if (!err) return RR_ERR_CUDA;
+  rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma),
+                    static_cast<const char*>(beta), static_cast<char*>(y), mean, rstd, err, cols, eps};
+  if ((st = launch(pl, p, stream)) != RR_OK) return st;
+  return ok();
+}
+
+static rr_status lnbwd_plan(int64_t rows, int64_t cols, rr_dtype dtype, bool aligned_rows, Plan* pl,
+                            size_t* ws_bytes) {
+  rr_status st = plan_any(kLnBwd, dtype, aligned_rows, true, rows, cols, pl);
+  if (st != RR_OK) return st;
+  *ws_bytes = (size_t)pl->partials * 2 * (size_t)cols * sizeof(float);
+  return RR_OK;
+}
+
+size_t rr_layernorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtype) {
+  if (check_shape(rows, cols, dtype) != RR_OK) return 0;
+  if (rows == 0) return 2 * (size_t)cols * sizeof(float);
+  // The element-mode plan never needs fewer partials than the chunk-mode one
+  // for the same shape, but the caller does not know which mode the pointers
+  // will select, so report the larger of the two.
+  size_t best = 0;
+  for (int m = 0; m < 2; ++m) {
+    Plan pl;
+    size_t ws = 0;
+    if (lnbwd_plan(rows, cols, dtype, m == 0, &pl, &ws) == RR_OK && ws > best) best = ws;
+  }
+  return best;
+}
+
+rr_status rr_layernorm_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+                           const void* gamma, void* dx, void* dgamma, void* dbeta, void* workspace,
+                           size_t workspace_bytes, int64_t rows, int64_t cols, rr_dtype dtype,
+                           cudaStream_t stream) {
+  rr_status st = check_shape(rows, cols, dtype);
+  if (st != RR_OK) return st;
+  if (!dy || !x || !mean || !rstd || !gamma || !dx || !dgamma || !dbeta || !workspace)
+    return fail(RR_ERR_INVALID_ARG, "null pointer");
+  const size_t E = dtype == RR_BF16 ? 2 : 4;
+  if (!aligned(dy, E) || !aligned(x, E) || !aligned(dx, E) || !aligned(gamma, E) || !aligned(dgamma, E) ||
+      !aligned(dbeta, E) || !aligned(mean, 4) || !aligned(rstd, 4) || !aligned(workspace, 16))
+    return fail(RR_ERR_INVALID_ARG, "misaligned pointer (workspace needs 16 bytes)");
+  const size_t n = (size_t)rows * cols * E, nc = (size_t)cols * E, nr = (size_t)rows * 4;
+  if (dx != dy && overlaps(dx, n, dy, n)) return fail(RR_ERR_ALIASING, "dx and dy partially overlap");
+  if (dx != x && overlaps(dx, n, x, n)) return fail(RR_ERR_ALIASING, "dx and x partially overlap");
+  const void* outs[] = {dgamma, dbeta, workspace};
+  const size_t outn[] = {nc, nc, workspace_bytes};
+  const void* ins[] = {dy, x, mean, rstd, gamma, dx};
+  const size_t inn[] = {n, n, nr, nr, nc, n};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (overlaps(outs[i], outn[i], ins[j], inn[j])) return fail(RR_ERR_ALIASING, "output overlaps an input");
+    for (int j = i + 1; j < 3; ++j)
+      if (overlaps(outs[i], outn[i], outs[j], outn[j])) return fail(RR_ERR_ALIASING, "outputs overlap");
+  }
+  if (overlaps(dx, n, mean, nr) || overlaps(dx, n, rstd, nr) || overlaps(dx, n, gamma, nc))
+    return fail(RR_ERR_ALIASING, "dx overlaps mean / rstd / gamma");
+  const bool al = (cols * E) % 16 == 0 && aligned(dy, 16) && aligned(x, 16) && aligned(dx, 16) &&
+                  aligned(gamma, 16);
+  Plan pl;
+  size_t need = 0;
+  if (rows == 0) {
+    // Nothing to read: dgamma = dbeta = 0 through a one-partial workspace.
+    need = 2 * (size_t)cols * sizeof(float);
+    if (workspace_bytes < need)
+      return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, need, stream);
+    if (e != cudaSuccess) return fail(RR_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+    pl.partials = 1;
+  } else {
+    if ((st = lnbwd_plan(rows, cols, dtype, al, &pl, &need)) != RR_OK) return st;
+    if (workspace_bytes < need)
+      return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+    int* err = device_error_word();
+    if (!err) return RR_ERR_CUDA;
+    rr::LnBwdParams p{static_cast<const char*>(dy), static_cast<const char*>(x), mean, rstd,
+                      static_cast<const char*>(gamma), static_cast<char*>(dx),
+                      static_cast<float*>(workspace), err, cols};
+    if ((st = launch(pl, p, stream)) != RR_OK) return st;
+  }
+  const void* cr = dtype == RR_BF16 ? rr::col_reduce_kernel_ptr_bf16() : rr::col_reduce_kernel_ptr_f32();
+  const float* ws = static_cast<const float*>(workspace);
+  int64_t P = pl.partials;
+  char* dg = static_cast<char*>(dgamma);
+  char* db = static_cast<char*>(dbeta);
+  void* args[] = {&ws, &P, &cols, &dg, &db};
+  cudaError_t e = cudaLaunchKernel(cr, dim3((unsigned)cdiv(2 * cols, 32)), dim3(256), args, 0, stream);
+  if (e != cudaSuccess) return fail(RR_ERR_CUDA, "column reduce launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+rr_status rr_read_device_error(int device, int* value, int reset) {
+  if (!value) return fail(RR_ERR_INVALID_ARG, "null pointer");
+  int prev = 0;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return fail(RR_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if ((e = cudaSetDevice(device)) != cudaSuccess)
+    return fail(RR_ERR_CUDA, "cudaSetDevice(%d): %s", device, cudaGetErrorString(e));
+  rr_status st = RR_OK;
+  int v = 0;
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess ||
+      (e = cudaMemcpyFromSymbol(&v, g_rr_device_error, sizeof v)) != cudaSuccess) {
+    st = fail(RR_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+  } else if (reset) {
+    const int zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_rr_device_error, &zero, sizeof zero)) != cudaSuccess)
+      st = fail(RR_ERR_CUDA, "clearing the error word: %s", cudaGetErrorString(e));
+  }
+  cudaSetDevice(prev);
+  *value = v;
+  return st == RR_OK ? ok() : st;
+}
+
+}  // extern "C"

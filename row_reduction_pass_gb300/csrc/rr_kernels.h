@@ -1,0 +1,29 @@
+// rr_kernels.h -- host-side view of the compiled kernel variants.
+#pragma once
+
+namespace rr {
+
+constexpr int kNumDirectG = 9;  // row groups of 1, 2, 4, ..., 256 threads
+
+// The variants of one operation for one storage type.  Index [m] is the mode:
+// 0 = 16-byte chunks, 1 = single elements.
+struct KernelSet {
+  const void* direct[2][kNumDirectG];
+  const void* staged[2];
+  int nq_direct[2];
+  int nq_staged[2];
+  int maxt_direct;
+  int maxt_staged;
+  int stats_bytes;
+};
+
+KernelSet softmax_kernels_f32();
+KernelSet softmax_kernels_bf16();
+KernelSet lnfwd_kernels_f32();
+KernelSet lnfwd_kernels_bf16();
+KernelSet lnbwd_kernels_f32();
+KernelSet lnbwd_kernels_bf16();
+const void* col_reduce_kernel_ptr_f32();
+const void* col_reduce_kernel_ptr_bf16();
+
+}  // namespace rr

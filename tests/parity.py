@@ -1,0 +1,166 @@
+"""Helpers shared by the GPU parity tests: host<->device marshalling of the
+seeded inputs, the comparison rule, and one call per operation through the C
+ABI (via the package binding) next to the float64 oracle on the same inputs.
+
+Comparison rule (elementwise, both sides NaN counts as equal):
+    |gpu - ref| <= atol + rtol * |ref|
+  outputs in the I/O dtype:  fp32 rtol 1e-5, atol 1e-5;  bf16 rtol 2e-2, atol 1e-5
+  float32 outputs (loss, mean, rstd):                   rtol 1e-5, atol 1e-5
+  dgamma / dbeta (sums over rows):
+    |gpu - ref| <= rtol_io * |ref| + 1e-5 * sum_r |term_r| + 1e-5
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import row_reduction_pass_gb300 as rr
+
+TOL = {"f32": (1e-5, 1e-5), "bf16": (2e-2, 1e-5)}
+TOL_F32_OUT = (1e-5, 1e-5)
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def to_dev(a: np.ndarray, pad_elems: int = 0) -> torch.Tensor:
+    """Copy a host array (float32 or bf16 bits) to the GPU.  pad_elems > 0 places
+    it pad_elems elements past a 16-byte aligned start (a misaligned base)."""
+    if a.dtype == np.uint16:
+        flat = torch.from_numpy(np.ascontiguousarray(a).view(np.int16).reshape(-1))
+        tdt = torch.bfloat16
+    elif a.dtype == np.float32:
+        flat = torch.from_numpy(np.ascontiguousarray(a).reshape(-1))
+        tdt = torch.float32
+    elif a.dtype == np.int32:
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    else:
+        raise TypeError(a.dtype)
+    buf = torch.empty(a.size + pad_elems + 16, dtype=flat.dtype, device=dev())
+    view = buf[pad_elems:pad_elems + a.size]
+    view.copy_(flat.to(dev()))
+    view = view.view(tdt) if tdt == torch.bfloat16 else view
+    return view.view(a.shape)
+
+
+def empty_like_dev(shape, dtype: str, pad_elems: int = 0, fill=float("nan")) -> torch.Tensor:
+    """Device buffer poisoned with NaN (so unwritten outputs are caught)."""
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    n = int(np.prod(shape))
+    buf = torch.full((n + pad_elems + 16,), fill, dtype=tdt, device=dev())
+    return buf[pad_elems:pad_elems + n].view(shape)
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def compare(name: str, got: np.ndarray, ref: np.ndarray, rtol: float, atol: float,
+            scale: np.ndarray | None = None):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, f"{name}: shape {got.shape} != {ref.shape}"
+    both_nan = np.isnan(got) & np.isnan(ref)
+    err = np.abs(got - ref)
+    bound = atol + rtol * np.abs(ref)
+    if scale is not None:
+        bound = bound + 1e-5 * scale
+    same_inf = np.isinf(got) & np.isinf(ref) & (np.sign(got) == np.sign(ref))
+    ok = both_nan | same_inf | (err <= bound)
+    if not ok.all():
+        idx = np.unravel_index(np.argmax(np.where(ok, -1.0, np.nan_to_num(err, nan=np.inf))),
+                               got.shape)
+        raise AssertionError(
+            f"{name}: {int((~ok).sum())} of {ok.size} outside tolerance; worst at {idx}: "
+            f"gpu={got[idx]!r} ref={ref[idx]!r} bound={bound[idx]!r}")
+    finite = np.isfinite(got) & np.isfinite(ref)
+    return float(err[finite].max()) if finite.any() else 0.0
+
+
+# ----------------------------------------------------------------- ops ----
+
+def run_softmax(x: np.ndarray, dtype: str, pad_in=0, pad_out=0, inplace=False):
+    xd = to_dev(x, pad_in)
+    y = xd if inplace else empty_like_dev(x.shape, dtype, pad_out)
+    rr.rr_softmax_fwd(xd, y)
+    torch.cuda.synchronize()
+    return host(y)
+
+
+def check_softmax(x, dtype, **kw):
+    got = run_softmax(x, dtype, **kw)
+    ref = oracle.softmax(x)
+    rtol, atol = TOL[dtype]
+    compare("softmax y", got, ref, rtol, atol)
+
+
+def run_xent(logits, labels, dtype, ignore_index=-100, pad_in=0, pad_out=0, inplace=False):
+    xd = to_dev(logits, pad_in)
+    lab = to_dev(labels)
+    loss = torch.full((logits.shape[0],), float("nan"), device=dev())
+    dl = xd if inplace else empty_like_dev(logits.shape, dtype, pad_out)
+    bad = torch.zeros(1, dtype=torch.int32, device=dev())
+    rr.rr_softmax_xent_fwd_bwd(xd, lab, loss, dl, ignore_index=ignore_index, bad_label_count=bad)
+    torch.cuda.synchronize()
+    return host(loss), host(dl), int(bad.item())
+
+
+def check_xent(logits, labels, dtype, ignore_index=-100, **kw):
+    loss, dl, bad = run_xent(logits, labels, dtype, ignore_index, **kw)
+    rloss, rdl, rbad = oracle.xent(logits, labels, ignore_index)
+    rtol, atol = TOL[dtype]
+    compare("xent loss", loss, rloss, *TOL_F32_OUT)
+    compare("xent dlogits", dl, rdl, rtol, atol)
+    assert bad == rbad, f"bad label count {bad} != {rbad}"
+
+
+def run_ln(x, gamma, beta, dy, eps, dtype, pad=(0, 0, 0, 0, 0), oracle_stats=True):
+    """LayerNorm fwd then bwd on the GPU.  pad = element offsets of
+    (x, y, gamma/beta, dy, dx).  The backward gets the oracle's mean / rstd
+    (rounded to float32) when oracle_stats, else the GPU forward's."""
+    xd = to_dev(x, pad[0])
+    gd = to_dev(gamma, pad[2])
+    bd = to_dev(beta, pad[2])
+    y = empty_like_dev(x.shape, dtype, pad[1])
+    rows = x.shape[0]
+    mean = torch.full((rows,), float("nan"), device=dev())
+    rstd = torch.full((rows,), float("nan"), device=dev())
+    rr.rr_layernorm_fwd(xd, gd, bd, y, mean, rstd, eps=eps)
+    _, rmean, rrstd = oracle.ln_fwd(x, gamma, beta, eps, want_y=False)
+    if oracle_stats:
+        m_in = torch.from_numpy(rmean.astype(np.float32)).to(dev())
+        r_in = torch.from_numpy(rrstd.astype(np.float32)).to(dev())
+    else:
+        m_in, r_in = mean, rstd
+    dyd = to_dev(dy, pad[3])
+    dx = empty_like_dev(x.shape, dtype, pad[4])
+    dg = empty_like_dev(gamma.shape, dtype)
+    db = empty_like_dev(gamma.shape, dtype)
+    rr.rr_layernorm_bwd(dyd, xd, m_in, r_in, gd, dx, dg, db)
+    torch.cuda.synchronize()
+    return dict(y=host(y), mean=host(mean), rstd=host(rstd), dx=host(dx), dgamma=host(dg),
+                dbeta=host(db), mean_in=m_in.cpu().numpy().astype(np.float64),
+                rstd_in=r_in.cpu().numpy().astype(np.float64))
+
+
+def check_ln(x, gamma, beta, dy, eps, dtype, pad=(0, 0, 0, 0, 0), oracle_stats=True):
+    g = run_ln(x, gamma, beta, dy, eps, dtype, pad, oracle_stats)
+    ry, rmean, rrstd = oracle.ln_fwd(x, gamma, beta, eps)
+    rtol, atol = TOL[dtype]
+    compare("ln y", g["y"], ry, rtol, atol)
+    compare("ln mean", g["mean"], rmean, *TOL_F32_OUT)
+    compare("ln rstd", g["rstd"], rrstd, *TOL_F32_OUT)
+    # The backward's own inputs include mean / rstd: the oracle gets exactly the
+    # float32 values the GPU was given (the oracle's statistics rounded to
+    # float32).  In the chained check (GPU statistics into the GPU backward) the
+    # oracle chains its own float64 statistics instead.
+    if oracle_stats:
+        rdx, rdg, rdb, sdg, sdb = oracle.ln_bwd(dy, x, g["mean_in"], g["rstd_in"], gamma)
+    else:
+        rdx, rdg, rdb, sdg, sdb = oracle.ln_bwd(dy, x, rmean, rrstd, gamma)
+    compare("ln dx", g["dx"], rdx, rtol, atol)
+    compare("ln dgamma", g["dgamma"], rdg, rtol, atol, scale=sdg)
+    compare("ln dbeta", g["dbeta"], rdb, rtol, atol, scale=sdb)
+    return g

@@ -1,0 +1,112 @@
+"""GPU parity: every operation through the C ABI against the float64 oracle on
+the same seeded inputs, over row lengths that exercise every kernel variant
+(one thread per row up to clusters of CTAs per row), ragged tails, misaligned
+bases (element mode), in-place outputs, masked and ignored rows."""
+import numpy as np
+import pytest
+
+from row_reduction_pass_gb300 import synth
+
+from parity import check_ln, check_softmax, check_xent
+
+pytestmark = pytest.mark.gpu
+
+COLS = [1, 2, 3, 5, 8, 31, 32, 33, 97, 127, 256, 512, 768, 1000, 1023, 2049, 4097, 8192,
+        12289, 16385, 50304, 65537]
+
+
+def rows_for(cols: int) -> int:
+    if cols >= 4097:
+        return 320 if cols <= 16385 else 160
+    return int(max(3, min(3000, (1 << 21) // cols)))
+
+
+def logits(rows, cols, dtype, seed, sigma=3.0, outliers=0.01, masked_every=37):
+    x, lab = synth.xent_inputs(rows, cols, dtype, sigma, seed, ignore_frac=0.05,
+                               outlier_frac=outliers, masked_row_every=masked_every)
+    return x, lab
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", COLS)
+def test_softmax(cols, dtype):
+    x, _ = logits(rows_for(cols), cols, dtype, 100 + cols)
+    check_softmax(x, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", [1, 3, 33, 97, 1000, 4097, 50304])
+@pytest.mark.parametrize("layout", ["both_misaligned", "out_misaligned", "inplace"])
+def test_softmax_layouts(cols, dtype, layout):
+    x, _ = logits(rows_for(cols) // 2 + 1, cols, dtype, 200 + cols)
+    if layout == "both_misaligned":
+        check_softmax(x, dtype, pad_in=1, pad_out=1)
+    elif layout == "out_misaligned":
+        check_softmax(x, dtype, pad_in=0, pad_out=1)
+    else:
+        check_softmax(x, dtype, pad_in=1, inplace=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", COLS)
+def test_xent(cols, dtype):
+    x, lab = logits(rows_for(cols), cols, dtype, 300 + cols)
+    lab[1::50] = cols + 3          # out of range -> NaN loss, counted
+    lab[2::97] = -7                # negative, not the ignore index
+    check_xent(x, lab, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", [1, 5, 31, 1000, 4097, 50304, 65537])
+@pytest.mark.parametrize("layout", ["inplace", "misaligned_inplace", "out_misaligned"])
+def test_xent_layouts(cols, dtype, layout):
+    x, lab = logits(rows_for(cols) // 2 + 1, cols, dtype, 400 + cols)
+    if layout == "inplace":
+        check_xent(x, lab, dtype, inplace=True)
+    elif layout == "misaligned_inplace":
+        check_xent(x, lab, dtype, pad_in=3, inplace=True)
+    else:
+        check_xent(x, lab, dtype, pad_in=0, pad_out=1)
+
+
+def test_xent_custom_ignore_index():
+    x, lab = logits(50, 77, "f32", 5)
+    lab[::3] = 7                   # a valid class used as the ignore index
+    check_xent(x, lab, "f32", ignore_index=7)
+
+
+LN_COLS = [1, 2, 3, 8, 31, 32, 97, 128, 256, 768, 1000, 1024, 2049, 4096, 4097, 8192, 12289,
+           16384, 32768, 65537]
+
+
+def ln_case(rows, cols, dtype, seed):
+    return synth.ln_inputs(rows, cols, dtype, seed, row_offset=10.0, gamma_std=0.1,
+                           beta_std=0.1, outlier_frac=0.005, masked_row_every=41)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", LN_COLS)
+def test_layernorm(cols, dtype):
+    x, g, b, dy = ln_case(rows_for(cols), cols, dtype, 500 + cols)
+    check_ln(x, g, b, dy, 1e-5, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", [1, 31, 768, 1000, 4097, 16384])
+@pytest.mark.parametrize("pad", [(1, 1, 1, 1, 1), (0, 0, 1, 0, 0), (0, 1, 0, 0, 1)])
+def test_layernorm_misaligned(cols, dtype, pad):
+    x, g, b, dy = ln_case(rows_for(cols) // 2 + 1, cols, dtype, 600 + cols)
+    check_ln(x, g, b, dy, 1e-5, dtype, pad=pad)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_layernorm_chain_uses_gpu_stats(dtype):
+    """fwd -> bwd with the GPU's own float32 mean / rstd."""
+    x, g, b, dy = ln_case(1000, 768, dtype, 7)
+    check_ln(x, g, b, dy, 1e-5, dtype, oracle_stats=False)
+
+
+def test_layernorm_eps_zero_and_large():
+    x, g, b, dy = ln_case(64, 100, "f32", 8)
+    check_ln(x, g, b, dy, 0.0, "f32")
+    check_ln(x, g, b, dy, 10.0, "f32")
