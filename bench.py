@@ -411,6 +411,46 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_profile_case(args):
+    """Runs one kernel of the step alone (W warm-up + K launches) on a smaller
+    batch, for ncu captures of a single kernel; prints a one-line summary."""
+    import torch
+    import row_reduction_pass_gb300 as rr
+
+    dev = torch.device("cuda", 0)
+    rr.load_library()
+
+    def bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    if args.profile == "xent":
+        xe = synth.make("xent_bf16_16384x50304", rows=args.profile_rows or 4096)
+        x, lab = bf16(xe["logits"]), torch.from_numpy(xe["labels"]).to(dev)
+        loss = torch.empty(x.shape[0], device=dev)
+        fn = lambda: rr.rr_softmax_xent_fwd_bwd(x, lab, loss, x)  # noqa: E731
+    elif args.profile == "softmax":
+        sm = synth.make("softmax_bf16_causal_65536x512")
+        x = bf16(sm["x"])
+        y = torch.empty_like(x)
+        fn = lambda: rr.rr_softmax_fwd(x, y)  # noqa: E731
+    else:
+        ln = synth.make("ln_f32_4096x768", rows=args.profile_rows or 4096)
+        x, g, b, dy = (torch.from_numpy(ln[k]).to(dev) for k in ("x", "gamma", "beta", "dy"))
+        y = torch.empty_like(x)
+        mean = torch.empty(x.shape[0], device=dev)
+        rstd = torch.empty(x.shape[0], device=dev)
+        rr.rr_layernorm_fwd(x, g, b, y, mean, rstd, eps=ln["eps"])
+        dx, dg, db = torch.empty_like(x), torch.empty_like(g), torch.empty_like(g)
+        if args.profile == "ln_fwd":
+            fn = lambda: rr.rr_layernorm_fwd(x, g, b, y, mean, rstd, eps=ln["eps"])  # noqa: E731
+        else:
+            fn = lambda: rr.rr_layernorm_bwd(dy, x, mean, rstd, g, dx, dg, db)  # noqa: E731
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,7 +460,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["xent", "softmax", "ln_fwd", "ln_bwd"], default=None,
+                    help="run only this kernel (for ncu captures of one kernel)")
+    ap.add_argument("--profile-rows", type=int, default=0)
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -16,7 +16,8 @@
  *     (per-column vectors are [cols], per-row vectors are [rows]).
  *   - Every pointer is a DEVICE pointer on the current CUDA device, allocated
  *     and owned by the caller; the library allocates nothing and keeps no state
- *     beyond a per-device cache of attributes.  Any alignment is accepted;
+ *     beyond a per-device cache of attributes (and the fixed scratch array of
+ *     rr_layernorm_bwd_noalloc).  Any alignment is accepted;
  *     16-byte aligned bases and rows whose byte length is a multiple of 16 take
  *     the vectorised path.
  *   - `dtype` (RR_F32 or RR_BF16) is the storage type of x, y, logits, dlogits,
@@ -132,6 +133,31 @@ rr_status rr_layernorm_bwd(const void *dy, const void *x, const float *mean,
                            void *dgamma, void *dbeta, void *workspace,
                            size_t workspace_bytes, int64_t rows, int64_t cols,
                            rr_dtype dtype, cudaStream_t stream);
+
+/*
+ * LayerNorm backward without a caller-provided workspace (this entry point has
+ * no counterpart in the pages; it is a convenience of this library).
+ * For callers that cannot allocate device memory at call time -- code under a
+ * framework's memory planner that owns every allocation, plugin interfaces
+ * that receive only input and output buffers, latency-critical paths where an
+ * allocation is not allowed.  Same arguments, results and error behaviour as
+ * rr_layernorm_bwd, minus the workspace: the column partials go to a scratch
+ * array of 8 MiB inside the library, held on every GPU that loads the library
+ * until the process exits.  This entry point allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ *   - Shapes whose partials need more than 8 MiB (see
+ *     rr_layernorm_bwd_workspace_size) return RR_ERR_WORKSPACE_TOO_SMALL.
+ *   - The first call on each device resolves the scratch's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one scratch array, which keeps the last
+ *     call's contents.  Calls that overlap on the GPU (e.g. on two streams
+ *     without ordering between them) race on it and give wrong dgamma / dbeta.
+ */
+rr_status rr_layernorm_bwd_noalloc(const void *dy, const void *x, const float *mean,
+                                   const float *rstd, const void *gamma, void *dx,
+                                   void *dgamma, void *dbeta, int64_t rows, int64_t cols,
+                                   rr_dtype dtype, cudaStream_t stream);
 
 /*
  * Reads (and if `reset` is non-zero clears) the error word of `device` that

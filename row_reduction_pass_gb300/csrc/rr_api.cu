@@ -307,6 +307,9 @@ int* device_error_word() {
 
 }  // namespace
 
+// Lets the other translation units of the library report a detail string.
+void rr_set_error_detail(const char* msg) { g_detail = msg ? msg : ""; }
+
 extern "C" {
 
 const char* rr_status_string(rr_status s) {

@@ -64,6 +64,8 @@ def load_library():
         lib.rr_layernorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
                                          i64, i64, st, vp]
         lib.rr_layernorm_bwd.restype = st
+        lib.rr_layernorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, st, vp]
+        lib.rr_layernorm_bwd_noalloc.restype = st
         lib.rr_last_error_detail.argtypes = []
         lib.rr_last_error_detail.restype = ctypes.c_char_p
         lib.rr_read_device_error.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), st]
@@ -155,6 +157,17 @@ def rr_layernorm_bwd(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, workspace=None
     _check("rr_layernorm_bwd", load_library().rr_layernorm_bwd(
         _p(dy), _p(x), _p(mean), _p(rstd), _p(gamma), _p(dx), _p(dgamma), _p(dbeta),
         _p(workspace), workspace.numel() * workspace.element_size(), rows, cols,
+        _dtype(x), _stream(stream)))
+
+
+def rr_layernorm_bwd_noalloc(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, stream=None):
+    """rr_layernorm_bwd without a workspace argument: the library's fixed 8 MiB
+    scratch holds the column partials (for callers that cannot allocate).
+    Calls on one device must not overlap on the GPU."""
+    _contig(dy, x, mean, rstd, gamma, dx, dgamma, dbeta)
+    rows, cols = x.shape
+    _check("rr_layernorm_bwd_noalloc", load_library().rr_layernorm_bwd_noalloc(
+        _p(dy), _p(x), _p(mean), _p(rstd), _p(gamma), _p(dx), _p(dgamma), _p(dbeta), rows, cols,
         _dtype(x), _stream(stream)))
 
 
