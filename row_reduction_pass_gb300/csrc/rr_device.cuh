@@ -26,6 +26,38 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Elementwise maximum of two packed bf16 pairs (exact; -inf is neutral).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Packed two-lane float32 arithmetic (one FMA-pipe instruction for two
+// values; each lane is an IEEE round-to-nearest operation like its scalar form).
+__device__ __forceinline__ void fma2(float& dx, float& dy, float ax, float ay, float bx, float by,
+                                     float cx, float cy) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(dx), "=f"(dy)
+      : "f"(ax), "f"(ay), "f"(bx), "f"(by), "f"(cx), "f"(cy));
+}
+__device__ __forceinline__ void add2(float& dx, float& dy, float ax, float ay, float bx, float by) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(dx), "=f"(dy)
+      : "f"(ax), "f"(ay), "f"(bx), "f"(by));
+}
+__device__ __forceinline__ void mul2(float& dx, float& dy, float ax, float ay, float bx, float by) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(dx), "=f"(dy)
+      : "f"(ax), "f"(ay), "f"(bx), "f"(by));
+}
+
 // ---------------------------------------------------------------- storage ---
 
 __device__ __forceinline__ uint32_t word_of(const uint4& c, int k) {

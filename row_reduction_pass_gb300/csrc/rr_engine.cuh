@@ -54,55 +54,72 @@ struct RowRegs {
   }
 };
 
-// Where one thread's chunks of the current row slice live.
+// Where one thread's chunks of the current row slice live.  Indices inside a
+// row are 32-bit (rows are limited to 2^31 columns); per row the thread's
+// chunk count and the range of its full (fully valid) chunks are computed once.
 template <int DT, int W>
 struct RowGeo {
   static constexpr int E = DType<DT>::E;
   static constexpr bool kChunk = (W > 1);
-  int64_t c0, c1;     // valid columns of the slice
-  int64_t colbase;    // column of element 0 of chunk 0 (c0 - head in chunk mode)
-  int64_t nch;        // chunks (elements in element mode) of the slice
-  int64_t first;      // this thread's first chunk index
-  int32_t step;       // chunk stride between a thread's chunks (= G)
-  int32_t head_bytes; // (slice start) - (chunk 0 address), 0..15 (chunk mode)
+  int c0, c1;       // valid columns of the slice
+  int colbase;      // column of element 0 of chunk 0 (c0 - head in chunk mode)
+  int nch;          // chunks (elements in element mode) of the slice
+  int first;        // this thread's first chunk index
+  int step;         // chunk stride between a thread's chunks (= G)
+  int head_bytes;   // (slice start) - (chunk 0 address), 0..15 (chunk mode)
+  int nq;           // chunks this thread owns
+  int qlo, qhi;     // its chunks q in [qlo, qhi) are full
 
-  // Set up for a slice whose first element sits at byte offset `start_off` of
-  // tensor 0 (all tensors of a row share the offset modulo 16 in chunk mode).
   __device__ __forceinline__ void init(int64_t c0_, int64_t c1_, uint64_t start_addr,
-                                       int64_t first_, int step_) {
-    c0 = c0_;
-    c1 = c1_;
+                                       int first_, int step_) {
+    c0 = static_cast<int>(c0_);
+    c1 = static_cast<int>(c1_);
     first = first_;
     step = step_;
+    int cf_lo, cf_hi;
     if constexpr (kChunk) {
-      int head = static_cast<int>(start_addr & 15u) / E;
+      const int head = static_cast<int>(start_addr & 15u) / E;
       head_bytes = head * E;
       colbase = c0 - head;
-      nch = (head + (c1 - c0) + W - 1) / W;
+      const int span = head + (c1 - c0);
+      nch = span > 0 ? (span + W - 1) / W : 0;
+      cf_lo = head > 0 ? 1 : 0;
+      cf_hi = span > 0 ? span / W : 0;
     } else {
       head_bytes = 0;
       colbase = c0;
-      nch = c1 - c0;
+      nch = c1 > c0 ? c1 - c0 : 0;
+      cf_lo = 0;
+      cf_hi = nch;
     }
+    nq = nch > first ? (nch - first + step - 1) / step : 0;
+    qlo = first < cf_lo ? 1 : 0;
+    qhi = cf_hi > first ? (cf_hi - first + step - 1) / step : 0;
   }
-  __device__ __forceinline__ int64_t chunk(int q) const { return first + (int64_t)q * step; }
-  __device__ __forceinline__ bool has(int q) const { return chunk(q) < nch; }
-  __device__ __forceinline__ int64_t col(int q, int e) const { return colbase + chunk(q) * W + e; }
-  __device__ __forceinline__ bool full(int q) const {
-    if constexpr (kChunk) {
-      int64_t j = colbase + chunk(q) * W;
-      return j >= c0 && j + W <= c1;
-    } else {
-      return true;
-    }
-  }
+  __device__ __forceinline__ int chunk(int q) const { return first + q * step; }
+  __device__ __forceinline__ bool has(int q) const { return q < nq; }
+  __device__ __forceinline__ int col(int q, int e) const { return colbase + chunk(q) * W + e; }
+  __device__ __forceinline__ bool full(int q) const { return q >= qlo && q < qhi; }
   __device__ __forceinline__ bool valid(int q, int e) const {
-    int64_t j = col(q, e);
+    const int j = col(q, e);
     return j >= c0 && j < c1;
   }
   // Byte offset of chunk q from the slice's chunk-0 address.
   __device__ __forceinline__ int64_t off(int q) const {
-    return kChunk ? chunk(q) * 16 : chunk(q) * E;
+    return kChunk ? (int64_t)chunk(q) * 16 : (int64_t)chunk(q) * E;
+  }
+  // (q, e) of column j if this thread owns it, else q = -1.
+  __device__ __forceinline__ void locate(int j, int& q, int& e) const {
+    q = -1;
+    e = 0;
+    const int lc = j - colbase;
+    if (j < c0 || j >= c1 || lc < 0) return;
+    const int c = lc / W;
+    const int d = c - first;
+    if (d < 0 || d % step != 0) return;
+    if (d / step >= nq) return;
+    q = d / step;
+    e = lc - c * W;
   }
 
   // Calls f(q, e) for every valid element this thread owns.
@@ -144,6 +161,22 @@ struct RowGeo {
       } else {
         st_elem<DT>(p, out(q, 0));
       }
+    }
+  }
+
+  // Stores chunk q from the W values f[] (only its valid elements if ragged).
+  __device__ __forceinline__ void store_chunk(char* g0, int q, const float* f) const {
+    char* p = g0 + off(q);
+    if constexpr (kChunk) {
+      if (full(q)) {
+        st_chunk_stream(p, chunk_pack<DT>(f));
+      } else {
+#pragma unroll
+        for (int e = 0; e < W; ++e)
+          if (valid(q, e)) st_elem<DT>(p + e * E, f[e]);
+      }
+    } else {
+      st_elem<DT>(p, f[0]);
     }
   }
 };
@@ -217,7 +250,19 @@ __device__ __forceinline__ void load_staged(RowRegs<DT, W, NT, NQ>& r, int t,
 template <class S, int G, class M>
 __device__ __forceinline__ S reduce_group(S s, M merge, S* red, int parity, int gt,
                                           int bar_id) {
-  if constexpr (G <= 32) {
+  if constexpr (S::kNary) {
+    // n-ary form of the pairwise merge: M = max_i m_i, D = sum_i d_i e^(m_i - M);
+    // butterflies of max and of plain sums are bitwise identical on every lane.
+    s = S::template nary<(G < 32 ? G : 32)>(s);
+    if constexpr (G > 32) {
+      const int lane = threadIdx.x & 31;
+      S* slot = red + parity * 32;
+      if (lane == 0) slot[gt >> 5] = s;
+      named_bar(bar_id, G);
+      s = S::template nary<32>((lane < G / 32) ? slot[lane] : S::identity());
+    }
+    return s;
+  } else if constexpr (G <= 32) {
     return group_reduce<S, M, G>(s, merge);
   } else {
     s = group_reduce<S, M, 32>(s, merge);
@@ -372,11 +417,18 @@ __global__ void __launch_bounds__(MAXT) row_kernel(const typename Op::Params p, 
       }
     }
     uint32_t phase = 0;  // bit b: parity of the next completion of buffer b
+    // per-row metadata is loaded one row ahead (and, for the copy issuer, the
+    // row nbuf ahead) so no global load sits on the per-row critical path
+    typename Op::Meta m_next = Op::meta(p, cid < geo.rows ? cid : -1);
     for (int64_t i = 0;; ++i) {
       const int64_t r = cid + i * ncl;
       if (r >= geo.rows) break;
       const int b = static_cast<int>(i % geo.nbuf);
-      typename Op::Meta m = Op::meta(p, r);
+      const typename Op::Meta m = m_next;
+      m_next = Op::meta(p, r + ncl < geo.rows ? r + ncl : -1);
+      const int64_t rfar = r + (int64_t)geo.nbuf * ncl;
+      typename Op::Meta m_far{};
+      if (threadIdx.x == 0 && rfar < geo.rows) m_far = Op::meta(p, rfar);
       RowGeo<DT, W> g;
       g.init(c0, c1, Op::start_addr(p, r, c0), gt, G);
       const bool use = !Op::skip(m);
@@ -393,10 +445,7 @@ __global__ void __launch_bounds__(MAXT) row_kernel(const typename Op::Params p, 
       S s = use ? Op::thread_stats(ts, cur, g, m) : S::identity();
       s = reduce_group<S, G>(s, typename Op::Merge(), red, static_cast<int>(i & 1), gt, bar_id);
       // every thread is done reading buffer b: refill it with the row nbuf ahead
-      if (threadIdx.x == 0) {
-        const int64_t rn = r + (int64_t)geo.nbuf * ncl;
-        if (rn < geo.rows && !Op::skip(Op::meta(p, rn))) issue(rn, b);
-      }
+      if (threadIdx.x == 0 && rfar < geo.rows && !Op::skip(m_far)) issue(rfar, b);
       if (K > 1) s = reduce_cluster<S>(s, typename Op::Merge(), cl_slot, static_cast<int>(i & 1), K);
       Op::finish(ts, p, geo, r, m, s, cur, g, gt == 0 && rank == 0);
     }

@@ -55,7 +55,19 @@ struct LnBwdParams {
 
 // Online-softmax state: running maximum m and sum d of exp(x - m).
 struct MaxSum {
+  static constexpr bool kNary = true;
   float m, d;
+  // Merge of the states of L consecutive lanes (L a power of two <= 32).
+  template <int L>
+  __device__ __forceinline__ static MaxSum nary(MaxSum v) {
+    float m = v.m;
+#pragma unroll
+    for (int off = L / 2; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float d = (v.m == -INFINITY) ? 0.f : v.d * ex2((v.m - m) * kLog2e);
+#pragma unroll
+    for (int off = L / 2; off >= 1; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    return {m, d};
+  }
   __device__ __forceinline__ static MaxSum identity() { return {-INFINITY, 0.f}; }
   __device__ __forceinline__ static MaxSum shfl_xor(const MaxSum& v, int off) {
     return {__shfl_xor_sync(0xffffffffu, v.m, off), __shfl_xor_sync(0xffffffffu, v.d, off)};
@@ -80,6 +92,7 @@ struct MergeMaxSum {
 // even when large values cancel: (count n, sum S = sh + sl, M2 = sum of squared
 // deviations from the mean).
 struct Moments {
+  static constexpr bool kNary = false;
   float n, sh, sl, m2;
   __device__ __forceinline__ static Moments identity() { return {0.f, 0.f, 0.f, 0.f}; }
   __device__ __forceinline__ static Moments shfl_xor(const Moments& v, int off) {
@@ -134,6 +147,7 @@ struct MergeMoments {
 
 // Two plain sums.
 struct Sum2 {
+  static constexpr bool kNary = false;
   float s1, s2;
   __device__ __forceinline__ static Sum2 identity() { return {0.f, 0.f}; }
   __device__ __forceinline__ static Sum2 shfl_xor(const Sum2& v, int off) {
@@ -214,14 +228,57 @@ struct OpSoftmaxXent {
   __device__ __forceinline__ static void thread_init(Thread&, const Params&, const Geo&, int64_t,
                                                      int64_t, int, int) {}
 
+  // Row maximum of the thread's slots.  Ragged slots hold -inf, so every slot
+  // of every owned chunk can take part (bf16: packed max, two values at once).
+  __device__ __forceinline__ static float thread_max(const RowRegs<DT, W, NT, NQ>& x,
+                                                     const RowGeo<DT, W>& g) {
+    if constexpr (W > 1 && DT == kBF16) {
+      uint32_t mw = 0xff80ff80u;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (!g.has(q)) break;
+        const uint4 c = x.v[0][q];
+        mw = bf16x2_max(mw, bf16x2_max(bf16x2_max(c.x, c.y), bf16x2_max(c.z, c.w)));
+      }
+      return fmaxf(__uint_as_float(mw << 16), __uint_as_float(mw & 0xffff0000u));
+    } else {
+      float m = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (!g.has(q)) break;
+#pragma unroll
+        for (int e = 0; e < W; ++e) m = fmaxf(m, x.get(0, q, e));
+      }
+      return m;
+    }
+  }
+
+  // Online-softmax state of the thread: m = its maximum, d = sum of exp(x - m).
+  // The exponent is one FMA, x*log2(e) - fl(m*log2(e)); the rounding residual
+  // r of fl(m*log2(e)) shifts every term by the same factor 2^r, which is
+  // divided out once (so d is the plain sum of exp(x - m)).
   __device__ __forceinline__ static Stats thread_stats(Thread&, const RowRegs<DT, W, NT, NQ>& x,
                                                        const RowGeo<DT, W>& g, const Meta&) {
-    float m = -INFINITY;
-    g.template for_each<NQ>([&](int q, int e) { m = fmaxf(m, x.get(0, q, e)); });
-    float d = 0.f;
-    if (m != -INFINITY)
-      g.template for_each<NQ>([&](int q, int e) { d += ex2((x.get(0, q, e) - m) * kLog2e); });
-    return {m, d};
+    const float m = thread_max(x, g);
+    if (m == -INFINITY) return {m, 0.f};
+    const float mL = m * kLog2e;
+    const float r = fmaf(m, kLog2e, -mL);
+    float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (!g.has(q)) break;
+#pragma unroll
+      for (int e = 0; e < W; e += 2) {
+        if constexpr (W > 1) {
+          float t0, t1;
+          fma2(t0, t1, x.get(0, q, e), x.get(0, q, e + 1), kLog2e, kLog2e, -mL, -mL);
+          add2(d0, d1, d0, d1, ex2(t0), ex2(t1));
+        } else {
+          d0 += ex2(fmaf(x.get(0, q, e), kLog2e, -mL));
+        }
+      }
+    }
+    return {m, (d0 + d1) * ex2(-r)};
   }
 
   __device__ __forceinline__ static void finish(Thread&, const Params& p, const Geo& geo,
@@ -230,32 +287,61 @@ struct OpSoftmaxXent {
                                                 const RowGeo<DT, W>& g, bool leader) {
     char* y0 = p.y + (r * p.cols + g.c0) * E - g.head_bytes;
     const bool masked = (s.m == -INFINITY);
+    int ql = -1, el = 0;  // where this thread holds the label column, if it does
     if (p.labels != nullptr) {
       const int32_t label = mt.label;
       const bool in_range = label >= 0 && (int64_t)label < geo.cols;
       // an out-of-range label is counted whatever the row holds
       if (!mt.skip && !in_range && leader && p.bad != nullptr) atomicAdd(p.bad, 1);
+      if (in_range && !mt.skip) g.locate(label, ql, el);
       if (mt.skip || masked) {
         if (leader) p.loss[r] = 0.f;
       } else if (!in_range) {
         if (leader) p.loss[r] = __int_as_float(0x7fc00000);
-      } else {
-        g.template for_each<NQ>([&](int q, int e) {
-          if (g.col(q, e) == label) p.loss[r] = (s.m - x.get(0, q, e)) + logf(s.d);
-        });
+      } else if (ql >= 0) {
+        float xl = 0.f;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+#pragma unroll
+          for (int e = 0; e < W; ++e)
+            if (q == ql && e == el) xl = x.get(0, q, e);
+        p.loss[r] = (s.m - xl) + logf(s.d);
       }
     }
     if (mt.skip || masked) {
-      g.template store<NQ>(y0, [&](int, int) { return 0.f; });
+      const float z[W] = {};
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (!g.has(q)) break;
+        g.store_chunk(y0, q, z);
+      }
       return;
     }
-    const float inv = 1.0f / s.d;
-    const int64_t label = (p.labels != nullptr) ? (int64_t)mt.label : (int64_t)-1;
-    g.template store<NQ>(y0, [&](int q, int e) {
-      float v = ex2((x.get(0, q, e) - s.m) * kLog2e) * inv;
-      if (g.col(q, e) == label) v -= 1.0f;
-      return v;
-    });
+    // p_j = 2^(x_j log2 e - fl(m log2 e)) * 2^(-r) / d
+    const float mL = s.m * kLog2e;
+    const float rr = fmaf(s.m, kLog2e, -mL);
+    const float inv = ex2(-rr) / s.d;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (!g.has(q)) break;
+      float f[W];
+      if constexpr (W > 1) {
+#pragma unroll
+        for (int e = 0; e < W; e += 2) {
+          float t0, t1;
+          fma2(t0, t1, x.get(0, q, e), x.get(0, q, e + 1), kLog2e, kLog2e, -mL, -mL);
+          mul2(f[e], f[e + 1], ex2(t0), ex2(t1), inv, inv);
+        }
+      } else {
+        f[0] = ex2(fmaf(x.get(0, q, 0), kLog2e, -mL)) * inv;
+      }
+      if (q == ql) {
+#pragma unroll
+        for (int e = 0; e < W; ++e)
+          if (e == el) f[e] -= 1.0f;
+      }
+      g.store_chunk(y0, q, f);
+    }
   }
   __device__ __forceinline__ static void epilogue(Thread&, const Params&, const Geo&,
                                                   unsigned char*, int64_t, int64_t, int64_t, int,
