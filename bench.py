@@ -451,6 +451,85 @@ def run_profile_case(args):
     print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps}))
 
 
+def run_sweep(args):
+    """Times every operation of every measured workload on its own (L2 flushed
+    between repetitions by writing a 256 MB buffer), against the HBM roofline.
+    Prints one JSON line per case; not the contract line."""
+    import torch
+    import row_reduction_pass_gb300 as rr
+
+    dev = torch.device("cuda", 0)
+    rr.load_library()
+    peak, peak_src = hbm_peak()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    reps = max(3, args.steps)
+
+    def tdev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def report(name, op, nbytes, ms):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        print(json.dumps({"case": name, "op": op, "bytes": nbytes, "us": round(ms * 1e3, 2),
+                          "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                          "peak": peak, "peak_source": peak_src}), flush=True)
+
+    names = ["xent_f32_64x1000", "ln_f32_4096x768", "softmax_bf16_causal_65536x512",
+             "xent_bf16_16384x50304"]
+    names += [f"sweep_{k}_{dt}_c{c}" for dt in ("f32", "bf16") for c in synth.SWEEP_COLS
+              for k in ("xent", "ln")]
+    if args.cases:
+        names = [n for n in names if any(c in n for c in args.cases.split(","))]
+    for name in names:
+        d = synth.make(name)
+        e = 2 if d["dtype"] == "bf16" else 4
+        if d["kind"] == "xent":
+            x, lab = tdev(d["logits"]), tdev(d["labels"])
+            R, C = x.shape
+            loss = torch.empty(R, device=dev)
+            y = torch.empty_like(x)
+            n_ign = int((d["labels"] == synth.IGNORE_INDEX).sum())
+            ms = timed(lambda: rr.rr_softmax_xent_fwd_bwd(x, lab, loss, y))
+            report(name, "xent", xent_bytes(R, C, e, n_ign), ms)
+        elif d["kind"] == "causal":
+            x = tdev(d["x"])
+            y = torch.empty_like(x)
+            ms = timed(lambda: rr.rr_softmax_fwd(x, y))
+            report(name, "softmax", softmax_bytes(*x.shape, e), ms)
+        else:
+            x, g, b, dy = (tdev(d[k]) for k in ("x", "gamma", "beta", "dy"))
+            R, C = x.shape
+            y, dx = torch.empty_like(x), torch.empty_like(x)
+            mean, rstd = torch.empty(R, device=dev), torch.empty(R, device=dev)
+            dg, db = torch.empty_like(g), torch.empty_like(g)
+            ws = torch.empty(max(1, rr.rr_layernorm_bwd_workspace_size(R, C, x.dtype)),
+                             dtype=torch.uint8, device=dev)
+            fb, bb = ln_bytes(R, C, e)
+            mf = timed(lambda: rr.rr_layernorm_fwd(x, g, b, y, mean, rstd, eps=d["eps"]))
+            mb = timed(lambda: rr.rr_layernorm_bwd(dy, x, mean, rstd, g, dx, dg, db, ws))
+            report(name, "ln_fwd", fb, mf)
+            report(name, "ln_bwd", bb, mb)
+            report(name, "ln_fwd+bwd", fb + bb, mf + mb)
+        del d
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -463,7 +542,13 @@ def main():
     ap.add_argument("--profile", choices=["xent", "softmax", "ln_fwd", "ln_bwd"], default=None,
                     help="run only this kernel (for ncu captures of one kernel)")
     ap.add_argument("--profile-rows", type=int, default=0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every workload and sweep case separately (one JSON line each)")
+    ap.add_argument("--cases", default="", help="comma-separated name filters for --sweep")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.profile:
         run_profile_case(args)
         return
