@@ -470,19 +470,39 @@ def run_sweep(args):
         return torch.from_numpy(a).to(dev)
 
     def timed(fn):
+        """Device time of one call: CUDA-graph replay of `reps` x (L2 flush, call)
+        minus the replay of `reps` x (L2 flush), so host launch latency is
+        excluded and every call starts with a cold L2."""
         for _ in range(args.warmup):
             fn()
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g_both, g_flush = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g_both, stream=s):
+                for _ in range(reps):
+                    flush.zero_()
+                    fn()
+            with torch.cuda.graph(g_flush, stream=s):
+                for _ in range(reps):
+                    flush.zero_()
+        torch.cuda.synchronize()
+
+        def run(gr):
+            gr.replay()
+            torch.cuda.synchronize()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()
-            fn()
+            gr.replay()
             b.record()
             torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
+            return a.elapsed_time(b)
+
+        t_both = min(run(g_both) for _ in range(3))
+        t_flush = min(run(g_flush) for _ in range(3))
+        return max(t_both - t_flush, 1e-6) / reps
 
     def report(name, op, nbytes, ms):
         gbs = nbytes / (ms * 1e-3) / 1e9

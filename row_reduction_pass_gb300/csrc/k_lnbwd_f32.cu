@@ -3,6 +3,6 @@
 #include "rr_instantiate.cuh"
 
 namespace rr {
-KernelSet lnbwd_kernels_f32() { return make_kernel_set<OpLnBwd, kF32, 2, 8, 512, 2, 18, 512>(); }
+KernelSet lnbwd_kernels_f32() { return make_kernel_set<OpLnBwd, kF32, 3, 8, 512, 5, 18, 512>(); }
 const void* col_reduce_kernel_ptr_f32() { return (const void*)col_reduce_kernel<kF32>; }
 }  // namespace rr

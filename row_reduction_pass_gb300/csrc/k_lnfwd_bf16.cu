@@ -3,5 +3,5 @@
 #include "rr_instantiate.cuh"
 
 namespace rr {
-KernelSet lnfwd_kernels_bf16() { return make_kernel_set<OpLnFwd, kBF16, 4, 8, 256, 4, 18, 512>(); }
+KernelSet lnfwd_kernels_bf16() { return make_kernel_set<OpLnFwd, kBF16, 4, 8, 256, 8, 18, 512>(); }
 }  // namespace rr

@@ -3,5 +3,5 @@
 #include "rr_instantiate.cuh"
 
 namespace rr {
-KernelSet softmax_kernels_bf16() { return make_kernel_set<OpSoftmaxXent, kBF16, 4, 8, 256, 8, 16, 1024>(); }
+KernelSet softmax_kernels_bf16() { return make_kernel_set<OpSoftmaxXent, kBF16, 2, 8, 256, 8, 16, 1024>(); }
 }  // namespace rr

@@ -3,5 +3,5 @@
 #include "rr_instantiate.cuh"
 
 namespace rr {
-KernelSet softmax_kernels_f32() { return make_kernel_set<OpSoftmaxXent, kF32, 4, 8, 256, 8, 16, 1024>(); }
+KernelSet softmax_kernels_f32() { return make_kernel_set<OpSoftmaxXent, kF32, 2, 8, 256, 8, 16, 1024>(); }
 }  // namespace rr

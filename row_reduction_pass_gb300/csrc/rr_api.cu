@@ -120,7 +120,6 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
   const int E = dt == RR_BF16 ? 2 : 4;
   const int V = 16 / E;
   const int NT = op == kLnBwd ? 2 : 1;
-  const int sb = ks.stats_bytes;
   pl->mode = mode;
   pl->geo.rows = rows;
   pl->geo.cols = cols;
@@ -137,8 +136,9 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
     const int G = 1 << gi;
     const int T = ks.maxt_direct;
     const int ngroups = T / G;
-    size_t red = (size_t)((G > 32 ? ngroups * 64 : 0) + 2) * sb;
-    size_t col = (op == kLnBwd && ngroups > 1) ? (size_t)ngroups * 2 * cols * 4 : 0;
+    size_t red = (size_t)(G > 32 ? ngroups * 1024 : 0) + 32;
+    const int W = mode == 0 ? V : 1;
+    size_t col = (op == kLnBwd) ? (size_t)ngroups * 2 * round_up(cols, W) * 4 : 0;
     size_t smem = round_up((int64_t)red, 16) + col;
     if ((int64_t)smem <= di->smem_optin) {
       const void* fn = ks.direct[mode][gi];
@@ -188,14 +188,16 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
     return fail(RR_ERR_INVALID_ARG, "cols=%lld is beyond the supported row length for this operation",
                 (long long)cols);
   const int64_t buf_bytes = round_up(slice * E + 32, 128);
-  const int64_t fixed = 2 * 8 + 16 + (int64_t)(64 + 2) * sb;
+  const int64_t colb = (op == kLnBwd) ? 2 * round_up(slice, mode == 0 ? V : 1) * 4 : 0;
+  const int64_t fixed = 2 * 8 + 32 + 1024 + 32 + colb;
   int nbuf = 2;
   if (nbuf * NT * buf_bytes + fixed > di->smem_optin) nbuf = 1;
   if (nbuf * NT * buf_bytes + fixed > di->smem_optin)
     return fail(RR_ERR_INVALID_ARG, "row slice of %lld bytes does not fit shared memory",
                 (long long)(slice * E));
   const int64_t red_off = round_up(nbuf * NT * buf_bytes + nbuf * 8, 16);
-  const size_t smem = (size_t)(red_off + (int64_t)(64 + 2) * sb);
+  const int64_t col_off = round_up(red_off + 1024 + 32, 16);
+  const size_t smem = (size_t)(col_off + colb);
   const void* fn = ks.staged[mode];
   if ((st = set_smem(di, fn, smem)) != RR_OK) return st;
   int64_t grid;
@@ -239,7 +241,7 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
   pl->geo.nbuf = nbuf;
   pl->geo.buf_bytes = (int32_t)buf_bytes;
   pl->geo.red_off = (int32_t)red_off;
-  pl->geo.col_off = (int32_t)smem;
+  pl->geo.col_off = (int32_t)col_off;
   return RR_OK;
 }
 
@@ -401,14 +403,15 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
       overlaps(rstd, nr, y, n) || overlaps(mean, nr, gamma, nc) || overlaps(mean, nr, beta, nc) ||
       overlaps(rstd, nr, gamma, nc) || overlaps(rstd, nr, beta, nc))
     return fail(RR_ERR_ALIASING, "outputs overlap inputs");
-  const bool al = (cols * E) % 16 == 0 && aligned(x, 16) && aligned(y, 16) && aligned(gamma, 16) &&
-                  aligned(beta, 16);
+  // column-aligned chunks need 16-byte aligned gamma / beta; rows may have any alignment
+  const bool al = aligned(gamma, 16) && aligned(beta, 16);
   Plan pl;
   if ((st = plan_any(kLnFwd, dtype, al, true, rows, cols, &pl)) != RR_OK) return st;
   int* err = device_error_word();
   if (!err) return RR_ERR_CUDA;
   rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma),
-                    static_cast<const char*>(beta), static_cast<char*>(y), mean, rstd, err, cols, eps};
+                    static_cast<const char*>(beta), static_cast<char*>(y), mean, rstd, err, cols, eps,
+                    static_cast<float>(1.0 / static_cast<double>(cols))};
   if ((st = launch(pl, p, stream)) != RR_OK) return st;
   return ok();
 }
@@ -463,8 +466,7 @@ rr_status rr_layernorm_bwd(const void* dy, const void* x, const float* mean, con
   }
   if (overlaps(dx, n, mean, nr) || overlaps(dx, n, rstd, nr) || overlaps(dx, n, gamma, nc))
     return fail(RR_ERR_ALIASING, "dx overlaps mean / rstd / gamma");
-  const bool al = (cols * E) % 16 == 0 && aligned(dy, 16) && aligned(x, 16) && aligned(dx, 16) &&
-                  aligned(gamma, 16);
+  const bool al = aligned(gamma, 16);
   Plan pl;
   size_t need = 0;
   if (rows == 0) {
@@ -483,7 +485,8 @@ rr_status rr_layernorm_bwd(const void* dy, const void* x, const float* mean, con
     if (!err) return RR_ERR_CUDA;
     rr::LnBwdParams p{static_cast<const char*>(dy), static_cast<const char*>(x), mean, rstd,
                       static_cast<const char*>(gamma), static_cast<char*>(dx),
-                      static_cast<float*>(workspace), err, cols};
+                      static_cast<float*>(workspace), err, cols,
+                      static_cast<float>(1.0 / static_cast<double>(cols))};
     if ((st = launch(pl, p, stream)) != RR_OK) return st;
   }
   const void* cr = dtype == RR_BF16 ? rr::col_reduce_kernel_ptr_bf16() : rr::col_reduce_kernel_ptr_f32();
@@ -492,7 +495,7 @@ rr_status rr_layernorm_bwd(const void* dy, const void* x, const float* mean, con
   char* dg = static_cast<char*>(dgamma);
   char* db = static_cast<char*>(dbeta);
   void* args[] = {&ws, &P, &cols, &dg, &db};
-  cudaError_t e = cudaLaunchKernel(cr, dim3((unsigned)cdiv(2 * cols, 32)), dim3(256), args, 0, stream);
+  cudaError_t e = cudaLaunchKernel(cr, dim3((unsigned)cdiv(2 * cols, 32)), dim3(1024), args, 0, stream);
   if (e != cudaSuccess) return fail(RR_ERR_CUDA, "column reduce launch: %s", cudaGetErrorString(e));
   return ok();
 }

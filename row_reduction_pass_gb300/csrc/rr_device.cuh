@@ -172,6 +172,71 @@ __device__ __forceinline__ void st_chunk_stream(char* p, uint4 v) {
   __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
+// --- 16-byte accesses at addresses that are element-aligned but not 16-byte
+// aligned (rows whose start is not 16-byte aligned, read in column-aligned
+// chunks).  h = address % 16 (a multiple of the element size).
+
+// Bytes [h, h + 16) of the 32-byte pair lo:hi.
+__device__ __forceinline__ uint4 funnel16(const uint4& lo, const uint4& hi, int h) {
+  const int sh = (h & 3) * 8;
+  uint32_t a0, a1, a2, a3, a4;
+  switch (h >> 2) {
+    case 0: a0 = lo.x; a1 = lo.y; a2 = lo.z; a3 = lo.w; a4 = hi.x; break;
+    case 1: a0 = lo.y; a1 = lo.z; a2 = lo.w; a3 = hi.x; a4 = hi.y; break;
+    case 2: a0 = lo.z; a1 = lo.w; a2 = hi.x; a3 = hi.y; a4 = hi.z; break;
+    default: a0 = lo.w; a1 = hi.x; a2 = hi.y; a3 = hi.z; a4 = hi.w; break;
+  }
+  return make_uint4(__funnelshift_r(a0, a1, sh), __funnelshift_r(a1, a2, sh),
+                    __funnelshift_r(a2, a3, sh), __funnelshift_r(a3, a4, sh));
+}
+
+// Loads [p, p + 16) through the two aligned 16-byte chunks that hold it (read
+// through L1, where the neighbouring lane's load of the same chunk hits).  The
+// caller guarantees both aligned chunks lie inside the allocation.
+__device__ __forceinline__ uint4 ld16_split(const char* p) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uint4* b = reinterpret_cast<const uint4*>(a & ~uintptr_t(15));
+  return funnel16(__ldg(b), __ldg(b + 1), static_cast<int>(a & 15));
+}
+
+__device__ __forceinline__ void st_b16(char* p, uint32_t v) {
+  asm volatile("st.global.cs.b16 [%0], %1;" ::"l"(p), "h"(static_cast<unsigned short>(v)) : "memory");
+}
+__device__ __forceinline__ void st_b32(char* p, uint32_t v) {
+  asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_v2(char* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+// Stores the 16 bytes v at p (p % 16 != 0, p % 2 == 0) as aligned pieces.
+__device__ __forceinline__ void st16_split(char* p, const uint4& v) {
+  const int h = static_cast<int>(reinterpret_cast<uintptr_t>(p) & 15);
+  if ((h & 3) == 0) {
+    if (h == 8) {
+      st_v2(p, v.x, v.y);
+      st_v2(p + 8, v.z, v.w);
+    } else {  // h = 4 or 12: p + 4 is 8-byte aligned
+      st_b32(p, v.x);
+      st_v2(p + 4, v.y, v.z);
+      st_b32(p + 12, v.w);
+    }
+  } else {  // h = 2 mod 4: the middle 12 bytes are v shifted by 16 bits
+    const uint32_t u0 = __funnelshift_r(v.x, v.y, 16);
+    const uint32_t u1 = __funnelshift_r(v.y, v.z, 16);
+    const uint32_t u2 = __funnelshift_r(v.z, v.w, 16);
+    st_b16(p, v.x & 0xffffu);
+    if ((reinterpret_cast<uintptr_t>(p + 2) & 7) == 0) {
+      st_v2(p + 2, u0, u1);
+      st_b32(p + 10, u2);
+    } else {
+      st_b32(p + 2, u0);
+      st_v2(p + 6, u1, u2);
+    }
+    st_b16(p + 14, v.w >> 16);
+  }
+}
+
 // ------------------------------------------------------------- reductions ---
 
 // Ordered butterfly over the lanes of a G-lane group (G a power of two <= 32):

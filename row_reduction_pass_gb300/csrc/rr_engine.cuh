@@ -181,9 +181,10 @@ struct RowGeo {
   }
 };
 
-// Direct load of a thread's share of tensor t (fill = value for ragged slots).
+// Direct load of a thread's share of tensor t in memory-aligned chunks (fill =
+// value for ragged slots).
 template <int DT, int W, int NT, int NQ>
-__device__ __forceinline__ void load_direct(RowRegs<DT, W, NT, NQ>& r, int t,
+__device__ __forceinline__ void load_direct_mem(RowRegs<DT, W, NT, NQ>& r, int t,
                                             const RowGeo<DT, W>& g, const char* g0,
                                             float fill) {
   constexpr int E = DType<DT>::E;
@@ -211,7 +212,7 @@ __device__ __forceinline__ void load_direct(RowRegs<DT, W, NT, NQ>& r, int t,
 // mirror of the slice, whose byte 0 corresponds to address floor16(slice start);
 // ragged pieces are read from global memory.
 template <int DT, int W, int NT, int NQ>
-__device__ __forceinline__ void load_staged(RowRegs<DT, W, NT, NQ>& r, int t,
+__device__ __forceinline__ void load_staged_mem(RowRegs<DT, W, NT, NQ>& r, int t,
                                             const RowGeo<DT, W>& g, const char* g0,
                                             const unsigned char* sbuf, float fill) {
   constexpr int E = DType<DT>::E;
@@ -243,58 +244,172 @@ __device__ __forceinline__ void load_staged(RowRegs<DT, W, NT, NQ>& r, int t,
   }
 }
 
-// Group-wide reduction of a statistic for groups of G threads (G <= 32: warp
-// shuffles only; G > 32: shuffles, then the per-warp results through shared
-// memory and a named barrier for the group).  `red` points at this group's
-// scratch of 2 x 32 statistics (double-buffered by row parity).
-template <class S, int G, class M>
-__device__ __forceinline__ S reduce_group(S s, M merge, S* red, int parity, int gt,
-                                          int bar_id) {
-  if constexpr (S::kNary) {
-    // n-ary form of the pairwise merge: M = max_i m_i, D = sum_i d_i e^(m_i - M);
-    // butterflies of max and of plain sums are bitwise identical on every lane.
-    s = S::template nary<(G < 32 ? G : 32)>(s);
-    if constexpr (G > 32) {
-      const int lane = threadIdx.x & 31;
-      S* slot = red + parity * 32;
-      if (lane == 0) slot[gt >> 5] = s;
-      named_bar(bar_id, G);
-      s = S::template nary<32>((lane < G / 32) ? slot[lane] : S::identity());
+// Loads a thread's column-aligned chunks of one row tensor.  Chunk k covers
+// columns c0 + kW .. c0 + kW + W - 1 of the slice and sits at s0 + 16k, where s0
+// (the slice start) may have any element alignment: an aligned chunk is one
+// 128-bit load; a misaligned one is the funnel shift of the two aligned chunks
+// holding it (from the shared-memory mirror when staged, else through L1), or
+// element loads where those would leave [tbeg, tend).  The last chunk of a row
+// may be ragged (columns >= c1 are filled with 0).
+template <int DT, int W, int NT, int NQ>
+__device__ __forceinline__ void load_cols(RowRegs<DT, W, NT, NQ>& r, int t, const RowGeo<DT, W>& g,
+                                          const char* s0, const char* tbeg, const char* tend,
+                                          const unsigned char* sbuf) {
+  constexpr int E = DType<DT>::E;
+  const uintptr_t sa = reinterpret_cast<uintptr_t>(s0);
+  const int h = static_cast<int>(sa & 15);
+  const uintptr_t mbase = sa & ~uintptr_t(15);
+  const uintptr_t mlo = (sa + 15) & ~uintptr_t(15);
+  const uintptr_t mhi = (sa + (uintptr_t)(g.c1 - g.c0) * E) & ~uintptr_t(15);
+  const uintptr_t tb = reinterpret_cast<uintptr_t>(tbeg), te = reinterpret_cast<uintptr_t>(tend);
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    if (!g.has(q)) break;
+    const char* a = s0 + (int64_t)g.chunk(q) * (W * E);
+    const uintptr_t aa = reinterpret_cast<uintptr_t>(a);
+    if constexpr (W > 1) {
+      if (g.full(q)) {
+        if (h == 0) {
+          r.v[t][q] = sbuf ? *reinterpret_cast<const uint4*>(sbuf + (aa - mbase)) : ld_chunk_stream(a);
+          continue;
+        }
+        const uintptr_t fa = aa & ~uintptr_t(15);
+        if (sbuf != nullptr && fa >= mlo && fa + 32 <= mhi) {
+          const uint4* m = reinterpret_cast<const uint4*>(sbuf + (fa - mbase));
+          r.v[t][q] = funnel16(m[0], m[1], h);
+          continue;
+        }
+        if (sbuf == nullptr && fa >= tb && fa + 32 <= te) {
+          r.v[t][q] = ld16_split(a);
+          continue;
+        }
+      }
+      uint4 c = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int e = 0; e < W; ++e)
+        if (g.valid(q, e)) chunk_set_bits<DT>(c, e, ld_elem_bits<DT>(a + e * E));
+      r.v[t][q] = c;
+    } else {
+      if (sbuf != nullptr && aa >= mlo && aa < mhi)
+        r.v[t][q] = ld_smem_elem<DT>(reinterpret_cast<const char*>(sbuf) + (aa - mbase));
+      else
+        r.v[t][q] = ld_elem<DT>(a);
     }
-    return s;
-  } else if constexpr (G <= 32) {
-    return group_reduce<S, M, G>(s, merge);
-  } else {
-    s = group_reduce<S, M, 32>(s, merge);
-    const int lane = threadIdx.x & 31;
-    const int w = gt >> 5;
-    S* slot = red + parity * 32;
-    if (lane == 0) slot[w] = s;
-    named_bar(bar_id, G);
-    S o = (lane < G / 32) ? slot[lane] : S::identity();
-    return group_reduce<S, M, 32>(o, merge);
   }
 }
 
-// Merge of the K per-CTA statistics of a cluster through distributed shared
-// memory; slot is this CTA's 2-entry slot array (double-buffered by parity).
-template <class S, class M>
-__device__ __forceinline__ S reduce_cluster(S s, M merge, S* slot, int parity, int K) {
-  if (threadIdx.x == 0) slot[parity] = s;
-  cluster_sync();
-  const int lane = threadIdx.x & 31;
-  S o = S::identity();
-  if (lane < K) o = S::load_remote(map_to_rank(&slot[parity], lane));
-  return group_reduce<S, M, 32>(o, merge);
+// Stores column-aligned chunk q, already packed into storage bits (chunk mode).
+template <int DT, int W>
+__device__ __forceinline__ void store_cols_bits(const RowGeo<DT, W>& g, char* s0, int q,
+                                                const uint4& v) {
+  constexpr int E = DType<DT>::E;
+  char* a = s0 + (int64_t)g.chunk(q) * (W * E);
+  if (g.full(q)) {
+    if ((reinterpret_cast<uintptr_t>(a) & 15) == 0) st_chunk_stream(a, v);
+    else st16_split(a, v);
+  } else {
+#pragma unroll
+    for (int e = 0; e < W; ++e)
+      if (g.valid(q, e)) st_elem<DT>(a + e * E, chunk_get<DT>(v, e));
+  }
 }
+
+// Stores column-aligned chunk q (W values f) of one row tensor whose slice
+// starts at s0 (any element alignment): one 128-bit store when aligned, aligned
+// 2/4/8-byte pieces when not, element stores for a ragged last chunk.
+template <int DT, int W>
+__device__ __forceinline__ void store_cols(const RowGeo<DT, W>& g, char* s0, int q, const float* f) {
+  constexpr int E = DType<DT>::E;
+  char* a = s0 + (int64_t)g.chunk(q) * (W * E);
+  if constexpr (W > 1) {
+    if (g.full(q)) {
+      const uint4 v = chunk_pack<DT>(f);
+      if ((reinterpret_cast<uintptr_t>(a) & 15) == 0) st_chunk_stream(a, v);
+      else st16_split(a, v);
+    } else {
+#pragma unroll
+      for (int e = 0; e < W; ++e)
+        if (g.valid(q, e)) st_elem<DT>(a + e * E, f[e]);
+    }
+  } else {
+    st_elem<DT>(a, f[0]);
+  }
+}
+
+// Reductions of one thread's row statistics across its row group (and, for a
+// row split over a cluster, across the cluster's CTAs).  An operation calls
+// reduce() / cluster() as often as it needs per row; every thread of the group
+// (and every CTA of the cluster) makes the same calls in the same order.
+//   reduce():  G <= 32: warp shuffles only.  G > 32: shuffles, then the per-warp
+//              results through shared memory and a named barrier for the group.
+//   cluster(): the CTAs' results through distributed shared memory after a
+//              cluster barrier (identity when the cluster is one CTA).
+// Scratch slots are 16 bytes and double-buffered by call parity: a slot is
+// rewritten two calls later, after a barrier every reader has passed.
+// Statistic types S provide identity(), shfl_xor(), load_remote() and a
+// kNary flag (with nary<L>() for the n-ary forms).
+struct NoHook {
+  __device__ __forceinline__ void operator()() const {}
+};
+
+template <int G, class Hook>
+struct Reducer {
+  unsigned char* red;  // this group's scratch: 2 parities x 32 warps x 16 B
+  unsigned char* cl;   // this CTA's cluster slots: 2 parities x 16 B
+  const Hook* hook;    // run once per row by thread 0 after the group's first barrier
+  int& gcalls;
+  int& ccalls;
+  int gt, bar_id, K;
+  bool hooked;
+
+  template <class S, class M>
+  __device__ __forceinline__ S reduce(S s, M merge) {
+    static_assert(sizeof(S) <= 16, "statistic larger than a scratch slot");
+    if constexpr (G <= 32) {
+      if constexpr (S::kNary) return S::template nary<G>(s);
+      else return group_reduce<S, M, G>(s, merge);
+    } else {
+      const int parity = gcalls & 1;
+      ++gcalls;
+      if constexpr (S::kNary) s = S::template nary<32>(s);
+      else s = group_reduce<S, M, 32>(s, merge);
+      const int lane = threadIdx.x & 31;
+      unsigned char* base = red + parity * 512;
+      if (lane == 0) *reinterpret_cast<S*>(base + 16 * (gt >> 5)) = s;
+      named_bar(bar_id, G);
+      if (!hooked) {
+        hooked = true;
+        if (threadIdx.x == 0) (*hook)();
+      }
+      const S o = (lane < G / 32) ? *reinterpret_cast<const S*>(base + 16 * lane) : S::identity();
+      if constexpr (S::kNary) return S::template nary<32>(o);
+      else return group_reduce<S, M, 32>(o, merge);
+    }
+  }
+
+  template <class S, class M>
+  __device__ __forceinline__ S cluster(S s, M merge) {
+    if (K == 1) return s;
+    const int parity = ccalls & 1;
+    ++ccalls;
+    S* slot = reinterpret_cast<S*>(cl + 16 * parity);
+    if (threadIdx.x == 0) *slot = s;
+    cluster_sync();
+    const int lane = threadIdx.x & 31;
+    S o = S::identity();
+    if (lane < K) o = S::load_remote(map_to_rank(slot, lane));
+    return group_reduce<S, M, 32>(o, merge);
+  }
+};
 
 // The engine.  G threads per row group; T = blockDim.x (multiple of G);
 // NQ = chunks per thread; STAGED = rows brought in by bulk copies (G == T).
+// Direct variants are held to 64 registers per thread (full occupancy).
 template <class Op, int G, int NQ, int MAXT, bool STAGED>
-__global__ void __launch_bounds__(MAXT) row_kernel(const typename Op::Params p, const Geo geo) {
+__global__ void __launch_bounds__(MAXT, STAGED ? 1 : 1024 / MAXT)
+    row_kernel(const typename Op::Params p, const Geo geo) {
   constexpr int DT = Op::DT, W = Op::W, NT = Op::NT;
   constexpr int E = DType<DT>::E;
-  using S = typename Op::Stats;
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int T = blockDim.x;
@@ -315,48 +430,44 @@ __global__ void __launch_bounds__(MAXT) row_kernel(const typename Op::Params p, 
   // first row of the warp's first group: keeps sub-warp groups in lock step
   const int64_t warp_first = cid * ngroups + ((threadIdx.x & ~31) / G);
 
-  S* red = reinterpret_cast<S*>(smem + geo.red_off) + (G > 32 ? grp * 64 : 0);
-  S* cl_slot = reinterpret_cast<S*>(smem + geo.red_off) + 64 * (ngroups > 0 ? ngroups : 1);
-  const int bar_id = 1 + grp;
+  unsigned char* red = smem + geo.red_off + (G > 32 ? grp * 1024 : 0);
+  unsigned char* cl = smem + geo.red_off + 1024 * (ngroups > 0 ? ngroups : 1);
+  int gcalls = 0, ccalls = 0;
 
   typename Op::Thread ts;
-  Op::thread_init(ts, p, geo, c0, c1, gt, G);
+  Op::thread_init(ts, p, geo, c0, c1, gt, G, smem + geo.col_off, grp, ngroups);
+  __syncthreads();  // per-group scratch initialised before any row is processed
 
   RowRegs<DT, W, NT, NQ> cur;
 
   if constexpr (!STAGED) {
-    // ------------------------------------------------ direct, register double buffer
+    // ------------------------------------------------ direct
+    constexpr bool kPre = Op::kPrefetch;  // register double buffer of the next row
+    const NoHook nohook;
     typename Op::Meta m_cur = Op::meta(p, my_first < geo.rows ? my_first : -1);
     RowGeo<DT, W> g_cur;
-    if (my_first < geo.rows) {
-      g_cur.init(c0, c1, Op::start_addr(p, my_first, c0), gt, G);
-      if (!Op::skip(m_cur))
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-          load_direct(cur, t, g_cur, Op::in_chunk0(p, t, my_first, c0, g_cur), Op::fill());
+    if (my_first < geo.rows) g_cur.init(c0, c1, Op::start_addr(p, my_first, c0), gt, G);
+    if constexpr (kPre) {
+      if (my_first < geo.rows && !Op::skip(m_cur)) Op::load_direct(cur, g_cur, p, geo, my_first, c0);
     }
     for (int64_t i = 0;; ++i) {
       const int64_t wr = warp_first + i * step;
       if (wr >= geo.rows) break;
       const int64_t r = my_first + i * step;
       const bool active = r < geo.rows;
-      // prefetch the next row into a second register set
       const int64_t rn = r + step;
       typename Op::Meta m_nxt = Op::meta(p, rn < geo.rows ? rn : -1);
       RowGeo<DT, W> g_nxt;
+      if (rn < geo.rows) g_nxt.init(c0, c1, Op::start_addr(p, rn, c0), gt, G);
       RowRegs<DT, W, NT, NQ> nxt;
-      if (rn < geo.rows) {
-        g_nxt.init(c0, c1, Op::start_addr(p, rn, c0), gt, G);
-        if (!Op::skip(m_nxt))
-#pragma unroll
-          for (int t = 0; t < NT; ++t)
-            load_direct(nxt, t, g_nxt, Op::in_chunk0(p, t, rn, c0, g_nxt), Op::fill());
+      if constexpr (kPre) {
+        if (rn < geo.rows && !Op::skip(m_nxt)) Op::load_direct(nxt, g_nxt, p, geo, rn, c0);
+      } else {
+        if (active && !Op::skip(m_cur)) Op::load_direct(cur, g_cur, p, geo, r, c0);
       }
-      const bool use = active && !Op::skip(m_cur);
-      S s = use ? Op::thread_stats(ts, cur, g_cur, m_cur) : S::identity();
-      s = reduce_group<S, G>(s, typename Op::Merge(), red, static_cast<int>(i & 1), gt, bar_id);
-      if (active) Op::finish(ts, p, geo, r, m_cur, s, cur, g_cur, gt == 0);
-      cur = nxt;
+      Reducer<G, NoHook> rd{red, cl, &nohook, gcalls, ccalls, gt, 1 + grp, 1, true};
+      Op::process(ts, p, geo, r, m_cur, cur, g_cur, gt == 0, active, rd);
+      if constexpr (kPre) cur = nxt;
       g_cur = g_nxt;
       m_cur = m_nxt;
     }
@@ -400,13 +511,12 @@ __global__ void __launch_bounds__(MAXT) row_kernel(const typename Op::Params p, 
     // Whether row r is brought in by a copy (same answer on every thread).
     auto copied = [&](int64_t r, const typename Op::Meta& m) -> bool {
       if (Op::skip(m)) return false;
-      const uint64_t s0 = reinterpret_cast<uint64_t>(Op::in_slice_start(p, 0, r, c0));
-      const uint64_t s1 = s0 + (uint64_t)(c1 - c0) * E;
-      bool any = ((s1 & ~uint64_t(15)) > ((s0 + 15) & ~uint64_t(15)));
-      if constexpr (NT > 1) {
-        const uint64_t u0 = reinterpret_cast<uint64_t>(Op::in_slice_start(p, 1, r, c0));
-        const uint64_t u1 = u0 + (uint64_t)(c1 - c0) * E;
-        any = any || ((u1 & ~uint64_t(15)) > ((u0 + 15) & ~uint64_t(15)));
+      bool any = false;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const uint64_t s0 = reinterpret_cast<uint64_t>(Op::in_slice_start(p, t, r, c0));
+        const uint64_t s1 = s0 + (uint64_t)(c1 - c0) * E;
+        any = any || ((s1 & ~uint64_t(15)) > ((s0 + 15) & ~uint64_t(15)));
       }
       return any;
     };
@@ -431,23 +541,25 @@ __global__ void __launch_bounds__(MAXT) row_kernel(const typename Op::Params p, 
       if (threadIdx.x == 0 && rfar < geo.rows) m_far = Op::meta(p, rfar);
       RowGeo<DT, W> g;
       g.init(c0, c1, Op::start_addr(p, r, c0), gt, G);
-      const bool use = !Op::skip(m);
-      if (use) {
+      if (!Op::skip(m)) {
         if (copied(r, m)) {
           mbar_wait_bounded(&bars[b], (phase >> b) & 1u, p.err);
           phase ^= (1u << b);
         }
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-          load_staged(cur, t, g, Op::in_chunk0(p, t, r, c0, g),
-                      smem + ((size_t)b * NT + t) * geo.buf_bytes, Op::fill());
+        Op::load_staged(cur, g, p, geo, r, c0, smem + (size_t)b * NT * geo.buf_bytes,
+                        geo.buf_bytes);
       }
-      S s = use ? Op::thread_stats(ts, cur, g, m) : S::identity();
-      s = reduce_group<S, G>(s, typename Op::Merge(), red, static_cast<int>(i & 1), gt, bar_id);
-      // every thread is done reading buffer b: refill it with the row nbuf ahead
-      if (threadIdx.x == 0 && rfar < geo.rows && !Op::skip(m_far)) issue(rfar, b);
-      if (K > 1) s = reduce_cluster<S>(s, typename Op::Merge(), cl_slot, static_cast<int>(i & 1), K);
-      Op::finish(ts, p, geo, r, m, s, cur, g, gt == 0 && rank == 0);
+      // every thread is done reading buffer b once the row's first group
+      // barrier is passed: refill it with the row nbuf ahead
+      auto refill = [&]() {
+        if (rfar < geo.rows && !Op::skip(m_far)) issue(rfar, b);
+      };
+      Reducer<G, decltype(refill)> rd{red, cl, &refill, gcalls, ccalls, gt, 1, K, false};
+      Op::process(ts, p, geo, r, m, cur, g, gt == 0 && rank == 0, true, rd);
+      if (!rd.hooked) {  // no group barrier this row: make one before the refill
+        named_bar(1, G);
+        if (threadIdx.x == 0) refill();
+      }
     }
     Op::epilogue(ts, p, geo, smem + geo.col_off, c0, c1, cid, 0, 1, gt, G);
     if (K > 1) cluster_sync();  // peers may still read this CTA's slots

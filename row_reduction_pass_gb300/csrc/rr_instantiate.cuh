@@ -39,7 +39,6 @@ KernelSet make_kernel_set() {
   k.nq_staged[1] = NQSE;
   k.maxt_direct = MAXT_D;
   k.maxt_staged = MAXT_S;
-  k.stats_bytes = sizeof(typename OC::Stats);
   return k;
 }
 

@@ -14,7 +14,6 @@ struct KernelSet {
   int nq_staged[2];
   int maxt_direct;
   int maxt_staged;
-  int stats_bytes;
 };
 
 KernelSet softmax_kernels_f32();

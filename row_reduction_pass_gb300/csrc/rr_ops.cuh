@@ -4,8 +4,11 @@
 //                  loss + dlogits = softmax - onehot in the same pass
 //                  ("Engineering a CUDA Machine Learning Framework from Scratch",
 //                  sec. 3.1 "Online FlashSoftmax" and sec. 2.1).
-//   OpLnFwd        LayerNorm forward with one-pass moments merged by the
-//                  Welford / Chan pairwise rule (same page, sec. 3.2).
+//   OpLnFwd        LayerNorm forward with its moments from one pass over
+//                  global memory (same page, sec. 3.2): exact mean from a
+//                  compensated sum, then M2 about it, in registers; row slices
+//                  held by the CTAs of a cluster merged with the Chan / Welford
+//                  pairwise update.
 //   OpLnBwd        analytic LayerNorm backward (same page, sec. 2.2): dx per
 //                  row, and per-column partial sums of dy*xhat and dy that a
 //                  second, fixed-order pass reduces into dgamma / dbeta.
@@ -38,6 +41,7 @@ struct LnFwdParams {
   int* err;
   int64_t cols;
   float eps;
+  float inv_cols;  // 1 / cols (rounded)
 };
 struct LnBwdParams {
   const char* dy;
@@ -49,6 +53,7 @@ struct LnBwdParams {
   float* ws;  // [partials][2][cols] float32 column partials
   int* err;
   int64_t cols;
+  float inv_cols;  // 1 / cols (rounded)
 };
 
 // ---------------------------------------------------------- statistics ----
@@ -87,6 +92,35 @@ struct MergeMaxSum {
   }
 };
 
+// A double-float sum (sh + sl, unevaluated).
+struct DFSum {
+  static constexpr bool kNary = false;
+  float sh, sl;
+  __device__ __forceinline__ static DFSum identity() { return {0.f, 0.f}; }
+  __device__ __forceinline__ static DFSum shfl_xor(const DFSum& v, int off) {
+    return {__shfl_xor_sync(0xffffffffu, v.sh, off), __shfl_xor_sync(0xffffffffu, v.sl, off)};
+  }
+  __device__ __forceinline__ static DFSum load_remote(uint32_t a) {
+    return {ld_cluster_f32(a), ld_cluster_f32(a + 4)};
+  }
+};
+
+// One plain sum.
+struct Sum1 {
+  static constexpr bool kNary = false;
+  float s;
+  __device__ __forceinline__ static Sum1 identity() { return {0.f}; }
+  __device__ __forceinline__ static Sum1 shfl_xor(const Sum1& v, int off) {
+    return {__shfl_xor_sync(0xffffffffu, v.s, off)};
+  }
+  __device__ __forceinline__ static Sum1 load_remote(uint32_t a) { return {ld_cluster_f32(a)}; }
+};
+struct MergeSum1 {
+  __device__ __forceinline__ Sum1 operator()(const Sum1& a, const Sum1& b) const {
+    return {a.s + b.s};
+  }
+};
+
 // Moments of a set of values, with the sum kept as an unevaluated pair of
 // floats (sh + sl, "double-float") so the mean stays exact to ~2^-48 relative
 // even when large values cancel: (count n, sum S = sh + sl, M2 = sum of squared
@@ -112,11 +146,30 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = (a - (s - bb)) + (b - bb);
 }
 
-// Mean S / n of a double-float sum as a double-float (mh + ml).
+// Double-float addition (exact error of the leading sum kept; commutative
+// bit for bit, so butterflies leave every lane with the same value).
+struct MergeDF {
+  __device__ __forceinline__ DFSum operator()(const DFSum& a, const DFSum& b) const {
+    float s, e;
+    two_sum(a.sh, b.sh, s, e);
+    e += a.sl + b.sl;
+    float h, l;
+    two_sum(s, e, h, l);
+    return {h, l};
+  }
+};
+
+// Mean S / n of a double-float sum as a double-float (mh + ml), given inv = 1/n
+// rounded: mh = fl(S_h * inv), the remainder S_h - mh*n is exact in one FMA, and
+// ml = (remainder + S_l) * inv.
+__device__ __forceinline__ void df_mean(float sh, float sl, float n, float inv, float& mh,
+                                        float& ml) {
+  mh = sh * inv;
+  const float r = fmaf(-mh, n, sh);
+  ml = (r + sl) * inv;
+}
 __device__ __forceinline__ void df_div(float sh, float sl, float n, float& mh, float& ml) {
-  mh = sh / n;
-  const float r = fmaf(-mh, n, sh);  // exact remainder of the division
-  ml = (r + sl) / n;
+  df_mean(sh, sl, n, __frcp_rn(n), mh, ml);
 }
 
 // Chan, Golub & LeVeque pairwise update (the parallel form of Welford's
@@ -163,43 +216,13 @@ struct MergeSum2 {
   }
 };
 
-// Per-column vector (gamma, beta) slots a thread keeps for its own columns.
-template <int DT, int W, int NQ>
-struct ColRegs {
-  using Slot = typename std::conditional<(W > 1), uint4, float>::type;
-  Slot v[NQ];
-  __device__ __forceinline__ float get(int q, int e) const {
-    if constexpr (W > 1) return chunk_get<DT>(v[q], e);
-    else return v[q];
-  }
-  // Loads the thread's columns (chunk c = first + q * step covers columns
-  // c0 + c*W ... ; chunk mode is only used when every row is 16-byte aligned).
-  __device__ __forceinline__ void load(const char* base, int64_t c0, int64_t c1, int64_t first,
-                                       int step) {
-    constexpr int E = DType<DT>::E;
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-      const int64_t c = first + (int64_t)q * step;
-      const int64_t j = c0 + c * W;
-      if (j < c1) {
-        if constexpr (W > 1) v[q] = ld_chunk_cached(base + j * E);
-        else v[q] = ld_elem_cached<DT>(base + j * E);
-      } else {
-        if constexpr (W > 1) v[q] = make_uint4(0, 0, 0, 0);
-        else v[q] = 0.f;
-      }
-    }
-  }
-};
-
 // ------------------------------------------------- softmax / cross-entropy --
 
 template <int DT_, int W_, int NQ_>
 struct OpSoftmaxXent {
   static constexpr int DT = DT_, W = W_, NT = 1, NQ = NQ_;
   static constexpr int E = DType<DT>::E;
-  using Stats = MaxSum;
-  using Merge = MergeMaxSum;
+  static constexpr bool kPrefetch = true;
   using Params = SoftmaxParams;
   struct Meta {
     int32_t label;
@@ -226,7 +249,18 @@ struct OpSoftmaxXent {
     return in_slice_start(p, t, r, c0) - g.head_bytes;
   }
   __device__ __forceinline__ static void thread_init(Thread&, const Params&, const Geo&, int64_t,
-                                                     int64_t, int, int) {}
+                                                     int64_t, int, int, unsigned char*, int, int) {}
+  __device__ __forceinline__ static void load_direct(RowRegs<DT, W, NT, NQ>& x,
+                                                     const RowGeo<DT, W>& g, const Params& p,
+                                                     const Geo&, int64_t r, int64_t c0) {
+    load_direct_mem(x, 0, g, in_chunk0(p, 0, r, c0, g), fill());
+  }
+  __device__ __forceinline__ static void load_staged(RowRegs<DT, W, NT, NQ>& x,
+                                                     const RowGeo<DT, W>& g, const Params& p,
+                                                     const Geo&, int64_t r, int64_t c0,
+                                                     const unsigned char* sbuf, int) {
+    load_staged_mem(x, 0, g, in_chunk0(p, 0, r, c0, g), sbuf, fill());
+  }
 
   // Row maximum of the thread's slots.  Ragged slots hold -inf, so every slot
   // of every owned chunk can take part (bf16: packed max, two values at once).
@@ -257,8 +291,8 @@ struct OpSoftmaxXent {
   // The exponent is one FMA, x*log2(e) - fl(m*log2(e)); the rounding residual
   // r of fl(m*log2(e)) shifts every term by the same factor 2^r, which is
   // divided out once (so d is the plain sum of exp(x - m)).
-  __device__ __forceinline__ static Stats thread_stats(Thread&, const RowRegs<DT, W, NT, NQ>& x,
-                                                       const RowGeo<DT, W>& g, const Meta&) {
+  __device__ __forceinline__ static MaxSum thread_stats(const RowRegs<DT, W, NT, NQ>& x,
+                                                        const RowGeo<DT, W>& g) {
     const float m = thread_max(x, g);
     if (m == -INFINITY) return {m, 0.f};
     const float mL = m * kLog2e;
@@ -281,10 +315,17 @@ struct OpSoftmaxXent {
     return {m, (d0 + d1) * ex2(-r)};
   }
 
-  __device__ __forceinline__ static void finish(Thread&, const Params& p, const Geo& geo,
-                                                int64_t r, const Meta& mt, const Stats& s,
-                                                const RowRegs<DT, W, NT, NQ>& x,
-                                                const RowGeo<DT, W>& g, bool leader) {
+  template <class R>
+  __device__ __forceinline__ static void process(Thread&, const Params& p, const Geo& geo,
+                                                 int64_t r, const Meta& mt,
+                                                 const RowRegs<DT, W, NT, NQ>& x,
+                                                 const RowGeo<DT, W>& g, bool leader, bool active,
+                                                 R& rd) {
+    const bool use = active && !mt.skip;
+    MaxSum s = use ? thread_stats(x, g) : MaxSum::identity();
+    s = rd.reduce(s, MergeMaxSum());
+    s = rd.cluster(s, MergeMaxSum());
+    if (!active) return;
     char* y0 = p.y + (r * p.cols + g.c0) * E - g.head_bytes;
     const bool masked = (s.m == -INFINITY);
     int ql = -1, el = 0;  // where this thread holds the label column, if it does
@@ -349,92 +390,185 @@ struct OpSoftmaxXent {
 };
 
 // ------------------------------------------------------- LayerNorm forward --
+//
+// Both LayerNorm operations work on column-aligned chunks (chunk k of a thread is
+// columns c0 + kW ...), whatever the alignment of the row in memory, so gamma,
+// beta and the column partials are plain 16-byte vectors.
+//
+// Moments: one pass over global memory.  In registers, a compensated sum gives
+// the exact mean (double-float), then the squared deviations from it give M2;
+// each is reduced over the row group.  A row split over a cluster merges its
+// CTAs' (n, S, M2) with the Chan/Welford pairwise update.
 
 template <int DT_, int W_, int NQ_>
 struct OpLnFwd {
   static constexpr int DT = DT_, W = W_, NT = 1, NQ = NQ_;
   static constexpr int E = DType<DT>::E;
-  using Stats = Moments;
-  using Merge = MergeMoments;
+  static constexpr bool kPrefetch = false;
   using Params = LnFwdParams;
   struct Meta {};
-  struct Thread {
-    ColRegs<DT, W, NQ> gamma, beta;
-  };
+  struct Thread {};
 
   __device__ __forceinline__ static Meta meta(const Params&, int64_t) { return {}; }
   __device__ __forceinline__ static bool skip(const Meta&) { return false; }
-  __device__ __forceinline__ static float fill() { return 0.f; }
   __device__ __forceinline__ static const char* in_slice_start(const Params& p, int, int64_t r,
                                                                int64_t c0) {
     return p.x + (r * p.cols + c0) * E;
   }
-  __device__ __forceinline__ static uint64_t start_addr(const Params& p, int64_t r, int64_t c0) {
-    return reinterpret_cast<uint64_t>(in_slice_start(p, 0, r, c0));
+  // column space: the row geometry never has a ragged head
+  __device__ __forceinline__ static uint64_t start_addr(const Params&, int64_t, int64_t) {
+    return 0;
   }
-  __device__ __forceinline__ static const char* in_chunk0(const Params& p, int t, int64_t r,
-                                                          int64_t c0, const RowGeo<DT, W>& g) {
-    return in_slice_start(p, t, r, c0) - g.head_bytes;
+  __device__ __forceinline__ static void thread_init(Thread&, const Params&, const Geo&, int64_t,
+                                                     int64_t, int, int, unsigned char*, int, int) {}
+  __device__ __forceinline__ static void load_direct(RowRegs<DT, W, NT, NQ>& x,
+                                                     const RowGeo<DT, W>& g, const Params& p,
+                                                     const Geo& geo, int64_t r, int64_t c0) {
+    load_cols(x, 0, g, in_slice_start(p, 0, r, c0), p.x, p.x + geo.rows * geo.cols * E, nullptr);
   }
-  __device__ __forceinline__ static void thread_init(Thread& ts, const Params& p, const Geo&,
-                                                     int64_t c0, int64_t c1, int gt, int G) {
-    ts.gamma.load(p.gamma, c0, c1, gt, G);
-    ts.beta.load(p.beta, c0, c1, gt, G);
-  }
-
-  // Moments of the thread's own values: a compensated (Neumaier) sum, then the
-  // squared deviations from that exact mean (two passes over registers); the
-  // threads' moments are then merged with the pairwise update.
-  __device__ __forceinline__ static Stats thread_stats(Thread&, const RowRegs<DT, W, NT, NQ>& x,
-                                                       const RowGeo<DT, W>& g, const Meta&) {
-    float n = 0.f, s = 0.f, c = 0.f;
-    g.template for_each<NQ>([&](int q, int e) {
-      const float v = x.get(0, q, e);
-      const float t = s + v;
-      c += (fabsf(s) >= fabsf(v)) ? ((s - t) + v) : ((v - t) + s);
-      s = t;
-      n += 1.f;
-    });
-    if (n == 0.f) return Stats::identity();
-    float sh, sl;
-    two_sum(s, c, sh, sl);
-    float mh, ml;
-    df_div(sh, sl, n, mh, ml);
-    float m2 = 0.f;
-    g.template for_each<NQ>([&](int q, int e) {
-      const float d = (x.get(0, q, e) - mh) - ml;
-      m2 = fmaf(d, d, m2);
-    });
-    return {n, sh, sl, m2};
+  __device__ __forceinline__ static void load_staged(RowRegs<DT, W, NT, NQ>& x,
+                                                     const RowGeo<DT, W>& g, const Params& p,
+                                                     const Geo& geo, int64_t r, int64_t c0,
+                                                     const unsigned char* sbuf, int) {
+    load_cols(x, 0, g, in_slice_start(p, 0, r, c0), p.x, p.x + geo.rows * geo.cols * E, sbuf);
   }
 
-  __device__ __forceinline__ static void finish(Thread& ts, const Params& p, const Geo& geo,
-                                                int64_t r, const Meta&, const Stats& s,
-                                                const RowRegs<DT, W, NT, NQ>& x,
-                                                const RowGeo<DT, W>& g, bool leader) {
-    char* y0 = p.y + (r * p.cols + g.c0) * E - g.head_bytes;
-    const float n = static_cast<float>(geo.cols);
-    float mh, ml;
-    df_div(s.sh, s.sl, n, mh, ml);
-    const float var = s.m2 / n;
-    const bool masked = !(isfinite(mh) && isfinite(ml) && isfinite(var));
-    if (masked) {
-      if (leader) {
-        p.mean[r] = 0.f;
-        p.rstd[r] = 0.f;
+  template <class R>
+  __device__ __forceinline__ static void process(Thread&, const Params& p, const Geo& geo,
+                                                 int64_t r, const Meta&,
+                                                 const RowRegs<DT, W, NT, NQ>& x,
+                                                 const RowGeo<DT, W>& g, bool leader, bool active,
+                                                 R& rd) {
+    // 1. compensated sum of the thread's values (two interleaved TwoSum
+    //    accumulators per packed pair; ragged slots hold 0) -> group sum -> mean
+    float s = 0.f, c = 0.f;
+    if (active) {
+      if constexpr (W > 1) {
+        float s0 = 0.f, s1 = 0.f, c0 = 0.f, c1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          if (!g.has(q)) break;
+#pragma unroll
+          for (int e = 0; e < W; e += 2) {
+            const float v0 = x.get(0, q, e), v1 = x.get(0, q, e + 1);
+            float t0, t1, b0, b1, u0, u1, w0, w1;
+            add2(t0, t1, s0, s1, v0, v1);            // t = s + v
+            add2(b0, b1, t0, t1, -s0, -s1);          // bb = t - s
+            add2(u0, u1, t0, t1, -b0, -b1);          // t - bb
+            add2(u0, u1, s0, s1, -u0, -u1);          // s - (t - bb)
+            add2(w0, w1, v0, v1, -b0, -b1);          // v - bb
+            add2(u0, u1, u0, u1, w0, w1);            // exact error of s + v
+            add2(c0, c1, c0, c1, u0, u1);
+            s0 = t0;
+            s1 = t1;
+          }
+        }
+        float e;
+        two_sum(s0, s1, s, e);
+        c = (c0 + c1) + e;
+      } else {
+        g.template for_each<NQ>([&](int q, int e) {
+          const float v = x.get(0, q, e);
+          float t, err;
+          two_sum(s, v, t, err);
+          c += err;
+          s = t;
+        });
       }
-      g.template store<NQ>(y0, [&](int, int) { return 0.f; });
-      return;
     }
-    const float rstd = 1.0f / sqrtf(var + p.eps);
+    DFSum S;
+    two_sum(s, c, S.sh, S.sl);
+    S = rd.reduce(S, MergeDF());
+    const float ns = static_cast<float>(g.c1 - g.c0);
+    const bool whole = (rd.K == 1);
+    const float inv_n = whole ? p.inv_cols : __frcp_rn(ns);
+    float mh, ml;
+    df_mean(S.sh, S.sl, ns, inv_n, mh, ml);
+    // 2. squared deviations from that mean -> group sum (ragged slots excluded)
+    float m2 = 0.f;
+    if (active) {
+      if constexpr (W > 1) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          if (!g.has(q)) break;
+          const bool fullq = g.full(q);
+#pragma unroll
+          for (int e = 0; e < W; e += 2) {
+            float d0, d1;
+            add2(d0, d1, x.get(0, q, e), x.get(0, q, e + 1), -mh, -mh);
+            add2(d0, d1, d0, d1, -ml, -ml);
+            if (!fullq) {
+              if (!g.valid(q, e)) d0 = 0.f;
+              if (!g.valid(q, e + 1)) d1 = 0.f;
+            }
+            fma2(a0, a1, d0, d1, d0, d1, a0, a1);
+          }
+        }
+        m2 = a0 + a1;
+      } else {
+        g.template for_each<NQ>([&](int q, int e) {
+          const float d = (x.get(0, q, e) - mh) - ml;
+          m2 = fmaf(d, d, m2);
+        });
+      }
+    }
+    m2 = rd.reduce(Sum1{m2}, MergeSum1()).s;
+    if (!whole) {
+      // 3. slices of a cluster: Chan/Welford pairwise merge of (n, S, M2)
+      Moments mo = rd.cluster(Moments{ns, S.sh, S.sl, m2}, MergeMoments());
+      df_mean(mo.sh, mo.sl, mo.n, p.inv_cols, mh, ml);
+      m2 = mo.m2;
+    }
+    if (!active) return;
+    const float var = m2 * p.inv_cols;
+    const bool masked = !(isfinite(mh) && isfinite(ml) && isfinite(var));
+    const float rstd = masked ? 0.f : rsqrtf(var + p.eps);
     if (leader) {
-      p.mean[r] = mh + ml;
+      p.mean[r] = masked ? 0.f : mh + ml;
       p.rstd[r] = rstd;
     }
-    g.template store<NQ>(y0, [&](int q, int e) {
-      const float xh = ((x.get(0, q, e) - mh) - ml) * rstd;
-      return fmaf(xh, ts.gamma.get(q, e), ts.beta.get(q, e));
-    });
+    char* y0 = p.y + (r * p.cols + g.c0) * E;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (!g.has(q)) break;
+      float f[W];
+      if (masked) {
+#pragma unroll
+        for (int e = 0; e < W; ++e) f[e] = 0.f;
+      } else {
+        const int64_t j = g.c0 + (int64_t)g.chunk(q) * W;
+        if constexpr (W > 1) {
+          uint4 gv, bv;
+          if (g.full(q)) {
+            gv = ld_chunk_cached(p.gamma + j * E);
+            bv = ld_chunk_cached(p.beta + j * E);
+          } else {
+            gv = make_uint4(0, 0, 0, 0);
+            bv = gv;
+#pragma unroll
+            for (int e = 0; e < W; ++e)
+              if (g.valid(q, e)) {
+                chunk_set_bits<DT>(gv, e, ld_elem_bits<DT>(p.gamma + (j + e) * E));
+                chunk_set_bits<DT>(bv, e, ld_elem_bits<DT>(p.beta + (j + e) * E));
+              }
+          }
+#pragma unroll
+          for (int e = 0; e < W; e += 2) {
+            float t0, t1;
+            add2(t0, t1, x.get(0, q, e), x.get(0, q, e + 1), -mh, -mh);
+            add2(t0, t1, t0, t1, -ml, -ml);
+            mul2(t0, t1, t0, t1, rstd, rstd);
+            fma2(f[e], f[e + 1], t0, t1, chunk_get<DT>(gv, e), chunk_get<DT>(gv, e + 1),
+                 chunk_get<DT>(bv, e), chunk_get<DT>(bv, e + 1));
+          }
+        } else {
+          const float xh = ((x.get(0, q, 0) - mh) - ml) * rstd;
+          f[0] = fmaf(xh, ld_elem_cached<DT>(p.gamma + j * E), ld_elem_cached<DT>(p.beta + j * E));
+        }
+      }
+      store_cols(g, y0, q, f);
+    }
   }
   __device__ __forceinline__ static void epilogue(Thread&, const Params&, const Geo&,
                                                   unsigned char*, int64_t, int64_t, int64_t, int,
@@ -447,16 +581,18 @@ template <int DT_, int W_, int NQ_>
 struct OpLnBwd {
   static constexpr int DT = DT_, W = W_, NT = 2, NQ = NQ_;  // tensor 0: dy, 1: x
   static constexpr int E = DType<DT>::E;
-  using Stats = Sum2;
-  using Merge = MergeSum2;
+  static constexpr bool kPrefetch = false;
   using Params = LnBwdParams;
   struct Meta {
     float mean, rstd;
   };
+  // part: this group's column partials in shared memory, part[j] = sum of
+  // dy*xhat and part[npad + j] = sum of dy over the rows the group processed
+  // (j local to the slice).
   struct Thread {
-    ColRegs<DT, W, NQ> gamma;
-    float dg[NQ][W];
-    float db[NQ][W];
+    float* part;
+    const char* gamma;  // gamma at the slice start
+    int npad;
   };
 
   __device__ __forceinline__ static Meta meta(const Params& p, int64_t r) {
@@ -465,143 +601,218 @@ struct OpLnBwd {
   }
   // A row the forward masked (rstd == 0) is neither read nor accumulated.
   __device__ __forceinline__ static bool skip(const Meta& m) { return m.rstd == 0.f; }
-  __device__ __forceinline__ static float fill() { return 0.f; }
   __device__ __forceinline__ static const char* in_slice_start(const Params& p, int t, int64_t r,
                                                                int64_t c0) {
     return (t == 0 ? p.dy : p.x) + (r * p.cols + c0) * E;
   }
-  __device__ __forceinline__ static uint64_t start_addr(const Params& p, int64_t r, int64_t c0) {
-    return reinterpret_cast<uint64_t>(in_slice_start(p, 0, r, c0));
-  }
-  __device__ __forceinline__ static const char* in_chunk0(const Params& p, int t, int64_t r,
-                                                          int64_t c0, const RowGeo<DT, W>& g) {
-    return in_slice_start(p, t, r, c0) - g.head_bytes;
+  __device__ __forceinline__ static uint64_t start_addr(const Params&, int64_t, int64_t) {
+    return 0;
   }
   __device__ __forceinline__ static void thread_init(Thread& ts, const Params& p, const Geo&,
-                                                     int64_t c0, int64_t c1, int gt, int G) {
-    ts.gamma.load(p.gamma, c0, c1, gt, G);
-#pragma unroll
-    for (int q = 0; q < NQ; ++q)
-#pragma unroll
-      for (int e = 0; e < W; ++e) {
-        ts.dg[q][e] = 0.f;
-        ts.db[q][e] = 0.f;
-      }
+                                                     int64_t c0, int64_t c1, int gt, int G,
+                                                     unsigned char* colbuf, int grp, int) {
+    ts.npad = static_cast<int>(((c1 - c0) + W - 1) / W * W);
+    ts.part = reinterpret_cast<float*>(colbuf) + (size_t)grp * 2 * ts.npad;
+    ts.gamma = p.gamma + c0 * E;
+    for (int i = gt; i < 2 * ts.npad; i += G) ts.part[i] = 0.f;
+  }
+  __device__ __forceinline__ static void load_direct(RowRegs<DT, W, NT, NQ>& v,
+                                                     const RowGeo<DT, W>& g, const Params& p,
+                                                     const Geo& geo, int64_t r, int64_t c0) {
+    const int64_t n = geo.rows * geo.cols * E;
+    load_cols(v, 0, g, in_slice_start(p, 0, r, c0), p.dy, p.dy + n, nullptr);
+    load_cols(v, 1, g, in_slice_start(p, 1, r, c0), p.x, p.x + n, nullptr);
+  }
+  __device__ __forceinline__ static void load_staged(RowRegs<DT, W, NT, NQ>& v,
+                                                     const RowGeo<DT, W>& g, const Params& p,
+                                                     const Geo& geo, int64_t r, int64_t c0,
+                                                     const unsigned char* sbuf, int buf_bytes) {
+    const int64_t n = geo.rows * geo.cols * E;
+    load_cols(v, 0, g, in_slice_start(p, 0, r, c0), p.dy, p.dy + n, sbuf);
+    load_cols(v, 1, g, in_slice_start(p, 1, r, c0), p.x, p.x + n, sbuf + buf_bytes);
   }
 
-  __device__ __forceinline__ static Stats thread_stats(Thread& ts,
-                                                       const RowRegs<DT, W, NT, NQ>& v,
-                                                       const RowGeo<DT, W>& g, const Meta& m) {
+  // gamma of chunk q as storage bits (zero past the row end); element mode: the value
+  __device__ __forceinline__ static uint4 gamma_raw(const Thread& ts, const RowGeo<DT, W>& g,
+                                                    int q) {
+    const int64_t j = (int64_t)g.chunk(q) * W;
+    if constexpr (W > 1) {
+      if (g.full(q)) return ld_chunk_cached(ts.gamma + j * E);
+      uint4 c = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int e = 0; e < W; ++e)
+        if (g.valid(q, e)) chunk_set_bits<DT>(c, e, ld_elem_bits<DT>(ts.gamma + (j + e) * E));
+      return c;
+    } else {
+      return make_uint4(__float_as_uint(ld_elem_cached<DT>(ts.gamma + j * E)), 0, 0, 0);
+    }
+  }
+  __device__ __forceinline__ static float gam(const uint4& c, int e) {
+    if constexpr (W > 1) return chunk_get<DT>(c, e);
+    else return __uint_as_float(c.x);
+  }
+
+  template <class R>
+  __device__ __forceinline__ static void process(Thread& ts, const Params& p, const Geo& geo,
+                                                 int64_t r, const Meta& m,
+                                                 const RowRegs<DT, W, NT, NQ>& v,
+                                                 const RowGeo<DT, W>& g, bool, bool active,
+                                                 R& rd) {
+    const bool use = active && !skip(m);
+    // S1 = sum g, S2 = sum g * xhat with g = dy * gamma, xhat = (x - mean) * rstd
+    // (ragged slots hold dy = 0, x = 0 and gamma = 0, so they add nothing)
     float s1 = 0.f, s2 = 0.f;
-    g.template for_each<NQ>([&](int q, int e) {
-      const float xh = (v.get(1, q, e) - m.mean) * m.rstd;
-      // rounded product (never fused into an FMA) so finish() sees the same g
-      const float gg = __fmul_rn(v.get(0, q, e), ts.gamma.get(q, e));
-      s1 += gg;
-      s2 = fmaf(gg, xh, s2);
-    });
-    return {s1, s2};
-  }
-
-  __device__ __forceinline__ static void finish(Thread& ts, const Params& p, const Geo& geo,
-                                                int64_t r, const Meta& m, const Stats& s,
-                                                const RowRegs<DT, W, NT, NQ>& v,
-                                                const RowGeo<DT, W>& g, bool) {
-    char* dx0 = p.dx + (r * p.cols + g.c0) * E - g.head_bytes;
-    if (skip(m)) {
-      g.template store<NQ>(dx0, [&](int, int) { return 0.f; });
+    if (use) {
+      float sa = 0.f, sb = 0.f, qa = 0.f, qb = 0.f;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (!g.has(q)) break;
+        const uint4 gr = gamma_raw(ts, g, q);
+        if constexpr (W > 1) {
+#pragma unroll
+          for (int e = 0; e < W; e += 2) {
+            float h0, h1;
+            // g is a rounded scalar product: the packed multiply may be fused
+            // with the add that follows it, and the output pass must recompute
+            // exactly the g whose sum is S1 (so that g - mean(g) = 0 when C = 1)
+            const float g0 = __fmul_rn(v.get(0, q, e), gam(gr, e));
+            const float g1 = __fmul_rn(v.get(0, q, e + 1), gam(gr, e + 1));
+            add2(h0, h1, v.get(1, q, e), v.get(1, q, e + 1), -m.mean, -m.mean);
+            mul2(h0, h1, h0, h1, m.rstd, m.rstd);
+            add2(sa, sb, sa, sb, g0, g1);
+            fma2(qa, qb, g0, g1, h0, h1, qa, qb);
+          }
+        } else {
+          const float gg = __fmul_rn(v.get(0, q, 0), gam(gr, 0));
+          const float xh = (v.get(1, q, 0) - m.mean) * m.rstd;
+          sa += gg;
+          qa = fmaf(gg, xh, qa);
+        }
+      }
+      s1 = sa + sb;
+      s2 = qa + qb;
+    }
+    Sum2 s = rd.reduce(Sum2{s1, s2}, MergeSum2());
+    s = rd.cluster(s, MergeSum2());
+    if (!active) return;
+    char* dx0 = p.dx + (r * p.cols + g.c0) * E;
+    if (!use) {
+      const float z[W] = {};
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (!g.has(q)) break;
+        store_cols(g, dx0, q, z);
+      }
       return;
     }
-    const float invc = 1.0f / static_cast<float>(geo.cols);
-    const float a = s.s1 * invc;
-    const float b = s.s2 * invc;
-    g.template store<NQ>(dx0, [&](int q, int e) {
-      const float xh = (v.get(1, q, e) - m.mean) * m.rstd;
-      const float gg = __fmul_rn(v.get(0, q, e), ts.gamma.get(q, e));
-      return m.rstd * ((gg - a) - xh * b);
-    });
-    g.template for_each<NQ>([&](int q, int e) {
-      const float dyv = v.get(0, q, e);
-      const float xh = (v.get(1, q, e) - m.mean) * m.rstd;
-      ts.dg[q][e] = fmaf(dyv, xh, ts.dg[q][e]);
-      ts.db[q][e] += dyv;
-    });
-  }
-
-  // Writes this CTA's (or cluster's) column partials: partial row `part` of the
-  // workspace.  With several row groups per CTA the groups are summed through
-  // shared memory in a fixed order first.
-  __device__ __forceinline__ static void epilogue(Thread& ts, const Params& p, const Geo& geo,
-                                                  unsigned char* colbuf, int64_t c0, int64_t c1,
-                                                  int64_t part, int grp, int ngroups, int gt,
-                                                  int G) {
-    const int64_t cols = geo.cols;
-    float* out = p.ws + part * 2 * cols;
-    if (ngroups == 1) {
+    const float a = s.s1 * p.inv_cols;
+    const float b = s.s2 * p.inv_cols;
 #pragma unroll
-      for (int q = 0; q < NQ; ++q)
+    for (int q = 0; q < NQ; ++q) {
+      if (!g.has(q)) break;
+      const uint4 gr = gamma_raw(ts, g, q);
+      float* pp = ts.part + g.chunk(q) * W;
+      if constexpr (W > 1) {
+        uint4 out = make_uint4(0, 0, 0, 0);
+        // four columns at a time: dx, and the column partials dy*xhat and dy
+        // added into shared memory (ragged slots add dy = 0)
 #pragma unroll
-        for (int e = 0; e < W; ++e) {
-          const int64_t j = c0 + ((int64_t)gt + (int64_t)q * G) * W + e;
-          if (j < c1) {
-            out[j] = ts.dg[q][e];
-            out[cols + j] = ts.db[q][e];
+        for (int e0 = 0; e0 < W; e0 += 4) {
+          float f[4], pg[4];
+#pragma unroll
+          for (int e = e0; e < e0 + 4; e += 2) {
+            const float y0 = v.get(0, q, e), y1 = v.get(0, q, e + 1);
+            float h0, h1, t0, t1;
+            const float g0 = __fmul_rn(y0, gam(gr, e)), g1 = __fmul_rn(y1, gam(gr, e + 1));
+            add2(h0, h1, v.get(1, q, e), v.get(1, q, e + 1), -m.mean, -m.mean);
+            mul2(h0, h1, h0, h1, m.rstd, m.rstd);  // xhat
+            add2(t0, t1, g0, g1, -a, -a);          // g - a
+            fma2(t0, t1, h0, h1, -b, -b, t0, t1);  // (g - a) - xhat b
+            mul2(f[e - e0], f[e - e0 + 1], t0, t1, m.rstd, m.rstd);
+            mul2(pg[e - e0], pg[e - e0 + 1], y0, y1, h0, h1);
+          }
+          float4 u = *reinterpret_cast<float4*>(pp + e0);
+          float4 w = *reinterpret_cast<float4*>(pp + ts.npad + e0);
+          add2(u.x, u.y, u.x, u.y, pg[0], pg[1]);
+          add2(u.z, u.w, u.z, u.w, pg[2], pg[3]);
+          add2(w.x, w.y, w.x, w.y, v.get(0, q, e0), v.get(0, q, e0 + 1));
+          add2(w.z, w.w, w.z, w.w, v.get(0, q, e0 + 2), v.get(0, q, e0 + 3));
+          *reinterpret_cast<float4*>(pp + e0) = u;
+          *reinterpret_cast<float4*>(pp + ts.npad + e0) = w;
+          if constexpr (DT == kBF16) {
+            const uint32_t lo = pack_bf16x2(f[0], f[1]), hi = pack_bf16x2(f[2], f[3]);
+            set_word(out, e0 / 2, lo);
+            set_word(out, e0 / 2 + 1, hi);
+          } else {
+            out = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                             __float_as_uint(f[3]));
           }
         }
-      return;
-    }
-    float* sc = reinterpret_cast<float*>(colbuf);  // [ngroups][2][cols]
-#pragma unroll
-    for (int q = 0; q < NQ; ++q)
-#pragma unroll
-      for (int e = 0; e < W; ++e) {
-        const int64_t j = c0 + ((int64_t)gt + (int64_t)q * G) * W + e;
-        if (j < c1) {
-          sc[(int64_t)grp * 2 * cols + j] = ts.dg[q][e];
-          sc[(int64_t)grp * 2 * cols + cols + j] = ts.db[q][e];
-        }
+        store_cols_bits(g, dx0, q, out);
+      } else {
+        const float dyv = v.get(0, q, 0);
+        const float gg = __fmul_rn(dyv, gam(gr, 0));
+        const float xh = (v.get(1, q, 0) - m.mean) * m.rstd;
+        const float f = m.rstd * ((gg - a) - xh * b);
+        pp[0] += dyv * xh;
+        pp[ts.npad] += dyv;
+        store_cols(g, dx0, q, &f);
       }
+    }
+  }
+
+  // Writes this CTA's (or cluster rank's) column partials as partial row `part`
+  // of the workspace: the row groups of the CTA summed in a fixed order.
+  __device__ __forceinline__ static void epilogue(Thread& ts, const Params& p, const Geo& geo,
+                                                  unsigned char* colbuf, int64_t c0, int64_t c1,
+                                                  int64_t part, int, int ngroups, int, int) {
     __syncthreads();
-    for (int64_t k = threadIdx.x; k < 2 * cols; k += blockDim.x) {
+    const int64_t cols = geo.cols;
+    const int n = static_cast<int>(c1 - c0);
+    const float* sc = reinterpret_cast<const float*>(colbuf);
+    float* out = p.ws + part * 2 * cols;
+    for (int k = threadIdx.x; k < 2 * n; k += blockDim.x) {
+      const int half = k >= n ? 1 : 0;
+      const int j = k - half * n;
       float acc = 0.f;
-      for (int gi = 0; gi < ngroups; ++gi) acc += sc[(int64_t)gi * 2 * cols + k];
-      out[k] = acc;
+      for (int gi = 0; gi < ngroups; ++gi) acc += sc[(size_t)gi * 2 * ts.npad + half * ts.npad + j];
+      out[half * cols + c0 + j] = acc;
     }
   }
 };
 
 // Second stage of the LayerNorm backward: dgamma_j / dbeta_j = sum over the P
-// partial rows, in a fixed order (warp w takes partials w, w+8, ...; the eight
+// partial rows, in a fixed order (warp w takes partials w, w+32, ...; the 32
 // warp sums are then added in warp order), so the result is deterministic.
 template <int DT>
-__global__ void __launch_bounds__(256) col_reduce_kernel(const float* __restrict__ ws, int64_t P,
-                                                         int64_t cols, char* dgamma, char* dbeta) {
+__global__ void __launch_bounds__(1024) col_reduce_kernel(const float* __restrict__ ws, int64_t P,
+                                                          int64_t cols, char* dgamma, char* dbeta) {
   constexpr int E = DType<DT>::E;
-  __shared__ float part[8][33];
+  __shared__ float part[32][33];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t k = (int64_t)blockIdx.x * 32 + lane;
   const int64_t n2 = 2 * cols;
   float s = 0.f;
   if (k < n2) {
     int64_t pp = w;
-    for (; pp + 24 < P; pp += 32) {
+    for (; pp + 96 < P; pp += 128) {
       const float a0 = __ldcs(ws + pp * n2 + k);
-      const float a1 = __ldcs(ws + (pp + 8) * n2 + k);
-      const float a2 = __ldcs(ws + (pp + 16) * n2 + k);
-      const float a3 = __ldcs(ws + (pp + 24) * n2 + k);
+      const float a1 = __ldcs(ws + (pp + 32) * n2 + k);
+      const float a2 = __ldcs(ws + (pp + 64) * n2 + k);
+      const float a3 = __ldcs(ws + (pp + 96) * n2 + k);
       s += a0;
       s += a1;
       s += a2;
       s += a3;
     }
-    for (; pp < P; pp += 8) s += __ldcs(ws + pp * n2 + k);
+    for (; pp < P; pp += 32) s += __ldcs(ws + pp * n2 + k);
   }
   part[w][lane] = s;
   __syncthreads();
   if (w == 0 && k < n2) {
     float t = part[0][lane];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) t += part[i][lane];
+    for (int i = 1; i < 32; ++i) t += part[i][lane];
     char* dst = (k < cols) ? dgamma + k * E : dbeta + (k - cols) * E;
     st_elem<DT>(dst, t);
   }
