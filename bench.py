@@ -135,10 +135,12 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(files=("rr_device.cuh", "rr_engine.cuh", "rr_ops.cuh",
+                               "rr_instantiate.cuh", "k_softmax_bf16.cu")):
+    """Hash of the sources the cross-entropy kernel is compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_reduction_pass_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
@@ -434,8 +436,16 @@ def run_profile_case(args):
         y = torch.empty_like(x)
         fn = lambda: rr.rr_softmax_fwd(x, y)  # noqa: E731
     else:
-        ln = synth.make("ln_f32_4096x768", rows=args.profile_rows or 4096)
-        x, g, b, dy = (torch.from_numpy(ln[k]).to(dev) for k in ("x", "gamma", "beta", "dy"))
+        if args.profile_workload:
+            ln = synth.make(args.profile_workload)
+        else:
+            ln = synth.make("ln_f32_4096x768", rows=args.profile_rows or 4096)
+
+        def tdev(a):
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(a).to(dev)
+        x, g, b, dy = (tdev(ln[k]) for k in ("x", "gamma", "beta", "dy"))
         y = torch.empty_like(x)
         mean = torch.empty(x.shape[0], device=dev)
         rstd = torch.empty(x.shape[0], device=dev)
@@ -562,6 +572,7 @@ def main():
     ap.add_argument("--profile", choices=["xent", "softmax", "ln_fwd", "ln_bwd"], default=None,
                     help="run only this kernel (for ncu captures of one kernel)")
     ap.add_argument("--profile-rows", type=int, default=0)
+    ap.add_argument("--profile-workload", default="", help="LayerNorm workload name for --profile")
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload and sweep case separately (one JSON line each)")
     ap.add_argument("--cases", default="", help="comma-separated name filters for --sweep")
