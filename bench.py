@@ -426,8 +426,13 @@ def run_profile_case(args):
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
 
     if args.profile == "xent":
-        xe = synth.make("xent_bf16_16384x50304", rows=args.profile_rows or 4096)
-        x, lab = bf16(xe["logits"]), torch.from_numpy(xe["labels"]).to(dev)
+        if args.profile_workload:
+            xe = synth.make(args.profile_workload)
+        else:
+            xe = synth.make("xent_bf16_16384x50304", rows=args.profile_rows or 4096)
+        lg = xe["logits"]
+        x = bf16(lg) if lg.dtype == np.uint16 else torch.from_numpy(lg).to(dev)
+        lab = torch.from_numpy(xe["labels"]).to(dev)
         loss = torch.empty(x.shape[0], device=dev)
         fn = lambda: rr.rr_softmax_xent_fwd_bwd(x, lab, loss, x)  # noqa: E731
     elif args.profile == "softmax":

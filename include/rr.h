@@ -145,8 +145,10 @@ rr_status rr_layernorm_bwd(const void *dy, const void *x, const float *mean,
  * array of 8 MiB inside the library, held on every GPU that loads the library
  * until the process exits.  This entry point allocates nothing (no cudaMalloc,
  * cudaFree or allocating library routine).
- *   - Shapes whose partials need more than 8 MiB (see
- *     rr_layernorm_bwd_workspace_size) return RR_ERR_WORKSPACE_TOO_SMALL.
+ *   - The launch is planned with no more column partials (2 * cols fp32 each)
+ *     than 8 MiB holds, so shapes whose rr_layernorm_bwd plan would need more
+ *     run with fewer row groups.  Rows too long for even one partial
+ *     (cols > 1048576) return RR_ERR_WORKSPACE_TOO_SMALL.
  *   - The first call on each device resolves the scratch's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.

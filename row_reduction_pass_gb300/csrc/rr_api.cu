@@ -108,10 +108,11 @@ struct Plan {
 
 // Chooses the kernel variant and launch shape for (op, dtype, mode, rows, cols)
 // on the current device.  head_free: every row starts 16-byte aligned, so a
-// row needs no extra chunk for a ragged head.  Deterministic for a given device, so the workspace
-// size query and the launch agree.
+// row needs no extra chunk for a ragged head.  max_partials caps the number of
+// row groups (direct) or clusters (staged) that each leave a column partial.
+// Deterministic for a given device, so the workspace size query and the launch agree.
 rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t rows, int64_t cols,
-                    Plan* pl) {
+                    Plan* pl, int64_t max_partials) {
   std::lock_guard<std::mutex> lock(g_mu);
   DevInfo* di = nullptr;
   rr_status st = device_info(&di);
@@ -134,7 +135,7 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
     }
   if (gi >= 0) {
     const int G = 1 << gi;
-    const int T = ks.maxt_direct;
+    const int T = ks.maxt_direct > G ? ks.maxt_direct : G;
     const int ngroups = T / G;
     size_t red = (size_t)(G > 32 ? ngroups * 1024 : 0) + 32;
     const int W = mode == 0 ? V : 1;
@@ -152,6 +153,7 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
       int64_t per_sm = op == kLnBwd ? (occ < 2 ? occ : 2) : occ;
       int64_t grid = cdiv(rows, ngroups);
       if (grid > (int64_t)di->sms * per_sm) grid = (int64_t)di->sms * per_sm;
+      if (grid > max_partials) grid = max_partials;
       pl->staged = false;
       pl->G = G;
       pl->T = T;
@@ -209,6 +211,7 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
         return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
     }
     grid = rows < (int64_t)di->sms * occ ? rows : (int64_t)di->sms * occ;
+    if (grid > max_partials) grid = max_partials;
   } else {
     int& ncl = di->ncl[{fn, ((long long)K << 32) | (long long)smem}];
     if (ncl == 0) {
@@ -227,7 +230,9 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
       if (e != cudaSuccess || ncl <= 0)
         return fail(RR_ERR_CUDA, "cluster occupancy query (K=%d): %s", K, cudaGetErrorString(e));
     }
-    grid = (int64_t)K * (rows < ncl ? rows : ncl);
+    int64_t nc = rows < ncl ? rows : ncl;
+    if (nc > max_partials) nc = max_partials;
+    grid = (int64_t)K * nc;
   }
   pl->staged = true;
   pl->G = T;
@@ -248,12 +253,12 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
 // Plans in chunk mode when allowed, falling back to element mode (which holds
 // longer rows per CTA) when the row does not fit the chunk-mode variants.
 rr_status plan_any(OpKind op, rr_dtype dt, bool chunk_ok, bool head_free, int64_t rows,
-                   int64_t cols, Plan* pl) {
+                   int64_t cols, Plan* pl, int64_t max_partials = INT64_MAX) {
   if (chunk_ok) {
-    rr_status st = make_plan(op, dt, 0, head_free, rows, cols, pl);
+    rr_status st = make_plan(op, dt, 0, head_free, rows, cols, pl, max_partials);
     if (st != RR_ERR_INVALID_ARG) return st;
   }
-  return make_plan(op, dt, 1, false, rows, cols, pl);
+  return make_plan(op, dt, 1, false, rows, cols, pl, max_partials);
 }
 
 template <class P>
@@ -417,8 +422,8 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
 }
 
 static rr_status lnbwd_plan(int64_t rows, int64_t cols, rr_dtype dtype, bool aligned_rows, Plan* pl,
-                            size_t* ws_bytes) {
-  rr_status st = plan_any(kLnBwd, dtype, aligned_rows, true, rows, cols, pl);
+                            size_t* ws_bytes, int64_t max_partials = INT64_MAX) {
+  rr_status st = plan_any(kLnBwd, dtype, aligned_rows, true, rows, cols, pl, max_partials);
   if (st != RR_OK) return st;
   *ws_bytes = (size_t)pl->partials * 2 * (size_t)cols * sizeof(float);
   return RR_OK;
@@ -439,10 +444,14 @@ size_t rr_layernorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtyp
   return best;
 }
 
-rr_status rr_layernorm_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
-                           const void* gamma, void* dx, void* dgamma, void* dbeta, void* workspace,
-                           size_t workspace_bytes, int64_t rows, int64_t cols, rr_dtype dtype,
-                           cudaStream_t stream) {
+}  // extern "C"
+
+// rr_layernorm_bwd with at most max_partials column partials (the no-allocation
+// entry point sizes this to its fixed scratch).
+rr_status layernorm_bwd_capped(const void* dy, const void* x, const float* mean, const float* rstd,
+                               const void* gamma, void* dx, void* dgamma, void* dbeta,
+                               void* workspace, size_t workspace_bytes, int64_t rows, int64_t cols,
+                               rr_dtype dtype, cudaStream_t stream, int64_t max_partials) {
   rr_status st = check_shape(rows, cols, dtype);
   if (st != RR_OK) return st;
   if (!dy || !x || !mean || !rstd || !gamma || !dx || !dgamma || !dbeta || !workspace)
@@ -478,7 +487,7 @@ rr_status rr_layernorm_bwd(const void* dy, const void* x, const float* mean, con
     if (e != cudaSuccess) return fail(RR_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
     pl.partials = 1;
   } else {
-    if ((st = lnbwd_plan(rows, cols, dtype, al, &pl, &need)) != RR_OK) return st;
+    if ((st = lnbwd_plan(rows, cols, dtype, al, &pl, &need, max_partials)) != RR_OK) return st;
     if (workspace_bytes < need)
       return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
     int* err = device_error_word();
@@ -498,6 +507,16 @@ rr_status rr_layernorm_bwd(const void* dy, const void* x, const float* mean, con
   cudaError_t e = cudaLaunchKernel(cr, dim3((unsigned)cdiv(2 * cols, 32)), dim3(1024), args, 0, stream);
   if (e != cudaSuccess) return fail(RR_ERR_CUDA, "column reduce launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+extern "C" {
+
+rr_status rr_layernorm_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+                           const void* gamma, void* dx, void* dgamma, void* dbeta, void* workspace,
+                           size_t workspace_bytes, int64_t rows, int64_t cols, rr_dtype dtype,
+                           cudaStream_t stream) {
+  return layernorm_bwd_capped(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, workspace,
+                              workspace_bytes, rows, cols, dtype, stream, INT64_MAX);
 }
 
 rr_status rr_read_device_error(int device, int* value, int reset) {

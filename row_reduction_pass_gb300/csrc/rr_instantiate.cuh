@@ -31,6 +31,12 @@ KernelSet make_kernel_set() {
   k.direct[1][6] = (const void*)row_kernel<OE, 64, NQE, MAXT_D, false>;
   k.direct[1][7] = (const void*)row_kernel<OE, 128, NQE, MAXT_D, false>;
   k.direct[1][8] = (const void*)row_kernel<OE, 256, NQE, MAXT_D, false>;
+  // one row per block for the widest groups (the block grows to the group)
+  constexpr int T512 = MAXT_D > 512 ? MAXT_D : 512;
+  k.direct[0][9] = (const void*)row_kernel<OC, 512, NQC, T512, false>;
+  k.direct[0][10] = (const void*)row_kernel<OC, 1024, NQC, 1024, false>;
+  k.direct[1][9] = (const void*)row_kernel<OE, 512, NQE, T512, false>;
+  k.direct[1][10] = (const void*)row_kernel<OE, 1024, NQE, 1024, false>;
   k.staged[0] = (const void*)row_kernel<OpT<DT, V, NQSC>, MAXT_S, NQSC, MAXT_S, true>;
   k.staged[1] = (const void*)row_kernel<OpT<DT, 1, NQSE>, MAXT_S, NQSE, MAXT_S, true>;
   k.nq_direct[0] = NQC;

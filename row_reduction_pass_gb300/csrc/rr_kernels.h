@@ -3,7 +3,7 @@
 
 namespace rr {
 
-constexpr int kNumDirectG = 9;  // row groups of 1, 2, 4, ..., 256 threads
+constexpr int kNumDirectG = 11;  // row groups of 1, 2, 4, ..., 1024 threads
 
 // The variants of one operation for one storage type.  Index [m] is the mode:
 // 0 = 16-byte chunks, 1 = single elements.

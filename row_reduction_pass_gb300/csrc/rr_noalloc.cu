@@ -34,16 +34,25 @@ void* g_ptr[kMaxDev];
 
 // Sets the detail string returned by rr_last_error_detail (defined in rr_api.cu).
 void rr_set_error_detail(const char* msg);
+// rr_layernorm_bwd with at most max_partials column partials (rr_api.cu).
+rr_status layernorm_bwd_capped(const void* dy, const void* x, const float* mean, const float* rstd,
+                               const void* gamma, void* dx, void* dgamma, void* dbeta,
+                               void* workspace, size_t workspace_bytes, int64_t rows, int64_t cols,
+                               rr_dtype dtype, cudaStream_t stream, int64_t max_partials);
 
 extern "C" rr_status rr_layernorm_bwd_noalloc(const void* dy, const void* x, const float* mean,
                                               const float* rstd, const void* gamma, void* dx,
                                               void* dgamma, void* dbeta, int64_t rows,
                                               int64_t cols, rr_dtype dtype, cudaStream_t stream) {
-  const size_t need = rr_layernorm_bwd_workspace_size(rows, cols, dtype);
-  if (need > kNoAllocScratchBytes) {
+  // One column partial is a row of dgamma and a row of dbeta sums in fp32; the
+  // launch is planned with no more partials than the scratch holds (fewer
+  // row groups than rr_layernorm_bwd would use when the columns are many).
+  const int64_t per_partial = cols > 0 ? 2 * cols * (int64_t)sizeof(float) : 1;
+  const int64_t max_partials = (int64_t)kNoAllocScratchBytes / per_partial;
+  if (max_partials < 1) {
     rr_set_error_detail(
-        "rr_layernorm_bwd_noalloc: this shape needs more column-partial scratch than the "
-        "library's fixed 8 MiB; use rr_layernorm_bwd with a caller-provided workspace");
+        "rr_layernorm_bwd_noalloc: one column partial (2 * cols * 4 bytes) exceeds the "
+        "library's fixed 8 MiB scratch; use rr_layernorm_bwd with a caller-provided workspace");
     return RR_ERR_WORKSPACE_TOO_SMALL;
   }
   int dev = 0;
@@ -66,6 +75,6 @@ extern "C" rr_status rr_layernorm_bwd_noalloc(const void* dy, const void* x, con
     }
     ptr = g_ptr[dev];
   }
-  return rr_layernorm_bwd(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, ptr, kNoAllocScratchBytes,
-                          rows, cols, dtype, stream);
+  return layernorm_bwd_capped(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, ptr,
+                              kNoAllocScratchBytes, rows, cols, dtype, stream, max_partials);
 }

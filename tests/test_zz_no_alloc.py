@@ -41,8 +41,11 @@ def _call_noalloc(lib, dyd, xd, mean, rstd, gd, dx, dg, db):
     assert st == 0, lib.rr_last_error_detail()
 
 
+# (1000, 9001, f32): rr_layernorm_bwd's plan wants more than 8 MiB of partials,
+# so this one runs with fewer row groups than the workspace variant
 @pytest.mark.parametrize("rows,cols,dtype", [(4096, 768, "f32"), (3000, 97, "bf16"),
-                                             (1000, 2048, "f32"), (777, 4097, "bf16")])
+                                             (1000, 2048, "f32"), (777, 4097, "bf16"),
+                                             (1000, 9001, "f32")])
 def test_noalloc_matches_workspace_variant_twice(rows, cols, dtype):
     lib = rr.load_library()
     xd, gd, dyd, mean, rstd = _dev_inputs(rows, cols, dtype, 11 + cols)
@@ -50,6 +53,13 @@ def test_noalloc_matches_workspace_variant_twice(rows, cols, dtype):
     rr.rr_layernorm_bwd(dyd, xd, mean, rstd, gd, ref_dx, ref_dg, ref_db)
     torch.cuda.synchronize()
     rtol, atol = TOL[dtype]
+    # dgamma / dbeta are fp32 column sums whose rounding follows the number of
+    # row groups; both calls are held to the parity bound against sum_r |term_r|
+    live = (rstd != 0)[:, None]           # rstd == 0 marks a masked row: no terms
+    xh = (xd.double() - mean.double()[:, None]) * rstd.double()[:, None]
+    zero = torch.zeros((), dtype=torch.float64, device=xd.device)
+    sdg = host(torch.where(live, (dyd.double() * xh).abs(), zero).sum(0))
+    sdb = host(torch.where(live, dyd.double().abs(), zero).sum(0))
     for _ in range(2):
         dx = torch.full_like(xd, float("nan"))
         dg = torch.full_like(gd, float("nan"))
@@ -57,15 +67,13 @@ def test_noalloc_matches_workspace_variant_twice(rows, cols, dtype):
         _call_noalloc(lib, dyd, xd, mean, rstd, gd, dx, dg, db)
         torch.cuda.synchronize()
         compare("noalloc dx", host(dx), host(ref_dx), rtol, atol)
-        compare("noalloc dgamma", host(dg), host(ref_dg), rtol, atol)
-        compare("noalloc dbeta", host(db), host(ref_db), rtol, atol)
+        compare("noalloc dgamma", host(dg), host(ref_dg), rtol, atol, scale=2 * sdg)
+        compare("noalloc dbeta", host(db), host(ref_db), rtol, atol, scale=2 * sdb)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib = rr.load_library()
-    rows, cols = 1000, 9001              # partials beyond 8 MiB; nothing is launched
-    need = lib.rr_layernorm_bwd_workspace_size(rows, cols, 0)
-    assert need > (8 << 20)
+    rows, cols = 2, (1 << 20) + 1        # one partial alone is beyond 8 MiB; nothing is launched
     fake = ctypes.c_void_p(1 << 20)
     st = lib.rr_layernorm_bwd_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, rows, cols, 0,
                                       ctypes.c_void_p(0))
