@@ -468,7 +468,8 @@ def run_profile_case(args):
 
 def run_sweep(args):
     """Times every operation of every measured workload on its own (L2 flushed
-    between repetitions by writing a 256 MB buffer), against the HBM roofline.
+    between repetitions by writing a 256 MB buffer and reading another), against
+    the HBM roofline.
     Prints one JSON line per case; not the contract line."""
     import torch
     import row_reduction_pass_gb300 as rr
@@ -476,7 +477,17 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     rr.load_library()
     peak, peak_src = hbm_peak()
+    # L2 flush between calls: write 256 MB (twice the L2), then read another
+    # 256 MB, so the flush's own dirty lines are written back inside the flush
+    # and the timed call starts with an L2 of clean lines that hold none of its data
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.zeros(32 << 20, dtype=torch.int64, device=dev)
+    flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def l2_flush():
+        flush.zero_()
+        torch.sum(flush_rd, dim=0, out=flush_sink)
+
     reps = max(3, args.steps)
 
     def tdev(a):
@@ -497,11 +508,11 @@ def run_sweep(args):
         with torch.cuda.stream(s):
             with torch.cuda.graph(g_both, stream=s):
                 for _ in range(reps):
-                    flush.zero_()
+                    l2_flush()
                     fn()
             with torch.cuda.graph(g_flush, stream=s):
                 for _ in range(reps):
-                    flush.zero_()
+                    l2_flush()
         torch.cuda.synchronize()
 
         def run(gr):

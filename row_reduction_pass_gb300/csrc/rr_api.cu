@@ -11,6 +11,7 @@
 
 #include "../../include/rr.h"
 #include "rr_kernels.h"
+#include "rr_ln.cuh"
 #include "rr_ops.cuh"
 
 namespace {
@@ -92,10 +93,19 @@ const KernelSet& kernels(OpKind op, rr_dtype dt) {
   return sets[op][dt];
 }
 
+const rr::LnKernelSet& ln_kernels(OpKind op, rr_dtype dt) {
+  static rr::LnKernelSet sets[2][2] = {
+      {rr::ln_fwd_rowgroup_kernels_f32(), rr::ln_fwd_rowgroup_kernels_bf16()},
+      {rr::ln_bwd_rowgroup_kernels_f32(), rr::ln_bwd_rowgroup_kernels_bf16()},
+  };
+  return sets[op == kLnFwd ? 0 : 1][dt];
+}
+
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
 struct Plan {
+  int kind = 0;  // 0: row engine (rr::Geo), 1: row-group LayerNorm (rr::LnGeo)
   bool staged = false;
   int mode = 0;  // 0: 16-byte chunks, 1: elements
   int G = 0, T = 0, K = 1;
@@ -104,6 +114,7 @@ struct Plan {
   size_t smem = 0;
   int64_t partials = 0;  // LayerNorm backward: rows of column partials
   rr::Geo geo{};
+  rr::LnGeo lgeo{};
 };
 
 // Chooses the kernel variant and launch shape for (op, dtype, mode, rows, cols)
@@ -133,7 +144,7 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
       gi = i;
       break;
     }
-  if (gi >= 0) {
+  if (gi >= 0 && ks.direct[mode][0] != nullptr) {
     const int G = 1 << gi;
     const int T = ks.maxt_direct > G ? ks.maxt_direct : G;
     const int ngroups = T / G;
@@ -250,6 +261,74 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
   return RR_OK;
 }
 
+// Row-group LayerNorm plan (rr_ln.cuh): the smallest group G whose threads
+// hold a row, G = 1 .. 1024, with gamma / beta (and the backward's column
+// partials) in shared memory.  lmode: 0 chunks with aligned rows, 1 chunks
+// with any row alignment, 2 elements.  RR_ERR_INVALID_ARG when the row does
+// not fit one group (the caller then plans the staged engine kernels).
+rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64_t cols, Plan* pl,
+                           int64_t max_partials) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo* di = nullptr;
+  rr_status st = device_info(&di);
+  if (st != RR_OK) return st;
+  const rr::LnKernelSet& ls = ln_kernels(op, dt);
+  const int E = dt == RR_BF16 ? 2 : 4;
+  const int W = lmode == 2 ? 1 : 16 / E;
+  const int64_t nfull = cols / W, rag = cols % W, nch = nfull + (rag > 0 ? 1 : 0);
+  const int nq = ls.nq[lmode];
+  int gi = -1;
+  for (int i = 0; i < rr::kNumLnG; ++i)
+    if ((int64_t)nq << i >= nch) {
+      gi = i;
+      break;
+    }
+  if (gi < 0 || ls.k[lmode][gi] == nullptr)
+    return fail(RR_ERR_INVALID_ARG, "row longer than one row group holds");
+  const void* fn = ls.k[lmode][gi];
+  // rows of at most 32 chunks: one chunk per thread where that variant exists
+  for (int i = 0; i <= 5; ++i)
+    if (((int64_t)1 << i) >= nch) {
+      if (ls.k1[lmode][i] != nullptr) {
+        gi = i;
+        fn = ls.k1[lmode][i];
+      }
+      break;
+    }
+  const int G = 1 << gi;
+  const int M1 = op == kLnFwd ? 256 : 512;
+  const int T = G > M1 ? G : M1;
+  const int ngroups = T / G;
+  const int64_t npad = nch * W;
+  const int64_t red_off = round_up((op == kLnFwd ? 2 : 1) * npad * 4, 16);
+  const int64_t acc_off = round_up(red_off + (G > 32 ? (int64_t)ngroups * 1024 : 0), 16);
+  const int64_t smem = acc_off + (op == kLnBwd ? (int64_t)ngroups * 2 * npad * 4 : 0);
+  if (smem > di->smem_optin) return fail(RR_ERR_INVALID_ARG, "row-group shared memory too large");
+  if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
+  int& occ = di->occ[{fn, ((long long)T << 32) | (long long)smem}];
+  if (occ == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, T, (size_t)smem);
+    if (e != cudaSuccess || occ <= 0)
+      return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+  }
+  int64_t grid = cdiv(rows, ngroups);
+  if (grid > (int64_t)di->sms * occ) grid = (int64_t)di->sms * occ;
+  if (grid > max_partials) grid = max_partials;
+  pl->kind = 1;
+  pl->staged = false;
+  pl->mode = lmode;
+  pl->G = G;
+  pl->T = T;
+  pl->K = 1;
+  pl->fn = fn;
+  pl->grid = grid;
+  pl->smem = (size_t)smem;
+  pl->partials = grid;
+  pl->lgeo = rr::LnGeo{rows, (int32_t)cols, (int32_t)nfull, (int32_t)rag, (int32_t)nch,
+                       (int32_t)red_off, (int32_t)acc_off};
+  return RR_OK;
+}
+
 // Plans in chunk mode when allowed, falling back to element mode (which holds
 // longer rows per CTA) when the row does not fit the chunk-mode variants.
 rr_status plan_any(OpKind op, rr_dtype dt, bool chunk_ok, bool head_free, int64_t rows,
@@ -280,7 +359,8 @@ rr_status launch(const Plan& pl, const P& params, cudaStream_t stream) {
   }
   P pcopy = params;
   rr::Geo g = pl.geo;
-  void* args[] = {&pcopy, &g};
+  rr::LnGeo lg = pl.lgeo;
+  void* args[] = {&pcopy, pl.kind == 1 ? static_cast<void*>(&lg) : static_cast<void*>(&g)};
   cudaError_t e = cudaLaunchKernelExC(&cfg, pl.fn, args);
   if (e != cudaSuccess)
     return fail(RR_ERR_CUDA, "launch (grid %lld, block %d, smem %zu, cluster %d): %s",
@@ -410,8 +490,11 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
     return fail(RR_ERR_ALIASING, "outputs overlap inputs");
   // column-aligned chunks need 16-byte aligned gamma / beta; rows may have any alignment
   const bool al = aligned(gamma, 16) && aligned(beta, 16);
+  const bool rows_al = (cols * (int64_t)E) % 16 == 0 && aligned(x, 16) && aligned(y, 16);
   Plan pl;
-  if ((st = plan_any(kLnFwd, dtype, al, true, rows, cols, &pl)) != RR_OK) return st;
+  st = ln_rowgroup_plan(kLnFwd, dtype, al ? (rows_al ? 0 : 1) : 2, rows, cols, &pl, INT64_MAX);
+  if (st == RR_ERR_INVALID_ARG) st = plan_any(kLnFwd, dtype, al, true, rows, cols, &pl);
+  if (st != RR_OK) return st;
   int* err = device_error_word();
   if (!err) return RR_ERR_CUDA;
   rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma),
@@ -421,9 +504,13 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
   return ok();
 }
 
-static rr_status lnbwd_plan(int64_t rows, int64_t cols, rr_dtype dtype, bool aligned_rows, Plan* pl,
+// lmode as for ln_rowgroup_plan; rows too long for one row group go to the
+// staged engine kernels (chunk mode unless lmode == 2).
+static rr_status lnbwd_plan(int64_t rows, int64_t cols, rr_dtype dtype, int lmode, Plan* pl,
                             size_t* ws_bytes, int64_t max_partials = INT64_MAX) {
-  rr_status st = plan_any(kLnBwd, dtype, aligned_rows, true, rows, cols, pl, max_partials);
+  rr_status st = ln_rowgroup_plan(kLnBwd, dtype, lmode, rows, cols, pl, max_partials);
+  if (st == RR_ERR_INVALID_ARG)
+    st = plan_any(kLnBwd, dtype, lmode != 2, true, rows, cols, pl, max_partials);
   if (st != RR_OK) return st;
   *ws_bytes = (size_t)pl->partials * 2 * (size_t)cols * sizeof(float);
   return RR_OK;
@@ -436,10 +523,10 @@ size_t rr_layernorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtyp
   // for the same shape, but the caller does not know which mode the pointers
   // will select, so report the larger of the two.
   size_t best = 0;
-  for (int m = 0; m < 2; ++m) {
+  for (int m = 0; m < 3; m += 2) {  // chunk modes 0 and 1 plan alike
     Plan pl;
     size_t ws = 0;
-    if (lnbwd_plan(rows, cols, dtype, m == 0, &pl, &ws) == RR_OK && ws > best) best = ws;
+    if (lnbwd_plan(rows, cols, dtype, m, &pl, &ws) == RR_OK && ws > best) best = ws;
   }
   return best;
 }
@@ -487,7 +574,10 @@ rr_status layernorm_bwd_capped(const void* dy, const void* x, const float* mean,
     if (e != cudaSuccess) return fail(RR_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
     pl.partials = 1;
   } else {
-    if ((st = lnbwd_plan(rows, cols, dtype, al, &pl, &need, max_partials)) != RR_OK) return st;
+    const bool rows_al = (cols * (int64_t)E) % 16 == 0 && aligned(dy, 16) && aligned(x, 16) &&
+                         aligned(dx, 16);
+    const int lmode = al ? (rows_al ? 0 : 1) : 2;
+    if ((st = lnbwd_plan(rows, cols, dtype, lmode, &pl, &need, max_partials)) != RR_OK) return st;
     if (workspace_bytes < need)
       return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
     int* err = device_error_word();

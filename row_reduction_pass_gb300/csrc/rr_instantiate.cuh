@@ -6,13 +6,16 @@
 
 namespace rr {
 
+// DIRECT = false: staged variants only (the operation's direct rows go to
+// other kernels); the direct table is left empty.
 template <template <int, int, int> class OpT, int DT, int NQC, int NQE, int MAXT_D, int NQSC,
-          int NQSE, int MAXT_S>
+          int NQSE, int MAXT_S, bool DIRECT = true>
 KernelSet make_kernel_set() {
   constexpr int V = DType<DT>::V;
   using OC = OpT<DT, V, NQC>;
   using OE = OpT<DT, 1, NQE>;
   KernelSet k{};
+  if constexpr (DIRECT) {
   k.direct[0][0] = (const void*)row_kernel<OC, 1, NQC, MAXT_D, false>;
   k.direct[0][1] = (const void*)row_kernel<OC, 2, NQC, MAXT_D, false>;
   k.direct[0][2] = (const void*)row_kernel<OC, 4, NQC, MAXT_D, false>;
@@ -37,6 +40,7 @@ KernelSet make_kernel_set() {
   k.direct[0][10] = (const void*)row_kernel<OC, 1024, NQC, 1024, false>;
   k.direct[1][9] = (const void*)row_kernel<OE, 512, NQE, T512, false>;
   k.direct[1][10] = (const void*)row_kernel<OE, 1024, NQE, 1024, false>;
+  }
   k.staged[0] = (const void*)row_kernel<OpT<DT, V, NQSC>, MAXT_S, NQSC, MAXT_S, true>;
   k.staged[1] = (const void*)row_kernel<OpT<DT, 1, NQSE>, MAXT_S, NQSE, MAXT_S, true>;
   k.nq_direct[0] = NQC;

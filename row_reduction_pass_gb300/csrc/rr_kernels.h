@@ -16,12 +16,28 @@ struct KernelSet {
   int maxt_staged;
 };
 
+// Row-group LayerNorm kernels (rr_ln.cuh).  Index [m][i]: m = 0 chunk mode
+// with every row start 16-byte aligned, 1 chunk mode with any element
+// alignment, 2 element mode; G = 2^i threads per row group.
+constexpr int kNumLnG = 11;
+struct LnKernelSet {
+  const void* k[3][kNumLnG];
+  int nq[3];  // chunks (elements in element mode) per thread
+  // One chunk per thread, G <= 32 (backward: fewer registers, so more warps
+  // per SM for short rows); null where not built.
+  const void* k1[3][kNumLnG];
+};
+
 KernelSet softmax_kernels_f32();
 KernelSet softmax_kernels_bf16();
 KernelSet lnfwd_kernels_f32();
 KernelSet lnfwd_kernels_bf16();
 KernelSet lnbwd_kernels_f32();
 KernelSet lnbwd_kernels_bf16();
+LnKernelSet ln_fwd_rowgroup_kernels_f32();
+LnKernelSet ln_fwd_rowgroup_kernels_bf16();
+LnKernelSet ln_bwd_rowgroup_kernels_f32();
+LnKernelSet ln_bwd_rowgroup_kernels_bf16();
 const void* col_reduce_kernel_ptr_f32();
 const void* col_reduce_kernel_ptr_bf16();
 

@@ -1,0 +1,602 @@
+// rr_ln.cuh -- LayerNorm forward and backward on column-owned row groups
+// ("Engineering a CUDA Machine Learning Framework from Scratch", sec. 3.2 for
+// the one-pass moments, sec. 2.2 for the analytic backward).
+//
+// Rows that fit in the registers of one row group of G threads (G = 1 ..
+// 1024) take these kernels.  Thread gt of a group owns the column-aligned
+// chunks k = gt + q*G (q < NQ) of every row the group processes; a chunk is W
+// columns (W = 16 bytes / element size, or one element in element mode).
+// Which of its chunks are whole and whether it holds the row's ragged last
+// chunk are therefore the same for every row and are worked out once per
+// launch; gamma / beta are converted to fp32 once per block into shared
+// memory; the backward keeps its per-column partial sums (sum_r dy*xhat and
+// sum_r dy) in registers across all the rows a thread processes and writes
+// them out once per block.
+//
+// Ragged slots of the last chunk are loaded as 0: they add exactly nothing to
+// the compensated sum, to sum dy*gamma, to sum dy*gamma*xhat (dy = 0 there) or
+// to the column partials, so only the squared deviations and the stores mask
+// them.
+#pragma once
+
+#include "rr_kernels.h"
+#include "rr_ops.cuh"
+
+namespace rr {
+
+// Launch geometry of a row-group LayerNorm launch (host-computed).
+struct LnGeo {
+  int64_t rows;
+  int32_t cols;
+  int32_t nfull;    // whole chunks per row (cols / W)
+  int32_t rag;      // elements of the ragged last chunk (0: none)
+  int32_t nch;      // chunks per row
+  int32_t red_off;  // group-reduction scratch (G > 32): 1 KB per group
+  int32_t acc_off;  // backward: column partials, ngroups x 2 x (nch * W) floats
+};
+
+// Register sizes.  Forward: 64 per thread at any block size.  Backward: up to
+// 128 (a thread keeps g = dy*gamma, xhat and its two column accumulators), 64
+// for the one-chunk variants of short rows.
+template <int MAXT> constexpr int ln_fwd_min_blocks() { return 1024 / MAXT; }
+template <int MAXT, int NQ> constexpr int ln_bwd_min_blocks() { return (NQ == 1 ? 1024 : 512) / MAXT; }
+
+// A sum carried as a leading float s and an accumulated error e (cascaded
+// summation in the manner of Ogita, Rump and Oishi's Sum2): a merge adds the
+// leading parts with TwoSum and the rest in plain fp32, so the result is as
+// accurate as a sum in twice the precision; renormalised once at the end.
+struct CascSum {
+  float s, e;
+  __device__ __forceinline__ static CascSum identity() { return {0.f, 0.f}; }
+  __device__ __forceinline__ static CascSum shfl_xor(const CascSum& v, int off) {
+    return {__shfl_xor_sync(0xffffffffu, v.s, off), __shfl_xor_sync(0xffffffffu, v.e, off)};
+  }
+};
+struct MergeCasc {
+  __device__ __forceinline__ CascSum operator()(const CascSum& a, const CascSum& b) const {
+    float s, err;
+    two_sum(a.s, b.s, s, err);
+    return {s, (a.e + b.e) + err};
+  }
+};
+
+// Per-row reductions across a row group: G <= 32 lanes by an ordered
+// butterfly; wider groups by a butterfly per warp, the warp results through
+// shared memory (two slots per warp, alternating by call parity, so one named
+// barrier per call suffices) and a butterfly over those G/32 values (lane l
+// reads warp l mod G/32, so every aligned block of G/32 lanes holds them all).
+// Every thread of the group ends with the same bits.
+template <int G>
+struct LnRed {
+  unsigned char* slot;
+  int calls;
+  int bar;
+  template <class S, class M>
+  __device__ __forceinline__ S operator()(S s, M merge) {
+    static_assert(sizeof(S) <= 16, "statistic larger than a scratch slot");
+    if constexpr (G <= 32) {
+      return group_reduce<S, M, G>(s, merge);
+    } else {
+      s = group_reduce<S, M, 32>(s, merge);
+      unsigned char* base = slot + (calls & 1) * 512;
+      ++calls;
+      const int lane = threadIdx.x & 31;
+      if (lane == 0) *reinterpret_cast<S*>(base + 16 * ((threadIdx.x % G) >> 5)) = s;
+      named_bar(bar, G);
+      const S o = *reinterpret_cast<const S*>(base + 16 * (lane & (G / 32 - 1)));
+      return group_reduce<S, M, G / 32>(o, merge);
+    }
+  }
+};
+
+// The chunks of one thread: q < nf are whole, q < nown are owned (the ragged
+// last chunk of the row, when this thread holds it, is q = nf).
+template <int G, int NQ>
+struct LnCols {
+  int nf, nown;
+  __device__ __forceinline__ void init(int gt, int nfull, int rag) {
+    nf = nfull > gt ? (nfull - gt + G - 1) / G : 0;
+    nf = nf < NQ ? nf : NQ;
+    const bool rq = rag > 0 && nfull >= gt && (nfull - gt) % G == 0 && (nfull - gt) / G < NQ;
+    nown = nf + (rq ? 1 : 0);
+  }
+};
+
+template <int DT, int W>
+__device__ __forceinline__ float ln_get(const uint4& c, int e) {
+  if constexpr (W == 1) return bits_to_f32<DT>(c.x);
+  else return chunk_get<DT>(c, e);
+}
+
+// Loads the thread's chunks of the row starting at rs (a tensor spanning
+// [tb, te)).  AL: every row start is 16-byte aligned.  Otherwise a row whose
+// start is not is read as the funnel shift of the two aligned chunks holding
+// each of its chunks (neighbouring lanes share those through L1), or element by
+// element where that pair would leave the tensor.
+template <int DT, int W, int G, int NQ, bool AL>
+__device__ __forceinline__ void ln_load(uint4 (&v)[NQ], const char* rs, int gt,
+                                        const LnCols<G, NQ>& cs, int rag, const char* tb,
+                                        const char* te) {
+  constexpr int E = DType<DT>::E;
+  if constexpr (W == 1) {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+      v[q] = make_uint4(q < cs.nown ? ld_elem_bits<DT>(rs + (int64_t)(gt + q * G) * E) : 0u, 0u,
+                        0u, 0u);
+  } else {
+    const uintptr_t ra = reinterpret_cast<uintptr_t>(rs);
+    const int h = AL ? 0 : static_cast<int>(ra & 15);
+    bool split = false;
+    if constexpr (!AL) {
+      if (h != 0 && cs.nf > 0) {
+        const uintptr_t lo = (ra + (uintptr_t)gt * 16) & ~uintptr_t(15);
+        const uintptr_t hi = ((ra + (uintptr_t)(gt + (cs.nf - 1) * G) * 16) & ~uintptr_t(15)) + 32;
+        split = lo >= reinterpret_cast<uintptr_t>(tb) && hi <= reinterpret_cast<uintptr_t>(te);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const char* a = rs + (int64_t)(gt + q * G) * 16;
+      uint4 c = make_uint4(0u, 0u, 0u, 0u);
+      if (q < cs.nf) {
+        if (AL || h == 0) {
+          c = ld_chunk_stream(a);
+        } else if (split) {
+          c = ld16_split(a);
+        } else {
+#pragma unroll
+          for (int e = 0; e < W; ++e) chunk_set_bits<DT>(c, e, ld_elem_bits<DT>(a + e * E));
+        }
+      } else if (q < cs.nown) {
+#pragma unroll
+        for (int e = 0; e < W; ++e)
+          if (e < rag) chunk_set_bits<DT>(c, e, ld_elem_bits<DT>(a + e * E));
+      }
+      v[q] = c;
+    }
+  }
+}
+
+// Stores chunk q (W values f) of the row starting at rs: whole chunks as one
+// 128-bit store when the row start is aligned, else as aligned pieces; the
+// ragged chunk element by element.
+template <int DT, int W, int G, int NQ, bool AL>
+__device__ __forceinline__ void ln_store(char* rs, int gt, int q, const LnCols<G, NQ>& cs,
+                                         int rag, const float (&f)[W]) {
+  constexpr int E = DType<DT>::E;
+  if constexpr (W == 1) {
+    st_elem<DT>(rs + (int64_t)(gt + q * G) * E, f[0]);
+  } else {
+    char* a = rs + (int64_t)(gt + q * G) * 16;
+    if (q < cs.nf) {
+      const uint4 c = chunk_pack<DT>(f);
+      if (AL || (reinterpret_cast<uintptr_t>(rs) & 15) == 0) st_chunk_stream(a, c);
+      else st16_split(a, c);
+    } else {
+#pragma unroll
+      for (int e = 0; e < W; ++e)
+        if (e < rag) st_elem<DT>(a + e * E, f[e]);
+    }
+  }
+}
+
+// gamma / beta (or gamma alone) as fp32 in shared memory.  Chunk mode keeps
+// the four columns e = 4p .. 4p+3 of chunk k at plane p, offset 4k, so a lane
+// reads 16 contiguous bytes per plane (conflict-free for consecutive chunks).
+template <int W>
+struct LnPlanes {
+  float* base;
+  int npl;  // floats per plane
+  // The W values of chunk k (W >= 4) or the value of column k (W == 1).
+  __device__ __forceinline__ void get(int k, float (&out)[W]) const {
+    if constexpr (W >= 4) {
+#pragma unroll
+      for (int p = 0; p < W / 4; ++p) {
+        const float4 t = *reinterpret_cast<const float4*>(base + p * npl + k * 4);
+        out[4 * p] = t.x;
+        out[4 * p + 1] = t.y;
+        out[4 * p + 2] = t.z;
+        out[4 * p + 3] = t.w;
+      }
+    } else {
+      out[0] = base[k];
+    }
+  }
+};
+
+// Converts gamma (or beta) into its planes.  Chunk mode: one 16-byte load per
+// chunk (the vector is 16-byte aligned there), up to four chunks in flight per
+// thread so the L2 round trips overlap; element mode: scalar loads, unrolled.
+template <int DT, int W>
+__device__ __forceinline__ void ln_stage(const LnPlanes<W>& pl, const char* src, int cols, int nch) {
+  constexpr int E = DType<DT>::E;
+  if constexpr (W >= 4) {
+    const int nfull = cols / W;
+    for (int k0 = threadIdx.x; k0 < nch; k0 += 4 * blockDim.x) {
+      uint4 c[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = k0 + u * blockDim.x;
+        c[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (k < nfull) {
+          c[u] = ld_chunk_cached(src + (int64_t)k * 16);
+        } else if (k < nch) {
+#pragma unroll
+          for (int e = 0; e < W; ++e)
+            if (k * W + e < cols) {
+              const float f = ld_elem_cached<DT>(src + (int64_t)(k * W + e) * E);
+              chunk_set_bits<DT>(c[u], e, DT == kF32 ? __float_as_uint(f) : __float_as_uint(f) >> 16);
+            }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = k0 + u * blockDim.x;
+        if (k < nch) {
+#pragma unroll
+          for (int p = 0; p < W / 4; ++p)
+            *reinterpret_cast<float4*>(pl.base + p * pl.npl + k * 4) =
+                make_float4(chunk_get<DT>(c[u], 4 * p), chunk_get<DT>(c[u], 4 * p + 1),
+                            chunk_get<DT>(c[u], 4 * p + 2), chunk_get<DT>(c[u], 4 * p + 3));
+        }
+      }
+    }
+  } else {
+#pragma unroll 8
+    for (int j = threadIdx.x; j < cols; j += blockDim.x)
+      pl.base[j] = ld_elem_cached<DT>(src + (int64_t)j * E);
+  }
+}
+
+// ------------------------------------------------------------ forward ------
+//
+// Per row: compensated (TwoSum) sum of the thread's values, reduced over the
+// group as a double-float -> exact mean mh + ml; squared deviations
+// ((x - mh) - ml)^2 -> M2 -> rstd = 1/sqrt(M2/C + eps); y = xhat*gamma + beta.
+// A row with a non-finite mean or variance is masked: y = 0, mean = rstd = 0.
+template <int DT, int W, int G, int NQ, bool AL, int MAXT>
+__global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
+    ln_fwd_kernel(const LnFwdParams p, const LnGeo geo) {
+  constexpr int E = DType<DT>::E;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int npad = geo.nch * W;
+  const int npl = W >= 4 ? geo.nch * 4 : geo.nch;
+  const LnPlanes<W> sg{reinterpret_cast<float*>(smem), npl};
+  const LnPlanes<W> sb{reinterpret_cast<float*>(smem) + npad, npl};
+  ln_stage<DT, W>(sg, p.gamma, geo.cols, geo.nch);
+  ln_stage<DT, W>(sb, p.beta, geo.cols, geo.nch);
+  __syncthreads();
+
+  constexpr int ngroups = MAXT / G;
+  const int grp = threadIdx.x / G, gt = threadIdx.x % G;
+  LnCols<G, NQ> cs;
+  cs.init(gt, geo.nfull, geo.rag);
+  LnRed<G> rd{smem + geo.red_off + grp * 1024, 0, 1 + grp};
+  const int64_t step = (int64_t)gridDim.x * ngroups;
+  const int64_t r0 = (int64_t)blockIdx.x * ngroups + grp;
+  // first row of the warp's first group: sub-warp groups stay in lock step
+  const int64_t w0 = (int64_t)blockIdx.x * ngroups + (G < 32 ? (threadIdx.x & ~31) / G : grp);
+  const int64_t rowb = (int64_t)geo.cols * E;
+  const char* xend = p.x + geo.rows * rowb;
+  const float ns = static_cast<float>(geo.cols);
+
+  for (int64_t it = 0;; ++it) {
+    if (w0 + it * step >= geo.rows) break;
+    const int64_t r = r0 + it * step;
+    const bool active = r < geo.rows;
+    uint4 v[NQ];
+    if (active) {
+      ln_load<DT, W, G, NQ, AL>(v, p.x + r * rowb, gt, cs, geo.rag, p.x, xend);
+    } else {
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
+    }
+
+    // 1. compensated sum (two interleaved TwoSum accumulators per packed pair)
+    float s0 = 0.f, s1 = 0.f, c0 = 0.f, c1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (q < cs.nown) {
+        if constexpr (W > 1) {
+#pragma unroll
+          for (int e = 0; e < W; e += 2) {
+            const float v0 = ln_get<DT, W>(v[q], e), v1 = ln_get<DT, W>(v[q], e + 1);
+            float t0, t1, b0, b1, u0, u1, w0_, w1_;
+            add2(t0, t1, s0, s1, v0, v1);      // t = s + v
+            add2(b0, b1, t0, t1, -s0, -s1);    // bb = t - s
+            add2(u0, u1, t0, t1, -b0, -b1);    // t - bb
+            add2(u0, u1, s0, s1, -u0, -u1);    // s - (t - bb)
+            add2(w0_, w1_, v0, v1, -b0, -b1);  // v - bb
+            add2(u0, u1, u0, u1, w0_, w1_);    // exact error of s + v
+            add2(c0, c1, c0, c1, u0, u1);
+            s0 = t0;
+            s1 = t1;
+          }
+        } else {
+          float t, err;
+          two_sum(s0, ln_get<DT, W>(v[q], 0), t, err);
+          c0 += err;
+          s0 = t;
+        }
+      }
+    }
+    CascSum S;
+    {
+      float s, e;
+      two_sum(s0, s1, s, e);
+      S = {s, (c0 + c1) + e};
+    }
+    S = rd(S, MergeCasc());
+    float mh, ml;
+    {
+      float sh, sl;
+      two_sum(S.s, S.e, sh, sl);
+      df_mean(sh, sl, ns, p.inv_cols, mh, ml);
+    }
+
+    // 2. squared deviations from the exact mean (ragged slots excluded)
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (q < cs.nown) {
+        if constexpr (W > 1) {
+          const bool whole = q < cs.nf;
+#pragma unroll
+          for (int e = 0; e < W; e += 2) {
+            float d0, d1;
+            add2(d0, d1, ln_get<DT, W>(v[q], e), ln_get<DT, W>(v[q], e + 1), -mh, -mh);
+            add2(d0, d1, d0, d1, -ml, -ml);
+            if (!whole) {
+              if (e >= geo.rag) d0 = 0.f;
+              if (e + 1 >= geo.rag) d1 = 0.f;
+            }
+            fma2(a0, a1, d0, d1, d0, d1, a0, a1);
+          }
+        } else {
+          const float d = (ln_get<DT, W>(v[q], 0) - mh) - ml;
+          a0 = fmaf(d, d, a0);
+        }
+      }
+    }
+    const float m2 = rd(Sum1{a0 + a1}, MergeSum1()).s;
+    if (!active) continue;
+    const float var = m2 * p.inv_cols;
+    const bool masked = !(isfinite(mh) && isfinite(ml) && isfinite(var));
+    const float rstd = masked ? 0.f : rsqrtf(var + p.eps);
+    if (gt == 0) {
+      p.mean[r] = masked ? 0.f : mh + ml;
+      p.rstd[r] = rstd;
+    }
+
+    // 3. y = ((x - mh) - ml) * rstd * gamma + beta
+    char* yr = p.y + r * rowb;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (q < cs.nown) {
+        float f[W];
+        if (masked) {
+#pragma unroll
+          for (int e = 0; e < W; ++e) f[e] = 0.f;
+        } else {
+          const int k = gt + q * G;
+          float gm[W], bt[W];
+          sg.get(k, gm);
+          sb.get(k, bt);
+          if constexpr (W > 1) {
+#pragma unroll
+            for (int e = 0; e < W; e += 2) {
+              float t0, t1;
+              add2(t0, t1, ln_get<DT, W>(v[q], e), ln_get<DT, W>(v[q], e + 1), -mh, -mh);
+              add2(t0, t1, t0, t1, -ml, -ml);
+              mul2(t0, t1, t0, t1, rstd, rstd);
+              fma2(f[e], f[e + 1], t0, t1, gm[e], gm[e + 1], bt[e], bt[e + 1]);
+            }
+          } else {
+            f[0] = fmaf(((ln_get<DT, W>(v[q], 0) - mh) - ml) * rstd, gm[0], bt[0]);
+          }
+        }
+        ln_store<DT, W, G, NQ, AL>(yr, gt, q, cs, geo.rag, f);
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------- backward ------
+//
+// Per row (mean, rstd as saved by the forward; rstd == 0 marks a masked row):
+// xhat = (x - mean) * rstd, g = dy * gamma (rounded once and used everywhere),
+// S1 = sum g, S2 = sum g * xhat over the group, then
+// dx = rstd * ((g - S1/C) - xhat * S2/C).  The thread's column partials
+// sum dy*xhat and sum dy stay in registers; at the end the groups of a block
+// add theirs in a fixed order into one partial row of the workspace
+// ([gridDim.x][2][cols] floats), which col_reduce_kernel sums.
+template <int DT, int W, int G, int NQ, bool AL, int MAXT>
+__global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
+    ln_bwd_kernel(const LnBwdParams p, const LnGeo geo) {
+  constexpr int E = DType<DT>::E;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int npad = geo.nch * W;
+  const int npl = W >= 4 ? geo.nch * 4 : geo.nch;
+  const LnPlanes<W> sg{reinterpret_cast<float*>(smem), npl};
+  ln_stage<DT, W>(sg, p.gamma, geo.cols, geo.nch);
+  __syncthreads();
+
+  constexpr int ngroups = MAXT / G;
+  const int grp = threadIdx.x / G, gt = threadIdx.x % G;
+  LnCols<G, NQ> cs;
+  cs.init(gt, geo.nfull, geo.rag);
+  LnRed<G> rd{smem + geo.red_off + grp * 1024, 0, 1 + grp};
+  const int64_t step = (int64_t)gridDim.x * ngroups;
+  const int64_t r0 = (int64_t)blockIdx.x * ngroups + grp;
+  const int64_t w0 = (int64_t)blockIdx.x * ngroups + (G < 32 ? (threadIdx.x & ~31) / G : grp);
+  const int64_t rowb = (int64_t)geo.cols * E;
+  const int64_t nbytes = geo.rows * rowb;
+
+  float ag[NQ][W], ab[NQ][W];  // column partials: sum dy*xhat, sum dy
+#pragma unroll
+  for (int q = 0; q < NQ; ++q)
+#pragma unroll
+    for (int e = 0; e < W; ++e) ag[q][e] = ab[q][e] = 0.f;
+
+  for (int64_t it = 0;; ++it) {
+    if (w0 + it * step >= geo.rows) break;
+    const int64_t r = r0 + it * step;
+    const bool active = r < geo.rows;
+    float mean = 0.f, rstd = 0.f;
+    if (active) {
+      mean = __ldg(p.mean + r);
+      rstd = __ldg(p.rstd + r);
+    }
+    const bool use = active && rstd != 0.f;
+    float gv[NQ][W], hv[NQ][W];
+    float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
+    if (use) {
+      uint4 dv[NQ], xv[NQ];
+      ln_load<DT, W, G, NQ, AL>(dv, p.dy + r * rowb, gt, cs, geo.rag, p.dy, p.dy + nbytes);
+      ln_load<DT, W, G, NQ, AL>(xv, p.x + r * rowb, gt, cs, geo.rag, p.x, p.x + nbytes);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (q < cs.nown) {
+          float gm[W];
+          sg.get(gt + q * G, gm);
+          if constexpr (W > 1) {
+#pragma unroll
+            for (int e = 0; e < W; e += 2) {
+              const float y0 = ln_get<DT, W>(dv[q], e), y1 = ln_get<DT, W>(dv[q], e + 1);
+              float h0, h1;
+              add2(h0, h1, ln_get<DT, W>(xv[q], e), ln_get<DT, W>(xv[q], e + 1), -mean, -mean);
+              mul2(h0, h1, h0, h1, rstd, rstd);
+              const float g0 = __fmul_rn(y0, gm[e]), g1 = __fmul_rn(y1, gm[e + 1]);
+              add2(s1a, s1b, s1a, s1b, g0, g1);
+              fma2(s2a, s2b, g0, g1, h0, h1, s2a, s2b);
+              fma2(ag[q][e], ag[q][e + 1], y0, y1, h0, h1, ag[q][e], ag[q][e + 1]);
+              add2(ab[q][e], ab[q][e + 1], ab[q][e], ab[q][e + 1], y0, y1);
+              gv[q][e] = g0;
+              gv[q][e + 1] = g1;
+              hv[q][e] = h0;
+              hv[q][e + 1] = h1;
+            }
+          } else {
+            const float y0 = ln_get<DT, W>(dv[q], 0);
+            const float h0 = (ln_get<DT, W>(xv[q], 0) - mean) * rstd;
+            const float g0 = __fmul_rn(y0, gm[0]);
+            s1a += g0;
+            s2a = fmaf(g0, h0, s2a);
+            ag[q][0] = fmaf(y0, h0, ag[q][0]);
+            ab[q][0] += y0;
+            gv[q][0] = g0;
+            hv[q][0] = h0;
+          }
+        }
+      }
+    }
+    const Sum2 s = rd(Sum2{s1a + s1b, s2a + s2b}, MergeSum2());
+    if (!active) continue;
+    const float a = s.s1 * p.inv_cols;
+    const float b = s.s2 * p.inv_cols;
+    char* dxr = p.dx + r * rowb;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (q < cs.nown) {
+        float f[W];
+        if (!use) {
+#pragma unroll
+          for (int e = 0; e < W; ++e) f[e] = 0.f;
+        } else if constexpr (W > 1) {
+#pragma unroll
+          for (int e = 0; e < W; e += 2) {
+            float t0, t1;
+            add2(t0, t1, gv[q][e], gv[q][e + 1], -a, -a);               // g - a
+            fma2(t0, t1, hv[q][e], hv[q][e + 1], -b, -b, t0, t1);      // (g - a) - xhat b
+            mul2(f[e], f[e + 1], t0, t1, rstd, rstd);
+          }
+        } else {
+          f[0] = rstd * ((gv[q][0] - a) - hv[q][0] * b);
+        }
+        ln_store<DT, W, G, NQ, AL>(dxr, gt, q, cs, geo.rag, f);
+      }
+    }
+  }
+
+  // Column partials: each group's to shared memory, then a fixed-order sum
+  // over the groups into this block's partial row.
+  float* acc = reinterpret_cast<float*>(smem + geo.acc_off) + (size_t)grp * 2 * npad;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    if (q < cs.nown) {
+      const int j = (gt + q * G) * W;
+#pragma unroll
+      for (int e = 0; e < W; ++e) {
+        acc[j + e] = ag[q][e];
+        acc[npad + j + e] = ab[q][e];
+      }
+    }
+  }
+  __syncthreads();
+  const float* all = reinterpret_cast<const float*>(smem + geo.acc_off);
+  float* out = p.ws + (int64_t)blockIdx.x * 2 * geo.cols;
+  for (int i = threadIdx.x; i < 2 * geo.cols; i += MAXT) {
+    const int half = i >= geo.cols ? 1 : 0;
+    const int j = i - half * geo.cols;
+    float t = 0.f;
+    for (int gi = 0; gi < ngroups; ++gi) t += all[(size_t)gi * 2 * npad + half * npad + j];
+    out[i] = t;
+  }
+}
+
+// Fills the variants G = 1 .. 1024 of one mode (block size max(256, G)
+// forward, max(512, G) backward; the backward stops at G = 512, beyond which a
+// 1024-thread block could not give a thread its 128 registers).
+template <int DT, int W, int NQ, bool AL, bool FWD, int G>
+const void* ln_variant() {
+  if constexpr (FWD) {
+    return (const void*)ln_fwd_kernel<DT, W, G, NQ, AL, (G > 256 ? G : 256)>;
+  } else if constexpr (G <= 512) {
+    return (const void*)ln_bwd_kernel<DT, W, G, NQ, AL, 512>;
+  } else {
+    return nullptr;
+  }
+}
+template <int DT, int W, int NQ, bool AL, bool FWD>
+void ln_fill_row(const void* (&row)[kNumLnG]) {
+  row[0] = ln_variant<DT, W, NQ, AL, FWD, 1>();
+  row[1] = ln_variant<DT, W, NQ, AL, FWD, 2>();
+  row[2] = ln_variant<DT, W, NQ, AL, FWD, 4>();
+  row[3] = ln_variant<DT, W, NQ, AL, FWD, 8>();
+  row[4] = ln_variant<DT, W, NQ, AL, FWD, 16>();
+  row[5] = ln_variant<DT, W, NQ, AL, FWD, 32>();
+  row[6] = ln_variant<DT, W, NQ, AL, FWD, 64>();
+  row[7] = ln_variant<DT, W, NQ, AL, FWD, 128>();
+  row[8] = ln_variant<DT, W, NQ, AL, FWD, 256>();
+  row[9] = ln_variant<DT, W, NQ, AL, FWD, 512>();
+  row[10] = ln_variant<DT, W, NQ, AL, FWD, 1024>();
+}
+
+template <int DT, int W, bool AL>
+void ln_fill_row1(const void* (&row)[kNumLnG]) {
+  row[0] = ln_variant<DT, W, 1, AL, false, 1>();
+  row[1] = ln_variant<DT, W, 1, AL, false, 2>();
+  row[2] = ln_variant<DT, W, 1, AL, false, 4>();
+  row[3] = ln_variant<DT, W, 1, AL, false, 8>();
+  row[4] = ln_variant<DT, W, 1, AL, false, 16>();
+  row[5] = ln_variant<DT, W, 1, AL, false, 32>();
+}
+
+template <int DT, bool FWD, int NQC, int NQE>
+LnKernelSet make_ln_set() {
+  constexpr int V = DType<DT>::V;
+  LnKernelSet s{};
+  ln_fill_row<DT, V, NQC, true, FWD>(s.k[0]);
+  ln_fill_row<DT, V, NQC, false, FWD>(s.k[1]);
+  ln_fill_row<DT, 1, NQE, false, FWD>(s.k[2]);
+  if constexpr (!FWD) {
+    ln_fill_row1<DT, V, true>(s.k1[0]);
+    ln_fill_row1<DT, V, false>(s.k1[1]);
+    ln_fill_row1<DT, 1, false>(s.k1[2]);
+  }
+  s.nq[0] = s.nq[1] = NQC;
+  s.nq[2] = NQE;
+  return s;
+}
+
+}  // namespace rr
