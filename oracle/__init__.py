@@ -69,6 +69,18 @@ def _load():
             lib.oracle_ln_bwd.argtypes = [_vp, _vp, _dp, _dp, _vp, ctypes.c_int,
                                           _i64, _i64, _dp, _dp, _dp, _dp, _dp]
             lib.oracle_ln_bwd.restype = None
+            lib.oracle_softmax_bwd.argtypes = [_vp, _vp, ctypes.c_int, _i64, _i64, _dp]
+            lib.oracle_softmax_bwd.restype = None
+            lib.oracle_log_softmax.argtypes = [_vp, ctypes.c_int, _i64, _i64, _dp]
+            lib.oracle_log_softmax.restype = None
+            lib.oracle_log_softmax_bwd.argtypes = [_vp, _vp, ctypes.c_int, _i64, _i64, _dp]
+            lib.oracle_log_softmax_bwd.restype = None
+            lib.oracle_rms_fwd.argtypes = [_vp, _vp, ctypes.c_int, _i64, _i64, ctypes.c_double,
+                                           _dp, _dp]
+            lib.oracle_rms_fwd.restype = None
+            lib.oracle_rms_bwd.argtypes = [_vp, _vp, _dp, _vp, ctypes.c_int, _i64, _i64, _dp,
+                                           _dp, _dp]
+            lib.oracle_rms_bwd.restype = None
             lib.oracle_online_softmax_stats.argtypes = [_dp, _i64, _dp, _dp]
             lib.oracle_online_softmax_stats.restype = None
             lib.oracle_online_merge.argtypes = [ctypes.c_double] * 4 + [_dp, _dp]
@@ -162,6 +174,72 @@ def ln_bwd(dy: np.ndarray, x: np.ndarray, mean: np.ndarray, rstd: np.ndarray,
                           code, rows, cols, _dptr(dx), _dptr(dg), _dptr(db),
                           _dptr(dga), _dptr(dba))
     return dx, dg, db, dga, dba
+
+
+def softmax_bwd(y: np.ndarray, dy: np.ndarray) -> np.ndarray:
+    """Softmax vector-Jacobian product dx = y * (dy - sum(y * dy)) per row."""
+    y, dy = _c(y), _c(dy)
+    code = _dtype_code(y)
+    if _dtype_code(dy) != code:
+        raise TypeError("y and dy must share one storage dtype")
+    rows, cols = y.shape
+    dx = np.empty((rows, cols), np.float64)
+    _load().oracle_softmax_bwd(_ptr(y), _ptr(dy), code, rows, cols, _dptr(dx))
+    return dx
+
+
+def log_softmax(x: np.ndarray) -> np.ndarray:
+    """Log-softmax of each row (x - max - ln sum exp(x - max)); masked rows 0."""
+    x = _c(x)
+    rows, cols = x.shape
+    z = np.empty((rows, cols), np.float64)
+    _load().oracle_log_softmax(_ptr(x), _dtype_code(x), rows, cols, _dptr(z))
+    return z
+
+
+def log_softmax_bwd(z: np.ndarray, dz: np.ndarray) -> np.ndarray:
+    """Log-softmax vector-Jacobian product dx = dz - exp(z) * sum(dz) per row."""
+    z, dz = _c(z), _c(dz)
+    code = _dtype_code(z)
+    if _dtype_code(dz) != code:
+        raise TypeError("z and dz must share one storage dtype")
+    rows, cols = z.shape
+    dx = np.empty((rows, cols), np.float64)
+    _load().oracle_log_softmax_bwd(_ptr(z), _ptr(dz), code, rows, cols, _dptr(dx))
+    return dx
+
+
+def rms_fwd(x: np.ndarray, gamma: np.ndarray, eps: float, want_y: bool = True):
+    """RMSNorm forward.  Returns (y or None, rstd)."""
+    x, gamma = _c(x), _c(gamma)
+    code = _dtype_code(x)
+    if _dtype_code(gamma) != code:
+        raise TypeError("x and gamma must share one storage dtype")
+    rows, cols = x.shape
+    y = np.empty((rows, cols), np.float64) if want_y else None
+    rstd = np.empty(rows, np.float64)
+    _load().oracle_rms_fwd(_ptr(x), _ptr(gamma), code, rows, cols, float(eps), _dptr(y),
+                           _dptr(rstd))
+    return y, rstd
+
+
+def rms_bwd(dy: np.ndarray, x: np.ndarray, rstd: np.ndarray, gamma: np.ndarray,
+            want_dx: bool = True):
+    """RMSNorm backward from the saved rstd (float64).
+
+    Returns (dx or None, dgamma, sum|dy*xhat| per column)."""
+    dy, x, gamma = _c(dy), _c(x), _c(gamma)
+    rstd = _c(np.asarray(rstd, np.float64))
+    code = _dtype_code(x)
+    if _dtype_code(dy) != code or _dtype_code(gamma) != code:
+        raise TypeError("dy, x and gamma must share one storage dtype")
+    rows, cols = x.shape
+    dx = np.empty((rows, cols), np.float64) if want_dx else None
+    dg = np.empty(cols, np.float64)
+    dga = np.empty(cols, np.float64)
+    _load().oracle_rms_bwd(_ptr(dy), _ptr(x), _dptr(rstd), _ptr(gamma), code, rows, cols,
+                           _dptr(dx), _dptr(dg), _dptr(dga))
+    return dx, dg, dga
 
 
 # -- self-check helpers: the recurrences the GPU path uses ----------------------

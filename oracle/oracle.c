@@ -16,6 +16,9 @@
  *        sec. 2.1: loss gradients fused with the normalisation.
  *        sec. 2.2: the analytic (pre-derived) backward.
  *   [P2] "gpu-ml-learning" README, Module 3: softmax and cross-entropy loss.
+ *   [P3] "NexusGrad" README: the Softmax activation layer of the layer stack
+ *        (its backward is the softmax vector-Jacobian product) and RMSNorm
+ *        among the transformer components (no formula given).
  * The two recurrences the pages name but whose equations did not survive are
  * restated from their published sources:
  *   Milakov & Gimelshein (2018), "Online normalizer calculation for softmax";
@@ -34,7 +37,11 @@
  *   - a LayerNorm row whose mean is not finite is masked: y = 0, mean = 0,
  *     rstd = 0; in the backward a row with rstd == 0 is masked: dx = 0 and it
  *     adds nothing to dgamma / dbeta;
- *   - loss is per row (no reduction), dlogits is unscaled.
+ *   - loss is per row (no reduction), dlogits is unscaled;
+ *   - log-softmax of a fully masked row is 0 (as the softmax gives zeros);
+ *   - RMSNorm is y = x / sqrt(mean(x^2) + eps) * gamma (no bias, no mean
+ *     subtraction); a row whose mean square is not finite is masked like a
+ *     LayerNorm row (y = 0, rstd = 0; rstd == 0 masks it in the backward).
  *
  * Storage types: dtype 0 = IEEE float32, dtype 1 = bfloat16 (the upper 16 bits
  * of a float32).  Inputs are widened exactly to double.
@@ -231,6 +238,144 @@ void oracle_ln_bwd(const void *dy, const void *x, const double *mean,
             dbeta[j] += d;
             if (dgamma_abs) dgamma_abs[j] += fabs(d * xh);
             if (dbeta_abs) dbeta_abs[j] += fabs(d);
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Softmax backward (vector-Jacobian product of y = softmax(x), the       */
+/* derivative behind the Softmax activation layer of [P3] "NexusGrad",    */
+/* "Current main layer stack"): dx_j = y_j * (dy_j - sum_k y_k dy_k).      */
+/* y is the forward output as stored; a fully masked row (y = 0) gets 0.  */
+/* ---------------------------------------------------------------------- */
+void oracle_softmax_bwd(const void *y, const void *dy, int dtype, int64_t rows,
+                        int64_t cols, double *dx)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t off = r * cols;
+        double s = 0.0;
+        for (int64_t j = 0; j < cols; ++j)
+            s += load_elem(y, dtype, off + j) * load_elem(dy, dtype, off + j);
+        for (int64_t j = 0; j < cols; ++j)
+            dx[off + j] = load_elem(y, dtype, off + j) * (load_elem(dy, dtype, off + j) - s);
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Log-softmax forward from the same three passes as the softmax [P1 sec. */
+/* 3.1]: m = max_j x_j, d = sum_j exp(x_j - m), z_j = x_j - m - ln d.      */
+/* Reading: a fully masked row (m = -inf) gives z = 0, like the zeros the */
+/* softmax gives there (never NaN).                                       */
+/* ---------------------------------------------------------------------- */
+void oracle_log_softmax(const void *x, int dtype, int64_t rows, int64_t cols,
+                        double *z)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t off = r * cols;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < cols; ++j) {
+            double v = load_elem(x, dtype, off + j);
+            if (v > m) m = v;
+        }
+        if (m == -INFINITY) {
+            for (int64_t j = 0; j < cols; ++j) z[off + j] = 0.0;
+            continue;
+        }
+        double d = 0.0;
+        for (int64_t j = 0; j < cols; ++j) d += exp(load_elem(x, dtype, off + j) - m);
+        double lse = m + log(d);
+        for (int64_t j = 0; j < cols; ++j) z[off + j] = load_elem(x, dtype, off + j) - lse;
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Log-softmax backward (VJP of z = log_softmax(x)):                      */
+/*   dx_j = dz_j - exp(z_j) * sum_k dz_k,  exp(z) being the softmax.      */
+/* The forward output z is taken as stored and the formula is applied to */
+/* every row (a fully masked row, z = 0 from the forward, has no          */
+/* derivative of its own; it gets dx = dz - sum dz like any row of equal  */
+/* logits).                                                               */
+/* ---------------------------------------------------------------------- */
+void oracle_log_softmax_bwd(const void *z, const void *dz, int dtype, int64_t rows,
+                            int64_t cols, double *dx)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t off = r * cols;
+        double s = 0.0;
+        for (int64_t j = 0; j < cols; ++j) s += load_elem(dz, dtype, off + j);
+        for (int64_t j = 0; j < cols; ++j)
+            dx[off + j] = load_elem(dz, dtype, off + j) - exp(load_elem(z, dtype, off + j)) * s;
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* RMSNorm forward ([P3] "NexusGrad", "Core Capabilities" lists RMSNorm   */
+/* without a formula; reading: the standard definition of Zhang &         */
+/* Sennrich (2019)): ms = (1/C) sum_j x_j^2, rstd = 1/sqrt(ms + eps),      */
+/* y_j = x_j * rstd * gamma_j.  A row whose ms is not finite is masked:   */
+/* y = 0, rstd = 0 (the LayerNorm convention).                            */
+/* ---------------------------------------------------------------------- */
+void oracle_rms_fwd(const void *x, const void *gamma, int dtype, int64_t rows,
+                    int64_t cols, double eps, double *y, double *rstd)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t off = r * cols;
+        double ss = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            double v = load_elem(x, dtype, off + j);
+            ss += v * v;
+        }
+        double ms = ss / (double)cols;
+        if (!isfinite(ms)) {
+            rstd[r] = 0.0;
+            if (y)
+                for (int64_t j = 0; j < cols; ++j) y[off + j] = 0.0;
+            continue;
+        }
+        double rs = 1.0 / sqrt(ms + eps);
+        rstd[r] = rs;
+        if (y)
+            for (int64_t j = 0; j < cols; ++j)
+                y[off + j] = load_elem(x, dtype, off + j) * rs * load_elem(gamma, dtype, j);
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* RMSNorm backward, the analytic derivative of the forward above: with   */
+/* xhat = x * rstd and g = dy * gamma,                                    */
+/*   dx = rstd * (g - xhat * mean_j(g * xhat)),  dgamma_j = sum_r dy*xhat. */
+/* rstd == 0 marks a masked row (dx = 0, nothing added to dgamma).        */
+/* dgamma_abs (nullable) receives sum_r |dy * xhat|.                      */
+/* ---------------------------------------------------------------------- */
+void oracle_rms_bwd(const void *dy, const void *x, const double *rstd,
+                    const void *gamma, int dtype, int64_t rows, int64_t cols,
+                    double *dx, double *dgamma, double *dgamma_abs)
+{
+    for (int64_t j = 0; j < cols; ++j) {
+        dgamma[j] = 0.0;
+        if (dgamma_abs) dgamma_abs[j] = 0.0;
+    }
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t off = r * cols;
+        double rs = rstd[r];
+        if (rs == 0.0) {
+            if (dx)
+                for (int64_t j = 0; j < cols; ++j) dx[off + j] = 0.0;
+            continue;
+        }
+        double sgx = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            double xh = load_elem(x, dtype, off + j) * rs;
+            sgx += load_elem(dy, dtype, off + j) * load_elem(gamma, dtype, j) * xh;
+        }
+        double mgx = sgx / (double)cols;
+        for (int64_t j = 0; j < cols; ++j) {
+            double xh = load_elem(x, dtype, off + j) * rs;
+            double d = load_elem(dy, dtype, off + j);
+            double g = d * load_elem(gamma, dtype, j);
+            if (dx) dx[off + j] = rs * (g - xh * mgx);
+            dgamma[j] += d * xh;
+            if (dgamma_abs) dgamma_abs[j] += fabs(d * xh);
         }
     }
 }
