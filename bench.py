@@ -48,6 +48,12 @@ def ln_bytes(rows, cols, e):
     return fwd, bwd
 
 
+def rms_bytes(rows, cols, e):
+    fwd = 2 * rows * cols * e + cols * e + 4 * rows              # x, y, gamma, rstd
+    bwd = 3 * rows * cols * e + 2 * cols * e + 4 * rows          # dy, x, dx, gamma, dg, rstd
+    return fwd, bwd
+
+
 def softmax_bytes(rows, cols, e):
     return 2 * rows * cols * e
 
@@ -545,6 +551,12 @@ def run_sweep(args):
     for name in names:
         d = synth.make(name)
         e = 2 if d["dtype"] == "bf16" else 4
+        # reference: a plain device copy of one [rows x cols] tensor, timed the same way
+        src = d.get("logits", d.get("x"))
+        cs = tdev(src)
+        cd = torch.empty_like(cs)
+        report(name, "copy_ref", 2 * cs.numel() * e, timed(lambda: cd.copy_(cs)))
+        del cs, cd
         if d["kind"] == "xent":
             x, lab = tdev(d["logits"]), tdev(d["labels"])
             R, C = x.shape
@@ -572,6 +584,16 @@ def run_sweep(args):
             report(name, "ln_fwd", fb, mf)
             report(name, "ln_bwd", bb, mb)
             report(name, "ln_fwd+bwd", fb + bb, mf + mb)
+            if rr.rr_rmsnorm_bwd_workspace_size(R, C, x.dtype) > 0:
+                # RMSNorm on the same rows (rows of up to 8192 columns)
+                ws_r = torch.empty(rr.rr_rmsnorm_bwd_workspace_size(R, C, x.dtype),
+                                   dtype=torch.uint8, device=dev)
+                rf, rb = rms_bytes(R, C, e)
+                tf = timed(lambda: rr.rr_rmsnorm_fwd(x, g, y, rstd, eps=d["eps"]))
+                tb = timed(lambda: rr.rr_rmsnorm_bwd(dy, x, rstd, g, dx, dg, ws_r))
+                report(name, "rms_fwd", rf, tf)
+                report(name, "rms_bwd", rb, tb)
+                report(name, "rms_fwd+bwd", rf + rb, tf + tb)
         del d
         torch.cuda.empty_cache()
 

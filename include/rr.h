@@ -135,6 +135,44 @@ rr_status rr_layernorm_bwd(const void *dy, const void *x, const float *mean,
                            rr_dtype dtype, cudaStream_t stream);
 
 /*
+ * RMSNorm forward ("NexusGrad" README, "Core Capabilities", which lists
+ * RMSNorm among its transformer components without a formula; this library
+ * takes the standard definition):
+ *   ms = (1/C) sum_j x_j^2,  rstd = 1 / sqrt(ms + eps),  y_j = x_j * rstd * gamma_j.
+ *   x, y : [rows x cols] dtype (y == x allowed).  gamma : [cols] dtype.
+ *   rstd : [rows] float32 output, saved for rr_rmsnorm_bwd.  eps : >= 0, finite.
+ * A row whose mean square is not finite is masked: y = 0, rstd = 0.  Rows must
+ * fit one row group of threads: up to 16384 columns (32768 for bf16 with a
+ * 16-byte aligned gamma); longer rows return RR_ERR_INVALID_ARG.
+ */
+rr_status rr_rmsnorm_fwd(const void *x, const void *gamma, void *y, float *rstd,
+                         int64_t rows, int64_t cols, float eps, rr_dtype dtype,
+                         cudaStream_t stream);
+
+/* Bytes of device workspace rr_rmsnorm_bwd needs for (rows, cols, dtype); 0 if
+ * the arguments are invalid or the rows are too long.  Depends on the current
+ * device. */
+size_t rr_rmsnorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtype);
+
+/*
+ * RMSNorm backward (analytic derivative of rr_rmsnorm_fwd): with
+ * xhat = x * rstd and g = dy * gamma,
+ *   dx_j = rstd * (g_j - xhat_j * mean_j(g * xhat)),  dgamma_j = sum_r dy_rj * xhat_rj.
+ *   dy, x, dx : [rows x cols] dtype (dx may equal dy).  gamma, dgamma : [cols]
+ *   dtype.  rstd : [rows] float32 from rr_rmsnorm_fwd.
+ *   workspace : device scratch of workspace_bytes >= the size query's answer
+ *   (16-byte aligned), owned by the caller; its contents on entry are ignored.
+ * A row with rstd == 0 gets dx = 0 and adds nothing to dgamma, which is summed
+ * over rows in a fixed order (deterministic for a given device and shape).
+ * Rows must fit one row group: up to 8192 columns; longer rows return
+ * RR_ERR_INVALID_ARG.
+ */
+rr_status rr_rmsnorm_bwd(const void *dy, const void *x, const float *rstd,
+                         const void *gamma, void *dx, void *dgamma, void *workspace,
+                         size_t workspace_bytes, int64_t rows, int64_t cols,
+                         rr_dtype dtype, cudaStream_t stream);
+
+/*
  * LayerNorm backward without a caller-provided workspace (this entry point has
  * no counterpart in the pages; it is a convenience of this library).
  * For callers that cannot allocate device memory at call time -- code under a

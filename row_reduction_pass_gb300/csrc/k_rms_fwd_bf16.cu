@@ -1,0 +1,7 @@
+// Row-group RMSNorm fwd variants for bf16 storage (one translation unit per
+// operation and storage type so they compile in parallel).
+#include "rr_ln.cuh"
+
+namespace rr {
+LnKernelSet rms_fwd_rowgroup_kernels_bf16() { return make_ln_set<kBF16, true, 4, 16, true>(); }
+}  // namespace rr

@@ -82,7 +82,7 @@ rr_status set_smem(DevInfo* di, const void* fn, size_t smem) {
   return RR_OK;
 }
 
-enum OpKind { kSoftmax = 0, kLnFwd = 1, kLnBwd = 2 };
+enum OpKind { kSoftmax = 0, kLnFwd = 1, kLnBwd = 2, kRmsFwd = 3, kRmsBwd = 4 };
 
 const KernelSet& kernels(OpKind op, rr_dtype dt) {
   static KernelSet sets[3][2] = {
@@ -94,11 +94,13 @@ const KernelSet& kernels(OpKind op, rr_dtype dt) {
 }
 
 const rr::LnKernelSet& ln_kernels(OpKind op, rr_dtype dt) {
-  static rr::LnKernelSet sets[2][2] = {
+  static rr::LnKernelSet sets[4][2] = {
       {rr::ln_fwd_rowgroup_kernels_f32(), rr::ln_fwd_rowgroup_kernels_bf16()},
       {rr::ln_bwd_rowgroup_kernels_f32(), rr::ln_bwd_rowgroup_kernels_bf16()},
+      {rr::rms_fwd_rowgroup_kernels_f32(), rr::rms_fwd_rowgroup_kernels_bf16()},
+      {rr::rms_bwd_rowgroup_kernels_f32(), rr::rms_bwd_rowgroup_kernels_bf16()},
   };
-  return sets[op == kLnFwd ? 0 : 1][dt];
+  return sets[op - kLnFwd][dt];
 }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -261,9 +263,9 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
   return RR_OK;
 }
 
-// Row-group LayerNorm plan (rr_ln.cuh): the smallest group G whose threads
-// hold a row, G = 1 .. 1024, with gamma / beta (and the backward's column
-// partials) in shared memory.  lmode: 0 chunks with aligned rows, 1 chunks
+// Row-group LayerNorm / RMSNorm plan (rr_ln.cuh): the smallest group G whose
+// threads hold a row, G = 1 .. 1024, with gamma (/ beta, and the backward's
+// column partials) in shared memory.  lmode: 0 chunks with aligned rows, 1 chunks
 // with any row alignment, 2 elements.  RR_ERR_INVALID_ARG when the row does
 // not fit one group (the caller then plans the staged engine kernels).
 rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64_t cols, Plan* pl,
@@ -296,13 +298,15 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
       break;
     }
   const int G = 1 << gi;
-  const int M1 = op == kLnFwd ? 256 : 512;
+  const bool fwdk = op == kLnFwd || op == kRmsFwd;
+  const int planes = (op == kLnFwd || op == kLnBwd) ? 2 : 1;  // gamma, beta / dgamma, dbeta
+  const int M1 = fwdk ? 256 : 512;
   const int T = G > M1 ? G : M1;
   const int ngroups = T / G;
   const int64_t npad = nch * W;
-  const int64_t red_off = round_up((op == kLnFwd ? 2 : 1) * npad * 4, 16);
+  const int64_t red_off = round_up((fwdk ? planes : 1) * npad * 4, 16);
   const int64_t acc_off = round_up(red_off + (G > 32 ? (int64_t)ngroups * 1024 : 0), 16);
-  const int64_t smem = acc_off + (op == kLnBwd ? (int64_t)ngroups * 2 * npad * 4 : 0);
+  const int64_t smem = acc_off + (fwdk ? 0 : (int64_t)ngroups * planes * npad * 4);
   if (smem > di->smem_optin) return fail(RR_ERR_INVALID_ARG, "row-group shared memory too large");
   if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
   int& occ = di->occ[{fn, ((long long)T << 32) | (long long)smem}];
@@ -370,9 +374,11 @@ rr_status launch(const Plan& pl, const P& params, cudaStream_t stream) {
 
 // ------------------------------------------------------------- checks ----
 
+// Whether [a, a + na) and [b, b + nb) share a byte (an absent, null, tensor
+// overlaps nothing).
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
-  return na && nb && pa < pb + nb && pb < pa + na;
+  return a && b && na && nb && pa < pb + nb && pb < pa + na;
 }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -504,21 +510,60 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
   return ok();
 }
 
-// lmode as for ln_rowgroup_plan; rows too long for one row group go to the
-// staged engine kernels (chunk mode unless lmode == 2).
-static rr_status lnbwd_plan(int64_t rows, int64_t cols, rr_dtype dtype, int lmode, Plan* pl,
-                            size_t* ws_bytes, int64_t max_partials = INT64_MAX) {
-  rr_status st = ln_rowgroup_plan(kLnBwd, dtype, lmode, rows, cols, pl, max_partials);
-  if (st == RR_ERR_INVALID_ARG)
-    st = plan_any(kLnBwd, dtype, lmode != 2, true, rows, cols, pl, max_partials);
+rr_status rr_rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd, int64_t rows,
+                         int64_t cols, float eps, rr_dtype dtype, cudaStream_t stream) {
+  rr_status st = check_shape(rows, cols, dtype);
   if (st != RR_OK) return st;
-  *ws_bytes = (size_t)pl->partials * 2 * (size_t)cols * sizeof(float);
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(RR_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (rows == 0) return ok();
+  if (!x || !gamma || !y || !rstd) return fail(RR_ERR_INVALID_ARG, "null pointer");
+  const size_t E = dtype == RR_BF16 ? 2 : 4;
+  if (!aligned(x, E) || !aligned(y, E) || !aligned(gamma, E) || !aligned(rstd, 4))
+    return fail(RR_ERR_INVALID_ARG, "misaligned pointer");
+  const size_t n = (size_t)rows * cols * E, nc = (size_t)cols * E, nr = (size_t)rows * 4;
+  if (x != y && overlaps(x, n, y, n)) return fail(RR_ERR_ALIASING, "x and y partially overlap");
+  if (overlaps(y, n, gamma, nc) || overlaps(rstd, nr, x, n) || overlaps(rstd, nr, y, n) ||
+      overlaps(rstd, nr, gamma, nc))
+    return fail(RR_ERR_ALIASING, "outputs overlap inputs");
+  const bool al = aligned(gamma, 16);
+  const bool rows_al = (cols * (int64_t)E) % 16 == 0 && aligned(x, 16) && aligned(y, 16);
+  Plan pl;
+  st = ln_rowgroup_plan(kRmsFwd, dtype, al ? (rows_al ? 0 : 1) : 2, rows, cols, &pl, INT64_MAX);
+  if (st == RR_ERR_INVALID_ARG)
+    return fail(RR_ERR_INVALID_ARG, "RMSNorm rows of %lld columns are longer than one row group holds",
+                (long long)cols);
+  if (st != RR_OK) return st;
+  int* err = device_error_word();
+  if (!err) return RR_ERR_CUDA;
+  rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma), nullptr,
+                    static_cast<char*>(y), nullptr, rstd, err, cols, eps,
+                    static_cast<float>(1.0 / static_cast<double>(cols))};
+  if ((st = launch(pl, p, stream)) != RR_OK) return st;
+  return ok();
+}
+
+// Backward plan of LayerNorm (rms = false) or RMSNorm.  lmode as for
+// ln_rowgroup_plan; LayerNorm rows too long for one row group go to the staged
+// engine kernels (chunk mode unless lmode == 2).  ws_bytes: the column
+// partials, [partials][planes][cols] floats.
+static rr_status norm_bwd_plan(bool rms, int64_t rows, int64_t cols, rr_dtype dtype, int lmode,
+                               Plan* pl, size_t* ws_bytes, int64_t max_partials = INT64_MAX) {
+  rr_status st = ln_rowgroup_plan(rms ? kRmsBwd : kLnBwd, dtype, lmode, rows, cols, pl, max_partials);
+  if (st == RR_ERR_INVALID_ARG) {
+    if (rms)
+      return fail(RR_ERR_INVALID_ARG,
+                  "RMSNorm rows of %lld columns are longer than one row group holds",
+                  (long long)cols);
+    st = plan_any(kLnBwd, dtype, lmode != 2, true, rows, cols, pl, max_partials);
+  }
+  if (st != RR_OK) return st;
+  *ws_bytes = (size_t)pl->partials * (rms ? 1 : 2) * (size_t)cols * sizeof(float);
   return RR_OK;
 }
 
-size_t rr_layernorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtype) {
+static size_t norm_bwd_workspace_size(bool rms, int64_t rows, int64_t cols, rr_dtype dtype) {
   if (check_shape(rows, cols, dtype) != RR_OK) return 0;
-  if (rows == 0) return 2 * (size_t)cols * sizeof(float);
+  if (rows == 0) return (rms ? 1 : 2) * (size_t)cols * sizeof(float);
   // The element-mode plan never needs fewer partials than the chunk-mode one
   // for the same shape, but the caller does not know which mode the pointers
   // will select, so report the larger of the two.
@@ -526,27 +571,38 @@ size_t rr_layernorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtyp
   for (int m = 0; m < 3; m += 2) {  // chunk modes 0 and 1 plan alike
     Plan pl;
     size_t ws = 0;
-    if (lnbwd_plan(rows, cols, dtype, m, &pl, &ws) == RR_OK && ws > best) best = ws;
+    if (norm_bwd_plan(rms, rows, cols, dtype, m, &pl, &ws) == RR_OK && ws > best) best = ws;
   }
   return best;
 }
 
+size_t rr_layernorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtype) {
+  return norm_bwd_workspace_size(false, rows, cols, dtype);
+}
+
+size_t rr_rmsnorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtype) {
+  return norm_bwd_workspace_size(true, rows, cols, dtype);
+}
+
 }  // extern "C"
 
-// rr_layernorm_bwd with at most max_partials column partials (the no-allocation
-// entry point sizes this to its fixed scratch).
-rr_status layernorm_bwd_capped(const void* dy, const void* x, const float* mean, const float* rstd,
-                               const void* gamma, void* dx, void* dgamma, void* dbeta,
-                               void* workspace, size_t workspace_bytes, int64_t rows, int64_t cols,
-                               rr_dtype dtype, cudaStream_t stream, int64_t max_partials) {
+// LayerNorm (rms = false) or RMSNorm backward with at most max_partials column
+// partials (the no-allocation entry point sizes this to its fixed scratch).
+// RMSNorm has no mean and no dbeta (both null).
+static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* mean,
+                          const float* rstd, const void* gamma, void* dx, void* dgamma, void* dbeta,
+                          void* workspace, size_t workspace_bytes, int64_t rows, int64_t cols,
+                          rr_dtype dtype, cudaStream_t stream, int64_t max_partials) {
   rr_status st = check_shape(rows, cols, dtype);
   if (st != RR_OK) return st;
-  if (!dy || !x || !mean || !rstd || !gamma || !dx || !dgamma || !dbeta || !workspace)
+  if (!dy || !x || (!rms && !mean) || !rstd || !gamma || !dx || !dgamma || (!rms && !dbeta) ||
+      !workspace)
     return fail(RR_ERR_INVALID_ARG, "null pointer");
   const size_t E = dtype == RR_BF16 ? 2 : 4;
   if (!aligned(dy, E) || !aligned(x, E) || !aligned(dx, E) || !aligned(gamma, E) || !aligned(dgamma, E) ||
       !aligned(dbeta, E) || !aligned(mean, 4) || !aligned(rstd, 4) || !aligned(workspace, 16))
     return fail(RR_ERR_INVALID_ARG, "misaligned pointer (workspace needs 16 bytes)");
+  const int64_t planes = rms ? 1 : 2;
   const size_t n = (size_t)rows * cols * E, nc = (size_t)cols * E, nr = (size_t)rows * 4;
   if (dx != dy && overlaps(dx, n, dy, n)) return fail(RR_ERR_ALIASING, "dx and dy partially overlap");
   if (dx != x && overlaps(dx, n, x, n)) return fail(RR_ERR_ALIASING, "dx and x partially overlap");
@@ -567,7 +623,7 @@ rr_status layernorm_bwd_capped(const void* dy, const void* x, const float* mean,
   size_t need = 0;
   if (rows == 0) {
     // Nothing to read: dgamma = dbeta = 0 through a one-partial workspace.
-    need = 2 * (size_t)cols * sizeof(float);
+    need = planes * (size_t)cols * sizeof(float);
     if (workspace_bytes < need)
       return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
     cudaError_t e = cudaMemsetAsync(workspace, 0, need, stream);
@@ -577,7 +633,8 @@ rr_status layernorm_bwd_capped(const void* dy, const void* x, const float* mean,
     const bool rows_al = (cols * (int64_t)E) % 16 == 0 && aligned(dy, 16) && aligned(x, 16) &&
                          aligned(dx, 16);
     const int lmode = al ? (rows_al ? 0 : 1) : 2;
-    if ((st = lnbwd_plan(rows, cols, dtype, lmode, &pl, &need, max_partials)) != RR_OK) return st;
+    if ((st = norm_bwd_plan(rms, rows, cols, dtype, lmode, &pl, &need, max_partials)) != RR_OK)
+      return st;
     if (workspace_bytes < need)
       return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
     int* err = device_error_word();
@@ -593,10 +650,22 @@ rr_status layernorm_bwd_capped(const void* dy, const void* x, const float* mean,
   int64_t P = pl.partials;
   char* dg = static_cast<char*>(dgamma);
   char* db = static_cast<char*>(dbeta);
-  void* args[] = {&ws, &P, &cols, &dg, &db};
-  cudaError_t e = cudaLaunchKernel(cr, dim3((unsigned)cdiv(2 * cols, 32)), dim3(1024), args, 0, stream);
+  int64_t pl_n = planes;
+  void* args[] = {&ws, &P, &cols, &pl_n, &dg, &db};
+  cudaError_t e =
+      cudaLaunchKernel(cr, dim3((unsigned)cdiv(planes * cols, 32)), dim3(1024), args, 0, stream);
   if (e != cudaSuccess) return fail(RR_ERR_CUDA, "column reduce launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+// rr_layernorm_bwd with at most max_partials column partials (the no-allocation
+// entry point sizes this to its fixed scratch).
+rr_status layernorm_bwd_capped(const void* dy, const void* x, const float* mean, const float* rstd,
+                               const void* gamma, void* dx, void* dgamma, void* dbeta,
+                               void* workspace, size_t workspace_bytes, int64_t rows, int64_t cols,
+                               rr_dtype dtype, cudaStream_t stream, int64_t max_partials) {
+  return norm_bwd(false, dy, x, mean, rstd, gamma, dx, dgamma, dbeta, workspace, workspace_bytes,
+                  rows, cols, dtype, stream, max_partials);
 }
 
 extern "C" {
@@ -605,8 +674,15 @@ rr_status rr_layernorm_bwd(const void* dy, const void* x, const float* mean, con
                            const void* gamma, void* dx, void* dgamma, void* dbeta, void* workspace,
                            size_t workspace_bytes, int64_t rows, int64_t cols, rr_dtype dtype,
                            cudaStream_t stream) {
-  return layernorm_bwd_capped(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, workspace,
-                              workspace_bytes, rows, cols, dtype, stream, INT64_MAX);
+  return norm_bwd(false, dy, x, mean, rstd, gamma, dx, dgamma, dbeta, workspace, workspace_bytes,
+                  rows, cols, dtype, stream, INT64_MAX);
+}
+
+rr_status rr_rmsnorm_bwd(const void* dy, const void* x, const float* rstd, const void* gamma,
+                         void* dx, void* dgamma, void* workspace, size_t workspace_bytes,
+                         int64_t rows, int64_t cols, rr_dtype dtype, cudaStream_t stream) {
+  return norm_bwd(true, dy, x, nullptr, rstd, gamma, dx, dgamma, nullptr, workspace,
+                  workspace_bytes, rows, cols, dtype, stream, INT64_MAX);
 }
 
 rr_status rr_read_device_error(int device, int* value, int reset) {

@@ -38,6 +38,10 @@ LnKernelSet ln_fwd_rowgroup_kernels_f32();
 LnKernelSet ln_fwd_rowgroup_kernels_bf16();
 LnKernelSet ln_bwd_rowgroup_kernels_f32();
 LnKernelSet ln_bwd_rowgroup_kernels_bf16();
+LnKernelSet rms_fwd_rowgroup_kernels_f32();
+LnKernelSet rms_fwd_rowgroup_kernels_bf16();
+LnKernelSet rms_bwd_rowgroup_kernels_f32();
+LnKernelSet rms_bwd_rowgroup_kernels_bf16();
 const void* col_reduce_kernel_ptr_f32();
 const void* col_reduce_kernel_ptr_bf16();
 

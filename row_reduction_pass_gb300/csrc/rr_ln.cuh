@@ -13,6 +13,10 @@
 // sum_r dy) in registers across all the rows a thread processes and writes
 // them out once per block.
 //
+// RMS = true turns both kernels into RMSNorm (y = x * rstd * gamma with
+// rstd = 1/sqrt(mean(x^2) + eps); no mean, no beta): the standard reading of the
+// RMSNorm that the "NexusGrad" README lists among its transformer components.
+//
 // Ragged slots of the last chunk are loaded as 0: they add exactly nothing to
 // the compensated sum, to sum dy*gamma, to sum dy*gamma*xhat (dy = 0 there) or
 // to the column partials, so only the squared deviations and the stores mask
@@ -254,7 +258,7 @@ __device__ __forceinline__ void ln_stage(const LnPlanes<W>& pl, const char* src,
 // group as a double-float -> exact mean mh + ml; squared deviations
 // ((x - mh) - ml)^2 -> M2 -> rstd = 1/sqrt(M2/C + eps); y = xhat*gamma + beta.
 // A row with a non-finite mean or variance is masked: y = 0, mean = rstd = 0.
-template <int DT, int W, int G, int NQ, bool AL, int MAXT>
+template <int DT, int W, int G, int NQ, bool AL, int MAXT, bool RMS>
 __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
     ln_fwd_kernel(const LnFwdParams p, const LnGeo geo) {
   constexpr int E = DType<DT>::E;
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
   const LnPlanes<W> sg{reinterpret_cast<float*>(smem), npl};
   const LnPlanes<W> sb{reinterpret_cast<float*>(smem) + npad, npl};
   ln_stage<DT, W>(sg, p.gamma, geo.cols, geo.nch);
-  ln_stage<DT, W>(sb, p.beta, geo.cols, geo.nch);
+  if constexpr (!RMS) ln_stage<DT, W>(sb, p.beta, geo.cols, geo.nch);
   __syncthreads();
 
   constexpr int ngroups = MAXT / G;
@@ -292,83 +296,109 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
       for (int q = 0; q < NQ; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
     }
 
-    // 1. compensated sum (two interleaved TwoSum accumulators per packed pair)
-    float s0 = 0.f, s1 = 0.f, c0 = 0.f, c1 = 0.f;
+    float mh = 0.f, ml = 0.f, rstd;
+    bool masked;
+    if constexpr (RMS) {
+      // mean square (no cancellation: a plain fp32 sum of squares)
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-      if (q < cs.nown) {
-        if constexpr (W > 1) {
+      for (int q = 0; q < NQ; ++q) {
+        if (q < cs.nown) {
+          if constexpr (W > 1) {
 #pragma unroll
-          for (int e = 0; e < W; e += 2) {
-            const float v0 = ln_get<DT, W>(v[q], e), v1 = ln_get<DT, W>(v[q], e + 1);
-            float t0, t1, b0, b1, u0, u1, w0_, w1_;
-            add2(t0, t1, s0, s1, v0, v1);      // t = s + v
-            add2(b0, b1, t0, t1, -s0, -s1);    // bb = t - s
-            add2(u0, u1, t0, t1, -b0, -b1);    // t - bb
-            add2(u0, u1, s0, s1, -u0, -u1);    // s - (t - bb)
-            add2(w0_, w1_, v0, v1, -b0, -b1);  // v - bb
-            add2(u0, u1, u0, u1, w0_, w1_);    // exact error of s + v
-            add2(c0, c1, c0, c1, u0, u1);
-            s0 = t0;
-            s1 = t1;
-          }
-        } else {
-          float t, err;
-          two_sum(s0, ln_get<DT, W>(v[q], 0), t, err);
-          c0 += err;
-          s0 = t;
-        }
-      }
-    }
-    CascSum S;
-    {
-      float s, e;
-      two_sum(s0, s1, s, e);
-      S = {s, (c0 + c1) + e};
-    }
-    S = rd(S, MergeCasc());
-    float mh, ml;
-    {
-      float sh, sl;
-      two_sum(S.s, S.e, sh, sl);
-      df_mean(sh, sl, ns, p.inv_cols, mh, ml);
-    }
-
-    // 2. squared deviations from the exact mean (ragged slots excluded)
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-      if (q < cs.nown) {
-        if constexpr (W > 1) {
-          const bool whole = q < cs.nf;
-#pragma unroll
-          for (int e = 0; e < W; e += 2) {
-            float d0, d1;
-            add2(d0, d1, ln_get<DT, W>(v[q], e), ln_get<DT, W>(v[q], e + 1), -mh, -mh);
-            add2(d0, d1, d0, d1, -ml, -ml);
-            if (!whole) {
-              if (e >= geo.rag) d0 = 0.f;
-              if (e + 1 >= geo.rag) d1 = 0.f;
+            for (int e = 0; e < W; e += 2) {
+              const float v0 = ln_get<DT, W>(v[q], e), v1 = ln_get<DT, W>(v[q], e + 1);
+              fma2(a0, a1, v0, v1, v0, v1, a0, a1);
             }
-            fma2(a0, a1, d0, d1, d0, d1, a0, a1);
+          } else {
+            const float v0 = ln_get<DT, W>(v[q], 0);
+            a0 = fmaf(v0, v0, a0);
           }
-        } else {
-          const float d = (ln_get<DT, W>(v[q], 0) - mh) - ml;
-          a0 = fmaf(d, d, a0);
         }
       }
-    }
-    const float m2 = rd(Sum1{a0 + a1}, MergeSum1()).s;
-    if (!active) continue;
-    const float var = m2 * p.inv_cols;
-    const bool masked = !(isfinite(mh) && isfinite(ml) && isfinite(var));
-    const float rstd = masked ? 0.f : rsqrtf(var + p.eps);
-    if (gt == 0) {
-      p.mean[r] = masked ? 0.f : mh + ml;
-      p.rstd[r] = rstd;
+      const float ms = rd(Sum1{a0 + a1}, MergeSum1()).s * p.inv_cols;
+      if (!active) continue;
+      masked = !isfinite(ms);
+      rstd = masked ? 0.f : rsqrtf(ms + p.eps);
+      if (gt == 0) p.rstd[r] = rstd;
+    } else {
+      // 1. compensated sum (two interleaved TwoSum accumulators per packed pair)
+      float s0 = 0.f, s1 = 0.f, c0 = 0.f, c1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (q < cs.nown) {
+          if constexpr (W > 1) {
+#pragma unroll
+            for (int e = 0; e < W; e += 2) {
+              const float v0 = ln_get<DT, W>(v[q], e), v1 = ln_get<DT, W>(v[q], e + 1);
+              float t0, t1, b0, b1, u0, u1, w0_, w1_;
+              add2(t0, t1, s0, s1, v0, v1);      // t = s + v
+              add2(b0, b1, t0, t1, -s0, -s1);    // bb = t - s
+              add2(u0, u1, t0, t1, -b0, -b1);    // t - bb
+              add2(u0, u1, s0, s1, -u0, -u1);    // s - (t - bb)
+              add2(w0_, w1_, v0, v1, -b0, -b1);  // v - bb
+              add2(u0, u1, u0, u1, w0_, w1_);    // exact error of s + v
+              add2(c0, c1, c0, c1, u0, u1);
+              s0 = t0;
+              s1 = t1;
+            }
+          } else {
+            float t, err;
+            two_sum(s0, ln_get<DT, W>(v[q], 0), t, err);
+            c0 += err;
+            s0 = t;
+          }
+        }
+      }
+      CascSum S;
+      {
+        float s, e;
+        two_sum(s0, s1, s, e);
+        S = {s, (c0 + c1) + e};
+      }
+      S = rd(S, MergeCasc());
+      {
+        float sh, sl;
+        two_sum(S.s, S.e, sh, sl);
+        df_mean(sh, sl, ns, p.inv_cols, mh, ml);
+      }
+
+      // 2. squared deviations from the exact mean (ragged slots excluded)
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (q < cs.nown) {
+          if constexpr (W > 1) {
+            const bool whole = q < cs.nf;
+#pragma unroll
+            for (int e = 0; e < W; e += 2) {
+              float d0, d1;
+              add2(d0, d1, ln_get<DT, W>(v[q], e), ln_get<DT, W>(v[q], e + 1), -mh, -mh);
+              add2(d0, d1, d0, d1, -ml, -ml);
+              if (!whole) {
+                if (e >= geo.rag) d0 = 0.f;
+                if (e + 1 >= geo.rag) d1 = 0.f;
+              }
+              fma2(a0, a1, d0, d1, d0, d1, a0, a1);
+            }
+          } else {
+            const float d = (ln_get<DT, W>(v[q], 0) - mh) - ml;
+            a0 = fmaf(d, d, a0);
+          }
+        }
+      }
+      const float m2 = rd(Sum1{a0 + a1}, MergeSum1()).s;
+      if (!active) continue;
+      const float var = m2 * p.inv_cols;
+      masked = !(isfinite(mh) && isfinite(ml) && isfinite(var));
+      rstd = masked ? 0.f : rsqrtf(var + p.eps);
+      if (gt == 0) {
+        p.mean[r] = masked ? 0.f : mh + ml;
+        p.rstd[r] = rstd;
+      }
     }
 
-    // 3. y = ((x - mh) - ml) * rstd * gamma + beta
+    // 3. y = ((x - mh) - ml) * rstd * gamma + beta  (RMSNorm: x * rstd * gamma)
     char* yr = p.y + r * rowb;
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
@@ -381,8 +411,19 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
           const int k = gt + q * G;
           float gm[W], bt[W];
           sg.get(k, gm);
-          sb.get(k, bt);
-          if constexpr (W > 1) {
+          if constexpr (!RMS) sb.get(k, bt);
+          if constexpr (RMS) {
+            if constexpr (W > 1) {
+#pragma unroll
+              for (int e = 0; e < W; e += 2) {
+                float t0, t1;
+                mul2(t0, t1, ln_get<DT, W>(v[q], e), ln_get<DT, W>(v[q], e + 1), rstd, rstd);
+                mul2(f[e], f[e + 1], t0, t1, gm[e], gm[e + 1]);
+              }
+            } else {
+              f[0] = (ln_get<DT, W>(v[q], 0) * rstd) * gm[0];
+            }
+          } else if constexpr (W > 1) {
 #pragma unroll
             for (int e = 0; e < W; e += 2) {
               float t0, t1;
@@ -410,7 +451,7 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
 // sum dy*xhat and sum dy stay in registers; at the end the groups of a block
 // add theirs in a fixed order into one partial row of the workspace
 // ([gridDim.x][2][cols] floats), which col_reduce_kernel sums.
-template <int DT, int W, int G, int NQ, bool AL, int MAXT>
+template <int DT, int W, int G, int NQ, bool AL, int MAXT, bool RMS>
 __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
     ln_bwd_kernel(const LnBwdParams p, const LnGeo geo) {
   constexpr int E = DType<DT>::E;
@@ -432,7 +473,7 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
   const int64_t rowb = (int64_t)geo.cols * E;
   const int64_t nbytes = geo.rows * rowb;
 
-  float ag[NQ][W], ab[NQ][W];  // column partials: sum dy*xhat, sum dy
+  float ag[NQ][W], ab[NQ][W];  // column partials: sum dy*xhat, sum dy (LayerNorm only)
 #pragma unroll
   for (int q = 0; q < NQ; ++q)
 #pragma unroll
@@ -444,7 +485,7 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
     const bool active = r < geo.rows;
     float mean = 0.f, rstd = 0.f;
     if (active) {
-      mean = __ldg(p.mean + r);
+      if constexpr (!RMS) mean = __ldg(p.mean + r);
       rstd = __ldg(p.rstd + r);
     }
     const bool use = active && rstd != 0.f;
@@ -464,13 +505,17 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
             for (int e = 0; e < W; e += 2) {
               const float y0 = ln_get<DT, W>(dv[q], e), y1 = ln_get<DT, W>(dv[q], e + 1);
               float h0, h1;
-              add2(h0, h1, ln_get<DT, W>(xv[q], e), ln_get<DT, W>(xv[q], e + 1), -mean, -mean);
-              mul2(h0, h1, h0, h1, rstd, rstd);
+              if constexpr (RMS) {
+                mul2(h0, h1, ln_get<DT, W>(xv[q], e), ln_get<DT, W>(xv[q], e + 1), rstd, rstd);
+              } else {
+                add2(h0, h1, ln_get<DT, W>(xv[q], e), ln_get<DT, W>(xv[q], e + 1), -mean, -mean);
+                mul2(h0, h1, h0, h1, rstd, rstd);
+              }
               const float g0 = __fmul_rn(y0, gm[e]), g1 = __fmul_rn(y1, gm[e + 1]);
-              add2(s1a, s1b, s1a, s1b, g0, g1);
+              if constexpr (!RMS) add2(s1a, s1b, s1a, s1b, g0, g1);
               fma2(s2a, s2b, g0, g1, h0, h1, s2a, s2b);
               fma2(ag[q][e], ag[q][e + 1], y0, y1, h0, h1, ag[q][e], ag[q][e + 1]);
-              add2(ab[q][e], ab[q][e + 1], ab[q][e], ab[q][e + 1], y0, y1);
+              if constexpr (!RMS) add2(ab[q][e], ab[q][e + 1], ab[q][e], ab[q][e + 1], y0, y1);
               gv[q][e] = g0;
               gv[q][e + 1] = g1;
               hv[q][e] = h0;
@@ -478,12 +523,13 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
             }
           } else {
             const float y0 = ln_get<DT, W>(dv[q], 0);
-            const float h0 = (ln_get<DT, W>(xv[q], 0) - mean) * rstd;
+            const float h0 = RMS ? ln_get<DT, W>(xv[q], 0) * rstd
+                                 : (ln_get<DT, W>(xv[q], 0) - mean) * rstd;
             const float g0 = __fmul_rn(y0, gm[0]);
-            s1a += g0;
+            if constexpr (!RMS) s1a += g0;
             s2a = fmaf(g0, h0, s2a);
             ag[q][0] = fmaf(y0, h0, ag[q][0]);
-            ab[q][0] += y0;
+            if constexpr (!RMS) ab[q][0] += y0;
             gv[q][0] = g0;
             hv[q][0] = h0;
           }
@@ -520,7 +566,8 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
 
   // Column partials: each group's to shared memory, then a fixed-order sum
   // over the groups into this block's partial row.
-  float* acc = reinterpret_cast<float*>(smem + geo.acc_off) + (size_t)grp * 2 * npad;
+  constexpr int kPlanes = RMS ? 1 : 2;  // dgamma (, dbeta)
+  float* acc = reinterpret_cast<float*>(smem + geo.acc_off) + (size_t)grp * kPlanes * npad;
 #pragma unroll
   for (int q = 0; q < NQ; ++q) {
     if (q < cs.nown) {
@@ -528,18 +575,18 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
 #pragma unroll
       for (int e = 0; e < W; ++e) {
         acc[j + e] = ag[q][e];
-        acc[npad + j + e] = ab[q][e];
+        if constexpr (!RMS) acc[npad + j + e] = ab[q][e];
       }
     }
   }
   __syncthreads();
   const float* all = reinterpret_cast<const float*>(smem + geo.acc_off);
-  float* out = p.ws + (int64_t)blockIdx.x * 2 * geo.cols;
-  for (int i = threadIdx.x; i < 2 * geo.cols; i += MAXT) {
+  float* out = p.ws + (int64_t)blockIdx.x * kPlanes * geo.cols;
+  for (int i = threadIdx.x; i < kPlanes * geo.cols; i += MAXT) {
     const int half = i >= geo.cols ? 1 : 0;
     const int j = i - half * geo.cols;
     float t = 0.f;
-    for (int gi = 0; gi < ngroups; ++gi) t += all[(size_t)gi * 2 * npad + half * npad + j];
+    for (int gi = 0; gi < ngroups; ++gi) t += all[(size_t)gi * kPlanes * npad + half * npad + j];
     out[i] = t;
   }
 }
@@ -547,52 +594,52 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
 // Fills the variants G = 1 .. 1024 of one mode (block size max(256, G)
 // forward, max(512, G) backward; the backward stops at G = 512, beyond which a
 // 1024-thread block could not give a thread its 128 registers).
-template <int DT, int W, int NQ, bool AL, bool FWD, int G>
+template <int DT, int W, int NQ, bool AL, bool FWD, int G, bool RMS>
 const void* ln_variant() {
   if constexpr (FWD) {
-    return (const void*)ln_fwd_kernel<DT, W, G, NQ, AL, (G > 256 ? G : 256)>;
+    return (const void*)ln_fwd_kernel<DT, W, G, NQ, AL, (G > 256 ? G : 256), RMS>;
   } else if constexpr (G <= 512) {
-    return (const void*)ln_bwd_kernel<DT, W, G, NQ, AL, 512>;
+    return (const void*)ln_bwd_kernel<DT, W, G, NQ, AL, 512, RMS>;
   } else {
     return nullptr;
   }
 }
-template <int DT, int W, int NQ, bool AL, bool FWD>
+template <int DT, int W, int NQ, bool AL, bool FWD, bool RMS>
 void ln_fill_row(const void* (&row)[kNumLnG]) {
-  row[0] = ln_variant<DT, W, NQ, AL, FWD, 1>();
-  row[1] = ln_variant<DT, W, NQ, AL, FWD, 2>();
-  row[2] = ln_variant<DT, W, NQ, AL, FWD, 4>();
-  row[3] = ln_variant<DT, W, NQ, AL, FWD, 8>();
-  row[4] = ln_variant<DT, W, NQ, AL, FWD, 16>();
-  row[5] = ln_variant<DT, W, NQ, AL, FWD, 32>();
-  row[6] = ln_variant<DT, W, NQ, AL, FWD, 64>();
-  row[7] = ln_variant<DT, W, NQ, AL, FWD, 128>();
-  row[8] = ln_variant<DT, W, NQ, AL, FWD, 256>();
-  row[9] = ln_variant<DT, W, NQ, AL, FWD, 512>();
-  row[10] = ln_variant<DT, W, NQ, AL, FWD, 1024>();
+  row[0] = ln_variant<DT, W, NQ, AL, FWD, 1, RMS>();
+  row[1] = ln_variant<DT, W, NQ, AL, FWD, 2, RMS>();
+  row[2] = ln_variant<DT, W, NQ, AL, FWD, 4, RMS>();
+  row[3] = ln_variant<DT, W, NQ, AL, FWD, 8, RMS>();
+  row[4] = ln_variant<DT, W, NQ, AL, FWD, 16, RMS>();
+  row[5] = ln_variant<DT, W, NQ, AL, FWD, 32, RMS>();
+  row[6] = ln_variant<DT, W, NQ, AL, FWD, 64, RMS>();
+  row[7] = ln_variant<DT, W, NQ, AL, FWD, 128, RMS>();
+  row[8] = ln_variant<DT, W, NQ, AL, FWD, 256, RMS>();
+  row[9] = ln_variant<DT, W, NQ, AL, FWD, 512, RMS>();
+  row[10] = ln_variant<DT, W, NQ, AL, FWD, 1024, RMS>();
 }
 
-template <int DT, int W, bool AL>
+template <int DT, int W, bool AL, bool RMS>
 void ln_fill_row1(const void* (&row)[kNumLnG]) {
-  row[0] = ln_variant<DT, W, 1, AL, false, 1>();
-  row[1] = ln_variant<DT, W, 1, AL, false, 2>();
-  row[2] = ln_variant<DT, W, 1, AL, false, 4>();
-  row[3] = ln_variant<DT, W, 1, AL, false, 8>();
-  row[4] = ln_variant<DT, W, 1, AL, false, 16>();
-  row[5] = ln_variant<DT, W, 1, AL, false, 32>();
+  row[0] = ln_variant<DT, W, 1, AL, false, 1, RMS>();
+  row[1] = ln_variant<DT, W, 1, AL, false, 2, RMS>();
+  row[2] = ln_variant<DT, W, 1, AL, false, 4, RMS>();
+  row[3] = ln_variant<DT, W, 1, AL, false, 8, RMS>();
+  row[4] = ln_variant<DT, W, 1, AL, false, 16, RMS>();
+  row[5] = ln_variant<DT, W, 1, AL, false, 32, RMS>();
 }
 
-template <int DT, bool FWD, int NQC, int NQE>
+template <int DT, bool FWD, int NQC, int NQE, bool RMS = false>
 LnKernelSet make_ln_set() {
   constexpr int V = DType<DT>::V;
   LnKernelSet s{};
-  ln_fill_row<DT, V, NQC, true, FWD>(s.k[0]);
-  ln_fill_row<DT, V, NQC, false, FWD>(s.k[1]);
-  ln_fill_row<DT, 1, NQE, false, FWD>(s.k[2]);
+  ln_fill_row<DT, V, NQC, true, FWD, RMS>(s.k[0]);
+  ln_fill_row<DT, V, NQC, false, FWD, RMS>(s.k[1]);
+  ln_fill_row<DT, 1, NQE, false, FWD, RMS>(s.k[2]);
   if constexpr (!FWD) {
-    ln_fill_row1<DT, V, true>(s.k1[0]);
-    ln_fill_row1<DT, V, false>(s.k1[1]);
-    ln_fill_row1<DT, 1, false>(s.k1[2]);
+    ln_fill_row1<DT, V, true, RMS>(s.k1[0]);
+    ln_fill_row1<DT, V, false, RMS>(s.k1[1]);
+    ln_fill_row1<DT, 1, false, RMS>(s.k1[2]);
   }
   s.nq[0] = s.nq[1] = NQC;
   s.nq[2] = NQE;

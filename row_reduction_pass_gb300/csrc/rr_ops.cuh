@@ -781,17 +781,19 @@ struct OpLnBwd {
   }
 };
 
-// Second stage of the LayerNorm backward: dgamma_j / dbeta_j = sum over the P
-// partial rows, in a fixed order (warp w takes partials w, w+32, ...; the 32
+// Second stage of the LayerNorm / RMSNorm backward: dgamma_j (and dbeta_j) =
+// sum over the P partial rows ([P][planes][cols], planes = 2 for LayerNorm, 1
+// for RMSNorm), in a fixed order (warp w takes partials w, w+32, ...; the 32
 // warp sums are then added in warp order), so the result is deterministic.
 template <int DT>
 __global__ void __launch_bounds__(1024) col_reduce_kernel(const float* __restrict__ ws, int64_t P,
-                                                          int64_t cols, char* dgamma, char* dbeta) {
+                                                          int64_t cols, int64_t planes,
+                                                          char* dgamma, char* dbeta) {
   constexpr int E = DType<DT>::E;
   __shared__ float part[32][33];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t k = (int64_t)blockIdx.x * 32 + lane;
-  const int64_t n2 = 2 * cols;
+  const int64_t n2 = planes * cols;
   float s = 0.f;
   if (k < n2) {
     int64_t pp = w;

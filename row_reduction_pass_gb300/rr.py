@@ -64,6 +64,13 @@ def load_library():
         lib.rr_layernorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
                                          i64, i64, st, vp]
         lib.rr_layernorm_bwd.restype = st
+        lib.rr_rmsnorm_fwd.argtypes = [vp, vp, vp, vp, i64, i64, ctypes.c_float, st, vp]
+        lib.rr_rmsnorm_fwd.restype = st
+        lib.rr_rmsnorm_bwd_workspace_size.argtypes = [i64, i64, st]
+        lib.rr_rmsnorm_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.rr_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i64, i64, st,
+                                       vp]
+        lib.rr_rmsnorm_bwd.restype = st
         lib.rr_layernorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, st, vp]
         lib.rr_layernorm_bwd_noalloc.restype = st
         lib.rr_last_error_detail.argtypes = []
@@ -169,6 +176,37 @@ def rr_layernorm_bwd_noalloc(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, stream
     _check("rr_layernorm_bwd_noalloc", load_library().rr_layernorm_bwd_noalloc(
         _p(dy), _p(x), _p(mean), _p(rstd), _p(gamma), _p(dx), _p(dgamma), _p(dbeta), rows, cols,
         _dtype(x), _stream(stream)))
+
+
+def rr_rmsnorm_fwd(x, gamma, y, rstd, eps=1e-5, stream=None):
+    """y = x * rstd * gamma with rstd = 1/sqrt(mean(x^2) + eps) (fp32, saved)."""
+    _contig(x, gamma, y, rstd)
+    rows, cols = x.shape
+    _check("rr_rmsnorm_fwd", load_library().rr_rmsnorm_fwd(
+        _p(x), _p(gamma), _p(y), _p(rstd), rows, cols, ctypes.c_float(eps), _dtype(x),
+        _stream(stream)))
+
+
+def rr_rmsnorm_bwd_workspace_size(rows: int, cols: int, dtype) -> int:
+    import torch
+    code = {torch.float32: RR_F32, torch.bfloat16: RR_BF16}.get(dtype, dtype)
+    return int(load_library().rr_rmsnorm_bwd_workspace_size(rows, cols, int(code)))
+
+
+def rr_rmsnorm_bwd(dy, x, rstd, gamma, dx, dgamma, workspace=None, stream=None):
+    """dx and dgamma of RMSNorm from the saved rstd.
+
+    ``workspace`` is a uint8 CUDA tensor of at least
+    ``rr_rmsnorm_bwd_workspace_size`` bytes; it is allocated here if omitted."""
+    import torch
+    _contig(dy, x, rstd, gamma, dx, dgamma)
+    rows, cols = x.shape
+    need = rr_rmsnorm_bwd_workspace_size(rows, cols, x.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    _check("rr_rmsnorm_bwd", load_library().rr_rmsnorm_bwd(
+        _p(dy), _p(x), _p(rstd), _p(gamma), _p(dx), _p(dgamma), _p(workspace),
+        workspace.numel() * workspace.element_size(), rows, cols, _dtype(x), _stream(stream)))
 
 
 def rr_read_device_error(device: int = 0, reset: bool = True) -> int:

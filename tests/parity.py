@@ -164,3 +164,35 @@ def check_ln(x, gamma, beta, dy, eps, dtype, pad=(0, 0, 0, 0, 0), oracle_stats=T
     compare("ln dgamma", g["dgamma"], rdg, rtol, atol, scale=sdg)
     compare("ln dbeta", g["dbeta"], rdb, rtol, atol, scale=sdb)
     return g
+
+
+def run_rms(x, gamma, dy, eps, dtype, pad=(0, 0, 0, 0, 0), oracle_stats=True):
+    """RMSNorm fwd then bwd on the GPU; pad as for run_ln (the beta slot unused).
+    The backward gets the oracle's rstd rounded to float32 when oracle_stats."""
+    xd = to_dev(x, pad[0])
+    gd = to_dev(gamma, pad[2])
+    y = empty_like_dev(x.shape, dtype, pad[1])
+    rows = x.shape[0]
+    rstd = torch.full((rows,), float("nan"), device=dev())
+    rr.rr_rmsnorm_fwd(xd, gd, y, rstd, eps=eps)
+    _, rrstd = oracle.rms_fwd(x, gamma, eps, want_y=False)
+    r_in = torch.from_numpy(rrstd.astype(np.float32)).to(dev()) if oracle_stats else rstd
+    dyd = to_dev(dy, pad[3])
+    dx = empty_like_dev(x.shape, dtype, pad[4])
+    dg = empty_like_dev(gamma.shape, dtype)
+    rr.rr_rmsnorm_bwd(dyd, xd, r_in, gd, dx, dg)
+    torch.cuda.synchronize()
+    return dict(y=host(y), rstd=host(rstd), dx=host(dx), dgamma=host(dg),
+                rstd_in=r_in.cpu().numpy().astype(np.float64))
+
+
+def check_rms(x, gamma, dy, eps, dtype, pad=(0, 0, 0, 0, 0), oracle_stats=True):
+    g = run_rms(x, gamma, dy, eps, dtype, pad, oracle_stats)
+    ry, rrstd = oracle.rms_fwd(x, gamma, eps)
+    rtol, atol = TOL[dtype]
+    compare("rms y", g["y"], ry, rtol, atol)
+    compare("rms rstd", g["rstd"], rrstd, *TOL_F32_OUT)
+    rdx, rdg, sdg = oracle.rms_bwd(dy, x, g["rstd_in"] if oracle_stats else rrstd, gamma)
+    compare("rms dx", g["dx"], rdx, rtol, atol)
+    compare("rms dgamma", g["dgamma"], rdg, rtol, atol, scale=sdg)
+    return g

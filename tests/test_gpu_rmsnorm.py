@@ -1,0 +1,63 @@
+"""GPU parity of RMSNorm forward / backward (rr_rmsnorm_fwd, rr_rmsnorm_bwd)
+against the float64 oracle, through the C ABI: row lengths across the
+row-group sizes and their boundaries, ragged last chunks, misaligned tensors,
+masked rows and +-1e4 outliers, a chained GPU-forward-into-backward check, and
+the rejection of rows longer than one row group holds."""
+import numpy as np
+import pytest
+import torch
+
+import row_reduction_pass_gb300 as rr
+from row_reduction_pass_gb300 import synth
+
+from parity import check_rms
+
+pytestmark = pytest.mark.gpu
+
+RMS_COLS = [1, 2, 3, 8, 31, 32, 97, 128, 768, 1000, 1024, 2049, 4096, 4097, 6144, 8192]
+
+
+def rows_for(cols: int) -> int:
+    return 320 if cols >= 4096 else int(max(3, min(3000, (1 << 21) // cols)))
+
+
+def case(rows, cols, dtype, seed):
+    x, g, _, dy = synth.ln_inputs(rows, cols, dtype, seed, row_offset=2.0, gamma_std=0.1,
+                                  outlier_frac=0.005, masked_row_every=41)
+    return x, g, dy
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", RMS_COLS)
+def test_rmsnorm(cols, dtype):
+    x, g, dy = case(rows_for(cols), cols, dtype, 900 + cols)
+    check_rms(x, g, dy, 1e-5, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", [1, 31, 768, 1000, 4097])
+@pytest.mark.parametrize("pad", [(1, 1, 1, 1, 1), (0, 0, 1, 0, 0), (0, 1, 0, 0, 1)])
+def test_rmsnorm_misaligned(cols, dtype, pad):
+    x, g, dy = case(rows_for(cols) // 2 + 1, cols, dtype, 950 + cols)
+    check_rms(x, g, dy, 1e-5, dtype, pad=pad)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rmsnorm_chained_gpu_statistics(dtype):
+    x, g, _, dy = synth.ln_inputs(512, 1000, dtype, 77, row_offset=1.0)
+    check_rms(x, g, dy, 1e-5, dtype, oracle_stats=False)
+
+
+def test_rmsnorm_rejects_rows_beyond_one_group():
+    dev = torch.device("cuda", 0)
+    x = torch.zeros(4, 16385, device=dev)
+    g = torch.ones(16385, device=dev)
+    with pytest.raises(rr.RRError):
+        rr.rr_rmsnorm_fwd(x, g, torch.empty_like(x), torch.empty(4, device=dev))
+    x = torch.zeros(4, 8193, device=dev)
+    g = torch.ones(8193, device=dev)
+    assert rr.rr_rmsnorm_bwd_workspace_size(4, 8193, torch.float32) == 0
+    with pytest.raises(rr.RRError):
+        rr.rr_rmsnorm_bwd(x, x, torch.ones(4, device=dev), g, torch.empty_like(x),
+                          torch.empty_like(g), workspace=torch.empty(1 << 20, dtype=torch.uint8,
+                                                                      device=dev))
