@@ -565,6 +565,15 @@ def run_sweep(args):
             n_ign = int((d["labels"] == synth.IGNORE_INDEX).sum())
             ms = timed(lambda: rr.rr_softmax_xent_fwd_bwd(x, lab, loss, y))
             report(name, "xent", xent_bytes(R, C, e, n_ign), ms)
+            # the softmax family on the same logits: log-softmax forward, and the
+            # softmax / log-softmax backward with a second, distinct input (dy)
+            report(name, "log_softmax", softmax_bytes(R, C, e),
+                   timed(lambda: rr.rr_log_softmax_fwd(x, y)))
+            dyt = x.clone()
+            report(name, "softmax_bwd", 3 * R * C * e, timed(lambda: rr.rr_softmax_bwd(x, dyt, y)))
+            report(name, "log_softmax_bwd", 3 * R * C * e,
+                   timed(lambda: rr.rr_log_softmax_bwd(x, dyt, y)))
+            del dyt
         elif d["kind"] == "causal":
             x = tdev(d["x"])
             y = torch.empty_like(x)

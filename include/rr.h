@@ -75,6 +75,37 @@ rr_status rr_softmax_fwd(const void *x, void *y, int64_t rows, int64_t cols,
                          rr_dtype dtype, cudaStream_t stream);
 
 /*
+ * Log-softmax forward of each row: z_j = (x_j - m) - ln d with m = max_j x_j
+ * and d = sum_j exp(x_j - m), from the same one-pass online normaliser as
+ * rr_softmax_fwd (sec. 3.1).  x, z : [rows x cols] dtype (z == x allowed).
+ * A fully masked row (maximum -inf) gives z = 0; a -inf entry of a live row
+ * gives -inf.
+ */
+rr_status rr_log_softmax_fwd(const void *x, void *z, int64_t rows, int64_t cols,
+                             rr_dtype dtype, cudaStream_t stream);
+
+/*
+ * Softmax backward, the vector-Jacobian product of y = softmax(x) (the
+ * Softmax layer of the "NexusGrad" README's layer stack):
+ *   dx_j = y_j * (dy_j - sum_k y_k dy_k).
+ *   y : the forward's output, dy : upstream gradient, dx : [rows x cols] dtype.
+ * dx may equal y or dy exactly (partial overlap is RR_ERR_ALIASING).  A fully
+ * masked row (y = 0) gets dx = 0.
+ */
+rr_status rr_softmax_bwd(const void *y, const void *dy, void *dx, int64_t rows,
+                         int64_t cols, rr_dtype dtype, cudaStream_t stream);
+
+/*
+ * Log-softmax backward, the vector-Jacobian product of z = log_softmax(x):
+ *   dx_j = dz_j - exp(z_j) * sum_k dz_k.
+ *   z : the forward's output, dz : upstream gradient, dx : [rows x cols] dtype.
+ * dx may equal z or dz exactly.  The formula is applied to every row (a row
+ * the forward masked to z = 0 has no derivative of its own).
+ */
+rr_status rr_log_softmax_bwd(const void *z, const void *dz, void *dx, int64_t rows,
+                             int64_t cols, rr_dtype dtype, cudaStream_t stream);
+
+/*
  * Fused softmax cross-entropy, forward and backward in one pass (sec. 2.1
  * and sec. 3.1; cross-entropy as in Module 3 of "gpu-ml-learning"):
  *   loss_r      = m + log d - logits[r, label_r]           (float32, [rows])

@@ -1,4 +1,5 @@
-"""GB300-native fused row reductions: online softmax, fused softmax cross-entropy
+"""GB300-native fused row reductions: online softmax and log-softmax (forward and
+backward), fused softmax cross-entropy
 (loss and dlogits in one pass), Welford LayerNorm forward / backward and
 RMSNorm forward / backward.
 
@@ -7,6 +8,7 @@ sm_103a; :mod:`row_reduction_pass_gb300.rr` binds its entry points by name.
 """
 from .rr import (RRError, rr_layernorm_bwd, rr_layernorm_bwd_noalloc,  # noqa: F401
                  rr_layernorm_bwd_workspace_size,
-                 rr_layernorm_fwd, rr_rmsnorm_bwd, rr_rmsnorm_bwd_workspace_size,
-                 rr_rmsnorm_fwd, rr_softmax_fwd, rr_softmax_xent_fwd_bwd,
+                 rr_layernorm_fwd, rr_log_softmax_bwd, rr_log_softmax_fwd,
+                 rr_rmsnorm_bwd, rr_rmsnorm_bwd_workspace_size,
+                 rr_rmsnorm_fwd, rr_softmax_bwd, rr_softmax_fwd, rr_softmax_xent_fwd_bwd,
                  rr_status_string, library_path, load_library)

@@ -82,15 +82,17 @@ rr_status set_smem(DevInfo* di, const void* fn, size_t smem) {
   return RR_OK;
 }
 
-enum OpKind { kSoftmax = 0, kLnFwd = 1, kLnBwd = 2, kRmsFwd = 3, kRmsBwd = 4 };
+enum OpKind { kSoftmax = 0, kLnFwd = 1, kLnBwd = 2, kRmsFwd = 3, kRmsBwd = 4, kSoftmaxBwd = 5 };
 
+// Row-engine kernel sets (the RMSNorm kinds have none: row-group kernels only).
 const KernelSet& kernels(OpKind op, rr_dtype dt) {
-  static KernelSet sets[3][2] = {
+  static KernelSet sets[4][2] = {
       {rr::softmax_kernels_f32(), rr::softmax_kernels_bf16()},
       {rr::lnfwd_kernels_f32(), rr::lnfwd_kernels_bf16()},
       {rr::lnbwd_kernels_f32(), rr::lnbwd_kernels_bf16()},
+      {rr::softmax_bwd_kernels_f32(), rr::softmax_bwd_kernels_bf16()},
   };
-  return sets[op][dt];
+  return sets[op == kSoftmaxBwd ? 3 : op][dt];
 }
 
 const rr::LnKernelSet& ln_kernels(OpKind op, rr_dtype dt) {
@@ -133,7 +135,7 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
   const KernelSet& ks = kernels(op, dt);
   const int E = dt == RR_BF16 ? 2 : 4;
   const int V = 16 / E;
-  const int NT = op == kLnBwd ? 2 : 1;
+  const int NT = (op == kLnBwd || op == kSoftmaxBwd) ? 2 : 1;
   pl->mode = mode;
   pl->geo.rows = rows;
   pl->geo.cols = cols;
@@ -420,8 +422,8 @@ const char* rr_status_string(rr_status s) {
 
 const char* rr_last_error_detail(void) { return g_detail.c_str(); }
 
-rr_status rr_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, rr_dtype dtype,
-                         cudaStream_t stream) {
+static rr_status softmax_fwd_impl(const void* x, void* y, int64_t rows, int64_t cols,
+                                  rr_dtype dtype, cudaStream_t stream, int32_t log) {
   rr_status st = check_shape(rows, cols, dtype);
   if (st != RR_OK) return st;
   if (rows == 0) return ok();
@@ -437,9 +439,59 @@ rr_status rr_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, rr_
   int* err = device_error_word();
   if (!err) return RR_ERR_CUDA;
   rr::SoftmaxParams p{static_cast<const char*>(x), static_cast<char*>(y), nullptr, nullptr, nullptr,
-                      err, cols, 0};
+                      err, cols, 0, log};
   if ((st = launch(pl, p, stream)) != RR_OK) return st;
   return ok();
+}
+
+rr_status rr_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, rr_dtype dtype,
+                         cudaStream_t stream) {
+  return softmax_fwd_impl(x, y, rows, cols, dtype, stream, 0);
+}
+
+rr_status rr_log_softmax_fwd(const void* x, void* z, int64_t rows, int64_t cols, rr_dtype dtype,
+                             cudaStream_t stream) {
+  return softmax_fwd_impl(x, z, rows, cols, dtype, stream, 1);
+}
+
+// Softmax (log = 0: y, dy) or log-softmax (log = 1: z, dz) backward.  dx may be
+// either input exactly (each row is read whole before it is written).
+static rr_status softmax_bwd_impl(const void* y, const void* dy, void* dx, int64_t rows,
+                                  int64_t cols, rr_dtype dtype, cudaStream_t stream, int32_t log) {
+  rr_status st = check_shape(rows, cols, dtype);
+  if (st != RR_OK) return st;
+  if (rows == 0) return ok();
+  if (!y || !dy || !dx) return fail(RR_ERR_INVALID_ARG, "null pointer");
+  const size_t E = dtype == RR_BF16 ? 2 : 4;
+  if (!aligned(y, E) || !aligned(dy, E) || !aligned(dx, E))
+    return fail(RR_ERR_INVALID_ARG, "misaligned element pointer");
+  const size_t n = (size_t)rows * cols * E;
+  if ((dx != y && overlaps(dx, n, y, n)) || (dx != dy && overlaps(dx, n, dy, n)))
+    return fail(RR_ERR_ALIASING, "dx partially overlaps an input");
+  // memory-aligned chunks hold the same columns of all three tensors only when
+  // they share their alignment; otherwise element mode
+  const uintptr_t a = reinterpret_cast<uintptr_t>(y) & 15;
+  const bool same = a == (reinterpret_cast<uintptr_t>(dy) & 15) &&
+                    a == (reinterpret_cast<uintptr_t>(dx) & 15);
+  const bool head_free = same && a == 0 && (cols * E) % 16 == 0;
+  Plan pl;
+  if ((st = plan_any(kSoftmaxBwd, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
+  int* err = device_error_word();
+  if (!err) return RR_ERR_CUDA;
+  rr::SoftmaxBwdParams p{static_cast<const char*>(y), static_cast<const char*>(dy),
+                         static_cast<char*>(dx), err, cols, log};
+  if ((st = launch(pl, p, stream)) != RR_OK) return st;
+  return ok();
+}
+
+rr_status rr_softmax_bwd(const void* y, const void* dy, void* dx, int64_t rows, int64_t cols,
+                         rr_dtype dtype, cudaStream_t stream) {
+  return softmax_bwd_impl(y, dy, dx, rows, cols, dtype, stream, 0);
+}
+
+rr_status rr_log_softmax_bwd(const void* z, const void* dz, void* dx, int64_t rows, int64_t cols,
+                             rr_dtype dtype, cudaStream_t stream) {
+  return softmax_bwd_impl(z, dz, dx, rows, cols, dtype, stream, 1);
 }
 
 rr_status rr_softmax_xent_fwd_bwd(const void* logits, const int32_t* labels, float* loss,

@@ -30,6 +30,8 @@ struct LnKernelSet {
 
 KernelSet softmax_kernels_f32();
 KernelSet softmax_kernels_bf16();
+KernelSet softmax_bwd_kernels_f32();
+KernelSet softmax_bwd_kernels_bf16();
 KernelSet lnfwd_kernels_f32();
 KernelSet lnfwd_kernels_bf16();
 KernelSet lnbwd_kernels_f32();

@@ -4,6 +4,11 @@
 //                  loss + dlogits = softmax - onehot in the same pass
 //                  ("Engineering a CUDA Machine Learning Framework from Scratch",
 //                  sec. 3.1 "Online FlashSoftmax" and sec. 2.1).
+//                  With SoftmaxParams::log set it writes the log-softmax
+//                  z = (x - m) - ln d instead.
+//   OpSoftmaxBwd   softmax backward dx = y * (dy - sum y*dy) and log-softmax
+//                  backward dx = dz - exp(z) * sum dz (the vector-Jacobian
+//                  products of the Softmax layer of the "NexusGrad" README).
 //   OpLnFwd        LayerNorm forward with its moments from one pass over
 //                  global memory (same page, sec. 3.2): exact mean from a
 //                  compensated sum, then M2 about it, in registers; row slices
@@ -30,6 +35,15 @@ struct SoftmaxParams {
   int* err;
   int64_t cols;
   int32_t ignore;
+  int32_t log;  // 1: write the log-softmax (x - m) - ln d instead of the softmax
+};
+struct SoftmaxBwdParams {
+  const char* y;   // the forward output: softmax y, or log-softmax z when log
+  const char* dy;  // upstream gradient
+  char* dx;
+  int* err;
+  int64_t cols;
+  int32_t log;
 };
 struct LnFwdParams {
   const char* x;
@@ -358,6 +372,26 @@ struct OpSoftmaxXent {
       }
       return;
     }
+    if (p.log) {
+      // z_j = (x_j - m) - ln d: x - m first, so z keeps its relative accuracy
+      const float lnd = logf(s.d);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (!g.has(q)) break;
+        float f[W];
+        if constexpr (W > 1) {
+#pragma unroll
+          for (int e = 0; e < W; e += 2) {
+            add2(f[e], f[e + 1], x.get(0, q, e), x.get(0, q, e + 1), -s.m, -s.m);
+            add2(f[e], f[e + 1], f[e], f[e + 1], -lnd, -lnd);
+          }
+        } else {
+          f[0] = (x.get(0, q, 0) - s.m) - lnd;
+        }
+        g.store_chunk(y0, q, f);
+      }
+      return;
+    }
     // p_j = 2^(x_j log2 e - fl(m log2 e)) * 2^(-r) / d
     const float mL = s.m * kLog2e;
     const float rr = fmaf(s.m, kLog2e, -mL);
@@ -382,6 +416,109 @@ struct OpSoftmaxXent {
           if (e == el) f[e] -= 1.0f;
       }
       g.store_chunk(y0, q, f);
+    }
+  }
+  __device__ __forceinline__ static void epilogue(Thread&, const Params&, const Geo&,
+                                                  unsigned char*, int64_t, int64_t, int64_t, int,
+                                                  int, int, int) {}
+};
+
+// ------------------------------------------- softmax / log-softmax backward --
+//
+// Two row tensors read in the same memory-aligned chunks (the caller gives y,
+// dy and dx the same 16-byte alignment, else element mode): one sum per row,
+// S = sum y*dy (softmax) or sum dz (log-softmax), then
+//   dx = y * (dy - S)            or   dx = dz - exp(z) * S.
+// Ragged slots hold 0 in both tensors and add nothing to S.
+
+template <int DT_, int W_, int NQ_>
+struct OpSoftmaxBwd {
+  static constexpr int DT = DT_, W = W_, NT = 2, NQ = NQ_;
+  static constexpr int E = DType<DT>::E;
+  static constexpr bool kPrefetch = true;
+  using Params = SoftmaxBwdParams;
+  struct Meta {};
+  struct Thread {};
+
+  __device__ __forceinline__ static Meta meta(const Params&, int64_t) { return {}; }
+  __device__ __forceinline__ static bool skip(const Meta&) { return false; }
+  __device__ __forceinline__ static const char* in_slice_start(const Params& p, int t, int64_t r,
+                                                               int64_t c0) {
+    return (t == 0 ? p.y : p.dy) + (r * p.cols + c0) * E;
+  }
+  __device__ __forceinline__ static uint64_t start_addr(const Params& p, int64_t r, int64_t c0) {
+    return reinterpret_cast<uint64_t>(in_slice_start(p, 0, r, c0));
+  }
+  __device__ __forceinline__ static const char* in_chunk0(const Params& p, int t, int64_t r,
+                                                          int64_t c0, const RowGeo<DT, W>& g) {
+    return in_slice_start(p, t, r, c0) - g.head_bytes;
+  }
+  __device__ __forceinline__ static void thread_init(Thread&, const Params&, const Geo&, int64_t,
+                                                     int64_t, int, int, unsigned char*, int, int) {}
+  __device__ __forceinline__ static void load_direct(RowRegs<DT, W, NT, NQ>& v,
+                                                     const RowGeo<DT, W>& g, const Params& p,
+                                                     const Geo&, int64_t r, int64_t c0) {
+    load_direct_mem(v, 0, g, in_chunk0(p, 0, r, c0, g), 0.f);
+    load_direct_mem(v, 1, g, in_chunk0(p, 1, r, c0, g), 0.f);
+  }
+  __device__ __forceinline__ static void load_staged(RowRegs<DT, W, NT, NQ>& v,
+                                                     const RowGeo<DT, W>& g, const Params& p,
+                                                     const Geo&, int64_t r, int64_t c0,
+                                                     const unsigned char* sbuf, int buf_bytes) {
+    load_staged_mem(v, 0, g, in_chunk0(p, 0, r, c0, g), sbuf, 0.f);
+    load_staged_mem(v, 1, g, in_chunk0(p, 1, r, c0, g), sbuf + buf_bytes, 0.f);
+  }
+
+  template <class R>
+  __device__ __forceinline__ static void process(Thread&, const Params& p, const Geo&, int64_t r,
+                                                 const Meta&, const RowRegs<DT, W, NT, NQ>& v,
+                                                 const RowGeo<DT, W>& g, bool, bool active,
+                                                 R& rd) {
+    float s0 = 0.f, s1 = 0.f;
+    if (active) {
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (!g.has(q)) break;
+        if constexpr (W > 1) {
+#pragma unroll
+          for (int e = 0; e < W; e += 2) {
+            if (p.log)
+              add2(s0, s1, s0, s1, v.get(1, q, e), v.get(1, q, e + 1));
+            else
+              fma2(s0, s1, v.get(0, q, e), v.get(0, q, e + 1), v.get(1, q, e), v.get(1, q, e + 1),
+                   s0, s1);
+          }
+        } else {
+          s0 = p.log ? s0 + v.get(1, q, 0) : fmaf(v.get(0, q, 0), v.get(1, q, 0), s0);
+        }
+      }
+    }
+    Sum1 S{s0 + s1};
+    S = rd.reduce(S, MergeSum1());
+    S = rd.cluster(S, MergeSum1());
+    if (!active) return;
+    char* dx0 = p.dx + (r * p.cols + g.c0) * E - g.head_bytes;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (!g.has(q)) break;
+      float f[W];
+      if constexpr (W > 1) {
+#pragma unroll
+        for (int e = 0; e < W; e += 2) {
+          if (p.log) {
+            const float p0 = ex2(v.get(0, q, e) * kLog2e), p1 = ex2(v.get(0, q, e + 1) * kLog2e);
+            fma2(f[e], f[e + 1], p0, p1, -S.s, -S.s, v.get(1, q, e), v.get(1, q, e + 1));
+          } else {
+            float t0, t1;
+            add2(t0, t1, v.get(1, q, e), v.get(1, q, e + 1), -S.s, -S.s);
+            mul2(f[e], f[e + 1], v.get(0, q, e), v.get(0, q, e + 1), t0, t1);
+          }
+        }
+      } else {
+        f[0] = p.log ? fmaf(ex2(v.get(0, q, 0) * kLog2e), -S.s, v.get(1, q, 0))
+                     : v.get(0, q, 0) * (v.get(1, q, 0) - S.s);
+      }
+      g.store_chunk(dx0, q, f);
     }
   }
   __device__ __forceinline__ static void epilogue(Thread&, const Params&, const Geo&,

@@ -56,6 +56,12 @@ def load_library():
         lib.rr_softmax_fwd.restype = st
         lib.rr_softmax_xent_fwd_bwd.argtypes = [vp, vp, vp, vp, i64, i64, i32, vp, st, vp]
         lib.rr_softmax_xent_fwd_bwd.restype = st
+        lib.rr_log_softmax_fwd.argtypes = [vp, vp, i64, i64, st, vp]
+        lib.rr_log_softmax_fwd.restype = st
+        lib.rr_softmax_bwd.argtypes = [vp, vp, vp, i64, i64, st, vp]
+        lib.rr_softmax_bwd.restype = st
+        lib.rr_log_softmax_bwd.argtypes = [vp, vp, vp, i64, i64, st, vp]
+        lib.rr_log_softmax_bwd.restype = st
         lib.rr_layernorm_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, ctypes.c_float,
                                          st, vp]
         lib.rr_layernorm_fwd.restype = st
@@ -132,6 +138,30 @@ def rr_softmax_xent_fwd_bwd(logits, labels, loss, dlogits, ignore_index=-100,
     _check("rr_softmax_xent_fwd_bwd", load_library().rr_softmax_xent_fwd_bwd(
         _p(logits), _p(labels), _p(loss), _p(dlogits), rows, cols, int(ignore_index),
         _p(bad_label_count), _dtype(logits), _stream(stream)))
+
+
+def rr_log_softmax_fwd(x, z, stream=None):
+    """z = log_softmax(x) per row (z may be x)."""
+    _contig(x, z)
+    rows, cols = x.shape
+    _check("rr_log_softmax_fwd", load_library().rr_log_softmax_fwd(
+        _p(x), _p(z), rows, cols, _dtype(x), _stream(stream)))
+
+
+def rr_softmax_bwd(y, dy, dx, stream=None):
+    """dx = y * (dy - sum(y * dy)) per row, y the softmax output."""
+    _contig(y, dy, dx)
+    rows, cols = y.shape
+    _check("rr_softmax_bwd", load_library().rr_softmax_bwd(
+        _p(y), _p(dy), _p(dx), rows, cols, _dtype(y), _stream(stream)))
+
+
+def rr_log_softmax_bwd(z, dz, dx, stream=None):
+    """dx = dz - exp(z) * sum(dz) per row, z the log-softmax output."""
+    _contig(z, dz, dx)
+    rows, cols = z.shape
+    _check("rr_log_softmax_bwd", load_library().rr_log_softmax_bwd(
+        _p(z), _p(dz), _p(dx), rows, cols, _dtype(z), _stream(stream)))
 
 
 def rr_layernorm_fwd(x, gamma, beta, y, mean, rstd, eps=1e-5, stream=None):

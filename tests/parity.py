@@ -16,6 +16,7 @@ import torch
 
 import oracle
 import row_reduction_pass_gb300 as rr
+from row_reduction_pass_gb300 import synth
 
 TOL = {"f32": (1e-5, 1e-5), "bf16": (2e-2, 1e-5)}
 TOL_F32_OUT = (1e-5, 1e-5)
@@ -63,7 +64,8 @@ def compare(name: str, got: np.ndarray, ref: np.ndarray, rtol: float, atol: floa
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, f"{name}: shape {got.shape} != {ref.shape}"
     both_nan = np.isnan(got) & np.isnan(ref)
-    err = np.abs(got - ref)
+    with np.errstate(invalid="ignore"):  # inf - inf where both are infinite
+        err = np.abs(got - ref)
     bound = atol + rtol * np.abs(ref)
     if scale is not None:
         bound = bound + 1e-5 * scale
@@ -196,3 +198,36 @@ def check_rms(x, gamma, dy, eps, dtype, pad=(0, 0, 0, 0, 0), oracle_stats=True):
     compare("rms dx", g["dx"], rdx, rtol, atol)
     compare("rms dgamma", g["dgamma"], rdg, rtol, atol, scale=sdg)
     return g
+
+
+def store(a64: np.ndarray, dtype: str) -> np.ndarray:
+    """A float64 host array as stored inputs (float32, or bf16 bits)."""
+    a32 = np.ascontiguousarray(a64, np.float32)
+    return a32 if dtype == "f32" else synth.bf16_bits(a32)
+
+
+def check_log_softmax(x, dtype, pad_in=0, pad_out=0, inplace=False):
+    xd = to_dev(x, pad_in)
+    z = xd if inplace else empty_like_dev(x.shape, dtype, pad_out)
+    rr.rr_log_softmax_fwd(xd, z)
+    torch.cuda.synchronize()
+    rtol, atol = TOL[dtype]
+    compare("log_softmax z", host(z), oracle.log_softmax(x), rtol, atol)
+
+
+def check_softmax_bwd(y, dy, dtype, log=False, pads=(0, 0, 0), inplace=None):
+    """y (softmax output, or log-softmax output z when log) and dy are stored
+    inputs; inplace = "y" or "dy" writes dx over that input."""
+    yd = to_dev(y, pads[0])
+    dyd = to_dev(dy, pads[1])
+    if inplace == "y":
+        dx = yd
+    elif inplace == "dy":
+        dx = dyd
+    else:
+        dx = empty_like_dev(y.shape, dtype, pads[2])
+    (rr.rr_log_softmax_bwd if log else rr.rr_softmax_bwd)(yd, dyd, dx)
+    torch.cuda.synchronize()
+    ref = oracle.log_softmax_bwd(y, dy) if log else oracle.softmax_bwd(y, dy)
+    rtol, atol = TOL[dtype]
+    compare("log_softmax dx" if log else "softmax dx", host(dx), ref, rtol, atol)
