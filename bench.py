@@ -551,12 +551,6 @@ def run_sweep(args):
     for name in names:
         d = synth.make(name)
         e = 2 if d["dtype"] == "bf16" else 4
-        # reference: a plain device copy of one [rows x cols] tensor, timed the same way
-        src = d.get("logits", d.get("x"))
-        cs = tdev(src)
-        cd = torch.empty_like(cs)
-        report(name, "copy_ref", 2 * cs.numel() * e, timed(lambda: cd.copy_(cs)))
-        del cs, cd
         if d["kind"] == "xent":
             x, lab = tdev(d["logits"]), tdev(d["labels"])
             R, C = x.shape
@@ -605,6 +599,61 @@ def run_sweep(args):
                 report(name, "rms_fwd+bwd", rf + rb, tf + tb)
         del d
         torch.cuda.empty_cache()
+    if not args.cases or "graph" in args.cases:
+        run_graph_lines(rr, torch, dev)
+
+
+def run_graph_lines(rr, torch, dev, iters=200):
+    """Small shapes, where host launch overhead dominates: the per-step time of
+    back-to-back eager calls against the replay of a CUDA graph of the same
+    calls (LayerNorm fwd -> bwd at 4096 x 768 fp32, cross-entropy at 64 x 1000
+    fp32).  L2-warm on purpose: these inputs fit in L2 whichever way they run."""
+    ln = synth.make("ln_f32_4096x768")
+    x, g, b, dy = (torch.from_numpy(ln[k]).to(dev) for k in ("x", "gamma", "beta", "dy"))
+    R, C = x.shape
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+    mean, rstd = torch.empty(R, device=dev), torch.empty(R, device=dev)
+    dg, db = torch.empty_like(g), torch.empty_like(g)
+    ws = torch.empty(rr.rr_layernorm_bwd_workspace_size(R, C, x.dtype), dtype=torch.uint8,
+                     device=dev)
+    xe = synth.make("xent_f32_64x1000")
+    lx = torch.from_numpy(xe["logits"]).to(dev)
+    lab = torch.from_numpy(xe["labels"]).to(dev)
+    loss, dl = torch.empty(lx.shape[0], device=dev), torch.empty_like(lx)
+    steps = {
+        "ln_f32_4096x768 fwd+bwd": (lambda: (rr.rr_layernorm_fwd(x, g, b, y, mean, rstd),
+                                             rr.rr_layernorm_bwd(dy, x, mean, rstd, g, dx, dg, db,
+                                                                 ws)), 3),
+        "xent_f32_64x1000": (lambda: rr.rr_softmax_xent_fwd_bwd(lx, lab, loss, dl), 1),
+    }
+    for name, (fn, nl) in steps.items():
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(iters):
+                fn()
+            e.record(s)
+            torch.cuda.synchronize()
+            eager = a.elapsed_time(e) / iters
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                fn()
+            graph.replay()
+            torch.cuda.synchronize()
+            a.record(s)
+            for _ in range(iters):
+                graph.replay()
+            e.record(s)
+            torch.cuda.synchronize()
+            rep = a.elapsed_time(e) / iters
+        print(json.dumps({"case": name, "op": "eager_vs_graph", "kernels_per_step": nl,
+                          "eager_us": round(eager * 1e3, 2), "graph_us": round(rep * 1e3, 2)}),
+              flush=True)
 
 
 def main():
