@@ -308,7 +308,12 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
   const int64_t npad = nch * W;
   const int64_t red_off = round_up((fwdk ? planes : 1) * npad * 4, 16);
   const int64_t acc_off = round_up(red_off + (G > 32 ? (int64_t)ngroups * 1024 : 0), 16);
-  const int64_t smem = acc_off + (fwdk ? 0 : (int64_t)ngroups * planes * npad * 4);
+  const int64_t acc_end = acc_off + (fwdk ? 0 : (int64_t)ngroups * planes * npad * 4);
+  // backward with aligned rows: per-thread prefetch slots [2][2][chunks per thread][T]
+  const int nq_used = (fn == ls.k1[lmode][gi]) ? 1 : nq;
+  const int64_t pf_off = round_up(acc_end, 16);
+  const int64_t smem =
+      pf_off + (lmode == 0 ? (int64_t)(fwdk ? 2 : 4) * nq_used * 16 * T : 0);
   if (smem > di->smem_optin) return fail(RR_ERR_INVALID_ARG, "row-group shared memory too large");
   if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
   int& occ = di->occ[{fn, ((long long)T << 32) | (long long)smem}];
@@ -330,8 +335,9 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
   pl->grid = grid;
   pl->smem = (size_t)smem;
   pl->partials = grid;
-  pl->lgeo = rr::LnGeo{rows, (int32_t)cols, (int32_t)nfull, (int32_t)rag, (int32_t)nch,
-                       (int32_t)red_off, (int32_t)acc_off};
+  pl->lgeo = rr::LnGeo{rows,           (int32_t)cols,    (int32_t)nfull,
+                       (int32_t)rag,   (int32_t)nch,     (int32_t)red_off,
+                       (int32_t)acc_off, (int32_t)pf_off};
   return RR_OK;
 }
 

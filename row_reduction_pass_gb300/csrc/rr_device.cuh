@@ -254,6 +254,24 @@ __device__ __forceinline__ S group_reduce(S v, M merge) {
   return v;
 }
 
+// ------------------------------------------------- per-thread async copies --
+// 16-byte global -> shared copies issued by one thread for itself (both
+// addresses 16-byte aligned), grouped with commit and waited for by count; the
+// issuing thread may read its own slots once the wait returns.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ------------------------------------------------- bulk copy and barriers ---
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

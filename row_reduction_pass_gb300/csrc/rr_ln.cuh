@@ -37,6 +37,7 @@ struct LnGeo {
   int32_t nch;      // chunks per row
   int32_t red_off;  // group-reduction scratch (G > 32): 1 KB per group
   int32_t acc_off;  // backward: column partials, ngroups x 2 x (nch * W) floats
+  int32_t pf_off;   // backward with aligned rows: [2][2][NQ][block] 16-byte prefetch slots
 };
 
 // Register sizes.  Forward: 64 per thread at any block size.  Backward: up to
@@ -284,12 +285,36 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
   const char* xend = p.x + geo.rows * rowb;
   const float ns = static_cast<float>(geo.cols);
 
+  // aligned rows: the next row's chunks are copied with cp.async into this
+  // thread's own shared-memory slots [2 stages][NQ][block] while it works on
+  // the current row (as in the backward below)
+  constexpr bool PF = AL && W > 1;
+  uint4* pf = reinterpret_cast<uint4*>(smem + geo.pf_off);
+  auto issue = [&](int64_t rr, int stage) {
+    if (rr < geo.rows) {
+      const char* x0 = p.x + rr * rowb;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q)
+        if (q < cs.nf)
+          cp_async16(pf + (stage * NQ + q) * MAXT + threadIdx.x, x0 + (int64_t)(gt + q * G) * 16);
+    }
+    cp_async_commit();
+  };
+  if constexpr (PF) issue(r0, 0);
+
   for (int64_t it = 0;; ++it) {
     if (w0 + it * step >= geo.rows) break;
     const int64_t r = r0 + it * step;
     const bool active = r < geo.rows;
     uint4 v[NQ];
-    if (active) {
+    if constexpr (PF) {
+      issue(r + step, (int)((it + 1) & 1));
+      cp_async_wait<1>();
+#pragma unroll
+      for (int q = 0; q < NQ; ++q)
+        v[q] = (active && q < cs.nf) ? pf[((int)(it & 1) * NQ + q) * MAXT + threadIdx.x]
+                                     : make_uint4(0u, 0u, 0u, 0u);
+    } else if (active) {
       ln_load<DT, W, G, NQ, AL>(v, p.x + r * rowb, gt, cs, geo.rag, p.x, xend);
     } else {
 #pragma unroll
@@ -440,6 +465,7 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
       }
     }
   }
+  if constexpr (PF) cp_async_wait<0>();
 }
 
 // ----------------------------------------------------------- backward ------
@@ -451,9 +477,16 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
 // sum dy*xhat and sum dy stay in registers; at the end the groups of a block
 // add theirs in a fixed order into one partial row of the workspace
 // ([gridDim.x][2][cols] floats), which col_reduce_kernel sums.
+//
+// With aligned rows (AL, chunk mode) each thread copies its chunks of dy and x
+// for the row after the current one into its own shared-memory slots with
+// cp.async while it works on the current row (no registers held, no barrier:
+// a thread reads only the slots it filled), and the row statistics one row
+// ahead into registers.
 template <int DT, int W, int G, int NQ, bool AL, int MAXT, bool RMS>
 __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
     ln_bwd_kernel(const LnBwdParams p, const LnGeo geo) {
+  constexpr bool PF = AL && W > 1;
   constexpr int E = DType<DT>::E;
   extern __shared__ __align__(128) unsigned char smem[];
   const int npad = geo.nch * W;
@@ -479,22 +512,67 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
 #pragma unroll
     for (int e = 0; e < W; ++e) ag[q][e] = ab[q][e] = 0.f;
 
+  uint4* pf = reinterpret_cast<uint4*>(smem + geo.pf_off);
+  auto slot = [&](int stage, int t, int q) -> uint4* {
+    return pf + ((stage * 2 + t) * NQ + q) * MAXT + threadIdx.x;
+  };
+  // row rr's chunks into stage `stage` (an empty group past the last row)
+  auto issue = [&](int64_t rr, int stage) {
+    if (rr < geo.rows) {
+      const char* d0 = p.dy + rr * rowb;
+      const char* x0 = p.x + rr * rowb;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q)
+        if (q < cs.nf) {
+          cp_async16(slot(stage, 0, q), d0 + (int64_t)(gt + q * G) * 16);
+          cp_async16(slot(stage, 1, q), x0 + (int64_t)(gt + q * G) * 16);
+        }
+    }
+    cp_async_commit();
+  };
+  auto stats = [&](int64_t rr, float& mu, float& rs) {
+    mu = 0.f;
+    rs = 0.f;
+    if (rr < geo.rows) {
+      if constexpr (!RMS) mu = __ldg(p.mean + rr);
+      rs = __ldg(p.rstd + rr);
+    }
+  };
+  float nmean = 0.f, nrstd = 0.f;
+  if constexpr (PF) {
+    issue(r0, 0);
+    stats(r0, nmean, nrstd);
+  }
+
   for (int64_t it = 0;; ++it) {
     if (w0 + it * step >= geo.rows) break;
     const int64_t r = r0 + it * step;
     const bool active = r < geo.rows;
-    float mean = 0.f, rstd = 0.f;
-    if (active) {
-      if constexpr (!RMS) mean = __ldg(p.mean + r);
-      rstd = __ldg(p.rstd + r);
+    float mean, rstd;
+    if constexpr (PF) {
+      mean = nmean;
+      rstd = nrstd;
+      issue(r + step, (int)((it + 1) & 1));
+      stats(r + step, nmean, nrstd);
+      cp_async_wait<1>();
+    } else {
+      stats(r, mean, rstd);
     }
     const bool use = active && rstd != 0.f;
     float gv[NQ][W], hv[NQ][W];
     float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
     if (use) {
       uint4 dv[NQ], xv[NQ];
-      ln_load<DT, W, G, NQ, AL>(dv, p.dy + r * rowb, gt, cs, geo.rag, p.dy, p.dy + nbytes);
-      ln_load<DT, W, G, NQ, AL>(xv, p.x + r * rowb, gt, cs, geo.rag, p.x, p.x + nbytes);
+      if constexpr (PF) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          dv[q] = q < cs.nf ? *slot((int)(it & 1), 0, q) : make_uint4(0u, 0u, 0u, 0u);
+          xv[q] = q < cs.nf ? *slot((int)(it & 1), 1, q) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      } else {
+        ln_load<DT, W, G, NQ, AL>(dv, p.dy + r * rowb, gt, cs, geo.rag, p.dy, p.dy + nbytes);
+        ln_load<DT, W, G, NQ, AL>(xv, p.x + r * rowb, gt, cs, geo.rag, p.x, p.x + nbytes);
+      }
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {
         if (q < cs.nown) {
@@ -563,6 +641,8 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
       }
     }
   }
+
+  if constexpr (PF) cp_async_wait<0>();
 
   // Column partials: each group's to shared memory, then a fixed-order sum
   // over the groups into this block's partial row.
