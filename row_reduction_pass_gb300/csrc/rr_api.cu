@@ -312,8 +312,14 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
   // backward with aligned rows: per-thread prefetch slots [2][2][chunks per thread][T]
   const int nq_used = (fn == ls.k1[lmode][gi]) ? 1 : nq;
   const int64_t pf_off = round_up(acc_end, 16);
-  const int64_t smem =
-      pf_off + (lmode == 0 ? (int64_t)(fwdk ? 2 : 4) * nq_used * 16 * T : 0);
+  // prefetch space: aligned rows, per-thread slots [2][tensors][chunks per thread][T];
+  // misaligned rows (chunk mode), per-group row buffers [tensors][2][chunks + 2]
+  const int ntens = fwdk ? 1 : 2;
+  int64_t pf_bytes = 0;
+  if (lmode == 0) pf_bytes = (int64_t)2 * ntens * nq_used * 16 * T;
+  if (lmode == 1 && (fwdk ? G >= 32 : nq_used > 1))
+    pf_bytes = (int64_t)ngroups * 2 * ntens * (nch + 2) * 16;
+  const int64_t smem = pf_off + pf_bytes;
   if (smem > di->smem_optin) return fail(RR_ERR_INVALID_ARG, "row-group shared memory too large");
   if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
   int& occ = di->occ[{fn, ((long long)T << 32) | (long long)smem}];

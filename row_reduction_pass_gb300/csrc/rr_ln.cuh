@@ -209,6 +209,68 @@ struct LnPlanes {
   }
 };
 
+// Misaligned rows (chunk mode): a row group's two buffers of the aligned
+// 16-byte blocks that cover a row.  Every thread of the group copies blocks
+// gt, gt + G, ... of the next row with cp.async; once the copies have landed and
+// the group has synchronised, chunk k of the row is the funnel shift of blocks k
+// and k + 1 by the row's start address mod 16.  A row whose covering blocks
+// would leave the tensor (the first or last rows of a tensor with a misaligned
+// base) is not copied; the caller reads it directly.
+template <int DT, int W, int G, int NQ>
+struct LnRowPf {
+  uint4* buf;  // [2 stages][nb] blocks
+  int nb;
+  int h0, h1;     // row start address mod 16, stage 0 / 1
+  bool ok0, ok1;  // the stage holds its row
+  __device__ __forceinline__ void issue(const char* rs, int64_t rowb, const char* tb,
+                                        const char* te, int stage, int gt, bool valid) {
+    bool ok = false;
+    int h = 0;
+    if (valid) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(rs);
+      const uintptr_t lo = a & ~uintptr_t(15), hi = (a + rowb + 15) & ~uintptr_t(15);
+      h = static_cast<int>(a & 15);
+      ok = lo >= reinterpret_cast<uintptr_t>(tb) && hi <= reinterpret_cast<uintptr_t>(te);
+      if (ok) {
+        const int n = static_cast<int>((hi - lo) >> 4);
+        uint4* d = buf + stage * nb;
+        for (int j = gt; j < n; j += G)
+          cp_async16(d + j, reinterpret_cast<const void*>(lo + (uintptr_t)j * 16));
+      }
+    }
+    if (stage) {
+      ok1 = ok;
+      h1 = h;
+    } else {
+      ok0 = ok;
+      h0 = h;
+    }
+  }
+  // The thread's chunks of the row in stage s (ragged slots 0); false when the
+  // row was not copied.
+  __device__ __forceinline__ bool get(uint4 (&v)[NQ], int s, int gt, const LnCols<G, NQ>& cs,
+                                      int rag) const {
+    if (!(s ? ok1 : ok0)) return false;
+    const int h = s ? h1 : h0;
+    const uint4* b = buf + s * nb;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      uint4 c = make_uint4(0u, 0u, 0u, 0u);
+      if (q < cs.nown) {
+        const int k = gt + q * G;
+        c = funnel16(b[k], b[k + 1], h);
+        if (q >= cs.nf) {
+#pragma unroll
+          for (int e = 0; e < W; ++e)
+            if (e >= rag) chunk_set_bits<DT>(c, e, 0u);
+        }
+      }
+      v[q] = c;
+    }
+    return true;
+  }
+};
+
 // Converts gamma (or beta) into its planes.  Chunk mode: one 16-byte load per
 // chunk (the vector is 16-byte aligned there), up to four chunks in flight per
 // thread so the L2 round trips overlap; element mode: scalar loads, unrolled.
@@ -285,22 +347,34 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
   const char* xend = p.x + geo.rows * rowb;
   const float ns = static_cast<float>(geo.cols);
 
-  // aligned rows: the next row's chunks are copied with cp.async into this
-  // thread's own shared-memory slots [2 stages][NQ][block] while it works on
-  // the current row (as in the backward below)
+  // The next row is copied with cp.async while the current one is worked on
+  // (as in the backward below): aligned rows into this thread's own slots
+  // [2 stages][NQ][block]; misaligned rows into the group's row buffers.
   constexpr bool PF = AL && W > 1;
+  constexpr bool PFR = !AL && W > 1 && G >= 32;  // short rows: the per-row sync costs more
   uint4* pf = reinterpret_cast<uint4*>(smem + geo.pf_off);
+  LnRowPf<DT, W, G, NQ> rpx{pf + (size_t)grp * 2 * (geo.nch + 2), geo.nch + 2, 0, 0, false, false};
   auto issue = [&](int64_t rr, int stage) {
-    if (rr < geo.rows) {
-      const char* x0 = p.x + rr * rowb;
+    if constexpr (PF) {
+      if (rr < geo.rows) {
+        const char* x0 = p.x + rr * rowb;
 #pragma unroll
-      for (int q = 0; q < NQ; ++q)
-        if (q < cs.nf)
-          cp_async16(pf + (stage * NQ + q) * MAXT + threadIdx.x, x0 + (int64_t)(gt + q * G) * 16);
+        for (int q = 0; q < NQ; ++q)
+          if (q < cs.nf)
+            cp_async16(pf + (stage * NQ + q) * MAXT + threadIdx.x,
+                       x0 + (int64_t)(gt + q * G) * 16);
+      }
+    } else if constexpr (PFR) {
+      const bool valid = rr < geo.rows;
+      rpx.issue(valid ? p.x + rr * rowb : p.x, rowb, p.x, xend, stage, gt, valid);
     }
     cp_async_commit();
   };
-  if constexpr (PF) issue(r0, 0);
+  auto group_sync = [&]() {
+    if constexpr (G > 32) named_bar(1 + grp, G);
+    else __syncwarp();
+  };
+  if constexpr (PF || PFR) issue(r0, 0);
 
   for (int64_t it = 0;; ++it) {
     if (w0 + it * step >= geo.rows) break;
@@ -314,6 +388,18 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
       for (int q = 0; q < NQ; ++q)
         v[q] = (active && q < cs.nf) ? pf[((int)(it & 1) * NQ + q) * MAXT + threadIdx.x]
                                      : make_uint4(0u, 0u, 0u, 0u);
+    } else if constexpr (PFR) {
+      issue(r + step, (int)((it + 1) & 1));
+      cp_async_wait<1>();
+      group_sync();
+      if (!(active && rpx.get(v, (int)(it & 1), gt, cs, geo.rag))) {
+        if (active) {
+          ln_load<DT, W, G, NQ, AL>(v, p.x + r * rowb, gt, cs, geo.rag, p.x, xend);
+        } else {
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
     } else if (active) {
       ln_load<DT, W, G, NQ, AL>(v, p.x + r * rowb, gt, cs, geo.rag, p.x, xend);
     } else {
@@ -465,7 +551,7 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
       }
     }
   }
-  if constexpr (PF) cp_async_wait<0>();
+  if constexpr (PF || PFR) cp_async_wait<0>();
 }
 
 // ----------------------------------------------------------- backward ------
@@ -487,6 +573,7 @@ template <int DT, int W, int G, int NQ, bool AL, int MAXT, bool RMS>
 __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
     ln_bwd_kernel(const LnBwdParams p, const LnGeo geo) {
   constexpr bool PF = AL && W > 1;
+  constexpr bool PFR = !AL && W > 1 && NQ > 1;  // one-chunk variants: no room
   constexpr int E = DType<DT>::E;
   extern __shared__ __align__(128) unsigned char smem[];
   const int npad = geo.nch * W;
@@ -516,19 +603,33 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
   auto slot = [&](int stage, int t, int q) -> uint4* {
     return pf + ((stage * 2 + t) * NQ + q) * MAXT + threadIdx.x;
   };
+  // misaligned rows: the group's row buffers, [dy | x][2 stages][nb]
+  LnRowPf<DT, W, G, NQ> rpd{pf + (size_t)grp * 4 * (geo.nch + 2), geo.nch + 2, 0, 0, false, false};
+  LnRowPf<DT, W, G, NQ> rpx{pf + (size_t)grp * 4 * (geo.nch + 2) + 2 * (geo.nch + 2), geo.nch + 2,
+                            0, 0, false, false};
   // row rr's chunks into stage `stage` (an empty group past the last row)
   auto issue = [&](int64_t rr, int stage) {
-    if (rr < geo.rows) {
-      const char* d0 = p.dy + rr * rowb;
-      const char* x0 = p.x + rr * rowb;
+    if constexpr (PF) {
+      if (rr < geo.rows) {
+        const char* d0 = p.dy + rr * rowb;
+        const char* x0 = p.x + rr * rowb;
 #pragma unroll
-      for (int q = 0; q < NQ; ++q)
-        if (q < cs.nf) {
-          cp_async16(slot(stage, 0, q), d0 + (int64_t)(gt + q * G) * 16);
-          cp_async16(slot(stage, 1, q), x0 + (int64_t)(gt + q * G) * 16);
-        }
+        for (int q = 0; q < NQ; ++q)
+          if (q < cs.nf) {
+            cp_async16(slot(stage, 0, q), d0 + (int64_t)(gt + q * G) * 16);
+            cp_async16(slot(stage, 1, q), x0 + (int64_t)(gt + q * G) * 16);
+          }
+      }
+    } else if constexpr (PFR) {
+      const bool valid = rr < geo.rows;
+      rpd.issue(valid ? p.dy + rr * rowb : p.dy, rowb, p.dy, p.dy + nbytes, stage, gt, valid);
+      rpx.issue(valid ? p.x + rr * rowb : p.x, rowb, p.x, p.x + nbytes, stage, gt, valid);
     }
     cp_async_commit();
+  };
+  auto group_sync = [&]() {
+    if constexpr (G > 32) named_bar(1 + grp, G);
+    else __syncwarp();
   };
   auto stats = [&](int64_t rr, float& mu, float& rs) {
     mu = 0.f;
@@ -539,7 +640,7 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
     }
   };
   float nmean = 0.f, nrstd = 0.f;
-  if constexpr (PF) {
+  if constexpr (PF || PFR) {
     issue(r0, 0);
     stats(r0, nmean, nrstd);
   }
@@ -549,12 +650,13 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
     const int64_t r = r0 + it * step;
     const bool active = r < geo.rows;
     float mean, rstd;
-    if constexpr (PF) {
+    if constexpr (PF || PFR) {
       mean = nmean;
       rstd = nrstd;
       issue(r + step, (int)((it + 1) & 1));
       stats(r + step, nmean, nrstd);
       cp_async_wait<1>();
+      if constexpr (PFR) group_sync();
     } else {
       stats(r, mean, rstd);
     }
@@ -569,6 +671,11 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
           dv[q] = q < cs.nf ? *slot((int)(it & 1), 0, q) : make_uint4(0u, 0u, 0u, 0u);
           xv[q] = q < cs.nf ? *slot((int)(it & 1), 1, q) : make_uint4(0u, 0u, 0u, 0u);
         }
+      } else if constexpr (PFR) {
+        if (!rpd.get(dv, (int)(it & 1), gt, cs, geo.rag))
+          ln_load<DT, W, G, NQ, AL>(dv, p.dy + r * rowb, gt, cs, geo.rag, p.dy, p.dy + nbytes);
+        if (!rpx.get(xv, (int)(it & 1), gt, cs, geo.rag))
+          ln_load<DT, W, G, NQ, AL>(xv, p.x + r * rowb, gt, cs, geo.rag, p.x, p.x + nbytes);
       } else {
         ln_load<DT, W, G, NQ, AL>(dv, p.dy + r * rowb, gt, cs, geo.rag, p.dy, p.dy + nbytes);
         ln_load<DT, W, G, NQ, AL>(xv, p.x + r * rowb, gt, cs, geo.rag, p.x, p.x + nbytes);
@@ -642,7 +749,7 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
     }
   }
 
-  if constexpr (PF) cp_async_wait<0>();
+  if constexpr (PF || PFR) cp_async_wait<0>();
 
   // Column partials: each group's to shared memory, then a fixed-order sum
   // over the groups into this block's partial row.
