@@ -341,9 +341,107 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
   pl->grid = grid;
   pl->smem = (size_t)smem;
   pl->partials = grid;
-  pl->lgeo = rr::LnGeo{rows,           (int32_t)cols,    (int32_t)nfull,
-                       (int32_t)rag,   (int32_t)nch,     (int32_t)red_off,
-                       (int32_t)acc_off, (int32_t)pf_off};
+  pl->lgeo = rr::LnGeo{rows,          (int32_t)cols,    (int32_t)nfull,   (int32_t)rag,
+                       (int32_t)nch,  (int32_t)red_off, (int32_t)acc_off, (int32_t)pf_off,
+                       (int32_t)cols, 0};
+  return RR_OK;
+}
+
+// Forward rows too long for one row group: the row is split over a cluster of K
+// blocks (K = 2 .. 8), each one group of 256 / 512 / 1024 threads holding a
+// slice of whole chunks (rr_ln.cuh, CL).  Among the (K, group size) pairs that
+// fit, the one with the least estimated time: rounds of rows (rows / clusters
+// resident on the device) x (chunks per thread + 2 for the per-row reductions).
+rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64_t cols, Plan* pl) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo* di = nullptr;
+  rr_status st = device_info(&di);
+  if (st != RR_OK) return st;
+  const rr::LnKernelSet& ls = ln_kernels(op, dt);
+  const int E = dt == RR_BF16 ? 2 : 4;
+  const int W = lmode == 2 ? 1 : 16 / E;
+  const int nq = ls.nq[lmode];
+  const int planes = op == kLnFwd ? 2 : 1;
+  struct Choice {
+    int K = 0, T = 0, ncl = 0;
+    int64_t S = 0, nchs = 0, smem = 0, red_off = 0, cl_off = 0, pf_off = 0;
+    const void* fn = nullptr;
+    double cost = 0.0;
+  } best;
+  for (int K = 2; K <= 8; ++K) {
+    const int64_t S = round_up(cdiv(cols, K), W);
+    if ((K - 1) * S >= cols) continue;  // every block of the cluster gets columns
+    const int64_t nchs = S / W, npad = nchs * W;
+    for (int gi = 0; gi < 3; ++gi) {
+      const int T = 256 << gi;
+      const void* fn = ls.kc[lmode][gi];
+      if (fn == nullptr || (int64_t)nq * T < nchs) continue;
+      const int64_t red_off = round_up(planes * npad * 4, 16);
+      const int64_t cl_off = round_up(red_off + 1024, 16);
+      const int64_t pf_off = round_up(cl_off + 32, 16);
+      int64_t pf_bytes = 0;
+      if (lmode == 0) pf_bytes = (int64_t)2 * nq * 16 * T;
+      if (lmode == 1) pf_bytes = (int64_t)2 * (nchs + 2) * 16;
+      const int64_t smem = pf_off + pf_bytes;
+      if (smem > di->smem_optin) continue;
+      if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
+      int& ncl = di->ncl[{fn, ((long long)K << 32) | (long long)smem}];
+      if (ncl == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = K;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3((unsigned)(K * di->sms));
+        cfg.blockDim = dim3((unsigned)T);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg);
+        if (e != cudaSuccess)
+          return fail(RR_ERR_CUDA, "cluster occupancy query (K=%d): %s", K, cudaGetErrorString(e));
+        if (ncl <= 0) ncl = -1;  // cannot be resident: remembered, skipped
+      }
+      if (ncl <= 0) continue;
+      const double rounds = (double)cdiv(rows, ncl);
+      const double cost = rounds * (double)(cdiv(nchs, T) + 2);
+      if (best.K == 0 || cost < best.cost - 1e-9) {
+        best.K = K;
+        best.T = T;
+        best.ncl = ncl;
+        best.S = S;
+        best.nchs = nchs;
+        best.smem = smem;
+        best.red_off = red_off;
+        best.cl_off = cl_off;
+        best.pf_off = pf_off;
+        best.fn = fn;
+        best.cost = cost;
+      }
+    }
+  }
+  if (best.K == 0) return fail(RR_ERR_INVALID_ARG, "row longer than a cluster of row groups holds");
+  pl->kind = 1;
+  pl->staged = false;
+  pl->mode = lmode;
+  pl->G = best.T;
+  pl->T = best.T;
+  pl->K = best.K;
+  pl->fn = best.fn;
+  pl->grid = (int64_t)best.K * (rows < best.ncl ? rows : best.ncl);
+  pl->smem = (size_t)best.smem;
+  pl->partials = pl->grid / best.K;
+  pl->lgeo = rr::LnGeo{rows,
+                       (int32_t)cols,
+                       (int32_t)best.nchs,
+                       0,
+                       (int32_t)best.nchs,
+                       (int32_t)best.red_off,
+                       (int32_t)best.cl_off,
+                       (int32_t)best.pf_off,
+                       (int32_t)best.S,
+                       (int32_t)best.cl_off};
   return RR_OK;
 }
 
@@ -562,7 +660,9 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
   const bool al = aligned(gamma, 16) && aligned(beta, 16);
   const bool rows_al = (cols * (int64_t)E) % 16 == 0 && aligned(x, 16) && aligned(y, 16);
   Plan pl;
-  st = ln_rowgroup_plan(kLnFwd, dtype, al ? (rows_al ? 0 : 1) : 2, rows, cols, &pl, INT64_MAX);
+  const int lmode = al ? (rows_al ? 0 : 1) : 2;
+  st = ln_rowgroup_plan(kLnFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
+  if (st == RR_ERR_INVALID_ARG) st = ln_cluster_plan(kLnFwd, dtype, lmode, rows, cols, &pl);
   if (st == RR_ERR_INVALID_ARG) st = plan_any(kLnFwd, dtype, al, true, rows, cols, &pl);
   if (st != RR_OK) return st;
   int* err = device_error_word();
@@ -592,7 +692,9 @@ rr_status rr_rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
   const bool al = aligned(gamma, 16);
   const bool rows_al = (cols * (int64_t)E) % 16 == 0 && aligned(x, 16) && aligned(y, 16);
   Plan pl;
-  st = ln_rowgroup_plan(kRmsFwd, dtype, al ? (rows_al ? 0 : 1) : 2, rows, cols, &pl, INT64_MAX);
+  const int lmode = al ? (rows_al ? 0 : 1) : 2;
+  st = ln_rowgroup_plan(kRmsFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
+  if (st == RR_ERR_INVALID_ARG) st = ln_cluster_plan(kRmsFwd, dtype, lmode, rows, cols, &pl);
   if (st == RR_ERR_INVALID_ARG)
     return fail(RR_ERR_INVALID_ARG, "RMSNorm rows of %lld columns are longer than one row group holds",
                 (long long)cols);

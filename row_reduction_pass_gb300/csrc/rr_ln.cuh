@@ -37,7 +37,9 @@ struct LnGeo {
   int32_t nch;      // chunks per row
   int32_t red_off;  // group-reduction scratch (G > 32): 1 KB per group
   int32_t acc_off;  // backward: column partials, ngroups x 2 x (nch * W) floats
-  int32_t pf_off;   // backward with aligned rows: [2][2][NQ][block] 16-byte prefetch slots
+  int32_t pf_off;   // cp.async prefetch slots / row buffers
+  int32_t slice;    // columns per block of a cluster (= cols without clusters)
+  int32_t cl_off;   // cluster exchange slots (2 x 16 bytes)
 };
 
 // Register sizes.  Forward: 64 per thread at any block size.  Backward: up to
@@ -53,6 +55,9 @@ template <int MAXT, int NQ> constexpr int ln_bwd_min_blocks() { return (NQ == 1 
 struct CascSum {
   float s, e;
   __device__ __forceinline__ static CascSum identity() { return {0.f, 0.f}; }
+  __device__ __forceinline__ static CascSum load_remote(uint32_t a) {
+    return {ld_cluster_f32(a), ld_cluster_f32(a + 4)};
+  }
   __device__ __forceinline__ static CascSum shfl_xor(const CascSum& v, int off) {
     return {__shfl_xor_sync(0xffffffffu, v.s, off), __shfl_xor_sync(0xffffffffu, v.e, off)};
   }
@@ -93,6 +98,22 @@ struct LnRed {
     }
   }
 };
+
+// A row split over the K blocks of a cluster: each block's statistic (already
+// reduced over its threads) goes to its exchange slot, and after a cluster
+// barrier every thread merges the K slots in rank order, so all blocks hold the
+// same bits.  Slots alternate by call parity: a slot is rewritten two calls
+// later, after the next barrier, which every reader of it has passed.
+template <class S, class M>
+__device__ __forceinline__ S ln_cluster(S s, M merge, unsigned char* slots, int& calls, int K) {
+  S* slot = reinterpret_cast<S*>(slots + 16 * (calls & 1));
+  ++calls;
+  if (threadIdx.x == 0) *slot = s;
+  cluster_sync();
+  S acc = S::load_remote(map_to_rank(slot, 0));
+  for (int k = 1; k < K; ++k) acc = merge(acc, S::load_remote(map_to_rank(slot, k)));
+  return acc;
+}
 
 // The chunks of one thread: q < nf are whole, q < nown are owned (the ragged
 // last chunk of the row, when this thread holds it, is q = nf).
@@ -321,29 +342,48 @@ __device__ __forceinline__ void ln_stage(const LnPlanes<W>& pl, const char* src,
 // group as a double-float -> exact mean mh + ml; squared deviations
 // ((x - mh) - ml)^2 -> M2 -> rstd = 1/sqrt(M2/C + eps); y = xhat*gamma + beta.
 // A row with a non-finite mean or variance is masked: y = 0, mean = rstd = 0.
-template <int DT, int W, int G, int NQ, bool AL, int MAXT, bool RMS>
+//
+// CL: the row is split over the K blocks of a thread-block cluster (one group
+// per block, G = block size); block k owns columns [k*slice, (k+1)*slice) and
+// the per-row statistics are merged across the cluster (ln_cluster).
+template <int DT, int W, int G, int NQ, bool AL, int MAXT, bool RMS, bool CL = false>
 __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
     ln_fwd_kernel(const LnFwdParams p, const LnGeo geo) {
   constexpr int E = DType<DT>::E;
   extern __shared__ __align__(128) unsigned char smem[];
+  int K = 1, rank = 0;
+  if constexpr (CL) {
+    K = static_cast<int>(cluster_nrank());
+    rank = static_cast<int>(cluster_rank());
+  }
+  // this block's columns: the whole row, or its slice of a clustered row
+  const int c0 = rank * geo.slice;
+  const int ncols = CL ? min(geo.slice, geo.cols - c0) : geo.cols;
+  const int nfull = CL ? ncols / W : geo.nfull;
+  const int rag = CL ? ncols - nfull * W : geo.rag;
+  const int nchb = CL ? nfull + (rag > 0 ? 1 : 0) : geo.nch;
+  const int64_t coff = (int64_t)c0 * E;
   const int npad = geo.nch * W;
   const int npl = W >= 4 ? geo.nch * 4 : geo.nch;
   const LnPlanes<W> sg{reinterpret_cast<float*>(smem), npl};
   const LnPlanes<W> sb{reinterpret_cast<float*>(smem) + npad, npl};
-  ln_stage<DT, W>(sg, p.gamma, geo.cols, geo.nch);
-  if constexpr (!RMS) ln_stage<DT, W>(sb, p.beta, geo.cols, geo.nch);
+  ln_stage<DT, W>(sg, p.gamma + coff, ncols, nchb);
+  if constexpr (!RMS) ln_stage<DT, W>(sb, p.beta + coff, ncols, nchb);
   __syncthreads();
 
   constexpr int ngroups = MAXT / G;
   const int grp = threadIdx.x / G, gt = threadIdx.x % G;
   LnCols<G, NQ> cs;
-  cs.init(gt, geo.nfull, geo.rag);
+  cs.init(gt, nfull, rag);
   LnRed<G> rd{smem + geo.red_off + grp * 1024, 0, 1 + grp};
-  const int64_t step = (int64_t)gridDim.x * ngroups;
-  const int64_t r0 = (int64_t)blockIdx.x * ngroups + grp;
+  int ccalls = 0;
+  const int64_t blk = blockIdx.x / K;  // the block's (cluster's) index among row owners
+  const int64_t step = (int64_t)(gridDim.x / K) * ngroups;
+  const int64_t r0 = blk * ngroups + grp;
   // first row of the warp's first group: sub-warp groups stay in lock step
-  const int64_t w0 = (int64_t)blockIdx.x * ngroups + (G < 32 ? (threadIdx.x & ~31) / G : grp);
+  const int64_t w0 = blk * ngroups + (G < 32 ? (threadIdx.x & ~31) / G : grp);
   const int64_t rowb = (int64_t)geo.cols * E;
+  const int64_t sbytes = (int64_t)ncols * E;
   const char* xend = p.x + geo.rows * rowb;
   const float ns = static_cast<float>(geo.cols);
 
@@ -357,7 +397,7 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
   auto issue = [&](int64_t rr, int stage) {
     if constexpr (PF) {
       if (rr < geo.rows) {
-        const char* x0 = p.x + rr * rowb;
+        const char* x0 = p.x + rr * rowb + coff;
 #pragma unroll
         for (int q = 0; q < NQ; ++q)
           if (q < cs.nf)
@@ -366,7 +406,7 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
       }
     } else if constexpr (PFR) {
       const bool valid = rr < geo.rows;
-      rpx.issue(valid ? p.x + rr * rowb : p.x, rowb, p.x, xend, stage, gt, valid);
+      rpx.issue(valid ? p.x + rr * rowb + coff : p.x, sbytes, p.x, xend, stage, gt, valid);
     }
     cp_async_commit();
   };
@@ -392,16 +432,16 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
       issue(r + step, (int)((it + 1) & 1));
       cp_async_wait<1>();
       group_sync();
-      if (!(active && rpx.get(v, (int)(it & 1), gt, cs, geo.rag))) {
+      if (!(active && rpx.get(v, (int)(it & 1), gt, cs, rag))) {
         if (active) {
-          ln_load<DT, W, G, NQ, AL>(v, p.x + r * rowb, gt, cs, geo.rag, p.x, xend);
+          ln_load<DT, W, G, NQ, AL>(v, p.x + r * rowb + coff, gt, cs, rag, p.x, xend);
         } else {
 #pragma unroll
           for (int q = 0; q < NQ; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
     } else if (active) {
-      ln_load<DT, W, G, NQ, AL>(v, p.x + r * rowb, gt, cs, geo.rag, p.x, xend);
+      ln_load<DT, W, G, NQ, AL>(v, p.x + r * rowb + coff, gt, cs, rag, p.x, xend);
     } else {
 #pragma unroll
       for (int q = 0; q < NQ; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
@@ -427,11 +467,13 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
           }
         }
       }
-      const float ms = rd(Sum1{a0 + a1}, MergeSum1()).s * p.inv_cols;
+      Sum1 t = rd(Sum1{a0 + a1}, MergeSum1());
+      if constexpr (CL) t = ln_cluster(t, MergeSum1(), smem + geo.cl_off, ccalls, K);
+      const float ms = t.s * p.inv_cols;
       if (!active) continue;
       masked = !isfinite(ms);
       rstd = masked ? 0.f : rsqrtf(ms + p.eps);
-      if (gt == 0) p.rstd[r] = rstd;
+      if (gt == 0 && rank == 0) p.rstd[r] = rstd;
     } else {
       // 1. compensated sum (two interleaved TwoSum accumulators per packed pair)
       float s0 = 0.f, s1 = 0.f, c0 = 0.f, c1 = 0.f;
@@ -468,6 +510,7 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
         S = {s, (c0 + c1) + e};
       }
       S = rd(S, MergeCasc());
+      if constexpr (CL) S = ln_cluster(S, MergeCasc(), smem + geo.cl_off, ccalls, K);
       {
         float sh, sl;
         two_sum(S.s, S.e, sh, sl);
@@ -487,8 +530,8 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
               add2(d0, d1, ln_get<DT, W>(v[q], e), ln_get<DT, W>(v[q], e + 1), -mh, -mh);
               add2(d0, d1, d0, d1, -ml, -ml);
               if (!whole) {
-                if (e >= geo.rag) d0 = 0.f;
-                if (e + 1 >= geo.rag) d1 = 0.f;
+                if (e >= rag) d0 = 0.f;
+                if (e + 1 >= rag) d1 = 0.f;
               }
               fma2(a0, a1, d0, d1, d0, d1, a0, a1);
             }
@@ -498,19 +541,21 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
           }
         }
       }
-      const float m2 = rd(Sum1{a0 + a1}, MergeSum1()).s;
+      Sum1 t = rd(Sum1{a0 + a1}, MergeSum1());
+      if constexpr (CL) t = ln_cluster(t, MergeSum1(), smem + geo.cl_off, ccalls, K);
+      const float m2 = t.s;
       if (!active) continue;
       const float var = m2 * p.inv_cols;
       masked = !(isfinite(mh) && isfinite(ml) && isfinite(var));
       rstd = masked ? 0.f : rsqrtf(var + p.eps);
-      if (gt == 0) {
+      if (gt == 0 && rank == 0) {
         p.mean[r] = masked ? 0.f : mh + ml;
         p.rstd[r] = rstd;
       }
     }
 
     // 3. y = ((x - mh) - ml) * rstd * gamma + beta  (RMSNorm: x * rstd * gamma)
-    char* yr = p.y + r * rowb;
+    char* yr = p.y + r * rowb + coff;
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
       if (q < cs.nown) {
@@ -547,11 +592,12 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
             f[0] = fmaf(((ln_get<DT, W>(v[q], 0) - mh) - ml) * rstd, gm[0], bt[0]);
           }
         }
-        ln_store<DT, W, G, NQ, AL>(yr, gt, q, cs, geo.rag, f);
+        ln_store<DT, W, G, NQ, AL>(yr, gt, q, cs, rag, f);
       }
     }
   }
   if constexpr (PF || PFR) cp_async_wait<0>();
+  if constexpr (CL) cluster_sync();  // peers may still read this block's slots
 }
 
 // ----------------------------------------------------------- backward ------
@@ -781,6 +827,14 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
 // Fills the variants G = 1 .. 1024 of one mode (block size max(256, G)
 // forward, max(512, G) backward; the backward stops at G = 512, beyond which a
 // 1024-thread block could not give a thread its 128 registers).
+// Clustered forward variants: one group of G = 256 / 512 / 1024 threads per block.
+template <int DT, int W, int NQ, bool AL, bool RMS>
+void ln_fill_cluster(const void* (&row)[3]) {
+  row[0] = (const void*)ln_fwd_kernel<DT, W, 256, NQ, AL, 256, RMS, true>;
+  row[1] = (const void*)ln_fwd_kernel<DT, W, 512, NQ, AL, 512, RMS, true>;
+  row[2] = (const void*)ln_fwd_kernel<DT, W, 1024, NQ, AL, 1024, RMS, true>;
+}
+
 template <int DT, int W, int NQ, bool AL, bool FWD, int G, bool RMS>
 const void* ln_variant() {
   if constexpr (FWD) {
@@ -823,7 +877,11 @@ LnKernelSet make_ln_set() {
   ln_fill_row<DT, V, NQC, true, FWD, RMS>(s.k[0]);
   ln_fill_row<DT, V, NQC, false, FWD, RMS>(s.k[1]);
   ln_fill_row<DT, 1, NQE, false, FWD, RMS>(s.k[2]);
-  if constexpr (!FWD) {
+  if constexpr (FWD) {
+    ln_fill_cluster<DT, V, NQC, true, RMS>(s.kc[0]);
+    ln_fill_cluster<DT, V, NQC, false, RMS>(s.kc[1]);
+    ln_fill_cluster<DT, 1, NQE, false, RMS>(s.kc[2]);
+  } else {
     ln_fill_row1<DT, V, true, RMS>(s.k1[0]);
     ln_fill_row1<DT, V, false, RMS>(s.k1[1]);
     ln_fill_row1<DT, 1, false, RMS>(s.k1[2]);

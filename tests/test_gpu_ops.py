@@ -92,7 +92,7 @@ def test_layernorm(cols, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("cols", [1, 31, 768, 1000, 4097, 16384])
+@pytest.mark.parametrize("cols", [1, 31, 768, 1000, 4097, 16384, 40000])
 @pytest.mark.parametrize("pad", [(1, 1, 1, 1, 1), (0, 0, 1, 0, 0), (0, 1, 0, 0, 1)])
 def test_layernorm_misaligned(cols, dtype, pad):
     x, g, b, dy = ln_case(rows_for(cols) // 2 + 1, cols, dtype, 600 + cols)

@@ -7,10 +7,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import row_reduction_pass_gb300 as rr
 from row_reduction_pass_gb300 import synth
 
-from parity import check_rms
+from parity import TOL, TOL_F32_OUT, check_rms, compare, empty_like_dev, host, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -48,13 +49,30 @@ def test_rmsnorm_chained_gpu_statistics(dtype):
     check_rms(x, g, dy, 1e-5, dtype, oracle_stats=False)
 
 
-def test_rmsnorm_rejects_rows_beyond_one_group():
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", [16385, 40000, 65537])
+@pytest.mark.parametrize("pad", [(0, 0, 0, 0, 0), (1, 1, 0, 0, 0), (0, 0, 1, 0, 0)])
+def test_rmsnorm_fwd_clustered_rows(cols, dtype, pad):
+    """Forward rows longer than one row group are split over a thread-block cluster."""
+    x, g, _ = case(64, cols, dtype, 990 + cols)
+    xd, gd = to_dev(x, pad[0]), to_dev(g, pad[2])
+    y = empty_like_dev(x.shape, dtype, pad[1])
+    rstd = torch.full((x.shape[0],), float("nan"), device="cuda")
+    rr.rr_rmsnorm_fwd(xd, gd, y, rstd, eps=1e-5)
+    torch.cuda.synchronize()
+    ry, rrstd = oracle.rms_fwd(x, g, 1e-5)
+    rtol, atol = TOL[dtype]
+    compare("rms y (clustered)", host(y), ry, rtol, atol)
+    compare("rms rstd (clustered)", host(rstd), rrstd, *TOL_F32_OUT)
+
+
+def test_rmsnorm_rejects_rows_beyond_its_kernels():
     dev = torch.device("cuda", 0)
-    x = torch.zeros(4, 16385, device=dev)
-    g = torch.ones(16385, device=dev)
+    x = torch.zeros(2, 300000, device=dev)          # beyond a cluster of 8 row groups
+    g = torch.ones(300000, device=dev)
     with pytest.raises(rr.RRError):
-        rr.rr_rmsnorm_fwd(x, g, torch.empty_like(x), torch.empty(4, device=dev))
-    x = torch.zeros(4, 8193, device=dev)
+        rr.rr_rmsnorm_fwd(x, g, torch.empty_like(x), torch.empty(2, device=dev))
+    x = torch.zeros(4, 8193, device=dev)             # the backward holds 8192 columns
     g = torch.ones(8193, device=dev)
     assert rr.rr_rmsnorm_bwd_workspace_size(4, 8193, torch.float32) == 0
     with pytest.raises(rr.RRError):
