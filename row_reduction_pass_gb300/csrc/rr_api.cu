@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -350,8 +351,9 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
 // Forward rows too long for one row group: the row is split over a cluster of K
 // blocks (K = 2 .. 8), each one group of 256 / 512 / 1024 threads holding a
 // slice of whole chunks (rr_ln.cuh, CL).  Among the (K, group size) pairs that
-// fit, the one with the least estimated time: rounds of rows (rows / clusters
-// resident on the device) x (chunks per thread + 2 for the per-row reductions).
+// fit: the wide 256-thread variant first, then the least estimated time, rounds
+// of rows (rows / clusters resident on the device) x (chunks per thread + 2 for
+// the per-row reductions).
 rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64_t cols, Plan* pl) {
   std::lock_guard<std::mutex> lock(g_mu);
   DevInfo* di = nullptr;
@@ -362,6 +364,10 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
   const int W = lmode == 2 ? 1 : 16 / E;
   const int nq = ls.nq[lmode];
   const int planes = op == kLnFwd ? 2 : 1;
+  // RR_LN_CLUSTER="K:v" forces cluster size K and variant v (0..3: 256, 512,
+  // 1024 threads, or the wide 256-thread one) when that pair fits (tuning aid).
+  int forceK = 0, forceV = -1;
+  if (const char* f = std::getenv("RR_LN_CLUSTER")) std::sscanf(f, "%d:%d", &forceK, &forceV);
   struct Choice {
     int K = 0, T = 0, ncl = 0;
     int64_t S = 0, nchs = 0, smem = 0, red_off = 0, cl_off = 0, pf_off = 0;
@@ -372,15 +378,18 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
     const int64_t S = round_up(cdiv(cols, K), W);
     if ((K - 1) * S >= cols) continue;  // every block of the cluster gets columns
     const int64_t nchs = S / W, npad = nchs * W;
-    for (int gi = 0; gi < 3; ++gi) {
-      const int T = 256 << gi;
+    if (forceK > 0 && K != forceK) continue;
+    for (int gi = 0; gi < 4; ++gi) {
+      if (forceV >= 0 && gi != forceV) continue;
+      const int T = gi < 3 ? 256 << gi : 256;
+      const int nqv = gi < 3 ? nq : 2 * nq;  // [3]: the wide 256-thread variant
       const void* fn = ls.kc[lmode][gi];
-      if (fn == nullptr || (int64_t)nq * T < nchs) continue;
+      if (fn == nullptr || (int64_t)nqv * T < nchs) continue;
       const int64_t red_off = round_up(planes * npad * 4, 16);
       const int64_t cl_off = round_up(red_off + 1024, 16);
       const int64_t pf_off = round_up(cl_off + 32, 16);
       int64_t pf_bytes = 0;
-      if (lmode == 0) pf_bytes = (int64_t)2 * nq * 16 * T;
+      if (lmode == 0) pf_bytes = (int64_t)2 * nqv * 16 * T;
       if (lmode == 1) pf_bytes = (int64_t)2 * (nchs + 2) * 16;
       const int64_t smem = pf_off + pf_bytes;
       if (smem > di->smem_optin) continue;
@@ -404,8 +413,11 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
         if (ncl <= 0) ncl = -1;  // cannot be resident: remembered, skipped
       }
       if (ncl <= 0) continue;
+      // measured on 65537-column rows: the wide variant (fewer, fuller threads:
+      // the per-row reductions are paid by half as many threads) beats the others
+      // wherever it fits, so it is ranked first; among equals, rounds x chunks
       const double rounds = (double)cdiv(rows, ncl);
-      const double cost = rounds * (double)(cdiv(nchs, T) + 2);
+      const double cost = rounds * (double)(cdiv(nchs, T) + 2) + (gi == 3 ? 0.0 : 1e9);
       if (best.K == 0 || cost < best.cost - 1e-9) {
         best.K = K;
         best.T = T;

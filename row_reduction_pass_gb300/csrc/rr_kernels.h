@@ -26,9 +26,10 @@ struct LnKernelSet {
   // One chunk per thread, G <= 32 (backward: fewer registers, so more warps
   // per SM for short rows); null where not built.
   const void* k1[3][kNumLnG];
-  // Forward rows split over a thread-block cluster, one group of 256 / 512 /
-  // 1024 threads per block; null where not built.
-  const void* kc[3][3];
+  // Forward rows split over a thread-block cluster: one group of 256 / 512 /
+  // 1024 threads per block with nq chunks per thread, and [3] a 256-thread
+  // group with 2 * nq; null where not built.
+  const void* kc[3][4];
 };
 
 KernelSet softmax_kernels_f32();

@@ -45,7 +45,9 @@ struct LnGeo {
 // Register sizes.  Forward: 64 per thread at any block size.  Backward: up to
 // 128 (a thread keeps g = dy*gamma, xhat and its two column accumulators), 64
 // for the one-chunk variants of short rows.
-template <int MAXT> constexpr int ln_fwd_min_blocks() { return 1024 / MAXT; }
+template <int MAXT, int NQ = 4> constexpr int ln_fwd_min_blocks() {
+  return NQ > 4 ? 2 : 1024 / MAXT;  // the wide cluster variant: 128 registers
+}
 template <int MAXT, int NQ> constexpr int ln_bwd_min_blocks() { return (NQ == 1 ? 1024 : 512) / MAXT; }
 
 // A sum carried as a leading float s and an accumulated error e (cascaded
@@ -347,7 +349,7 @@ __device__ __forceinline__ void ln_stage(const LnPlanes<W>& pl, const char* src,
 // per block, G = block size); block k owns columns [k*slice, (k+1)*slice) and
 // the per-row statistics are merged across the cluster (ln_cluster).
 template <int DT, int W, int G, int NQ, bool AL, int MAXT, bool RMS, bool CL = false>
-__global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT>())
+__global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT, NQ>())
     ln_fwd_kernel(const LnFwdParams p, const LnGeo geo) {
   constexpr int E = DType<DT>::E;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -827,12 +829,15 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
 // Fills the variants G = 1 .. 1024 of one mode (block size max(256, G)
 // forward, max(512, G) backward; the backward stops at G = 512, beyond which a
 // 1024-thread block could not give a thread its 128 registers).
-// Clustered forward variants: one group of G = 256 / 512 / 1024 threads per block.
+// Clustered forward variants: one group of G = 256 / 512 / 1024 threads per
+// block, and a 256-thread group holding twice the chunks per thread (fewer,
+// fuller threads per slice: the per-row reductions are paid over more values).
 template <int DT, int W, int NQ, bool AL, bool RMS>
-void ln_fill_cluster(const void* (&row)[3]) {
+void ln_fill_cluster(const void* (&row)[4]) {
   row[0] = (const void*)ln_fwd_kernel<DT, W, 256, NQ, AL, 256, RMS, true>;
   row[1] = (const void*)ln_fwd_kernel<DT, W, 512, NQ, AL, 512, RMS, true>;
   row[2] = (const void*)ln_fwd_kernel<DT, W, 1024, NQ, AL, 1024, RMS, true>;
+  row[3] = (const void*)ln_fwd_kernel<DT, W, 256, 2 * NQ, AL, 256, RMS, true>;
 }
 
 template <int DT, int W, int NQ, bool AL, bool FWD, int G, bool RMS>
