@@ -302,15 +302,13 @@ def run_ours(args, rank, world):
 
     # max over ranks
     if world > 1:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+        ms, e2e_ms = max_over_ranks([ms, e2e_ms], device=dev)
     if rank != 0:
         return None
 
     ms_step = ms / args.steps
     peak, peak_src = hbm_peak()
-    value = world * total_bytes / (ms_step * 1e-3) / 1e9
+    value = job_value(world, total_bytes, ms_step)
     x_ms = statistics.mean(per["xent"])
     x_gbs = nbytes["xent"] / (x_ms * 1e-3) / 1e9
     kernels = {}
@@ -343,7 +341,7 @@ def run_ours(args, rank, world):
                      "kernel": "row_kernel<OpSoftmaxXent bf16 chunks, staged> (xent 16384x50304)",
                      "peak_source": peak_src},
         "clocks": clk.summary(),
-        "e2e": {"value": round(world * total_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(job_value(world, total_bytes, e2e_ms), 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
@@ -379,6 +377,22 @@ def cpu_baseline(seconds: float):
     return {"value": round(nb / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"float64 C oracle, single thread, on {frac:.4%} of the rows of every "
                       f"workload of the step ({nb / 1e6:.1f} MB algorithmic) in {t:.2f} s"}
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of per-rank timings across the process group (every
+    rank calls it; the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_value(world, bytes_per_step, ms_per_step):
+    """Whole-job throughput in GB/s: every rank processes its own replica of the
+    step's bytes (weak scaling), in the slowest rank's time."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
 
 
 def run_reference(args, rank, world):
