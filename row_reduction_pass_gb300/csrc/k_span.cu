@@ -1,0 +1,16 @@
+// Short-row span variants of softmax, log-softmax and cross-entropy (fp32 and
+// bf16 storage).
+#include "rr_span.cuh"
+
+namespace rr {
+SpanKernelSet span_kernels() {
+  SpanKernelSet s{};
+  s.k[0][0] = (const void*)span_softmax_kernel<kF32, 0>;
+  s.k[0][1] = (const void*)span_softmax_kernel<kF32, 1>;
+  s.k[0][2] = (const void*)span_softmax_kernel<kF32, 2>;
+  s.k[1][0] = (const void*)span_softmax_kernel<kBF16, 0>;
+  s.k[1][1] = (const void*)span_softmax_kernel<kBF16, 1>;
+  s.k[1][2] = (const void*)span_softmax_kernel<kBF16, 2>;
+  return s;
+}
+}  // namespace rr

@@ -13,6 +13,7 @@
 #include "../../include/rr.h"
 #include "rr_kernels.h"
 #include "rr_ln.cuh"
+#include "rr_span.cuh"
 #include "rr_ops.cuh"
 
 namespace {
@@ -468,6 +469,53 @@ rr_status plan_any(OpKind op, rr_dtype dt, bool chunk_ok, bool head_free, int64_
   return make_plan(op, dt, 1, false, rows, cols, pl, max_partials);
 }
 
+// Short rows (cols * E <= 128 bytes, 16-byte aligned row tensors): the span
+// kernels (rr_span.cuh), one warp per span of 32 x rpl rows of ~3 KB.  mode 0
+// softmax, 1 log-softmax, 2 cross-entropy.  RR_ERR_INVALID_ARG when not eligible.
+rr_status span_launch(const rr::SoftmaxParams& p, rr_dtype dt, int mode, int64_t rows,
+                      int64_t cols, bool labels_aligned, cudaStream_t stream) {
+  const int E = dt == RR_BF16 ? 2 : 4;
+  if (cols * E > 128) return RR_ERR_INVALID_ARG;
+  const void* fn = nullptr;
+  int64_t smem = 0;
+  int64_t grid = 0;
+  rr::SpanGeo geo{};
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevInfo* di = nullptr;
+    rr_status st = device_info(&di);
+    if (st != RR_OK) return st;
+    static const rr::SpanKernelSet ks = rr::span_kernels();
+    fn = ks.k[dt][mode];
+    // ~3 KB of row data (and staged labels) per span: large enough per copy,
+    // small enough for 3-4 blocks (24-32 warps) per SM
+    int64_t rpl = 3072 / (32 * (cols * E + (mode == 2 ? 4 : 0)));
+    if (rpl < 1) rpl = 1;
+    const int64_t span_b = 32 * rpl * cols * E;  // a multiple of 16
+    const int64_t lab_b = (mode == 2 && labels_aligned) ? 32 * rpl * 4 : 0;
+    smem = (int64_t)rr::kSpanWarps * 2 * (span_b + lab_b);
+    if (smem > di->smem_optin) return RR_ERR_INVALID_ARG;
+    if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
+    const int T = 32 * rr::kSpanWarps;
+    int& occ = di->occ[{fn, ((long long)T << 32) | (long long)smem}];
+    if (occ == 0) {
+      cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, T, (size_t)smem);
+      if (e != cudaSuccess || occ <= 0)
+        return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+    }
+    const int64_t nspans = cdiv(rows, 32 * rpl);
+    grid = cdiv(nspans, rr::kSpanWarps);
+    if (grid > (int64_t)di->sms * occ) grid = (int64_t)di->sms * occ;
+    geo = rr::SpanGeo{rows, (int32_t)cols, (int32_t)rpl, (int32_t)span_b, (int32_t)lab_b};
+  }
+  rr::SoftmaxParams pc = p;
+  void* args[] = {&pc, &geo};
+  cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(32 * rr::kSpanWarps), args,
+                                   (size_t)smem, stream);
+  if (e != cudaSuccess) return fail(RR_ERR_CUDA, "span launch: %s", cudaGetErrorString(e));
+  return RR_OK;
+}
+
 template <class P>
 rr_status launch(const Plan& pl, const P& params, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -556,12 +604,16 @@ static rr_status softmax_fwd_impl(const void* x, void* y, int64_t rows, int64_t 
   if (x != y && overlaps(x, n, y, n)) return fail(RR_ERR_ALIASING, "x and y partially overlap");
   const bool same = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(y) & 15);
   const bool head_free = same && aligned(x, 16) && (cols * E) % 16 == 0;
-  Plan pl;
-  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
   int* err = device_error_word();
   if (!err) return RR_ERR_CUDA;
   rr::SoftmaxParams p{static_cast<const char*>(x), static_cast<char*>(y), nullptr, nullptr, nullptr,
                       err, cols, 0, log};
+  if (aligned(x, 16) && aligned(y, 16)) {
+    st = span_launch(p, dtype, log ? 1 : 0, rows, cols, false, stream);
+    if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
+  }
+  Plan pl;
+  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
   if ((st = launch(pl, p, stream)) != RR_OK) return st;
   return ok();
 }
@@ -639,12 +691,16 @@ rr_status rr_softmax_xent_fwd_bwd(const void* logits, const int32_t* labels, flo
   const bool same =
       (reinterpret_cast<uintptr_t>(logits) & 15) == (reinterpret_cast<uintptr_t>(dlogits) & 15);
   const bool head_free = same && aligned(logits, 16) && (cols * E) % 16 == 0;
-  Plan pl;
-  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
   int* err = device_error_word();
   if (!err) return RR_ERR_CUDA;
   rr::SoftmaxParams p{static_cast<const char*>(logits), static_cast<char*>(dlogits), labels, loss,
                       bad_label_count, err, cols, ignore_index};
+  if (aligned(logits, 16) && aligned(dlogits, 16)) {
+    st = span_launch(p, dtype, 2, rows, cols, aligned(labels, 16), stream);
+    if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
+  }
+  Plan pl;
+  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
   if ((st = launch(pl, p, stream)) != RR_OK) return st;
   return ok();
 }

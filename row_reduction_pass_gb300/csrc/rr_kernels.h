@@ -32,6 +32,13 @@ struct LnKernelSet {
   const void* kc[3][4];
 };
 
+// Short-row span kernels (rr_span.cuh): [dtype][mode], mode 0 softmax,
+// 1 log-softmax, 2 cross-entropy.
+struct SpanKernelSet {
+  const void* k[2][3];
+};
+SpanKernelSet span_kernels();
+
 KernelSet softmax_kernels_f32();
 KernelSet softmax_kernels_bf16();
 KernelSet softmax_bwd_kernels_f32();

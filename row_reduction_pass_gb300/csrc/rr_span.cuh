@@ -1,0 +1,165 @@
+// rr_span.cuh -- softmax, log-softmax and cross-entropy for short rows
+// (C x element size <= 128 bytes) as contiguous spans of rows per warp.
+//
+// With rows this short a row-group kernel moves only a few bytes per thread
+// per row, far too little in flight to cover DRAM latency.  Here each warp owns
+// a span of S = 32 x RPL consecutive rows (about 3 KB; a multiple of 16 bytes,
+// so spans start 16-byte aligned when the tensor does): its lanes copy the span
+// into the warp's shared-memory buffer with 16-byte cp.async copies, one span
+// ahead (two buffers), then lane l computes rows l, l + 32, ... of the span from
+// shared memory, writes each row's outputs back over its inputs, and the warp
+// stores the span out as 16-byte blocks.  Only warp-level synchronisation: no
+// block barrier.  The arithmetic of a row is the online normaliser of the row
+// engine (rr_ops.cuh, OpSoftmaxXent) done by one lane: max, sum of exp, output.
+#pragma once
+
+#include "rr_kernels.h"
+#include "rr_ops.cuh"
+
+namespace rr {
+
+struct SpanGeo {
+  int64_t rows;
+  int32_t cols;
+  int32_t rpl;      // rows per lane per span
+  int32_t span_b;   // bytes per span buffer (rows_per_span * cols * E, a multiple of 16)
+  int32_t lab_b;    // cross-entropy with 16-byte aligned labels: label bytes per span, else 0
+};
+
+constexpr int kSpanWarps = 8;  // warps per block
+
+template <int DT>
+__device__ __forceinline__ float span_ld(const unsigned char* s, int i) {
+  if constexpr (DT == kF32) return reinterpret_cast<const float*>(s)[i];
+  else return bf16_bits_to_f32(reinterpret_cast<const unsigned short*>(s)[i]);
+}
+template <int DT>
+__device__ __forceinline__ void span_st(unsigned char* s, int i, float f) {
+  if constexpr (DT == kF32) reinterpret_cast<float*>(s)[i] = f;
+  else reinterpret_cast<unsigned short*>(s)[i] = f32_to_bf16_bits(f);
+}
+
+// MODE 0: softmax, 1: log-softmax, 2: cross-entropy (loss, dlogits).
+template <int DT, int MODE>
+__global__ void __launch_bounds__(32 * kSpanWarps)
+    span_softmax_kernel(const SoftmaxParams p, const SpanGeo geo) {
+  constexpr int E = DType<DT>::E;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int C = geo.cols;
+  const int rps = 32 * geo.rpl;  // rows per span
+  const int64_t nspans = (geo.rows + rps - 1) / rps;
+  const int64_t gw = (int64_t)blockIdx.x * kSpanWarps + warp;
+  const int64_t nw = (int64_t)gridDim.x * kSpanWarps;
+  unsigned char* buf = smem + (size_t)warp * 2 * geo.span_b;
+  // staged labels (cross-entropy): [warps][2 stages][rows per span] int32
+  int32_t* lbuf = reinterpret_cast<int32_t*>(smem + (size_t)kSpanWarps * 2 * geo.span_b +
+                                             (size_t)warp * 2 * geo.lab_b);
+  const int64_t rowb = (int64_t)C * E;
+  const int64_t total = geo.rows * rowb;
+
+  // bytes of span s: [s * span_b, min(.., total)); whole 16-byte blocks by
+  // cp.async, the ragged end of the tensor's last span element by element
+  auto span_bytes = [&](int64_t s) -> int64_t {
+    const int64_t b0 = s * geo.span_b;
+    const int64_t b1 = b0 + geo.span_b < total ? b0 + geo.span_b : total;
+    return b1 - b0;
+  };
+  auto issue = [&](int64_t s, int stage) {
+    if (s < nspans) {
+      const int64_t nb = span_bytes(s);
+      const char* src = p.x + s * geo.span_b;
+      unsigned char* dst = buf + stage * geo.span_b;
+      for (int64_t j = lane; j < nb / 16; j += 32) cp_async16(dst + 16 * j, src + 16 * j);
+      if (MODE == 2 && geo.lab_b > 0) {
+        // the span's labels: whole 16-byte blocks (4 rows each); a last span's
+        // ragged rows are read directly
+        const int64_t r0 = s * rps;
+        const int64_t nr = geo.rows - r0 < rps ? geo.rows - r0 : rps;
+        const int32_t* lsrc = p.labels + r0;
+        int32_t* ldst = lbuf + stage * (geo.lab_b / 4);
+        for (int64_t j = lane; j < nr / 4; j += 32) cp_async16(ldst + 4 * j, lsrc + 4 * j);
+      }
+    }
+    cp_async_commit();
+  };
+
+  issue(gw, 0);
+  for (int64_t it = 0;; ++it) {
+    const int64_t s = gw + it * nw;
+    if (s >= nspans) break;
+    const int stage = (int)(it & 1);
+    unsigned char* sb = buf + stage * geo.span_b;
+    const int64_t r0 = s * rps;
+    const int nrows = (int)(geo.rows - r0 < rps ? geo.rows - r0 : rps);
+    issue(s + nw, stage ^ 1);
+    cp_async_wait<1>();
+    const int64_t nb = span_bytes(s);
+    if (lane == 0)
+      for (int64_t b = nb & ~int64_t(15); b < nb; b += E)
+        span_st<DT>(sb, (int)(b / E), ld_elem<DT>(p.x + s * geo.span_b + b));
+    __syncwarp();
+
+    for (int k = 0; k < geo.rpl; ++k) {
+      const int i = lane + 32 * k;
+      if (i >= nrows) break;
+      const int base = i * C;
+      float m = -INFINITY;
+      for (int j = 0; j < C; ++j) m = fmaxf(m, span_ld<DT>(sb, base + j));
+      const int64_t r = r0 + i;
+      bool skip = false;
+      int32_t label = -1;
+      if constexpr (MODE == 2) {
+        label = (geo.lab_b > 0 && i < (nrows & ~3)) ? lbuf[stage * (geo.lab_b / 4) + i]
+                                                      : __ldg(p.labels + r);
+        skip = label == p.ignore;
+        const bool in_range = label >= 0 && label < C;
+        if (!skip && !in_range && p.bad != nullptr) atomicAdd(p.bad, 1);
+        if (skip || m == -INFINITY) {
+          p.loss[r] = 0.f;
+        } else if (!in_range) {
+          p.loss[r] = __int_as_float(0x7fc00000);
+        }
+      }
+      if (skip || m == -INFINITY) {
+        for (int j = 0; j < C; ++j) span_st<DT>(sb, base + j, 0.f);
+        continue;
+      }
+      // d = sum exp(x - m) as sum 2^(x log2e - fl(m log2e)) * 2^(-r), r the
+      // rounding residual of fl(m log2e)
+      const float mL = m * kLog2e;
+      const float rr = fmaf(m, kLog2e, -mL);
+      float d = 0.f;
+      for (int j = 0; j < C; ++j) d += ex2(fmaf(span_ld<DT>(sb, base + j), kLog2e, -mL));
+      d *= ex2(-rr);
+      if constexpr (MODE == 1) {
+        const float lnd = logf(d);
+        for (int j = 0; j < C; ++j)
+          span_st<DT>(sb, base + j, (span_ld<DT>(sb, base + j) - m) - lnd);
+      } else {
+        if constexpr (MODE == 2) {
+          if (label >= 0 && label < C)
+            p.loss[r] = (m - span_ld<DT>(sb, base + label)) + logf(d);
+        }
+        const float inv = ex2(-rr) / d;
+        for (int j = 0; j < C; ++j) {
+          float f = ex2(fmaf(span_ld<DT>(sb, base + j), kLog2e, -mL)) * inv;
+          if (MODE == 2 && j == label) f -= 1.0f;
+          span_st<DT>(sb, base + j, f);
+        }
+      }
+    }
+    __syncwarp();
+    // the span out: whole blocks as 16-byte stores, the ragged end by lane 0
+    char* dst = p.y + s * geo.span_b;
+    for (int64_t j = lane; j < nb / 16; j += 32)
+      st_chunk_stream(dst + 16 * j, *reinterpret_cast<const uint4*>(sb + 16 * j));
+    if (lane == 0)
+      for (int64_t b = nb & ~int64_t(15); b < nb; b += E)
+        st_elem<DT>(dst + b, span_ld<DT>(sb, (int)(b / E)));
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+}
+
+}  // namespace rr
