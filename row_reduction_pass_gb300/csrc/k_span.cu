@@ -1,5 +1,5 @@
-// Short-row span variants of softmax, log-softmax and cross-entropy (fp32 and
-// bf16 storage).
+// Short-row span variants of softmax, log-softmax, cross-entropy and the
+// softmax / log-softmax backward (fp32 and bf16 storage).
 #include "rr_span.cuh"
 
 namespace rr {
@@ -11,6 +11,10 @@ SpanKernelSet span_kernels() {
   s.k[1][0] = (const void*)span_softmax_kernel<kBF16, 0>;
   s.k[1][1] = (const void*)span_softmax_kernel<kBF16, 1>;
   s.k[1][2] = (const void*)span_softmax_kernel<kBF16, 2>;
+  s.k[0][3] = (const void*)span_softmax_bwd_kernel<kF32, false>;
+  s.k[0][4] = (const void*)span_softmax_bwd_kernel<kF32, true>;
+  s.k[1][3] = (const void*)span_softmax_bwd_kernel<kBF16, false>;
+  s.k[1][4] = (const void*)span_softmax_bwd_kernel<kBF16, true>;
   return s;
 }
 }  // namespace rr

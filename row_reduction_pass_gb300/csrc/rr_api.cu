@@ -472,8 +472,9 @@ rr_status plan_any(OpKind op, rr_dtype dt, bool chunk_ok, bool head_free, int64_
 // Short rows (cols * E <= 128 bytes, 16-byte aligned row tensors): the span
 // kernels (rr_span.cuh), one warp per span of 32 x rpl rows of ~3 KB.  mode 0
 // softmax, 1 log-softmax, 2 cross-entropy.  RR_ERR_INVALID_ARG when not eligible.
-rr_status span_launch(const rr::SoftmaxParams& p, rr_dtype dt, int mode, int64_t rows,
-                      int64_t cols, bool labels_aligned, cudaStream_t stream) {
+template <class P>
+rr_status span_launch(const P& p, rr_dtype dt, int mode, int64_t rows, int64_t cols,
+                      bool labels_aligned, cudaStream_t stream) {
   const int E = dt == RR_BF16 ? 2 : 4;
   if (cols * E > 128) return RR_ERR_INVALID_ARG;
   const void* fn = nullptr;
@@ -489,11 +490,12 @@ rr_status span_launch(const rr::SoftmaxParams& p, rr_dtype dt, int mode, int64_t
     fn = ks.k[dt][mode];
     // ~3 KB of row data (and staged labels) per span: large enough per copy,
     // small enough for 3-4 blocks (24-32 warps) per SM
-    int64_t rpl = 3072 / (32 * (cols * E + (mode == 2 ? 4 : 0)));
+    const int ntens = mode >= 3 ? 2 : 1;  // the backward passes read two row tensors
+    int64_t rpl = 3072 / (32 * (ntens * cols * E + (mode == 2 ? 4 : 0)));
     if (rpl < 1) rpl = 1;
     const int64_t span_b = 32 * rpl * cols * E;  // a multiple of 16
     const int64_t lab_b = (mode == 2 && labels_aligned) ? 32 * rpl * 4 : 0;
-    smem = (int64_t)rr::kSpanWarps * 2 * (span_b + lab_b);
+    smem = (int64_t)rr::kSpanWarps * 2 * (ntens * span_b + lab_b);
     if (smem > di->smem_optin) return RR_ERR_INVALID_ARG;
     if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
     const int T = 32 * rr::kSpanWarps;
@@ -508,7 +510,7 @@ rr_status span_launch(const rr::SoftmaxParams& p, rr_dtype dt, int mode, int64_t
     if (grid > (int64_t)di->sms * occ) grid = (int64_t)di->sms * occ;
     geo = rr::SpanGeo{rows, (int32_t)cols, (int32_t)rpl, (int32_t)span_b, (int32_t)lab_b};
   }
-  rr::SoftmaxParams pc = p;
+  P pc = p;
   void* args[] = {&pc, &geo};
   cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(32 * rr::kSpanWarps), args,
                                    (size_t)smem, stream);
@@ -648,12 +650,16 @@ static rr_status softmax_bwd_impl(const void* y, const void* dy, void* dx, int64
   const bool same = a == (reinterpret_cast<uintptr_t>(dy) & 15) &&
                     a == (reinterpret_cast<uintptr_t>(dx) & 15);
   const bool head_free = same && a == 0 && (cols * E) % 16 == 0;
-  Plan pl;
-  if ((st = plan_any(kSoftmaxBwd, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
   int* err = device_error_word();
   if (!err) return RR_ERR_CUDA;
   rr::SoftmaxBwdParams p{static_cast<const char*>(y), static_cast<const char*>(dy),
                          static_cast<char*>(dx), err, cols, log};
+  if (same && a == 0) {
+    st = span_launch(p, dtype, log ? 4 : 3, rows, cols, false, stream);
+    if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
+  }
+  Plan pl;
+  if ((st = plan_any(kSoftmaxBwd, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
   if ((st = launch(pl, p, stream)) != RR_OK) return st;
   return ok();
 }

@@ -33,9 +33,9 @@ struct LnKernelSet {
 };
 
 // Short-row span kernels (rr_span.cuh): [dtype][mode], mode 0 softmax,
-// 1 log-softmax, 2 cross-entropy.
+// 1 log-softmax, 2 cross-entropy, 3 softmax backward, 4 log-softmax backward.
 struct SpanKernelSet {
-  const void* k[2][3];
+  const void* k[2][5];
 };
 SpanKernelSet span_kernels();
 

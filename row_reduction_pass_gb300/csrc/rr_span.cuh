@@ -162,4 +162,84 @@ __global__ void __launch_bounds__(32 * kSpanWarps)
   cp_async_wait<0>();
 }
 
+// Softmax (LOG = false: y, dy) or log-softmax (LOG = true: z, dz) backward of
+// short rows, spans as above with two input buffers per stage; dx is written
+// over the dy buffer and stored out.  Per row: S = sum y*dy (or sum dz), then
+// dx = y * (dy - S) (or dz - exp(z) * S), as OpSoftmaxBwd in rr_ops.cuh.
+template <int DT, bool LOG>
+__global__ void __launch_bounds__(32 * kSpanWarps)
+    span_softmax_bwd_kernel(const SoftmaxBwdParams p, const SpanGeo geo) {
+  constexpr int E = DType<DT>::E;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int C = geo.cols;
+  const int rps = 32 * geo.rpl;
+  const int64_t nspans = (geo.rows + rps - 1) / rps;
+  const int64_t gw = (int64_t)blockIdx.x * kSpanWarps + warp;
+  const int64_t nw = (int64_t)gridDim.x * kSpanWarps;
+  unsigned char* buf = smem + (size_t)warp * 4 * geo.span_b;  // [stage][y | dy]
+  const int64_t total = geo.rows * (int64_t)C * E;
+  auto span_bytes = [&](int64_t s) -> int64_t {
+    const int64_t b0 = s * geo.span_b;
+    const int64_t b1 = b0 + geo.span_b < total ? b0 + geo.span_b : total;
+    return b1 - b0;
+  };
+  auto issue = [&](int64_t s, int stage) {
+    if (s < nspans) {
+      const int64_t nb = span_bytes(s);
+      unsigned char* d0 = buf + (2 * stage) * geo.span_b;
+      unsigned char* d1 = d0 + geo.span_b;
+      const char* s0 = p.y + s * geo.span_b;
+      const char* s1 = p.dy + s * geo.span_b;
+      for (int64_t j = lane; j < nb / 16; j += 32) {
+        cp_async16(d0 + 16 * j, s0 + 16 * j);
+        cp_async16(d1 + 16 * j, s1 + 16 * j);
+      }
+    }
+    cp_async_commit();
+  };
+
+  issue(gw, 0);
+  for (int64_t it = 0;; ++it) {
+    const int64_t s = gw + it * nw;
+    if (s >= nspans) break;
+    const int stage = (int)(it & 1);
+    unsigned char* yb = buf + (2 * stage) * geo.span_b;
+    unsigned char* gb = yb + geo.span_b;
+    const int64_t r0 = s * rps;
+    const int nrows = (int)(geo.rows - r0 < rps ? geo.rows - r0 : rps);
+    issue(s + nw, stage ^ 1);
+    cp_async_wait<1>();
+    const int64_t nb = span_bytes(s);
+    if (lane == 0)
+      for (int64_t b = nb & ~int64_t(15); b < nb; b += E) {
+        span_st<DT>(yb, (int)(b / E), ld_elem<DT>(p.y + s * geo.span_b + b));
+        span_st<DT>(gb, (int)(b / E), ld_elem<DT>(p.dy + s * geo.span_b + b));
+      }
+    __syncwarp();
+    for (int k = 0; k < geo.rpl; ++k) {
+      const int i = lane + 32 * k;
+      if (i >= nrows) break;
+      const int base = i * C;
+      float S = 0.f;
+      for (int j = 0; j < C; ++j)
+        S = LOG ? S + span_ld<DT>(gb, base + j)
+                : fmaf(span_ld<DT>(yb, base + j), span_ld<DT>(gb, base + j), S);
+      for (int j = 0; j < C; ++j) {
+        const float yv = span_ld<DT>(yb, base + j), gv = span_ld<DT>(gb, base + j);
+        span_st<DT>(gb, base + j, LOG ? fmaf(ex2(yv * kLog2e), -S, gv) : yv * (gv - S));
+      }
+    }
+    __syncwarp();
+    char* dst = p.dx + s * geo.span_b;
+    for (int64_t j = lane; j < nb / 16; j += 32)
+      st_chunk_stream(dst + 16 * j, *reinterpret_cast<const uint4*>(gb + 16 * j));
+    if (lane == 0)
+      for (int64_t b = nb & ~int64_t(15); b < nb; b += E)
+        st_elem<DT>(dst + b, span_ld<DT>(gb, (int)(b / E)));
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+}
+
 }  // namespace rr
