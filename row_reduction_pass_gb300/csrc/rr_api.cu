@@ -496,6 +496,7 @@ rr_status span_launch(const P& p, rr_dtype dt, int mode, int64_t rows, int64_t c
     const int64_t span_b = 32 * rpl * cols * E;  // a multiple of 16
     const int64_t lab_b = (mode == 2 && labels_aligned) ? 32 * rpl * 4 : 0;
     smem = (int64_t)rr::kSpanWarps * 2 * (ntens * span_b + lab_b);
+    if (mode >= 5) smem += round_up(2 * cols * 4, 16);  // gamma, beta as fp32
     if (smem > di->smem_optin) return RR_ERR_INVALID_ARG;
     if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
     const int T = 32 * rr::kSpanWarps;
@@ -735,6 +736,17 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
   const bool rows_al = (cols * (int64_t)E) % 16 == 0 && aligned(x, 16) && aligned(y, 16);
   Plan pl;
   const int lmode = al ? (rows_al ? 0 : 1) : 2;
+  {
+    int* err = device_error_word();
+    if (!err) return RR_ERR_CUDA;
+    rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma),
+                      static_cast<const char*>(beta), static_cast<char*>(y), mean, rstd, err, cols,
+                      eps, static_cast<float>(1.0 / static_cast<double>(cols))};
+    if (aligned(x, 16) && aligned(y, 16)) {
+      st = span_launch(p, dtype, 5, rows, cols, false, stream);
+      if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
+    }
+  }
   st = ln_rowgroup_plan(kLnFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
   if (st == RR_ERR_INVALID_ARG) st = ln_cluster_plan(kLnFwd, dtype, lmode, rows, cols, &pl);
   if (st == RR_ERR_INVALID_ARG) st = plan_any(kLnFwd, dtype, al, true, rows, cols, &pl);
@@ -767,6 +779,17 @@ rr_status rr_rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
   const bool rows_al = (cols * (int64_t)E) % 16 == 0 && aligned(x, 16) && aligned(y, 16);
   Plan pl;
   const int lmode = al ? (rows_al ? 0 : 1) : 2;
+  {
+    int* err = device_error_word();
+    if (!err) return RR_ERR_CUDA;
+    rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma), nullptr,
+                      static_cast<char*>(y), nullptr, rstd, err, cols, eps,
+                      static_cast<float>(1.0 / static_cast<double>(cols))};
+    if (aligned(x, 16) && aligned(y, 16)) {
+      st = span_launch(p, dtype, 6, rows, cols, false, stream);
+      if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
+    }
+  }
   st = ln_rowgroup_plan(kRmsFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
   if (st == RR_ERR_INVALID_ARG) st = ln_cluster_plan(kRmsFwd, dtype, lmode, rows, cols, &pl);
   if (st == RR_ERR_INVALID_ARG)

@@ -33,9 +33,10 @@ struct LnKernelSet {
 };
 
 // Short-row span kernels (rr_span.cuh): [dtype][mode], mode 0 softmax,
-// 1 log-softmax, 2 cross-entropy, 3 softmax backward, 4 log-softmax backward.
+// 1 log-softmax, 2 cross-entropy, 3 softmax backward, 4 log-softmax backward,
+// 5 LayerNorm forward, 6 RMSNorm forward.
 struct SpanKernelSet {
-  const void* k[2][5];
+  const void* k[2][7];
 };
 SpanKernelSet span_kernels();
 

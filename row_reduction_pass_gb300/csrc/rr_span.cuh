@@ -242,4 +242,116 @@ __global__ void __launch_bounds__(32 * kSpanWarps)
   cp_async_wait<0>();
 }
 
+// LayerNorm (RMS = false) or RMSNorm forward of short rows, spans as above.
+// One lane owns a whole row, so no reduction across threads: a compensated
+// (TwoSum) sum gives the exact mean (mh + ml), then M2 about it (RMSNorm: the
+// plain sum of squares), as ln_fwd_kernel in rr_ln.cuh.  gamma / beta are
+// converted to fp32 once per block into shared memory after the span buffers.
+template <int DT, bool RMS>
+__global__ void __launch_bounds__(32 * kSpanWarps)
+    span_ln_fwd_kernel(const LnFwdParams p, const SpanGeo geo) {
+  constexpr int E = DType<DT>::E;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int C = geo.cols;
+  const int rps = 32 * geo.rpl;
+  const int64_t nspans = (geo.rows + rps - 1) / rps;
+  const int64_t gw = (int64_t)blockIdx.x * kSpanWarps + warp;
+  const int64_t nw = (int64_t)gridDim.x * kSpanWarps;
+  unsigned char* buf = smem + (size_t)warp * 2 * geo.span_b;
+  float* sg = reinterpret_cast<float*>(smem + (size_t)kSpanWarps * 2 * geo.span_b);
+  float* sbeta = sg + C;
+  for (int j = threadIdx.x; j < C; j += blockDim.x) {
+    sg[j] = ld_elem_cached<DT>(p.gamma + (int64_t)j * E);
+    if constexpr (!RMS) sbeta[j] = ld_elem_cached<DT>(p.beta + (int64_t)j * E);
+  }
+  __syncthreads();
+  const int64_t total = geo.rows * (int64_t)C * E;
+  const float ns = static_cast<float>(C);
+  auto span_bytes = [&](int64_t s) -> int64_t {
+    const int64_t b0 = s * geo.span_b;
+    const int64_t b1 = b0 + geo.span_b < total ? b0 + geo.span_b : total;
+    return b1 - b0;
+  };
+  auto issue = [&](int64_t s, int stage) {
+    if (s < nspans) {
+      const int64_t nb = span_bytes(s);
+      const char* src = p.x + s * geo.span_b;
+      unsigned char* dst = buf + stage * geo.span_b;
+      for (int64_t j = lane; j < nb / 16; j += 32) cp_async16(dst + 16 * j, src + 16 * j);
+    }
+    cp_async_commit();
+  };
+
+  issue(gw, 0);
+  for (int64_t it = 0;; ++it) {
+    const int64_t s = gw + it * nw;
+    if (s >= nspans) break;
+    const int stage = (int)(it & 1);
+    unsigned char* sb = buf + stage * geo.span_b;
+    const int64_t r0 = s * rps;
+    const int nrows = (int)(geo.rows - r0 < rps ? geo.rows - r0 : rps);
+    issue(s + nw, stage ^ 1);
+    cp_async_wait<1>();
+    const int64_t nb = span_bytes(s);
+    if (lane == 0)
+      for (int64_t b = nb & ~int64_t(15); b < nb; b += E)
+        span_st<DT>(sb, (int)(b / E), ld_elem<DT>(p.x + s * geo.span_b + b));
+    __syncwarp();
+    for (int k = 0; k < geo.rpl; ++k) {
+      const int i = lane + 32 * k;
+      if (i >= nrows) break;
+      const int base = i * C;
+      const int64_t r = r0 + i;
+      float mh = 0.f, ml = 0.f, var;
+      if constexpr (RMS) {
+        float a = 0.f;
+        for (int j = 0; j < C; ++j) {
+          const float v = span_ld<DT>(sb, base + j);
+          a = fmaf(v, v, a);
+        }
+        var = a * p.inv_cols;
+      } else {
+        float sum = 0.f, c = 0.f;
+        for (int j = 0; j < C; ++j) {
+          float t, e;
+          two_sum(sum, span_ld<DT>(sb, base + j), t, e);
+          sum = t;
+          c += e;
+        }
+        float sh, sl;
+        two_sum(sum, c, sh, sl);
+        df_mean(sh, sl, ns, p.inv_cols, mh, ml);
+        float a = 0.f;
+        for (int j = 0; j < C; ++j) {
+          const float d = (span_ld<DT>(sb, base + j) - mh) - ml;
+          a = fmaf(d, d, a);
+        }
+        var = a * p.inv_cols;
+      }
+      const bool masked = RMS ? !isfinite(var) : !(isfinite(mh) && isfinite(ml) && isfinite(var));
+      const float rstd = masked ? 0.f : rsqrtf(var + p.eps);
+      if constexpr (!RMS) p.mean[r] = masked ? 0.f : mh + ml;
+      p.rstd[r] = rstd;
+      for (int j = 0; j < C; ++j) {
+        float f = 0.f;
+        if (!masked) {
+          const float v = span_ld<DT>(sb, base + j);
+          f = RMS ? (v * rstd) * sg[j] : fmaf(((v - mh) - ml) * rstd, sg[j], sbeta[j]);
+        }
+        span_st<DT>(sb, base + j, f);
+      }
+    }
+    __syncwarp();
+    char* dst = p.y + s * geo.span_b;
+    for (int64_t j = lane; j < nb / 16; j += 32)
+      st_chunk_stream(dst + 16 * j, *reinterpret_cast<const uint4*>(sb + 16 * j));
+    if (lane == 0)
+      for (int64_t b = nb & ~int64_t(15); b < nb; b += E)
+        st_elem<DT>(dst + b, span_ld<DT>(sb, (int)(b / E)));
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+}
+
 }  // namespace rr
