@@ -1,6 +1,6 @@
 // Short-row span variants of softmax, log-softmax, cross-entropy and the
-// softmax / log-softmax backward, and the LayerNorm / RMSNorm forward (fp32
-// and bf16 storage).
+// softmax / log-softmax backward, and the LayerNorm / RMSNorm forward and
+// backward (fp32 and bf16 storage).
 #include "rr_span.cuh"
 
 namespace rr {
@@ -20,6 +20,10 @@ SpanKernelSet span_kernels() {
   s.k[0][6] = (const void*)span_ln_fwd_kernel<kF32, true>;
   s.k[1][5] = (const void*)span_ln_fwd_kernel<kBF16, false>;
   s.k[1][6] = (const void*)span_ln_fwd_kernel<kBF16, true>;
+  s.k[0][7] = (const void*)span_ln_bwd_kernel<kF32, false>;
+  s.k[0][8] = (const void*)span_ln_bwd_kernel<kF32, true>;
+  s.k[1][7] = (const void*)span_ln_bwd_kernel<kBF16, false>;
+  s.k[1][8] = (const void*)span_ln_bwd_kernel<kBF16, true>;
   return s;
 }
 }  // namespace rr

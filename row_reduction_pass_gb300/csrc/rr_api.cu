@@ -469,54 +469,84 @@ rr_status plan_any(OpKind op, rr_dtype dt, bool chunk_ok, bool head_free, int64_
   return make_plan(op, dt, 1, false, rows, cols, pl, max_partials);
 }
 
-// Short rows (cols * E <= 128 bytes, 16-byte aligned row tensors): the span
+// Short rows (cols * E <= 128 bytes, 64 for the norm backward; 16-byte aligned
+// row tensors): the span
 // kernels (rr_span.cuh), one warp per span of 32 x rpl rows of ~3 KB.  mode 0
-// softmax, 1 log-softmax, 2 cross-entropy.  RR_ERR_INVALID_ARG when not eligible.
-template <class P>
-rr_status span_launch(const P& p, rr_dtype dt, int mode, int64_t rows, int64_t cols,
-                      bool labels_aligned, cudaStream_t stream) {
-  const int E = dt == RR_BF16 ? 2 : 4;
-  if (cols * E > 128) return RR_ERR_INVALID_ARG;
+// softmax, 1 log-softmax, 2 cross-entropy, 3 softmax backward, 4 log-softmax
+// backward, 5 LayerNorm forward, 6 RMSNorm forward, 7 LayerNorm backward,
+// 8 RMSNorm backward.  aux_aligned: the labels (mode 2) or the row statistics
+// (modes 7, 8) are 16-byte aligned and staged with the span.  The grid is at
+// most max_grid blocks (the norm backward writes one column partial per block).
+// RR_ERR_INVALID_ARG when not eligible.
+struct SpanPlan {
   const void* fn = nullptr;
-  int64_t smem = 0;
-  int64_t grid = 0;
+  int64_t smem = 0, grid = 0;
   rr::SpanGeo geo{};
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    DevInfo* di = nullptr;
-    rr_status st = device_info(&di);
-    if (st != RR_OK) return st;
-    static const rr::SpanKernelSet ks = rr::span_kernels();
-    fn = ks.k[dt][mode];
-    // ~3 KB of row data (and staged labels) per span: large enough per copy,
-    // small enough for 3-4 blocks (24-32 warps) per SM
-    const int ntens = mode >= 3 ? 2 : 1;  // the backward passes read two row tensors
-    int64_t rpl = 3072 / (32 * (ntens * cols * E + (mode == 2 ? 4 : 0)));
-    if (rpl < 1) rpl = 1;
-    const int64_t span_b = 32 * rpl * cols * E;  // a multiple of 16
-    const int64_t lab_b = (mode == 2 && labels_aligned) ? 32 * rpl * 4 : 0;
-    smem = (int64_t)rr::kSpanWarps * 2 * (ntens * span_b + lab_b);
-    if (mode >= 5) smem += round_up(2 * cols * 4, 16);  // gamma, beta as fp32
-    if (smem > di->smem_optin) return RR_ERR_INVALID_ARG;
-    if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
-    const int T = 32 * rr::kSpanWarps;
-    int& occ = di->occ[{fn, ((long long)T << 32) | (long long)smem}];
-    if (occ == 0) {
-      cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, T, (size_t)smem);
-      if (e != cudaSuccess || occ <= 0)
-        return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
-    }
-    const int64_t nspans = cdiv(rows, 32 * rpl);
-    grid = cdiv(nspans, rr::kSpanWarps);
-    if (grid > (int64_t)di->sms * occ) grid = (int64_t)di->sms * occ;
-    geo = rr::SpanGeo{rows, (int32_t)cols, (int32_t)rpl, (int32_t)span_b, (int32_t)lab_b};
+};
+
+static rr_status span_plan(rr_dtype dt, int mode, int64_t rows, int64_t cols, bool aux_aligned,
+                           int64_t max_grid, SpanPlan* sp) {
+  const int E = dt == RR_BF16 ? 2 : 4;
+  // the norm backward's spans hold two tensors: rows of up to 64 bytes
+  if (cols * E > (mode >= 7 ? 64 : 128) || rows <= 0 || max_grid < 1) return RR_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo* di = nullptr;
+  rr_status st = device_info(&di);
+  if (st != RR_OK) return st;
+  static const rr::SpanKernelSet ks = rr::span_kernels();
+  sp->fn = ks.k[dt][mode];
+  // ~3 KB of row data (and staged labels or statistics) per span: large enough
+  // per copy, small enough for 3-4 blocks (24-32 warps) per SM
+  const bool two = mode == 3 || mode == 4 || mode >= 7;  // two row tensors in
+  const int ntens = two ? 2 : 1;
+  const int aux = mode == 2 ? 4 : mode >= 7 ? 8 : 0;  // label or statistics bytes per row
+  int64_t rpl = 3072 / (32 * (ntens * cols * E + aux));
+  if (rpl < 1) rpl = 1;
+  const int64_t span_b = 32 * rpl * cols * E;  // a multiple of 16
+  int64_t lab_b = (mode == 2 && aux_aligned) ? 32 * rpl * 4 : 0;
+  if (mode >= 7) lab_b = 32 * rpl * 4;  // the statistics buffer is always there
+  const int nstat = mode >= 7 ? 2 : 1;
+  int64_t smem = (int64_t)rr::kSpanWarps * 2 * (ntens * span_b + nstat * lab_b);
+  if (mode == 5 || mode == 6) smem += round_up(2 * cols * 4, 16);  // gamma, beta as fp32
+  if (mode >= 7) smem += round_up(cols * 4, 16);                   // gamma as fp32
+  if (smem > di->smem_optin) return RR_ERR_INVALID_ARG;
+  if ((st = set_smem(di, sp->fn, (size_t)smem)) != RR_OK) return st;
+  const int T = 32 * rr::kSpanWarps;
+  int& occ = di->occ[{sp->fn, ((long long)T << 32) | (long long)smem}];
+  if (occ == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sp->fn, T, (size_t)smem);
+    if (e != cudaSuccess || occ <= 0)
+      return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
   }
+  const int64_t nspans = cdiv(rows, 32 * rpl);
+  int64_t grid = cdiv(nspans, rr::kSpanWarps);
+  if (grid > (int64_t)di->sms * occ) grid = (int64_t)di->sms * occ;
+  if (grid > max_grid) grid = max_grid;
+  sp->smem = smem;
+  sp->grid = grid;
+  sp->geo = rr::SpanGeo{rows, (int32_t)cols, (int32_t)rpl, (int32_t)span_b, (int32_t)lab_b,
+                        (int32_t)(mode >= 7 && aux_aligned)};
+  return RR_OK;
+}
+
+template <class P>
+rr_status span_launch(const P& p, const SpanPlan& sp, cudaStream_t stream) {
   P pc = p;
+  rr::SpanGeo geo = sp.geo;
   void* args[] = {&pc, &geo};
-  cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(32 * rr::kSpanWarps), args,
-                                   (size_t)smem, stream);
+  cudaError_t e = cudaLaunchKernel(sp.fn, dim3((unsigned)sp.grid), dim3(32 * rr::kSpanWarps), args,
+                                   (size_t)sp.smem, stream);
   if (e != cudaSuccess) return fail(RR_ERR_CUDA, "span launch: %s", cudaGetErrorString(e));
   return RR_OK;
+}
+
+template <class P>
+rr_status span_launch(const P& p, rr_dtype dt, int mode, int64_t rows, int64_t cols,
+                      bool aux_aligned, cudaStream_t stream) {
+  SpanPlan sp;
+  rr_status st = span_plan(dt, mode, rows, cols, aux_aligned, INT64_MAX, &sp);
+  if (st != RR_OK) return st;
+  return span_launch(p, sp, stream);
 }
 
 template <class P>
@@ -836,6 +866,11 @@ static size_t norm_bwd_workspace_size(bool rms, int64_t rows, int64_t cols, rr_d
     size_t ws = 0;
     if (norm_bwd_plan(rms, rows, cols, dtype, m, &pl, &ws) == RR_OK && ws > best) best = ws;
   }
+  SpanPlan sp;  // short rows with 16-byte aligned tensors: one partial per span block
+  if (span_plan(dtype, rms ? 8 : 7, rows, cols, false, INT64_MAX, &sp) == RR_OK) {
+    const size_t ws = (size_t)sp.grid * (rms ? 1 : 2) * (size_t)cols * sizeof(float);
+    if (ws > best) best = ws;
+  }
   return best;
 }
 
@@ -896,17 +931,32 @@ static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* 
     const bool rows_al = (cols * (int64_t)E) % 16 == 0 && aligned(dy, 16) && aligned(x, 16) &&
                          aligned(dx, 16);
     const int lmode = al ? (rows_al ? 0 : 1) : 2;
-    if ((st = norm_bwd_plan(rms, rows, cols, dtype, lmode, &pl, &need, max_partials)) != RR_OK)
-      return st;
-    if (workspace_bytes < need)
-      return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
     int* err = device_error_word();
     if (!err) return RR_ERR_CUDA;
     rr::LnBwdParams p{static_cast<const char*>(dy), static_cast<const char*>(x), mean, rstd,
                       static_cast<const char*>(gamma), static_cast<char*>(dx),
                       static_cast<float*>(workspace), err, cols,
                       static_cast<float>(1.0 / static_cast<double>(cols))};
-    if ((st = launch(pl, p, stream)) != RR_OK) return st;
+    SpanPlan sp;
+    st = RR_ERR_INVALID_ARG;
+    if (aligned(dy, 16) && aligned(x, 16) && aligned(dx, 16)) {
+      const bool stats_al = aligned(rstd, 16) && (rms || aligned(mean, 16));
+      st = span_plan(dtype, rms ? 8 : 7, rows, cols, stats_al, max_partials, &sp);
+      if (st != RR_OK && st != RR_ERR_INVALID_ARG) return st;
+    }
+    if (st == RR_OK) {
+      need = (size_t)sp.grid * planes * (size_t)cols * sizeof(float);
+      if (workspace_bytes < need)
+        return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+      if ((st = span_launch(p, sp, stream)) != RR_OK) return st;
+      pl.partials = sp.grid;
+    } else {
+      if ((st = norm_bwd_plan(rms, rows, cols, dtype, lmode, &pl, &need, max_partials)) != RR_OK)
+        return st;
+      if (workspace_bytes < need)
+        return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+      if ((st = launch(pl, p, stream)) != RR_OK) return st;
+    }
   }
   const void* cr = dtype == RR_BF16 ? rr::col_reduce_kernel_ptr_bf16() : rr::col_reduce_kernel_ptr_f32();
   const float* ws = static_cast<const float*>(workspace);

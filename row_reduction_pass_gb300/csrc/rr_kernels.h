@@ -34,9 +34,10 @@ struct LnKernelSet {
 
 // Short-row span kernels (rr_span.cuh): [dtype][mode], mode 0 softmax,
 // 1 log-softmax, 2 cross-entropy, 3 softmax backward, 4 log-softmax backward,
-// 5 LayerNorm forward, 6 RMSNorm forward.
+// 5 LayerNorm forward, 6 RMSNorm forward, 7 LayerNorm backward, 8 RMSNorm
+// backward.
 struct SpanKernelSet {
-  const void* k[2][7];
+  const void* k[2][9];
 };
 SpanKernelSet span_kernels();
 

@@ -23,7 +23,9 @@ struct SpanGeo {
   int32_t cols;
   int32_t rpl;      // rows per lane per span
   int32_t span_b;   // bytes per span buffer (rows_per_span * cols * E, a multiple of 16)
-  int32_t lab_b;    // cross-entropy with 16-byte aligned labels: label bytes per span, else 0
+  int32_t lab_b;    // cross-entropy with 16-byte aligned labels: label bytes per span, else 0;
+                    // norm backward: bytes of one row statistic per span
+  int32_t staged;   // norm backward: mean / rstd 16-byte aligned, copied with the span
 };
 
 constexpr int kSpanWarps = 8;  // warps per block
@@ -352,6 +354,171 @@ __global__ void __launch_bounds__(32 * kSpanWarps)
     __syncwarp();
   }
   cp_async_wait<0>();
+}
+
+// LayerNorm (RMS = false) or RMSNorm backward of short rows (C x element size
+// <= 64 bytes, so C <= 32; with longer rows two tensors' spans leave room for
+// one block per SM and the row-group kernels are faster).  Per stage a warp
+// copies spans of dy and x and the span's row statistics (mean, rstd: by
+// cp.async when they are 16-byte aligned, else loaded into the same buffer).
+// Two passes over the staged span:
+//  - columns: the column partials sum dy*xhat (and sum dy) in registers, lane
+//    l taking column l % C of rows l / C, l / C + 32 / C, ...: consecutive
+//    lanes read consecutive elements;
+//  - rows: lane l takes rows l, l + 32, ...: S1 = sum g, S2 = sum g*xhat with
+//    g = dy*gamma, and dx = rstd*((g - S1/C) - xhat*S2/C), written over dy in
+//    shared memory and stored out as 16-byte blocks.
+// rstd == 0 marks a row the forward masked: dx = 0 and no contribution.  At the
+// end the block adds its lanes' partials in a fixed order (warp, then row
+// phase) into its row of the workspace, [gridDim.x][planes][C] floats, which
+// col_reduce_kernel sums.
+template <int DT, bool RMS>
+__global__ void __launch_bounds__(32 * kSpanWarps, 3)
+    span_ln_bwd_kernel(const LnBwdParams p, const SpanGeo geo) {
+  constexpr int E = DType<DT>::E;
+  constexpr int kPlanes = RMS ? 1 : 2;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int C = geo.cols;
+  const int rps = 32 * geo.rpl;
+  const int64_t nspans = (geo.rows + rps - 1) / rps;
+  const int64_t gw = (int64_t)blockIdx.x * kSpanWarps + warp;
+  const int64_t nw = (int64_t)gridDim.x * kSpanWarps;
+  // [warps][2 stages][dy | x] spans, then [warps][2 stages][mean | rstd][rps]
+  // floats, then gamma as fp32
+  unsigned char* buf = smem + (size_t)warp * 4 * geo.span_b;
+  const int nst = geo.lab_b / 4;  // rows per span, as floats
+  float* stats = reinterpret_cast<float*>(smem + (size_t)kSpanWarps * 4 * geo.span_b) +
+                 (size_t)warp * 4 * nst;
+  float* sg = reinterpret_cast<float*>(smem + (size_t)kSpanWarps * 4 * (geo.span_b + geo.lab_b));
+  for (int j = threadIdx.x; j < C; j += blockDim.x) sg[j] = ld_elem_cached<DT>(p.gamma + (int64_t)j * E);
+  __syncthreads();
+
+  // column pass geometry: nph row phases of C lanes
+  const int nph = 32 / C;
+  const int ph = lane / C;
+  const int j0 = lane % C;
+  const bool on = ph < nph;
+  float ag = 0.f, ab = 0.f;
+
+  const int64_t total = geo.rows * (int64_t)C * E;
+  auto span_bytes = [&](int64_t s) -> int64_t {
+    const int64_t b0 = s * geo.span_b;
+    const int64_t b1 = b0 + geo.span_b < total ? b0 + geo.span_b : total;
+    return b1 - b0;
+  };
+  auto issue = [&](int64_t s, int stage) {
+    if (s < nspans) {
+      const int64_t nb = span_bytes(s);
+      unsigned char* d0 = buf + (2 * stage) * geo.span_b;
+      unsigned char* d1 = d0 + geo.span_b;
+      const char* s0 = p.dy + s * geo.span_b;
+      const char* s1 = p.x + s * geo.span_b;
+      for (int64_t j = lane; j < nb / 16; j += 32) {
+        cp_async16(d0 + 16 * j, s0 + 16 * j);
+        cp_async16(d1 + 16 * j, s1 + 16 * j);
+      }
+      if (geo.staged) {
+        const int64_t r0 = s * rps;
+        const int64_t nr = geo.rows - r0 < rps ? geo.rows - r0 : rps;
+        float* sm = stats + (2 * stage) * nst;
+        for (int64_t j = lane; j < nr / 4; j += 32) {
+          if (!RMS) cp_async16(sm + 4 * j, p.mean + r0 + 4 * j);
+          cp_async16(sm + nst + 4 * j, p.rstd + r0 + 4 * j);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  issue(gw, 0);
+  for (int64_t it = 0;; ++it) {
+    const int64_t s = gw + it * nw;
+    if (s >= nspans) break;
+    const int stage = (int)(it & 1);
+    unsigned char* gbuf = buf + (2 * stage) * geo.span_b;  // dy, then dx
+    unsigned char* xbuf = gbuf + geo.span_b;
+    float* smean = stats + (2 * stage) * nst;
+    float* srstd = smean + nst;
+    const int64_t r0 = s * rps;
+    const int nrows = (int)(geo.rows - r0 < rps ? geo.rows - r0 : rps);
+    issue(s + nw, stage ^ 1);
+    cp_async_wait<1>();
+    const int64_t nb = span_bytes(s);
+    if (lane == 0)
+      for (int64_t b = nb & ~int64_t(15); b < nb; b += E) {
+        span_st<DT>(gbuf, (int)(b / E), ld_elem<DT>(p.dy + s * geo.span_b + b));
+        span_st<DT>(xbuf, (int)(b / E), ld_elem<DT>(p.x + s * geo.span_b + b));
+      }
+    for (int i = lane + (geo.staged ? (nrows & ~3) : 0); i < nrows; i += 32) {
+      if (!RMS) smean[i] = __ldg(p.mean + r0 + i);
+      srstd[i] = __ldg(p.rstd + r0 + i);
+    }
+    __syncwarp();
+    if (on)
+      for (int i = ph; i < nrows; i += nph) {
+        const float rs = srstd[i];
+        if (rs == 0.f) continue;
+        const float mu = RMS ? 0.f : smean[i];
+        const float dyv = span_ld<DT>(gbuf, i * C + j0);
+        const float xv = span_ld<DT>(xbuf, i * C + j0);
+        const float xh = RMS ? xv * rs : (xv - mu) * rs;
+        ag = fmaf(dyv, xh, ag);
+        if (!RMS) ab += dyv;
+      }
+    __syncwarp();
+    for (int k = 0; k < geo.rpl; ++k) {
+      const int i = lane + 32 * k;
+      if (i >= nrows) break;
+      const int base = i * C;
+      const float rstd = srstd[i];
+      if (rstd == 0.f) {
+        for (int j = 0; j < C; ++j) span_st<DT>(gbuf, base + j, 0.f);
+        continue;
+      }
+      const float mean = RMS ? 0.f : smean[i];
+      float s1 = 0.f, s2 = 0.f;
+      for (int j = 0; j < C; ++j) {
+        const float xv = span_ld<DT>(xbuf, base + j);
+        const float xh = RMS ? xv * rstd : (xv - mean) * rstd;
+        const float g = __fmul_rn(span_ld<DT>(gbuf, base + j), sg[j]);
+        if (!RMS) s1 += g;
+        s2 = fmaf(g, xh, s2);
+      }
+      const float a = RMS ? 0.f : s1 * p.inv_cols;
+      const float b = s2 * p.inv_cols;
+      for (int j = 0; j < C; ++j) {
+        const float xv = span_ld<DT>(xbuf, base + j);
+        const float xh = RMS ? xv * rstd : (xv - mean) * rstd;
+        const float g = __fmul_rn(span_ld<DT>(gbuf, base + j), sg[j]);
+        span_st<DT>(gbuf, base + j, fmaf(xh, -b, g - a) * rstd);
+      }
+    }
+    __syncwarp();
+    char* dst = p.dx + s * geo.span_b;
+    for (int64_t j = lane; j < nb / 16; j += 32)
+      st_chunk_stream(dst + 16 * j, *reinterpret_cast<const uint4*>(gbuf + 16 * j));
+    if (lane == 0)
+      for (int64_t b = nb & ~int64_t(15); b < nb; b += E)
+        st_elem<DT>(dst + b, span_ld<DT>(gbuf, (int)(b / E)));
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  // the lanes' partials, [warps][planes][32] floats over the (now idle) span
+  // buffers: slot lane holds column j0 of phase ph
+  float* red = reinterpret_cast<float*>(smem);
+  red[(warp * kPlanes) * 32 + lane] = ag;
+  if (!RMS) red[(warp * kPlanes + 1) * 32 + lane] = ab;
+  __syncthreads();
+  float* out = p.ws + (int64_t)blockIdx.x * kPlanes * C;
+  for (int idx = threadIdx.x; idx < kPlanes * C; idx += blockDim.x) {
+    const int pl = idx / C, j = idx % C;
+    float t = 0.f;
+    for (int w = 0; w < kSpanWarps; ++w)
+      for (int q = 0; q < nph; ++q) t += red[(w * kPlanes + pl) * 32 + q * C + j];
+    out[idx] = t;
+  }
 }
 
 }  // namespace rr

@@ -168,6 +168,37 @@ def check_ln(x, gamma, beta, dy, eps, dtype, pad=(0, 0, 0, 0, 0), oracle_stats=T
     return g
 
 
+def check_norm_bwd(x, gamma, beta, dy, dtype, rms=False, stat_pad=0, inplace=None):
+    """The LayerNorm (or RMSNorm) backward alone, given the oracle's statistics
+    rounded to float32 and stored stat_pad elements past a 16-byte boundary;
+    inplace = "dy" or "x" writes dx over that input."""
+    rows = x.shape[0]
+    if rms:
+        _, rrstd = oracle.rms_fwd(x, gamma, 1e-5, want_y=False)
+        rmean = np.zeros(rows)
+    else:
+        _, rmean, rrstd = oracle.ln_fwd(x, gamma, beta, 1e-5, want_y=False)
+    m32, r32 = rmean.astype(np.float32), rrstd.astype(np.float32)
+    m_in, r_in = to_dev(m32, stat_pad), to_dev(r32, stat_pad)
+    xd, dyd, gd = to_dev(x), to_dev(dy), to_dev(gamma)
+    dx = {"dy": dyd, "x": xd}.get(inplace) if inplace else empty_like_dev(x.shape, dtype)
+    dg = empty_like_dev(gamma.shape, dtype)
+    rtol, atol = TOL[dtype]
+    if rms:
+        rr.rr_rmsnorm_bwd(dyd, xd, r_in, gd, dx, dg)
+        torch.cuda.synchronize()
+        rdx, rdg, sdg = oracle.rms_bwd(dy, x, r32.astype(np.float64), gamma)
+    else:
+        db = empty_like_dev(gamma.shape, dtype)
+        rr.rr_layernorm_bwd(dyd, xd, m_in, r_in, gd, dx, dg, db)
+        torch.cuda.synchronize()
+        rdx, rdg, rdb, sdg, sdb = oracle.ln_bwd(dy, x, m32.astype(np.float64),
+                                                r32.astype(np.float64), gamma)
+        compare("norm bwd dbeta", host(db), rdb, rtol, atol, scale=sdb)
+    compare("norm bwd dx", host(dx), rdx, rtol, atol)
+    compare("norm bwd dgamma", host(dg), rdg, rtol, atol, scale=sdg)
+
+
 def run_rms(x, gamma, dy, eps, dtype, pad=(0, 0, 0, 0, 0), oracle_stats=True):
     """RMSNorm fwd then bwd on the GPU; pad as for run_ln (the beta slot unused).
     The backward gets the oracle's rstd rounded to float32 when oracle_stats."""

@@ -7,7 +7,7 @@ import pytest
 
 from row_reduction_pass_gb300 import synth
 
-from parity import check_ln, check_softmax, check_xent
+from parity import check_ln, check_norm_bwd, check_softmax, check_xent
 
 pytestmark = pytest.mark.gpu
 
@@ -110,3 +110,22 @@ def test_layernorm_eps_zero_and_large():
     x, g, b, dy = ln_case(64, 100, "f32", 8)
     check_ln(x, g, b, dy, 0.0, "f32")
     check_ln(x, g, b, dy, 10.0, "f32")
+
+
+SHORT = [("f32", c) for c in (1, 3, 17, 31, 32)] + [("bf16", c) for c in (1, 5, 32, 33, 47, 64)]
+
+
+@pytest.mark.parametrize("dtype,cols", SHORT)
+@pytest.mark.parametrize("rows", [1, 37, 4099, 60001, 1000003])
+@pytest.mark.parametrize("layout", ["plain", "stats_misaligned", "dx_over_dy", "dx_over_x"])
+def test_layernorm_bwd_short_rows(dtype, cols, rows, layout):
+    """Rows of at most 128 bytes: spans of rows per warp (a million rows: several
+    spans per warp through both stages), ragged last span, statistics staged
+    with the span (16-byte aligned) or loaded, dx in place."""
+    if rows * cols > 400000 and layout != "plain":
+        pytest.skip("large shapes run in the plain layout only")
+    if rows > 100000 and cols > 5:
+        pytest.skip("a million rows for the shortest rows only")
+    x, g, b, dy = ln_case(rows, cols, dtype, 700 + cols + rows)
+    check_norm_bwd(x, g, b, dy, dtype, stat_pad=1 if layout == "stats_misaligned" else 0,
+                   inplace={"dx_over_dy": "dy", "dx_over_x": "x"}.get(layout))

@@ -11,7 +11,7 @@ import oracle
 import row_reduction_pass_gb300 as rr
 from row_reduction_pass_gb300 import synth
 
-from parity import TOL, TOL_F32_OUT, check_rms, compare, empty_like_dev, host, to_dev
+from parity import TOL, TOL_F32_OUT, check_norm_bwd, check_rms, compare, empty_like_dev, host, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -79,3 +79,21 @@ def test_rmsnorm_rejects_rows_beyond_its_kernels():
         rr.rr_rmsnorm_bwd(x, x, torch.ones(4, device=dev), g, torch.empty_like(x),
                           torch.empty_like(g), workspace=torch.empty(1 << 20, dtype=torch.uint8,
                                                                       device=dev))
+
+
+SHORT = [("f32", c) for c in (1, 3, 17, 32)] + [("bf16", c) for c in (1, 5, 33, 64)]
+
+
+@pytest.mark.parametrize("dtype,cols", SHORT)
+@pytest.mark.parametrize("rows", [1, 37, 4099, 60001, 1000003])
+@pytest.mark.parametrize("layout", ["plain", "stats_misaligned", "dx_over_x"])
+def test_rmsnorm_bwd_short_rows(dtype, cols, rows, layout):
+    """The RMSNorm backward of rows of at most 128 bytes (spans of rows per warp)."""
+    if rows * cols > 400000 and layout != "plain":
+        pytest.skip("large shapes run in the plain layout only")
+    if rows > 100000 and cols > 5:
+        pytest.skip("a million rows for the shortest rows only")
+    x, g, dy = case(rows, cols, dtype, 950 + cols + rows)
+    check_norm_bwd(x, g, None, dy, dtype, rms=True,
+                   stat_pad=1 if layout == "stats_misaligned" else 0,
+                   inplace={"dx_over_x": "x"}.get(layout))
