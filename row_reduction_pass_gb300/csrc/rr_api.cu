@@ -282,18 +282,32 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
   const int E = dt == RR_BF16 ? 2 : 4;
   const int W = lmode == 2 ? 1 : 16 / E;
   const int64_t nfull = cols / W, rag = cols % W, nch = nfull + (rag > 0 ? 1 : 0);
-  const int nq = ls.nq[lmode];
+  int nq = ls.nq[lmode];
   int gi = -1;
   for (int i = 0; i < rr::kNumLnG; ++i)
     if ((int64_t)nq << i >= nch) {
       gi = i;
       break;
     }
-  if (gi < 0 || ls.k[lmode][gi] == nullptr)
+  // Rows the standard variants would give 128 or more threads: the deep
+  // variants where built (more chunks per thread, so the per-row reductions are
+  // paid by fewer threads).  RR_LN_DEEP=0 keeps the standard ones (tuning aid).
+  bool deep = lmode < 2 && ls.nqd > 0 && gi >= 7;
+  if (const char* f = std::getenv("RR_LN_DEEP")) deep = deep && f[0] != '0';
+  if (deep) {
+    for (int i = 6; i < rr::kNumLnG; ++i)
+      if ((int64_t)ls.nqd << i >= nch && ls.kd[lmode][i] != nullptr) {
+        gi = i;
+        nq = ls.nqd;
+        break;
+      }
+    deep = nq == ls.nqd;
+  }
+  if (gi < 0 || (deep ? ls.kd[lmode][gi] : ls.k[lmode][gi]) == nullptr)
     return fail(RR_ERR_INVALID_ARG, "row longer than one row group holds");
-  const void* fn = ls.k[lmode][gi];
+  const void* fn = deep ? ls.kd[lmode][gi] : ls.k[lmode][gi];
   // rows of at most 32 chunks: one chunk per thread where that variant exists
-  for (int i = 0; i <= 5; ++i)
+  for (int i = 0; i <= 5 && !deep; ++i)
     if (((int64_t)1 << i) >= nch) {
       if (ls.k1[lmode][i] != nullptr) {
         gi = i;

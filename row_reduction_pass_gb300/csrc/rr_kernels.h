@@ -30,6 +30,11 @@ struct LnKernelSet {
   // 1024 threads per block with nq chunks per thread, and [3] a 256-thread
   // group with 2 * nq; null where not built.
   const void* kc[3][4];
+  // Chunk modes, rows of many chunks: nqd (> nq) chunks per thread so a row
+  // needs fewer threads and each pays the per-row reductions over more data;
+  // G >= 64 only, null where not built.
+  const void* kd[2][kNumLnG];
+  int nqd;
 };
 
 // Short-row span kernels (rr_span.cuh): [dtype][mode], mode 0 softmax,

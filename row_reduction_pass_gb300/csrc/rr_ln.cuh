@@ -46,7 +46,9 @@ struct LnGeo {
 // 128 (a thread keeps g = dy*gamma, xhat and its two column accumulators), 64
 // for the one-chunk variants of short rows.
 template <int MAXT, int NQ = 4> constexpr int ln_fwd_min_blocks() {
-  return NQ > 4 ? 2 : 1024 / MAXT;  // the wide cluster variant: 128 registers
+  // more than 4 chunks per thread (the deep and the wide cluster variants):
+  // up to 128 registers (64 for 1024-thread blocks)
+  return NQ > 4 ? (MAXT >= 512 ? 1 : 2) : 1024 / MAXT;
 }
 template <int MAXT, int NQ> constexpr int ln_bwd_min_blocks() { return (NQ == 1 ? 1024 : 512) / MAXT; }
 
@@ -101,19 +103,27 @@ struct LnRed {
   }
 };
 
-// A row split over the K blocks of a cluster: each block's statistic (already
-// reduced over its threads) goes to its exchange slot, and after a cluster
-// barrier every thread merges the K slots in rank order, so all blocks hold the
-// same bits.  Slots alternate by call parity: a slot is rewritten two calls
-// later, after the next barrier, which every reader of it has passed.
+// A row split over the K <= 8 blocks of a cluster: each block's statistic
+// (already reduced over its threads) goes to its exchange slot, and after a
+// cluster barrier every thread reads the K slots (all loads issued before the
+// first merge, so their remote latencies overlap) and merges them in rank
+// order, so all blocks hold the same bits.  Slots alternate by call parity: a
+// slot is rewritten two calls later, after the next barrier, which every
+// reader of it has passed.
 template <class S, class M>
 __device__ __forceinline__ S ln_cluster(S s, M merge, unsigned char* slots, int& calls, int K) {
   S* slot = reinterpret_cast<S*>(slots + 16 * (calls & 1));
   ++calls;
   if (threadIdx.x == 0) *slot = s;
   cluster_sync();
-  S acc = S::load_remote(map_to_rank(slot, 0));
-  for (int k = 1; k < K; ++k) acc = merge(acc, S::load_remote(map_to_rank(slot, k)));
+  S v[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (k < K) v[k] = S::load_remote(map_to_rank(slot, k));
+  S acc = v[0];
+#pragma unroll
+  for (int k = 1; k < 8; ++k)
+    if (k < K) acc = merge(acc, v[k]);
   return acc;
 }
 
@@ -875,13 +885,29 @@ void ln_fill_row1(const void* (&row)[kNumLnG]) {
   row[5] = ln_variant<DT, W, 1, AL, false, 32, RMS>();
 }
 
-template <int DT, bool FWD, int NQC, int NQE, bool RMS = false>
+template <int DT, int W, int NQ, bool AL, bool FWD, bool RMS>
+void ln_fill_deep(const void* (&row)[kNumLnG]) {
+  row[6] = ln_variant<DT, W, NQ, AL, FWD, 64, RMS>();
+  row[7] = ln_variant<DT, W, NQ, AL, FWD, 128, RMS>();
+  row[8] = ln_variant<DT, W, NQ, AL, FWD, 256, RMS>();
+  row[9] = ln_variant<DT, W, NQ, AL, FWD, 512, RMS>();
+  row[10] = ln_variant<DT, W, NQ, AL, FWD, 1024, RMS>();
+}
+
+// NQC / NQE: chunks (elements) per thread of the chunk (element) mode
+// variants; NQD > 0: the deep chunk-mode variants with NQD chunks per thread.
+template <int DT, bool FWD, int NQC, int NQE, bool RMS = false, int NQD = 0>
 LnKernelSet make_ln_set() {
   constexpr int V = DType<DT>::V;
   LnKernelSet s{};
   ln_fill_row<DT, V, NQC, true, FWD, RMS>(s.k[0]);
   ln_fill_row<DT, V, NQC, false, FWD, RMS>(s.k[1]);
   ln_fill_row<DT, 1, NQE, false, FWD, RMS>(s.k[2]);
+  if constexpr (NQD > 0) {
+    ln_fill_deep<DT, V, NQD, true, FWD, RMS>(s.kd[0]);
+    ln_fill_deep<DT, V, NQD, false, FWD, RMS>(s.kd[1]);
+  }
+  s.nqd = NQD;
   if constexpr (FWD) {
     ln_fill_cluster<DT, V, NQC, true, RMS>(s.kc[0]);
     ln_fill_cluster<DT, V, NQC, false, RMS>(s.kc[1]);
