@@ -3,5 +3,5 @@
 #include "rr_ln.cuh"
 
 namespace rr {
-LnKernelSet ln_bwd_rowgroup_kernels_bf16() { return make_ln_set<kBF16, false, 2, 8>(); }
+LnKernelSet ln_bwd_rowgroup_kernels_bf16() { return make_ln_set<kBF16, false, 2, 8, false, 8>(); }
 }  // namespace rr

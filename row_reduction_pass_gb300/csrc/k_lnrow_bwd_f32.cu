@@ -3,5 +3,5 @@
 #include "rr_ln.cuh"
 
 namespace rr {
-LnKernelSet ln_bwd_rowgroup_kernels_f32() { return make_ln_set<kF32, false, 3, 8>(); }
+LnKernelSet ln_bwd_rowgroup_kernels_f32() { return make_ln_set<kF32, false, 3, 8, false, 8>(); }
 }  // namespace rr

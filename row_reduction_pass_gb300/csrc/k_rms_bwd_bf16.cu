@@ -3,5 +3,5 @@
 #include "rr_ln.cuh"
 
 namespace rr {
-LnKernelSet rms_bwd_rowgroup_kernels_bf16() { return make_ln_set<kBF16, false, 2, 16, true>(); }
+LnKernelSet rms_bwd_rowgroup_kernels_bf16() { return make_ln_set<kBF16, false, 2, 16, true, 8>(); }
 }  // namespace rr

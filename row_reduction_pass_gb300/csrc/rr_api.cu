@@ -272,8 +272,9 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
 // column partials) in shared memory.  lmode: 0 chunks with aligned rows, 1 chunks
 // with any row alignment, 2 elements.  RR_ERR_INVALID_ARG when the row does
 // not fit one group (the caller then plans the staged engine kernels).
-rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64_t cols, Plan* pl,
-                           int64_t max_partials) {
+static rr_status ln_rowgroup_plan_impl(OpKind op, rr_dtype dt, int lmode, int64_t rows,
+                                       int64_t cols, Plan* pl, int64_t max_partials,
+                                       bool allow_deep, bool* used_deep) {
   std::lock_guard<std::mutex> lock(g_mu);
   DevInfo* di = nullptr;
   rr_status st = device_info(&di);
@@ -289,10 +290,16 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
       gi = i;
       break;
     }
-  // Rows the standard variants would give 128 or more threads: the deep
-  // variants where built (more chunks per thread, so the per-row reductions are
-  // paid by fewer threads).  RR_LN_DEEP=0 keeps the standard ones (tuning aid).
-  bool deep = lmode < 2 && ls.nqd > 0 && gi >= 7;
+  // The deep variants where built (more chunks per thread, so the per-row
+  // work is paid by fewer threads; the backward ones keep their column partials
+  // in shared memory), chosen where they measured faster: forward rows the
+  // standard variants would give 128 threads or more, RMSNorm backward rows
+  // they would give 512, and LayerNorm backward rows longer than the standard
+  // variants hold (two planes of shared-memory partials cost more than the
+  // fewer threads save).  RR_LN_DEEP=0 keeps the standard ones (tuning aid).
+  const bool fwdop = op == kLnFwd || op == kRmsFwd;
+  const int deep_from = fwdop ? 7 : op == kRmsBwd ? 9 : 10;
+  bool deep = allow_deep && lmode < 2 && ls.nqd > 0 && gi >= deep_from;
   if (const char* f = std::getenv("RR_LN_DEEP")) deep = deep && f[0] != '0';
   if (deep) {
     for (int i = 6; i < rr::kNumLnG; ++i)
@@ -303,6 +310,7 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
       }
     deep = nq == ls.nqd;
   }
+  *used_deep = deep;
   if (gi < 0 || (deep ? ls.kd[lmode][gi] : ls.k[lmode][gi]) == nullptr)
     return fail(RR_ERR_INVALID_ARG, "row longer than one row group holds");
   const void* fn = deep ? ls.kd[lmode][gi] : ls.k[lmode][gi];
@@ -316,9 +324,9 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
       break;
     }
   const int G = 1 << gi;
-  const bool fwdk = op == kLnFwd || op == kRmsFwd;
+  const bool fwdk = fwdop;
   const int planes = (op == kLnFwd || op == kLnBwd) ? 2 : 1;  // gamma, beta / dgamma, dbeta
-  const int M1 = fwdk ? 256 : 512;
+  const int M1 = fwdk ? 256 : deep ? 128 : 512;
   const int T = G > M1 ? G : M1;
   const int ngroups = T / G;
   const int64_t npad = nch * W;
@@ -361,6 +369,18 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
                        (int32_t)nch,  (int32_t)red_off, (int32_t)acc_off, (int32_t)pf_off,
                        (int32_t)cols, 0};
   return RR_OK;
+}
+
+// The plan above, falling back to the standard variants where a deep one does
+// not fit shared memory (its per-group row buffers and partials grow with the
+// row).
+rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64_t cols, Plan* pl,
+                           int64_t max_partials) {
+  bool deep = false;
+  rr_status st = ln_rowgroup_plan_impl(op, dt, lmode, rows, cols, pl, max_partials, true, &deep);
+  if (st == RR_ERR_INVALID_ARG && deep)
+    st = ln_rowgroup_plan_impl(op, dt, lmode, rows, cols, pl, max_partials, false, &deep);
+  return st;
 }
 
 // Forward rows too long for one row group: the row is split over a cluster of K
@@ -871,11 +891,11 @@ static rr_status norm_bwd_plan(bool rms, int64_t rows, int64_t cols, rr_dtype dt
 static size_t norm_bwd_workspace_size(bool rms, int64_t rows, int64_t cols, rr_dtype dtype) {
   if (check_shape(rows, cols, dtype) != RR_OK) return 0;
   if (rows == 0) return (rms ? 1 : 2) * (size_t)cols * sizeof(float);
-  // The element-mode plan never needs fewer partials than the chunk-mode one
-  // for the same shape, but the caller does not know which mode the pointers
-  // will select, so report the larger of the two.
+  // The caller does not know which mode the pointers will select (aligned or
+  // misaligned chunks, elements: different shared memory, so different
+  // occupancy and grid), so report the largest of the three.
   size_t best = 0;
-  for (int m = 0; m < 3; m += 2) {  // chunk modes 0 and 1 plan alike
+  for (int m = 0; m < 3; ++m) {
     Plan pl;
     size_t ws = 0;
     if (norm_bwd_plan(rms, rows, cols, dtype, m, &pl, &ws) == RR_OK && ws > best) best = ws;

@@ -627,7 +627,14 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT, NQ>())
 // cp.async while it works on the current row (no registers held, no barrier:
 // a thread reads only the slots it filled), and the row statistics one row
 // ahead into registers.
-template <int DT, int W, int G, int NQ, bool AL, int MAXT, bool RMS>
+//
+// SA (the deep variants, many chunks per thread): the column partials live in
+// the group's region of shared memory instead of registers (planes of four
+// columns, so a lane reads and writes 16 contiguous bytes; each slot touched
+// only by the thread owning its chunk), and g and xhat are recomputed from the
+// stored chunks for dx instead of being held: far fewer registers, so fewer
+// threads per row and more rows in flight per SM.
+template <int DT, int W, int G, int NQ, bool AL, int MAXT, bool RMS, bool SA = false>
 __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
     ln_bwd_kernel(const LnBwdParams p, const LnGeo geo) {
   constexpr bool PF = AL && W > 1;
@@ -651,11 +658,28 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
   const int64_t rowb = (int64_t)geo.cols * E;
   const int64_t nbytes = geo.rows * rowb;
 
-  float ag[NQ][W], ab[NQ][W];  // column partials: sum dy*xhat, sum dy (LayerNorm only)
+  static_assert(!SA || W >= 4, "shared-memory partials are for chunk mode");
+  constexpr int kPlanes = RMS ? 1 : 2;  // dgamma (, dbeta)
+  // column partials: sum dy*xhat, sum dy (LayerNorm only)
+  float ag[SA ? 1 : NQ][W], ab[SA ? 1 : NQ][W];
+  // SA: this group's partials, [kPlanes][W / 4][nch][4] floats
+  float* sacc = reinterpret_cast<float*>(smem + geo.acc_off) + (size_t)grp * kPlanes * npad;
+  const int spl = geo.nch * 4;  // floats per plane of four columns
+  if constexpr (SA) {
 #pragma unroll
-  for (int q = 0; q < NQ; ++q)
+    for (int q = 0; q < NQ; ++q)
+      if (q < cs.nown) {
+        const int k = gt + q * G;
 #pragma unroll
-    for (int e = 0; e < W; ++e) ag[q][e] = ab[q][e] = 0.f;
+        for (int pl = 0; pl < kPlanes * (W / 4); ++pl)
+          *reinterpret_cast<float4*>(sacc + pl * spl + k * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+  } else {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+#pragma unroll
+      for (int e = 0; e < W; ++e) ag[q][e] = ab[q][e] = 0.f;
+  }
 
   uint4* pf = reinterpret_cast<uint4*>(smem + geo.pf_off);
   auto slot = [&](int stage, int t, int q) -> uint4* {
@@ -719,10 +743,10 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
       stats(r, mean, rstd);
     }
     const bool use = active && rstd != 0.f;
-    float gv[NQ][W], hv[NQ][W];
+    float gv[SA ? 1 : NQ][W], hv[SA ? 1 : NQ][W];
     float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
+    uint4 dv[NQ], xv[NQ];
     if (use) {
-      uint4 dv[NQ], xv[NQ];
       if constexpr (PF) {
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
@@ -744,6 +768,22 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
           float gm[W];
           sg.get(gt + q * G, gm);
           if constexpr (W > 1) {
+            // SA: this chunk's partials from shared memory, updated, written back
+            const int qa = SA ? 0 : q;
+            const int k = gt + q * G;
+            if constexpr (SA) {
+#pragma unroll
+              for (int pq = 0; pq < W / 4; ++pq) {
+                const float4 tg = *reinterpret_cast<const float4*>(sacc + pq * spl + k * 4);
+                ag[0][4 * pq] = tg.x; ag[0][4 * pq + 1] = tg.y;
+                ag[0][4 * pq + 2] = tg.z; ag[0][4 * pq + 3] = tg.w;
+                if constexpr (!RMS) {
+                  const float4 tb = *reinterpret_cast<const float4*>(sacc + (W / 4 + pq) * spl + k * 4);
+                  ab[0][4 * pq] = tb.x; ab[0][4 * pq + 1] = tb.y;
+                  ab[0][4 * pq + 2] = tb.z; ab[0][4 * pq + 3] = tb.w;
+                }
+              }
+            }
 #pragma unroll
             for (int e = 0; e < W; e += 2) {
               const float y0 = ln_get<DT, W>(dv[q], e), y1 = ln_get<DT, W>(dv[q], e + 1);
@@ -757,12 +797,24 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
               const float g0 = __fmul_rn(y0, gm[e]), g1 = __fmul_rn(y1, gm[e + 1]);
               if constexpr (!RMS) add2(s1a, s1b, s1a, s1b, g0, g1);
               fma2(s2a, s2b, g0, g1, h0, h1, s2a, s2b);
-              fma2(ag[q][e], ag[q][e + 1], y0, y1, h0, h1, ag[q][e], ag[q][e + 1]);
-              if constexpr (!RMS) add2(ab[q][e], ab[q][e + 1], ab[q][e], ab[q][e + 1], y0, y1);
-              gv[q][e] = g0;
-              gv[q][e + 1] = g1;
-              hv[q][e] = h0;
-              hv[q][e + 1] = h1;
+              fma2(ag[qa][e], ag[qa][e + 1], y0, y1, h0, h1, ag[qa][e], ag[qa][e + 1]);
+              if constexpr (!RMS) add2(ab[qa][e], ab[qa][e + 1], ab[qa][e], ab[qa][e + 1], y0, y1);
+              if constexpr (!SA) {
+                gv[q][e] = g0;
+                gv[q][e + 1] = g1;
+                hv[q][e] = h0;
+                hv[q][e + 1] = h1;
+              }
+            }
+            if constexpr (SA) {
+#pragma unroll
+              for (int pq = 0; pq < W / 4; ++pq) {
+                *reinterpret_cast<float4*>(sacc + pq * spl + k * 4) =
+                    make_float4(ag[0][4 * pq], ag[0][4 * pq + 1], ag[0][4 * pq + 2], ag[0][4 * pq + 3]);
+                if constexpr (!RMS)
+                  *reinterpret_cast<float4*>(sacc + (W / 4 + pq) * spl + k * 4) = make_float4(
+                      ab[0][4 * pq], ab[0][4 * pq + 1], ab[0][4 * pq + 2], ab[0][4 * pq + 3]);
+              }
             }
           } else {
             const float y0 = ln_get<DT, W>(dv[q], 0);
@@ -791,6 +843,27 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
         if (!use) {
 #pragma unroll
           for (int e = 0; e < W; ++e) f[e] = 0.f;
+        } else if constexpr (SA) {
+          // g and xhat again from the stored chunks (the same operations, the
+          // same bits as in the first pass)
+          float gm[W];
+          sg.get(gt + q * G, gm);
+#pragma unroll
+          for (int e = 0; e < W; e += 2) {
+            const float y0 = ln_get<DT, W>(dv[q], e), y1 = ln_get<DT, W>(dv[q], e + 1);
+            float h0, h1;
+            if constexpr (RMS) {
+              mul2(h0, h1, ln_get<DT, W>(xv[q], e), ln_get<DT, W>(xv[q], e + 1), rstd, rstd);
+            } else {
+              add2(h0, h1, ln_get<DT, W>(xv[q], e), ln_get<DT, W>(xv[q], e + 1), -mean, -mean);
+              mul2(h0, h1, h0, h1, rstd, rstd);
+            }
+            const float g0 = __fmul_rn(y0, gm[e]), g1 = __fmul_rn(y1, gm[e + 1]);
+            float t0, t1;
+            add2(t0, t1, g0, g1, -a, -a);
+            fma2(t0, t1, h0, h1, -b, -b, t0, t1);
+            mul2(f[e], f[e + 1], t0, t1, rstd, rstd);
+          }
         } else if constexpr (W > 1) {
 #pragma unroll
           for (int e = 0; e < W; e += 2) {
@@ -809,18 +882,18 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
 
   if constexpr (PF || PFR) cp_async_wait<0>();
 
-  // Column partials: each group's to shared memory, then a fixed-order sum
-  // over the groups into this block's partial row.
-  constexpr int kPlanes = RMS ? 1 : 2;  // dgamma (, dbeta)
-  float* acc = reinterpret_cast<float*>(smem + geo.acc_off) + (size_t)grp * kPlanes * npad;
+  // Column partials: each group's to shared memory (SA: already there), then
+  // a fixed-order sum over the groups into this block's partial row.
+  if constexpr (!SA) {
 #pragma unroll
-  for (int q = 0; q < NQ; ++q) {
-    if (q < cs.nown) {
-      const int j = (gt + q * G) * W;
+    for (int q = 0; q < NQ; ++q) {
+      if (q < cs.nown) {
+        const int j = (gt + q * G) * W;
 #pragma unroll
-      for (int e = 0; e < W; ++e) {
-        acc[j + e] = ag[q][e];
-        if constexpr (!RMS) acc[npad + j + e] = ab[q][e];
+        for (int e = 0; e < W; ++e) {
+          sacc[j + e] = ag[q][e];
+          if constexpr (!RMS) sacc[npad + j + e] = ab[q][e];
+        }
       }
     }
   }
@@ -830,8 +903,10 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
   for (int i = threadIdx.x; i < kPlanes * geo.cols; i += MAXT) {
     const int half = i >= geo.cols ? 1 : 0;
     const int j = i - half * geo.cols;
+    // column j of a group's region: SA planes of four columns, else in order
+    const int o = SA ? half * npad + ((j % W) >> 2) * spl + (j / W) * 4 + (j & 3) : half * npad + j;
     float t = 0.f;
-    for (int gi = 0; gi < ngroups; ++gi) t += all[(size_t)gi * kPlanes * npad + half * npad + j];
+    for (int gi = 0; gi < ngroups; ++gi) t += all[(size_t)gi * kPlanes * npad + o];
     out[i] = t;
   }
 }
@@ -850,10 +925,12 @@ void ln_fill_cluster(const void* (&row)[4]) {
   row[3] = (const void*)ln_fwd_kernel<DT, W, 256, 2 * NQ, AL, 256, RMS, true>;
 }
 
-template <int DT, int W, int NQ, bool AL, bool FWD, int G, bool RMS>
+template <int DT, int W, int NQ, bool AL, bool FWD, int G, bool RMS, bool SA = false>
 const void* ln_variant() {
   if constexpr (FWD) {
     return (const void*)ln_fwd_kernel<DT, W, G, NQ, AL, (G > 256 ? G : 256), RMS>;
+  } else if constexpr (G <= 512 && SA) {
+    return (const void*)ln_bwd_kernel<DT, W, G, NQ, AL, (G > 128 ? G : 128), RMS, true>;
   } else if constexpr (G <= 512) {
     return (const void*)ln_bwd_kernel<DT, W, G, NQ, AL, 512, RMS>;
   } else {
@@ -885,13 +962,15 @@ void ln_fill_row1(const void* (&row)[kNumLnG]) {
   row[5] = ln_variant<DT, W, 1, AL, false, 32, RMS>();
 }
 
+// The deep variants: G >= 64; the backward ones keep their column partials in
+// shared memory (SA), block size max(G, 128).
 template <int DT, int W, int NQ, bool AL, bool FWD, bool RMS>
 void ln_fill_deep(const void* (&row)[kNumLnG]) {
-  row[6] = ln_variant<DT, W, NQ, AL, FWD, 64, RMS>();
-  row[7] = ln_variant<DT, W, NQ, AL, FWD, 128, RMS>();
-  row[8] = ln_variant<DT, W, NQ, AL, FWD, 256, RMS>();
-  row[9] = ln_variant<DT, W, NQ, AL, FWD, 512, RMS>();
-  row[10] = ln_variant<DT, W, NQ, AL, FWD, 1024, RMS>();
+  row[6] = ln_variant<DT, W, NQ, AL, FWD, 64, RMS, !FWD>();
+  row[7] = ln_variant<DT, W, NQ, AL, FWD, 128, RMS, !FWD>();
+  row[8] = ln_variant<DT, W, NQ, AL, FWD, 256, RMS, !FWD>();
+  row[9] = ln_variant<DT, W, NQ, AL, FWD, 512, RMS, !FWD>();
+  row[10] = ln_variant<DT, W, NQ, AL, FWD, 1024, RMS, !FWD>();
 }
 
 // NQC / NQE: chunks (elements) per thread of the chunk (element) mode

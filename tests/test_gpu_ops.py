@@ -75,8 +75,8 @@ def test_xent_custom_ignore_index():
     check_xent(x, lab, "f32", ignore_index=7)
 
 
-LN_COLS = [1, 2, 3, 8, 31, 32, 97, 128, 256, 768, 1000, 1024, 2049, 4096, 4097, 8192, 12289,
-           16384, 32768, 65537]
+LN_COLS = [1, 2, 3, 8, 31, 32, 97, 128, 256, 768, 1000, 1024, 2049, 4096, 4097, 6145, 8192, 8193,
+           12289, 16384, 32768, 65537]
 
 
 def ln_case(rows, cols, dtype, seed):

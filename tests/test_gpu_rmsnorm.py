@@ -15,7 +15,7 @@ from parity import TOL, TOL_F32_OUT, check_norm_bwd, check_rms, compare, empty_l
 
 pytestmark = pytest.mark.gpu
 
-RMS_COLS = [1, 2, 3, 8, 31, 32, 97, 128, 768, 1000, 1024, 2049, 4096, 4097, 6144, 8192]
+RMS_COLS = [1, 2, 3, 8, 31, 32, 97, 128, 768, 1000, 1024, 2049, 4096, 4097, 6144, 8192, 8193]
 
 
 def rows_for(cols: int) -> int:
@@ -33,6 +33,12 @@ def case(rows, cols, dtype, seed):
 def test_rmsnorm(cols, dtype):
     x, g, dy = case(rows_for(cols), cols, dtype, 900 + cols)
     check_rms(x, g, dy, 1e-5, dtype)
+
+
+def test_rmsnorm_bf16_rows_beyond_8192():
+    """bf16 rows of 12289 columns: the deep backward (shared-memory partials)."""
+    x, g, dy = case(200, 12289, "bf16", 912289)
+    check_rms(x, g, dy, 1e-5, "bf16")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -72,9 +78,9 @@ def test_rmsnorm_rejects_rows_beyond_its_kernels():
     g = torch.ones(300000, device=dev)
     with pytest.raises(rr.RRError):
         rr.rr_rmsnorm_fwd(x, g, torch.empty_like(x), torch.empty(2, device=dev))
-    x = torch.zeros(4, 8193, device=dev)             # the backward holds 8192 columns
-    g = torch.ones(8193, device=dev)
-    assert rr.rr_rmsnorm_bwd_workspace_size(4, 8193, torch.float32) == 0
+    x = torch.zeros(4, 16385, device=dev)            # the backward holds 16384 fp32 columns
+    g = torch.ones(16385, device=dev)
+    assert rr.rr_rmsnorm_bwd_workspace_size(4, 16385, torch.float32) == 0
     with pytest.raises(rr.RRError):
         rr.rr_rmsnorm_bwd(x, x, torch.ones(4, device=dev), g, torch.empty_like(x),
                           torch.empty_like(g), workspace=torch.empty(1 << 20, dtype=torch.uint8,
