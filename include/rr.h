@@ -32,6 +32,13 @@
  *   - Waits inside the kernels are bounded; a wait that gives up records
  *     RR_ERR_DEVICE_TIMEOUT in a per-device error word read by
  *     rr_read_device_error(), and the kernel returns instead of hanging.
+ *   - The kernel tier is chosen per call from the row's byte length, the
+ *     pointers' alignment and the device.  The environment variable
+ *     RR_FORCE_TIER (read at every call; for tests and tuning) forces one:
+ *     0 spans of short rows through shared memory, 1 a row in registers,
+ *     2 staged rows (one per CTA, bulk copies to shared memory), 3 rows split
+ *     over a thread-block cluster.  A shape the forced tier cannot hold returns
+ *     RR_ERR_INVALID_ARG; so does a value other than 0..3 (or T0..T3).
  */
 #ifndef RR_H
 #define RR_H

@@ -128,8 +128,10 @@ struct Plan {
 // row needs no extra chunk for a ragged head.  max_partials caps the number of
 // row groups (direct) or clusters (staged) that each leave a column partial.
 // Deterministic for a given device, so the workspace size query and the launch agree.
+// force: -1 any tier, 1 direct variants only, 2 staged one row per CTA only,
+// 3 staged cluster-split rows only (K >= 2).
 rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t rows, int64_t cols,
-                    Plan* pl, int64_t max_partials) {
+                    Plan* pl, int64_t max_partials, int force) {
   std::lock_guard<std::mutex> lock(g_mu);
   DevInfo* di = nullptr;
   rr_status st = device_info(&di);
@@ -150,7 +152,7 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
       gi = i;
       break;
     }
-  if (gi >= 0 && ks.direct[mode][0] != nullptr) {
+  if (gi >= 0 && ks.direct[mode][0] != nullptr && force != 2 && force != 3) {
     const int G = 1 << gi;
     const int T = ks.maxt_direct > G ? ks.maxt_direct : G;
     const int ngroups = T / G;
@@ -188,12 +190,16 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
     }
   }
 
+  if (force == 1)
+    return fail(RR_ERR_INVALID_ARG, "tier 1 (row in registers) cannot hold rows of %lld columns",
+                (long long)cols);
+
   // Staged variants: one row (slice) per CTA, K-CTA clusters for long rows.
   const int T = ks.maxt_staged;
   const int nq = ks.nq_staged[mode];
   int K = 0;
   int64_t slice = 0;
-  for (int k = 1; k <= 8; k *= 2) {
+  for (int k = force == 3 ? 2 : 1; k <= (force == 2 ? 1 : 8); k *= 2) {
     const int64_t sl = round_up(cdiv(cols, k), V);
     if (k > 1 && (k - 1) * sl >= cols) break;
     const int64_t su = mode == 0 ? cdiv(sl * E + (head_free ? 0 : 15), 16) : sl;
@@ -204,8 +210,10 @@ rr_status make_plan(OpKind op, rr_dtype dt, int mode, bool head_free, int64_t ro
     }
   }
   if (K == 0)
-    return fail(RR_ERR_INVALID_ARG, "cols=%lld is beyond the supported row length for this operation",
-                (long long)cols);
+    return fail(RR_ERR_INVALID_ARG,
+                force >= 2 ? "tier %d cannot hold rows of %lld columns"
+                           : "cols=%lld is beyond the supported row length for this operation",
+                force >= 2 ? force : (long long)cols, (long long)cols);
   const int64_t buf_bytes = round_up(slice * E + 32, 128);
   const int64_t colb = (op == kLnBwd) ? 2 * round_up(slice, mode == 0 ? V : 1) * 4 : 0;
   const int64_t fixed = 2 * 8 + 32 + 1024 + 32 + colb;
@@ -495,12 +503,33 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
 // Plans in chunk mode when allowed, falling back to element mode (which holds
 // longer rows per CTA) when the row does not fit the chunk-mode variants.
 rr_status plan_any(OpKind op, rr_dtype dt, bool chunk_ok, bool head_free, int64_t rows,
-                   int64_t cols, Plan* pl, int64_t max_partials = INT64_MAX) {
+                   int64_t cols, Plan* pl, int64_t max_partials = INT64_MAX, int force = -1) {
   if (chunk_ok) {
-    rr_status st = make_plan(op, dt, 0, head_free, rows, cols, pl, max_partials);
+    rr_status st = make_plan(op, dt, 0, head_free, rows, cols, pl, max_partials, force);
     if (st != RR_ERR_INVALID_ARG) return st;
   }
-  return make_plan(op, dt, 1, false, rows, cols, pl, max_partials);
+  return make_plan(op, dt, 1, false, rows, cols, pl, max_partials, force);
+}
+
+// RR_FORCE_TIER = 0 .. 3 (or T0 .. T3) makes every call use one kernel tier,
+// so tests can run each tier on any shape it can hold: 0 spans of short rows,
+// 1 a row in registers (engine direct variants, LayerNorm / RMSNorm row
+// groups), 2 staged rows, one per CTA, 3 cluster-split rows (LayerNorm /
+// RMSNorm forward: clusters of row groups; otherwise the staged engine with
+// K >= 2).  A shape the forced tier cannot hold fails with RR_ERR_INVALID_ARG.
+// Returns -1 when unset, -2 for a value outside those.
+static int forced_tier() {
+  const char* f = std::getenv("RR_FORCE_TIER");
+  if (f == nullptr || *f == 0) return -1;
+  if (*f == 'T' || *f == 't') ++f;
+  if (f[0] >= '0' && f[0] <= '3' && f[1] == 0) return f[0] - '0';
+  return -2;
+}
+static rr_status bad_tier() { return fail(RR_ERR_INVALID_ARG, "RR_FORCE_TIER must be 0..3 or T0..T3"); }
+static rr_status no_span(int64_t cols) {
+  return fail(RR_ERR_INVALID_ARG,
+              "tier 0 (spans) takes 16-byte aligned tensors with rows of at most 128 bytes "
+              "(64 for the norm backward), not %lld columns", (long long)cols);
 }
 
 // Short rows (cols * E <= 128 bytes, 64 for the norm backward; 16-byte aligned
@@ -675,12 +704,16 @@ static rr_status softmax_fwd_impl(const void* x, void* y, int64_t rows, int64_t 
   if (!err) return RR_ERR_CUDA;
   rr::SoftmaxParams p{static_cast<const char*>(x), static_cast<char*>(y), nullptr, nullptr, nullptr,
                       err, cols, 0, log};
-  if (aligned(x, 16) && aligned(y, 16)) {
+  const int ft = forced_tier();
+  if (ft == -2) return bad_tier();
+  if (ft <= 0 && aligned(x, 16) && aligned(y, 16)) {
     st = span_launch(p, dtype, log ? 1 : 0, rows, cols, false, stream);
     if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
   }
+  if (ft == 0) return no_span(cols);
   Plan pl;
-  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
+  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl, INT64_MAX, ft)) != RR_OK)
+    return st;
   if ((st = launch(pl, p, stream)) != RR_OK) return st;
   return ok();
 }
@@ -719,12 +752,16 @@ static rr_status softmax_bwd_impl(const void* y, const void* dy, void* dx, int64
   if (!err) return RR_ERR_CUDA;
   rr::SoftmaxBwdParams p{static_cast<const char*>(y), static_cast<const char*>(dy),
                          static_cast<char*>(dx), err, cols, log};
-  if (same && a == 0) {
+  const int ft = forced_tier();
+  if (ft == -2) return bad_tier();
+  if (ft <= 0 && same && a == 0) {
     st = span_launch(p, dtype, log ? 4 : 3, rows, cols, false, stream);
     if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
   }
+  if (ft == 0) return no_span(cols);
   Plan pl;
-  if ((st = plan_any(kSoftmaxBwd, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
+  if ((st = plan_any(kSoftmaxBwd, dtype, same, head_free, rows, cols, &pl, INT64_MAX, ft)) != RR_OK)
+    return st;
   if ((st = launch(pl, p, stream)) != RR_OK) return st;
   return ok();
 }
@@ -766,12 +803,16 @@ rr_status rr_softmax_xent_fwd_bwd(const void* logits, const int32_t* labels, flo
   if (!err) return RR_ERR_CUDA;
   rr::SoftmaxParams p{static_cast<const char*>(logits), static_cast<char*>(dlogits), labels, loss,
                       bad_label_count, err, cols, ignore_index};
-  if (aligned(logits, 16) && aligned(dlogits, 16)) {
+  const int ft = forced_tier();
+  if (ft == -2) return bad_tier();
+  if (ft <= 0 && aligned(logits, 16) && aligned(dlogits, 16)) {
     st = span_launch(p, dtype, 2, rows, cols, aligned(labels, 16), stream);
     if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
   }
+  if (ft == 0) return no_span(cols);
   Plan pl;
-  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl)) != RR_OK) return st;
+  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl, INT64_MAX, ft)) != RR_OK)
+    return st;
   if ((st = launch(pl, p, stream)) != RR_OK) return st;
   return ok();
 }
@@ -800,20 +841,26 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
   const bool rows_al = (cols * (int64_t)E) % 16 == 0 && aligned(x, 16) && aligned(y, 16);
   Plan pl;
   const int lmode = al ? (rows_al ? 0 : 1) : 2;
+  const int ft = forced_tier();
+  if (ft == -2) return bad_tier();
   {
     int* err = device_error_word();
     if (!err) return RR_ERR_CUDA;
     rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma),
                       static_cast<const char*>(beta), static_cast<char*>(y), mean, rstd, err, cols,
                       eps, static_cast<float>(1.0 / static_cast<double>(cols))};
-    if (aligned(x, 16) && aligned(y, 16)) {
+    if (ft <= 0 && aligned(x, 16) && aligned(y, 16)) {
       st = span_launch(p, dtype, 5, rows, cols, false, stream);
       if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
     }
   }
-  st = ln_rowgroup_plan(kLnFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
-  if (st == RR_ERR_INVALID_ARG) st = ln_cluster_plan(kLnFwd, dtype, lmode, rows, cols, &pl);
-  if (st == RR_ERR_INVALID_ARG) st = plan_any(kLnFwd, dtype, al, true, rows, cols, &pl);
+  if (ft == 0) return no_span(cols);
+  st = RR_ERR_INVALID_ARG;
+  if (ft < 0 || ft == 1) st = ln_rowgroup_plan(kLnFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
+  if ((ft < 0 && st == RR_ERR_INVALID_ARG) || ft == 3)
+    st = ln_cluster_plan(kLnFwd, dtype, lmode, rows, cols, &pl);
+  if ((ft < 0 && st == RR_ERR_INVALID_ARG) || ft == 2)
+    st = plan_any(kLnFwd, dtype, al, true, rows, cols, &pl, INT64_MAX, ft < 0 ? -1 : 2);
   if (st != RR_OK) return st;
   int* err = device_error_word();
   if (!err) return RR_ERR_CUDA;
@@ -843,19 +890,26 @@ rr_status rr_rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
   const bool rows_al = (cols * (int64_t)E) % 16 == 0 && aligned(x, 16) && aligned(y, 16);
   Plan pl;
   const int lmode = al ? (rows_al ? 0 : 1) : 2;
+  const int ft = forced_tier();
+  if (ft == -2) return bad_tier();
+  if (ft == 2) return fail(RR_ERR_INVALID_ARG, "tier 2 (staged rows) has no RMSNorm kernel");
   {
     int* err = device_error_word();
     if (!err) return RR_ERR_CUDA;
     rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma), nullptr,
                       static_cast<char*>(y), nullptr, rstd, err, cols, eps,
                       static_cast<float>(1.0 / static_cast<double>(cols))};
-    if (aligned(x, 16) && aligned(y, 16)) {
+    if (ft <= 0 && aligned(x, 16) && aligned(y, 16)) {
       st = span_launch(p, dtype, 6, rows, cols, false, stream);
       if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
     }
   }
-  st = ln_rowgroup_plan(kRmsFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
-  if (st == RR_ERR_INVALID_ARG) st = ln_cluster_plan(kRmsFwd, dtype, lmode, rows, cols, &pl);
+  if (ft == 0) return no_span(cols);
+  st = RR_ERR_INVALID_ARG;
+  if (ft < 0 || ft == 1) st = ln_rowgroup_plan(kRmsFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
+  if ((ft < 0 && st == RR_ERR_INVALID_ARG) || ft == 3)
+    st = ln_cluster_plan(kRmsFwd, dtype, lmode, rows, cols, &pl);
+  if (ft >= 1 && st != RR_OK) return st;
   if (st == RR_ERR_INVALID_ARG)
     return fail(RR_ERR_INVALID_ARG, "RMSNorm rows of %lld columns are longer than one row group holds",
                 (long long)cols);
@@ -875,13 +929,20 @@ rr_status rr_rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
 // partials, [partials][planes][cols] floats.
 static rr_status norm_bwd_plan(bool rms, int64_t rows, int64_t cols, rr_dtype dtype, int lmode,
                                Plan* pl, size_t* ws_bytes, int64_t max_partials = INT64_MAX) {
-  rr_status st = ln_rowgroup_plan(rms ? kRmsBwd : kLnBwd, dtype, lmode, rows, cols, pl, max_partials);
-  if (st == RR_ERR_INVALID_ARG) {
+  const int ft = forced_tier();
+  if (ft == -2) return bad_tier();
+  if (ft == 0) return no_span(cols);
+  if (rms && ft >= 2)
+    return fail(RR_ERR_INVALID_ARG, "tier %d has no RMSNorm backward kernel", ft);
+  rr_status st = RR_ERR_INVALID_ARG;
+  if (ft < 0 || ft == 1)
+    st = ln_rowgroup_plan(rms ? kRmsBwd : kLnBwd, dtype, lmode, rows, cols, pl, max_partials);
+  if (st == RR_ERR_INVALID_ARG && ft != 1) {
     if (rms)
       return fail(RR_ERR_INVALID_ARG,
                   "RMSNorm rows of %lld columns are longer than one row group holds",
                   (long long)cols);
-    st = plan_any(kLnBwd, dtype, lmode != 2, true, rows, cols, pl, max_partials);
+    st = plan_any(kLnBwd, dtype, lmode != 2, true, rows, cols, pl, max_partials, ft < 0 ? -1 : ft);
   }
   if (st != RR_OK) return st;
   *ws_bytes = (size_t)pl->partials * (rms ? 1 : 2) * (size_t)cols * sizeof(float);
@@ -901,7 +962,7 @@ static size_t norm_bwd_workspace_size(bool rms, int64_t rows, int64_t cols, rr_d
     if (norm_bwd_plan(rms, rows, cols, dtype, m, &pl, &ws) == RR_OK && ws > best) best = ws;
   }
   SpanPlan sp;  // short rows with 16-byte aligned tensors: one partial per span block
-  if (span_plan(dtype, rms ? 8 : 7, rows, cols, false, INT64_MAX, &sp) == RR_OK) {
+  if (forced_tier() <= 0 && span_plan(dtype, rms ? 8 : 7, rows, cols, false, INT64_MAX, &sp) == RR_OK) {
     const size_t ws = (size_t)sp.grid * (rms ? 1 : 2) * (size_t)cols * sizeof(float);
     if (ws > best) best = ws;
   }
@@ -973,7 +1034,8 @@ static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* 
                       static_cast<float>(1.0 / static_cast<double>(cols))};
     SpanPlan sp;
     st = RR_ERR_INVALID_ARG;
-    if (aligned(dy, 16) && aligned(x, 16) && aligned(dx, 16)) {
+    const int ft = forced_tier();
+    if (ft <= 0 && aligned(dy, 16) && aligned(x, 16) && aligned(dx, 16)) {
       const bool stats_al = aligned(rstd, 16) && (rms || aligned(mean, 16));
       st = span_plan(dtype, rms ? 8 : 7, rows, cols, stats_al, max_partials, &sp);
       if (st != RR_OK && st != RR_ERR_INVALID_ARG) return st;
