@@ -202,11 +202,10 @@ size_t rr_rmsnorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtype)
  *   (16-byte aligned), owned by the caller; its contents on entry are ignored.
  * A row with rstd == 0 gets dx = 0 and adds nothing to dgamma, which is summed
  * over rows in a fixed order (deterministic for a given device and shape).
- * Rows must fit one row group in shared memory: at least 8192 columns for
- * fp32 and bf16, somewhat more depending on dtype and alignment (about 12 K
- * bf16 columns with 16-byte aligned gamma); longer rows return
- * RR_ERR_INVALID_ARG (and the size query returns 0 when no alignment mode
- * holds them).
+ * Rows must fit one row group (at least 8192 columns) or, with 16-byte
+ * aligned gamma, a thread-block cluster of up to 8 row groups (beyond 65536
+ * columns for fp32 and bf16); longer rows return RR_ERR_INVALID_ARG (and the
+ * size query returns 0 when no alignment mode holds them).
  */
 rr_status rr_rmsnorm_bwd(const void *dy, const void *x, const float *rstd,
                          const void *gamma, void *dx, void *dgamma, void *workspace,

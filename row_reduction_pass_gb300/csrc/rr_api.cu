@@ -397,7 +397,8 @@ rr_status ln_rowgroup_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int6
 // fit: the wide 256-thread variant first, then the least estimated time, rounds
 // of rows (rows / clusters resident on the device) x (chunks per thread + 2 for
 // the per-row reductions).
-rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64_t cols, Plan* pl) {
+rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64_t cols, Plan* pl,
+                          int64_t max_partials = INT64_MAX) {
   std::lock_guard<std::mutex> lock(g_mu);
   DevInfo* di = nullptr;
   rr_status st = device_info(&di);
@@ -406,14 +407,17 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
   const int E = dt == RR_BF16 ? 2 : 4;
   const int W = lmode == 2 ? 1 : 16 / E;
   const int nq = ls.nq[lmode];
-  const int planes = op == kLnFwd ? 2 : 1;
+  const bool fwdop = op == kLnFwd || op == kRmsFwd;
+  const int planes = op == kLnFwd ? 2 : 1;           // gamma (, beta) staged as fp32
+  const int kp = fwdop ? 0 : op == kLnBwd ? 2 : 1;  // backward: planes of column partials
+  const int ntens = fwdop ? 1 : 2;
   // RR_LN_CLUSTER="K:v" forces cluster size K and variant v (0..3: 256, 512,
   // 1024 threads, or the wide 256-thread one) when that pair fits (tuning aid).
   int forceK = 0, forceV = -1;
   if (const char* f = std::getenv("RR_LN_CLUSTER")) std::sscanf(f, "%d:%d", &forceK, &forceV);
   struct Choice {
     int K = 0, T = 0, ncl = 0;
-    int64_t S = 0, nchs = 0, smem = 0, red_off = 0, cl_off = 0, pf_off = 0;
+    int64_t S = 0, nchs = 0, smem = 0, red_off = 0, cl_off = 0, acc_off = 0, pf_off = 0;
     const void* fn = nullptr;
     double cost = 0.0;
   } best;
@@ -425,15 +429,17 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
     for (int gi = 0; gi < 4; ++gi) {
       if (forceV >= 0 && gi != forceV) continue;
       const int T = gi < 3 ? 256 << gi : 256;
-      const int nqv = gi < 3 ? nq : 2 * nq;  // [3]: the wide 256-thread variant
+      // forward [3]: the wide 256-thread variant; backward: the deep chunk count
+      const int nqv = fwdop ? (gi < 3 ? nq : 2 * nq) : ls.nqd;
       const void* fn = ls.kc[lmode][gi];
       if (fn == nullptr || (int64_t)nqv * T < nchs) continue;
       const int64_t red_off = round_up(planes * npad * 4, 16);
       const int64_t cl_off = round_up(red_off + 1024, 16);
-      const int64_t pf_off = round_up(cl_off + 32, 16);
+      const int64_t acc_off = round_up(cl_off + 32, 16);
+      const int64_t pf_off = round_up(acc_off + (int64_t)kp * npad * 4, 16);
       int64_t pf_bytes = 0;
-      if (lmode == 0) pf_bytes = (int64_t)2 * nqv * 16 * T;
-      if (lmode == 1) pf_bytes = (int64_t)2 * (nchs + 2) * 16;
+      if (lmode == 0) pf_bytes = (int64_t)2 * ntens * nqv * 16 * T;
+      if (lmode == 1) pf_bytes = (int64_t)2 * ntens * (nchs + 2) * 16;
       const int64_t smem = pf_off + pf_bytes;
       if (smem > di->smem_optin) continue;
       if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
@@ -460,7 +466,7 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
       // the per-row reductions are paid by half as many threads) beats the others
       // wherever it fits, so it is ranked first; among equals, rounds x chunks
       const double rounds = (double)cdiv(rows, ncl);
-      const double cost = rounds * (double)(cdiv(nchs, T) + 2) + (gi == 3 ? 0.0 : 1e9);
+      const double cost = rounds * (double)(cdiv(nchs, T) + 2) + (fwdop && gi != 3 ? 1e9 : 0.0);
       if (best.K == 0 || cost < best.cost - 1e-9) {
         best.K = K;
         best.T = T;
@@ -470,6 +476,7 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
         best.smem = smem;
         best.red_off = red_off;
         best.cl_off = cl_off;
+        best.acc_off = acc_off;
         best.pf_off = pf_off;
         best.fn = fn;
         best.cost = cost;
@@ -484,7 +491,9 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
   pl->T = best.T;
   pl->K = best.K;
   pl->fn = best.fn;
-  pl->grid = (int64_t)best.K * (rows < best.ncl ? rows : best.ncl);
+  int64_t nc = rows < best.ncl ? rows : best.ncl;
+  if (nc > max_partials) nc = max_partials;  // the backward writes one partial row per cluster
+  pl->grid = (int64_t)best.K * nc;
   pl->smem = (size_t)best.smem;
   pl->partials = pl->grid / best.K;
   pl->lgeo = rr::LnGeo{rows,
@@ -493,7 +502,7 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
                        0,
                        (int32_t)best.nchs,
                        (int32_t)best.red_off,
-                       (int32_t)best.cl_off,
+                       (int32_t)best.acc_off,
                        (int32_t)best.pf_off,
                        (int32_t)best.S,
                        (int32_t)best.cl_off};
@@ -515,8 +524,9 @@ rr_status plan_any(OpKind op, rr_dtype dt, bool chunk_ok, bool head_free, int64_
 // so tests can run each tier on any shape it can hold: 0 spans of short rows,
 // 1 a row in registers (engine direct variants, LayerNorm / RMSNorm row
 // groups), 2 staged rows, one per CTA, 3 cluster-split rows (LayerNorm /
-// RMSNorm forward: clusters of row groups; otherwise the staged engine with
-// K >= 2).  A shape the forced tier cannot hold fails with RR_ERR_INVALID_ARG.
+// RMSNorm: clusters of row groups, the LayerNorm backward falling back to the
+// staged engine with K >= 2; softmax family: the staged engine with K >= 2).
+// A shape the forced tier cannot hold fails with RR_ERR_INVALID_ARG.
 // Returns -1 when unset, -2 for a value outside those.
 static int forced_tier() {
   const char* f = std::getenv("RR_FORCE_TIER");
@@ -932,16 +942,19 @@ static rr_status norm_bwd_plan(bool rms, int64_t rows, int64_t cols, rr_dtype dt
   const int ft = forced_tier();
   if (ft == -2) return bad_tier();
   if (ft == 0) return no_span(cols);
-  if (rms && ft >= 2)
-    return fail(RR_ERR_INVALID_ARG, "tier %d has no RMSNorm backward kernel", ft);
+  if (rms && ft == 2)
+    return fail(RR_ERR_INVALID_ARG, "tier 2 (staged rows) has no RMSNorm backward kernel");
   rr_status st = RR_ERR_INVALID_ARG;
   if (ft < 0 || ft == 1)
     st = ln_rowgroup_plan(rms ? kRmsBwd : kLnBwd, dtype, lmode, rows, cols, pl, max_partials);
+  // rows longer than one row group: clusters of row groups (chunk mode)
+  if ((ft < 0 && st == RR_ERR_INVALID_ARG) || ft == 3)
+    st = ln_cluster_plan(rms ? kRmsBwd : kLnBwd, dtype, lmode, rows, cols, pl, max_partials);
   if (st == RR_ERR_INVALID_ARG && ft != 1) {
     if (rms)
       return fail(RR_ERR_INVALID_ARG,
-                  "RMSNorm rows of %lld columns are longer than one row group holds",
-                  (long long)cols);
+                  "RMSNorm backward rows of %lld columns fit neither one row group nor a "
+                  "cluster of them (16-byte aligned gamma)", (long long)cols);
     st = plan_any(kLnBwd, dtype, lmode != 2, true, rows, cols, pl, max_partials, ft < 0 ? -1 : ft);
   }
   if (st != RR_OK) return st;

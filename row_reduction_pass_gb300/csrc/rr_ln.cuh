@@ -634,28 +634,44 @@ __global__ void __launch_bounds__(MAXT, ln_fwd_min_blocks<MAXT, NQ>())
 // only by the thread owning its chunk), and g and xhat are recomputed from the
 // stored chunks for dx instead of being held: far fewer registers, so fewer
 // threads per row and more rows in flight per SM.
-template <int DT, int W, int G, int NQ, bool AL, int MAXT, bool RMS, bool SA = false>
+template <int DT, int W, int G, int NQ, bool AL, int MAXT, bool RMS, bool SA = false,
+          bool CL = false>
 __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
     ln_bwd_kernel(const LnBwdParams p, const LnGeo geo) {
   constexpr bool PF = AL && W > 1;
   constexpr bool PFR = !AL && W > 1 && NQ > 1;  // one-chunk variants: no room
   constexpr int E = DType<DT>::E;
   extern __shared__ __align__(128) unsigned char smem[];
+  int K = 1, rank = 0;
+  if constexpr (CL) {
+    K = static_cast<int>(cluster_nrank());
+    rank = static_cast<int>(cluster_rank());
+  }
+  // this block's columns: the whole row, or its slice of a clustered row
+  const int c0 = rank * geo.slice;
+  const int ncols = CL ? min(geo.slice, geo.cols - c0) : geo.cols;
+  const int nfull = CL ? ncols / W : geo.nfull;
+  const int rag = CL ? ncols - nfull * W : geo.rag;
+  const int nchb = CL ? nfull + (rag > 0 ? 1 : 0) : geo.nch;
+  const int64_t coff = (int64_t)c0 * E;
   const int npad = geo.nch * W;
   const int npl = W >= 4 ? geo.nch * 4 : geo.nch;
   const LnPlanes<W> sg{reinterpret_cast<float*>(smem), npl};
-  ln_stage<DT, W>(sg, p.gamma, geo.cols, geo.nch);
+  ln_stage<DT, W>(sg, p.gamma + coff, ncols, nchb);
   __syncthreads();
 
   constexpr int ngroups = MAXT / G;
   const int grp = threadIdx.x / G, gt = threadIdx.x % G;
   LnCols<G, NQ> cs;
-  cs.init(gt, geo.nfull, geo.rag);
+  cs.init(gt, nfull, rag);
   LnRed<G> rd{smem + geo.red_off + grp * 1024, 0, 1 + grp};
-  const int64_t step = (int64_t)gridDim.x * ngroups;
-  const int64_t r0 = (int64_t)blockIdx.x * ngroups + grp;
-  const int64_t w0 = (int64_t)blockIdx.x * ngroups + (G < 32 ? (threadIdx.x & ~31) / G : grp);
+  int ccalls = 0;
+  const int64_t blk = blockIdx.x / K;  // the block's (cluster's) index among row owners
+  const int64_t step = (int64_t)(gridDim.x / K) * ngroups;
+  const int64_t r0 = blk * ngroups + grp;
+  const int64_t w0 = blk * ngroups + (G < 32 ? (threadIdx.x & ~31) / G : grp);
   const int64_t rowb = (int64_t)geo.cols * E;
+  const int64_t sbytes = (int64_t)ncols * E;
   const int64_t nbytes = geo.rows * rowb;
 
   static_assert(!SA || W >= 4, "shared-memory partials are for chunk mode");
@@ -693,8 +709,8 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
   auto issue = [&](int64_t rr, int stage) {
     if constexpr (PF) {
       if (rr < geo.rows) {
-        const char* d0 = p.dy + rr * rowb;
-        const char* x0 = p.x + rr * rowb;
+        const char* d0 = p.dy + rr * rowb + coff;
+        const char* x0 = p.x + rr * rowb + coff;
 #pragma unroll
         for (int q = 0; q < NQ; ++q)
           if (q < cs.nf) {
@@ -704,8 +720,9 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
       }
     } else if constexpr (PFR) {
       const bool valid = rr < geo.rows;
-      rpd.issue(valid ? p.dy + rr * rowb : p.dy, rowb, p.dy, p.dy + nbytes, stage, gt, valid);
-      rpx.issue(valid ? p.x + rr * rowb : p.x, rowb, p.x, p.x + nbytes, stage, gt, valid);
+      rpd.issue(valid ? p.dy + rr * rowb + coff : p.dy, sbytes, p.dy, p.dy + nbytes, stage, gt,
+                valid);
+      rpx.issue(valid ? p.x + rr * rowb + coff : p.x, sbytes, p.x, p.x + nbytes, stage, gt, valid);
     }
     cp_async_commit();
   };
@@ -754,13 +771,13 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
           xv[q] = q < cs.nf ? *slot((int)(it & 1), 1, q) : make_uint4(0u, 0u, 0u, 0u);
         }
       } else if constexpr (PFR) {
-        if (!rpd.get(dv, (int)(it & 1), gt, cs, geo.rag))
-          ln_load<DT, W, G, NQ, AL>(dv, p.dy + r * rowb, gt, cs, geo.rag, p.dy, p.dy + nbytes);
-        if (!rpx.get(xv, (int)(it & 1), gt, cs, geo.rag))
-          ln_load<DT, W, G, NQ, AL>(xv, p.x + r * rowb, gt, cs, geo.rag, p.x, p.x + nbytes);
+        if (!rpd.get(dv, (int)(it & 1), gt, cs, rag))
+          ln_load<DT, W, G, NQ, AL>(dv, p.dy + r * rowb + coff, gt, cs, rag, p.dy, p.dy + nbytes);
+        if (!rpx.get(xv, (int)(it & 1), gt, cs, rag))
+          ln_load<DT, W, G, NQ, AL>(xv, p.x + r * rowb + coff, gt, cs, rag, p.x, p.x + nbytes);
       } else {
-        ln_load<DT, W, G, NQ, AL>(dv, p.dy + r * rowb, gt, cs, geo.rag, p.dy, p.dy + nbytes);
-        ln_load<DT, W, G, NQ, AL>(xv, p.x + r * rowb, gt, cs, geo.rag, p.x, p.x + nbytes);
+        ln_load<DT, W, G, NQ, AL>(dv, p.dy + r * rowb + coff, gt, cs, rag, p.dy, p.dy + nbytes);
+        ln_load<DT, W, G, NQ, AL>(xv, p.x + r * rowb + coff, gt, cs, rag, p.x, p.x + nbytes);
       }
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {
@@ -831,11 +848,12 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
         }
       }
     }
-    const Sum2 s = rd(Sum2{s1a + s1b, s2a + s2b}, MergeSum2());
+    Sum2 s = rd(Sum2{s1a + s1b, s2a + s2b}, MergeSum2());
+    if constexpr (CL) s = ln_cluster(s, MergeSum2(), smem + geo.cl_off, ccalls, K);
     if (!active) continue;
     const float a = s.s1 * p.inv_cols;
     const float b = s.s2 * p.inv_cols;
-    char* dxr = p.dx + r * rowb;
+    char* dxr = p.dx + r * rowb + coff;
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
       if (q < cs.nown) {
@@ -875,12 +893,13 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
         } else {
           f[0] = rstd * ((gv[q][0] - a) - hv[q][0] * b);
         }
-        ln_store<DT, W, G, NQ, AL>(dxr, gt, q, cs, geo.rag, f);
+        ln_store<DT, W, G, NQ, AL>(dxr, gt, q, cs, rag, f);
       }
     }
   }
 
   if constexpr (PF || PFR) cp_async_wait<0>();
+  if constexpr (CL) cluster_sync();  // peers may still read this block's slots
 
   // Column partials: each group's to shared memory (SA: already there), then
   // a fixed-order sum over the groups into this block's partial row.
@@ -898,16 +917,17 @@ __global__ void __launch_bounds__(MAXT, ln_bwd_min_blocks<MAXT, NQ>())
     }
   }
   __syncthreads();
+  // (clusters: the block's slice of its cluster's partial row)
   const float* all = reinterpret_cast<const float*>(smem + geo.acc_off);
-  float* out = p.ws + (int64_t)blockIdx.x * kPlanes * geo.cols;
-  for (int i = threadIdx.x; i < kPlanes * geo.cols; i += MAXT) {
-    const int half = i >= geo.cols ? 1 : 0;
-    const int j = i - half * geo.cols;
+  float* out = p.ws + blk * kPlanes * geo.cols + c0;
+  for (int i = threadIdx.x; i < kPlanes * ncols; i += MAXT) {
+    const int half = i >= ncols ? 1 : 0;
+    const int j = i - half * ncols;
     // column j of a group's region: SA planes of four columns, else in order
     const int o = SA ? half * npad + ((j % W) >> 2) * spl + (j / W) * 4 + (j & 3) : half * npad + j;
     float t = 0.f;
     for (int gi = 0; gi < ngroups; ++gi) t += all[(size_t)gi * kPlanes * npad + o];
-    out[i] = t;
+    out[(int64_t)half * geo.cols + j] = t;
   }
 }
 
@@ -923,6 +943,16 @@ void ln_fill_cluster(const void* (&row)[4]) {
   row[1] = (const void*)ln_fwd_kernel<DT, W, 512, NQ, AL, 512, RMS, true>;
   row[2] = (const void*)ln_fwd_kernel<DT, W, 1024, NQ, AL, 1024, RMS, true>;
   row[3] = (const void*)ln_fwd_kernel<DT, W, 256, 2 * NQ, AL, 256, RMS, true>;
+}
+
+// Clustered backward variants (chunk mode only): one group of 256 / 512 threads
+// per block with NQ chunks per thread and the column partials in shared memory.
+template <int DT, int W, int NQ, bool AL, bool RMS>
+void ln_fill_cluster_bwd(const void* (&row)[4]) {
+  row[0] = (const void*)ln_bwd_kernel<DT, W, 256, NQ, AL, 256, RMS, true, true>;
+  row[1] = (const void*)ln_bwd_kernel<DT, W, 512, NQ, AL, 512, RMS, true, true>;
+  row[2] = nullptr;
+  row[3] = nullptr;
 }
 
 template <int DT, int W, int NQ, bool AL, bool FWD, int G, bool RMS, bool SA = false>
@@ -985,6 +1015,10 @@ LnKernelSet make_ln_set() {
   if constexpr (NQD > 0) {
     ln_fill_deep<DT, V, NQD, true, FWD, RMS>(s.kd[0]);
     ln_fill_deep<DT, V, NQD, false, FWD, RMS>(s.kd[1]);
+    if constexpr (!FWD) {
+      ln_fill_cluster_bwd<DT, V, NQD, true, RMS>(s.kc[0]);
+      ln_fill_cluster_bwd<DT, V, NQD, false, RMS>(s.kc[1]);
+    }
   }
   s.nqd = NQD;
   if constexpr (FWD) {

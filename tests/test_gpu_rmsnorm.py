@@ -78,9 +78,9 @@ def test_rmsnorm_rejects_rows_beyond_its_kernels():
     g = torch.ones(300000, device=dev)
     with pytest.raises(rr.RRError):
         rr.rr_rmsnorm_fwd(x, g, torch.empty_like(x), torch.empty(2, device=dev))
-    x = torch.zeros(4, 16385, device=dev)            # the backward holds 16384 fp32 columns
-    g = torch.ones(16385, device=dev)
-    assert rr.rr_rmsnorm_bwd_workspace_size(4, 16385, torch.float32) == 0
+    x = torch.zeros(4, 300000, device=dev)           # nor a cluster of backward row groups
+    g = torch.ones(300000, device=dev)
+    assert rr.rr_rmsnorm_bwd_workspace_size(4, 300000, torch.float32) == 0
     with pytest.raises(rr.RRError):
         rr.rr_rmsnorm_bwd(x, x, torch.ones(4, device=dev), g, torch.empty_like(x),
                           torch.empty_like(g), workspace=torch.empty(1 << 20, dtype=torch.uint8,

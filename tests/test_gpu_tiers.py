@@ -48,10 +48,10 @@ def holds(op: str, t: int, cols: int, e: int) -> bool:
     if t == 2:
         return not op.startswith("rms")  # no staged RMSNorm kernel
     # t == 3: a split into K >= 2 slices of whole 16-byte chunks needs a second
-    # slice with columns in it; no cluster-split RMSNorm backward
+    # slice with columns in it
     v = 16 // e
     half = -(-cols // 2)
-    return op != "rms_bwd" and (-(-half // v) * v) < cols
+    return (-(-half // v) * v) < cols
 
 
 def expect(op, t, cols, dtype, fn):
