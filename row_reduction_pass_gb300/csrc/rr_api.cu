@@ -561,7 +561,10 @@ static rr_status span_plan(rr_dtype dt, int mode, int64_t rows, int64_t cols, bo
                            int64_t max_grid, SpanPlan* sp) {
   const int E = dt == RR_BF16 ? 2 : 4;
   // the norm backward's spans hold two tensors: rows of up to 64 bytes
-  if (cols * E > (mode >= 7 ? 64 : 128) || rows <= 0 || max_grid < 1) return RR_ERR_INVALID_ARG;
+  // (RR_SPAN_MAX_BYTES overrides the 128-byte limit of the others: tuning aid)
+  int64_t lim = 128;
+  if (const char* f = std::getenv("RR_SPAN_MAX_BYTES")) lim = std::atoll(f);
+  if (cols * E > (mode >= 7 ? 64 : lim) || rows <= 0 || max_grid < 1) return RR_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
   DevInfo* di = nullptr;
   rr_status st = device_info(&di);
