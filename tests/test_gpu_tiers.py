@@ -41,8 +41,9 @@ def tier(t):
 def holds(op: str, t: int, cols: int, e: int) -> bool:
     """Whether forced tier t takes rows of `cols` elements of e bytes (16-byte
     aligned tensors) for operation `op`."""
-    if t == 0:
-        return cols * e <= (64 if op in ("ln_bwd", "rms_bwd") else 128)
+    if t == 0:  # rows of a byte length not a multiple of 16, up to 128 (norm backward 64)
+        rb = cols * e
+        return rb <= (64 if op in ("ln_bwd", "rms_bwd") else 128) and rb % 16 != 0
     if t == 1:
         return True  # every row length used here fits one row group
     if t == 2:
