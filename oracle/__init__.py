@@ -17,7 +17,10 @@ Definitions followed (page titles as published):
   * "gpu-ml-learning" README, Module 3 (softmax, cross-entropy).
 The online-softmax and Welford/Chan recurrences, whose equations were lost
 from the pages, are restated from Milakov & Gimelshein (2018), Welford (1962)
-and Chan, Golub & LeVeque (1979).
+and Chan, Golub & LeVeque (1979).  Attention (the pages' named extension of
+the online softmax, "Engineering a CUDA Machine Learning Framework from
+Scratch" sec. 6.4) is scaled dot-product attention as defined by Vaswani et
+al. (2017), computed here by its plain three-pass definition per query row.
 """
 from __future__ import annotations
 
@@ -89,6 +92,9 @@ def _load():
             lib.oracle_welford.restype = None
             lib.oracle_chan_merge.argtypes = [ctypes.c_double] * 6 + [_dp, _dp, _dp]
             lib.oracle_chan_merge.restype = None
+            lib.oracle_attention.argtypes = [_vp, _vp, _vp, ctypes.c_int, _i64, _i64, _i64,
+                                             ctypes.c_double, ctypes.c_int, _dp, _dp, _dp]
+            lib.oracle_attention.restype = None
             _lib = lib
     return _lib
 
@@ -271,3 +277,21 @@ def chan_merge(na, mean_a, m2a, nb, mean_b, m2b):
     _load().oracle_chan_merge(na, mean_a, m2a, nb, mean_b, m2b, ctypes.byref(n),
                               ctypes.byref(mean), ctypes.byref(m2))
     return n.value, mean.value, m2.value
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool = True):
+    """Scaled dot-product attention of [bh, s, d] arrays (float32 or bfloat16
+    bits), causal or not; returns (o [bh, s, d], lse [bh, s]) in float64."""
+    q, k, v = _c(q), _c(k), _c(v)
+    if not (q.shape == k.shape == v.shape and q.ndim == 3):
+        raise ValueError("q, k, v must share one [bh, s, d] shape")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one storage dtype")
+    bh, s, d = q.shape
+    o = np.empty((bh, s, d), np.float64)
+    lse = np.empty((bh, s), np.float64)
+    scratch = np.empty(max(1, s), np.float64)
+    _load().oracle_attention(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), bh, s, d,
+                             float(scale), 1 if causal else 0, _dptr(o), _dptr(lse),
+                             _dptr(scratch))
+    return o, lse

@@ -456,3 +456,47 @@ void oracle_chan_merge(double na, double mean_a, double m2a, double nb,
     *mean_out = mean_a + delta * nb / n;
     *m2_out = m2a + m2b + delta * delta * na * nb / n;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Scaled dot-product attention, forward [P1 sec. 6.4 and P3: the          */
+/* FlashAttention-style extension of the online softmax; the attention     */
+/* itself as defined by Vaswani et al. (2017)].  For each head b and query */
+/* row i: s_j = scale * sum_c q_ic k_jc over the keys j it may see (j <= i */
+/* when causal, all j otherwise), o_i = sum_j softmax(s)_j v_j and         */
+/* lse_i = m + log sum_j exp(s_j - m), m = max_j s_j.  The plain           */
+/* three-pass definition per row (scores, maximum and normaliser, output); */
+/* no tiling.  q, k, v: [bh][s][d] stored dtype; o: [bh][s][d] and         */
+/* lse: [bh][s] float64; scores: caller's scratch of s doubles.            */
+/* ---------------------------------------------------------------------- */
+void oracle_attention(const void *q, const void *k, const void *v, int dtype,
+                      int64_t bh, int64_t s, int64_t d, double scale, int causal,
+                      double *o, double *lse, double *scores)
+{
+    for (int64_t b = 0; b < bh; ++b) {
+        const int64_t base = b * s * d;
+        for (int64_t i = 0; i < s; ++i) {
+            const int64_t nk = causal ? i + 1 : s;
+            /* pass 1: scores and their maximum */
+            double m = -INFINITY;
+            for (int64_t j = 0; j < nk; ++j) {
+                double acc = 0.0;
+                for (int64_t c = 0; c < d; ++c)
+                    acc += load_elem(q, dtype, base + i * d + c) *
+                           load_elem(k, dtype, base + j * d + c);
+                scores[j] = scale * acc;
+                if (scores[j] > m) m = scores[j];
+            }
+            /* pass 2: normaliser */
+            double l = 0.0;
+            for (int64_t j = 0; j < nk; ++j) l += exp(scores[j] - m);
+            /* pass 3: output row */
+            for (int64_t c = 0; c < d; ++c) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < nk; ++j)
+                    acc += exp(scores[j] - m) * load_elem(v, dtype, base + j * d + c);
+                o[base + i * d + c] = acc / l;
+            }
+            lse[b * s + i] = m + log(l);
+        }
+    }
+}
