@@ -127,6 +127,32 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ peaks ----
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def bf16_peak(sustained: bool = False):
+    """Dense bf16 tensor TFLOP/s: MEASURED_PEAKS.json (burst or sustained), else
+    the fallback figure."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                d = json.load(f)
+            k = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+            if d.get(k):
+                return float(d[k]), "measured"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def attn_flops(bh: int, seq: int, d: int, causal: bool) -> float:
+    """Algorithmic flops of attention: two products of 2 * d flops per visible
+    (query, key) pair."""
+    pairs = seq * (seq + 1) // 2 if causal else seq * seq
+    return 4.0 * bh * d * pairs
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -613,6 +639,23 @@ def run_sweep(args):
                 report(name, "rms_fwd+bwd", rf + rb, tf + tb)
         del d
         torch.cuda.empty_cache()
+    if not args.cases or "attention" in args.cases:
+        # the online softmax extended to causal attention: 8 batches x 16 heads
+        # x 512 queries (the causal softmax's shape), head_dim 64 and 128, bf16
+        tpk, tsrc = bf16_peak()
+        for d_head in (64, 128):
+            bh, seq = 128, 512
+            q, k, v = (tdev(a) for a in synth.attn_inputs(bh, seq, d_head, 31 + d_head))
+            o = torch.empty_like(q)
+            lse = torch.empty((bh, seq), device=dev)
+            ms = timed(lambda: rr.rr_attention_fwd(q, k, v, o, lse, causal=True))
+            fl = attn_flops(bh, seq, d_head, True)
+            print(json.dumps({"case": f"attention_bf16_{bh}x{seq}x{d_head}_causal", "op": "attention",
+                              "flops": fl, "us": round(ms * 1e3, 2),
+                              "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+                              "frac_of_tensor_peak": round(fl / (ms * 1e-3) / 1e12 / tpk, 4),
+                              "tensor_peak": tpk, "peak_source": tsrc}), flush=True)
+            del q, k, v, o, lse
     if not args.cases or "graph" in args.cases:
         run_graph_lines(rr, torch, dev)
 

@@ -240,6 +240,26 @@ rr_status rr_layernorm_bwd_noalloc(const void *dy, const void *x, const float *m
                                    rr_dtype dtype, cudaStream_t stream);
 
 /*
+ * Scaled dot-product attention forward, causal or not, built on the online
+ * softmax: the extension the source names for it ("Engineering a CUDA Machine
+ * Learning Framework from Scratch", sec. 6.4, FlashAttention-style fusion of
+ * the sec. 3.1 online normaliser; attention as defined by Vaswani et al.
+ * 2017).  For each head b and query row i:
+ *   s_j = scale * q_i . k_j over the keys j it may see (j <= i when causal),
+ *   o_i = sum_j softmax(s)_j v_j,   lse_i = log sum_j exp(s_j).
+ *   q, k, v, o : [bh x seq x head_dim] bf16 (dtype must be RR_BF16), 16-byte
+ *   aligned, o must not overlap q, k or v.  lse : [bh x seq] float32, or NULL.
+ *   head_dim : 64 or 128;  seq : a multiple of 64;  scale > 0 (usually
+ *   1 / sqrt(head_dim)).
+ * Products on the tensor cores (bf16 in, fp32 accumulate), softmax in fp32,
+ * P rounded to bf16 for P V.  Other shapes or dtypes return
+ * RR_ERR_INVALID_ARG / RR_ERR_UNSUPPORTED_DTYPE; bh == 0 or seq == 0 is a no-op.
+ */
+rr_status rr_attention_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int64_t bh, int64_t seq, int64_t head_dim, float scale, int causal,
+                           rr_dtype dtype, cudaStream_t stream);
+
+/*
  * Reads (and if `reset` is non-zero clears) the error word of `device` that
  * the kernels set when a bounded wait gives up.  *value receives 0 or an
  * rr_status such as RR_ERR_DEVICE_TIMEOUT.  Synchronous: it waits for the

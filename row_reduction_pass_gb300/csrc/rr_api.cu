@@ -1119,6 +1119,47 @@ rr_status rr_rmsnorm_bwd(const void* dy, const void* x, const float* rstd, const
                   workspace_bytes, rows, cols, dtype, stream, INT64_MAX);
 }
 
+rr_status rr_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int64_t bh, int64_t seq, int64_t head_dim, float scale, int causal,
+                           rr_dtype dtype, cudaStream_t stream) {
+  if (dtype != RR_BF16)
+    return fail(RR_ERR_UNSUPPORTED_DTYPE, "attention takes bf16 q, k, v (tensor-core path)");
+  if (bh < 0 || seq < 0) return fail(RR_ERR_INVALID_ARG, "negative size");
+  if (bh == 0 || seq == 0) return ok();
+  if (seq % 64 != 0) return fail(RR_ERR_INVALID_ARG, "seq must be a multiple of 64");
+  if (bh > 65535) return fail(RR_ERR_INVALID_ARG, "at most 65535 heads per call");
+  if (seq > (int64_t)64 * 65535) return fail(RR_ERR_INVALID_ARG, "seq too long");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RR_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (!q || !k || !v || !o) return fail(RR_ERR_INVALID_ARG, "null pointer");
+  const rr::AttnKernel ak = rr::attn_fwd_kernel_for((int)head_dim);
+  if (ak.fn == nullptr) return fail(RR_ERR_INVALID_ARG, "head_dim must be 64 or 128");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      (lse != nullptr && !aligned(lse, 4)))
+    return fail(RR_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned");
+  const size_t n = (size_t)bh * seq * head_dim * 2, nl = (size_t)bh * seq * 4;
+  if (overlaps(o, n, q, n) || overlaps(o, n, k, n) || overlaps(o, n, v, n))
+    return fail(RR_ERR_ALIASING, "o overlaps q, k or v");
+  if (lse != nullptr && (overlaps(lse, nl, q, n) || overlaps(lse, nl, k, n) ||
+                         overlaps(lse, nl, v, n) || overlaps(lse, nl, o, n)))
+    return fail(RR_ERR_ALIASING, "lse overlaps a tensor");
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevInfo* di = nullptr;
+    rr_status st = device_info(&di);
+    if (st != RR_OK) return st;
+    if (ak.smem > di->smem_optin) return fail(RR_ERR_INVALID_ARG, "attention tile exceeds shared memory");
+    if ((st = set_smem(di, ak.fn, (size_t)ak.smem)) != RR_OK) return st;
+  }
+  rr::AttnParams p{static_cast<const char*>(q), static_cast<const char*>(k),
+                   static_cast<const char*>(v), static_cast<char*>(o), lse, seq,
+                   scale * 1.4426950408889634f, causal ? 1 : 0};
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchKernel(ak.fn, dim3((unsigned)(seq / 64), (unsigned)bh), dim3(128), args,
+                                   (size_t)ak.smem, stream);
+  if (e != cudaSuccess) return fail(RR_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 rr_status rr_read_device_error(int device, int* value, int reset) {
   if (!value) return fail(RR_ERR_INVALID_ARG, "null pointer");
   int prev = 0;

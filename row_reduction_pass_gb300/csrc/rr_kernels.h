@@ -62,6 +62,23 @@ LnKernelSet rms_fwd_rowgroup_kernels_f32();
 LnKernelSet rms_fwd_rowgroup_kernels_bf16();
 LnKernelSet rms_bwd_rowgroup_kernels_f32();
 LnKernelSet rms_bwd_rowgroup_kernels_bf16();
+// Scaled dot-product attention forward (k_attn.cu): bf16 [bh][seq][d]
+// tensors, scores scaled by scale_log2 = scale * log2 e.
+struct AttnParams {
+  const char* q;
+  const char* k;
+  const char* v;
+  char* o;
+  float* lse;  // [bh][seq] natural-log sum of exp of the scaled scores, or null
+  int64_t seq;
+  float scale_log2;
+  int32_t causal;
+};
+struct AttnKernel {
+  const void* fn;  // null for an unsupported head dimension
+  int smem;        // dynamic shared memory bytes
+};
+AttnKernel attn_fwd_kernel_for(int d);
 const void* col_reduce_kernel_ptr_f32();
 const void* col_reduce_kernel_ptr_bf16();
 

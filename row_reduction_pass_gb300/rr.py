@@ -83,6 +83,9 @@ def load_library():
         lib.rr_last_error_detail.restype = ctypes.c_char_p
         lib.rr_read_device_error.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), st]
         lib.rr_read_device_error.restype = st
+        lib.rr_attention_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_float,
+                                         ctypes.c_int, st, vp]
+        lib.rr_attention_fwd.restype = st
         _lib = lib
         return lib
 
@@ -162,6 +165,21 @@ def rr_log_softmax_bwd(z, dz, dx, stream=None):
     rows, cols = z.shape
     _check("rr_log_softmax_bwd", load_library().rr_log_softmax_bwd(
         _p(z), _p(dz), _p(dx), rows, cols, _dtype(z), _stream(stream)))
+
+
+def rr_attention_fwd(q, k, v, o, lse=None, scale=None, causal=True, stream=None):
+    """Scaled dot-product attention of [bh, seq, head_dim] bf16 tensors:
+    o = softmax(scale * q k^T (causal mask)) v, lse (fp32 [bh, seq]) optional;
+    scale defaults to 1 / sqrt(head_dim)."""
+    _contig(q, k, v, o)
+    if lse is not None:
+        _contig(lse)
+    bh, seq, d = q.shape
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    _check("rr_attention_fwd", load_library().rr_attention_fwd(
+        _p(q), _p(k), _p(v), _p(o), _p(lse), bh, seq, d, ctypes.c_float(scale),
+        1 if causal else 0, _dtype(q), _stream(stream)))
 
 
 def rr_layernorm_fwd(x, gamma, beta, y, mean, rstd, eps=1e-5, stream=None):

@@ -134,6 +134,19 @@ def causal_scores(batch: int, heads: int, queries: int, keys: int, dtype: str,
     return _store(a.reshape(rows, keys), dtype)
 
 
+def attn_inputs(bh: int, seq: int, head_dim: int, seed: int, sigma: float = 1.0):
+    """Attention q, k, v ~ N(0, sigma^2) as [bh, seq, head_dim] bfloat16 bits
+    (three independent streams of one seed)."""
+    n = bh * seq * head_dim
+    out = []
+    for stream in range(3):
+        a = standard_normal(n, seed, 10 + stream).reshape(bh, seq, head_dim)
+        if sigma != 1.0:
+            a *= np.float32(sigma)
+        out.append(_store(a, "bf16"))
+    return tuple(out)
+
+
 def ln_inputs(rows: int, cols: int, dtype: str, seed: int, row_offset: float = 0.0,
               gamma_mean: float = 1.0, gamma_std: float = 0.1, beta_std: float = 0.1,
               outlier_frac: float = 0.0, outlier_value: float = 1e4,

@@ -59,7 +59,7 @@ def host(t: torch.Tensor) -> np.ndarray:
 
 
 def compare(name: str, got: np.ndarray, ref: np.ndarray, rtol: float, atol: float,
-            scale: np.ndarray | None = None):
+            scale: np.ndarray | None = None, scale_rtol: float = 1e-5):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, f"{name}: shape {got.shape} != {ref.shape}"
@@ -68,7 +68,7 @@ def compare(name: str, got: np.ndarray, ref: np.ndarray, rtol: float, atol: floa
         err = np.abs(got - ref)
     bound = atol + rtol * np.abs(ref)
     if scale is not None:
-        bound = bound + 1e-5 * scale
+        bound = bound + scale_rtol * scale
     same_inf = np.isinf(got) & np.isinf(ref) & (np.sign(got) == np.sign(ref))
     ok = both_nan | same_inf | (err <= bound)
     if not ok.all():
