@@ -80,9 +80,11 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const AttnParams p) {
   uint16_t* ks = qs + kBr * LD;        // [2][kBc][LD]
   uint16_t* vs = ks + 2 * kBc * LD;    // [2][kBc][LD]
 
+  // grid (heads, query tiles): blocks are dispatched x fastest, so every head's
+  // heaviest causal tile (the most key tiles) goes out before any lighter one
   const int nq = static_cast<int>(p.seq / kBr);
-  const int qt = nq - 1 - static_cast<int>(blockIdx.x);  // heaviest (causal) tiles first
-  const int64_t head = blockIdx.y;
+  const int qt = nq - 1 - static_cast<int>(blockIdx.y);
+  const int64_t head = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;  // mma fragment row group / thread in group
   const int64_t hoff = head * p.seq * D * 2;  // bytes to this head

@@ -1127,7 +1127,7 @@ rr_status rr_attention_fwd(const void* q, const void* k, const void* v, void* o,
   if (bh < 0 || seq < 0) return fail(RR_ERR_INVALID_ARG, "negative size");
   if (bh == 0 || seq == 0) return ok();
   if (seq % 64 != 0) return fail(RR_ERR_INVALID_ARG, "seq must be a multiple of 64");
-  if (bh > 65535) return fail(RR_ERR_INVALID_ARG, "at most 65535 heads per call");
+  if (bh > INT32_MAX) return fail(RR_ERR_INVALID_ARG, "too many heads per call");
   if (seq > (int64_t)64 * 65535) return fail(RR_ERR_INVALID_ARG, "seq too long");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RR_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (!q || !k || !v || !o) return fail(RR_ERR_INVALID_ARG, "null pointer");
@@ -1154,7 +1154,7 @@ rr_status rr_attention_fwd(const void* q, const void* k, const void* v, void* o,
                    static_cast<const char*>(v), static_cast<char*>(o), lse, seq,
                    scale * 1.4426950408889634f, causal ? 1 : 0};
   void* args[] = {&p};
-  cudaError_t e = cudaLaunchKernel(ak.fn, dim3((unsigned)(seq / 64), (unsigned)bh), dim3(128), args,
+  cudaError_t e = cudaLaunchKernel(ak.fn, dim3((unsigned)bh, (unsigned)(seq / 64)), dim3(128), args,
                                    (size_t)ak.smem, stream);
   if (e != cudaSuccess) return fail(RR_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
   return ok();
