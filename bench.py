@@ -421,9 +421,22 @@ def _oracle_ncores(frac: float, n: int):
     procs = [ctx.Process(target=_oracle_part, args=(frac / n, barrier, results)) for _ in range(n)]
     for p in procs:
         p.start()
-    got = [results.get(timeout=900) for _ in procs]
-    for p in procs:
-        p.join(timeout=60)
+    got = []
+    deadline = time.monotonic() + 180.0
+    try:
+        while len(got) < n:
+            try:
+                got.append(results.get(timeout=1.0))
+            except Exception:  # queue.Empty: check that every worker is still going
+                if time.monotonic() > deadline or any(
+                        not p.is_alive() and p.exitcode not in (0, None) for p in procs):
+                    raise RuntimeError("an oracle worker failed or ran out of time")
+    finally:
+        for p in procs:
+            p.join(timeout=5)
+            if p.is_alive():
+                p.terminate()
+                p.join(timeout=5)
     return sum(g[0] for g in got), max(g[1] for g in got)
 
 
