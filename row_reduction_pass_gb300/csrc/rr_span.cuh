@@ -1,8 +1,11 @@
-// rr_span.cuh -- softmax, log-softmax and cross-entropy for short rows
-// (C x element size <= 128 bytes) as contiguous spans of rows per warp.
+// rr_span.cuh -- short rows as contiguous spans of rows per warp: softmax,
+// log-softmax and cross-entropy, the softmax / log-softmax backward, and the
+// LayerNorm / RMSNorm forward and backward, for rows whose byte length is not
+// a multiple of 16 (up to 128 bytes; 64 for the norm backward).
 //
 // With rows this short a row-group kernel moves only a few bytes per thread
-// per row, far too little in flight to cover DRAM latency.  Here each warp owns
+// per row, far too little in flight to cover DRAM latency, and a misaligned row
+// costs it funnel shifts or element loads.  Here each warp owns
 // a span of S = 32 x RPL consecutive rows (about 3 KB; a multiple of 16 bytes,
 // so spans start 16-byte aligned when the tensor does): its lanes copy the span
 // into the warp's shared-memory buffer with 16-byte cp.async copies, one span
