@@ -542,9 +542,9 @@ static rr_status no_span(int64_t cols) {
               "(64 for the norm backward), not %lld columns", (long long)cols);
 }
 
-// Short rows (cols * E <= 128 bytes, 64 for the norm backward; 16-byte aligned
-// row tensors): the span
-// kernels (rr_span.cuh), one warp per span of 32 x rpl rows of ~3 KB.  mode 0
+// Short misaligned rows (byte length not a multiple of 16, up to 128 bytes, 64
+// for the norm backward; 16-byte aligned row tensors): the span kernels
+// (rr_span.cuh), one warp per span of 32 x rpl rows of ~3 KB.  mode 0
 // softmax, 1 log-softmax, 2 cross-entropy, 3 softmax backward, 4 log-softmax
 // backward, 5 LayerNorm forward, 6 RMSNorm forward, 7 LayerNorm backward,
 // 8 RMSNorm backward.  aux_aligned: the labels (mode 2) or the row statistics
