@@ -10,6 +10,11 @@
  *   rr_softmax_xent_fwd_bwd  per-row cross-entropy loss and dlogits = softmax - onehot
  *   rr_layernorm_fwd         y = (x - mean) * rstd * gamma + beta, saving mean / rstd
  *   rr_layernorm_bwd         dx, dgamma, dbeta from the saved mean / rstd
+ * and, built on the same machinery:
+ *   rr_log_softmax_fwd, rr_softmax_bwd, rr_log_softmax_bwd   the softmax pair
+ *   rr_rmsnorm_fwd, rr_rmsnorm_bwd                           RMSNorm
+ *   rr_attention_fwd         causal scaled dot-product attention on the online softmax
+ *   rr_layernorm_bwd_noalloc the LayerNorm backward without a caller workspace
  *
  * Common conventions
  *   - Every tensor is dense, row-major [rows x cols] with row stride = cols
