@@ -26,7 +26,7 @@
  *   (1979).  They are here only so tests can check that they reach the
  *   three-pass / two-pass definitions (oracle_online_*, oracle_welford*).
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - variance is the biased (population) one, rstd = 1/sqrt(var + eps);
  *   - a softmax / cross-entropy row whose maximum is -inf (fully masked) gives
  *     zeros: y = 0, loss = 0, dlogits = 0;
