@@ -22,23 +22,23 @@ from parity import TOL, TOL_F32_OUT, check_ln, check_softmax, check_xent, compar
 pytestmark = pytest.mark.gpu
 
 
-def test_config1_xent_f32_64x1000():
+def test_xent_f32_64x1000():
     d = synth.make("xent_f32_64x1000")
     check_xent(d["logits"], d["labels"], "f32")
 
 
-def test_config2_layernorm_f32_4096x768():
+def test_layernorm_f32_4096x768():
     d = synth.make("ln_f32_4096x768")
     check_ln(d["x"], d["gamma"], d["beta"], d["dy"], d["eps"], "f32")
     check_ln(d["x"], d["gamma"], d["beta"], d["dy"], d["eps"], "f32", oracle_stats=False)
 
 
-def test_config3_causal_softmax_bf16_65536x512():
+def test_causal_softmax_bf16_65536x512():
     d = synth.make("softmax_bf16_causal_65536x512")
     check_softmax(d["x"], "bf16")
 
 
-def test_config4_lm_head_xent_bf16_16384x50304_in_place():
+def test_lm_head_xent_bf16_16384x50304_in_place():
     d = synth.make("xent_bf16_16384x50304")
     logits, labels = d["logits"], d["labels"]
     rows, cols = logits.shape
@@ -52,7 +52,7 @@ def test_config4_lm_head_xent_bf16_16384x50304_in_place():
     assert int(bad.item()) == 0
     rloss, _, rbad = oracle.xent(logits, labels, d["ignore_index"], want_dlogits=False)
     assert rbad == 0
-    compare("config4 loss (all rows)", host(loss), rloss, *TOL_F32_OUT)
+    compare("lm-head xent loss (all rows)", host(loss), rloss, *TOL_F32_OUT)
     ignored = np.nonzero(labels == d["ignore_index"])[0]
     assert ignored.size > 0
     sample_ign = torch.from_numpy(ignored[:64]).to(xd.device)
@@ -62,18 +62,18 @@ def test_config4_lm_head_xent_bf16_16384x50304_in_place():
     got = host(xd.index_select(0, torch.from_numpy(sample).to(xd.device)))
     _, rdl, _ = oracle.xent(logits[sample], labels[sample], d["ignore_index"])
     rtol, atol = TOL["bf16"]
-    compare("config4 dlogits (sampled rows)", got, rdl, rtol, atol)
+    compare("lm-head xent dlogits (sampled rows)", got, rdl, rtol, atol)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("cols", synth.SWEEP_COLS)
-def test_config5_sweep_xent(cols, dtype):
+def test_sweep_xent(cols, dtype):
     d = synth.make(f"sweep_xent_{dtype}_c{cols}")
     check_xent(d["logits"], d["labels"], dtype)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("cols", synth.SWEEP_COLS)
-def test_config5_sweep_layernorm(cols, dtype):
+def test_sweep_layernorm(cols, dtype):
     d = synth.make(f"sweep_ln_{dtype}_c{cols}")
     check_ln(d["x"], d["gamma"], d["beta"], d["dy"], d["eps"], dtype)
