@@ -142,8 +142,10 @@ rr_status rr_softmax_xent_fwd_bwd(const void *logits, const int32_t *labels,
  * LayerNorm forward ("Welford Single-Pass Normalization", sec. 3.2): per row,
  *   mean = (1/C) sum_j x_j,  var = (1/C) sum_j (x_j - mean)^2 (biased),
  *   rstd = 1 / sqrt(var + eps),  y_j = (x_j - mean) * rstd * gamma_j + beta_j,
- * the moments computed in one pass over global memory and merged across
- * threads with the Chan/Welford pairwise update.
+ * the moments from one pass over global memory: with the row (or its slice)
+ * held on chip, an exact mean from a compensated sum and then the squared
+ * deviations about it; the staged kernels for rows beyond one row group merge
+ * per-thread moments with the Chan/Welford pairwise update.
  *   x, y : [rows x cols] dtype (y == x allowed).  gamma, beta : [cols] dtype.
  *   mean, rstd : [rows] float32 outputs, saved for rr_layernorm_bwd.
  *   eps : >= 0 and finite.
@@ -163,8 +165,8 @@ size_t rr_layernorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtyp
  * xhat = (x - mean) * rstd and g = dy * gamma,
  *   dx_j     = rstd * (g_j - mean_j(g) - xhat_j * mean_j(g * xhat)),
  *   dgamma_j = sum_r dy_rj * xhat_rj,   dbeta_j = sum_r dy_rj.
- *   dy, x, dx : [rows x cols] dtype (dx may equal dy).  gamma, dgamma, dbeta :
- *   [cols] dtype.  mean, rstd : [rows] float32 from rr_layernorm_fwd.
+ *   dy, x, dx : [rows x cols] dtype (dx may equal dy or x).  gamma, dgamma,
+ *   dbeta : [cols] dtype.  mean, rstd : [rows] float32 from rr_layernorm_fwd.
  *   workspace : device scratch of workspace_bytes >= the size query's answer
  *   (16-byte aligned), owned by the caller; its contents on entry are ignored.
  * A row with rstd == 0 (masked by the forward) gets dx = 0 and adds nothing to
