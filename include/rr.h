@@ -144,8 +144,9 @@ rr_status rr_softmax_xent_fwd_bwd(const void *logits, const int32_t *labels,
  *   rstd = 1 / sqrt(var + eps),  y_j = (x_j - mean) * rstd * gamma_j + beta_j,
  * the moments from one pass over global memory: with the row (or its slice)
  * held on chip, an exact mean from a compensated sum and then the squared
- * deviations about it; the staged kernels for rows beyond one row group merge
- * per-thread moments with the Chan/Welford pairwise update.
+ * deviations about it (row groups, clusters of them, spans); the staged
+ * engine kernels, left for rows no row group holds with gamma / beta not
+ * 16-byte aligned, merge per-thread moments with the Chan/Welford update.
  *   x, y : [rows x cols] dtype (y == x allowed).  gamma, beta : [cols] dtype.
  *   mean, rstd : [rows] float32 outputs, saved for rr_layernorm_bwd.
  *   eps : >= 0 and finite.
@@ -203,7 +204,7 @@ size_t rr_rmsnorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtype)
  * RMSNorm backward (analytic derivative of rr_rmsnorm_fwd): with
  * xhat = x * rstd and g = dy * gamma,
  *   dx_j = rstd * (g_j - xhat_j * mean_j(g * xhat)),  dgamma_j = sum_r dy_rj * xhat_rj.
- *   dy, x, dx : [rows x cols] dtype (dx may equal dy).  gamma, dgamma : [cols]
+ *   dy, x, dx : [rows x cols] dtype (dx may equal dy or x).  gamma, dgamma : [cols]
  *   dtype.  rstd : [rows] float32 from rr_rmsnorm_fwd.
  *   workspace : device scratch of workspace_bytes >= the size query's answer
  *   (16-byte aligned), owned by the caller; its contents on entry are ignored.
