@@ -145,8 +145,8 @@ rr_status rr_softmax_xent_fwd_bwd(const void *logits, const int32_t *labels,
  * the moments from one pass over global memory: with the row (or its slice)
  * held on chip, an exact mean from a compensated sum and then the squared
  * deviations about it (row groups, clusters of them, spans); the staged
- * engine kernels, left for rows no row group holds with gamma / beta not
- * 16-byte aligned, merge per-thread moments with the Chan/Welford update.
+ * engine kernels, left for rows no row group or cluster of them takes, merge
+ * per-thread moments with the Chan/Welford update.
  *   x, y : [rows x cols] dtype (y == x allowed).  gamma, beta : [cols] dtype.
  *   mean, rstd : [rows] float32 outputs, saved for rr_layernorm_bwd.
  *   eps : >= 0 and finite.
