@@ -97,3 +97,26 @@ def test_header_documents_every_entry_point():
         m = re.search(r"\n[a-z][a-z_ ]*\*?\s*" + n + r"\s*\(", src)
         assert m, f"{n} is not declared at the start of a line"
         assert "*/" in src[max(0, m.start() - 400):m.start()], f"{n} has no comment block"
+
+
+def test_attention_argument_errors(lib):
+    fa = lib.rr_attention_fwd
+    q, k, v, o = (ctypes.c_void_p(a) for a in (0x100000, 0x200000, 0x300000, 0x400000))
+    sc = ctypes.c_float(0.125)
+    # dtype: fp32 has no tensor-core path here
+    assert fa(q, k, v, o, None, 2, 128, 64, sc, 1, 0, S0) == 2
+    assert fa(q, k, v, o, None, 0, 128, 64, sc, 1, 1, S0) == 0          # no heads: no-op
+    assert fa(q, k, v, o, None, 2, 96, 64, sc, 1, 1, S0) == 1           # seq % 64
+    assert fa(q, k, v, o, None, 2, 128, 96, sc, 1, 1, S0) == 1          # head_dim
+    assert fa(q, k, v, o, None, 2, 128, 64, ctypes.c_float(0.0), 1, 1, S0) == 1
+    assert fa(q, k, v, ctypes.c_void_p(0x400008), None, 2, 128, 64, sc, 1, 1, S0) == 1  # alignment
+    assert fa(q, k, v, q, None, 2, 128, 64, sc, 1, 1, S0) == 3          # o over q
+    assert fa(q, k, v, None, None, 2, 128, 64, sc, 1, 1, S0) == 1       # null
+
+
+def test_every_entry_point_has_a_binding():
+    bound = set(dir(b))
+    for n in declared_symbols():
+        if n in ("rr_last_error_detail",):
+            continue
+        assert n in bound, f"{n} has no Python binding of the same name"
