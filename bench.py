@@ -354,9 +354,10 @@ def run_ours(args, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16+f32 I/O, f32 accumulate",
+        "dtype": "f32",
         "data": "synthetic (seeded numpy PCG64, recipes in row_reduction_pass_gb300/synth.py)",
         "config": {"workload": WORKLOAD, "bytes_per_step": total_bytes,
+                   "storage": "bf16 and f32 tensors (per workload), f32 arithmetic",
                    "l2": "inputs larger than L2: the 3.3 GB xent pass streams through the "
                          "129 MB L2 every step", "frac_of_peak": round(value / world / peak, 4),
                    "parallelism": f"replicas x{world} (rows are independent; no collective)"},
@@ -514,7 +515,7 @@ def run_reference(args, rank, world):
     return {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (same seeded generators, row sample)",
             "config": {"workload": WORKLOAD, "sample_fraction": frac},
             "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1,
