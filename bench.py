@@ -36,8 +36,14 @@ from row_reduction_pass_gb300 import synth  # noqa: E402
 
 METRIC = "achieved HBM GB/s (% of GB300 peak) for softmax-xent & LayerNorm fwd+bwd"
 FALLBACK_HBM_GBS = 6800.0
+LN_BF16_COLS = (1000, 4097, 65537)   # the sweep's bf16 LayerNorm cases, 2^24 elements each
 WORKLOAD = ("hot-path step: LN fwd+bwd fp32 4096x768 + causal softmax fwd bf16 65536x512 + "
+            "LN fwd+bwd bf16 16777x1000, 4095x4097, 255x65537 (sweep cases) + "
             "softmax-xent fwd+bwd bf16 16384x50304 (in place, 5% ignored)")
+XENT_IN_PLACE = ("dlogits are written over the logits (the configuration's in-place call), so "
+                 "every step after the first reads the previous step's dlogits: the same bytes "
+                 "and the same work (the kernel's time does not depend on the values; ignored "
+                 "rows stay ignored)")
 
 
 # ------------------------------------------------------------ byte counts ----
@@ -197,22 +203,48 @@ def recorded_traffic(key: str):
 # ------------------------------------------------------------- the workload --
 
 def make_inputs(scale_rows: float = 1.0):
-    """Host arrays of the step's four workloads (rows scaled for samples)."""
-    ln = synth.make("ln_f32_4096x768", rows=max(1, int(4096 * scale_rows)))
-    sm = synth.make("softmax_bf16_causal_65536x512")
+    """Host arrays of the step's workloads (rows scaled for samples): config 2's
+    LayerNorm, config 3's causal softmax, the sweep's bf16 LayerNorm cases and
+    config 4's cross-entropy."""
+    def rows(n):
+        return max(1, int(n * scale_rows))
+    w = {"ln": synth.make("ln_f32_4096x768", rows=rows(4096))}
+    w["sm"] = synth.make("softmax_bf16_causal_65536x512")
     if scale_rows < 1.0:
-        sm["x"] = sm["x"][:max(1, int(65536 * scale_rows))]
-    xe = synth.make("xent_bf16_16384x50304", rows=max(1, int(16384 * scale_rows)))
-    return ln, sm, xe
+        w["sm"]["x"] = w["sm"]["x"][:rows(65536)]
+    for c in LN_BF16_COLS:
+        w[f"lnb{c}"] = synth.make(f"sweep_ln_bf16_c{c}", rows=rows((1 << 24) // c))
+    w["xe"] = synth.make("xent_bf16_16384x50304", rows=rows(16384))
+    return w
 
 
-def step_bytes(ln, sm, xe):
-    r, c = ln["x"].shape
+def step_bytes(w):
+    """Algorithmic bytes of every launch group of the step, in step order."""
+    r, c = w["ln"]["x"].shape
     lf, lb = ln_bytes(r, c, 4)
-    sb = softmax_bytes(*sm["x"].shape, 2)
+    out = {"ln_fwd": lf, "softmax": softmax_bytes(*w["sm"]["x"].shape, 2), "ln_bwd": lb}
+    for cc in LN_BF16_COLS:
+        bf, bb = ln_bytes(*w[f"lnb{cc}"]["x"].shape, 2)
+        out[f"ln_bf16_c{cc}_fwd"] = bf
+        out[f"ln_bf16_c{cc}_bwd"] = bb
+    xe = w["xe"]
     n_ign = int((xe["labels"] == synth.IGNORE_INDEX).sum())
-    xb = xent_bytes(*xe["logits"].shape, 2, n_ign)
-    return {"ln_fwd": lf, "softmax": sb, "ln_bwd": lb, "xent": xb}
+    out["xent"] = xent_bytes(*xe["logits"].shape, 2, n_ign)
+    return out
+
+
+def oracle_step(w):
+    """The float64 oracle over every workload of the step (CPU legs only)."""
+    import oracle
+    ln = w["ln"]
+    _, mean, rstd = oracle.ln_fwd(ln["x"], ln["gamma"], ln["beta"], ln["eps"])
+    oracle.softmax(w["sm"]["x"])
+    oracle.ln_bwd(ln["dy"], ln["x"], mean, rstd, ln["gamma"])
+    for c in LN_BF16_COLS:
+        b = w[f"lnb{c}"]
+        _, m, r = oracle.ln_fwd(b["x"], b["gamma"], b["beta"], b["eps"])
+        oracle.ln_bwd(b["dy"], b["x"], m, r, b["gamma"])
+    oracle.xent(w["xe"]["logits"], w["xe"]["labels"])
 
 
 def run_ours(args, rank, world):
@@ -222,62 +254,76 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(rank % max(1, torch.cuda.device_count()))
     dev = torch.device("cuda", torch.cuda.current_device())
     rr.load_library()
-    ln, sm, xe = make_inputs()
-    nbytes = step_bytes(ln, sm, xe)
+    w = make_inputs()
+    nbytes = step_bytes(w)
     total_bytes = sum(nbytes.values())
 
     def bf16(a):
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
 
+    def host(a):
+        return (bf16(a) if a.dtype == np.uint16 else torch.from_numpy(a)).pin_memory()
+
     # pinned host copies (for the end-to-end leg) and device-resident inputs
-    h = {
-        "ln_x": torch.from_numpy(ln["x"]).pin_memory(),
-        "ln_g": torch.from_numpy(ln["gamma"]).pin_memory(),
-        "ln_b": torch.from_numpy(ln["beta"]).pin_memory(),
-        "ln_dy": torch.from_numpy(ln["dy"]).pin_memory(),
-        "sm_x": bf16(sm["x"]).pin_memory(),
-        "xe_x": bf16(xe["logits"]).pin_memory(),
-        "xe_l": torch.from_numpy(xe["labels"]).pin_memory(),
-    }
+    h = {}
+    for k in ["ln"] + [f"lnb{c}" for c in LN_BF16_COLS]:
+        for t in ("x", "gamma", "beta", "dy"):
+            h[f"{k}_{t}"] = host(w[k][t])
+    h["sm_x"] = host(w["sm"]["x"])
+    h["xe_x"] = host(w["xe"]["logits"])
+    h["xe_l"] = host(w["xe"]["labels"])
     d = {k: v.to(dev) for k, v in h.items()}
-    R, C = ln["x"].shape
-    o = {
-        "ln_y": torch.empty_like(d["ln_x"]), "ln_mean": torch.empty(R, device=dev),
-        "ln_rstd": torch.empty(R, device=dev), "ln_dx": torch.empty_like(d["ln_x"]),
-        "ln_dg": torch.empty_like(d["ln_g"]), "ln_db": torch.empty_like(d["ln_g"]),
-        "sm_y": torch.empty_like(d["sm_x"]),
-        "xe_loss": torch.empty(xe["logits"].shape[0], device=dev),
-    }
-    ws = torch.empty(rr.rr_layernorm_bwd_workspace_size(R, C, torch.float32), dtype=torch.uint8,
-                     device=dev)
-    eps = ln["eps"]
+    o = {"sm_y": torch.empty_like(d["sm_x"]),
+         "xe_loss": torch.empty(w["xe"]["logits"].shape[0], device=dev)}
+    ws = {}
+    for k in ["ln"] + [f"lnb{c}" for c in LN_BF16_COLS]:
+        x = d[f"{k}_x"]
+        R, C = x.shape
+        o[f"{k}_y"], o[f"{k}_dx"] = torch.empty_like(x), torch.empty_like(x)
+        o[f"{k}_mean"] = torch.empty(R, device=dev)
+        o[f"{k}_rstd"] = torch.empty(R, device=dev)
+        o[f"{k}_dg"], o[f"{k}_db"] = torch.empty_like(d[f"{k}_gamma"]), torch.empty_like(
+            d[f"{k}_gamma"])
+        ws[k] = torch.empty(max(1, rr.rr_layernorm_bwd_workspace_size(R, C, x.dtype)),
+                            dtype=torch.uint8, device=dev)
+
+    def ln_fwd(k):
+        rr.rr_layernorm_fwd(d[f"{k}_x"], d[f"{k}_gamma"], d[f"{k}_beta"], o[f"{k}_y"],
+                            o[f"{k}_mean"], o[f"{k}_rstd"], eps=w[k]["eps"])
+
+    def ln_bwd(k):
+        rr.rr_layernorm_bwd(d[f"{k}_dy"], d[f"{k}_x"], o[f"{k}_mean"], o[f"{k}_rstd"],
+                            d[f"{k}_gamma"], o[f"{k}_dx"], o[f"{k}_dg"], o[f"{k}_db"], ws[k])
+
+    # the step, in order: (name, call, kernel launches); the names match nbytes
+    stages = [("ln_fwd", lambda: ln_fwd("ln"), 1),
+              ("softmax", lambda: rr.rr_softmax_fwd(d["sm_x"], o["sm_y"]), 1),
+              ("ln_bwd", lambda: ln_bwd("ln"), 2)]
+    for c in LN_BF16_COLS:
+        stages.append((f"ln_bf16_c{c}_fwd", (lambda k: lambda: ln_fwd(k))(f"lnb{c}"), 1))
+        stages.append((f"ln_bf16_c{c}_bwd", (lambda k: lambda: ln_bwd(k))(f"lnb{c}"), 2))
+    stages.append(("xent", lambda: rr.rr_softmax_xent_fwd_bwd(d["xe_x"], d["xe_l"],
+                                                               o["xe_loss"], d["xe_x"]), 1))
+    assert [n for n, _, _ in stages] == list(nbytes)
+    launches_per_step = sum(n for _, _, n in stages)
 
     def step(ev=None):
+        for i, (_, fn, _) in enumerate(stages):
+            if ev is not None:
+                ev[i].record()
+            fn()
         if ev is not None:
-            ev[0].record()
-        rr.rr_layernorm_fwd(d["ln_x"], d["ln_g"], d["ln_b"], o["ln_y"], o["ln_mean"],
-                            o["ln_rstd"], eps=eps)
-        if ev is not None:
-            ev[1].record()
-        rr.rr_softmax_fwd(d["sm_x"], o["sm_y"])
-        if ev is not None:
-            ev[2].record()
-        rr.rr_layernorm_bwd(d["ln_dy"], d["ln_x"], o["ln_mean"], o["ln_rstd"], d["ln_g"],
-                            o["ln_dx"], o["ln_dg"], o["ln_db"], ws)
-        if ev is not None:
-            ev[3].record()
-        rr.rr_softmax_xent_fwd_bwd(d["xe_x"], d["xe_l"], o["xe_loss"], d["xe_x"])  # in place
-        if ev is not None:
-            ev[4].record()
+            ev[len(stages)].record()
 
-    launches_per_step = 5  # LN fwd, softmax, LN bwd rows + column pass, xent
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    nst = len(stages)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
+           for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -290,30 +336,24 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     ms = t_start.elapsed_time(t_end)
-    per = {k: [] for k in ("ln_fwd", "softmax", "ln_bwd", "xent")}
-    for e in evs:
-        per["ln_fwd"].append(e[0].elapsed_time(e[1]))
-        per["softmax"].append(e[1].elapsed_time(e[2]))
-        per["ln_bwd"].append(e[2].elapsed_time(e[3]))
-        per["xent"].append(e[3].elapsed_time(e[4]))
+    per = {n: [e[i].elapsed_time(e[i + 1]) for e in evs] for i, (n, _, _) in enumerate(stages)}
     err = rr.rr.rr_read_device_error(torch.cuda.current_device())
 
     # end to end through the public API with host buffers: H2D of every input,
     # the step, D2H of the per-row loss and of dgamma / dbeta.
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    loss_h = torch.empty_like(o["xe_loss"], device="cpu").pin_memory()
-    dg_h = torch.empty_like(o["ln_dg"], device="cpu").pin_memory()
-    db_h = torch.empty_like(o["ln_db"], device="cpu").pin_memory()
+    outs = ["xe_loss"] + [f"{k}_{t}" for k in ["ln"] + [f"lnb{c}" for c in LN_BF16_COLS]
+                          for t in ("dg", "db")]
+    oh = {k: torch.empty_like(o[k], device="cpu").pin_memory() for k in outs}
     h2d = sum(v.numel() * v.element_size() for v in h.values())
-    d2h = sum(v.numel() * v.element_size() for v in (loss_h, dg_h, db_h))
+    d2h = sum(v.numel() * v.element_size() for v in oh.values())
 
     def e2e_step():
         for k, v in h.items():
             d[k].copy_(v, non_blocking=True)
         step()
-        loss_h.copy_(o["xe_loss"], non_blocking=True)
-        dg_h.copy_(o["ln_dg"], non_blocking=True)
-        db_h.copy_(o["ln_db"], non_blocking=True)
+        for k, v in oh.items():
+            v.copy_(o[k], non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -343,6 +383,14 @@ def run_ours(args, rank, world):
         kernels[k] = {"ms_median": round(t, 5), "bytes": nbytes[k],
                       "gbs": round(nbytes[k] / (t * 1e-3) / 1e9, 1),
                       "frac_of_peak": round(nbytes[k] / (t * 1e-3) / 1e9 / peak, 4)}
+    # LayerNorm fwd+bwd pairs: (bytes_fwd + bytes_bwd) / (t_fwd + t_bwd)
+    for pre in ["ln"] + [f"ln_bf16_c{c}" for c in LN_BF16_COLS]:
+        f, b = kernels[f"{pre}_fwd"], kernels[f"{pre}_bwd"]
+        t = f["ms_median"] + b["ms_median"]
+        nb = f["bytes"] + b["bytes"]
+        kernels[f"{pre}_fwd+bwd"] = {"ms_median": round(t, 5), "bytes": nb,
+                                     "gbs": round(nb / (t * 1e-3) / 1e9, 1),
+                                     "frac_of_peak": round(nb / (t * 1e-3) / 1e9 / peak, 4)}
     out = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -357,9 +405,11 @@ def run_ours(args, rank, world):
         "dtype": "f32",
         "data": "synthetic (seeded numpy PCG64, recipes in row_reduction_pass_gb300/synth.py)",
         "config": {"workload": WORKLOAD, "bytes_per_step": total_bytes,
+                   "xent_in_place": XENT_IN_PLACE,
                    "storage": "bf16 and f32 tensors (per workload), f32 arithmetic",
                    "l2": "inputs larger than L2: the 3.3 GB xent pass streams through the "
-                         "129 MB L2 every step", "frac_of_peak": round(value / world / peak, 4),
+                         "129 MB L2 every step (the LayerNorm and softmax inputs are read "
+                         "after it)", "frac_of_peak": round(value / world / peak, 4),
                    "parallelism": f"replicas x{world} (rows are independent; no collective)"},
         "kernels": kernels,
         "roofline": {"bound": "hbm", "achieved": round(x_gbs, 1), "peak": peak,
@@ -384,14 +434,10 @@ def run_ours(args, rank, world):
 def _oracle_sample(frac):
     """Run the oracle over `frac` of every workload of the step; returns
     (algorithmic bytes of the sample, seconds)."""
-    import oracle
-    ln, sm, xe = make_inputs(scale_rows=frac)
-    nb = sum(step_bytes(ln, sm, xe).values())
+    w = make_inputs(scale_rows=frac)
+    nb = sum(step_bytes(w).values())
     t0 = time.perf_counter()
-    _, mean, rstd = oracle.ln_fwd(ln["x"], ln["gamma"], ln["beta"], ln["eps"])
-    oracle.softmax(sm["x"])
-    oracle.ln_bwd(ln["dy"], ln["x"], mean, rstd, ln["gamma"])
-    oracle.xent(xe["logits"], xe["labels"])
+    oracle_step(w)
     return nb, time.perf_counter() - t0
 
 
@@ -400,14 +446,11 @@ def _oracle_part(frac, barrier, results):
     waits for every worker, then times the oracle over it."""
     import oracle
     oracle.build()
-    ln, sm, xe = make_inputs(scale_rows=frac)
-    nb = sum(step_bytes(ln, sm, xe).values())
+    w = make_inputs(scale_rows=frac)
+    nb = sum(step_bytes(w).values())
     barrier.wait()
     t0 = time.perf_counter()
-    _, mean, rstd = oracle.ln_fwd(ln["x"], ln["gamma"], ln["beta"], ln["eps"])
-    oracle.softmax(sm["x"])
-    oracle.ln_bwd(ln["dy"], ln["x"], mean, rstd, ln["gamma"])
-    oracle.xent(xe["logits"], xe["labels"])
+    oracle_step(w)
     results.put((nb, time.perf_counter() - t0))
 
 
@@ -494,19 +537,14 @@ def run_reference(args, rank, world):
     frac = 1 / 2048
     nb, t = _oracle_sample(frac)
     frac = max(1 / 65536, min(1.0, frac * budget / max(t, 1e-4)))
-    import oracle  # noqa: F401
-    ln, sm, xe = make_inputs(scale_rows=frac)
-    nb = sum(step_bytes(ln, sm, xe).values())
-    import oracle as orc
+    w = make_inputs(scale_rows=frac)
+    nb = sum(step_bytes(w).values())
     for _ in range(args.warmup):
-        _, m, r = orc.ln_fwd(ln["x"], ln["gamma"], ln["beta"], ln["eps"])
+        oracle_step(w)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _, m, r = orc.ln_fwd(ln["x"], ln["gamma"], ln["beta"], ln["eps"])
-        orc.softmax(sm["x"])
-        orc.ln_bwd(ln["dy"], ln["x"], m, r, ln["gamma"])
-        orc.xent(xe["logits"], xe["labels"])
+        oracle_step(w)
         times.append(time.perf_counter() - t0)
     tot = sum(times)
     value = nb * args.steps / tot / 1e9

@@ -15,6 +15,7 @@
  *   rr_rmsnorm_fwd, rr_rmsnorm_bwd                           RMSNorm
  *   rr_attention_fwd         causal scaled dot-product attention on the online softmax
  *   rr_layernorm_bwd_noalloc the LayerNorm backward without a caller workspace
+ *   rr_selftest_bounded_wait, rr_read_device_error   the bounded device waits
  *
  * Common conventions
  *   - Every tensor is dense, row-major [rows x cols] with row stride = cols
@@ -34,6 +35,11 @@
  *     rr_last_error_detail()); faults during execution surface at the caller's
  *     next synchronisation.  No C++ exception crosses this ABI.
  *   - rows == 0 is a no-op returning RR_OK.  cols must be >= 1.
+ *   - Per-device state (attributes, the device addresses of the library's
+ *     error word and scratch array) is resolved on the first call on a device
+ *     and kept for the life of the process: it assumes the device's primary
+ *     context lives that long.  After cudaDeviceReset of a device, do not call
+ *     the library on that device again in the same process.
  *   - Waits inside the kernels are bounded; a wait that gives up records
  *     RR_ERR_DEVICE_TIMEOUT in a per-device error word read by
  *     rr_read_device_error(), and the kernel returns instead of hanging.
@@ -188,8 +194,9 @@ rr_status rr_layernorm_bwd(const void *dy, const void *x, const float *mean,
  *   x, y : [rows x cols] dtype (y == x allowed).  gamma : [cols] dtype.
  *   rstd : [rows] float32 output, saved for rr_rmsnorm_bwd.  eps : >= 0, finite.
  * A row whose mean square is not finite is masked: y = 0, rstd = 0.  Rows must
- * fit one row group of threads: up to 16384 columns (32768 for bf16 with a
- * 16-byte aligned gamma); longer rows return RR_ERR_INVALID_ARG.
+ * fit one row group of threads or a thread-block cluster of up to 8 row groups
+ * (at least 65537 columns for fp32 and bf16, in every alignment); longer rows
+ * return RR_ERR_INVALID_ARG.
  */
 rr_status rr_rmsnorm_fwd(const void *x, const void *gamma, void *y, float *rstd,
                          int64_t rows, int64_t cols, float eps, rr_dtype dtype,
@@ -235,6 +242,8 @@ rr_status rr_rmsnorm_bwd(const void *dy, const void *x, const float *rstd,
  *     than 8 MiB holds, so shapes whose rr_layernorm_bwd plan would need more
  *     run with fewer row groups.  Rows too long for even one partial
  *     (cols > 1048576) return RR_ERR_WORKSPACE_TOO_SMALL.
+ *   - Arguments are checked on the host first, with the same statuses as
+ *     rr_layernorm_bwd; only then is the device touched.
  *   - The first call on each device resolves the scratch's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
@@ -266,6 +275,19 @@ rr_status rr_layernorm_bwd_noalloc(const void *dy, const void *x, const float *m
 rr_status rr_attention_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                            int64_t bh, int64_t seq, int64_t head_dim, float scale, int causal,
                            rr_dtype dtype, cudaStream_t stream);
+
+/*
+ * Self-test of the bounded device-side waits (a diagnostic of this library;
+ * the pages have no counterpart).  Launches one block that arms an mbarrier
+ * for 16 bytes of bulk-copy data that no copy ever delivers and waits on it
+ * with the same bounded wait the kernels use, giving up after limit_ns
+ * nanoseconds of device time (1 .. 10^9; otherwise RR_ERR_INVALID_ARG).  The
+ * wait gives up, RR_ERR_DEVICE_TIMEOUT is recorded in the current device's
+ * error word (see rr_read_device_error) and the block returns; no memory of
+ * the caller is touched and the context stays usable.  Asynchronous on
+ * `stream`.
+ */
+rr_status rr_selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream);
 
 /*
  * Reads (and if `reset` is non-zero clears) the error word of `device` that

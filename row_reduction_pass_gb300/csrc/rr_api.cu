@@ -933,7 +933,8 @@ rr_status rr_rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
     st = ln_cluster_plan(kRmsFwd, dtype, lmode, rows, cols, &pl);
   if (ft >= 1 && st != RR_OK) return st;
   if (st == RR_ERR_INVALID_ARG)
-    return fail(RR_ERR_INVALID_ARG, "RMSNorm rows of %lld columns are longer than one row group holds",
+    return fail(RR_ERR_INVALID_ARG,
+                "RMSNorm rows of %lld columns fit neither one row group nor a cluster of 8 of them",
                 (long long)cols);
   if (st != RR_OK) return st;
   int* err = device_error_word();
@@ -1004,27 +1005,29 @@ size_t rr_rmsnorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtype)
 
 }  // extern "C"
 
-// LayerNorm (rms = false) or RMSNorm backward with at most max_partials column
-// partials (the no-allocation entry point sizes this to its fixed scratch).
-// RMSNorm has no mean and no dbeta (both null).
-static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* mean,
-                          const float* rstd, const void* gamma, void* dx, void* dgamma, void* dbeta,
-                          void* workspace, size_t workspace_bytes, int64_t rows, int64_t cols,
-                          rr_dtype dtype, cudaStream_t stream, int64_t max_partials) {
+// Host-side argument checks of the LayerNorm (rms = false) or RMSNorm
+// backward: shape, dtype, null pointers, alignment and overlap.  No device
+// call.  check_ws = false skips the workspace (the no-allocation entry point's
+// scratch lives inside the library and cannot overlap a caller's tensor).
+static rr_status norm_bwd_check(bool rms, const void* dy, const void* x, const float* mean,
+                                const float* rstd, const void* gamma, const void* dx,
+                                const void* dgamma, const void* dbeta, const void* workspace,
+                                size_t workspace_bytes, int64_t rows, int64_t cols, rr_dtype dtype,
+                                bool check_ws) {
   rr_status st = check_shape(rows, cols, dtype);
   if (st != RR_OK) return st;
   if (!dy || !x || (!rms && !mean) || !rstd || !gamma || !dx || !dgamma || (!rms && !dbeta) ||
-      !workspace)
+      (check_ws && !workspace))
     return fail(RR_ERR_INVALID_ARG, "null pointer");
   const size_t E = dtype == RR_BF16 ? 2 : 4;
   if (!aligned(dy, E) || !aligned(x, E) || !aligned(dx, E) || !aligned(gamma, E) || !aligned(dgamma, E) ||
-      !aligned(dbeta, E) || !aligned(mean, 4) || !aligned(rstd, 4) || !aligned(workspace, 16))
+      !aligned(dbeta, E) || !aligned(mean, 4) || !aligned(rstd, 4) ||
+      (check_ws && !aligned(workspace, 16)))
     return fail(RR_ERR_INVALID_ARG, "misaligned pointer (workspace needs 16 bytes)");
-  const int64_t planes = rms ? 1 : 2;
   const size_t n = (size_t)rows * cols * E, nc = (size_t)cols * E, nr = (size_t)rows * 4;
   if (dx != dy && overlaps(dx, n, dy, n)) return fail(RR_ERR_ALIASING, "dx and dy partially overlap");
   if (dx != x && overlaps(dx, n, x, n)) return fail(RR_ERR_ALIASING, "dx and x partially overlap");
-  const void* outs[] = {dgamma, dbeta, workspace};
+  const void* outs[] = {dgamma, dbeta, check_ws ? workspace : nullptr};
   const size_t outn[] = {nc, nc, workspace_bytes};
   const void* ins[] = {dy, x, mean, rstd, gamma, dx};
   const size_t inn[] = {n, n, nr, nr, nc, n};
@@ -1036,6 +1039,21 @@ static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* 
   }
   if (overlaps(dx, n, mean, nr) || overlaps(dx, n, rstd, nr) || overlaps(dx, n, gamma, nc))
     return fail(RR_ERR_ALIASING, "dx overlaps mean / rstd / gamma");
+  return RR_OK;
+}
+
+// LayerNorm (rms = false) or RMSNorm backward with at most max_partials column
+// partials (the no-allocation entry point sizes this to its fixed scratch).
+// RMSNorm has no mean and no dbeta (both null).
+static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* mean,
+                          const float* rstd, const void* gamma, void* dx, void* dgamma, void* dbeta,
+                          void* workspace, size_t workspace_bytes, int64_t rows, int64_t cols,
+                          rr_dtype dtype, cudaStream_t stream, int64_t max_partials) {
+  rr_status st = norm_bwd_check(rms, dy, x, mean, rstd, gamma, dx, dgamma, dbeta, workspace,
+                                workspace_bytes, rows, cols, dtype, true);
+  if (st != RR_OK) return st;
+  const size_t E = dtype == RR_BF16 ? 2 : 4;
+  const int64_t planes = rms ? 1 : 2;
   const bool al = aligned(gamma, 16);
   Plan pl;
   size_t need = 0;
@@ -1090,6 +1108,16 @@ static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* 
       cudaLaunchKernel(cr, dim3((unsigned)cdiv(planes * cols, 32)), dim3(1024), args, 0, stream);
   if (e != cudaSuccess) return fail(RR_ERR_CUDA, "column reduce launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+// The LayerNorm backward's argument checks without a workspace (no device
+// call), for the no-allocation entry point.
+rr_status layernorm_bwd_check_args(const void* dy, const void* x, const float* mean,
+                                   const float* rstd, const void* gamma, const void* dx,
+                                   const void* dgamma, const void* dbeta, int64_t rows,
+                                   int64_t cols, rr_dtype dtype) {
+  return norm_bwd_check(false, dy, x, mean, rstd, gamma, dx, dgamma, dbeta, nullptr, 0, rows, cols,
+                        dtype, false);
 }
 
 // rr_layernorm_bwd with at most max_partials column partials (the no-allocation
@@ -1157,6 +1185,37 @@ rr_status rr_attention_fwd(const void* q, const void* k, const void* v, void* o,
   cudaError_t e = cudaLaunchKernel(ak.fn, dim3((unsigned)bh, (unsigned)(seq / 64)), dim3(128), args,
                                    (size_t)ak.smem, stream);
   if (e != cudaSuccess) return fail(RR_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+}  // extern "C"
+
+namespace {
+
+// One thread arms an mbarrier for 16 transaction bytes that no copy delivers
+// and waits on it with the kernels' bounded wait; the wait gives up after
+// limit_ns, records RR_ERR_DEVICE_TIMEOUT in *err and the block returns.
+__global__ void selftest_wait_kernel(int* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  rr::mbar_init(&bar, 1);
+  rr::fence_mbar_init();
+  rr::mbar_arrive_expect_tx(&bar, 16);
+  rr::mbar_wait_bounded(&bar, 0, err, limit_ns);
+}
+
+}  // namespace
+
+extern "C" {
+
+rr_status rr_selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream) {
+  if (limit_ns < 1 || limit_ns > 1000000000LL)
+    return fail(RR_ERR_INVALID_ARG, "limit_ns must be in [1, 1e9]");
+  int* err = device_error_word();
+  if (!err) return RR_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(err, (uint64_t)limit_ns);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(RR_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

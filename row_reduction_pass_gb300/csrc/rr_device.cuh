@@ -325,18 +325,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Bounded wait on an mbarrier phase: gives up after ~1 s of wall time and
-// records RR_ERR_DEVICE_TIMEOUT (6) in *err instead of spinning forever.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* err) {
+// Bounded wait on an mbarrier phase: gives up after limit_ns of wall time
+// (~1 s by default) and records RR_ERR_DEVICE_TIMEOUT (6) in *err instead of
+// spinning forever.  The loop itself is bounded as well (2^32 polls), in case
+// the global timer does not advance.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* err,
+                                                  uint64_t limit_ns = 1000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 0;; ++it) {
+  for (uint32_t it = 0; it != 0xffffffffu; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && global_timer_ns() - t0 > 1000000000ull) {
-      atomicCAS(err, 0, 6);
-      return false;
-    }
+    if ((it & 63u) == 63u && global_timer_ns() - t0 > limit_ns) break;
   }
+  atomicCAS(err, 0, 6);
+  return false;
 }
 
 // Cluster primitives (distributed shared memory, no multicast).

@@ -34,6 +34,11 @@ void* g_ptr[kMaxDev];
 
 // Sets the detail string returned by rr_last_error_detail (defined in rr_api.cu).
 void rr_set_error_detail(const char* msg);
+// rr_layernorm_bwd's argument checks, workspace aside; no device call (rr_api.cu).
+rr_status layernorm_bwd_check_args(const void* dy, const void* x, const float* mean,
+                                   const float* rstd, const void* gamma, const void* dx,
+                                   const void* dgamma, const void* dbeta, int64_t rows,
+                                   int64_t cols, rr_dtype dtype);
 // rr_layernorm_bwd with at most max_partials column partials (rr_api.cu).
 rr_status layernorm_bwd_capped(const void* dy, const void* x, const float* mean, const float* rstd,
                                const void* gamma, void* dx, void* dgamma, void* dbeta,
@@ -44,17 +49,23 @@ extern "C" rr_status rr_layernorm_bwd_noalloc(const void* dy, const void* x, con
                                               const float* rstd, const void* gamma, void* dx,
                                               void* dgamma, void* dbeta, int64_t rows,
                                               int64_t cols, rr_dtype dtype, cudaStream_t stream) {
+  // Every argument is checked on the host before the device is touched, with
+  // the same statuses as rr_layernorm_bwd (cols is then in [1, 2^31]).
+  rr_status st =
+      layernorm_bwd_check_args(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, rows, cols, dtype);
+  if (st != RR_OK) return st;
   // One column partial is a row of dgamma and a row of dbeta sums in fp32; the
   // launch is planned with no more partials than the scratch holds (fewer
   // row groups than rr_layernorm_bwd would use when the columns are many).
-  const int64_t per_partial = cols > 0 ? 2 * cols * (int64_t)sizeof(float) : 1;
-  const int64_t max_partials = (int64_t)kNoAllocScratchBytes / per_partial;
-  if (max_partials < 1) {
+  const int64_t per_partial_floats = 2;  // per column
+  if (cols > (int64_t)(kNoAllocScratchBytes / sizeof(float)) / per_partial_floats) {
     rr_set_error_detail(
         "rr_layernorm_bwd_noalloc: one column partial (2 * cols * 4 bytes) exceeds the "
         "library's fixed 8 MiB scratch; use rr_layernorm_bwd with a caller-provided workspace");
     return RR_ERR_WORKSPACE_TOO_SMALL;
   }
+  const int64_t max_partials =
+      (int64_t)kNoAllocScratchBytes / (per_partial_floats * cols * (int64_t)sizeof(float));
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDev) {

@@ -83,6 +83,8 @@ def load_library():
         lib.rr_last_error_detail.restype = ctypes.c_char_p
         lib.rr_read_device_error.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), st]
         lib.rr_read_device_error.restype = st
+        lib.rr_selftest_bounded_wait.argtypes = [i64, vp]
+        lib.rr_selftest_bounded_wait.restype = st
         lib.rr_attention_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_float,
                                          ctypes.c_int, st, vp]
         lib.rr_attention_fwd.restype = st
@@ -263,3 +265,12 @@ def rr_read_device_error(device: int = 0, reset: bool = True) -> int:
     _check("rr_read_device_error", load_library().rr_read_device_error(
         int(device), ctypes.byref(out), int(bool(reset))))
     return out.value
+
+
+def rr_selftest_bounded_wait(limit_ns: int, stream=None):
+    """Launch the bounded-wait self-test: one block waits on an mbarrier that
+    nothing completes, gives up after ``limit_ns`` and records
+    RR_ERR_DEVICE_TIMEOUT in the device error word (read it with
+    :func:`rr_read_device_error`)."""
+    _check("rr_selftest_bounded_wait", load_library().rr_selftest_bounded_wait(
+        int(limit_ns), _stream(stream)))

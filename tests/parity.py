@@ -8,6 +8,14 @@ Comparison rule (elementwise, both sides NaN counts as equal):
   float32 outputs (loss, mean, rstd):                   rtol 1e-5, atol 1e-5
   dgamma / dbeta (sums over rows):
     |gpu - ref| <= rtol_io * |ref| + 1e-5 * sum_r |term_r| + 1e-5
+
+Guard bands: every device buffer these helpers make (inputs, outputs, in-place
+tensors, per-row statistics, counters) sits inside a larger allocation whose
+GUARD elements before it (plus any misalignment padding) and GUARD elements
+after it hold a sentinel bit pattern.  check_guards() asserts that no kernel
+wrote a byte there; the run_* helpers call it after every launch, and an
+autouse fixture (conftest.py) calls it again when each test ends.  This is the
+out-of-bounds write check for the ragged, misaligned and in-place paths.
 """
 from __future__ import annotations
 
@@ -26,9 +34,49 @@ def dev():
     return torch.device("cuda:0")
 
 
+GUARD = 64  # sentinel elements before and after every buffer (>= 128 bytes)
+# Sentinel bits: a NaN payload no kernel produces (kernels write quiet NaNs
+# with the canonical payload, numbers, or nothing).
+_SENTINEL = {torch.float32: (torch.int32, 0x7FA5A5A5), torch.bfloat16: (torch.int16, 0x7FA5),
+             torch.int32: (torch.int32, 0x7FA5A5A5)}
+_GUARDED: list = []
+
+
+def _guarded(n: int, tdt, pad_elems: int) -> torch.Tensor:
+    """A 1-D device buffer of n elements of tdt that starts GUARD + pad_elems
+    elements into an allocation filled with the sentinel; registered for
+    check_guards().  GUARD * element size is a multiple of 16, so the view's
+    alignment modulo 16 is pad_elems * element size."""
+    itype, bits = _SENTINEL[tdt]
+    start = GUARD + pad_elems
+    raw = torch.full((start + n + GUARD,), bits, dtype=itype, device=dev())
+    _GUARDED.append((raw, start, n, bits))
+    view = raw[start:start + n]
+    return view if tdt == torch.int32 else view.view(tdt)
+
+
+def check_guards(clear: bool = False):
+    """Asserts that the guard bands of every registered buffer still hold the
+    sentinel (no out-of-bounds write); clear=True forgets the buffers."""
+    bad = []
+    for raw, start, n, bits in _GUARDED:
+        pre = raw[:start] != bits
+        post = raw[start + n:] != bits
+        if bool(pre.any()) or bool(post.any()):
+            i_pre = torch.nonzero(pre).flatten().tolist()
+            i_post = torch.nonzero(post).flatten().tolist()
+            bad.append(f"buffer of {n} elements: {len(i_pre)} written before it "
+                       f"(offsets {[i - start for i in i_pre[:4]]}), {len(i_post)} after it "
+                       f"(offsets {[n + i for i in i_post[:4]]})")
+    if clear:
+        _GUARDED.clear()
+    assert not bad, "out-of-bounds writes: " + "; ".join(bad)
+
+
 def to_dev(a: np.ndarray, pad_elems: int = 0) -> torch.Tensor:
-    """Copy a host array (float32 or bf16 bits) to the GPU.  pad_elems > 0 places
-    it pad_elems elements past a 16-byte aligned start (a misaligned base)."""
+    """Copy a host array (float32, bf16 bits or int32) to the GPU inside a
+    guard band.  pad_elems > 0 places it pad_elems elements past a 16-byte
+    aligned start (a misaligned base)."""
     if a.dtype == np.uint16:
         flat = torch.from_numpy(np.ascontiguousarray(a).view(np.int16).reshape(-1))
         tdt = torch.bfloat16
@@ -36,22 +84,34 @@ def to_dev(a: np.ndarray, pad_elems: int = 0) -> torch.Tensor:
         flat = torch.from_numpy(np.ascontiguousarray(a).reshape(-1))
         tdt = torch.float32
     elif a.dtype == np.int32:
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+        flat = torch.from_numpy(np.ascontiguousarray(a).reshape(-1))
+        tdt = torch.int32
     else:
         raise TypeError(a.dtype)
-    buf = torch.empty(a.size + pad_elems + 16, dtype=flat.dtype, device=dev())
-    view = buf[pad_elems:pad_elems + a.size]
-    view.copy_(flat.to(dev()))
-    view = view.view(tdt) if tdt == torch.bfloat16 else view
+    view = _guarded(a.size, tdt, pad_elems)
+    raw = view if tdt != torch.bfloat16 else view.view(torch.int16)
+    raw.copy_(flat.to(dev()))
     return view.view(a.shape)
 
 
 def empty_like_dev(shape, dtype: str, pad_elems: int = 0, fill=float("nan")) -> torch.Tensor:
-    """Device buffer poisoned with NaN (so unwritten outputs are caught)."""
-    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    """Device output buffer poisoned with NaN (so unwritten outputs are
+    caught), inside a guard band."""
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "i32": torch.int32}[dtype]
     n = int(np.prod(shape))
-    buf = torch.full((n + pad_elems + 16,), fill, dtype=tdt, device=dev())
-    return buf[pad_elems:pad_elems + n].view(shape)
+    view = _guarded(n, tdt, pad_elems)
+    view.fill_(fill)
+    return view.view(shape)
+
+
+def out_f32(n: int, pad_elems: int = 0) -> torch.Tensor:
+    """A float32 per-row output (loss, mean, rstd) poisoned with NaN, guarded."""
+    return empty_like_dev((n,), "f32", pad_elems)
+
+
+def zeros_i32(n: int) -> torch.Tensor:
+    """A zeroed int32 device counter, guarded."""
+    return empty_like_dev((n,), "i32", 0, fill=0)
 
 
 def host(t: torch.Tensor) -> np.ndarray:
@@ -88,6 +148,7 @@ def run_softmax(x: np.ndarray, dtype: str, pad_in=0, pad_out=0, inplace=False):
     y = xd if inplace else empty_like_dev(x.shape, dtype, pad_out)
     rr.rr_softmax_fwd(xd, y)
     torch.cuda.synchronize()
+    check_guards()
     return host(y)
 
 
@@ -101,11 +162,12 @@ def check_softmax(x, dtype, **kw):
 def run_xent(logits, labels, dtype, ignore_index=-100, pad_in=0, pad_out=0, inplace=False):
     xd = to_dev(logits, pad_in)
     lab = to_dev(labels)
-    loss = torch.full((logits.shape[0],), float("nan"), device=dev())
+    loss = out_f32(logits.shape[0])
     dl = xd if inplace else empty_like_dev(logits.shape, dtype, pad_out)
-    bad = torch.zeros(1, dtype=torch.int32, device=dev())
+    bad = zeros_i32(1)
     rr.rr_softmax_xent_fwd_bwd(xd, lab, loss, dl, ignore_index=ignore_index, bad_label_count=bad)
     torch.cuda.synchronize()
+    check_guards()
     return host(loss), host(dl), int(bad.item())
 
 
@@ -127,13 +189,13 @@ def run_ln(x, gamma, beta, dy, eps, dtype, pad=(0, 0, 0, 0, 0), oracle_stats=Tru
     bd = to_dev(beta, pad[2])
     y = empty_like_dev(x.shape, dtype, pad[1])
     rows = x.shape[0]
-    mean = torch.full((rows,), float("nan"), device=dev())
-    rstd = torch.full((rows,), float("nan"), device=dev())
+    mean = out_f32(rows)
+    rstd = out_f32(rows)
     rr.rr_layernorm_fwd(xd, gd, bd, y, mean, rstd, eps=eps)
     _, rmean, rrstd = oracle.ln_fwd(x, gamma, beta, eps, want_y=False)
     if oracle_stats:
-        m_in = torch.from_numpy(rmean.astype(np.float32)).to(dev())
-        r_in = torch.from_numpy(rrstd.astype(np.float32)).to(dev())
+        m_in = to_dev(rmean.astype(np.float32))
+        r_in = to_dev(rrstd.astype(np.float32))
     else:
         m_in, r_in = mean, rstd
     dyd = to_dev(dy, pad[3])
@@ -142,6 +204,7 @@ def run_ln(x, gamma, beta, dy, eps, dtype, pad=(0, 0, 0, 0, 0), oracle_stats=Tru
     db = empty_like_dev(gamma.shape, dtype)
     rr.rr_layernorm_bwd(dyd, xd, m_in, r_in, gd, dx, dg, db)
     torch.cuda.synchronize()
+    check_guards()
     return dict(y=host(y), mean=host(mean), rstd=host(rstd), dx=host(dx), dgamma=host(dg),
                 dbeta=host(db), mean_in=m_in.cpu().numpy().astype(np.float64),
                 rstd_in=r_in.cpu().numpy().astype(np.float64))
@@ -187,11 +250,13 @@ def check_norm_bwd(x, gamma, beta, dy, dtype, rms=False, stat_pad=0, inplace=Non
     if rms:
         rr.rr_rmsnorm_bwd(dyd, xd, r_in, gd, dx, dg)
         torch.cuda.synchronize()
+        check_guards()
         rdx, rdg, sdg = oracle.rms_bwd(dy, x, r32.astype(np.float64), gamma)
     else:
         db = empty_like_dev(gamma.shape, dtype)
         rr.rr_layernorm_bwd(dyd, xd, m_in, r_in, gd, dx, dg, db)
         torch.cuda.synchronize()
+        check_guards()
         rdx, rdg, rdb, sdg, sdb = oracle.ln_bwd(dy, x, m32.astype(np.float64),
                                                 r32.astype(np.float64), gamma)
         compare("norm bwd dbeta", host(db), rdb, rtol, atol, scale=sdb)
@@ -206,15 +271,16 @@ def run_rms(x, gamma, dy, eps, dtype, pad=(0, 0, 0, 0, 0), oracle_stats=True):
     gd = to_dev(gamma, pad[2])
     y = empty_like_dev(x.shape, dtype, pad[1])
     rows = x.shape[0]
-    rstd = torch.full((rows,), float("nan"), device=dev())
+    rstd = out_f32(rows)
     rr.rr_rmsnorm_fwd(xd, gd, y, rstd, eps=eps)
     _, rrstd = oracle.rms_fwd(x, gamma, eps, want_y=False)
-    r_in = torch.from_numpy(rrstd.astype(np.float32)).to(dev()) if oracle_stats else rstd
+    r_in = to_dev(rrstd.astype(np.float32)) if oracle_stats else rstd
     dyd = to_dev(dy, pad[3])
     dx = empty_like_dev(x.shape, dtype, pad[4])
     dg = empty_like_dev(gamma.shape, dtype)
     rr.rr_rmsnorm_bwd(dyd, xd, r_in, gd, dx, dg)
     torch.cuda.synchronize()
+    check_guards()
     return dict(y=host(y), rstd=host(rstd), dx=host(dx), dgamma=host(dg),
                 rstd_in=r_in.cpu().numpy().astype(np.float64))
 
@@ -242,6 +308,7 @@ def check_log_softmax(x, dtype, pad_in=0, pad_out=0, inplace=False):
     z = xd if inplace else empty_like_dev(x.shape, dtype, pad_out)
     rr.rr_log_softmax_fwd(xd, z)
     torch.cuda.synchronize()
+    check_guards()
     rtol, atol = TOL[dtype]
     compare("log_softmax z", host(z), oracle.log_softmax(x), rtol, atol)
 
@@ -259,6 +326,7 @@ def check_softmax_bwd(y, dy, dtype, log=False, pads=(0, 0, 0), inplace=None):
         dx = empty_like_dev(y.shape, dtype, pads[2])
     (rr.rr_log_softmax_bwd if log else rr.rr_softmax_bwd)(yd, dyd, dx)
     torch.cuda.synchronize()
+    check_guards()
     ref = oracle.log_softmax_bwd(y, dy) if log else oracle.softmax_bwd(y, dy)
     rtol, atol = TOL[dtype]
     compare("log_softmax dx" if log else "softmax dx", host(dx), ref, rtol, atol)

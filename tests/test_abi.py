@@ -91,6 +91,40 @@ def test_layernorm_argument_errors(lib):
     assert fb(P1, P2, m, r, g, ctypes.c_void_p(0x10004), dg, db, ws, 1 << 20, 4, 8, 0, S0) == 3
 
 
+def test_layernorm_noalloc_argument_errors(lib):
+    """The no-allocation LayerNorm backward rejects bad arguments on the host,
+    before any device call, with the same status rr_layernorm_bwd gives (its
+    workspace arguments set to a valid fake buffer)."""
+    fn = lib.rr_layernorm_bwd_noalloc
+    fb = lib.rr_layernorm_bwd
+    g, m, r = (ctypes.c_void_p(a) for a in (0x30000, 0x50000, 0x60000))
+    dx, dg, db, ws = (ctypes.c_void_p(a) for a in (0x70000, 0x80000, 0x88000, 0x7000000))
+    cases = [
+        dict(rows=4, cols=8, dtype=7),                   # dtype
+        dict(rows=-1, cols=8, dtype=0),                  # negative rows
+        dict(rows=4, cols=0, dtype=0),                   # cols == 0
+        dict(rows=4, cols=1 << 61, dtype=0),             # cols far beyond any row
+        dict(rows=4, cols=(1 << 31) + 1, dtype=0),       # cols beyond 2^31
+        dict(rows=4, cols=8, dtype=1, dy=None),          # null input
+        dict(rows=4, cols=8, dtype=0, dx=ctypes.c_void_p(0x10004)),   # dx partly over dy
+        dict(rows=4, cols=8, dtype=0, db=ctypes.c_void_p(0x80010)),   # dbeta over dgamma
+        dict(rows=4, cols=8, dtype=0, x=ctypes.c_void_p(0x20002)),    # fp32 misaligned
+    ]
+    for c in cases:
+        a = dict(dy=P1, x=P2, dx=dx, dg=dg, db=db)
+        a.update({k: v for k, v in c.items() if k in ("dy", "x", "dx", "db")})
+        want = fb(a["dy"], a["x"], m, r, g, a["dx"], a["dg"], a["db"], ws, 1 << 30,
+                  c["rows"], c["cols"], c["dtype"], S0)
+        got = fn(a["dy"], a["x"], m, r, g, a["dx"], a["dg"], a["db"], c["rows"], c["cols"],
+                 c["dtype"], S0)
+        assert want != 0, c
+        assert got == want, (c, got, want, lib.rr_last_error_detail())
+    # rows beyond the fixed scratch (one partial of 2 * cols fp32 over 8 MiB):
+    # rejected as too small a workspace, still before any device call
+    far = [ctypes.c_void_p((i + 1) << 40) for i in range(8)]   # disjoint fake buffers
+    assert fn(*far, 2, (1 << 20) + 1, 0, S0) == 4
+
+
 def test_header_documents_every_entry_point():
     src = open(os.path.join(ROOT, "include", "rr.h")).read()
     for n in declared_symbols():

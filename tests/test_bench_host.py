@@ -31,3 +31,20 @@ def test_cpu_baseline_one_thread_and_all_cores():
     assert r["cores"] in (1, n)
     if r["cores"] == n and n > 1:
         assert f"{n} processes" in r["sample"]
+
+
+def test_step_covers_every_workload_with_its_bytes():
+    """The timed step's launch groups: config 2's LayerNorm, config 3's causal
+    softmax, the sweep's bf16 LayerNorm cases at 1000, 4097 and 65537 columns
+    (fwd and bwd each) and config 4's cross-entropy, with their algorithmic bytes."""
+    w = bench.make_inputs(scale_rows=1 / 1024)
+    nb = bench.step_bytes(w)
+    want = ["ln_fwd", "softmax", "ln_bwd"]
+    for c in (1000, 4097, 65537):
+        want += [f"ln_bf16_c{c}_fwd", f"ln_bf16_c{c}_bwd"]
+    assert list(nb) == want + ["xent"]
+    for c in (1000, 4097, 65537):
+        r, cc = w[f"lnb{c}"]["x"].shape
+        assert cc == c and w[f"lnb{c}"]["x"].dtype.itemsize == 2
+        assert nb[f"ln_bf16_c{c}_fwd"] == 2 * r * c * 2 + 2 * c * 2 + 8 * r
+        assert nb[f"ln_bf16_c{c}_bwd"] == 3 * r * c * 2 + 3 * c * 2 + 8 * r

@@ -16,7 +16,7 @@ import oracle
 import row_reduction_pass_gb300 as rr
 from row_reduction_pass_gb300 import synth
 
-from parity import TOL_F32_OUT, compare, host
+from parity import TOL_F32_OUT, check_guards, compare, empty_like_dev, host, out_f32, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -27,12 +27,13 @@ def dev_bf16(bits: np.ndarray) -> torch.Tensor:
 
 def run_attention(bh, seq, d, seed, causal=True, sigma=1.0, heads_checked=None):
     q, k, v = synth.attn_inputs(bh, seq, d, seed, sigma)
-    qd, kd, vd = dev_bf16(q), dev_bf16(k), dev_bf16(v)
-    o = torch.full((bh, seq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
-    lse = torch.full((bh, seq), float("nan"), device="cuda")
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    o = empty_like_dev((bh, seq, d), "bf16")
+    lse = out_f32(bh * seq).view(bh, seq)
     scale = 1.0 / np.sqrt(d)
     rr.rr_attention_fwd(qd, kd, vd, o, lse, scale=scale, causal=causal)
     torch.cuda.synchronize()
+    check_guards()
     heads = range(bh) if heads_checked is None else heads_checked
     for h in heads:
         sl = slice(h, h + 1)

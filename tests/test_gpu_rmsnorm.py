@@ -11,7 +11,8 @@ import oracle
 import row_reduction_pass_gb300 as rr
 from row_reduction_pass_gb300 import synth
 
-from parity import TOL, TOL_F32_OUT, check_norm_bwd, check_rms, compare, empty_like_dev, host, to_dev
+from parity import (TOL, TOL_F32_OUT, check_guards, check_norm_bwd, check_rms, compare,
+                    empty_like_dev, host, out_f32, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -63,9 +64,10 @@ def test_rmsnorm_fwd_clustered_rows(cols, dtype, pad):
     x, g, _ = case(64, cols, dtype, 990 + cols)
     xd, gd = to_dev(x, pad[0]), to_dev(g, pad[2])
     y = empty_like_dev(x.shape, dtype, pad[1])
-    rstd = torch.full((x.shape[0],), float("nan"), device="cuda")
+    rstd = out_f32(x.shape[0])
     rr.rr_rmsnorm_fwd(xd, gd, y, rstd, eps=1e-5)
     torch.cuda.synchronize()
+    check_guards()
     ry, rrstd = oracle.rms_fwd(x, g, 1e-5)
     rtol, atol = TOL[dtype]
     compare("rms y (clustered)", host(y), ry, rtol, atol)

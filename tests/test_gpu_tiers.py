@@ -16,8 +16,9 @@ import oracle
 import row_reduction_pass_gb300 as rr
 from row_reduction_pass_gb300 import synth
 
-from parity import (TOL, TOL_F32_OUT, check_log_softmax, check_norm_bwd, check_softmax,
-                    check_softmax_bwd, check_xent, compare, empty_like_dev, host, store, to_dev)
+from parity import (TOL, TOL_F32_OUT, check_guards, check_log_softmax, check_norm_bwd,
+                    check_softmax, check_softmax_bwd, check_xent, compare, empty_like_dev, host,
+                    out_f32, store, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -85,16 +86,18 @@ def norm_fwd_only(x, g, b, dtype, rms):
     rows = x.shape[0]
     xd, gd = to_dev(x), to_dev(g)
     y = empty_like_dev(x.shape, dtype)
-    rstd = torch.full((rows,), float("nan"), device="cuda")
+    rstd = out_f32(rows)
     rtol, atol = TOL[dtype]
     if rms:
         rr.rr_rmsnorm_fwd(xd, gd, y, rstd, eps=1e-5)
         torch.cuda.synchronize()
+        check_guards()
         ry, rrstd = oracle.rms_fwd(x, g, 1e-5)
     else:
-        mean = torch.full((rows,), float("nan"), device="cuda")
+        mean = out_f32(rows)
         rr.rr_layernorm_fwd(xd, gd, to_dev(b), y, mean, rstd, eps=1e-5)
         torch.cuda.synchronize()
+        check_guards()
         ry, rmean, rrstd = oracle.ln_fwd(x, g, b, 1e-5)
         compare("ln mean", host(mean), rmean, *TOL_F32_OUT)
     compare("norm y", host(y), ry, rtol, atol)
