@@ -13,6 +13,7 @@
 #include "../../include/rr.h"
 #include "rr_kernels.h"
 #include "rr_ln.cuh"
+#include "rr_lnx.cuh"
 #include "rr_span.cuh"
 #include "rr_ops.cuh"
 
@@ -111,7 +112,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
 struct Plan {
-  int kind = 0;  // 0: row engine (rr::Geo), 1: row-group LayerNorm (rr::LnGeo)
+  int kind = 0;  // 0: row engine (rr::Geo), 1: row-group LayerNorm (rr::LnGeo), 2: rr::LnxGeo
   bool staged = false;
   int mode = 0;  // 0: 16-byte chunks, 1: elements
   int G = 0, T = 0, K = 1;
@@ -121,6 +122,7 @@ struct Plan {
   int64_t partials = 0;  // LayerNorm backward: rows of column partials
   rr::Geo geo{};
   rr::LnGeo lgeo{};
+  rr::LnxGeo xgeo{};
 };
 
 // Chooses the kernel variant and launch shape for (op, dtype, mode, rows, cols)
@@ -509,6 +511,138 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
   return RR_OK;
 }
 
+// Phase-aligned row kernels for long rows (rr_lnx.cuh): forward or backward of
+// LayerNorm / RMSNorm.  The row tensors must share their address modulo 16
+// (the caller checks); gamma / beta may have any alignment.  Rows of at least
+// kLnxMinBytes; one block per row (slice) of at most 512 threads holding NQ
+// chunks each, clusters of K = 2 .. 8 blocks for rows beyond one block (force:
+// -1 any, 1 one block only, 3 clusters only).  Rows of each of the P phase
+// classes go to bpc row owners; the backward writes one partial row per owner,
+// at most max_partials.  RR_LNX=0 turns these kernels off (tuning aid).
+// Rows of at least 8 KB: measured on 2^24-element rows (bf16, cold L2), they
+// beat the row-group kernels from there (4097 columns: backward 65.5 -> 55.5
+// us, RMSNorm forward 23.2 -> 19.3 us, forward 32.8 -> 31.2 us) and lose on
+// shorter rows (1000 columns: forward 16.9 against 28.6 us at best).
+constexpr int64_t kLnxMinBytes = 8192;
+
+rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
+                   int64_t max_partials, int force) {
+  if (const char* f = std::getenv("RR_LNX"); f != nullptr && f[0] == '0')
+    return fail(RR_ERR_INVALID_ARG, "phase-aligned kernels off");
+  const int E = dt == RR_BF16 ? 2 : 4, W = 16 / E;
+  if (cols * E < kLnxMinBytes || rows < 1) return fail(RR_ERR_INVALID_ARG, "short rows");
+  const bool fwd = op == kLnFwd || op == kRmsFwd;
+  const bool rms = op == kRmsFwd || op == kRmsBwd;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo* di = nullptr;
+  rr_status st = device_info(&di);
+  if (st != RR_OK) return st;
+  static const rr::LnxKernels fk[2] = {rr::lnx_fwd_kernels_f32(), rr::lnx_fwd_kernels_bf16()};
+  static const rr::LnxKernels bk[2] = {rr::lnx_bwd_kernels_f32(), rr::lnx_bwd_kernels_bf16()};
+  const int NQ = fwd ? fk[dt].nq_fwd : bk[dt].nq_bwd;
+  const int NT = fwd ? 1 : 2;
+  const int vecs = fwd ? (rms ? 1 : 2) : 1;  // gamma (, beta) planes
+  const int64_t rb = (cols * E) % 16;
+  int64_t P = 1;
+  if (rb != 0) {
+    int64_t a = 16, b = rb;
+    while (b) { const int64_t t = a % b; a = b; b = t; }
+    P = 16 / a;
+  }
+  const int64_t nch_min = cdiv(cols, W), nch_max = cdiv(cols + W - 1, W);
+  // The LayerNorm forward split over a cluster measured slower than the
+  // clusters of row groups (bf16 65537 columns: 65.9 against 49.4 us), so it
+  // takes this path only when tier 3 is forced.
+  const int kmax = force == 1 ? 1 : (op == kLnFwd && force != 3) ? 1 : 8;
+  for (int K = force == 3 ? 2 : 1; K <= kmax; ++K) {
+    const int64_t S = cdiv(nch_max, K);
+    if (K > 1 && (K - 1) * S >= nch_min) break;  // every rank of every phase gets chunks
+    const int64_t G = round_up(cdiv(S, NQ), 32);
+    if (G > rr::kLnxMaxT) continue;
+    const void* fn = fwd ? fk[dt].fwd[rms][K > 1] : bk[dt].bwd[rms][K > 1];
+    const int64_t planes = (int64_t)vecs * S * W * 4;
+    // R row groups per block (one per block in a cluster), up to 256 threads;
+    // NS stages per group's ring: the most that fit, four only where two blocks
+    // still fit an SM
+    int64_t rmax = K > 1 ? 1 : std::max<int64_t>(1, std::min<int64_t>(8, 256 / G));
+    // RR_LNX_SHAPE="R:NS" forces the groups per block and the stages (tuning aid)
+    int fR = 0, fNS = 0;
+    if (const char* f = std::getenv("RR_LNX_SHAPE")) std::sscanf(f, "%d:%d", &fR, &fNS);
+    if (fR > 0 && K == 1 && fR * G <= rr::kLnxMaxT) rmax = fR;
+    for (int64_t R = rmax; R >= 1; --R) {
+      for (int NS = 4; NS >= 2; --NS) {
+        if (fNS >= 2 && NS != fNS) continue;
+        if (fR > 0 && R != rmax) continue;
+        const int64_t red_off = round_up(planes, 16);
+        const int64_t bar_off = red_off + 1024 * R;
+        const int64_t ring_off = round_up(bar_off + 8 * NS * R, 128);
+        const int64_t cl_off = ring_off + R * NS * NT * S * 16;
+        const int64_t smem = cl_off + 32;
+        if (smem > di->smem_optin) continue;
+        if (NS > 2 && fNS == 0 && 2 * smem > di->smem_optin) continue;
+        const int T = (int)(R * G);
+        if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
+        int owners = 0;
+        if (K == 1) {
+          int& occ = di->occ[{fn, ((long long)T << 32) | (long long)smem}];
+          if (occ == 0) {
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, T, smem);
+            if (e != cudaSuccess || occ <= 0)
+              return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+          }
+          owners = di->sms * occ;
+        } else {
+          int& ncl = di->ncl[{fn, ((long long)K << 32) | (long long)smem | ((long long)T << 48)}];
+          if (ncl == 0) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = K;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3((unsigned)(K * di->sms));
+            cfg.blockDim = dim3((unsigned)T);
+            cfg.dynamicSmemBytes = (size_t)smem;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            cudaError_t e = cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg);
+            if (e != cudaSuccess)
+              return fail(RR_ERR_CUDA, "cluster occupancy query (K=%d): %s", K,
+                          cudaGetErrorString(e));
+            if (ncl <= 0) ncl = -1;
+          }
+          if (ncl <= 0) continue;
+          owners = ncl;
+        }
+        int64_t bpc = owners / P;
+        if (bpc < 1) bpc = 1;
+        const int64_t per_class = cdiv(cdiv(rows, P), R);  // blocks with a row for every group
+        if (bpc > per_class) bpc = per_class;
+        if (!fwd) {
+          if (max_partials < P) return fail(RR_ERR_INVALID_ARG, "too few column partials allowed");
+          if (bpc > max_partials / P) bpc = max_partials / P;
+        }
+        pl->kind = 2;
+        pl->staged = true;
+        pl->mode = 0;
+        pl->G = (int)G;
+        pl->T = T;
+        pl->K = K;
+        pl->fn = fn;
+        pl->grid = P * bpc * K;
+        pl->smem = (size_t)smem;
+        pl->partials = P * bpc;
+        pl->xgeo = rr::LnxGeo{rows,          (int32_t)cols,    (int32_t)P,
+                              (int32_t)bpc,  (int32_t)S,       NS,
+                              (int32_t)G,    0,                (int32_t)red_off,
+                              (int32_t)bar_off, (int32_t)ring_off, (int32_t)cl_off};
+        return RR_OK;
+      }
+    }
+  }
+  return fail(RR_ERR_INVALID_ARG, "row does not fit the phase-aligned kernels");
+}
+
 // Plans in chunk mode when allowed, falling back to element mode (which holds
 // longer rows per CTA) when the row does not fit the chunk-mode variants.
 rr_status plan_any(OpKind op, rr_dtype dt, bool chunk_ok, bool head_free, int64_t rows,
@@ -654,7 +788,10 @@ rr_status launch(const Plan& pl, const P& params, cudaStream_t stream) {
   P pcopy = params;
   rr::Geo g = pl.geo;
   rr::LnGeo lg = pl.lgeo;
-  void* args[] = {&pcopy, pl.kind == 1 ? static_cast<void*>(&lg) : static_cast<void*>(&g)};
+  rr::LnxGeo xg = pl.xgeo;
+  void* args[] = {&pcopy, pl.kind == 2   ? static_cast<void*>(&xg)
+                          : pl.kind == 1 ? static_cast<void*>(&lg)
+                                         : static_cast<void*>(&g)};
   cudaError_t e = cudaLaunchKernelExC(&cfg, pl.fn, args);
   if (e != cudaSuccess)
     return fail(RR_ERR_CUDA, "launch (grid %lld, block %d, smem %zu, cluster %d): %s",
@@ -877,11 +1014,16 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
     }
   }
   if (ft == 0) return no_span(cols);
+  // x and y at the same address modulo 16: phase-aligned kernels for long rows
+  const bool same16 = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(y) & 15);
   st = RR_ERR_INVALID_ARG;
-  if (ft < 0 || ft == 1) st = ln_rowgroup_plan(kLnFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
-  if ((ft < 0 && st == RR_ERR_INVALID_ARG) || ft == 3)
+  if (same16 && (ft < 0 || ft == 1 || ft == 3))
+    st = lnx_plan(kLnFwd, dtype, rows, cols, &pl, INT64_MAX, ft);
+  if (st == RR_ERR_INVALID_ARG && (ft < 0 || ft == 1))
+    st = ln_rowgroup_plan(kLnFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
+  if (st == RR_ERR_INVALID_ARG && (ft < 0 || ft == 3))
     st = ln_cluster_plan(kLnFwd, dtype, lmode, rows, cols, &pl);
-  if ((ft < 0 && st == RR_ERR_INVALID_ARG) || ft == 2)
+  if (st == RR_ERR_INVALID_ARG && (ft < 0 || ft == 2))
     st = plan_any(kLnFwd, dtype, al, true, rows, cols, &pl, INT64_MAX, ft < 0 ? -1 : 2);
   if (st != RR_OK) return st;
   int* err = device_error_word();
@@ -927,9 +1069,13 @@ rr_status rr_rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
     }
   }
   if (ft == 0) return no_span(cols);
+  const bool same16 = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(y) & 15);
   st = RR_ERR_INVALID_ARG;
-  if (ft < 0 || ft == 1) st = ln_rowgroup_plan(kRmsFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
-  if ((ft < 0 && st == RR_ERR_INVALID_ARG) || ft == 3)
+  if (same16 && (ft < 0 || ft == 1 || ft == 3))
+    st = lnx_plan(kRmsFwd, dtype, rows, cols, &pl, INT64_MAX, ft);
+  if (st == RR_ERR_INVALID_ARG && (ft < 0 || ft == 1))
+    st = ln_rowgroup_plan(kRmsFwd, dtype, lmode, rows, cols, &pl, INT64_MAX);
+  if (st == RR_ERR_INVALID_ARG && (ft < 0 || ft == 3))
     st = ln_cluster_plan(kRmsFwd, dtype, lmode, rows, cols, &pl);
   if (ft >= 1 && st != RR_OK) return st;
   if (st == RR_ERR_INVALID_ARG)
@@ -951,17 +1097,21 @@ rr_status rr_rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
 // engine kernels (chunk mode unless lmode == 2).  ws_bytes: the column
 // partials, [partials][planes][cols] floats.
 static rr_status norm_bwd_plan(bool rms, int64_t rows, int64_t cols, rr_dtype dtype, int lmode,
-                               Plan* pl, size_t* ws_bytes, int64_t max_partials = INT64_MAX) {
+                               bool lnx_ok, Plan* pl, size_t* ws_bytes,
+                               int64_t max_partials = INT64_MAX) {
   const int ft = forced_tier();
   if (ft == -2) return bad_tier();
   if (ft == 0) return no_span(cols);
   if (rms && ft == 2)
     return fail(RR_ERR_INVALID_ARG, "tier 2 (staged rows) has no RMSNorm backward kernel");
   rr_status st = RR_ERR_INVALID_ARG;
-  if (ft < 0 || ft == 1)
+  // dy, x and dx at the same address modulo 16: phase-aligned kernels for long rows
+  if (lnx_ok && (ft < 0 || ft == 1 || ft == 3))
+    st = lnx_plan(rms ? kRmsBwd : kLnBwd, dtype, rows, cols, pl, max_partials, ft);
+  if (st == RR_ERR_INVALID_ARG && (ft < 0 || ft == 1))
     st = ln_rowgroup_plan(rms ? kRmsBwd : kLnBwd, dtype, lmode, rows, cols, pl, max_partials);
   // rows longer than one row group: clusters of row groups (chunk mode)
-  if ((ft < 0 && st == RR_ERR_INVALID_ARG) || ft == 3)
+  if (st == RR_ERR_INVALID_ARG && (ft < 0 || ft == 3))
     st = ln_cluster_plan(rms ? kRmsBwd : kLnBwd, dtype, lmode, rows, cols, pl, max_partials);
   if (st == RR_ERR_INVALID_ARG && ft != 1) {
     if (rms)
@@ -982,11 +1132,13 @@ static size_t norm_bwd_workspace_size(bool rms, int64_t rows, int64_t cols, rr_d
   // misaligned chunks, elements: different shared memory, so different
   // occupancy and grid), so report the largest of the three.
   size_t best = 0;
-  for (int m = 0; m < 3; ++m) {
-    Plan pl;
-    size_t ws = 0;
-    if (norm_bwd_plan(rms, rows, cols, dtype, m, &pl, &ws) == RR_OK && ws > best) best = ws;
-  }
+  for (int lnx = 0; lnx < 2; ++lnx)
+    for (int m = 0; m < 3; ++m) {
+      Plan pl;
+      size_t ws = 0;
+      if (norm_bwd_plan(rms, rows, cols, dtype, m, lnx == 1, &pl, &ws) == RR_OK && ws > best)
+        best = ws;
+    }
   SpanPlan sp;  // short rows with 16-byte aligned tensors: one partial per span block
   if (forced_tier() <= 0 && span_plan(dtype, rms ? 8 : 7, rows, cols, false, INT64_MAX, &sp) == RR_OK) {
     const size_t ws = (size_t)sp.grid * (rms ? 1 : 2) * (size_t)cols * sizeof(float);
@@ -1090,7 +1242,11 @@ static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* 
       if ((st = span_launch(p, sp, stream)) != RR_OK) return st;
       pl.partials = sp.grid;
     } else {
-      if ((st = norm_bwd_plan(rms, rows, cols, dtype, lmode, &pl, &need, max_partials)) != RR_OK)
+      const uintptr_t a16 = reinterpret_cast<uintptr_t>(x) & 15;
+      const bool same16 = a16 == (reinterpret_cast<uintptr_t>(dy) & 15) &&
+                          a16 == (reinterpret_cast<uintptr_t>(dx) & 15);
+      if ((st = norm_bwd_plan(rms, rows, cols, dtype, lmode, same16, &pl, &need, max_partials)) !=
+          RR_OK)
         return st;
       if (workspace_bytes < need)
         return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);

@@ -319,11 +319,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same test, allowing the thread to be suspended for up to suspend_ns
+// while the phase is incomplete (it resumes when the phase completes), so a
+// waiting warp does not spin through issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// Longest suspension a waiting thread asks for per test of an mbarrier phase.
+constexpr uint32_t kMbarSuspendNs = 20000;
 
 // Bounded wait on an mbarrier phase: gives up after limit_ns of wall time
 // (~1 s by default) and records RR_ERR_DEVICE_TIMEOUT (6) in *err instead of
@@ -334,8 +352,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it != 0xffffffffu; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && global_timer_ns() - t0 > limit_ns) break;
+    if (mbar_try_wait_sleep(bar, parity, kMbarSuspendNs)) return true;
+    if (global_timer_ns() - t0 > limit_ns) break;
   }
   atomicCAS(err, 0, 6);
   return false;

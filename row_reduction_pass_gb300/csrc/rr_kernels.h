@@ -37,6 +37,18 @@ struct LnKernelSet {
   int nqd;
 };
 
+// Phase-aligned LayerNorm / RMSNorm kernels for long rows (rr_lnx.cuh):
+// [rms][cluster]; nq_* chunks per thread.  Each function fills its half.
+struct LnxKernels {
+  const void* fwd[2][2];
+  const void* bwd[2][2];
+  int nq_fwd, nq_bwd;
+};
+LnxKernels lnx_fwd_kernels_f32();
+LnxKernels lnx_fwd_kernels_bf16();
+LnxKernels lnx_bwd_kernels_f32();
+LnxKernels lnx_bwd_kernels_bf16();
+
 // Short-row span kernels (rr_span.cuh): [dtype][mode], mode 0 softmax,
 // 1 log-softmax, 2 cross-entropy, 3 softmax backward, 4 log-softmax backward,
 // 5 LayerNorm forward, 6 RMSNorm forward, 7 LayerNorm backward, 8 RMSNorm
