@@ -1,24 +1,38 @@
-// k_attn.cu -- scaled dot-product attention forward built on the online
-// softmax ("Engineering a CUDA Machine Learning Framework from Scratch",
-// sec. 6.4: the FlashAttention-style extension of sec. 3.1; attention as
-// defined by Vaswani et al. 2017, tiled as in Dao et al. 2022).
+// k_attn.cu -- scaled dot-product attention forward on the online softmax
+// ("Engineering a CUDA Machine Learning Framework from Scratch", sec. 6.4: the
+// FlashAttention-style extension of the sec. 3.1 online normaliser; attention
+// as defined by Vaswani et al. 2017, tiled as in Dao et al. 2022), with both
+// products on the 5th-generation tensor cores.
 //
-// One CTA of 4 warps owns 64 query rows of one head (16 per warp) and walks
-// the key / value tiles of 64 rows (causal: up to the diagonal tile).  Q and
-// the K / V tiles are copied into shared memory with 16-byte cp.async (K / V
-// double-buffered, rows padded by 8 elements so ldmatrix reads are
-// bank-conflict free).  Scores S = Q K^T and the output O += P V are
-// warp-level bf16 tensor-core products (mma.sync m16n8k16, fp32
-// accumulation); between them each warp keeps, per query row, the running
-// maximum m and sum l of the online softmax in the log2 domain (scores scaled
-// by scale * log2 e), rescales O by 2^(m_old - m_new) when the maximum grows,
-// and turns the probabilities into the bf16 A operand of P V directly from
-// the score accumulators.  At the end O / l is stored in bf16 and
-// lse = (m + log2 l) * ln 2 in fp32.
+// One CTA of four warps owns 128 query rows of one head; thread t owns query
+// row t, which is TMEM lane t of every accumulator.  Per key tile of 128 keys:
+//   1. S = Q K^T: tcgen05.mma (bf16 in, fp32 accumulate) of the Q tile and the
+//      K tile, both read from shared memory (128-byte swizzled, K-major, loaded
+//      by TMA), into 128 TMEM columns; issued by one thread, completion
+//      tracked on an mbarrier by tcgen05.commit.
+//   2. Each thread reads its row of S from TMEM (tcgen05.ld), scales it into
+//      the log2 domain, masks keys after its query (causal) or past the end,
+//      and updates its running maximum m and sum l of the online softmax; the
+//      probabilities 2^(s - m) go back to TMEM as bf16 (tcgen05.st), and the
+//      output accumulator O is rescaled in TMEM by 2^(m_old - m_new).
+//   3. O += P V: tcgen05.mma with A = P read from TMEM and B = the V tile from
+//      shared memory (MN-major: the head dimension is contiguous).
+// K / V tiles are double-buffered: the tile after next is loaded once the
+// product that last read its stage has completed.  At the end O / l is stored
+// in bf16 and lse = (m + log2 l) ln 2 in fp32.
+//
+// Loads are 3-D TMA boxes of [64 head-dim columns x 128 rows x 1 head] with
+// 128-byte swizzle; rows past seq are filled with zeros, so seq needs only be a
+// multiple of 64 (those keys are masked, those queries not stored).  Every
+// mbarrier wait is bounded (RR_ERR_DEVICE_TIMEOUT in the device error word);
+// the tensor memory is allocated by warp 0 and always released.
 //
 // Shapes: bf16 q, k, v, o of [bh][s][d], d = 64 or 128, s a multiple of 64,
 // 16-byte aligned tensors (checked by the caller).
 #include <cstdint>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "rr_device.cuh"
 #include "rr_kernels.h"
@@ -26,30 +40,113 @@
 namespace rr {
 namespace {
 
-constexpr int kBr = 64;   // query rows per CTA
-constexpr int kBc = 64;   // keys per tile
-constexpr int kPad = 8;   // padding elements per shared-memory row
+constexpr int kBM = 128;          // query rows per CTA: MMA M, TMEM lanes
+constexpr int kBN = 128;          // keys per tile: N of S = Q K^T, K of O = P V
+constexpr int kBoxBytes = kBM * 128;  // one TMA box: 128 rows x 64 bf16 (128 bytes)
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+template <int D>
+struct AttnCfg {
+  static constexpr int kBoxes = D / 64;                 // boxes per Q / K / V tile
+  static constexpr int kTile = kBoxes * kBoxBytes;      // bytes of a Q, K or V tile
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kTile;                  // [2 stages][K, V]
+  static constexpr int kOffBar = kTile + 4 * kTile;     // mbarriers and the TMEM address
+  static constexpr int kSmem = kOffBar + 128 + 1024;    // + slack for 1024-byte alignment
+  // TMEM columns: S [0, 128), P (bf16 pairs) [128, 192), O [kColO, kColO + D)
+  static constexpr uint32_t kCols = D == 64 ? 256 : 512;
+  static constexpr uint32_t kColS = 0, kColP = 128, kColO = D == 64 ? 192 : 256;
+  // instruction descriptors (kind::f16): D fp32, A and B bf16, M = 128;
+  // S: B K-major, N = 128.  O: B MN-major (bit 16), N = D.
+  static constexpr uint32_t kIdescS =
+      (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+  static constexpr uint32_t kIdescO = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                      ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+};
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
+// and stride byte offsets (16-byte units), the fixed 0b001 at bits 46-48.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3ffff) >> 4) | ((uint64_t)((lbo >> 4) & 0x3fff) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3fff) << 32) | (1ull << 46) | (2ull << 61);
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
-// D = A (16x16, row) * B (16x8, col) + D, bf16 in, fp32 accumulate
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc]
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// The mbarrier completes one arrival once every earlier tcgen05 operation of
+// this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 3-D TMA tile load [dst] <- map at {c0, c1, c2}, completing bytes on bar.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
 }
 // two floats as a bf16 pair, lo in the low half (round to nearest even)
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -58,180 +155,255 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
-// Copies a [64][D] bf16 tile (rows of D elements in global memory) into a
-// padded [64][D + kPad] shared-memory tile: 8 * D chunks of 16 bytes over the
-// CTA's 128 threads.
 template <int D>
-__device__ __forceinline__ void load_tile(uint16_t* dst, const char* src) {
-  constexpr int kChunksPerRow = D / 8;
-#pragma unroll
-  for (int c = threadIdx.x; c < kBr * kChunksPerRow; c += 128) {
-    const int row = c / kChunksPerRow, col8 = c % kChunksPerRow;
-    cp_async16(dst + row * (D + kPad) + col8 * 8, src + ((int64_t)row * D + col8 * 8) * 2);
-  }
-}
-
-template <int D>
-__global__ void __launch_bounds__(128) attn_fwd_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(128, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const AttnParams p) {
   static_assert(D == 64 || D == 128, "head dimension 64 or 128");
-  constexpr int LD = D + kPad;  // shared-memory row stride in elements
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint16_t* qs = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* ks = qs + kBr * LD;        // [2][kBc][LD]
-  uint16_t* vs = ks + 2 * kBc * LD;    // [2][kBc][LD]
+  using C = AttnCfg<D>;
+  extern __shared__ unsigned char smem_raw[];
+  // 128-byte swizzled tiles want 1024-byte alignment
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sq = smem + C::kOffQ;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* bar_q = bars + 0;
+  uint64_t* bar_full = bars + 1;  // [2]: K / V tile landed in the stage
+  uint64_t* bar_s = bars + 3;     // S = Q K^T done
+  uint64_t* bar_o = bars + 4;     // O += P V done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
+  auto stage_k = [&](int s) { return smem + C::kOffKV + (2 * s) * C::kTile; };
+  auto stage_v = [&](int s) { return smem + C::kOffKV + (2 * s + 1) * C::kTile; };
 
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int seq = static_cast<int>(p.seq);
+  const int head = static_cast<int>(blockIdx.x);
   // grid (heads, query tiles): blocks are dispatched x fastest, so every head's
   // heaviest causal tile (the most key tiles) goes out before any lighter one
-  const int nq = static_cast<int>(p.seq / kBr);
-  const int qt = nq - 1 - static_cast<int>(blockIdx.y);
-  const int64_t head = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;  // mma fragment row group / thread in group
-  const int64_t hoff = head * p.seq * D * 2;  // bytes to this head
-  const char* qg = p.q + hoff + (int64_t)qt * kBr * D * 2;
-  const char* kg = p.k + hoff;
-  const char* vg = p.v + hoff;
-  const int ntiles = p.causal ? qt + 1 : nq;
+  const int qt = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+  const int q0 = qt * kBM;
+  const int last_key = p.causal ? min(seq - 1, q0 + kBM - 1) : seq - 1;
+  const int nkv = last_key / kBN + 1;
 
-  load_tile<D>(qs, qg);
-  load_tile<D>(ks, kg);
-  load_tile<D>(vs, vg);
-  cp_async_commit();
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tslot)),
+                 "r"(C::kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
+  const uint32_t tS = tmem + lane_base + C::kColS;
+  const uint32_t tP = tmem + lane_base + C::kColP;
+  const uint32_t tO = tmem + lane_base + C::kColO;
 
-  uint32_t qf[D / 16][4];  // this warp's 16 query rows as A fragments
-  float o[D / 8][4];       // output accumulators: 16 rows x D
+  auto issue_kv = [&](int j) {  // key tile j into stage j & 1 (thread 0)
+    const int s = j & 1;
+    mbar_arrive_expect_tx(&bar_full[s], 2 * C::kTile);
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY;  // running maxima (log2 domain), rows g and g + 8
-  float l0 = 0.f, l1 = 0.f;              // this thread's share of the running sums
-
-  for (int kt = 0; kt < ntiles; ++kt) {
-    const int st = kt & 1;
-    if (kt + 1 < ntiles) {  // next tile into the other stage (freed at the end of kt - 1)
-      load_tile<D>(ks + (st ^ 1) * kBc * LD, kg + (int64_t)(kt + 1) * kBc * D * 2);
-      load_tile<D>(vs + (st ^ 1) * kBc * LD, vg + (int64_t)(kt + 1) * kBc * D * 2);
+    for (int b = 0; b < C::kBoxes; ++b) {
+      tma_load_3d(stage_k(s) + b * kBoxBytes, &tk, 64 * b, j * kBN, head, &bar_full[s]);
+      tma_load_3d(stage_v(s) + b * kBoxBytes, &tv, 64 * b, j * kBN, head, &bar_full[s]);
     }
-    cp_async_commit();
-    cp_async_wait<1>();
+  };
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_q, C::kTile);
+#pragma unroll
+    for (int b = 0; b < C::kBoxes; ++b) tma_load_3d(sq + b * kBoxBytes, &tq, 64 * b, q0, head, bar_q);
+    issue_kv(0);
+    if (nkv > 1) issue_kv(1);
+  }
+
+  const int row = q0 + tid;   // this thread's query
+  float m = -INFINITY, l = 0.f;  // running maximum (log2 domain) and sum
+  bool dead = false;             // a wait gave up: no further waits (the kernel still ends)
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    if (!dead) dead = !mbar_wait_bounded(bar, parity, p.err);
+  };
+  const uint32_t q_addr = smem_addr(sq);
+
+  for (int j = 0; j < nkv; ++j) {
+    const int s = j & 1;
+    if (tid == 0) {
+      wait(&bar_full[s], (uint32_t)((j >> 1) & 1));
+      if (j == 0) wait(bar_q, 0);
+      tc_fence_after();
+      const uint32_t k_addr = smem_addr(stage_k(s));
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        // K-step kk: box kk / 4, 32-byte column block kk % 4 within the 128-byte swizzle row
+        const uint32_t off = (uint32_t)((kk >> 2) * kBoxBytes + (kk & 3) * 32);
+        mma_ss(tmem + C::kColS, sw128_desc(q_addr + off, 16, 1024),
+               sw128_desc(k_addr + off, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar_s);
+      // the stage of tile j - 1 is free once O += P V of tile j - 1 is done:
+      // tile j + 1 goes there (tiles 0 and 1 were loaded up front)
+      if (j >= 1 && j + 1 < nkv) {
+        wait(bar_o, (uint32_t)((j - 1) & 1));
+        issue_kv(j + 1);
+      }
+    }
+    wait(bar_s, (uint32_t)(j & 1));  // also covers O += P V of tile j - 1 (committed earlier)
+    tc_fence_after();
+
+    // keys of this tile to mask: after the query (causal, diagonal tile) or past the end
+    const int key0 = j * kBN;
+    const bool need_mask = p.causal ? (key0 + kBN - 1 > q0) : (key0 + kBN > seq);
+    const int lim = p.causal ? min(row, seq - 1) : seq - 1;  // last visible key
+    // 1. the tile's row maximum (log2 domain)
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kBN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tS + 32 * c, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float x = __uint_as_float(v[i]) * p.scale_log2;
+        if (need_mask && key0 + 32 * c + i > lim) x = -INFINITY;
+        mx = fmaxf(mx, x);
+      }
+    }
+    const float m_new = fmaxf(m, mx);  // finite: key 0 is visible to every row
+    const float alpha = ex2(m - m_new);  // 0 on the first tile
+    // 2. P = 2^(s - m_new) as bf16 into TMEM, the row sum from the fp32 values
+    float ls = 0.f;
+#pragma unroll
+    for (int c = 0; c < kBN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tS + 32 * c, v);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        float x0 = __uint_as_float(v[i]) * p.scale_log2;
+        float x1 = __uint_as_float(v[i + 1]) * p.scale_log2;
+        if (need_mask && key0 + 32 * c + i > lim) x0 = -INFINITY;
+        if (need_mask && key0 + 32 * c + i + 1 > lim) x1 = -INFINITY;
+        const float p0 = ex2(x0 - m_new), p1 = ex2(x1 - m_new);
+        ls += p0 + p1;
+        pk[i >> 1] = pack_bf16(p0, p1);
+      }
+      tmem_st16(tP + 16 * c, pk);
+    }
+    l = l * alpha + ls;
+    m = m_new;
+    // 3. O *= alpha (O += P V of tile j - 1 is complete: see the wait above)
+    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + 32 * c, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+        tmem_st32(tO + 32 * c, v);
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
     __syncthreads();
-    if (kt == 0) {
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t v_addr = smem_addr(stage_v(s));
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        ldsm_x4(smem_addr(qs + (warp * 16 + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8),
-                qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+      for (int kk = 0; kk < kBN / 16; ++kk) {
+        // 16 keys per step: two 8-row groups of the swizzled V tile (1024 bytes
+        // each); the head dimension's 64-column blocks are kBoxBytes apart
+        mma_ts(tmem + C::kColO, tmem + C::kColP + 8 * kk,
+               sw128_desc(v_addr + kk * 2048, kBoxBytes, 1024), C::kIdescO,
+               (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(bar_o);
     }
-    const uint16_t* kb = ks + st * kBc * LD;
-    const uint16_t* vb = vs + st * kBc * LD;
+  }
 
-    // S = Q K^T for this warp's 16 rows and the tile's 64 keys (8 n-tiles)
-    float s[8][4];
+  // O / l in bf16 and lse, for the rows inside the sequence
+  wait(bar_o, (uint32_t)((nkv - 1) & 1));
+  tc_fence_after();
+  const float inv = 1.f / l;
+  char* orow = p.o + ((int64_t)head * seq + row) * D * 2;
 #pragma unroll
-    for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(tO + 32 * c, v);
+    if (row < seq) {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(smem_addr(kb + (np * 16 + (lane & 7) + ((lane >> 4) << 3)) * LD + kk * 16 +
-                          ((lane >> 3) & 1) * 8),
-                b0, b1, b2, b3);
-        mma_bf16(s[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-        mma_bf16(s[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+      for (int i = 0; i < 32; i += 8) {
+        const uint4 w = make_uint4(
+            pack_bf16(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv),
+            pack_bf16(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv),
+            pack_bf16(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv),
+            pack_bf16(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv));
+        *reinterpret_cast<uint4*>(orow + (32 * c + i) * 2) = w;
       }
     }
-    // scale into the log2 domain; mask keys after the query on the diagonal tile
-    const int r0 = warp * 16 + g;  // query row (in the tile) of s[.][0..1]; r0 + 8 of s[.][2..3]
-    float tm0 = -INFINITY, tm1 = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float x = s[n][e] * p.scale_log2;
-        const int key = n * 8 + 2 * t + (e & 1);
-        const int row = r0 + (e >> 1) * 8;
-        if (p.causal && kt == qt && key > row) x = -INFINITY;
-        s[n][e] = x;
-      }
-      tm0 = fmaxf(tm0, fmaxf(s[n][0], s[n][1]));
-      tm1 = fmaxf(tm1, fmaxf(s[n][2], s[n][3]));
-    }
-    // the four threads of a group share a row: reduce the tile maxima there
-    tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 1));
-    tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 2));
-    tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 1));
-    tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 2));
-    const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);  // finite: key 0 is always seen
-    const float a0 = ex2(m0 - mn0), a1 = ex2(m1 - mn1);     // 0 on the first tile
-    m0 = mn0;
-    m1 = mn1;
-    l0 *= a0;
-    l1 *= a1;
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o[n][0] *= a0;
-      o[n][1] *= a0;
-      o[n][2] *= a1;
-      o[n][3] *= a1;
-    }
-    // probabilities, their row sums, and P as bf16 A fragments (k = 16 keys)
-    uint32_t pf[4][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const float p0 = ex2(s[n][0] - m0), p1 = ex2(s[n][1] - m0);
-      const float p2 = ex2(s[n][2] - m1), p3 = ex2(s[n][3] - m1);
-      l0 += p0 + p1;
-      l1 += p2 + p3;
-      const int ks16 = n >> 1, hi = n & 1;
-      pf[ks16][hi * 2 + 0] = pack_bf16(p0, p1);  // rows g: a0a1 (n even) / a4a5 (n odd)
-      pf[ks16][hi * 2 + 1] = pack_bf16(p2, p3);  // rows g + 8: a2a3 / a6a7
-    }
-    // O += P V: V tile rows are keys (k), columns d (n); ldmatrix.trans gives B
-#pragma unroll
-    for (int ks16 = 0; ks16 < 4; ++ks16) {
-#pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_addr(vb + (ks16 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LD + dp * 16 +
-                            (lane >> 4) * 8),
-                  b0, b1, b2, b3);
-        mma_bf16(o[2 * dp], pf[ks16][0], pf[ks16][1], pf[ks16][2], pf[ks16][3], b0, b1);
-        mma_bf16(o[2 * dp + 1], pf[ks16][0], pf[ks16][1], pf[ks16][2], pf[ks16][3], b2, b3);
-      }
-    }
-    __syncthreads();  // every warp is done with stage st before it is refilled
   }
-  cp_async_wait<0>();
+  if (p.lse != nullptr && row < seq)
+    p.lse[(int64_t)head * seq + row] = (m + __log2f(l)) * 0.6931471805599453f;
 
-  // row sums over the group, then O / l and lse
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float inv0 = 1.f / l0, inv1 = 1.f / l1;
-  const int64_t row0 = (int64_t)qt * kBr + warp * 16 + g;  // query index of rows g, g + 8
-  char* og = p.o + hoff;
-#pragma unroll
-  for (int n = 0; n < D / 8; ++n) {
-    const int col = n * 8 + 2 * t;
-    *reinterpret_cast<uint32_t*>(og + (row0 * D + col) * 2) = pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
-    *reinterpret_cast<uint32_t*>(og + ((row0 + 8) * D + col) * 2) =
-        pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
-  }
-  if (p.lse != nullptr && t == 0) {
-    constexpr float kLn2 = 0.6931471805599453f;
-    p.lse[head * p.seq + row0] = (m0 + __log2f(l0)) * kLn2;
-    p.lse[head * p.seq + row0 + 8] = (m1 + __log2f(l1)) * kLn2;
-  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(C::kCols)
+                 : "memory");
+}
+
+// cuTensorMapEncodeTiled from the driver (resolved once; the library links
+// only the runtime).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
 }
 
 }  // namespace
 
 AttnKernel attn_fwd_kernel_for(int d) {
-  constexpr int kSmem64 = (kBr + 4 * kBc) * (64 + kPad) * 2;
-  constexpr int kSmem128 = (kBr + 4 * kBc) * (128 + kPad) * 2;
-  if (d == 64) return AttnKernel{(const void*)attn_fwd_kernel<64>, kSmem64};
-  if (d == 128) return AttnKernel{(const void*)attn_fwd_kernel<128>, kSmem128};
+  if (d == 64) return AttnKernel{(const void*)attn_fwd_kernel<64>, AttnCfg<64>::kSmem};
+  if (d == 128) return AttnKernel{(const void*)attn_fwd_kernel<128>, AttnCfg<128>::kSmem};
   return AttnKernel{nullptr, 0};
+}
+
+const char* attn_fwd_launch(const AttnParams& p, int64_t bh, int d, cudaStream_t stream) {
+  const AttnKernel ak = attn_fwd_kernel_for(d);
+  if (ak.fn == nullptr) return "head_dim must be 64 or 128";
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return "cuTensorMapEncodeTiled is not available from the driver";
+  // [bh][seq][d] bf16 as a 3-D tensor (d innermost); boxes of 64 x 128 x 1
+  // with 128-byte swizzle; rows past seq read as zeros
+  CUtensorMap maps[3];
+  const char* ptrs[3] = {p.q, p.k, p.v};
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)p.seq, (cuuint64_t)bh};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)p.seq * d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kBM, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  for (int i = 0; i < 3; ++i) {
+    if (encode(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<char*>(ptrs[i]), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return "tensor map encoding failed";
+  }
+  AttnParams pc = p;
+  void* args[] = {&maps[0], &maps[1], &maps[2], &pc};
+  const dim3 grid((unsigned)bh, (unsigned)((p.seq + kBM - 1) / kBM));
+  if (cudaLaunchKernel(ak.fn, grid, dim3(128), args, (size_t)ak.smem, stream) != cudaSuccess)
+    return "launch failed";
+  return nullptr;
 }
 
 }  // namespace rr

@@ -1334,13 +1334,15 @@ rr_status rr_attention_fwd(const void* q, const void* k, const void* v, void* o,
     if (ak.smem > di->smem_optin) return fail(RR_ERR_INVALID_ARG, "attention tile exceeds shared memory");
     if ((st = set_smem(di, ak.fn, (size_t)ak.smem)) != RR_OK) return st;
   }
+  int* err = device_error_word();
+  if (!err) return RR_ERR_CUDA;
   rr::AttnParams p{static_cast<const char*>(q), static_cast<const char*>(k),
-                   static_cast<const char*>(v), static_cast<char*>(o), lse, seq,
+                   static_cast<const char*>(v), static_cast<char*>(o), lse, err, seq,
                    scale * 1.4426950408889634f, causal ? 1 : 0};
-  void* args[] = {&p};
-  cudaError_t e = cudaLaunchKernel(ak.fn, dim3((unsigned)bh, (unsigned)(seq / 64)), dim3(128), args,
-                                   (size_t)ak.smem, stream);
-  if (e != cudaSuccess) return fail(RR_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  if (const char* why = rr::attn_fwd_launch(p, bh, (int)head_dim, stream)) {
+    cudaError_t e = cudaGetLastError();
+    return fail(RR_ERR_CUDA, "attention: %s (%s)", why, cudaGetErrorString(e));
+  }
   return ok();
 }
 

@@ -1,6 +1,9 @@
 // rr_kernels.h -- host-side view of the compiled kernel variants.
 #pragma once
 
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
 namespace rr {
 
 constexpr int kNumDirectG = 11;  // row groups of 1, 2, 4, ..., 1024 threads
@@ -82,6 +85,7 @@ struct AttnParams {
   const char* v;
   char* o;
   float* lse;  // [bh][seq] natural-log sum of exp of the scaled scores, or null
+  int* err;    // device error word (a bounded wait that gave up)
   int64_t seq;
   float scale_log2;
   int32_t causal;
@@ -91,6 +95,10 @@ struct AttnKernel {
   int smem;        // dynamic shared memory bytes
 };
 AttnKernel attn_fwd_kernel_for(int d);
+// Encodes the TMA tensor maps of q, k, v and launches the kernel for head
+// dimension d on stream: null on success, else a short reason (nothing
+// launched, or the launch failed).
+const char* attn_fwd_launch(const AttnParams& p, int64_t bh, int d, cudaStream_t stream);
 const void* col_reduce_kernel_ptr_f32();
 const void* col_reduce_kernel_ptr_bf16();
 
