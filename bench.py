@@ -584,6 +584,14 @@ def run_profile_case(args):
         lab = torch.from_numpy(xe["labels"]).to(dev)
         loss = torch.empty(x.shape[0], device=dev)
         fn = lambda: rr.rr_softmax_xent_fwd_bwd(x, lab, loss, x)  # noqa: E731
+    elif args.profile == "attention":
+        # causal attention, 8 batches x 16 heads x 512 queries; --profile-rows
+        # gives the head dimension (64 by default)
+        d_head = args.profile_rows or 64
+        q, k, v = (bf16(a) for a in synth.attn_inputs(128, 512, d_head, 31 + d_head))
+        o = torch.empty_like(q)
+        lse = torch.empty((128, 512), device=dev)
+        fn = lambda: rr.rr_attention_fwd(q, k, v, o, lse, causal=True)  # noqa: E731
     elif args.profile == "softmax":
         sm = synth.make("softmax_bf16_causal_65536x512")
         x = bf16(sm["x"])
@@ -825,7 +833,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["xent", "softmax", "ln_fwd", "ln_bwd"], default=None,
+    ap.add_argument("--profile", choices=["xent", "softmax", "ln_fwd", "ln_bwd", "attention"],
+                    default=None,
                     help="run only this kernel (for ncu captures of one kernel)")
     ap.add_argument("--profile-rows", type=int, default=0)
     ap.add_argument("--profile-workload", default="", help="LayerNorm workload name for --profile")

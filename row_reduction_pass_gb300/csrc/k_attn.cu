@@ -29,6 +29,7 @@
 //
 // Shapes: bf16 q, k, v, o of [bh][s][d], d = 64 or 128, s a multiple of 64,
 // 16-byte aligned tensors (checked by the caller).
+#include <algorithm>
 #include <cstdint>
 
 #include <cuda.h>
@@ -40,28 +41,17 @@
 namespace rr {
 namespace {
 
-constexpr int kBM = 128;          // query rows per CTA: MMA M, TMEM lanes
-constexpr int kBN = 128;          // keys per tile: N of S = Q K^T, K of O = P V
-constexpr int kBoxBytes = kBM * 128;  // one TMA box: 128 rows x 64 bf16 (128 bytes)
+constexpr int kBM = 128;              // query rows per tile: MMA M, TMEM lanes
+constexpr int kBoxBytes = kBM * 128;  // one Q box: 128 rows x 64 bf16 (128 bytes)
 
-template <int D>
-struct AttnCfg {
-  static constexpr int kBoxes = D / 64;                 // boxes per Q / K / V tile
-  static constexpr int kTile = kBoxes * kBoxBytes;      // bytes of a Q, K or V tile
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = kTile;                  // [2 stages][K, V]
-  static constexpr int kOffBar = kTile + 4 * kTile;     // mbarriers and the TMEM address
-  static constexpr int kSmem = kOffBar + 128 + 1024;    // + slack for 1024-byte alignment
-  // TMEM columns: S [0, 128), P (bf16 pairs) [128, 192), O [kColO, kColO + D)
-  static constexpr uint32_t kCols = D == 64 ? 256 : 512;
-  static constexpr uint32_t kColS = 0, kColP = 128, kColO = D == 64 ? 192 : 256;
-  // instruction descriptors (kind::f16): D fp32, A and B bf16, M = 128;
-  // S: B K-major, N = 128.  O: B MN-major (bit 16), N = D.
-  static constexpr uint32_t kIdescS =
-      (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-  static constexpr uint32_t kIdescO = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
-                                      ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-};
+// Instruction descriptors (kind::f16): D fp32 (bits 4-5), A and B bf16 (bits
+// 7-9, 10-12), B K-major or MN-major (bit 16), N >> 3 (bits 17-22), M >> 4
+// (bits 24-28).  S = Q K^T: B K-major, N = the key tile.  O = P V: B MN-major
+// (the head dimension is contiguous in V), N = D.
+__host__ __device__ constexpr uint32_t attn_idesc(int m, int n, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
 
 // Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
 // and stride byte offsets (16-byte units), the fixed 0b001 at bits 46-48.
@@ -155,204 +145,418 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// 32 TMEM columns of this thread's lane, without waiting (tcgen05.wait::ld
+// before the registers are used).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Bounded wait without asking to be suspended (the issuer reacts at once);
+// after a wait gave up (dead) it returns immediately.
+__device__ __forceinline__ void wait_spin(uint64_t* bar, uint32_t parity, bool& dead, int* err) {
+  if (dead) return;
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > 1000000000ull) {
+      atomicCAS(err, 0, 6);
+      dead = true;
+      return;
+    }
+  }
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Persistent CTAs (one per SM), each running two independent pipelines w =
+// 0, 1: a softmax warpgroup (warps 4w .. 4w + 3; thread t owns query row t of
+// the tile, TMEM lane t) and an issuer warp (warp 8 + w, lane 0) that issues
+// the pipeline's TMA loads and MMAs.  Pipeline w owns TMEM columns [256 w,
+// 256 w + 256): S [0, BN), P (bf16 pairs) [BN, BN + BN / 2), O [256 - D, 256),
+// and its own Q tile and two-stage rings of K and of V tiles in shared memory.
+// The two pipelines interleave on the SM: one's softmax runs while the tensor
+// cores work for the other.
+// A pipeline works through query tiles (head, tile) in a zigzag of the list
+// sorted heaviest first (causal: most key tiles first), so the pipelines of
+// all SMs end together.  Its key tiles are numbered t = 0, 1, ... across its
+// query tiles.  Issuer, per key tile t:
+//   S(t + 1) = Q K(t + 1)^T as soon as the softmax has read S(t) (so it runs
+//     during the softmax of t) -> bar_s; K(t + 2) then loads into the stage
+//     S(t) has finished with;
+//   once P(t) is written: O += P(t) V(t) -> bar_o; V(t + 1) then loads into
+//     the stage O += P V of t - 1 has finished with.
+//   The next query tile's Q loads once the current one's last S is done; its
+//   first O += P V (which overwrites O) waits for the softmax to read O.
+// Softmax, per key tile: [bar_s] read S -> bar_sfree; max, P = 2^(s - m),
+// sums; [O += P V of t - 1 done] write P, O *= alpha -> bar_p; after a query
+// tile's last key tile: [bar_o] O / l, lse -> bar_ofree.
 template <int D>
-__global__ void __launch_bounds__(128, 1)
+struct AttnPL {
+  static constexpr int BN = D == 64 ? 128 : 64;        // keys per tile
+  static constexpr int NS = 2;                         // K / V stages
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kQBytes = kBoxes * kBoxBytes;   // 128 rows
+  static constexpr int kKVBox = BN * 128;              // one K or V box of BN rows
+  static constexpr int kKVBytes = kBoxes * kKVBox;
+  static constexpr int kPipe = kQBytes + NS * 2 * kKVBytes;  // smem of one pipeline
+  static constexpr int kOffBar = 2 * kPipe;
+  static constexpr int kSmem = kOffBar + 512 + 1024;
+  static constexpr uint32_t kColS = 0, kColP = BN, kColO = 256 - D;
+  static constexpr uint32_t kIdescS = attn_idesc(kBM, BN, false);
+  static constexpr uint32_t kIdescO = attn_idesc(kBM, D, true);
+};
+
+// The r-th query tile of pipeline slot `slot` among nslots: a zigzag over the
+// list sorted by decreasing work (causal: tile nq - 1 of every head first),
+// or -1 past the end.  Writes the head and query tile.
+__device__ __forceinline__ bool attn_item(int r, int slot, int nslots, int bh, int nq, int& head,
+                                          int& qt) {
+  const int i = r * nslots + ((r & 1) ? nslots - 1 - slot : slot);
+  if (i >= bh * nq) return false;
+  qt = nq - 1 - i / bh;
+  head = i % bh;
+  return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const AttnParams p) {
   static_assert(D == 64 || D == 128, "head dimension 64 or 128");
-  using C = AttnCfg<D>;
+  using C = AttnPL<D>;
+  constexpr int BN = C::BN;
   extern __shared__ unsigned char smem_raw[];
-  // 128-byte swizzled tiles want 1024-byte alignment
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* sq = smem + C::kOffQ;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* bar_q = bars + 0;
-  uint64_t* bar_full = bars + 1;  // [2]: K / V tile landed in the stage
-  uint64_t* bar_s = bars + 3;     // S = Q K^T done
-  uint64_t* bar_o = bars + 4;     // O += P V done
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
-  auto stage_k = [&](int s) { return smem + C::kOffKV + (2 * s) * C::kTile; };
-  auto stage_v = [&](int s) { return smem + C::kOffKV + (2 * s + 1) * C::kTile; };
-
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int w = warp < 8 ? warp >> 2 : warp - 8;  // this thread's pipeline
+  unsigned char* pipe = smem + w * C::kPipe;
+  unsigned char* sq = pipe;
+  auto stage_k = [&](int s) { return pipe + C::kQBytes + (2 * s) * C::kKVBytes; };
+  auto stage_v = [&](int s) { return pipe + C::kQBytes + (2 * s + 1) * C::kKVBytes; };
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar) + w * 16;
+  uint64_t* bar_q = bars + 0;
+  uint64_t* bar_s = bars + 1;
+  uint64_t* bar_sfree = bars + 2;   // 128 arrivals
+  uint64_t* bar_p = bars + 3;       // 128 arrivals
+  uint64_t* bar_o = bars + 4;
+  uint64_t* bar_ofree = bars + 5;   // 128 arrivals
+  uint64_t* bar_kfull = bars + 6;   // [2] K tile landed
+  uint64_t* bar_vfull = bars + 8;   // [2] V tile landed
+  uint64_t* bar_kempty = bars + 10; // [2] S done with the K stage
+  uint64_t* bar_vempty = bars + 12; // [2] O += P V done with the V stage
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(reinterpret_cast<uint64_t*>(smem + C::kOffBar) + 40);
+
   const int seq = static_cast<int>(p.seq);
-  const int head = static_cast<int>(blockIdx.x);
-  // grid (heads, query tiles): blocks are dispatched x fastest, so every head's
-  // heaviest causal tile (the most key tiles) goes out before any lighter one
-  const int qt = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
-  const int q0 = qt * kBM;
-  const int last_key = p.causal ? min(seq - 1, q0 + kBM - 1) : seq - 1;
-  const int nkv = last_key / kBN + 1;
+  const int bh = static_cast<int>(p.bh);
+  const int nq = (seq + kBM - 1) / kBM;
+  const int slot = static_cast<int>(blockIdx.x) * 2 + w, nslots = 2 * static_cast<int>(gridDim.x);
+  auto tiles_of = [&](int qt) {  // key tiles a query tile needs
+    const int last_key = p.causal ? min(seq - 1, qt * kBM + kBM - 1) : seq - 1;
+    return last_key / BN + 1;
+  };
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tslot)),
-                 "r"(C::kCols)
+                 "r"(512u)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+  if (warp >= 8 && (tid & 31) == 0) {
+    mbar_init(bar_q, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_sfree, 128);
+    mbar_init(bar_p, 128);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_ofree, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_kfull[i], 1);
+      mbar_init(&bar_vfull[i], 1);
+      mbar_init(&bar_kempty[i], 1);
+      mbar_init(&bar_vempty[i], 1);
+    }
     fence_mbar_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tslot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
-  const uint32_t tS = tmem + lane_base + C::kColS;
-  const uint32_t tP = tmem + lane_base + C::kColP;
-  const uint32_t tO = tmem + lane_base + C::kColO;
-
-  auto issue_kv = [&](int j) {  // key tile j into stage j & 1 (thread 0)
-    const int s = j & 1;
-    mbar_arrive_expect_tx(&bar_full[s], 2 * C::kTile);
-#pragma unroll
-    for (int b = 0; b < C::kBoxes; ++b) {
-      tma_load_3d(stage_k(s) + b * kBoxBytes, &tk, 64 * b, j * kBN, head, &bar_full[s]);
-      tma_load_3d(stage_v(s) + b * kBoxBytes, &tv, 64 * b, j * kBN, head, &bar_full[s]);
-    }
-  };
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_q, C::kTile);
-#pragma unroll
-    for (int b = 0; b < C::kBoxes; ++b) tma_load_3d(sq + b * kBoxBytes, &tq, 64 * b, q0, head, bar_q);
-    issue_kv(0);
-    if (nkv > 1) issue_kv(1);
-  }
-
-  const int row = q0 + tid;   // this thread's query
-  float m = -INFINITY, l = 0.f;  // running maximum (log2 domain) and sum
-  bool dead = false;             // a wait gave up: no further waits (the kernel still ends)
+  const uint32_t tm = *tslot + 256u * w;  // this pipeline's columns
+  bool dead = false;  // a wait gave up: no further waits (the kernel still ends)
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     if (!dead) dead = !mbar_wait_bounded(bar, parity, p.err);
   };
-  const uint32_t q_addr = smem_addr(sq);
 
-  for (int j = 0; j < nkv; ++j) {
-    const int s = j & 1;
-    if (tid == 0) {
-      wait(&bar_full[s], (uint32_t)((j >> 1) & 1));
-      if (j == 0) wait(bar_q, 0);
+  if (warp >= 8) {
+    // ------------------------------------------------------- the issuer
+    if ((tid & 31) == 0) {
+      // the pipeline's key tiles in order: (query tile r, tile j of it, head)
+      struct Cur {
+        int r, j, n, head, qt;
+        bool ok;
+      };
+      auto first = [&]() {
+        Cur c{0, 0, 0, 0, 0, false};
+        c.ok = attn_item(0, slot, nslots, bh, nq, c.head, c.qt);
+        if (c.ok) c.n = tiles_of(c.qt);
+        return c;
+      };
+      auto advance = [&](Cur& c) {
+        if (++c.j == c.n) {
+          c.j = 0;
+          c.ok = attn_item(++c.r, slot, nslots, bh, nq, c.head, c.qt);
+          if (c.ok) c.n = tiles_of(c.qt);
+        }
+      };
+      Cur kc = first(), vc = first();  // next K / V tile to load
+      int kt = 0, vt = 0;              // their numbers
+      auto load_k = [&]() {
+        const int s = kt & 1;
+        mbar_arrive_expect_tx(&bar_kfull[s], C::kKVBytes);
+#pragma unroll
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d(stage_k(s) + b * C::kKVBox, &tk, 64 * b, kc.j * BN, kc.head, &bar_kfull[s]);
+        ++kt;
+        advance(kc);
+      };
+      auto load_v = [&]() {
+        const int s = vt & 1;
+        mbar_arrive_expect_tx(&bar_vfull[s], C::kKVBytes);
+#pragma unroll
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d(stage_v(s) + b * C::kKVBox, &tv, 64 * b, vc.j * BN, vc.head, &bar_vfull[s]);
+        ++vt;
+        advance(vc);
+      };
+      auto load_q = [&](const Cur& c) {
+        mbar_arrive_expect_tx(bar_q, C::kQBytes);
+#pragma unroll
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d(sq + b * kBoxBytes, &tq, 64 * b, c.qt * kBM, c.head, bar_q);
+      };
+      auto issue_s = [&](int t) {  // S = Q K^T of key tile t
+        const uint32_t q_addr = smem_addr(sq), k_addr = smem_addr(stage_k(t & 1));
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qo = (uint32_t)((kk >> 2) * kBoxBytes + (kk & 3) * 32);
+          const uint32_t ko = (uint32_t)((kk >> 2) * C::kKVBox + (kk & 3) * 32);
+          mma_ss(tm + C::kColS, sw128_desc(q_addr + qo, 16, 1024),
+                 sw128_desc(k_addr + ko, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_s);
+        mma_commit(&bar_kempty[t & 1]);
+      };
+      auto issue_pv = [&](int t, bool first_of_tile) {  // O (+)= P V of key tile t
+        const uint32_t v_addr = smem_addr(stage_v(t & 1));
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tm + C::kColO, tm + C::kColP + 8 * kk,
+                 sw128_desc(v_addr + kk * 2048, C::kKVBox, 1024), C::kIdescO,
+                 (!first_of_tile || kk > 0) ? 1u : 0u);
+        mma_commit(bar_o);
+        mma_commit(&bar_vempty[t & 1]);
+      };
+      int qr = 0;  // the last query tile whose Q has been loaded
+      // After S of key tile c (number t): if it is the last of its query tile,
+      // the next query tile's Q loads as soon as that S is done.
+      auto after_s = [&](const Cur& c, int t) {
+        if (c.j != c.n - 1) return;
+        Cur q2{c.r + 1, 0, 0, 0, 0, false};
+        q2.ok = attn_item(q2.r, slot, nslots, bh, nq, q2.head, q2.qt);
+        if (!q2.ok) return;
+        wait_spin(bar_s, (uint32_t)(t & 1), dead, p.err);
+        load_q(q2);
+        qr = q2.r;
+      };
+      Cur cur = first();  // key tile t
+      if (cur.ok) {
+        load_q(cur);
+        load_k();
+        load_v();
+        if (kc.ok) {
+          load_k();
+          load_v();
+        }
+        wait_spin(bar_q, 0, dead, p.err);
+        wait_spin(&bar_kfull[0], 0, dead, p.err);
+        issue_s(0);
+        after_s(cur, 0);
+      }
+      for (int t = 0; cur.ok; ++t) {
+        Cur nxt = cur;
+        advance(nxt);
+        // V(t + 1) into the stage O += P V of t - 1 used, as soon as that is
+        // done (it is needed only after the softmax of t + 1)
+        if (vc.ok && vt == t + 1 && t >= 1) {
+          wait_spin(&bar_vempty[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), dead, p.err);
+          load_v();
+        }
+        if (nxt.ok) {
+          // S(t + 1) once the softmax has read S(t); a new query tile's Q was
+          // loaded after the current one's last S
+          wait_spin(bar_sfree, (uint32_t)(t & 1), dead, p.err);
+          if (nxt.r != cur.r) {
+            if (qr < nxt.r) {  // not reached: after_s loaded it
+              load_q(nxt);
+              qr = nxt.r;
+            }
+            wait_spin(bar_q, (uint32_t)(nxt.r & 1), dead, p.err);
+          }
+          wait_spin(&bar_kfull[(t + 1) & 1], (uint32_t)(((t + 1) >> 1) & 1), dead, p.err);
+          issue_s(t + 1);
+          after_s(nxt, t + 1);
+          // K(t + 2) into the stage S(t) used
+          if (kc.ok && kt == t + 2) {
+            wait_spin(&bar_kempty[t & 1], (uint32_t)((t >> 1) & 1), dead, p.err);
+            load_k();
+          }
+        }
+        // O += P(t) V(t); the first of a query tile overwrites O
+        if (cur.j == 0 && cur.r > 0) wait_spin(bar_ofree, (uint32_t)((cur.r - 1) & 1), dead, p.err);
+        wait_spin(bar_p, (uint32_t)(t & 1), dead, p.err);
+        wait_spin(&bar_vfull[t & 1], (uint32_t)((t >> 1) & 1), dead, p.err);
+        issue_pv(t, cur.j == 0);
+        cur = nxt;
+      }
+    }
+  } else {
+    // ------------------------------------------------ softmax warpgroup
+    const int t_row = tid & 127;  // row in the tile, TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tm + lane_base + C::kColS;
+    const uint32_t tP = tm + lane_base + C::kColP;
+    const uint32_t tO = tm + lane_base + C::kColO;
+    const float sc = p.scale_log2;
+    int t = 0;
+    int head = 0, qt = 0;
+    for (int r = 0; attn_item(r, slot, nslots, bh, nq, head, qt); ++r) {
+      const int n = tiles_of(qt);
+      const int q0 = qt * kBM, row = q0 + t_row;
+      const int lim = p.causal ? min(row, seq - 1) : seq - 1;  // last visible key
+      float m = -INFINITY, l = 0.f;  // running maximum (log2 domain) and sum
+      for (int j = 0; j < n; ++j, ++t) {
+        wait(bar_s, (uint32_t)(t & 1));
+        tc_fence_after();
+        uint32_t v[BN / 32][32];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32_nowait(tS + 32 * c, v[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(bar_sfree);  // S may take the next tile
+        const int key0 = j * BN;
+        // keys to mask: after the query (causal, diagonal tiles) or past the end
+        if (p.causal ? (key0 + BN - 1 > q0) : (key0 + BN > seq)) {
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (key0 + 32 * c + i > lim) v[c][i] = __float_as_uint(-INFINITY);
+        }
+        // the tile's row maximum on the raw scores (scale > 0 keeps the order)
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            mx0 = fmaxf(mx0, __uint_as_float(v[c][i]));
+            mx1 = fmaxf(mx1, __uint_as_float(v[c][i + 1]));
+          }
+        // The running maximum m moves only when the tile's maximum exceeds it
+        // by more than 8 (log2 domain): otherwise P = 2^(s - m) stays below
+        // 2^8 and O, l keep their scale, so O is rarely rescaled.  (Finite
+        // after the first tile: key 0 is visible to every row.)
+        const float mt = fmaxf(mx0, mx1) * sc;
+        const float m_new = mt > m + 8.f ? mt : m;
+        const float alpha = ex2(m - m_new);  // 1 if m stays, 0 on the first tile
+        float l0 = 0.f, l1 = 0.f;
+        uint32_t pk[BN / 32][16];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(v[c][i]), sc, -m_new));
+            const float p1 = ex2(fmaf(__uint_as_float(v[c][i + 1]), sc, -m_new));
+            add2(l0, l1, l0, l1, p0, p1);
+            pk[c][i >> 1] = pack_bf16(p0, p1);
+          }
+        l = l * alpha + (l0 + l1);
+        m = m_new;
+        // O += P V of tile t - 1 must be done before P and O are written
+        if (t > 0) {
+          wait(bar_o, (uint32_t)((t - 1) & 1));
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_st16(tP + 16 * c, pk[c]);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          uint32_t o[D / 32][32];  // every load issued before the one wait
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(tO + 32 * c, o[c]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float a0, a1;
+              mul2(a0, a1, __uint_as_float(o[c][i]), __uint_as_float(o[c][i + 1]), alpha, alpha);
+              o[c][i] = __float_as_uint(a0);
+              o[c][i + 1] = __float_as_uint(a1);
+            }
+            tmem_st32(tO + 32 * c, o[c]);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_p);
+      }
+      // O / l in bf16 and lse, for rows inside the sequence
+      wait(bar_o, (uint32_t)((t - 1) & 1));
       tc_fence_after();
-      const uint32_t k_addr = smem_addr(stage_k(s));
+      const float inv = 1.f / l;
+      char* orow = p.o + ((int64_t)head * seq + row) * D * 2;
+      uint32_t o[D / 32][32];
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        // K-step kk: box kk / 4, 32-byte column block kk % 4 within the 128-byte swizzle row
-        const uint32_t off = (uint32_t)((kk >> 2) * kBoxBytes + (kk & 3) * 32);
-        mma_ss(tmem + C::kColS, sw128_desc(q_addr + off, 16, 1024),
-               sw128_desc(k_addr + off, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+      for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(tO + 32 * c, o[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(bar_ofree);  // O read: the next query tile may overwrite it
+      if (row < seq) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            const uint4 q4 = make_uint4(
+                pack_bf16(__uint_as_float(o[c][i]) * inv, __uint_as_float(o[c][i + 1]) * inv),
+                pack_bf16(__uint_as_float(o[c][i + 2]) * inv, __uint_as_float(o[c][i + 3]) * inv),
+                pack_bf16(__uint_as_float(o[c][i + 4]) * inv, __uint_as_float(o[c][i + 5]) * inv),
+                pack_bf16(__uint_as_float(o[c][i + 6]) * inv, __uint_as_float(o[c][i + 7]) * inv));
+            *reinterpret_cast<uint4*>(orow + (32 * c + i) * 2) = q4;
+          }
       }
-      mma_commit(bar_s);
-      // the stage of tile j - 1 is free once O += P V of tile j - 1 is done:
-      // tile j + 1 goes there (tiles 0 and 1 were loaded up front)
-      if (j >= 1 && j + 1 < nkv) {
-        wait(bar_o, (uint32_t)((j - 1) & 1));
-        issue_kv(j + 1);
-      }
-    }
-    wait(bar_s, (uint32_t)(j & 1));  // also covers O += P V of tile j - 1 (committed earlier)
-    tc_fence_after();
-
-    // keys of this tile to mask: after the query (causal, diagonal tile) or past the end
-    const int key0 = j * kBN;
-    const bool need_mask = p.causal ? (key0 + kBN - 1 > q0) : (key0 + kBN > seq);
-    const int lim = p.causal ? min(row, seq - 1) : seq - 1;  // last visible key
-    // 1. the tile's row maximum (log2 domain)
-    float mx = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kBN / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32(tS + 32 * c, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float x = __uint_as_float(v[i]) * p.scale_log2;
-        if (need_mask && key0 + 32 * c + i > lim) x = -INFINITY;
-        mx = fmaxf(mx, x);
-      }
-    }
-    const float m_new = fmaxf(m, mx);  // finite: key 0 is visible to every row
-    const float alpha = ex2(m - m_new);  // 0 on the first tile
-    // 2. P = 2^(s - m_new) as bf16 into TMEM, the row sum from the fp32 values
-    float ls = 0.f;
-#pragma unroll
-    for (int c = 0; c < kBN / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32(tS + 32 * c, v);
-      uint32_t pk[16];
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        float x0 = __uint_as_float(v[i]) * p.scale_log2;
-        float x1 = __uint_as_float(v[i + 1]) * p.scale_log2;
-        if (need_mask && key0 + 32 * c + i > lim) x0 = -INFINITY;
-        if (need_mask && key0 + 32 * c + i + 1 > lim) x1 = -INFINITY;
-        const float p0 = ex2(x0 - m_new), p1 = ex2(x1 - m_new);
-        ls += p0 + p1;
-        pk[i >> 1] = pack_bf16(p0, p1);
-      }
-      tmem_st16(tP + 16 * c, pk);
-    }
-    l = l * alpha + ls;
-    m = m_new;
-    // 3. O *= alpha (O += P V of tile j - 1 is complete: see the wait above)
-    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + 32 * c, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-        tmem_st32(tO + 32 * c, v);
-      }
-    }
-    tmem_st_wait();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t v_addr = smem_addr(stage_v(s));
-#pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk) {
-        // 16 keys per step: two 8-row groups of the swizzled V tile (1024 bytes
-        // each); the head dimension's 64-column blocks are kBoxBytes apart
-        mma_ts(tmem + C::kColO, tmem + C::kColP + 8 * kk,
-               sw128_desc(v_addr + kk * 2048, kBoxBytes, 1024), C::kIdescO,
-               (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      mma_commit(bar_o);
+      if (p.lse != nullptr && row < seq)
+        p.lse[(int64_t)head * seq + row] = (m + __log2f(l)) * 0.6931471805599453f;
     }
   }
-
-  // O / l in bf16 and lse, for the rows inside the sequence
-  wait(bar_o, (uint32_t)((nkv - 1) & 1));
-  tc_fence_after();
-  const float inv = 1.f / l;
-  char* orow = p.o + ((int64_t)head * seq + row) * D * 2;
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t v[32];
-    tmem_ld32(tO + 32 * c, v);
-    if (row < seq) {
-#pragma unroll
-      for (int i = 0; i < 32; i += 8) {
-        const uint4 w = make_uint4(
-            pack_bf16(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv),
-            pack_bf16(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv),
-            pack_bf16(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv),
-            pack_bf16(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv));
-        *reinterpret_cast<uint4*>(orow + (32 * c + i) * 2) = w;
-      }
-    }
-  }
-  if (p.lse != nullptr && row < seq)
-    p.lse[(int64_t)head * seq + row] = (m + __log2f(l)) * 0.6931471805599453f;
 
   tc_fence_before();
   __syncthreads();
   if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(C::kCols)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tslot), "r"(512u)
                  : "memory");
 }
 
@@ -374,25 +578,27 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }  // namespace
 
 AttnKernel attn_fwd_kernel_for(int d) {
-  if (d == 64) return AttnKernel{(const void*)attn_fwd_kernel<64>, AttnCfg<64>::kSmem};
-  if (d == 128) return AttnKernel{(const void*)attn_fwd_kernel<128>, AttnCfg<128>::kSmem};
+  if (d == 64) return AttnKernel{(const void*)attn_fwd_kernel<64>, AttnPL<64>::kSmem};
+  if (d == 128) return AttnKernel{(const void*)attn_fwd_kernel<128>, AttnPL<128>::kSmem};
   return AttnKernel{nullptr, 0};
 }
 
-const char* attn_fwd_launch(const AttnParams& p, int64_t bh, int d, cudaStream_t stream) {
+const char* attn_fwd_launch(const AttnParams& p, int d, int sms, cudaStream_t stream) {
   const AttnKernel ak = attn_fwd_kernel_for(d);
   if (ak.fn == nullptr) return "head_dim must be 64 or 128";
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return "cuTensorMapEncodeTiled is not available from the driver";
-  // [bh][seq][d] bf16 as a 3-D tensor (d innermost); boxes of 64 x 128 x 1
-  // with 128-byte swizzle; rows past seq read as zeros
+  // [bh][seq][d] bf16 as a 3-D tensor (d innermost); 128-byte swizzled boxes
+  // of 64 columns x rows x 1 head (Q: 128 rows, K / V: the key tile); rows
+  // past seq read as zeros
+  const int bn = d == 64 ? AttnPL<64>::BN : AttnPL<128>::BN;
   CUtensorMap maps[3];
   const char* ptrs[3] = {p.q, p.k, p.v};
-  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)p.seq, (cuuint64_t)bh};
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)p.seq, (cuuint64_t)p.bh};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)p.seq * d * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)kBM, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   for (int i = 0; i < 3; ++i) {
+    const cuuint32_t box[3] = {64, (cuuint32_t)(i == 0 ? kBM : bn), 1};
     if (encode(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<char*>(ptrs[i]), dims,
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -400,8 +606,11 @@ const char* attn_fwd_launch(const AttnParams& p, int64_t bh, int d, cudaStream_t
   }
   AttnParams pc = p;
   void* args[] = {&maps[0], &maps[1], &maps[2], &pc};
-  const dim3 grid((unsigned)bh, (unsigned)((p.seq + kBM - 1) / kBM));
-  if (cudaLaunchKernel(ak.fn, grid, dim3(128), args, (size_t)ak.smem, stream) != cudaSuccess)
+  // persistent: one CTA per SM (two pipelines each), fewer for small problems
+  const int64_t items = p.bh * ((p.seq + kBM - 1) / kBM);
+  const int64_t grid = std::min<int64_t>(sms, (items + 1) / 2);
+  if (cudaLaunchKernel(ak.fn, dim3((unsigned)grid), dim3(320), args, (size_t)ak.smem, stream) !=
+      cudaSuccess)
     return "launch failed";
   return nullptr;
 }

@@ -1326,6 +1326,7 @@ rr_status rr_attention_fwd(const void* q, const void* k, const void* v, void* o,
   if (lse != nullptr && (overlaps(lse, nl, q, n) || overlaps(lse, nl, k, n) ||
                          overlaps(lse, nl, v, n) || overlaps(lse, nl, o, n)))
     return fail(RR_ERR_ALIASING, "lse overlaps a tensor");
+  int sms = 0;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevInfo* di = nullptr;
@@ -1333,13 +1334,14 @@ rr_status rr_attention_fwd(const void* q, const void* k, const void* v, void* o,
     if (st != RR_OK) return st;
     if (ak.smem > di->smem_optin) return fail(RR_ERR_INVALID_ARG, "attention tile exceeds shared memory");
     if ((st = set_smem(di, ak.fn, (size_t)ak.smem)) != RR_OK) return st;
+    sms = di->sms;
   }
   int* err = device_error_word();
   if (!err) return RR_ERR_CUDA;
   rr::AttnParams p{static_cast<const char*>(q), static_cast<const char*>(k),
-                   static_cast<const char*>(v), static_cast<char*>(o), lse, err, seq,
+                   static_cast<const char*>(v), static_cast<char*>(o), lse, err, bh, seq,
                    scale * 1.4426950408889634f, causal ? 1 : 0};
-  if (const char* why = rr::attn_fwd_launch(p, bh, (int)head_dim, stream)) {
+  if (const char* why = rr::attn_fwd_launch(p, (int)head_dim, sms, stream)) {
     cudaError_t e = cudaGetLastError();
     return fail(RR_ERR_CUDA, "attention: %s (%s)", why, cudaGetErrorString(e));
   }

@@ -86,6 +86,7 @@ struct AttnParams {
   char* o;
   float* lse;  // [bh][seq] natural-log sum of exp of the scaled scores, or null
   int* err;    // device error word (a bounded wait that gave up)
+  int64_t bh;  // heads (batch x heads)
   int64_t seq;
   float scale_log2;
   int32_t causal;
@@ -96,9 +97,9 @@ struct AttnKernel {
 };
 AttnKernel attn_fwd_kernel_for(int d);
 // Encodes the TMA tensor maps of q, k, v and launches the kernel for head
-// dimension d on stream: null on success, else a short reason (nothing
-// launched, or the launch failed).
-const char* attn_fwd_launch(const AttnParams& p, int64_t bh, int d, cudaStream_t stream);
+// dimension d on stream (persistent: at most `sms` CTAs): null on success,
+// else a short reason (nothing launched, or the launch failed).
+const char* attn_fwd_launch(const AttnParams& p, int d, int sms, cudaStream_t stream);
 const void* col_reduce_kernel_ptr_f32();
 const void* col_reduce_kernel_ptr_bf16();
 

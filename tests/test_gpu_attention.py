@@ -64,6 +64,13 @@ def test_attention_full_shape_sampled_heads():
     run_attention(128, 512, 64, 2024, True, heads_checked=[0, 17, 35, 54, 71, 90, 109, 127])
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_attention_several_query_tiles_per_pipeline(d):
+    # 64 heads x 1024 keys, not causal: 512 query tiles, several per pipeline
+    # of the persistent kernel (query tile changes: Q reloads, O hand-over)
+    run_attention(64, 1024, d, 77 + d, False, heads_checked=[0, 21, 42, 63])
+
+
 def test_attention_lse_optional_and_empty():
     q, k, v = (dev_bf16(a) for a in synth.attn_inputs(2, 64, 64, 5))
     o = torch.empty_like(q)
