@@ -177,9 +177,6 @@ __device__ __forceinline__ void wait_spin(uint64_t* bar, uint32_t parity, bool& 
     }
   }
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
 
 // Persistent CTAs (one per SM), each running two independent pipelines w =
 // 0, 1: a softmax warpgroup (warps 4w .. 4w + 3; thread t owns query row t of

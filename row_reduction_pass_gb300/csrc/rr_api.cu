@@ -1,5 +1,6 @@
 // rr_api.cu -- the C ABI of librr.so: argument checks, per-device attribute
 // cache, choice of kernel variant, and launches on the caller's stream.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -525,9 +526,14 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
 // shorter rows (1000 columns: forward 16.9 against 28.6 us at best).
 constexpr int64_t kLnxMinBytes = 8192;
 
+//
+// op == kSoftmax takes the softmax-family kernels of rr_smx.cuh instead (smode
+// 0 softmax, 1 log-softmax, 2 cross-entropy): no gamma / beta, clusters for
+// rows beyond one block; RR_SMX=0 turns those off (tuning aid).
 rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
-                   int64_t max_partials, int force) {
-  if (const char* f = std::getenv("RR_LNX"); f != nullptr && f[0] == '0')
+                   int64_t max_partials, int force, int smode = -1) {
+  const bool smx = op == kSoftmax;
+  if (const char* f = std::getenv(smx ? "RR_SMX" : "RR_LNX"); f != nullptr && f[0] == '0')
     return fail(RR_ERR_INVALID_ARG, "phase-aligned kernels off");
   const int E = dt == RR_BF16 ? 2 : 4, W = 16 / E;
   if (cols * E < kLnxMinBytes || rows < 1) return fail(RR_ERR_INVALID_ARG, "short rows");
@@ -539,9 +545,10 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
   if (st != RR_OK) return st;
   static const rr::LnxKernels fk[2] = {rr::lnx_fwd_kernels_f32(), rr::lnx_fwd_kernels_bf16()};
   static const rr::LnxKernels bk[2] = {rr::lnx_bwd_kernels_f32(), rr::lnx_bwd_kernels_bf16()};
-  const int NQ = fwd ? fk[dt].nq_fwd : bk[dt].nq_bwd;
-  const int NT = fwd ? 1 : 2;
-  const int vecs = fwd ? (rms ? 1 : 2) : 1;  // gamma (, beta) planes
+  static const rr::SmxKernels sk[2] = {rr::smx_kernels_f32(), rr::smx_kernels_bf16()};
+  const int NQ = smx ? sk[dt].nq : fwd ? fk[dt].nq_fwd : bk[dt].nq_bwd;
+  const int NT = fwd || smx ? 1 : 2;
+  const int vecs = smx ? 0 : fwd ? (rms ? 1 : 2) : 1;  // gamma (, beta) planes
   const int64_t rb = (cols * E) % 16;
   int64_t P = 1;
   if (rb != 0) {
@@ -554,32 +561,56 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
   // clusters of row groups (bf16 65537 columns: 65.9 against 49.4 us), so it
   // takes this path only when tier 3 is forced.
   const int kmax = force == 1 ? 1 : (op == kLnFwd && force != 3) ? 1 : 8;
+  // Softmax family: the row stays in shared memory, so a thread holds no row
+  // in registers; NQ is the target of chunks per thread and a block takes up
+  // to 1024 threads.  A split that keeps three stages per ring is preferred
+  // to one with two (more rows in flight), and the norm kernels take any.
+  const int maxT = smx ? rr::kSmxMaxT : rr::kLnxMaxT;
+  int cpt = NQ, forceK = 0, blockT = smx ? 512 : 256, solo_max = 40;
+  // RR_SMX_CPT (chunks per thread), RR_SMX_BT (threads per block, groups of
+  // one-block rows), RR_SMX_SOLO (most chunks per lane of a row held by one
+  // warp, 0: never) and RR_LNX_K (cluster size) force a shape (tuning aids)
+  if (const char* f = std::getenv("RR_SMX_CPT"); smx && f) cpt = std::max(1, std::atoi(f));
+  if (const char* f = std::getenv("RR_SMX_BT"); smx && f) blockT = std::max(32, std::atoi(f));
+  if (const char* f = std::getenv("RR_SMX_SOLO")) solo_max = std::max(0, std::atoi(f));
+  if (const char* f = std::getenv("RR_LNX_K")) forceK = std::atoi(f);
+  for (int minNS = smx ? 3 : 2; minNS >= 2; --minNS)
   for (int K = force == 3 ? 2 : 1; K <= kmax; ++K) {
     const int64_t S = cdiv(nch_max, K);
     if (K > 1 && (K - 1) * S >= nch_min) break;  // every rank of every phase gets chunks
-    const int64_t G = round_up(cdiv(S, NQ), 32);
-    if (G > rr::kLnxMaxT) continue;
-    const void* fn = fwd ? fk[dt].fwd[rms][K > 1] : bk[dt].bwd[rms][K > 1];
+    if (forceK > 0 && K != forceK) continue;
+    // softmax family: one warp per row where its lanes hold at most solo_max
+    // chunks each (no merge across warps; two stages per ring suffice)
+    const bool solo = smx && K == 1 && S <= 32 * (int64_t)solo_max;
+    const int64_t G = solo ? 32 : std::max<int64_t>(32, round_up(cdiv(S, cpt), 32));
+    if (G > maxT) continue;
+    const void* fn = smx   ? sk[dt].k[smode][K > 1]
+                     : fwd ? fk[dt].fwd[rms][K > 1]
+                           : bk[dt].bwd[rms][K > 1];
     const int64_t planes = (int64_t)vecs * S * W * 4;
     // R row groups per block (one per block in a cluster), up to 256 threads;
     // NS stages per group's ring: the most that fit, four only where two blocks
     // still fit an SM
-    int64_t rmax = K > 1 ? 1 : std::max<int64_t>(1, std::min<int64_t>(8, 256 / G));
+    int64_t rmax = K > 1 ? 1 : std::max<int64_t>(1, std::min<int64_t>(smx ? 16 : 8, blockT / G));
     // RR_LNX_SHAPE="R:NS" forces the groups per block and the stages (tuning aid)
     int fR = 0, fNS = 0;
     if (const char* f = std::getenv("RR_LNX_SHAPE")) std::sscanf(f, "%d:%d", &fR, &fNS);
-    if (fR > 0 && K == 1 && fR * G <= rr::kLnxMaxT) rmax = fR;
+    if (fR > 0 && K == 1 && fR * G <= maxT) rmax = fR;
     for (int64_t R = rmax; R >= 1; --R) {
-      for (int NS = 4; NS >= 2; --NS) {
+      const bool two = solo && fNS == 0;  // one warp per row: two stages
+      for (int NS = two ? 2 : 4; NS >= (two ? 2 : minNS); --NS) {
         if (fNS >= 2 && NS != fNS) continue;
         if (fR > 0 && R != rmax) continue;
+        // softmax family: partial slots [2][K][warps] and barriers full /
+        // empty [NS] + merge [2] per group; norms: reduction slots and one
+        // barrier per stage
         const int64_t red_off = round_up(planes, 16);
-        const int64_t bar_off = red_off + 1024 * R;
-        const int64_t ring_off = round_up(bar_off + 8 * NS * R, 128);
+        const int64_t bar_off = red_off + 1024 * R * (smx ? K : 1);
+        const int64_t ring_off = round_up(bar_off + 8 * (smx ? 2 * NS + 2 : NS) * R, 128);
         const int64_t cl_off = ring_off + R * NS * NT * S * 16;
         const int64_t smem = cl_off + 32;
         if (smem > di->smem_optin) continue;
-        if (NS > 2 && fNS == 0 && 2 * smem > di->smem_optin) continue;
+        if (!smx && NS > 2 && fNS == 0 && 2 * smem > di->smem_optin) continue;
         const int T = (int)(R * G);
         if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
         int owners = 0;
@@ -618,7 +649,7 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
         if (bpc < 1) bpc = 1;
         const int64_t per_class = cdiv(cdiv(rows, P), R);  // blocks with a row for every group
         if (bpc > per_class) bpc = per_class;
-        if (!fwd) {
+        if (!fwd && !smx) {
           if (max_partials < P) return fail(RR_ERR_INVALID_ARG, "too few column partials allowed");
           if (bpc > max_partials / P) bpc = max_partials / P;
         }
@@ -871,8 +902,13 @@ static rr_status softmax_fwd_impl(const void* x, void* y, int64_t rows, int64_t 
   }
   if (ft == 0) return no_span(cols);
   Plan pl;
-  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl, INT64_MAX, ft)) != RR_OK)
-    return st;
+  // x and y at the same address modulo 16: phase-aligned kernels for long rows
+  st = RR_ERR_INVALID_ARG;
+  if (same && (ft < 0 || ft == 1 || ft == 3))
+    st = lnx_plan(kSoftmax, dtype, rows, cols, &pl, INT64_MAX, ft, log ? 1 : 0);
+  if (st == RR_ERR_INVALID_ARG)
+    st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl, INT64_MAX, ft);
+  if (st != RR_OK) return st;
   if ((st = launch(pl, p, stream)) != RR_OK) return st;
   return ok();
 }
@@ -970,8 +1006,12 @@ rr_status rr_softmax_xent_fwd_bwd(const void* logits, const int32_t* labels, flo
   }
   if (ft == 0) return no_span(cols);
   Plan pl;
-  if ((st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl, INT64_MAX, ft)) != RR_OK)
-    return st;
+  st = RR_ERR_INVALID_ARG;
+  if (same && (ft < 0 || ft == 1 || ft == 3))
+    st = lnx_plan(kSoftmax, dtype, rows, cols, &pl, INT64_MAX, ft, 2);
+  if (st == RR_ERR_INVALID_ARG)
+    st = plan_any(kSoftmax, dtype, same, head_free, rows, cols, &pl, INT64_MAX, ft);
+  if (st != RR_OK) return st;
   if ((st = launch(pl, p, stream)) != RR_OK) return st;
   return ok();
 }

@@ -334,6 +334,37 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// Arrival on an mbarrier of a CTA of this cluster (address from mapa), with
+// release at cluster scope: this thread's earlier writes (to that CTA's shared
+// memory, say) are visible to a thread that then sees the phase complete with
+// a cluster-scope acquire.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32x4(uint32_t cl_addr, float a, float b, float c,
+                                                 float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cl_addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+// try_wait with acquire at cluster scope (arrivals from other CTAs of the
+// cluster), allowing a suspension of up to suspend_ns.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                      uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -353,6 +384,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it != 0xffffffffu; ++it) {
     if (mbar_try_wait_sleep(bar, parity, kMbarSuspendNs)) return true;
+    if (global_timer_ns() - t0 > limit_ns) break;
+  }
+  atomicCAS(err, 0, 6);
+  return false;
+}
+
+// The same bounded wait for a phase completed by arrivals from other CTAs of
+// the cluster (cluster-scope acquire).
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t* bar, uint32_t parity, int* err,
+                                                          uint64_t limit_ns = 1000000000ull) {
+  if (mbar_try_wait_cluster(bar, parity, 0)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0; it != 0xffffffffu; ++it) {
+    if (mbar_try_wait_cluster(bar, parity, kMbarSuspendNs)) return true;
     if (global_timer_ns() - t0 > limit_ns) break;
   }
   atomicCAS(err, 0, 6);

@@ -52,6 +52,17 @@ LnxKernels lnx_fwd_kernels_bf16();
 LnxKernels lnx_bwd_kernels_f32();
 LnxKernels lnx_bwd_kernels_bf16();
 
+// Phase-aligned softmax-family kernels for long rows (rr_smx.cuh): [mode]
+// [cluster], mode 0 softmax, 1 log-softmax, 2 cross-entropy; nq chunks per
+// thread.
+struct SmxKernels {
+  const void* k[3][2];
+  int nq;  // target chunks per thread
+};
+constexpr int kSmxMaxT = 512;  // threads per block
+SmxKernels smx_kernels_f32();
+SmxKernels smx_kernels_bf16();
+
 // Short-row span kernels (rr_span.cuh): [dtype][mode], mode 0 softmax,
 // 1 log-softmax, 2 cross-entropy, 3 softmax backward, 4 log-softmax backward,
 // 5 LayerNorm forward, 6 RMSNorm forward, 7 LayerNorm backward, 8 RMSNorm

@@ -294,13 +294,15 @@ __device__ __forceinline__ void lnx_drain(uint64_t* bars, int NS, int64_t nit, i
   }
 }
 
-// Set-up shared by both kernels: the group's ring; its leader initialises the
-// ring's barriers and starts the first rows' copies (issue(i) copies the
-// group's row i into stage i % NS).  The other threads touch the barriers only
-// after the block's next __syncthreads.
+// Set-up shared by the long-row kernels: the group's ring; its leader
+// initialises the ring's barriers and starts the copies of the group's first
+// nfirst rows (default NS - 1; issue(i) copies the group's row i into stage
+// i % NS).  The other threads touch the barriers only after the block's next
+// __syncthreads.
 template <int NT, int W, class Issue>
 __device__ __forceinline__ void lnx_start(const LnxGeo& g, unsigned char* smem, const LnxGroup& gr,
-                                          const LnxRows<W>& rw, LnxRing<NT>& ring, Issue issue) {
+                                          const LnxRows<W>& rw, LnxRing<NT>& ring, Issue issue,
+                                          int nfirst = -1) {
   ring.ring = reinterpret_cast<uint4*>(smem + g.ring_off) + (size_t)gr.grp * g.NS * NT * g.S;
   ring.bars = reinterpret_cast<uint64_t*>(smem + g.bar_off) + (size_t)gr.grp * g.NS;
   ring.S = g.S;
@@ -309,7 +311,8 @@ __device__ __forceinline__ void lnx_start(const LnxGeo& g, unsigned char* smem, 
   if (gr.gt == 0) {
     for (int s = 0; s < g.NS; ++s) mbar_init(&ring.bars[s], 1);
     fence_mbar_init();
-    for (int s = 0; s < g.NS - 1; ++s)
+    const int n0 = nfirst < 0 ? g.NS - 1 : nfirst;
+    for (int s = 0; s < n0; ++s)
       if (rw.first + s * rw.step < g.rows) issue(s);
   }
 }
