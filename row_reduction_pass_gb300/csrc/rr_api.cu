@@ -567,10 +567,14 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
   // to one with two (more rows in flight), and the norm kernels take any.
   const int maxT = smx ? rr::kSmxMaxT : rr::kLnxMaxT;
   int cpt = NQ, forceK = 0, blockT = smx ? 512 : 256, solo_max = 40;
+  bool force_cpt = false;
   // RR_SMX_CPT (chunks per thread), RR_SMX_BT (threads per block, groups of
   // one-block rows), RR_SMX_SOLO (most chunks per lane of a row held by one
   // warp, 0: never) and RR_LNX_K (cluster size) force a shape (tuning aids)
-  if (const char* f = std::getenv("RR_SMX_CPT"); smx && f) cpt = std::max(1, std::atoi(f));
+  if (const char* f = std::getenv("RR_SMX_CPT"); smx && f) {
+    cpt = std::max(1, std::atoi(f));
+    force_cpt = true;
+  }
   if (const char* f = std::getenv("RR_SMX_BT"); smx && f) blockT = std::max(32, std::atoi(f));
   if (const char* f = std::getenv("RR_SMX_SOLO")) solo_max = std::max(0, std::atoi(f));
   if (const char* f = std::getenv("RR_LNX_K")) forceK = std::atoi(f);
@@ -579,10 +583,18 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
     const int64_t S = cdiv(nch_max, K);
     if (K > 1 && (K - 1) * S >= nch_min) break;  // every rank of every phase gets chunks
     if (forceK > 0 && K != forceK) continue;
+    // Softmax family split over a cluster: only for a few rows per SM.  With
+    // many rows the row engine's 1024-thread groups (the row and the next one
+    // in registers) stream better: bf16 16384 x 50304 cross-entropy 554 us
+    // there against 1050 us here; 256 rows of 65537 columns 33.9 against
+    // 25.8 us.
+    if (smx && K > 1 && rows >= 4 * (int64_t)di->sms && forceK == 0 && force != 3) break;
     // softmax family: one warp per row where its lanes hold at most solo_max
     // chunks each (no merge across warps; two stages per ring suffice)
     const bool solo = smx && K == 1 && S <= 32 * (int64_t)solo_max;
-    const int64_t G = solo ? 32 : std::max<int64_t>(32, round_up(cdiv(S, cpt), 32));
+    // a cluster rank holds one group: as many threads as the block takes
+    const int64_t kcpt = smx && K > 1 && !force_cpt ? std::max<int64_t>(1, cdiv(S, maxT)) : cpt;
+    const int64_t G = solo ? 32 : std::max<int64_t>(32, round_up(cdiv(S, kcpt), 32));
     if (G > maxT) continue;
     const void* fn = smx   ? sk[dt].k[smode][K > 1]
                      : fwd ? fk[dt].fwd[rms][K > 1]

@@ -5,10 +5,12 @@
 // the 128-bit accesses).
 //
 // Each row group brings its row (a cluster rank: its slice) into shared memory
-// by one 1-D bulk copy per row through a ring of stages, so every element is
-// read from global memory once.  The row stays in its stage while the group
-// works on it and is read twice from there, so a thread holds no row in
-// registers (many warps per SM hide the latencies); three reads in all:
+// through a ring of stages, several rows ahead: every thread copies its own
+// 16-byte chunks (gt, gt + G, ...) with asynchronous copies and is their only
+// reader, so no barrier guards the data.  Every element is read from global
+// memory once.  The row stays in its stage while the group works on it, so a
+// thread holds no row in registers (many warps per SM hide the latencies);
+// the chunks are read three times from there:
 //   1. every thread takes the maximum m of its chunks, then d = sum of
 //      2^(x log2 e - fl(m log2 e)) times 2^-r (r the rounding residual of
 //      fl(m log2 e)), so d is the sum of exp(x - m); the (m, d) pairs (and,
@@ -34,9 +36,8 @@
 // and arrives on the row's merge barrier, then takes row j - 1's statistics
 // (published one row earlier, so normally complete) and writes row j - 1's
 // outputs.  So the merge latency and the warps' skew hide behind a row of
-// work.  A stage is refilled (by the group's leader, NS rows ahead of its
-// last use) once every warp has arrived on its empty barrier after writing
-// that row's outputs.
+// work.  A thread refills a stage with the row NS ahead once it has written
+// that stage's row's outputs.
 #pragma once
 
 #include <type_traits>
@@ -172,40 +173,44 @@ __global__ void __launch_bounds__(kSmxMaxT, 1) smx_kernel(const SoftmaxParams p,
   auto row_of = [&](int64_t j) { return rw.first + j * rw.step; };
   const int NS = g.NS;
   const int lane = threadIdx.x & 31, wg = gr.gt >> 5;
-  // the group's barriers: full[NS] (a row landed), empty[NS] (every warp is
-  // done with a stage), merge[2] (every warp of every rank published its
-  // partial of a row, by row parity)
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.bar_off) + (size_t)gr.grp * (2 * NS + 2);
-  uint64_t* empty = full + NS;
-  uint64_t* mrg = full + 2 * NS;
+  // the group's merge barriers, by row parity: every warp of every rank
+  // published its partial of the row
+  uint64_t* mrg = reinterpret_cast<uint64_t*>(smem + g.bar_off) + (size_t)gr.grp * 2;
   // partial slots [row parity][rank][warp], 16 bytes each
   float4* slots = reinterpret_cast<float4*>(smem + g.red_off + (size_t)gr.grp * 1024 * K);
   const int nslot = K * gr.nw;
   // a one-warp group of a one-block row finishes each row in its own
   // iteration (no merge across warps): a stage is free one row earlier
   const bool solo = !CL && gr.nw == 1;
-  const int ahead = solo ? NS - 1 : NS - 2;
-  LnxRing<1> ring;
-  ring.ring = reinterpret_cast<uint4*>(smem + g.ring_off) + (size_t)gr.grp * NS * g.S;
-  ring.bars = full;
-  ring.S = g.S;
-  ring.NS = NS;
-  ring.policy = policy_evict_first();
-  auto issue = [&](int64_t j) {
-    const char* src[1] = {rw.slice(p.x, row_of(j), E)};
-    ring.issue(static_cast<int>(j % NS), src, rw.n);
-  };
-  int64_t issued = 0;  // the group's rows whose copy was issued (its leader's count)
-  bool dead = false;   // a wait gave up: later waits are skipped (the kernel still ends)
-  if (gr.gt == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], gr.nw);
+  const int ahead = solo ? NS - 1 : NS - 2;  // rows in flight beyond the current one
+  uint4* ring = reinterpret_cast<uint4*>(smem + g.ring_off) + (size_t)gr.grp * NS * g.S;
+  auto stage = [&](int64_t j) { return ring + (size_t)(j % NS) * g.S; };
+  // each thread copies its own chunks of row j into the row's stage (it is
+  // their only reader), one commit group per call (empty past the last row),
+  // so "row j landed" is a wait for all but the `ahead` newer groups
+  auto fetch = [&](int64_t j) {
+    if (row_of(j) < g.rows) {
+      const char* src = rw.slice(p.x, row_of(j), E);
+      uint4* dst = stage(j);
+      for (int q = 0; q < rw.nq; ++q) {
+        const int k = gr.gt + q * gr.G;
+        cp_async16(dst + k, src + (int64_t)k * 16);
+      }
     }
+    cp_async_commit();
+  };
+  auto landed = [&]() {
+    if (ahead <= 1) cp_async_wait<1>();
+    else if (ahead == 2) cp_async_wait<2>();
+    else cp_async_wait<3>();
+  };
+  bool dead = false;  // a wait gave up: later waits are skipped (the kernel still ends)
+  if (gr.gt == 0) {
     mbar_init(&mrg[0], nslot);
     mbar_init(&mrg[1], nslot);
     fence_mbar_init();
   }
+  for (int64_t i = 0; i < ahead; ++i) fetch(i);
   if constexpr (CL) cluster_sync();  // peers arrive on this block's barriers
   else __syncthreads();
   const int col0 = rw.k0 * W - rw.phi;  // column of lane 0 of local chunk 0
@@ -274,8 +279,7 @@ __global__ void __launch_bounds__(kSmxMaxT, 1) smx_kernel(const SoftmaxParams p,
   // step 2 for row j (statistics t): outputs, loss, and the stage released
   auto finish = [&](int64_t j, int32_t label, const MaxSumLab& t) {
     const int64_t r = row_of(j);
-    const int s = static_cast<int>(j % NS);
-    const uint4* st = ring.stage(s, 0);
+    const uint4* st = stage(j);
     char* ys = const_cast<char*>(rw.slice(p.y, r, E));
     const bool ignored = MODE == 2 && label == p.ignore;
     const bool in_range = MODE == 2 && label >= 0 && (int64_t)label < g.cols;
@@ -328,8 +332,6 @@ __global__ void __launch_bounds__(kSmxMaxT, 1) smx_kernel(const SoftmaxParams p,
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
   };
 
   int32_t lab_prev = 0, lab_cur = 0, lab_next = 0;  // labels of rows j - 1, j, j + 1
@@ -344,22 +346,14 @@ __global__ void __launch_bounds__(kSmxMaxT, 1) smx_kernel(const SoftmaxParams p,
       lab_cur = lab_next;
       if (row_of(j + 1) < g.rows) lab_next = __ldg(p.labels + row_of(j + 1));
     }
-    // the leader refills the stages that rows j - 2 and earlier (one warp
-    // per row: j - 1 and earlier) released
-    if (gr.gt == 0) {
-      for (; issued <= j + ahead && row_of(issued) < g.rows; ++issued) {
-        const int64_t old = issued - NS;  // the stage's previous row (none for the first NS)
-        if (old >= 0 && !dead)
-          dead = !mbar_wait_bounded(&empty[old % NS], static_cast<uint32_t>((old / NS) & 1), p.err);
-        issue(issued);
-      }
-    }
-    const int s = static_cast<int>(j % NS);
-    if (!dead) dead = !mbar_wait_bounded(&full[s], static_cast<uint32_t>((j / NS) & 1), p.err);
+    // row j + ahead into the stage that row j + ahead - NS left (finished by
+    // this thread in an earlier iteration), then row j's chunks
+    fetch(j + ahead);
+    landed();
     // step 1: this thread's online (m, d) (and the label's logit)
     MaxSumLab t = MaxSumLab::identity();
     if (!(MODE == 2 && lab_cur == p.ignore)) {
-      uint4* st = ring.stage(s, 0);
+      uint4* st = stage(j);
       smx_mask_stage<DT, W>(st, rw, gr.gt, gr.G);
       const MaxSum th = smx_thread_stats<DT>(st, gr.gt, gr.G, rw.nq);
       t.m = th.m;
@@ -384,7 +378,7 @@ __global__ void __launch_bounds__(kSmxMaxT, 1) smx_kernel(const SoftmaxParams p,
     lab_prev = lab_cur;
   }
   if (!solo && j >= 1) finish(j - 1, lab_prev, merged(j - 1));
-  if (dead && gr.gt == 0) lnx_drain(full, NS, issued, p.err);
+  cp_async_wait<0>();
   if constexpr (CL) cluster_sync();  // no peer still writes this block's slots
 }
 
