@@ -530,11 +530,12 @@ constexpr int64_t kLnxMinBytes = 8192;
 // op == kSoftmax takes the softmax-family kernels of rr_smx.cuh instead (smode
 // 0 softmax, 1 log-softmax, 2 cross-entropy): no gamma / beta, clusters for
 // rows beyond one block; RR_SMX=0 turns those off (tuning aid).
-rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
-                   int64_t max_partials, int force, int smode = -1) {
+rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
+                        int64_t max_partials, int force, int smode, bool lnp) {
   const bool smx = op == kSoftmax;
   if (const char* f = std::getenv(smx ? "RR_SMX" : "RR_LNX"); f != nullptr && f[0] == '0')
     return fail(RR_ERR_INVALID_ARG, "phase-aligned kernels off");
+  const bool pipe = smx || lnp;  // rows held in shared memory, merges pipelined
   const int E = dt == RR_BF16 ? 2 : 4, W = 16 / E;
   if (cols * E < kLnxMinBytes || rows < 1) return fail(RR_ERR_INVALID_ARG, "short rows");
   const bool fwd = op == kLnFwd || op == kRmsFwd;
@@ -546,7 +547,12 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
   static const rr::LnxKernels fk[2] = {rr::lnx_fwd_kernels_f32(), rr::lnx_fwd_kernels_bf16()};
   static const rr::LnxKernels bk[2] = {rr::lnx_bwd_kernels_f32(), rr::lnx_bwd_kernels_bf16()};
   static const rr::SmxKernels sk[2] = {rr::smx_kernels_f32(), rr::smx_kernels_bf16()};
-  const int NQ = smx ? sk[dt].nq : fwd ? fk[dt].nq_fwd : bk[dt].nq_bwd;
+  static const rr::LnpKernels pf[2] = {rr::lnp_fwd_kernels_f32(), rr::lnp_fwd_kernels_bf16()};
+  static const rr::LnpKernels pb[2] = {rr::lnp_bwd_kernels_f32(), rr::lnp_bwd_kernels_bf16()};
+  // chunks per thread: a target for the softmax family and the pipelined
+  // forward; at most nq_bwd in the pipelined backward (register partials)
+  const int NQ = smx ? sk[dt].nq : (lnp && fwd) ? sk[dt].nq : lnp ? pb[dt].nq_bwd
+                 : fwd ? fk[dt].nq_fwd : bk[dt].nq_bwd;
   const int NT = fwd || smx ? 1 : 2;
   const int vecs = smx ? 0 : fwd ? (rms ? 1 : 2) : 1;  // gamma (, beta) planes
   const int64_t rb = (cols * E) % 16;
@@ -560,25 +566,28 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
   // The LayerNorm forward split over a cluster measured slower than the
   // clusters of row groups (bf16 65537 columns: 65.9 against 49.4 us), so it
   // takes this path only when tier 3 is forced.
-  const int kmax = force == 1 ? 1 : (op == kLnFwd && force != 3) ? 1 : 8;
+  const int kmax = force == 1 ? 1 : (op == kLnFwd && !lnp && force != 3) ? 1 : 8;
   // Softmax family: the row stays in shared memory, so a thread holds no row
   // in registers; NQ is the target of chunks per thread and a block takes up
   // to 1024 threads.  A split that keeps three stages per ring is preferred
   // to one with two (more rows in flight), and the norm kernels take any.
-  const int maxT = smx ? rr::kSmxMaxT : rr::kLnxMaxT;
-  int cpt = NQ, forceK = 0, blockT = smx ? 512 : 256, solo_max = 40;
-  bool force_cpt = false;
+  const int maxT = pipe ? rr::kSmxMaxT : rr::kLnxMaxT;
+  // the pipelined backward keeps at most NQ chunks a thread (no one-warp rows
+  // beyond that)
+  const bool cap = lnp && !fwd;
+  int cpt = NQ, forceK = 0, blockT = pipe ? 512 : 256, solo_max = cap ? NQ : 40;
+  bool force_cpt = cap;
   // RR_SMX_CPT (chunks per thread), RR_SMX_BT (threads per block, groups of
   // one-block rows), RR_SMX_SOLO (most chunks per lane of a row held by one
   // warp, 0: never) and RR_LNX_K (cluster size) force a shape (tuning aids)
-  if (const char* f = std::getenv("RR_SMX_CPT"); smx && f) {
+  if (const char* f = std::getenv("RR_SMX_CPT"); pipe && !cap && f) {
     cpt = std::max(1, std::atoi(f));
     force_cpt = true;
   }
-  if (const char* f = std::getenv("RR_SMX_BT"); smx && f) blockT = std::max(32, std::atoi(f));
-  if (const char* f = std::getenv("RR_SMX_SOLO")) solo_max = std::max(0, std::atoi(f));
+  if (const char* f = std::getenv("RR_SMX_BT"); pipe && f) blockT = std::max(32, std::atoi(f));
+  if (const char* f = std::getenv("RR_SMX_SOLO"); f && !cap) solo_max = std::max(0, std::atoi(f));
   if (const char* f = std::getenv("RR_LNX_K")) forceK = std::atoi(f);
-  for (int minNS = smx ? 3 : 2; minNS >= 2; --minNS)
+  for (int minNS = pipe ? 3 : 2; minNS >= 2; --minNS)
   for (int K = force == 3 ? 2 : 1; K <= kmax; ++K) {
     const int64_t S = cdiv(nch_max, K);
     if (K > 1 && (K - 1) * S >= nch_min) break;  // every rank of every phase gets chunks
@@ -591,19 +600,20 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
     if (smx && K > 1 && rows >= 4 * (int64_t)di->sms && forceK == 0 && force != 3) break;
     // softmax family: one warp per row where its lanes hold at most solo_max
     // chunks each (no merge across warps; two stages per ring suffice)
-    const bool solo = smx && K == 1 && S <= 32 * (int64_t)solo_max;
+    const bool solo = pipe && K == 1 && S <= 32 * (int64_t)solo_max;
     // a cluster rank holds one group: as many threads as the block takes
-    const int64_t kcpt = smx && K > 1 && !force_cpt ? std::max<int64_t>(1, cdiv(S, maxT)) : cpt;
+    const int64_t kcpt = pipe && K > 1 && !force_cpt ? std::max<int64_t>(1, cdiv(S, maxT)) : cpt;
     const int64_t G = solo ? 32 : std::max<int64_t>(32, round_up(cdiv(S, kcpt), 32));
     if (G > maxT) continue;
     const void* fn = smx   ? sk[dt].k[smode][K > 1]
+                     : lnp ? (fwd ? pf[dt].fwd[rms][K > 1] : pb[dt].bwd[rms][K > 1])
                      : fwd ? fk[dt].fwd[rms][K > 1]
                            : bk[dt].bwd[rms][K > 1];
     const int64_t planes = (int64_t)vecs * S * W * 4;
     // R row groups per block (one per block in a cluster), up to 256 threads;
     // NS stages per group's ring: the most that fit, four only where two blocks
     // still fit an SM
-    int64_t rmax = K > 1 ? 1 : std::max<int64_t>(1, std::min<int64_t>(smx ? 16 : 8, blockT / G));
+    int64_t rmax = K > 1 ? 1 : std::max<int64_t>(1, std::min<int64_t>(pipe ? 16 : 8, blockT / G));
     // RR_LNX_SHAPE="R:NS" forces the groups per block and the stages (tuning aid)
     int fR = 0, fNS = 0;
     if (const char* f = std::getenv("RR_LNX_SHAPE")) std::sscanf(f, "%d:%d", &fR, &fNS);
@@ -613,16 +623,16 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
       for (int NS = two ? 2 : 4; NS >= (two ? 2 : minNS); --NS) {
         if (fNS >= 2 && NS != fNS) continue;
         if (fR > 0 && R != rmax) continue;
-        // softmax family: partial slots [2][K][warps] and barriers full /
-        // empty [NS] + merge [2] per group; norms: reduction slots and one
-        // barrier per stage
+        // pipelined kernels: partial slots [2][K][warps] and two merge
+        // barriers per group; the others: reduction slots and one barrier
+        // per stage
         const int64_t red_off = round_up(planes, 16);
-        const int64_t bar_off = red_off + 1024 * R * (smx ? K : 1);
-        const int64_t ring_off = round_up(bar_off + 8 * (smx ? 2 * NS + 2 : NS) * R, 128);
+        const int64_t bar_off = red_off + 1024 * R * (pipe ? K : 1);
+        const int64_t ring_off = round_up(bar_off + 8 * (pipe ? 2 : NS) * R, 128);
         const int64_t cl_off = ring_off + R * NS * NT * S * 16;
         const int64_t smem = cl_off + 32;
         if (smem > di->smem_optin) continue;
-        if (!smx && NS > 2 && fNS == 0 && 2 * smem > di->smem_optin) continue;
+        if (!pipe && NS > 2 && fNS == 0 && 2 * smem > di->smem_optin) continue;
         const int T = (int)(R * G);
         if ((st = set_smem(di, fn, (size_t)smem)) != RR_OK) return st;
         int owners = 0;
@@ -684,6 +694,33 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
     }
   }
   return fail(RR_ERR_INVALID_ARG, "row does not fit the phase-aligned kernels");
+}
+
+// LayerNorm / RMSNorm forward: the pipelined kernels of rr_lnp.cuh where a
+// warp holds a row and at least eight such warps share a block (rows of up to
+// ~8 KB), else the row-in-registers kernels of rr_lnx.cuh.  Measured on 2^24
+// elements (cold L2): bf16 4097 columns LayerNorm 33.1 -> 26.2 us, RMSNorm
+// 20.4 -> 18.4 us; where fewer warps fit (fp32 4097: six) or rows need several
+// warps, the pipelined kernels lost (fp32 4097 LayerNorm 47.5 against 37.3
+// us, bf16 65537 91.3 against 49.9 us), and so did the pipelined backward
+// (bf16 4097 67.6 against 55.7 us), which is not routed.  RR_LNP=0 turns the
+// pipelined kernels off, RR_LNP=1 takes them wherever they fit (tuning aids).
+rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
+                   int64_t max_partials, int force, int smode = -1) {
+  if (op == kSoftmax) return lnx_plan_impl(op, dt, rows, cols, pl, max_partials, force, smode, false);
+  const char* f = std::getenv("RR_LNP");
+  const int mode = f == nullptr ? -1 : f[0] == '0' ? 0 : 1;
+  const bool fwd = op == kLnFwd || op == kRmsFwd;
+  if (mode == 1 || (mode < 0 && fwd)) {
+    Plan tp;
+    const rr_status st = lnx_plan_impl(op, dt, rows, cols, &tp, max_partials, force, smode, true);
+    if (st == RR_OK && (mode == 1 || (tp.G == 32 && tp.T / tp.G >= 8))) {
+      *pl = tp;
+      return RR_OK;
+    }
+    if (st != RR_OK && st != RR_ERR_INVALID_ARG) return st;
+  }
+  return lnx_plan_impl(op, dt, rows, cols, pl, max_partials, force, smode, false);
 }
 
 // Plans in chunk mode when allowed, falling back to element mode (which holds

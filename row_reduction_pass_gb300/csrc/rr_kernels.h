@@ -60,6 +60,18 @@ struct SmxKernels {
   int nq;  // target chunks per thread
 };
 constexpr int kSmxMaxT = 512;  // threads per block
+
+// Pipelined LayerNorm / RMSNorm kernels for long rows (rr_lnp.cuh): [rms]
+// [cluster]; nq_bwd chunks per thread at most in the backward.
+struct LnpKernels {
+  const void* fwd[2][2];
+  const void* bwd[2][2];
+  int nq_bwd;
+};
+LnpKernels lnp_fwd_kernels_f32();
+LnpKernels lnp_fwd_kernels_bf16();
+LnpKernels lnp_bwd_kernels_f32();
+LnpKernels lnp_bwd_kernels_bf16();
 SmxKernels smx_kernels_f32();
 SmxKernels smx_kernels_bf16();
 

@@ -200,7 +200,8 @@ __global__ void __launch_bounds__(kSmxMaxT, 1) smx_kernel(const SoftmaxParams p,
     cp_async_commit();
   };
   auto landed = [&]() {
-    if (ahead <= 1) cp_async_wait<1>();
+    if (ahead <= 0) cp_async_wait<0>();
+    else if (ahead == 1) cp_async_wait<1>();
     else if (ahead == 2) cp_async_wait<2>();
     else cp_async_wait<3>();
   };

@@ -8,7 +8,9 @@ and with the cross-entropy's edge cases: labels in a row's first and last
 column (its shared head / tail chunk), ignored rows, labels outside the row,
 fully masked rows and outliers.  Each case also runs with these kernels turned
 off (RR_SMX=0 / RR_LNX=0), so the kernels they replace keep their coverage on
-the same shapes."""
+the same shapes, and the norms with each of their two long-row designs forced
+(RR_LNP=1: rows in shared memory with pipelined merges; RR_LNP=0: rows in
+registers)."""
 import contextlib
 import os
 
@@ -130,24 +132,33 @@ LN_SHAPES = [("bf16", 4097, 40), ("bf16", 4102, 11), ("f32", 2050, 13), ("f32", 
              ("bf16", 65537, 4), ("f32", 40001, 3)]
 
 
-@pytest.mark.parametrize("on", [True, False], ids=["phase", "off"])
+# routed (default), the pipelined kernels wherever they fit (RR_LNP=1), the
+# row-in-registers ones (RR_LNP=0) and neither (RR_LNX=0)
+NORM_KERNELS = {"routed": {}, "pipelined": {"RR_LNP": "1"}, "registers": {"RR_LNP": "0"},
+                "off": {"RR_LNX": "0"}}
+
+
+@pytest.mark.parametrize("kern", list(NORM_KERNELS))
 @pytest.mark.parametrize("dtype,cols,rows", LN_SHAPES)
-def test_norms_long_rows(dtype, cols, rows, on):
+def test_norms_long_rows(dtype, cols, rows, kern):
     x, g, b, dy = synth.ln_inputs(rows, cols, dtype, 7500 + cols, row_offset=10.0, gamma_std=0.1,
                                   beta_std=0.1, outlier_frac=0.002, masked_row_every=7)
-    with env(RR_LNX="1" if on else "0"):
+    with env(**NORM_KERNELS[kern]):
         check_ln(x, g, b, dy, 1e-5, dtype)
         check_rms(x, g, dy, 1e-5, dtype)
+        check_norm_bwd(x, g, b, dy, dtype, inplace="dy")
 
 
+@pytest.mark.parametrize("kern", ["routed", "pipelined"])
 @pytest.mark.parametrize("dtype,cols,rows", [("bf16", 4097, 17), ("f32", 2049, 9)])
-def test_norms_unaligned_bases(dtype, cols, rows):
+def test_norms_unaligned_bases(dtype, cols, rows, kern):
     x, g, b, dy = synth.ln_inputs(rows, cols, dtype, 7600 + cols, row_offset=3.0, gamma_std=0.2,
                                   beta_std=0.2)
     e = 2 if dtype == "bf16" else 4
     v = 16 // e
     # x, y, dy and dx at the same address modulo 16, other places; gamma /
     # beta elsewhere
-    check_ln(x, g, b, dy, 1e-5, dtype, pad=(3, 3 + v, 2, 3 + 2 * v, 3 + v))
-    check_norm_bwd(x, g, b, dy, dtype, stat_pad=1)
-    check_rms(x, g, dy, 1e-5, dtype, pad=(5, 5 + v, 1, 5, 5 + 2 * v))
+    with env(**NORM_KERNELS[kern]):
+        check_ln(x, g, b, dy, 1e-5, dtype, pad=(3, 3 + v, 2, 3 + 2 * v, 3 + v))
+        check_norm_bwd(x, g, b, dy, dtype, stat_pad=1)
+        check_rms(x, g, dy, 1e-5, dtype, pad=(5, 5 + v, 1, 5, 5 + 2 * v))
