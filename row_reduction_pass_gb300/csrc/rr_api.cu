@@ -1350,7 +1350,8 @@ static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* 
   int64_t pl_n = planes;
   void* args[] = {&ws, &P, &cols, &pl_n, &dg, &db};
   cudaError_t e =
-      cudaLaunchKernel(cr, dim3((unsigned)cdiv(planes * cols, 32)), dim3(1024), args, 0, stream);
+      cudaLaunchKernel(cr, dim3((unsigned)cdiv(planes * cols, 32 * (32 / rr::col_reduce_split(P)))),
+                       dim3(1024), args, 0, stream);
   if (e != cudaSuccess) return fail(RR_ERR_CUDA, "column reduce launch: %s", cudaGetErrorString(e));
   return ok();
 }

@@ -123,6 +123,15 @@ AttnKernel attn_fwd_kernel_for(int d);
 // dimension d on stream (persistent: at most `sms` CTAs): null on success,
 // else a short reason (nothing launched, or the launch failed).
 const char* attn_fwd_launch(const AttnParams& p, int d, int sms, cudaStream_t stream);
+// The column reduce's split of its 32 warps over the P partial rows: the
+// smallest power of two >= P / 16, at most 32 (the rest of the warps take
+// further columns), so each warp sums about 16 partials.  A block covers
+// 32 * (32 / split) columns.
+inline __host__ __device__ int col_reduce_split(int64_t P) {
+  int s = 1;
+  while (s < 32 && (int64_t)s * 16 < P) s <<= 1;
+  return s;
+}
 const void* col_reduce_kernel_ptr_f32();
 const void* col_reduce_kernel_ptr_bf16();
 

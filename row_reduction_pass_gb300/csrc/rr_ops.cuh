@@ -920,8 +920,11 @@ struct OpLnBwd {
 
 // Second stage of the LayerNorm / RMSNorm backward: dgamma_j (and dbeta_j) =
 // sum over the P partial rows ([P][planes][cols], planes = 2 for LayerNorm, 1
-// for RMSNorm), in a fixed order (warp w takes partials w, w+32, ...; the 32
-// warp sums are then added in warp order), so the result is deterministic.
+// for RMSNorm), in a fixed order, so the result is deterministic: the block's
+// 32 warps are split into `split` slices over the partials
+// (col_reduce_split(P)); warp (slice s, column warp c) sums partials s,
+// s + split, ... of its 32 columns, and the slices' sums are added in slice
+// order.
 template <int DT>
 __global__ void __launch_bounds__(1024) col_reduce_kernel(const float* __restrict__ ws, int64_t P,
                                                           int64_t cols, int64_t planes,
@@ -929,29 +932,32 @@ __global__ void __launch_bounds__(1024) col_reduce_kernel(const float* __restric
   constexpr int E = DType<DT>::E;
   __shared__ float part[32][33];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int64_t k = (int64_t)blockIdx.x * 32 + lane;
+  const int split = col_reduce_split(P);
+  const int ncw = 32 / split;             // column warps per block
+  const int cw = w % ncw, sl = w / ncw;   // this warp's columns and slice
+  const int64_t k = ((int64_t)blockIdx.x * ncw + cw) * 32 + lane;
   const int64_t n2 = planes * cols;
   float s = 0.f;
   if (k < n2) {
-    int64_t pp = w;
-    for (; pp + 96 < P; pp += 128) {
+    int64_t pp = sl;
+    const int64_t st = split;
+    for (; pp + 3 * st < P; pp += 4 * st) {
       const float a0 = __ldcs(ws + pp * n2 + k);
-      const float a1 = __ldcs(ws + (pp + 32) * n2 + k);
-      const float a2 = __ldcs(ws + (pp + 64) * n2 + k);
-      const float a3 = __ldcs(ws + (pp + 96) * n2 + k);
+      const float a1 = __ldcs(ws + (pp + st) * n2 + k);
+      const float a2 = __ldcs(ws + (pp + 2 * st) * n2 + k);
+      const float a3 = __ldcs(ws + (pp + 3 * st) * n2 + k);
       s += a0;
       s += a1;
       s += a2;
       s += a3;
     }
-    for (; pp < P; pp += 32) s += __ldcs(ws + pp * n2 + k);
+    for (; pp < P; pp += st) s += __ldcs(ws + pp * n2 + k);
   }
   part[w][lane] = s;
   __syncthreads();
-  if (w == 0 && k < n2) {
-    float t = part[0][lane];
-#pragma unroll
-    for (int i = 1; i < 32; ++i) t += part[i][lane];
+  if (sl == 0 && k < n2) {
+    float t = part[cw][lane];
+    for (int i = 1; i < split; ++i) t += part[i * ncw + cw][lane];
     char* dst = (k < cols) ? dgamma + k * E : dbeta + (k - cols) * E;
     st_elem<DT>(dst, t);
   }
