@@ -4,8 +4,9 @@
 // as defined by Vaswani et al. 2017, tiled as in Dao et al. 2022), with both
 // products on the 5th-generation tensor cores.
 //
-// One CTA of four warps owns 128 query rows of one head; thread t owns query
-// row t, which is TMEM lane t of every accumulator.  Per key tile of 128 keys:
+// A softmax warpgroup of four warps owns 128 query rows of one head at a time;
+// thread t owns query row t, which is TMEM lane t of every accumulator.  Per
+// key tile (128 keys for d = 64, 64 for d = 128):
 //   1. S = Q K^T: tcgen05.mma (bf16 in, fp32 accumulate) of the Q tile and the
 //      K tile, both read from shared memory (128-byte swizzled, K-major, loaded
 //      by TMA), into 128 TMEM columns; issued by one thread, completion
@@ -19,7 +20,8 @@
 //      shared memory (MN-major: the head dimension is contiguous).
 // K / V tiles are double-buffered: the tile after next is loaded once the
 // product that last read its stage has completed.  At the end O / l is stored
-// in bf16 and lse = (m + log2 l) ln 2 in fp32.
+// in bf16 and lse = (m + log2 l) ln 2 in fp32.  Each CTA (one per SM) runs two
+// such pipelines, each with its own issuer warp (below).
 //
 // Loads are 3-D TMA boxes of [64 head-dim columns x 128 rows x 1 head] with
 // 128-byte swizzle; rows past seq are filled with zeros, so seq needs only be a
