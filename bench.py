@@ -377,6 +377,7 @@ def run_ours(args, rank, world):
     value = job_value(world, total_bytes, ms_step)
     x_ms = statistics.mean(per["xent"])
     x_gbs = nbytes["xent"] / (x_ms * 1e-3) / 1e9
+    traffic = recorded_traffic("xent_bf16_16384x50304")
     kernels = {}
     for k in per:
         t = statistics.median(per[k])
@@ -414,7 +415,13 @@ def run_ours(args, rank, world):
         "kernels": kernels,
         "roofline": {"bound": "hbm", "achieved": round(x_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(x_gbs / peak, 4),
-                     "traffic": recorded_traffic("xent_bf16_16384x50304"),
+                     "traffic": traffic,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one "
+                                       "full launch (all 16384 rows, not scaled), "
+                                       "profiles/traffic.txt; null once the kernel's sources "
+                                       "change",
+                     "traffic_over_algorithmic": (round(traffic / nbytes["xent"], 4)
+                                                  if traffic else None),
                      "kernel": "row_kernel<OpSoftmaxXent bf16 chunks, staged> (xent 16384x50304)",
                      "peak_source": peak_src},
         "clocks": clk.summary(),
