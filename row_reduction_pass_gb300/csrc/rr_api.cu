@@ -587,6 +587,9 @@ rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan
   if (const char* f = std::getenv("RR_SMX_BT"); pipe && f) blockT = std::max(32, std::atoi(f));
   if (const char* f = std::getenv("RR_SMX_SOLO"); f && !cap) solo_max = std::max(0, std::atoi(f));
   if (const char* f = std::getenv("RR_LNX_K")) forceK = std::atoi(f);
+  // RR_LNX_2B=0 keeps the backward on the 128-register variant (tuning aid)
+  bool two_blocks = true;
+  if (const char* f = std::getenv("RR_LNX_2B"); f != nullptr && f[0] == '0') two_blocks = false;
   for (int minNS = pipe ? 3 : 2; minNS >= 2; --minNS)
   for (int K = force == 3 ? 2 : 1; K <= kmax; ++K) {
     const int64_t S = cdiv(nch_max, K);
@@ -605,10 +608,10 @@ rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan
     const int64_t kcpt = pipe && K > 1 && !force_cpt ? std::max<int64_t>(1, cdiv(S, maxT)) : cpt;
     const int64_t G = solo ? 32 : std::max<int64_t>(32, round_up(cdiv(S, kcpt), 32));
     if (G > maxT) continue;
-    const void* fn = smx   ? sk[dt].k[smode][K > 1]
-                     : lnp ? (fwd ? pf[dt].fwd[rms][K > 1] : pb[dt].bwd[rms][K > 1])
-                     : fwd ? fk[dt].fwd[rms][K > 1]
-                           : bk[dt].bwd[rms][K > 1];
+    const void* fn1 = smx   ? sk[dt].k[smode][K > 1]
+                      : lnp ? (fwd ? pf[dt].fwd[rms][K > 1] : pb[dt].bwd[rms][K > 1])
+                      : fwd ? fk[dt].fwd[rms][K > 1]
+                            : bk[dt].bwd[rms][K > 1];
     const int64_t planes = (int64_t)vecs * S * W * 4;
     // R row groups per block (one per block in a cluster), up to 256 threads;
     // NS stages per group's ring: the most that fit, four only where two blocks
@@ -619,6 +622,12 @@ rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan
     if (const char* f = std::getenv("RR_LNX_SHAPE")) std::sscanf(f, "%d:%d", &fR, &fNS);
     if (fR > 0 && K == 1 && fR * G <= maxT) rmax = fR;
     for (int64_t R = rmax; R >= 1; --R) {
+      // the row-in-registers RMSNorm backward, bf16: a variant capped at 96
+      // registers (two blocks of up to 320 threads per SM) where the block is
+      // that small (4097 columns: 47.2 -> 39.9 us).  The LayerNorm and fp32
+      // variants spill at that cap and lost (bf16 LayerNorm 54.5 -> 90.5 us).
+      const bool cap96 = !pipe && !fwd && rms && dt == RR_BF16 && K == 1 && R * G <= 320;
+      const void* fn = (cap96 && two_blocks) ? bk[dt].bwd2[rms] : fn1;
       const bool two = solo && fNS == 0;  // one warp per row: two stages
       for (int NS = two ? 2 : 4; NS >= (two ? 2 : minNS); --NS) {
         if (fNS >= 2 && NS != fNS) continue;

@@ -45,6 +45,7 @@ struct LnKernelSet {
 struct LnxKernels {
   const void* fwd[2][2];
   const void* bwd[2][2];
+  const void* bwd2[2];  // backward, one block, at most 320 threads, two blocks per SM
   int nq_fwd, nq_bwd;
 };
 LnxKernels lnx_fwd_kernels_f32();

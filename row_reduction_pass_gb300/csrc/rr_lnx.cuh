@@ -503,8 +503,10 @@ __global__ void __launch_bounds__(kLnxMaxT, 1) lnx_fwd_kernel(const LnFwdParams 
 }
 
 // ----------------------------------------------------------- backward ------
-template <int DT, int NQ, bool RMS, bool CL>
-__global__ void __launch_bounds__(kLnxMaxT, 1) lnx_bwd_kernel(const LnBwdParams p, const LnxGeo g) {
+// MINB = 2: blocks of at most 320 threads, two per SM (96 registers a thread).
+template <int DT, int NQ, bool RMS, bool CL, int MINB = 1>
+__global__ void __launch_bounds__(MINB == 2 ? 320 : kLnxMaxT, MINB)
+    lnx_bwd_kernel(const LnBwdParams p, const LnxGeo g) {
   constexpr int E = DType<DT>::E, W = DType<DT>::V;
   constexpr int kPlanes = RMS ? 1 : 2;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -688,6 +690,8 @@ LnxKernels make_lnx_bwd_set() {
   s.bwd[0][1] = (const void*)lnx_bwd_kernel<DT, NQ, false, true>;
   s.bwd[1][0] = (const void*)lnx_bwd_kernel<DT, NQ, true, false>;
   s.bwd[1][1] = (const void*)lnx_bwd_kernel<DT, NQ, true, true>;
+  s.bwd2[0] = nullptr;  // measured slower (spills at 96 registers)
+  s.bwd2[1] = (const void*)lnx_bwd_kernel<DT, NQ, true, false, 2>;
   s.nq_bwd = NQ;
   return s;
 }
