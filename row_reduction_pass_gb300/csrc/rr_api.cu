@@ -533,9 +533,10 @@ constexpr int64_t kLnxMinBytes = 8192;
 rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
                         int64_t max_partials, int force, int smode, bool lnp) {
   const bool smx = op == kSoftmax;
-  if (const char* f = std::getenv(smx ? "RR_SMX" : "RR_LNX"); f != nullptr && f[0] == '0')
+  const bool smb = op == kSoftmaxBwd;  // softmax / log-softmax backward (smode: log)
+  if (const char* f = std::getenv(smx || smb ? "RR_SMX" : "RR_LNX"); f != nullptr && f[0] == '0')
     return fail(RR_ERR_INVALID_ARG, "phase-aligned kernels off");
-  const bool pipe = smx || lnp;  // rows held in shared memory, merges pipelined
+  const bool pipe = smx || smb || lnp;  // rows held in shared memory, merges pipelined
   const int E = dt == RR_BF16 ? 2 : 4, W = 16 / E;
   if (cols * E < kLnxMinBytes || rows < 1) return fail(RR_ERR_INVALID_ARG, "short rows");
   const bool fwd = op == kLnFwd || op == kRmsFwd;
@@ -551,10 +552,11 @@ rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan
   static const rr::LnpKernels pb[2] = {rr::lnp_bwd_kernels_f32(), rr::lnp_bwd_kernels_bf16()};
   // chunks per thread: a target for the softmax family and the pipelined
   // forward; at most nq_bwd in the pipelined backward (register partials)
-  const int NQ = smx ? sk[dt].nq : (lnp && fwd) ? sk[dt].nq : lnp ? pb[dt].nq_bwd
+  static const rr::SmbKernels bb[2] = {rr::smb_kernels_f32(), rr::smb_kernels_bf16()};
+  const int NQ = smx || smb ? sk[dt].nq : (lnp && fwd) ? sk[dt].nq : lnp ? pb[dt].nq_bwd
                  : fwd ? fk[dt].nq_fwd : bk[dt].nq_bwd;
   const int NT = fwd || smx ? 1 : 2;
-  const int vecs = smx ? 0 : fwd ? (rms ? 1 : 2) : 1;  // gamma (, beta) planes
+  const int vecs = smx || smb ? 0 : fwd ? (rms ? 1 : 2) : 1;  // gamma (, beta) planes
   const int64_t rb = (cols * E) % 16;
   int64_t P = 1;
   if (rb != 0) {
@@ -600,7 +602,7 @@ rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan
     // in registers) stream better: bf16 16384 x 50304 cross-entropy 554 us
     // there against 1050 us here; 256 rows of 65537 columns 33.9 against
     // 25.8 us.
-    if (smx && K > 1 && rows >= 4 * (int64_t)di->sms && forceK == 0 && force != 3) break;
+    if ((smx || smb) && K > 1 && rows >= 4 * (int64_t)di->sms && forceK == 0 && force != 3) break;
     // softmax family: one warp per row where its lanes hold at most solo_max
     // chunks each (no merge across warps; two stages per ring suffice)
     const bool solo = pipe && K == 1 && S <= 32 * (int64_t)solo_max;
@@ -609,6 +611,7 @@ rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan
     const int64_t G = solo ? 32 : std::max<int64_t>(32, round_up(cdiv(S, kcpt), 32));
     if (G > maxT) continue;
     const void* fn1 = smx   ? sk[dt].k[smode][K > 1]
+                      : smb ? bb[dt].k[smode][K > 1]
                       : lnp ? (fwd ? pf[dt].fwd[rms][K > 1] : pb[dt].bwd[rms][K > 1])
                       : fwd ? fk[dt].fwd[rms][K > 1]
                             : bk[dt].bwd[rms][K > 1];
@@ -680,7 +683,7 @@ rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan
         if (bpc < 1) bpc = 1;
         const int64_t per_class = cdiv(cdiv(rows, P), R);  // blocks with a row for every group
         if (bpc > per_class) bpc = per_class;
-        if (!fwd && !smx) {
+        if (!fwd && !smx && !smb) {
           if (max_partials < P) return fail(RR_ERR_INVALID_ARG, "too few column partials allowed");
           if (bpc > max_partials / P) bpc = max_partials / P;
         }
@@ -717,6 +720,17 @@ rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan
 rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
                    int64_t max_partials, int force, int smode = -1) {
   if (op == kSoftmax) return lnx_plan_impl(op, dt, rows, cols, pl, max_partials, force, smode, false);
+  if (op == kSoftmaxBwd) {
+    // Softmax / log-softmax backward: bf16 rows only, where measured faster
+    // (4097 columns 39.5 -> 26.4 us, 65537 48.4 -> 45.3 us); fp32 rows, whose
+    // two tensors leave room for few rows per SM, lost (4097: 37.8 against
+    // 43.2 us, 65537: 73.0 against 141.6 us).  RR_SMB=1 takes them for fp32
+    // too (tests, tuning).
+    const char* f = std::getenv("RR_SMB");
+    if (dt != RR_BF16 && !(f != nullptr && f[0] == '1'))
+      return fail(RR_ERR_INVALID_ARG, "row engine for this dtype");
+    return lnx_plan_impl(op, dt, rows, cols, pl, max_partials, force, smode, false);
+  }
   const char* f = std::getenv("RR_LNP");
   const int mode = f == nullptr ? -1 : f[0] == '0' ? 0 : 1;
   const bool fwd = op == kLnFwd || op == kRmsFwd;
@@ -1013,8 +1027,14 @@ static rr_status softmax_bwd_impl(const void* y, const void* dy, void* dx, int64
   }
   if (ft == 0) return no_span(cols);
   Plan pl;
-  if ((st = plan_any(kSoftmaxBwd, dtype, same, head_free, rows, cols, &pl, INT64_MAX, ft)) != RR_OK)
-    return st;
+  // the three tensors at the same address modulo 16: phase-class kernels for
+  // long rows
+  st = RR_ERR_INVALID_ARG;
+  if (same && (ft < 0 || ft == 1 || ft == 3))
+    st = lnx_plan(kSoftmaxBwd, dtype, rows, cols, &pl, INT64_MAX, ft, log ? 1 : 0);
+  if (st == RR_ERR_INVALID_ARG)
+    st = plan_any(kSoftmaxBwd, dtype, same, head_free, rows, cols, &pl, INT64_MAX, ft);
+  if (st != RR_OK) return st;
   if ((st = launch(pl, p, stream)) != RR_OK) return st;
   return ok();
 }

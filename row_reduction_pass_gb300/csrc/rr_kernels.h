@@ -62,6 +62,13 @@ struct SmxKernels {
 };
 constexpr int kSmxMaxT = 512;  // threads per block
 
+// Softmax / log-softmax backward for long rows (rr_smb.cuh): [log][cluster].
+struct SmbKernels {
+  const void* k[2][2];
+};
+SmbKernels smb_kernels_f32();
+SmbKernels smb_kernels_bf16();
+
 // Pipelined LayerNorm / RMSNorm kernels for long rows (rr_lnp.cuh): [rms]
 // [cluster]; nq_bwd chunks per thread at most in the backward.
 struct LnpKernels {

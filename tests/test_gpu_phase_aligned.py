@@ -1,6 +1,7 @@
 """GPU parity of the phase-aligned long-row kernels (rows of at least 8 KB whose
 input and output tensors share their address modulo 16) against the float64
-oracle: softmax, log-softmax and softmax cross-entropy, and LayerNorm /
+oracle: softmax, log-softmax, softmax cross-entropy and the softmax /
+log-softmax backward, and LayerNorm /
 RMSNorm, on every phase-class count a row length can give (P = 1, 2, 4, 8
 classes of rows by start offset), on tensors whose base is not 16-byte aligned
 (every row shifted), in place, one block per row and rows split over a cluster,
@@ -20,7 +21,8 @@ import pytest
 import oracle
 from row_reduction_pass_gb300 import synth
 
-from parity import check_ln, check_log_softmax, check_norm_bwd, check_rms, check_softmax, check_xent
+from parity import (check_ln, check_log_softmax, check_norm_bwd, check_rms, check_softmax,
+                    check_softmax_bwd, check_xent, store)
 
 pytestmark = pytest.mark.gpu
 
@@ -60,6 +62,14 @@ def test_shapes_cover_every_phase_count():
     assert {("f32", p) for p in (1, 2, 4)} <= got
 
 
+def bwd_case(x, dtype, seed):
+    """The backward's inputs: the oracle's softmax and log-softmax of x (as
+    stored) and an upstream gradient dy ~ N(0, 1)."""
+    rng = np.random.default_rng(seed)
+    dy = store(rng.standard_normal(x.shape), dtype)
+    return store(oracle.softmax(x), dtype), store(oracle.log_softmax(x), dtype), dy
+
+
 def xent_case(rows, cols, dtype, seed):
     x, lab = synth.xent_inputs(rows, cols, dtype, 4.0, seed, ignore_frac=0.1, outlier_frac=0.002,
                                masked_row_every=5)
@@ -78,33 +88,45 @@ def xent_case(rows, cols, dtype, seed):
 @pytest.mark.parametrize("dtype,cols,rows", SMX_SHAPES)
 def test_softmax_family_long_rows(dtype, cols, rows, on):
     x, lab = xent_case(rows, cols, dtype, 7000 + cols)
-    with env(RR_SMX="1" if on else "0"):
+    y, z, dy = bwd_case(x, dtype, cols)
+    # RR_SMB=1: the backward's phase-class kernel for fp32 rows too
+    with env(RR_SMX="1" if on else "0", RR_SMB="1"):
         check_softmax(x, dtype)
         check_log_softmax(x, dtype)
         check_xent(x, lab, dtype)
+        check_softmax_bwd(y, dy, dtype)
+        check_softmax_bwd(z, dy, dtype, log=True)
 
 
 @pytest.mark.parametrize("pad", [1, 3, 8])
 @pytest.mark.parametrize("dtype,cols,rows", [("bf16", 4097, 24), ("f32", 2049, 20),
                                              ("bf16", 65537, 3)])
-def test_softmax_family_unaligned_bases(dtype, cols, rows, pad):
+def test_softmax_family_unaligned_bases(dtype, cols, rows, pad, monkeypatch):
     """Input and output shifted by the same element count: every row's phase
     moves, and the first row's copy reads bytes before the tensor."""
+    monkeypatch.setenv("RR_SMB", "1")
     x, lab = xent_case(rows, cols, dtype, 7100 + cols + pad)
     e = 2 if dtype == "bf16" else 4
     po = pad + 16 // e  # the same address modulo 16, another place
     check_softmax(x, dtype, pad_in=pad, pad_out=po)
     check_log_softmax(x, dtype, pad_in=pad, pad_out=po)
     check_xent(x, lab, dtype, pad_in=pad, pad_out=po)
+    y, z, dy = bwd_case(x, dtype, pad)
+    check_softmax_bwd(y, dy, dtype, pads=(pad, po, pad + 2 * (po - pad)))
+    check_softmax_bwd(z, dy, dtype, log=True, pads=(po, pad, pad))
 
 
 @pytest.mark.parametrize("dtype,cols,rows", [("bf16", 4097, 30), ("f32", 2050, 12),
                                              ("bf16", 40001, 4)])
-def test_softmax_family_in_place(dtype, cols, rows):
+def test_softmax_family_in_place(dtype, cols, rows, monkeypatch):
+    monkeypatch.setenv("RR_SMB", "1")
     x, lab = xent_case(rows, cols, dtype, 7200 + cols)
     check_softmax(x, dtype, pad_in=5, inplace=True)
     check_log_softmax(x, dtype, inplace=True)
     check_xent(x, lab, dtype, pad_in=3, inplace=True)
+    y, z, dy = bwd_case(x, dtype, 3)
+    check_softmax_bwd(y, dy, dtype, inplace="y")
+    check_softmax_bwd(z, dy, dtype, log=True, inplace="dy")
 
 
 def test_xent_every_label_position_of_a_chunk():
