@@ -466,15 +466,17 @@ __global__ void __launch_bounds__(320, 1)
             for (int i = 0; i < 32; ++i)
               if (key0 + 32 * c + i > lim) v[c][i] = __float_as_uint(-INFINITY);
         }
-        // the tile's row maximum on the raw scores (scale > 0 keeps the order)
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+        // the tile's row maximum on the raw scores (scale > 0 keeps the order);
+        // eight independent chains, so the reduction is not one long chain
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            mx0 = fmaxf(mx0, __uint_as_float(v[c][i]));
-            mx1 = fmaxf(mx1, __uint_as_float(v[c][i + 1]));
-          }
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(v[c][i]));
+        const float mx0 = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        const float mx1 = fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]));
         // The running maximum m moves only when the tile's maximum exceeds it
         // by more than 8 (log2 domain): otherwise P = 2^(s - m) stays below
         // 2^8 and O, l keep their scale, so O is rarely rescaled.  (Finite
@@ -482,18 +484,25 @@ __global__ void __launch_bounds__(320, 1)
         const float mt = fmaxf(mx0, mx1) * sc;
         const float m_new = mt > m + 8.f ? mt : m;
         const float alpha = ex2(m - m_new);  // 1 if m stays, 0 on the first tile
-        float l0 = 0.f, l1 = 0.f;
+        // P = 2^(s sc - m): packed exponent FMAs, the sum in four chains
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
         uint32_t pk[BN / 32][16];
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(v[c][i]), sc, -m_new));
-            const float p1 = ex2(fmaf(__uint_as_float(v[c][i + 1]), sc, -m_new));
+          for (int i = 0; i < 32; i += 4) {
+            float t0, t1, t2, t3;
+            fma2(t0, t1, __uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1]), sc, sc, -m_new,
+                 -m_new);
+            fma2(t2, t3, __uint_as_float(v[c][i + 2]), __uint_as_float(v[c][i + 3]), sc, sc,
+                 -m_new, -m_new);
+            const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
             add2(l0, l1, l0, l1, p0, p1);
+            add2(l2, l3, l2, l3, p2, p3);
             pk[c][i >> 1] = pack_bf16(p0, p1);
+            pk[c][(i >> 1) + 1] = pack_bf16(p2, p3);
           }
-        l = l * alpha + (l0 + l1);
+        l = l * alpha + ((l0 + l1) + (l2 + l3));
         m = m_new;
         // O += P V of tile t - 1 must be done before P and O are written
         if (t > 0) {
