@@ -50,6 +50,14 @@
  *     2 staged rows (one per CTA, bulk copies to shared memory), 3 rows split
  *     over a thread-block cluster.  A shape the forced tier cannot hold returns
  *     RR_ERR_INVALID_ARG; so does a value other than 0..3 (or T0..T3).
+ *   - Rows of at least 8 KB whose row tensors share their address modulo 16
+ *     run on kernels that group the rows by their start offset within a
+ *     16-byte block (every chunk then an aligned 16-byte block), where measured
+ *     faster.  RR_SMX=0 (softmax family) and RR_LNX=0 (LayerNorm / RMSNorm)
+ *     turn them off, RR_LNP=0/1 and RR_SMB=1 choose among their variants (tests
+ *     and tuning; read at every call).  Results agree within the tolerances of
+ *     the operation whichever kernel runs; they are not bit-identical across
+ *     kernels.
  */
 #ifndef RR_H
 #define RR_H
