@@ -538,7 +538,11 @@ rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan
     return fail(RR_ERR_INVALID_ARG, "phase-aligned kernels off");
   const bool pipe = smx || smb || lnp;  // rows held in shared memory, merges pipelined
   const int E = dt == RR_BF16 ? 2 : 4, W = 16 / E;
-  if (cols * E < kLnxMinBytes || rows < 1) return fail(RR_ERR_INVALID_ARG, "short rows");
+  // RR_LNX_MIN lowers (or raises) the row length these kernels take (bytes;
+  // tuning aid)
+  int64_t min_bytes = kLnxMinBytes;
+  if (const char* f = std::getenv("RR_LNX_MIN")) min_bytes = std::max<int64_t>(16, std::atoll(f));
+  if (cols * E < min_bytes || rows < 1) return fail(RR_ERR_INVALID_ARG, "short rows");
   const bool fwd = op == kLnFwd || op == kRmsFwd;
   const bool rms = op == kRmsFwd || op == kRmsBwd;
   std::lock_guard<std::mutex> lock(g_mu);
