@@ -512,24 +512,24 @@ rr_status ln_cluster_plan(OpKind op, rr_dtype dt, int lmode, int64_t rows, int64
   return RR_OK;
 }
 
-// Phase-aligned row kernels for long rows (rr_lnx.cuh): forward or backward of
-// LayerNorm / RMSNorm.  The row tensors must share their address modulo 16
-// (the caller checks); gamma / beta may have any alignment.  Rows of at least
-// kLnxMinBytes; one block per row (slice) of at most 512 threads holding NQ
-// chunks each, clusters of K = 2 .. 8 blocks for rows beyond one block (force:
-// -1 any, 1 one block only, 3 clusters only).  Rows of each of the P phase
-// classes go to bpc row owners; the backward writes one partial row per owner,
-// at most max_partials.  RR_LNX=0 turns these kernels off (tuning aid).
-// Rows of at least 8 KB: measured on 2^24-element rows (bf16, cold L2), they
-// beat the row-group kernels from there (4097 columns: backward 65.5 -> 55.5
-// us, RMSNorm forward 23.2 -> 19.3 us, forward 32.8 -> 31.2 us) and lose on
-// shorter rows (1000 columns: forward 16.9 against 28.6 us at best).
+// Phase-class kernels for long rows: the plan (kernel, geometry, launch shape)
+// of one call.  The row tensors must share their address modulo 16 (the caller
+// checks); gamma / beta may have any alignment.  Rows of at least kLnxMinBytes
+// (measured on 2^24-element rows, bf16, cold L2: the LayerNorm kernels beat the
+// row-group ones from there — 4097 columns: backward 65.5 -> 55.5 us, RMSNorm
+// forward 23.2 -> 19.3 us — and lose on shorter rows, 1000 columns: forward
+// 16.9 against 28.6 us at best).  Kernels by op:
+//   kLnFwd / kRmsFwd / kLnBwd / kRmsBwd: rr_lnx.cuh (rows in registers), or
+//     with lnp the pipelined rr_lnp.cuh ones;
+//   kSoftmax: rr_smx.cuh (smode 0 softmax, 1 log-softmax, 2 cross-entropy);
+//   kSoftmaxBwd: rr_smb.cuh (smode 1: log-softmax).
+// A block holds R row groups of G threads, or is one rank of a cluster of
+// K = 2 .. 8 blocks splitting rows beyond one block (force: -1 any, 1 one
+// block only, 3 clusters only).  Rows of each of the P phase classes go to
+// bpc row owners; the norm backward writes one partial row per owner, at most
+// max_partials.  RR_LNX=0 / RR_SMX=0 turn the kernels off (tuning aids).
 constexpr int64_t kLnxMinBytes = 8192;
 
-//
-// op == kSoftmax takes the softmax-family kernels of rr_smx.cuh instead (smode
-// 0 softmax, 1 log-softmax, 2 cross-entropy): no gamma / beta, clusters for
-// rows beyond one block; RR_SMX=0 turns those off (tuning aid).
 rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
                         int64_t max_partials, int force, int smode, bool lnp) {
   const bool smx = op == kSoftmax;
@@ -554,9 +554,9 @@ rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan
   static const rr::SmxKernels sk[2] = {rr::smx_kernels_f32(), rr::smx_kernels_bf16()};
   static const rr::LnpKernels pf[2] = {rr::lnp_fwd_kernels_f32(), rr::lnp_fwd_kernels_bf16()};
   static const rr::LnpKernels pb[2] = {rr::lnp_bwd_kernels_f32(), rr::lnp_bwd_kernels_bf16()};
+  static const rr::SmbKernels bb[2] = {rr::smb_kernels_f32(), rr::smb_kernels_bf16()};
   // chunks per thread: a target for the softmax family and the pipelined
   // forward; at most nq_bwd in the pipelined backward (register partials)
-  static const rr::SmbKernels bb[2] = {rr::smb_kernels_f32(), rr::smb_kernels_bf16()};
   const int NQ = smx || smb ? sk[dt].nq : (lnp && fwd) ? sk[dt].nq : lnp ? pb[dt].nq_bwd
                  : fwd ? fk[dt].nq_fwd : bk[dt].nq_bwd;
   const int NT = fwd || smx ? 1 : 2;
@@ -573,10 +573,10 @@ rr_status lnx_plan_impl(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan
   // clusters of row groups (bf16 65537 columns: 65.9 against 49.4 us), so it
   // takes this path only when tier 3 is forced.
   const int kmax = force == 1 ? 1 : (op == kLnFwd && !lnp && force != 3) ? 1 : 8;
-  // Softmax family: the row stays in shared memory, so a thread holds no row
-  // in registers; NQ is the target of chunks per thread and a block takes up
-  // to 1024 threads.  A split that keeps three stages per ring is preferred
-  // to one with two (more rows in flight), and the norm kernels take any.
+  // Pipelined kernels: the row stays in shared memory, so a thread holds no
+  // row in registers; NQ is the target of chunks per thread and a block takes
+  // up to kSmxMaxT threads.  A split that keeps three stages per ring is
+  // preferred to one with two (more rows in flight); the others take any.
   const int maxT = pipe ? rr::kSmxMaxT : rr::kLnxMaxT;
   // the pipelined backward keeps at most NQ chunks a thread (no one-warp rows
   // beyond that)
