@@ -74,6 +74,7 @@ SmbKernels smb_kernels_bf16();
 struct LnpKernels {
   const void* fwd[2][2];
   const void* bwd[2][2];
+  const void* bwd2[2];  // backward, one block, at most 320 threads, two blocks per SM
   int nq_bwd;
 };
 LnpKernels lnp_fwd_kernels_f32();

@@ -328,8 +328,10 @@ __global__ void __launch_bounds__(kSmxMaxT, 1) lnp_fwd_kernel(const LnFwdParams 
 }
 
 // ----------------------------------------------------------- backward ------
-template <int DT, int NQB, bool RMS, bool CL>
-__global__ void __launch_bounds__(kSmxMaxT, 1) lnp_bwd_kernel(const LnBwdParams p, const LnxGeo g) {
+// MINB = 2: blocks of at most 320 threads, two per SM (96 registers a thread).
+template <int DT, int NQB, bool RMS, bool CL, int MINB = 1>
+__global__ void __launch_bounds__(MINB == 2 ? 320 : kSmxMaxT, MINB)
+    lnp_bwd_kernel(const LnBwdParams p, const LnxGeo g) {
   constexpr int E = DType<DT>::E, W = DType<DT>::V;
   constexpr int kPlanes = RMS ? 1 : 2;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -512,6 +514,8 @@ LnpKernels make_lnp_bwd_set() {
   s.bwd[0][1] = (const void*)lnp_bwd_kernel<DT, NQB, false, true>;
   s.bwd[1][0] = (const void*)lnp_bwd_kernel<DT, NQB, true, false>;
   s.bwd[1][1] = (const void*)lnp_bwd_kernel<DT, NQB, true, true>;
+  s.bwd2[0] = (const void*)lnp_bwd_kernel<DT, NQB, false, false, 2>;
+  s.bwd2[1] = (const void*)lnp_bwd_kernel<DT, NQB, true, false, 2>;
   s.nq_bwd = NQB;
   return s;
 }
