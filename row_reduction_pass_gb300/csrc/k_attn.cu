@@ -25,7 +25,9 @@
 //
 // Loads are 3-D TMA boxes of [64 head-dim columns x 128 rows x 1 head] with
 // 128-byte swizzle; rows past seq are filled with zeros, so seq needs only be a
-// multiple of 64 (those keys are masked, those queries not stored).  Every
+// multiple of 64 (those keys are masked, those queries not stored).  O leaves
+// through shared memory: each warp's 32 rows x 64 columns go into a staging box
+// in the same swizzled layout and out by a TMA store of whole lines.  Every
 // mbarrier wait is bounded (RR_ERR_DEVICE_TIMEOUT in the device error word);
 // the tensor memory is allocated by warp 0 and always released.
 //
@@ -140,6 +142,26 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
       : "memory");
 }
+// 3-D TMA tile store map at {c0, c1, c2} <- [src] (this CTA's shared memory),
+// committed as one bulk group of this thread; elements outside the tensor are
+// not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(src))
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// This thread's bulk stores have read their shared memory (it may be
+// overwritten) / have completed.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 // two floats as a bf16 pair, lo in the low half (round to nearest even)
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
@@ -211,7 +233,9 @@ struct AttnPL {
   static constexpr int kKVBox = BN * 128;              // one K or V box of BN rows
   static constexpr int kKVBytes = kBoxes * kKVBox;
   static constexpr int kPipe = kQBytes + NS * 2 * kKVBytes;  // smem of one pipeline
-  static constexpr int kOffBar = 2 * kPipe;
+  static constexpr int kStageWarp = 32 * 128;          // O staging: 32 rows x 64 columns
+  static constexpr int kOffStage = 2 * kPipe;          // 4 warps' boxes per pipeline
+  static constexpr int kOffBar = kOffStage + 2 * 4 * kStageWarp;
   static constexpr int kSmem = kOffBar + 512 + 1024;
   static constexpr uint32_t kColS = 0, kColP = BN, kColO = 256 - D;
   static constexpr uint32_t kIdescS = attn_idesc(kBM, BN, false);
@@ -233,7 +257,8 @@ __device__ __forceinline__ bool attn_item(int r, int slot, int nslots, int bh, i
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const AttnParams p) {
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                    const AttnParams p) {
   static_assert(D == 64 || D == 128, "head dimension 64 or 128");
   using C = AttnPL<D>;
   constexpr int BN = C::BN;
@@ -532,33 +557,49 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_before();
         mbar_arrive(bar_p);
       }
-      // O / l in bf16 and lse, for rows inside the sequence
+      // O / l in bf16: each warp writes its 32 rows, 64 columns at a time,
+      // into its staging box (the 128-byte swizzled layout of the tensor map)
+      // and stores the box with one TMA store (whole 128-byte lines, where
+      // stores of a row per thread would each touch 32 lines)
       wait(bar_o, (uint32_t)((t - 1) & 1));
       tc_fence_after();
       const float inv = 1.f / l;
-      char* orow = p.o + ((int64_t)head * seq + row) * D * 2;
       uint32_t o[D / 32][32];
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(tO + 32 * c, o[c]);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(bar_ofree);  // O read: the next query tile may overwrite it
-      if (row < seq) {
+      {
+        const int lane = tid & 31, wq = warp & 3;
+        unsigned char* box = smem + C::kOffStage + (4 * w + wq) * C::kStageWarp;
+        const bool in_seq = q0 + 32 * wq < seq;  // seq is a multiple of 64: all or none
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c)
+        for (int b = 0; b < D / 64; ++b) {
+          if (lane == 0) bulk_wait_read();  // the box's previous store has read it
+          __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            const uint4 q4 = make_uint4(
-                pack_bf16(__uint_as_float(o[c][i]) * inv, __uint_as_float(o[c][i + 1]) * inv),
-                pack_bf16(__uint_as_float(o[c][i + 2]) * inv, __uint_as_float(o[c][i + 3]) * inv),
-                pack_bf16(__uint_as_float(o[c][i + 4]) * inv, __uint_as_float(o[c][i + 5]) * inv),
-                pack_bf16(__uint_as_float(o[c][i + 6]) * inv, __uint_as_float(o[c][i + 7]) * inv));
-            *reinterpret_cast<uint4*>(orow + (32 * c + i) * 2) = q4;
-          }
+          for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              const uint32_t* oc = o[2 * b + c2];
+              const uint4 q4 = make_uint4(
+                  pack_bf16(__uint_as_float(oc[i]) * inv, __uint_as_float(oc[i + 1]) * inv),
+                  pack_bf16(__uint_as_float(oc[i + 2]) * inv, __uint_as_float(oc[i + 3]) * inv),
+                  pack_bf16(__uint_as_float(oc[i + 4]) * inv, __uint_as_float(oc[i + 5]) * inv),
+                  pack_bf16(__uint_as_float(oc[i + 6]) * inv, __uint_as_float(oc[i + 7]) * inv));
+              const int ch = 4 * c2 + (i >> 3);  // 16-byte chunk of the 128-byte row
+              *reinterpret_cast<uint4*>(box + lane * 128 + ((ch ^ (lane & 7)) << 4)) = q4;
+            }
+          fence_proxy_async_smem();  // the writes are visible to the TMA store
+          __syncwarp();
+          if (lane == 0 && in_seq) tma_store_3d(&to, box, 64 * b, q0 + 32 * wq, head);
+        }
       }
       if (p.lse != nullptr && row < seq)
         p.lse[(int64_t)head * seq + row] = (m + __log2f(l)) * 0.6931471805599453f;
     }
+    if ((tid & 31) == 0) bulk_wait_all();  // the staging boxes are read, O written
   }
 
   tc_fence_before();
@@ -600,20 +641,20 @@ const char* attn_fwd_launch(const AttnParams& p, int d, int sms, cudaStream_t st
   // of 64 columns x rows x 1 head (Q: 128 rows, K / V: the key tile); rows
   // past seq read as zeros
   const int bn = d == 64 ? AttnPL<64>::BN : AttnPL<128>::BN;
-  CUtensorMap maps[3];
-  const char* ptrs[3] = {p.q, p.k, p.v};
+  CUtensorMap maps[4];
+  const char* ptrs[4] = {p.q, p.k, p.v, p.o};
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)p.seq, (cuuint64_t)p.bh};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)p.seq * d * 2};
   const cuuint32_t es[3] = {1, 1, 1};
-  for (int i = 0; i < 3; ++i) {
-    const cuuint32_t box[3] = {64, (cuuint32_t)(i == 0 ? kBM : bn), 1};
+  for (int i = 0; i < 4; ++i) {  // q, k, v loads; o stores of 32 rows
+    const cuuint32_t box[3] = {64, (cuuint32_t)(i == 0 ? kBM : i == 3 ? 32 : bn), 1};
     if (encode(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<char*>(ptrs[i]), dims,
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return "tensor map encoding failed";
   }
   AttnParams pc = p;
-  void* args[] = {&maps[0], &maps[1], &maps[2], &pc};
+  void* args[] = {&maps[0], &maps[1], &maps[2], &maps[3], &pc};
   // persistent: one CTA per SM (two pipelines each), fewer for small problems
   const int64_t items = p.bh * ((p.seq + kBM - 1) / kBM);
   const int64_t grid = std::min<int64_t>(sms, (items + 1) / 2);
