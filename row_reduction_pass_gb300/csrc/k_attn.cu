@@ -206,7 +206,8 @@ __device__ __forceinline__ void wait_spin(uint64_t* bar, uint32_t parity, bool& 
 // 0, 1: a softmax warpgroup (warps 4w .. 4w + 3; thread t owns query row t of
 // the tile, TMEM lane t) and an issuer warp (warp 8 + w, lane 0) that issues
 // the pipeline's TMA loads and MMAs.  Pipeline w owns TMEM columns [256 w,
-// 256 w + 256): S [0, BN), P (bf16 pairs) [BN, BN + BN / 2), O [256 - D, 256),
+// 256 w + 256): S [0, BN), NPB buffers of P (bf16 pairs, BN / 2 columns each)
+// from BN, O [256 - D, 256) (head_dim 128: two P buffers in the 256 columns),
 // and its own Q tile and two-stage rings of K and of V tiles in shared memory.
 // The two pipelines interleave on the SM: one's softmax runs while the tensor
 // cores work for the other.
@@ -217,17 +218,21 @@ __device__ __forceinline__ void wait_spin(uint64_t* bar, uint32_t parity, bool& 
 //   S(t + 1) = Q K(t + 1)^T as soon as the softmax has read S(t) (so it runs
 //     during the softmax of t) -> bar_s; K(t + 2) then loads into the stage
 //     S(t) has finished with;
-//   once P(t) is written: O += P(t) V(t) -> bar_o; V(t + 1) then loads into
+//   once P(t) is written: O += P(t) V(t) -> bar_o[t % NPB]; V(t + 1) loads into
 //     the stage O += P V of t - 1 has finished with.
 //   The next query tile's Q loads once the current one's last S is done; its
 //   first O += P V (which overwrites O) waits for the softmax to read O.
 // Softmax, per key tile: [bar_s] read S -> bar_sfree; max, P = 2^(s - m),
-// sums; [O += P V of t - 1 done] write P, O *= alpha -> bar_p; after a query
-// tile's last key tile: [bar_o] O / l, lse -> bar_ofree.
+// sums; [O += P V of t - NPB done] write P(t) into buffer t % NPB; [O += P V
+// of t - 1 done, only when O is rescaled] O *= alpha -> bar_p[t % NPB]; after
+// a query tile's last key tile: [its O += P V done] O / l, lse -> bar_ofree.
+// With two P buffers the softmax of t does not wait for O += P V of t - 1, so
+// it runs as soon as S(t) is there.
 template <int D>
 struct AttnPL {
   static constexpr int BN = D == 64 ? 128 : 64;        // keys per tile
   static constexpr int NS = 2;                         // K / V stages
+  static constexpr int NPB = D == 128 ? 2 : 1;         // P buffers in TMEM
   static constexpr int kBoxes = D / 64;
   static constexpr int kQBytes = kBoxes * kBoxBytes;   // 128 rows
   static constexpr int kKVBox = BN * 128;              // one K or V box of BN rows
@@ -255,7 +260,7 @@ __device__ __forceinline__ bool attn_item(int r, int slot, int nslots, int bh, i
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
                     const AttnParams p) {
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(320, 1)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int w = warp < 8 ? warp >> 2 : warp - 8;  // this thread's pipeline
+  const int w = warp < 8 ? warp >> 2 : (warp - 8) & 1;  // this thread's pipeline
   unsigned char* pipe = smem + w * C::kPipe;
   unsigned char* sq = pipe;
   auto stage_k = [&](int s) { return pipe + C::kQBytes + (2 * s) * C::kKVBytes; };
@@ -275,13 +280,13 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* bar_q = bars + 0;
   uint64_t* bar_s = bars + 1;
   uint64_t* bar_sfree = bars + 2;   // 128 arrivals
-  uint64_t* bar_p = bars + 3;       // 128 arrivals
-  uint64_t* bar_o = bars + 4;
-  uint64_t* bar_ofree = bars + 5;   // 128 arrivals
-  uint64_t* bar_kfull = bars + 6;   // [2] K tile landed
-  uint64_t* bar_vfull = bars + 8;   // [2] V tile landed
-  uint64_t* bar_kempty = bars + 10; // [2] S done with the K stage
-  uint64_t* bar_vempty = bars + 12; // [2] O += P V done with the V stage
+  uint64_t* bar_ofree = bars + 3;   // 128 arrivals
+  uint64_t* bar_p = bars + 4;       // [NPB] P written, 128 arrivals
+  uint64_t* bar_o = bars + 6;       // [NPB] O += P V done with the P buffer
+  uint64_t* bar_kfull = bars + 8;   // [2] K tile landed
+  uint64_t* bar_vfull = bars + 10;  // [2] V tile landed
+  uint64_t* bar_kempty = bars + 12; // [2] S done with the K stage
+  uint64_t* bar_vempty = bars + 14; // [2] O += P V done with the V stage
   uint32_t* tslot = reinterpret_cast<uint32_t*>(reinterpret_cast<uint64_t*>(smem + C::kOffBar) + 40);
 
   const int seq = static_cast<int>(p.seq);
@@ -300,14 +305,14 @@ __global__ void __launch_bounds__(320, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (warp >= 8 && (tid & 31) == 0) {
+  if ((warp == 8 || warp == 9) && (tid & 31) == 0) {
     mbar_init(bar_q, 1);
     mbar_init(bar_s, 1);
     mbar_init(bar_sfree, 128);
-    mbar_init(bar_p, 128);
-    mbar_init(bar_o, 1);
     mbar_init(bar_ofree, 128);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_p[i], 128);
+      mbar_init(&bar_o[i], 1);
       mbar_init(&bar_kfull[i], 1);
       mbar_init(&bar_vfull[i], 1);
       mbar_init(&bar_kempty[i], 1);
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(320, 1)
   };
 
   if (warp >= 8) {
-    // ------------------------------------------------------- the issuer
+    // ------------------------------------------------------ the issuers
     if ((tid & 31) == 0) {
       // the pipeline's key tiles in order: (query tile r, tile j of it, head)
       struct Cur {
@@ -389,10 +394,10 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tm + C::kColO, tm + C::kColP + 8 * kk,
+          mma_ts(tm + C::kColO, tm + C::kColP + (t % C::NPB) * (BN / 2) + 8 * kk,
                  sw128_desc(v_addr + kk * 2048, C::kKVBox, 1024), C::kIdescO,
                  (!first_of_tile || kk > 0) ? 1u : 0u);
-        mma_commit(bar_o);
+        mma_commit(&bar_o[t % C::NPB]);
         mma_commit(&bar_vempty[t & 1]);
       };
       int qr = 0;  // the last query tile whose Q has been loaded
@@ -407,55 +412,64 @@ __global__ void __launch_bounds__(320, 1)
         load_q(q2);
         qr = q2.r;
       };
-      Cur cur = first();  // key tile t
-      if (cur.ok) {
-        load_q(cur);
-        load_k();
-        load_v();
-        if (kc.ok) {
+      if (warp >= 10) {
+        // warp 10 + w: V loads and O += P V.  O += P(t) V(t) as soon as the
+        // softmax has written P(t) (the first of a query tile, which
+        // overwrites O, once the softmax has read O); V(t + 1) loads into
+        // the stage O += P V of t - 1 used once that is done
+        Cur c = first();
+        if (c.ok) {
+          load_v();
+          if (vc.ok) load_v();
+        }
+        for (int t = 0; c.ok; ++t) {
+          if (vc.ok && vt == t + 1 && t >= 1) {
+            wait_spin(&bar_vempty[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), dead, p.err);
+            load_v();
+          }
+          if (c.j == 0 && c.r > 0) wait_spin(bar_ofree, (uint32_t)((c.r - 1) & 1), dead, p.err);
+          wait_spin(&bar_p[t % C::NPB], (uint32_t)((t / C::NPB) & 1), dead, p.err);
+          wait_spin(&bar_vfull[t & 1], (uint32_t)((t >> 1) & 1), dead, p.err);
+          issue_pv(t, c.j == 0);
+          advance(c);
+        }
+      } else {
+        // warp 8 + w: Q / K loads and S = Q K^T
+        Cur cur = first();  // key tile t
+        if (cur.ok) {
+          load_q(cur);
           load_k();
-          load_v();
+          if (kc.ok) load_k();
+          wait_spin(bar_q, 0, dead, p.err);
+          wait_spin(&bar_kfull[0], 0, dead, p.err);
+          issue_s(0);
+          after_s(cur, 0);
         }
-        wait_spin(bar_q, 0, dead, p.err);
-        wait_spin(&bar_kfull[0], 0, dead, p.err);
-        issue_s(0);
-        after_s(cur, 0);
-      }
-      for (int t = 0; cur.ok; ++t) {
-        Cur nxt = cur;
-        advance(nxt);
-        // V(t + 1) into the stage O += P V of t - 1 used, as soon as that is
-        // done (it is needed only after the softmax of t + 1)
-        if (vc.ok && vt == t + 1 && t >= 1) {
-          wait_spin(&bar_vempty[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), dead, p.err);
-          load_v();
-        }
-        if (nxt.ok) {
-          // S(t + 1) once the softmax has read S(t); a new query tile's Q was
-          // loaded after the current one's last S
-          wait_spin(bar_sfree, (uint32_t)(t & 1), dead, p.err);
-          if (nxt.r != cur.r) {
-            if (qr < nxt.r) {  // not reached: after_s loaded it
-              load_q(nxt);
-              qr = nxt.r;
+        for (int t = 0; cur.ok; ++t) {
+          Cur nxt = cur;
+          advance(nxt);
+          if (nxt.ok) {
+            // S(t + 1) once the softmax has read S(t); a new query tile's Q
+            // was loaded after the current one's last S
+            wait_spin(bar_sfree, (uint32_t)(t & 1), dead, p.err);
+            if (nxt.r != cur.r) {
+              if (qr < nxt.r) {  // not reached: after_s loaded it
+                load_q(nxt);
+                qr = nxt.r;
+              }
+              wait_spin(bar_q, (uint32_t)(nxt.r & 1), dead, p.err);
             }
-            wait_spin(bar_q, (uint32_t)(nxt.r & 1), dead, p.err);
+            wait_spin(&bar_kfull[(t + 1) & 1], (uint32_t)(((t + 1) >> 1) & 1), dead, p.err);
+            issue_s(t + 1);
+            after_s(nxt, t + 1);
+            // K(t + 2) into the stage S(t) used
+            if (kc.ok && kt == t + 2) {
+              wait_spin(&bar_kempty[t & 1], (uint32_t)((t >> 1) & 1), dead, p.err);
+              load_k();
+            }
           }
-          wait_spin(&bar_kfull[(t + 1) & 1], (uint32_t)(((t + 1) >> 1) & 1), dead, p.err);
-          issue_s(t + 1);
-          after_s(nxt, t + 1);
-          // K(t + 2) into the stage S(t) used
-          if (kc.ok && kt == t + 2) {
-            wait_spin(&bar_kempty[t & 1], (uint32_t)((t >> 1) & 1), dead, p.err);
-            load_k();
-          }
+          cur = nxt;
         }
-        // O += P(t) V(t); the first of a query tile overwrites O
-        if (cur.j == 0 && cur.r > 0) wait_spin(bar_ofree, (uint32_t)((cur.r - 1) & 1), dead, p.err);
-        wait_spin(bar_p, (uint32_t)(t & 1), dead, p.err);
-        wait_spin(&bar_vfull[t & 1], (uint32_t)((t >> 1) & 1), dead, p.err);
-        issue_pv(t, cur.j == 0);
-        cur = nxt;
       }
     }
   } else {
@@ -463,7 +477,6 @@ __global__ void __launch_bounds__(320, 1)
     const int t_row = tid & 127;  // row in the tile, TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tm + lane_base + C::kColS;
-    const uint32_t tP = tm + lane_base + C::kColP;
     const uint32_t tO = tm + lane_base + C::kColO;
     const float sc = p.scale_log2;
     int t = 0;
@@ -529,14 +542,20 @@ __global__ void __launch_bounds__(320, 1)
           }
         l = l * alpha + ((l0 + l1) + (l2 + l3));
         m = m_new;
-        // O += P V of tile t - 1 must be done before P and O are written
-        if (t > 0) {
-          wait(bar_o, (uint32_t)((t - 1) & 1));
+        // P(t) goes into buffer t % NPB once O += P V of tile t - NPB is done
+        // with it; O is rescaled only after O += P V of tile t - 1
+        if (t >= C::NPB) {
+          wait(&bar_o[t % C::NPB], (uint32_t)((t / C::NPB - 1) & 1));
           tc_fence_after();
         }
+        const uint32_t tP = tm + lane_base + C::kColP + (t % C::NPB) * (BN / 2);
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) tmem_st16(tP + 16 * c, pk[c]);
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if constexpr (C::NPB > 1) {
+            wait(&bar_o[(t - 1) % C::NPB], (uint32_t)(((t - 1) / C::NPB) & 1));
+            tc_fence_after();
+          }
           uint32_t o[D / 32][32];  // every load issued before the one wait
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(tO + 32 * c, o[c]);
@@ -555,13 +574,13 @@ __global__ void __launch_bounds__(320, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar_p);
+        mbar_arrive(&bar_p[t % C::NPB]);
       }
       // O / l in bf16: each warp writes its 32 rows, 64 columns at a time,
       // into its staging box (the 128-byte swizzled layout of the tensor map)
       // and stores the box with one TMA store (whole 128-byte lines, where
       // stores of a row per thread would each touch 32 lines)
-      wait(bar_o, (uint32_t)((t - 1) & 1));
+      wait(&bar_o[(t - 1) % C::NPB], (uint32_t)(((t - 1) / C::NPB) & 1));
       tc_fence_after();
       const float inv = 1.f / l;
       uint32_t o[D / 32][32];
@@ -658,7 +677,7 @@ const char* attn_fwd_launch(const AttnParams& p, int d, int sms, cudaStream_t st
   // persistent: one CTA per SM (two pipelines each), fewer for small problems
   const int64_t items = p.bh * ((p.seq + kBM - 1) / kBM);
   const int64_t grid = std::min<int64_t>(sms, (items + 1) / 2);
-  if (cudaLaunchKernel(ak.fn, dim3((unsigned)grid), dim3(320), args, (size_t)ak.smem, stream) !=
+  if (cudaLaunchKernel(ak.fn, dim3((unsigned)grid), dim3(384), args, (size_t)ak.smem, stream) !=
       cudaSuccess)
     return "launch failed";
   return nullptr;
