@@ -21,7 +21,7 @@
 // K / V tiles are double-buffered: the tile after next is loaded once the
 // product that last read its stage has completed.  At the end O / l is stored
 // in bf16 and lse = (m + log2 l) ln 2 in fp32.  Each CTA (one per SM) runs two
-// such pipelines, each with its own issuer warp (below).
+// such pipelines, each with its own two issuer warps (below).
 //
 // Loads are 3-D TMA boxes of [64 head-dim columns x 128 rows x 1 head] with
 // 128-byte swizzle; rows past seq are filled with zeros, so seq needs only be a
@@ -190,8 +190,10 @@ __device__ __forceinline__ void wait_spin(uint64_t* bar, uint32_t parity, bool& 
 
 // Persistent CTAs (one per SM), each running two independent pipelines w =
 // 0, 1: a softmax warpgroup (warps 4w .. 4w + 3; thread t owns query row t of
-// the tile, TMEM lane t) and an issuer warp (warp 8 + w, lane 0) that issues
-// the pipeline's TMA loads and MMAs.  Pipeline w owns TMEM columns [256 w,
+// the tile, TMEM lane t) and two issuer warps (lane 0 of each): warp 8 + w
+// loads Q and K and issues S = Q K^T, warp 10 + w loads V and issues O += P V,
+// so neither product waits behind the other's loads and barrier waits.
+// Pipeline w owns TMEM columns [256 w,
 // 256 w + 256): S [0, BN), NPB buffers of P (bf16 pairs, BN / 2 columns each)
 // from BN, O [256 - D, 256) (head_dim 128: two P buffers in the 256 columns),
 // and its own Q tile and two-stage rings of K and of V tiles in shared memory.
@@ -200,7 +202,7 @@ __device__ __forceinline__ void wait_spin(uint64_t* bar, uint32_t parity, bool& 
 // A pipeline works through query tiles (head, tile) in a zigzag of the list
 // sorted heaviest first (causal: most key tiles first), so the pipelines of
 // all SMs end together.  Its key tiles are numbered t = 0, 1, ... across its
-// query tiles.  Issuer, per key tile t:
+// query tiles.  Issuers, per key tile t:
 //   S(t + 1) = Q K(t + 1)^T as soon as the softmax has read S(t) (so it runs
 //     during the softmax of t) -> bar_s; K(t + 2) then loads into the stage
 //     S(t) has finished with;
