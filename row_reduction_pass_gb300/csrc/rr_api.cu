@@ -757,6 +757,111 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
   return lnx_plan_impl(op, dt, rows, cols, pl, max_partials, force, smode, false);
 }
 
+// Column-block LayerNorm / RMSNorm kernels for very long rows (rr_lnc.cuh):
+// statistics, then outputs, in separate launches over (class, column block,
+// row group) items, so every SM streams from the first microsecond instead of
+// waiting on a row per block or cluster (bf16 255 x 65537: see the design
+// notes for the numbers).  Taken for rows of at least kLncMinBytes when no
+// tier is forced; RR_LNC=0 turns them off, RR_LNC_MIN (bytes) moves the
+// threshold (tuning aids).  Items: as many row groups per class as keep the
+// blocks within one wave (3 blocks per SM forward, 2 backward, their register
+// budgets), so each block streams as many rows as it can; each backward row
+// group adds a column-partial row for the column reduce to read.
+constexpr int64_t kLncMinBytes = 64 * 1024;
+
+struct LncPlan {
+  rr::LncGeo geo{};
+  int64_t items = 0;
+  int64_t partials = 0;   // backward: rows of column partials
+  size_t rec_bytes = 0;   // (row, block) records
+  size_t ws_bytes = 0;    // backward: partials + records
+};
+
+rr_status lnc_plan(bool bwd, bool rms, rr_dtype dt, int64_t rows, int64_t cols, LncPlan* lp,
+                   int64_t max_partials = INT64_MAX, size_t ws_limit = SIZE_MAX) {
+  if (const char* f = std::getenv("RR_LNC"); f != nullptr && f[0] == '0')
+    return fail(RR_ERR_INVALID_ARG, "column-block kernels off");
+  const int E = dt == RR_BF16 ? 2 : 4, W = 16 / E;
+  int64_t min_bytes = kLncMinBytes;
+  if (const char* f = std::getenv("RR_LNC_MIN")) min_bytes = std::max<int64_t>(16, std::atoll(f));
+  if (cols * E < min_bytes || rows < 1) return fail(RR_ERR_INVALID_ARG, "rows too short");
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevInfo* di = nullptr;
+    rr_status st = device_info(&di);
+    if (st != RR_OK) return st;
+    sms = di->sms;
+  }
+  const int64_t rb = (cols * E) % 16;
+  int64_t P = 1;
+  if (rb != 0) {
+    int64_t a = 16, b = rb;
+    while (b) { const int64_t t = a % b; a = b; b = t; }
+    P = 16 / a;
+  }
+  const int64_t cb = 32 * rr::kLncWarps * (bwd ? rr::kLncCplBwd : rr::kLncCplFwd);
+  const int64_t nb = cdiv(cdiv(cols + W - 1, W), cb);
+  const int64_t per_class = cdiv(rows, P);
+  const int64_t slots = (bwd ? 2 : 3) * (int64_t)sms;
+  int64_t ng = std::min<int64_t>(per_class, std::max<int64_t>(1, slots / (P * nb)));
+  for (;; --ng) {
+    const int64_t rg = cdiv(per_class, ng);
+    const int64_t g2 = cdiv(per_class, rg);
+    const int64_t planes = rms ? 1 : 2;
+    const size_t rec = (size_t)rows * nb * (bwd ? 8 : rms ? 4 : 16);
+    const size_t part = bwd ? (size_t)P * g2 * planes * cols * sizeof(float) : 0;
+    const size_t ws = bwd ? ((part + 15) & ~size_t(15)) + rec : 0;
+    if (ng > 1 && bwd && (P * g2 > max_partials || ws > ws_limit)) continue;
+    if (P * nb * g2 > INT32_MAX) return fail(RR_ERR_INVALID_ARG, "too many column blocks");
+    lp->geo = rr::LncGeo{rows, cols, (int32_t)P, (int32_t)nb, (int32_t)g2, (int32_t)rg,
+                         (int64_t)(((part + 15) & ~size_t(15)) / sizeof(float))};
+    lp->items = P * nb * g2;
+    lp->partials = P * g2;
+    lp->rec_bytes = rec;
+    lp->ws_bytes = ws;
+    break;
+  }
+  if (bwd && (lp->partials > max_partials || lp->ws_bytes > ws_limit))
+    return fail(RR_ERR_INVALID_ARG, "column-block partials exceed the workspace");
+  return RR_OK;
+}
+
+const rr::LncKernels& lnc_kernels(rr_dtype dt) {
+  static const rr::LncKernels k[2] = {rr::lnc_kernels_f32(), rr::lnc_kernels_bf16()};
+  return k[dt == RR_BF16 ? 1 : 0];
+}
+
+// Forward launches (records in y, then mean / rstd, then y).
+rr_status lnc_forward(bool rms, const LncPlan& lp, rr::LnFwdParams p, rr_dtype dt,
+                      cudaStream_t stream) {
+  const rr::LncKernels& k = lnc_kernels(dt);
+  rr::LncGeo g = lp.geo;
+  void* args[] = {&p, &g};
+  cudaError_t e = cudaLaunchKernel(k.stats[rms], dim3((unsigned)lp.items), dim3(32 * rr::kLncWarps),
+                                   args, 0, stream);
+  if (e == cudaSuccess)
+    e = cudaLaunchKernel(k.merge[rms], dim3((unsigned)cdiv(lp.geo.rows, 8)), dim3(256), args, 0,
+                         stream);
+  if (e == cudaSuccess)
+    e = cudaLaunchKernel(k.norm[rms], dim3((unsigned)lp.items), dim3(32 * rr::kLncWarps), args, 0,
+                         stream);
+  if (e != cudaSuccess) return fail(RR_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return RR_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb);
+
+// The forward's records live in y (rounded up to 16 bytes) until the last
+// launch overwrites it: they must fit, and y must not overlap x.
+bool lnc_fwd_fits(const LncPlan& lp, const void* x, const void* y, int64_t rows, int64_t cols,
+                  size_t E) {
+  const size_t n = (size_t)rows * cols * E;
+  if (overlaps(x, n, y, n)) return false;
+  const size_t pad = (16 - (reinterpret_cast<uintptr_t>(y) & 15)) & 15;
+  return pad + lp.rec_bytes <= n;
+}
+
 // Plans in chunk mode when allowed, falling back to element mode (which holds
 // longer rows per CTA) when the row does not fit the chunk-mode variants.
 rr_status plan_any(OpKind op, rr_dtype dt, bool chunk_ok, bool head_free, int64_t rows,
@@ -1144,7 +1249,22 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
   }
   if (ft == 0) return no_span(cols);
   // x and y at the same address modulo 16: phase-aligned kernels for long rows
+  // (column blocks for the longest, when y is a separate tensor)
   const bool same16 = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(y) & 15);
+  if (same16 && ft < 0) {
+    LncPlan lp;
+    st = lnc_plan(false, false, dtype, rows, cols, &lp);
+    if (st == RR_OK && lnc_fwd_fits(lp, x, y, rows, cols, E)) {
+      int* err = device_error_word();
+      if (!err) return RR_ERR_CUDA;
+      rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma),
+                        static_cast<const char*>(beta), static_cast<char*>(y), mean, rstd, err,
+                        cols, eps, static_cast<float>(1.0 / static_cast<double>(cols))};
+      if ((st = lnc_forward(false, lp, p, dtype, stream)) != RR_OK) return st;
+      return ok();
+    }
+    if (st != RR_OK && st != RR_ERR_INVALID_ARG) return st;
+  }
   st = RR_ERR_INVALID_ARG;
   if (same16 && (ft < 0 || ft == 1 || ft == 3))
     st = lnx_plan(kLnFwd, dtype, rows, cols, &pl, INT64_MAX, ft);
@@ -1199,6 +1319,20 @@ rr_status rr_rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
   }
   if (ft == 0) return no_span(cols);
   const bool same16 = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(y) & 15);
+  if (same16 && ft < 0) {
+    LncPlan lp;
+    st = lnc_plan(false, true, dtype, rows, cols, &lp);
+    if (st == RR_OK && lnc_fwd_fits(lp, x, y, rows, cols, E)) {
+      int* err = device_error_word();
+      if (!err) return RR_ERR_CUDA;
+      rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma), nullptr,
+                        static_cast<char*>(y), nullptr, rstd, err, cols, eps,
+                        static_cast<float>(1.0 / static_cast<double>(cols))};
+      if ((st = lnc_forward(true, lp, p, dtype, stream)) != RR_OK) return st;
+      return ok();
+    }
+    if (st != RR_OK && st != RR_ERR_INVALID_ARG) return st;
+  }
   st = RR_ERR_INVALID_ARG;
   if (same16 && (ft < 0 || ft == 1 || ft == 3))
     st = lnx_plan(kRmsFwd, dtype, rows, cols, &pl, INT64_MAX, ft);
@@ -1268,6 +1402,10 @@ static size_t norm_bwd_workspace_size(bool rms, int64_t rows, int64_t cols, rr_d
       if (norm_bwd_plan(rms, rows, cols, dtype, m, lnx == 1, &pl, &ws) == RR_OK && ws > best)
         best = ws;
     }
+  if (forced_tier() < 0) {  // the column-block kernels (partials and row records)
+    LncPlan lp;
+    if (lnc_plan(true, rms, dtype, rows, cols, &lp) == RR_OK && lp.ws_bytes > best) best = lp.ws_bytes;
+  }
   SpanPlan sp;  // short rows with 16-byte aligned tensors: one partial per span block
   if (forced_tier() <= 0 && span_plan(dtype, rms ? 8 : 7, rows, cols, false, INT64_MAX, &sp) == RR_OK) {
     const size_t ws = (size_t)sp.grid * (rms ? 1 : 2) * (size_t)cols * sizeof(float);
@@ -1374,12 +1512,33 @@ static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* 
       const uintptr_t a16 = reinterpret_cast<uintptr_t>(x) & 15;
       const bool same16 = a16 == (reinterpret_cast<uintptr_t>(dy) & 15) &&
                           a16 == (reinterpret_cast<uintptr_t>(dx) & 15);
-      if ((st = norm_bwd_plan(rms, rows, cols, dtype, lmode, same16, &pl, &need, max_partials)) !=
-          RR_OK)
-        return st;
-      if (workspace_bytes < need)
-        return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
-      if ((st = launch(pl, p, stream)) != RR_OK) return st;
+      // the longest rows: column-block kernels, where their partials and
+      // records fit the workspace
+      LncPlan lp;
+      st = RR_ERR_INVALID_ARG;
+      if (same16 && ft < 0) {
+        st = lnc_plan(true, rms, dtype, rows, cols, &lp, max_partials, workspace_bytes);
+        if (st != RR_OK && st != RR_ERR_INVALID_ARG) return st;
+      }
+      if (st == RR_OK) {
+        const rr::LncKernels& k = lnc_kernels(dtype);
+        rr::LncGeo g = lp.geo;
+        void* args[] = {&p, &g};
+        cudaError_t e = cudaLaunchKernel(k.part[rms], dim3((unsigned)lp.items),
+                                         dim3(32 * rr::kLncWarps), args, 0, stream);
+        if (e == cudaSuccess)
+          e = cudaLaunchKernel(k.dx[rms], dim3((unsigned)lp.items), dim3(32 * rr::kLncWarps),
+                               args, 0, stream);
+        if (e != cudaSuccess) return fail(RR_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+        pl.partials = lp.partials;
+      } else {
+        if ((st = norm_bwd_plan(rms, rows, cols, dtype, lmode, same16, &pl, &need, max_partials)) !=
+            RR_OK)
+          return st;
+        if (workspace_bytes < need)
+          return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+        if ((st = launch(pl, p, stream)) != RR_OK) return st;
+      }
     }
   }
   const void* cr = dtype == RR_BF16 ? rr::col_reduce_kernel_ptr_bf16() : rr::col_reduce_kernel_ptr_f32();

@@ -84,6 +84,32 @@ LnpKernels lnp_bwd_kernels_bf16();
 SmxKernels smx_kernels_f32();
 SmxKernels smx_kernels_bf16();
 
+// Column-block LayerNorm / RMSNorm kernels for very long rows (rr_lnc.cuh):
+// [rms].  Forward: stats, merge, norm launches; backward: part, dx launches
+// (then the column reduce).  A work item (one block) is (class, column block,
+// row group): item = cls + P * (b + nb * grp).
+struct LncGeo {
+  int64_t rows;
+  int64_t cols;
+  int32_t P;        // phase classes
+  int32_t nb;       // column blocks of kCB chunks
+  int32_t ng;       // row groups per class
+  int32_t rg;       // rows per group (of its class)
+  int64_t rec_off;  // backward: floats from the workspace to the (S1, S2) records
+};
+constexpr int kLncWarps = 8;    // warps per block (256 threads)
+constexpr int kLncCplFwd = 2;  // chunks per lane of a row, forward
+constexpr int kLncCplBwd = 1;  // chunks per lane of a row, backward
+struct LncKernels {
+  const void* stats[2];
+  const void* merge[2];
+  const void* norm[2];
+  const void* part[2];
+  const void* dx[2];
+};
+LncKernels lnc_kernels_f32();
+LncKernels lnc_kernels_bf16();
+
 // Short-row span kernels (rr_span.cuh): [dtype][mode], mode 0 softmax,
 // 1 log-softmax, 2 cross-entropy, 3 softmax backward, 4 log-softmax backward,
 // 5 LayerNorm forward, 6 RMSNorm forward, 7 LayerNorm backward, 8 RMSNorm

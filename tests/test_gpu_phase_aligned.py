@@ -17,12 +17,15 @@ import os
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from row_reduction_pass_gb300 import synth
 
-from parity import (check_ln, check_log_softmax, check_norm_bwd, check_rms, check_softmax,
-                    check_softmax_bwd, check_xent, store)
+import row_reduction_pass_gb300 as rr
+from parity import (TOL, TOL_F32_OUT, check_guards, check_ln, check_log_softmax, check_norm_bwd,
+                    check_rms, check_softmax, check_softmax_bwd, check_xent, compare, host,
+                    out_f32, store, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -151,13 +154,18 @@ def test_xent_custom_ignore_index_and_all_rows_ignored():
 
 # LayerNorm / RMSNorm on the same phase counts, bases and cluster splits
 LN_SHAPES = [("bf16", 4097, 40), ("bf16", 4102, 11), ("f32", 2050, 13), ("f32", 2052, 4),
-             ("bf16", 65537, 4), ("f32", 40001, 3)]
+             ("bf16", 65537, 4), ("f32", 40001, 3), ("bf16", 32771, 21), ("bf16", 32768, 6),
+             ("f32", 16387, 9)]
 
 
-# routed (default), the pipelined kernels wherever they fit (RR_LNP=1), the
-# row-in-registers ones (RR_LNP=0) and neither (RR_LNX=0)
-NORM_KERNELS = {"routed": {}, "pipelined": {"RR_LNP": "1"}, "registers": {"RR_LNP": "0"},
-                "off": {"RR_LNX": "0"}}
+# routed (default: the column-block kernels for rows of 64 KB and more), the
+# column-block kernels for every shape (RR_LNC_MIN=16), the pipelined kernels
+# wherever they fit (RR_LNP=1), the row-in-registers ones (RR_LNP=0) and
+# neither (RR_LNX=0); all but the first two with the column-block kernels off
+NORM_KERNELS = {"routed": {}, "column": {"RR_LNC_MIN": "16"},
+                "pipelined": {"RR_LNP": "1", "RR_LNC": "0"},
+                "registers": {"RR_LNP": "0", "RR_LNC": "0"},
+                "off": {"RR_LNX": "0", "RR_LNC": "0"}}
 
 
 @pytest.mark.parametrize("kern", list(NORM_KERNELS))
@@ -171,8 +179,9 @@ def test_norms_long_rows(dtype, cols, rows, kern):
         check_norm_bwd(x, g, b, dy, dtype, inplace="dy")
 
 
-@pytest.mark.parametrize("kern", ["routed", "pipelined"])
-@pytest.mark.parametrize("dtype,cols,rows", [("bf16", 4097, 17), ("f32", 2049, 9)])
+@pytest.mark.parametrize("kern", ["routed", "pipelined", "column"])
+@pytest.mark.parametrize("dtype,cols,rows", [("bf16", 4097, 17), ("f32", 2049, 9),
+                                             ("bf16", 32771, 10)])
 def test_norms_unaligned_bases(dtype, cols, rows, kern):
     x, g, b, dy = synth.ln_inputs(rows, cols, dtype, 7600 + cols, row_offset=3.0, gamma_std=0.2,
                                   beta_std=0.2)
@@ -184,3 +193,30 @@ def test_norms_unaligned_bases(dtype, cols, rows, kern):
         check_ln(x, g, b, dy, 1e-5, dtype, pad=(3, 3 + v, 2, 3 + 2 * v, 3 + v))
         check_norm_bwd(x, g, b, dy, dtype, stat_pad=1)
         check_rms(x, g, dy, 1e-5, dtype, pad=(5, 5 + v, 1, 5, 5 + 2 * v))
+
+
+@pytest.mark.parametrize("dtype,cols,rows", [("bf16", 32771, 9), ("f32", 16387, 5)])
+def test_norm_forward_in_place_long_rows(dtype, cols, rows):
+    """y == x for rows the column-block kernels take otherwise (they keep their
+    row records in y, so an in-place call goes to the phase-aligned kernels):
+    LayerNorm and RMSNorm against the oracle, guard bands intact."""
+    x, g, b, _ = synth.ln_inputs(rows, cols, dtype, 7700 + cols, row_offset=5.0, gamma_std=0.1,
+                                 beta_std=0.1, outlier_frac=0.002, masked_row_every=4)
+    rtol, atol = TOL[dtype]
+    ry, rmean, rrstd = oracle.ln_fwd(x, g, b, 1e-5)
+    xd, gd, bd = to_dev(x, 3), to_dev(g), to_dev(b)
+    mean, rstd = out_f32(rows), out_f32(rows)
+    rr.rr_layernorm_fwd(xd, gd, bd, xd, mean, rstd, eps=1e-5)
+    torch.cuda.synchronize()
+    check_guards()
+    compare("ln y in place", host(xd), ry, rtol, atol)
+    compare("ln mean", host(mean), rmean, *TOL_F32_OUT)
+    compare("ln rstd", host(rstd), rrstd, *TOL_F32_OUT)
+    ry, rrstd = oracle.rms_fwd(x, g, 1e-5)
+    xd = to_dev(x, 5)
+    rstd = out_f32(rows)
+    rr.rr_rmsnorm_fwd(xd, gd, xd, rstd, eps=1e-5)
+    torch.cuda.synchronize()
+    check_guards()
+    compare("rms y in place", host(xd), ry, rtol, atol)
+    compare("rms rstd", host(rstd), rrstd, *TOL_F32_OUT)
