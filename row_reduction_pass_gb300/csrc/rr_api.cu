@@ -764,10 +764,12 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
 // notes for the numbers).  Taken for rows of at least kLncMinBytes when no
 // tier is forced; RR_LNC=0 turns them off, RR_LNC_MIN (bytes) moves the
 // threshold (tuning aids).  Items: as many row groups per class as keep the
-// blocks within one wave (3 blocks per SM forward, 2 backward, their register
-// budgets), so each block streams as many rows as it can; each backward row
-// group adds a column-partial row for the column reduce to read.
+// blocks within one wave (5 blocks per SM: registers, 32 KB copy rings), so each
+// block streams as many rows as it can; each backward row group adds a
+// column-partial row for the column reduce to read.
 constexpr int64_t kLncMinBytes = 64 * 1024;
+
+const rr::LncKernels& lnc_kernels(rr_dtype dt);
 
 struct LncPlan {
   rr::LncGeo geo{};
@@ -792,6 +794,12 @@ rr_status lnc_plan(bool bwd, bool rms, rr_dtype dt, int64_t rows, int64_t cols, 
     rr_status st = device_info(&di);
     if (st != RR_OK) return st;
     sms = di->sms;
+    // the streaming kernels' copy rings (dynamic shared memory)
+    const rr::LncKernels& k = lnc_kernels(dt);
+    const size_t ring = (size_t)rr::lnc_ring_bytes(bwd);
+    const void* fns[2] = {bwd ? k.part[rms] : k.stats[rms], bwd ? k.dx[rms] : k.norm[rms]};
+    for (const void* fn : fns)
+      if ((st = set_smem(di, fn, ring)) != RR_OK) return st;
   }
   const int64_t rb = (cols * E) % 16;
   int64_t P = 1;
@@ -803,7 +811,7 @@ rr_status lnc_plan(bool bwd, bool rms, rr_dtype dt, int64_t rows, int64_t cols, 
   const int64_t cb = 32 * rr::kLncWarps * (bwd ? rr::kLncCplBwd : rr::kLncCplFwd);
   const int64_t nb = cdiv(cdiv(cols + W - 1, W), cb);
   const int64_t per_class = cdiv(rows, P);
-  const int64_t slots = (bwd ? 2 : 3) * (int64_t)sms;
+  const int64_t slots = 5 * (int64_t)sms;
   int64_t ng = std::min<int64_t>(per_class, std::max<int64_t>(1, slots / (P * nb)));
   for (;; --ng) {
     const int64_t rg = cdiv(per_class, ng);
@@ -838,14 +846,15 @@ rr_status lnc_forward(bool rms, const LncPlan& lp, rr::LnFwdParams p, rr_dtype d
   const rr::LncKernels& k = lnc_kernels(dt);
   rr::LncGeo g = lp.geo;
   void* args[] = {&p, &g};
+  const size_t ring = (size_t)rr::lnc_ring_bytes(false);
   cudaError_t e = cudaLaunchKernel(k.stats[rms], dim3((unsigned)lp.items), dim3(32 * rr::kLncWarps),
-                                   args, 0, stream);
+                                   args, ring, stream);
   if (e == cudaSuccess)
     e = cudaLaunchKernel(k.merge[rms], dim3((unsigned)cdiv(lp.geo.rows, 8)), dim3(256), args, 0,
                          stream);
   if (e == cudaSuccess)
-    e = cudaLaunchKernel(k.norm[rms], dim3((unsigned)lp.items), dim3(32 * rr::kLncWarps), args, 0,
-                         stream);
+    e = cudaLaunchKernel(k.norm[rms], dim3((unsigned)lp.items), dim3(32 * rr::kLncWarps), args,
+                         ring, stream);
   if (e != cudaSuccess) return fail(RR_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
   return RR_OK;
 }
@@ -1524,11 +1533,12 @@ static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* 
         const rr::LncKernels& k = lnc_kernels(dtype);
         rr::LncGeo g = lp.geo;
         void* args[] = {&p, &g};
+        const size_t ring = (size_t)rr::lnc_ring_bytes(true);
         cudaError_t e = cudaLaunchKernel(k.part[rms], dim3((unsigned)lp.items),
-                                         dim3(32 * rr::kLncWarps), args, 0, stream);
+                                         dim3(32 * rr::kLncWarps), args, ring, stream);
         if (e == cudaSuccess)
           e = cudaLaunchKernel(k.dx[rms], dim3((unsigned)lp.items), dim3(32 * rr::kLncWarps),
-                               args, 0, stream);
+                               args, ring, stream);
         if (e != cudaSuccess) return fail(RR_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
         pl.partials = lp.partials;
       } else {

@@ -97,9 +97,15 @@ struct LncGeo {
   int32_t rg;       // rows per group (of its class)
   int64_t rec_off;  // backward: floats from the workspace to the (S1, S2) records
 };
-constexpr int kLncWarps = 8;    // warps per block (256 threads)
-constexpr int kLncCplFwd = 2;  // chunks per lane of a row, forward
-constexpr int kLncCplBwd = 1;  // chunks per lane of a row, backward
+constexpr int kLncWarps = 4;    // warps per block (128 threads)
+constexpr int kLncCplFwd = 4;  // chunks per lane of a row, forward
+constexpr int kLncCplBwd = 2;  // chunks per lane of a row, backward
+constexpr int kLncDepth = 4;   // row stages of a block's copy ring (a pair of rows ahead)
+// dynamic shared memory of a column-block kernel: its ring of row stages and
+// their mbarriers
+constexpr int lnc_ring_bytes(bool bwd) {
+  return kLncDepth * (bwd ? 2 * kLncCplBwd : kLncCplFwd) * 32 * kLncWarps * 16 + 8 * kLncDepth;
+}
 struct LncKernels {
   const void* stats[2];
   const void* merge[2];

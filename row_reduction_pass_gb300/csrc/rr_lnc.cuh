@@ -49,24 +49,19 @@
 
 namespace rr {
 
-// Chunks per lane of one row and the chunks a block covers per row.
-template <int CPL>
-struct LncShape {
-  static constexpr int kCB = 32 * CPL * kLncWarps;
-};
+constexpr int kLncThreads = 32 * kLncWarps;
 
-// A block's work item and its view of the rows.
+// A block's work item and its view of the rows: rows r0 + i P (i < nr) of
+// the class; this lane's chunks k0 + 32 j (j < CPL) of each.
 template <int W, int CPL>
 struct LncItem {
   int cls, b, grp;
   int phi;          // row start offset within its first chunk, in elements
-  int64_t nch;      // chunks covering a row of the class
-  int tail_lanes;   // valid lanes of the row's last chunk (1 .. W)
-  int64_t r0;       // first row of the item; rows r0 + i * P (i < nr)
-  int nr;
-  int64_t k[CPL];   // this lane's chunks of the row
-  int lo[CPL], hi[CPL];  // their valid lanes [lo, hi) (empty outside the row)
-  int64_t rowb;     // bytes per row
+  int64_t r0;       // first row of the item
+  int nr;           // its rows
+  int64_t rstep;    // bytes from one of its rows to the next (P rows)
+  int64_t off0;     // bytes from a row's start to this lane's chunk j = 0
+  int lo[CPL], hi[CPL];  // valid lanes [lo, hi) of chunk j (empty outside the row)
 
   __device__ __forceinline__ void init(const LncGeo& g, const char* base, int E) {
     const int64_t it = blockIdx.x;
@@ -74,33 +69,35 @@ struct LncItem {
     const int64_t rest = it / g.P;
     b = static_cast<int>(rest % g.nb);
     grp = static_cast<int>(rest / g.nb);
-    rowb = g.cols * E;
+    const int64_t rowb = g.cols * E;
     phi = static_cast<int>(((reinterpret_cast<uintptr_t>(base) + (uint64_t)cls * rowb) & 15) / E);
-    nch = (phi + g.cols + W - 1) / W;
-    tail_lanes = static_cast<int>(phi + g.cols - (int64_t)W * (nch - 1));
+    const int64_t nch = (phi + g.cols + W - 1) / W;  // chunks covering a row of the class
+    const int tail = static_cast<int>(phi + g.cols - (int64_t)W * (nch - 1));
     // rows of the class: cls, cls + P, ...; this group's: [grp * rg, grp * rg + rg)
     const int64_t first = (int64_t)grp * g.rg;
     const int64_t in_class = g.rows > cls ? (g.rows - cls + g.P - 1) / g.P : 0;
     r0 = cls + (int64_t)g.P * first;
     nr = static_cast<int>(first < in_class ? (in_class - first < g.rg ? in_class - first : g.rg) : 0);
+    rstep = (int64_t)g.P * rowb;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t k0 = (int64_t)b * (32 * CPL * kLncWarps) + 32 * CPL * warp + lane;
+    off0 = k0 * 16 - (int64_t)phi * E;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
-      k[j] = (int64_t)b * LncShape<CPL>::kCB + 32 * CPL * warp + lane + 32 * j;
-      lo[j] = 0;
-      hi[j] = W;
-      if (k[j] >= nch) lo[j] = hi[j] = 0;
-      else {
-        if (k[j] == 0) lo[j] = phi;
-        if (k[j] == nch - 1) hi[j] = tail_lanes;
-      }
+      const int64_t k = k0 + 32 * j;
+      lo[j] = k == 0 ? phi : 0;
+      hi[j] = k == nch - 1 ? tail : W;
+      if (k >= nch) lo[j] = hi[j] = 0;
     }
   }
-  // Aligned address of chunk j of row r.
-  __device__ __forceinline__ const char* chunk(const char* base, int64_t r, int j, int E) const {
-    return base + r * rowb - (int64_t)phi * E + k[j] * 16;
+  // This lane's chunk 0 in row i of the item (chunk j is 512 j bytes on).
+  __device__ __forceinline__ const char* at_row(const char* base, int i, const LncGeo& g,
+                                                int64_t rowb) const {
+    return base + (r0 + (int64_t)i * g.P) * rowb + off0;
   }
-  __device__ __forceinline__ int64_t row(int i, const LncGeo& g) const { return r0 + (int64_t)i * g.P; }
+  __device__ __forceinline__ bool has(int j) const { return hi[j] > lo[j]; }
+  // Column of lane 0 of chunk j (negative for the lanes before the row).
+  __device__ __forceinline__ int64_t col0(int j, int E) const { return (off0 + 512 * j) / E; }
 };
 
 // The W values src[col0, col0 + W) of a [cols] vector as fp32, 0 outside
@@ -142,8 +139,23 @@ __device__ __forceinline__ void lnc_clip(float (&f)[W], int lo, int hi) {
   }
 }
 
-// Stores chunk j of a row: one aligned 128-bit store for an interior chunk,
-// the row's own lanes one by one for its first / last chunk.
+// Whether any lane of this warp holds a chunk with lanes outside the row (a
+// row's first or last chunk, or a chunk past it): only such warps (the first
+// and last of a row's blocks) take the masked code paths.
+template <bool B>
+struct LncMask {
+  static constexpr bool value = B;
+};
+template <int W, int CPL>
+__device__ __forceinline__ bool lnc_warp_ragged(const int (&lo)[CPL], const int (&hi)[CPL]) {
+  bool r = false;
+#pragma unroll
+  for (int j = 0; j < CPL; ++j) r |= lo[j] != 0 || hi[j] != W;
+  return __any_sync(0xffffffffu, r);
+}
+
+// Stores a chunk: one aligned 128-bit store for an interior chunk, the row's
+// own lanes one by one for its first / last chunk.
 template <int DT, int W>
 __device__ __forceinline__ void lnc_store(char* a, int lo, int hi, const float (&f)[W]) {
   constexpr int E = DType<DT>::E;
@@ -164,30 +176,117 @@ __device__ __forceinline__ float lnc_warp_sum(float v) {
   return v;
 }
 
-// Rows are streamed two at a time, the next two rows' chunks loaded before
-// the current two are used (double-buffered in registers), so every warp
-// keeps 2 x 2 x CPL (forward) or 2 x 2 x 2 x CPL (backward) 16-byte loads in
-// flight while it computes.
-constexpr int kLncRB = 2;
+__device__ __forceinline__ uint64_t lnc_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 
-// T tensors' chunks of rows i .. i + kLncRB - 1 of the item (zeros past nr or
-// outside the row).
-template <int T, int W, int CPL, bool STREAM>
-__device__ __forceinline__ void lnc_load(uint4 (&c)[kLncRB][T][CPL], const LncItem<W, CPL>& it,
-                                         const LncGeo& g, const char* const (&src)[T], int i,
-                                         int E) {
+// A block's ring of kLncDepth row stages in dynamic shared memory: stage
+// i mod depth holds the block's chunks of row i of the item for T tensors,
+// brought by one 1-D bulk copy (TMA) per tensor that thread 0 issues depth - 1
+// rows ahead, completing on the stage's mbarrier; every thread waits for the
+// stage's phase (bounded) and reads its own chunks.  Thread 0 refills a stage
+// only after a block barrier that follows every thread's last read of it.
+// Bulk copies keep ~56 KB per block in flight without per-thread request
+// slots (per-thread 16-byte copies capped these kernels at ~2.4 TB/s).
+// Reads: this thread's chunk j of the stage is local chunk 32 CPL warp + lane
+// + 32 j.  K1 kernels (whose data the next launch reads again) mark the lines
+// evict-last in L2, K2 kernels evict-first.
+template <int T, int CPL>
+struct LncBulk {
+  static constexpr int kCB = 32 * CPL * kLncWarps;  // chunks of a block's row
+  uint4* ring;
+  uint64_t* bars;
+  uint64_t policy;
+  uint32_t bytes;      // bytes of one tensor's copy (0: the block has no chunk)
+  const char* nxt[T];  // the block's first chunk of the next row to copy
+  int issued;
+  int local;           // this thread's local chunk j = 0
+
+  template <int W>
+  __device__ __forceinline__ void init(unsigned char* smem, const LncItem<W, CPL>& it,
+                                       const LncGeo& g, const char* const (&base)[T], int E,
+                                       bool keep) {
+    ring = reinterpret_cast<uint4*>(smem);
+    bars = reinterpret_cast<uint64_t*>(smem + kLncDepth * T * kCB * 16);
+    policy = keep ? lnc_policy_evict_last() : policy_evict_first();
+    const int64_t rowb = g.cols * E;
+    const int64_t phi_b = (int64_t)it.phi * E;
+    const int64_t nch = (phi_b + rowb + 15) / 16;
+    const int64_t kb = (int64_t)it.b * kCB;
+    const int64_t n = nch - kb < kCB ? nch - kb : kCB;
+    bytes = n > 0 ? static_cast<uint32_t>(n) * 16 : 0u;
 #pragma unroll
-  for (int u = 0; u < kLncRB; ++u)
+    for (int t = 0; t < T; ++t) nxt[t] = base[t] + it.r0 * rowb - phi_b + kb * 16;
+    issued = 0;
+    local = 32 * CPL * (threadIdx.x >> 5) + (threadIdx.x & 31);
+  }
+  __device__ __forceinline__ uint4* stage(int i, int t) const {
+    return ring + ((i & (kLncDepth - 1)) * T + t) * kCB;
+  }
+  __device__ __forceinline__ const uint4& at(int i, int t, int j) const {
+    return stage(i, t)[local + 32 * j];
+  }
+  // Thread 0: the next row's copies (none past the item's rows).
+  __device__ __forceinline__ void issue(int nr, int64_t rstep) {
+    if (issued < nr && bytes > 0) {
+      uint64_t* bar = &bars[issued & (kLncDepth - 1)];
+      fence_proxy_async_smem();  // earlier generic reads of the stage come first
+      mbar_arrive_expect_tx(bar, bytes * T);
 #pragma unroll
-    for (int t = 0; t < T; ++t)
+      for (int t = 0; t < T; ++t)
+        bulk_load(stage(issued, t), nxt[t], bytes, bar, policy);
+    }
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        c[u][t][j] = make_uint4(0u, 0u, 0u, 0u);
-        if (i + u < it.nr && it.hi[j] > it.lo[j]) {
-          const char* a = it.chunk(src[t], it.row(i + u, g), j, E);
-          c[u][t][j] = STREAM ? ld_chunk_stream(a) : ld_chunk_cached(a);
-        }
-      }
+    for (int t = 0; t < T; ++t) nxt[t] += rstep;
+    ++issued;
+  }
+  // Every thread: row i has landed (false if the wait gave up: error recorded).
+  __device__ __forceinline__ bool wait(int i, int* err) {
+    if (bytes == 0) return true;
+    return mbar_wait_bounded(&bars[i & (kLncDepth - 1)],
+                             static_cast<uint32_t>((i / kLncDepth) & 1), err);
+  }
+  // After a wait gave up: thread 0 waits (bounded) for the last copy issued
+  // into each stage, so none is still writing the block's shared memory.
+  __device__ __forceinline__ void drain(int nr, int* err) const {
+    if (bytes == 0) return;
+    const int n = issued < nr ? issued : nr;  // rows actually copied
+    for (int s = 0; s < kLncDepth; ++s) {
+      if (n <= s) continue;
+      const int last = s + ((n - 1 - s) / kLncDepth) * kLncDepth;
+      mbar_wait_bounded(&bars[s], static_cast<uint32_t>((last / kLncDepth) & 1), err, 100000000ull);
+    }
+  }
+};
+
+// Rows are taken two at a time (one ring refill and one block barrier per
+// pair).  The ring's set-up: thread 0 initialises the barriers and
+// issues the first depth - 2 rows; the block barrier publishes the barriers.
+template <int T, int W, int CPL>
+__device__ __forceinline__ void lnc_start(LncBulk<T, CPL>& ring, const LncItem<W, CPL>& it) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLncDepth; ++s) mbar_init(&ring.bars[s], 1);
+    fence_mbar_init();
+    for (int s = 0; s < kLncDepth - 2; ++s) ring.issue(it.nr, it.rstep);
+  }
+  __syncthreads();
+}
+
+// Top of rows i, i + 1: every thread is done with rows i - 2, i - 1 (block
+// barrier), thread 0 refills those stages with rows i + depth - 2 and
+// i + depth - 1, then all wait for rows i and i + 1.
+template <int T, int CPL>
+__device__ __forceinline__ void lnc_next2(LncBulk<T, CPL>& ring, int i, int nr, int64_t rstep,
+                                          bool& dead, int* err) {
+  if (i > 0) __syncthreads();
+  if (threadIdx.x == 0) {
+    ring.issue(nr, rstep);
+    ring.issue(nr, rstep);
+  }
+  if (!dead) dead = !ring.wait(i, err);
+  if (i + 1 < nr && !dead) dead = !ring.wait(i + 1, err);
 }
 
 // ------------------------------------------------------------- forward ----
@@ -195,105 +294,116 @@ __device__ __forceinline__ void lnc_load(uint4 (&c)[kLncRB][T][CPL], const LncIt
 // Launch 1: per (row, column block) records -- Moments (LayerNorm) or the sum
 // of squares (RMSNorm) -- into the scratch at p.y rounded up to 16 bytes.
 template <int DT, bool RMS, int CPL>
-__global__ void __launch_bounds__(32 * kLncWarps, 3) lnc_stats_kernel(const LnFwdParams p,
-                                                                      const LncGeo g) {
+__global__ void __launch_bounds__(kLncThreads, 5) lnc_stats_kernel(const LnFwdParams p,
+                                                                const LncGeo g) {
   constexpr int E = DType<DT>::E, W = DType<DT>::V;
-  constexpr int RS = 32;  // rows whose warp records are merged together
+  constexpr int RS = 32;  // rows whose warp records are merged together (even)
+  extern __shared__ __align__(128) unsigned char lnc_smem[];
   __shared__ Moments part[RS][kLncWarps];
   LncItem<W, CPL> it;
   it.init(g, p.x, E);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   char* recs = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(p.y) + 15) & ~uintptr_t(15));
+  LncBulk<1, CPL> ring;
+  {
+    const char* const base[1] = {p.x};
+    ring.init(lnc_smem, it, g, base, E, true);
+  }
+  lnc_start(ring, it);
+  bool dead = false;
   // valid values of this warp's slice of a row (the same for every row)
   int cnt = 0;
 #pragma unroll
   for (int j = 0; j < CPL; ++j) cnt += it.hi[j] - it.lo[j];
   const float nw = lnc_warp_sum(static_cast<float>(cnt));
   const float inv_nw = nw > 0.f ? 1.f / nw : 0.f;
-  const char* const src[1] = {p.x};
+  const bool ragged = lnc_warp_ragged<W, CPL>(it.lo, it.hi);
 
-  uint4 nxt[kLncRB][1][CPL];
-  lnc_load<1, W, CPL, false>(nxt, it, g, src, 0, E);
-  for (int i = 0; i < it.nr; i += kLncRB) {
-    uint4 cur[kLncRB][1][CPL];
+  // the moments of this warp's slice of row i (masked lanes only in ragged
+  // warps)
+  auto row_moments = [&](int i, auto tag) {
+    constexpr bool M = decltype(tag)::value;
+    float v[CPL][W];
 #pragma unroll
-    for (int u = 0; u < kLncRB; ++u)
+    for (int j = 0; j < CPL; ++j) {
+      if (!M || it.has(j)) lnc_unpack<DT, W>(ring.at(i, 0, j), v[j]);
+      if constexpr (M) lnc_clip<W>(v[j], it.lo[j], it.hi[j]);  // also a chunk past the row
+    }
+    Moments m;
+    if constexpr (RMS) {
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) cur[u][0][j] = nxt[u][0][j];
-    if (i + kLncRB < it.nr) lnc_load<1, W, CPL, false>(nxt, it, g, src, i + kLncRB, E);
+      for (int j = 0; j < CPL; ++j)
 #pragma unroll
-    for (int u = 0; u < kLncRB; ++u) {
-      if (i + u >= it.nr) break;
-      float v[CPL][W];
+        for (int e = 0; e < W; e += 2) fma2(a0, a1, v[j][e], v[j][e + 1], v[j][e], v[j][e + 1], a0, a1);
+      m = {0.f, lnc_warp_sum(a0 + a1), 0.f, 0.f};
+    } else {
+      // provisional mean, then the deviations about it
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j)
+#pragma unroll
+        for (int e = 0; e < W; e += 2) add2(s0, s1, s0, s1, v[j][e], v[j][e + 1]);
+      const float m0 = lnc_warp_sum(s0 + s1) * inv_nw;
+      float d0 = 0.f, d1 = 0.f, q0 = 0.f, q1 = 0.f;
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {
-        lnc_unpack<DT, W>(cur[u][0][j], v[j]);
-        lnc_clip<W>(v[j], it.lo[j], it.hi[j]);
-      }
-      Moments m;
-      if constexpr (RMS) {
-        float a0 = 0.f, a1 = 0.f;
+        float d[W];
 #pragma unroll
-        for (int j = 0; j < CPL; ++j)
+        for (int e = 0; e < W; e += 2) add2(d[e], d[e + 1], v[j][e], v[j][e + 1], -m0, -m0);
+        if constexpr (M) lnc_clip<W>(d, it.lo[j], it.hi[j]);
 #pragma unroll
-          for (int e = 0; e < W; e += 2) fma2(a0, a1, v[j][e], v[j][e + 1], v[j][e], v[j][e + 1], a0, a1);
-        m = {0.f, lnc_warp_sum(a0 + a1), 0.f, 0.f};
-      } else {
-        // provisional mean, then the deviations about it
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int j = 0; j < CPL; ++j)
-#pragma unroll
-          for (int e = 0; e < W; e += 2) add2(s0, s1, s0, s1, v[j][e], v[j][e + 1]);
-        const float m0 = lnc_warp_sum(s0 + s1) * inv_nw;
-        float d0 = 0.f, d1 = 0.f, q0 = 0.f, q1 = 0.f;
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-          float d[W];
-#pragma unroll
-          for (int e = 0; e < W; e += 2) add2(d[e], d[e + 1], v[j][e], v[j][e + 1], -m0, -m0);
-          lnc_clip<W>(d, it.lo[j], it.hi[j]);
-#pragma unroll
-          for (int e = 0; e < W; e += 2) {
-            add2(d0, d1, d0, d1, d[e], d[e + 1]);
-            fma2(q0, q1, d[e], d[e + 1], d[e], d[e + 1], q0, q1);
-          }
+        for (int e = 0; e < W; e += 2) {
+          add2(d0, d1, d0, d1, d[e], d[e + 1]);
+          fma2(q0, q1, d[e], d[e + 1], d[e], d[e + 1], q0, q1);
         }
-        const float sd = lnc_warp_sum(d0 + d1), q = lnc_warp_sum(q0 + q1);
-        // S = nw m0 + sd as a double-float (the product's error exact in one FMA)
-        const float pr = __fmul_rn(nw, m0), pe = fmaf(nw, m0, -pr);
-        float h, l;
-        two_sum(pr, sd, h, l);
-        l += pe;
-        float sh, sl;
-        two_sum(h, l, sh, sl);
-        const float t = q - (nw > 0.f ? sd * sd * inv_nw : 0.f);
-        m = {nw, nw > 0.f ? sh : 0.f, nw > 0.f ? sl : 0.f, t < 0.f ? 0.f : t};
       }
+      const float sd = lnc_warp_sum(d0 + d1), q = lnc_warp_sum(q0 + q1);
+      // S = nw m0 + sd as a double-float (the product's error exact in one FMA)
+      const float pr = __fmul_rn(nw, m0), pe = fmaf(nw, m0, -pr);
+      float h, l;
+      two_sum(pr, sd, h, l);
+      l += pe;
+      float sh, sl;
+      two_sum(h, l, sh, sl);
+      const float t = q - (nw > 0.f ? sd * sd * inv_nw : 0.f);
+      m = {nw, nw > 0.f ? sh : 0.f, nw > 0.f ? sl : 0.f, t < 0.f ? 0.f : t};
+    }
+    return m;
+  };
+
+  for (int i = 0; i < it.nr; i += 2) {
+    lnc_next2(ring, i, it.nr, it.rstep, dead, p.err);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (u == 1 && i + 1 >= it.nr) break;
+      const Moments m = ragged ? row_moments(i + u, LncMask<true>())
+                               : row_moments(i + u, LncMask<false>());
       if (lane == 0) part[(i + u) % RS][warp] = m;
     }
     // every RS rows (and at the end): the block's record of each row, its
     // warps' records merged in warp order
-    const int done = min(i + kLncRB, it.nr);
+    const int done = min(i + 2, it.nr);
     if (done % RS == 0 || done == it.nr) {
       __syncthreads();
       const int base = (done - 1) / RS * RS, ns = done - base;
       if (threadIdx.x < ns) {
         const int ri = threadIdx.x;
-        Moments m = part[ri][0];
+        Moments mm = part[ri][0];
         for (int w = 1; w < kLncWarps; ++w) {
-          if constexpr (RMS) m.sh += part[ri][w].sh;
-          else m = MergeMoments()(m, part[ri][w]);
+          if constexpr (RMS) mm.sh += part[ri][w].sh;
+          else mm = MergeMoments()(mm, part[ri][w]);
         }
-        const int64_t r = it.row(base + ri, g);
+        const int64_t r = it.r0 + (int64_t)(base + ri) * g.P;
         if constexpr (RMS)
-          reinterpret_cast<float*>(recs)[r * g.nb + it.b] = m.sh;
+          reinterpret_cast<float*>(recs)[r * g.nb + it.b] = mm.sh;
         else
-          reinterpret_cast<float4*>(recs)[r * g.nb + it.b] = make_float4(m.n, m.sh, m.sl, m.m2);
+          reinterpret_cast<float4*>(recs)[r * g.nb + it.b] = make_float4(mm.n, mm.sh, mm.sl, mm.m2);
       }
       __syncthreads();
     }
   }
+  if (dead && threadIdx.x == 0) ring.drain(it.nr, p.err);
 }
 
 // Launch 2: a warp per row merges the row's records (lane l: records l,
@@ -333,71 +443,78 @@ __global__ void __launch_bounds__(256) lnc_merge_kernel(const LnFwdParams p, con
 
 // Launch 3: y from x (read again), the saved mean / rstd and gamma / beta.
 template <int DT, bool RMS, int CPL>
-__global__ void __launch_bounds__(32 * kLncWarps, RMS ? 3 : 2) lnc_norm_kernel(const LnFwdParams p,
-                                                                     const LncGeo g) {
+__global__ void __launch_bounds__(kLncThreads, 5) lnc_norm_kernel(const LnFwdParams p,
+                                                               const LncGeo g) {
   constexpr int E = DType<DT>::E, W = DType<DT>::V;
+  extern __shared__ __align__(128) unsigned char lnc_smem[];
   LncItem<W, CPL> it;
   it.init(g, p.x, E);
-  const char* const src[1] = {p.x};
-  uint4 nxt[kLncRB][1][CPL];
-  lnc_load<1, W, CPL, true>(nxt, it, g, src, 0, E);
+  const int64_t rowb = g.cols * E;
+  LncBulk<1, CPL> ring;
+  {
+    const char* const base[1] = {p.x};
+    ring.init(lnc_smem, it, g, base, E, false);
+  }
+  lnc_start(ring, it);
+  bool dead = false;
   float gm[CPL][W], bt[CPL][W];
 #pragma unroll
   for (int j = 0; j < CPL; ++j) {
-    const int64_t col0 = it.k[j] * W - it.phi;
 #pragma unroll
     for (int e = 0; e < W; ++e) gm[j][e] = bt[j][e] = 0.f;
-    if (it.hi[j] > it.lo[j]) {
-      lnc_vec_chunk<DT, W>(p.gamma, g.cols, col0, gm[j]);
-      if constexpr (!RMS) lnc_vec_chunk<DT, W>(p.beta, g.cols, col0, bt[j]);
+    if (it.has(j)) {
+      lnc_vec_chunk<DT, W>(p.gamma, g.cols, it.col0(j, E), gm[j]);
+      if constexpr (!RMS) lnc_vec_chunk<DT, W>(p.beta, g.cols, it.col0(j, E), bt[j]);
     }
   }
-  for (int i = 0; i < it.nr; i += kLncRB) {
-    uint4 cur[kLncRB][1][CPL];
-    float mean[kLncRB], rstd[kLncRB];
+  const bool ragged = lnc_warp_ragged<W, CPL>(it.lo, it.hi);
+  // y of this warp's slice of row i (lane-wise stores only in ragged warps)
+  auto row_out = [&](int i, float mean, float rstd, char* out, auto tag) {
+    constexpr bool M = decltype(tag)::value;
 #pragma unroll
-    for (int u = 0; u < kLncRB; ++u) {
-      mean[u] = rstd[u] = 0.f;
-      if (i + u < it.nr) {
-        const int64_t r = it.row(i + u, g);
-        if constexpr (!RMS) mean[u] = __ldg(p.mean + r);
-        rstd[u] = __ldg(p.rstd + r);
-      }
+    for (int j = 0; j < CPL; ++j) {
+      if (M && !it.has(j)) continue;
+      float v[W], y[W];
+      lnc_unpack<DT, W>(ring.at(i, 0, j), v);
+      if (rstd == 0.f) {  // masked row
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) cur[u][0][j] = nxt[u][0][j];
-    }
-    if (i + kLncRB < it.nr) lnc_load<1, W, CPL, true>(nxt, it, g, src, i + kLncRB, E);
+        for (int e = 0; e < W; ++e) y[e] = 0.f;
+      } else {
 #pragma unroll
-    for (int u = 0; u < kLncRB; ++u) {
-      if (i + u >= it.nr) break;
-      const int64_t r = it.row(i + u, g);
-      const bool masked = rstd[u] == 0.f;
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        if (it.hi[j] <= it.lo[j]) continue;
-        float v[W], y[W];
-        lnc_unpack<DT, W>(cur[u][0][j], v);
-        if (masked) {
-#pragma unroll
-          for (int e = 0; e < W; ++e) y[e] = 0.f;
-        } else {
-#pragma unroll
-          for (int e = 0; e < W; e += 2) {
-            float t0, t1;
-            if constexpr (RMS) {
-              mul2(t0, t1, v[e], v[e + 1], rstd[u], rstd[u]);
-              mul2(y[e], y[e + 1], t0, t1, gm[j][e], gm[j][e + 1]);
-            } else {
-              add2(t0, t1, v[e], v[e + 1], -mean[u], -mean[u]);
-              mul2(t0, t1, t0, t1, rstd[u], rstd[u]);
-              fma2(y[e], y[e + 1], t0, t1, gm[j][e], gm[j][e + 1], bt[j][e], bt[j][e + 1]);
-            }
+        for (int e = 0; e < W; e += 2) {
+          float t0, t1;
+          if constexpr (RMS) {
+            mul2(t0, t1, v[e], v[e + 1], rstd, rstd);
+            mul2(y[e], y[e + 1], t0, t1, gm[j][e], gm[j][e + 1]);
+          } else {
+            add2(t0, t1, v[e], v[e + 1], -mean, -mean);
+            mul2(t0, t1, t0, t1, rstd, rstd);
+            fma2(y[e], y[e + 1], t0, t1, gm[j][e], gm[j][e + 1], bt[j][e], bt[j][e + 1]);
           }
         }
-        lnc_store<DT, W>(const_cast<char*>(it.chunk(p.y, r, j, E)), it.lo[j], it.hi[j], y);
       }
+      if constexpr (M) lnc_store<DT, W>(out + 512 * j, it.lo[j], it.hi[j], y);
+      else st_chunk_stream(out + 512 * j, chunk_pack<DT>(y));
+    }
+  };
+  char* out = const_cast<char*>(it.at_row(p.y, 0, g, rowb));
+  const float* pm = p.mean + it.r0;
+  const float* pr = p.rstd + it.r0;
+  const int64_t sP = g.P;
+  for (int i = 0; i < it.nr; i += 2, out += 2 * it.rstep, pm += 2 * sP, pr += 2 * sP) {
+    const bool two = i + 1 < it.nr;
+    const float mean0 = RMS ? 0.f : __ldg(pm), rstd0 = __ldg(pr);
+    const float mean1 = RMS || !two ? 0.f : __ldg(pm + sP), rstd1 = two ? __ldg(pr + sP) : 0.f;
+    lnc_next2(ring, i, it.nr, it.rstep, dead, p.err);
+    if (ragged) {
+      row_out(i, mean0, rstd0, out, LncMask<true>());
+      if (two) row_out(i + 1, mean1, rstd1, out + it.rstep, LncMask<true>());
+    } else {
+      row_out(i, mean0, rstd0, out, LncMask<false>());
+      if (two) row_out(i + 1, mean1, rstd1, out + it.rstep, LncMask<false>());
     }
   }
+  if (dead && threadIdx.x == 0) ring.drain(it.nr, p.err);
 }
 
 // ------------------------------------------------------------ backward ----
@@ -406,77 +523,94 @@ __global__ void __launch_bounds__(32 * kLncWarps, RMS ? 3 : 2) lnc_norm_kernel(c
 // floats, and the item's column partials (sum dy xhat, sum dy) in its partial
 // row (class, row group) of p.ws: [partial][planes][cols].
 template <int DT, bool RMS, int CPL>
-__global__ void __launch_bounds__(32 * kLncWarps, 2) lnc_bwd_part_kernel(const LnBwdParams p,
-                                                                         const LncGeo g) {
+__global__ void __launch_bounds__(kLncThreads, 5) lnc_bwd_part_kernel(const LnBwdParams p,
+                                                                   const LncGeo g) {
   constexpr int E = DType<DT>::E, W = DType<DT>::V;
   constexpr int kPlanes = RMS ? 1 : 2;
-  constexpr int RS = 32;
+  constexpr int RS = 32;  // even
+  extern __shared__ __align__(128) unsigned char lnc_smem[];
   __shared__ float2 part[RS][kLncWarps];
   LncItem<W, CPL> it;
   it.init(g, p.x, E);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float2* recs = reinterpret_cast<float2*>(p.ws + g.rec_off);
-  const char* const src[2] = {p.dy, p.x};
-  uint4 nxt[kLncRB][2][CPL];
-  lnc_load<2, W, CPL, false>(nxt, it, g, src, 0, E);
+  LncBulk<2, CPL> ring;
+  {
+    const char* const base[2] = {p.dy, p.x};
+    ring.init(lnc_smem, it, g, base, E, true);
+  }
+  lnc_start(ring, it);
+  bool dead = false;
   float gm[CPL][W], ag[CPL][W], ab[CPL][W];
 #pragma unroll
   for (int j = 0; j < CPL; ++j) {
 #pragma unroll
     for (int e = 0; e < W; ++e) gm[j][e] = ag[j][e] = ab[j][e] = 0.f;
-    if (it.hi[j] > it.lo[j]) lnc_vec_chunk<DT, W>(p.gamma, g.cols, it.k[j] * W - it.phi, gm[j]);
+    if (it.has(j)) lnc_vec_chunk<DT, W>(p.gamma, g.cols, it.col0(j, E), gm[j]);
   }
-  for (int i = 0; i < it.nr; i += kLncRB) {
-    uint4 cur[kLncRB][2][CPL];
-    float mean[kLncRB], rstd[kLncRB];
+  const bool ragged = lnc_warp_ragged<W, CPL>(it.lo, it.hi);
+  // this warp's slice of row i: its column partials, and (S1, S2) of the lanes
+  auto row_sums = [&](int i, float mean, float rstd, float& s1, float& s2, auto tag) {
+    constexpr bool M = decltype(tag)::value;
+    float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
+    if (rstd != 0.f) {  // a masked row adds nothing
 #pragma unroll
-    for (int u = 0; u < kLncRB; ++u) {
-      mean[u] = rstd[u] = 0.f;
-      if (i + u < it.nr) {
-        const int64_t r = it.row(i + u, g);
-        if constexpr (!RMS) mean[u] = __ldg(p.mean + r);
-        rstd[u] = __ldg(p.rstd + r);
-      }
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) cur[u][t][j] = nxt[u][t][j];
-    }
-    if (i + kLncRB < it.nr) lnc_load<2, W, CPL, false>(nxt, it, g, src, i + kLncRB, E);
-#pragma unroll
-    for (int u = 0; u < kLncRB; ++u) {
-      if (i + u >= it.nr) break;
-      float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
-      if (rstd[u] != 0.f) {  // a masked row adds nothing
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-          float dv[W], xv[W];
-          lnc_unpack<DT, W>(cur[u][0][j], dv);
-          lnc_unpack<DT, W>(cur[u][1][j], xv);
+      for (int j = 0; j < CPL; ++j) {
+        if (M && !it.has(j)) continue;
+        float dv[W], xv[W];
+        lnc_unpack<DT, W>(ring.at(i, 0, j), dv);
+        lnc_unpack<DT, W>(ring.at(i, 1, j), xv);
+        if constexpr (M) {
           lnc_clip<W>(dv, it.lo[j], it.hi[j]);
           lnc_clip<W>(xv, it.lo[j], it.hi[j]);
+        }
 #pragma unroll
-          for (int e = 0; e < W; e += 2) {
-            float h0, h1;
-            if constexpr (RMS) {
-              mul2(h0, h1, xv[e], xv[e + 1], rstd[u], rstd[u]);
-            } else {
-              add2(h0, h1, xv[e], xv[e + 1], -mean[u], -mean[u]);
-              mul2(h0, h1, h0, h1, rstd[u], rstd[u]);
-            }
-            // g rounded once (a product that must not fuse into the sums)
-            const float g0 = __fmul_rn(dv[e], gm[j][e]), g1 = __fmul_rn(dv[e + 1], gm[j][e + 1]);
-            if constexpr (!RMS) add2(s1a, s1b, s1a, s1b, g0, g1);
-            fma2(s2a, s2b, g0, g1, h0, h1, s2a, s2b);
-            fma2(ag[j][e], ag[j][e + 1], dv[e], dv[e + 1], h0, h1, ag[j][e], ag[j][e + 1]);
-            if constexpr (!RMS) add2(ab[j][e], ab[j][e + 1], ab[j][e], ab[j][e + 1], dv[e], dv[e + 1]);
+        for (int e = 0; e < W; e += 2) {
+          float h0, h1;
+          if constexpr (RMS) {
+            mul2(h0, h1, xv[e], xv[e + 1], rstd, rstd);
+          } else {
+            add2(h0, h1, xv[e], xv[e + 1], -mean, -mean);
+            mul2(h0, h1, h0, h1, rstd, rstd);
           }
+          // g rounded once (a product that must not fuse into the sums)
+          const float g0 = __fmul_rn(dv[e], gm[j][e]), g1 = __fmul_rn(dv[e + 1], gm[j][e + 1]);
+          if constexpr (!RMS) add2(s1a, s1b, s1a, s1b, g0, g1);
+          fma2(s2a, s2b, g0, g1, h0, h1, s2a, s2b);
+          fma2(ag[j][e], ag[j][e + 1], dv[e], dv[e + 1], h0, h1, ag[j][e], ag[j][e + 1]);
+          if constexpr (!RMS) add2(ab[j][e], ab[j][e + 1], ab[j][e], ab[j][e + 1], dv[e], dv[e + 1]);
         }
       }
-      const float s1 = RMS ? 0.f : lnc_warp_sum(s1a + s1b), s2 = lnc_warp_sum(s2a + s2b);
-      if (lane == 0) part[(i + u) % RS][warp] = make_float2(s1, s2);
     }
-    const int done = min(i + kLncRB, it.nr);
+    s1 = s1a + s1b;
+    s2 = s2a + s2b;
+  };
+  const float* pm = p.mean + it.r0;
+  const float* pr = p.rstd + it.r0;
+  const int64_t sP = g.P;
+  for (int i = 0; i < it.nr; i += 2, pm += 2 * sP, pr += 2 * sP) {
+    const bool two = i + 1 < it.nr;
+    const float mean0 = RMS ? 0.f : __ldg(pm), rstd0 = __ldg(pr);
+    const float mean1 = RMS || !two ? 0.f : __ldg(pm + sP), rstd1 = two ? __ldg(pr + sP) : 0.f;
+    lnc_next2(ring, i, it.nr, it.rstep, dead, p.err);
+    float s[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    if (ragged) {
+      row_sums(i, mean0, rstd0, s[0][0], s[0][1], LncMask<true>());
+      if (two) row_sums(i + 1, mean1, rstd1, s[1][0], s[1][1], LncMask<true>());
+    } else {
+      row_sums(i, mean0, rstd0, s[0][0], s[0][1], LncMask<false>());
+      if (two) row_sums(i + 1, mean1, rstd1, s[1][0], s[1][1], LncMask<false>());
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if constexpr (!RMS) s[u][0] = lnc_warp_sum(s[u][0]);
+      s[u][1] = lnc_warp_sum(s[u][1]);
+    }
+    if (lane == 0) {
+      part[i % RS][warp] = make_float2(s[0][0], s[0][1]);
+      if (two) part[(i + 1) % RS][warp] = make_float2(s[1][0], s[1][1]);
+    }
+    const int done = min(i + 2, it.nr);
     if (done % RS == 0 || done == it.nr) {
       __syncthreads();
       const int base = (done - 1) / RS * RS, ns = done - base;
@@ -487,22 +621,23 @@ __global__ void __launch_bounds__(32 * kLncWarps, 2) lnc_bwd_part_kernel(const L
           t.x += part[ri][w].x;
           t.y += part[ri][w].y;
         }
-        recs[it.row(base + ri, g) * g.nb + it.b] = t;
+        recs[(it.r0 + (int64_t)(base + ri) * g.P) * g.nb + it.b] = t;
       }
       __syncthreads();
     }
   }
+  if (dead && threadIdx.x == 0) ring.drain(it.nr, p.err);
   // the item's column partials: every column of the block, zeros included
   float* out = p.ws + ((int64_t)it.cls * g.ng + it.grp) * kPlanes * g.cols;
 #pragma unroll
   for (int j = 0; j < CPL; ++j) {
-    if (it.hi[j] <= it.lo[j]) continue;
-    const int64_t col0 = it.k[j] * W - it.phi;
+    if (!it.has(j)) continue;
+    const int64_t c0 = it.col0(j, E);
 #pragma unroll
     for (int e = 0; e < W; ++e) {
       if (e < it.lo[j] || e >= it.hi[j]) continue;
-      out[col0 + e] = ag[j][e];
-      if constexpr (!RMS) out[g.cols + col0 + e] = ab[j][e];
+      out[c0 + e] = ag[j][e];
+      if constexpr (!RMS) out[g.cols + c0 + e] = ab[j][e];
     }
   }
 }
@@ -510,84 +645,102 @@ __global__ void __launch_bounds__(32 * kLncWarps, 2) lnc_bwd_part_kernel(const L
 // Launch 2: dx from dy, x (read again), mean / rstd, gamma and the row's
 // (S1, S2) summed over its column blocks.
 template <int DT, bool RMS, int CPL>
-__global__ void __launch_bounds__(32 * kLncWarps, 2) lnc_bwd_dx_kernel(const LnBwdParams p,
-                                                                       const LncGeo g) {
+__global__ void __launch_bounds__(kLncThreads, 6) lnc_bwd_dx_kernel(const LnBwdParams p,
+                                                                 const LncGeo g) {
   constexpr int E = DType<DT>::E, W = DType<DT>::V;
+  extern __shared__ __align__(128) unsigned char lnc_smem[];
   LncItem<W, CPL> it;
   it.init(g, p.x, E);
+  const int64_t rowb = g.cols * E;
   const int lane = threadIdx.x & 31;
-  const float2* recs = reinterpret_cast<const float2*>(p.ws + g.rec_off);
-  const char* const src[2] = {p.dy, p.x};
-  uint4 nxt[kLncRB][2][CPL];
-  lnc_load<2, W, CPL, true>(nxt, it, g, src, 0, E);
+  LncBulk<2, CPL> ring;
+  {
+    const char* const base[2] = {p.dy, p.x};
+    ring.init(lnc_smem, it, g, base, E, false);
+  }
+  lnc_start(ring, it);
+  bool dead = false;
   float gm[CPL][W];
 #pragma unroll
   for (int j = 0; j < CPL; ++j) {
 #pragma unroll
     for (int e = 0; e < W; ++e) gm[j][e] = 0.f;
-    if (it.hi[j] > it.lo[j]) lnc_vec_chunk<DT, W>(p.gamma, g.cols, it.k[j] * W - it.phi, gm[j]);
+    if (it.has(j)) lnc_vec_chunk<DT, W>(p.gamma, g.cols, it.col0(j, E), gm[j]);
   }
-  for (int i = 0; i < it.nr; i += kLncRB) {
-    uint4 cur[kLncRB][2][CPL];
-    float mean[kLncRB], rstd[kLncRB], a[kLncRB], bq[kLncRB];
+  const bool ragged = lnc_warp_ragged<W, CPL>(it.lo, it.hi);
+  // dx of this warp's slice of row i (lane-wise stores only in ragged warps)
+  auto row_dx = [&](int i, float mean, float rstd, float a, float bq, char* out, auto tag) {
+    constexpr bool M = decltype(tag)::value;
 #pragma unroll
-    for (int u = 0; u < kLncRB; ++u) {
-      mean[u] = rstd[u] = a[u] = bq[u] = 0.f;
-      if (i + u < it.nr) {
-        const int64_t r = it.row(i + u, g);
-        if constexpr (!RMS) mean[u] = __ldg(p.mean + r);
-        rstd[u] = __ldg(p.rstd + r);
-        // the row's sums: lane l adds records l, l + 32, ... in order, then
-        // the lanes' sums by an ordered butterfly
-        float t1 = 0.f, t2 = 0.f;
+    for (int j = 0; j < CPL; ++j) {
+      if (M && !it.has(j)) continue;
+      float o[W];
+      if (rstd == 0.f) {
+#pragma unroll
+        for (int e = 0; e < W; ++e) o[e] = 0.f;
+      } else {
+        float dv[W], xv[W];
+        lnc_unpack<DT, W>(ring.at(i, 0, j), dv);
+        lnc_unpack<DT, W>(ring.at(i, 1, j), xv);
+#pragma unroll
+        for (int e = 0; e < W; e += 2) {
+          float h0, h1, t0, t1b;
+          if constexpr (RMS) {
+            mul2(h0, h1, xv[e], xv[e + 1], rstd, rstd);
+          } else {
+            add2(h0, h1, xv[e], xv[e + 1], -mean, -mean);
+            mul2(h0, h1, h0, h1, rstd, rstd);
+          }
+          const float g0 = __fmul_rn(dv[e], gm[j][e]), g1 = __fmul_rn(dv[e + 1], gm[j][e + 1]);
+          add2(t0, t1b, g0, g1, -a, -a);               // g - S1 / C
+          fma2(t0, t1b, h0, h1, -bq, -bq, t0, t1b);    // - xhat S2 / C
+          mul2(o[e], o[e + 1], t0, t1b, rstd, rstd);
+        }
+      }
+      if constexpr (M) lnc_store<DT, W>(out + 512 * j, it.lo[j], it.hi[j], o);
+      else st_chunk_stream(out + 512 * j, chunk_pack<DT>(o));
+    }
+  };
+  char* out = const_cast<char*>(it.at_row(p.dx, 0, g, rowb));
+  const float* pm = p.mean + it.r0;
+  const float* pr = p.rstd + it.r0;
+  const float2* rec = reinterpret_cast<const float2*>(p.ws + g.rec_off) + it.r0 * g.nb;
+  const int64_t sP = g.P, rec_step = (int64_t)g.P * g.nb;
+  for (int i = 0; i < it.nr; i += 2, out += 2 * it.rstep, pm += 2 * sP, pr += 2 * sP,
+           rec += 2 * rec_step) {
+    const bool two = i + 1 < it.nr;
+    float mean[2], rstd[2], a[2], bq[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      mean[u] = RMS || (u && !two) ? 0.f : __ldg(pm + u * sP);
+      rstd[u] = u && !two ? 0.f : __ldg(pr + u * sP);
+      // the row's sums: lane l adds records l, l + 32, ... in order, then the
+      // lanes' sums by an ordered butterfly
+      float t1 = 0.f, t2 = 0.f;
+      if (u == 0 || two)
         for (int b = lane; b < g.nb; b += 32) {
-          const float2 s = __ldg(recs + r * g.nb + b);
+          const float2 s = __ldg(rec + u * rec_step + b);
           t1 += s.x;
           t2 += s.y;
         }
-        a[u] = (RMS ? 0.f : lnc_warp_sum(t1)) * p.inv_cols;
-        bq[u] = lnc_warp_sum(t2) * p.inv_cols;
-      }
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) cur[u][t][j] = nxt[u][t][j];
+      a[u] = t1;
+      bq[u] = t2;
     }
-    if (i + kLncRB < it.nr) lnc_load<2, W, CPL, true>(nxt, it, g, src, i + kLncRB, E);
 #pragma unroll
-    for (int u = 0; u < kLncRB; ++u) {
-      if (i + u >= it.nr) break;
-      const int64_t r = it.row(i + u, g);
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        if (it.hi[j] <= it.lo[j]) continue;
-        float o[W];
-        if (rstd[u] == 0.f) {
-#pragma unroll
-          for (int e = 0; e < W; ++e) o[e] = 0.f;
-        } else {
-          float dv[W], xv[W];
-          lnc_unpack<DT, W>(cur[u][0][j], dv);
-          lnc_unpack<DT, W>(cur[u][1][j], xv);
-#pragma unroll
-          for (int e = 0; e < W; e += 2) {
-            float h0, h1, t0, t1;
-            if constexpr (RMS) {
-              mul2(h0, h1, xv[e], xv[e + 1], rstd[u], rstd[u]);
-            } else {
-              add2(h0, h1, xv[e], xv[e + 1], -mean[u], -mean[u]);
-              mul2(h0, h1, h0, h1, rstd[u], rstd[u]);
-            }
-            const float g0 = __fmul_rn(dv[e], gm[j][e]), g1 = __fmul_rn(dv[e + 1], gm[j][e + 1]);
-            add2(t0, t1, g0, g1, -a[u], -a[u]);             // g - S1 / C
-            fma2(t0, t1, h0, h1, -bq[u], -bq[u], t0, t1);   // - xhat S2 / C
-            mul2(o[e], o[e + 1], t0, t1, rstd[u], rstd[u]);
-          }
-        }
-        lnc_store<DT, W>(const_cast<char*>(it.chunk(p.dx, r, j, E)), it.lo[j], it.hi[j], o);
-      }
+    for (int u = 0; u < 2; ++u) {
+      a[u] = (RMS ? 0.f : lnc_warp_sum(a[u])) * p.inv_cols;
+      bq[u] = lnc_warp_sum(bq[u]) * p.inv_cols;
+    }
+    lnc_next2(ring, i, it.nr, it.rstep, dead, p.err);
+    if (ragged) {
+      row_dx(i, mean[0], rstd[0], a[0], bq[0], out, LncMask<true>());
+      if (two) row_dx(i + 1, mean[1], rstd[1], a[1], bq[1], out + it.rstep, LncMask<true>());
+    } else {
+      row_dx(i, mean[0], rstd[0], a[0], bq[0], out, LncMask<false>());
+      if (two) row_dx(i + 1, mean[1], rstd[1], a[1], bq[1], out + it.rstep, LncMask<false>());
     }
   }
+  if (dead && threadIdx.x == 0) ring.drain(it.nr, p.err);
 }
 
 template <int DT>
