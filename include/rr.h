@@ -55,9 +55,13 @@
  *     16-byte block (every chunk then an aligned 16-byte block), where measured
  *     faster.  RR_SMX=0 (softmax family) and RR_LNX=0 (LayerNorm / RMSNorm)
  *     turn them off, RR_LNP=0/1 and RR_SMB=1 choose among their variants (tests
- *     and tuning; read at every call).  Results agree within the tolerances of
- *     the operation whichever kernel runs; they are not bit-identical across
- *     kernels.
+ *     and tuning; read at every call).  LayerNorm / RMSNorm rows of at least
+ *     64 KB with no forced tier run on column-block kernels (row statistics in
+ *     one launch, the outputs in the next; the forward keeps its per-block
+ *     statistics in y until it writes y, so it takes them only when y does not
+ *     overlap x); RR_LNC=0 turns those off and RR_LNC_MIN (bytes) moves their
+ *     threshold.  Results agree within the tolerances of the operation
+ *     whichever kernel runs; they are not bit-identical across kernels.
  */
 #ifndef RR_H
 #define RR_H
@@ -201,18 +205,20 @@ rr_status rr_layernorm_bwd(const void *dy, const void *x, const float *mean,
  *   ms = (1/C) sum_j x_j^2,  rstd = 1 / sqrt(ms + eps),  y_j = x_j * rstd * gamma_j.
  *   x, y : [rows x cols] dtype (y == x allowed).  gamma : [cols] dtype.
  *   rstd : [rows] float32 output, saved for rr_rmsnorm_bwd.  eps : >= 0, finite.
- * A row whose mean square is not finite is masked: y = 0, rstd = 0.  Rows must
- * fit one row group of threads or a thread-block cluster of up to 8 row groups
- * (at least 65537 columns for fp32 and bf16, in every alignment); longer rows
- * return RR_ERR_INVALID_ARG.
+ * A row whose mean square is not finite is masked: y = 0, rstd = 0.  Rows of
+ * any length run where x and y share their address modulo 16 and do not
+ * overlap (the column-block kernels); otherwise rows must fit one row group of
+ * threads or a thread-block cluster of up to 8 row groups (at least 65537
+ * columns for fp32 and bf16, in every alignment), and longer rows return
+ * RR_ERR_INVALID_ARG.
  */
 rr_status rr_rmsnorm_fwd(const void *x, const void *gamma, void *y, float *rstd,
                          int64_t rows, int64_t cols, float eps, rr_dtype dtype,
                          cudaStream_t stream);
 
 /* Bytes of device workspace rr_rmsnorm_bwd needs for (rows, cols, dtype); 0 if
- * the arguments are invalid or the rows are too long.  Depends on the current
- * device. */
+ * the arguments are invalid or no kernel holds the rows.  Depends on the
+ * current device. */
 size_t rr_rmsnorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtype);
 
 /*
@@ -225,10 +231,12 @@ size_t rr_rmsnorm_bwd_workspace_size(int64_t rows, int64_t cols, rr_dtype dtype)
  *   (16-byte aligned), owned by the caller; its contents on entry are ignored.
  * A row with rstd == 0 gets dx = 0 and adds nothing to dgamma, which is summed
  * over rows in a fixed order (deterministic for a given device and shape).
- * Rows must fit one row group (at least 8192 columns) or, with 16-byte
- * aligned gamma, a thread-block cluster of up to 8 row groups (beyond 65536
- * columns for fp32 and bf16); longer rows return RR_ERR_INVALID_ARG (and the
- * size query returns 0 when no alignment mode holds them).
+ * Rows of any length run where dy, x and dx share their address modulo 16
+ * (the column-block kernels); otherwise rows must fit one row group (at least
+ * 8192 columns) or, with 16-byte aligned gamma, a thread-block cluster of up
+ * to 8 row groups (beyond 65536 columns for fp32 and bf16), and longer rows
+ * return RR_ERR_INVALID_ARG (the size query returns 0 when no kernel holds
+ * them).
  */
 rr_status rr_rmsnorm_bwd(const void *dy, const void *x, const float *rstd,
                          const void *gamma, void *dx, void *dgamma, void *workspace,

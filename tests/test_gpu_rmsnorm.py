@@ -1,8 +1,9 @@
 """GPU parity of RMSNorm forward / backward (rr_rmsnorm_fwd, rr_rmsnorm_bwd)
 against the float64 oracle, through the C ABI: row lengths across the
 row-group sizes and their boundaries, ragged last chunks, misaligned tensors,
-masked rows and +-1e4 outliers, a chained GPU-forward-into-backward check, and
-the rejection of rows longer than one row group holds."""
+masked rows and +-1e4 outliers, a chained GPU-forward-into-backward check,
+rows of any length on the column-block kernels, and the rejection of rows
+beyond a cluster of row groups where those kernels are off."""
 import numpy as np
 import pytest
 import torch
@@ -56,11 +57,16 @@ def test_rmsnorm_chained_gpu_statistics(dtype):
     check_rms(x, g, dy, 1e-5, dtype, oracle_stats=False)
 
 
+@pytest.mark.parametrize("kern", ["routed", "clusters"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("cols", [16385, 40000, 65537])
 @pytest.mark.parametrize("pad", [(0, 0, 0, 0, 0), (1, 1, 0, 0, 0), (0, 0, 1, 0, 0)])
-def test_rmsnorm_fwd_clustered_rows(cols, dtype, pad):
-    """Forward rows longer than one row group are split over a thread-block cluster."""
+def test_rmsnorm_fwd_clustered_rows(cols, dtype, pad, kern, monkeypatch):
+    """Forward rows longer than one row group: split over a thread-block
+    cluster (RR_LNC=0), or routed (the column-block kernels for rows of 64 KB
+    and more whose x and y share their address modulo 16)."""
+    if kern == "clusters":
+        monkeypatch.setenv("RR_LNC", "0")
     x, g, _ = case(64, cols, dtype, 990 + cols)
     xd, gd = to_dev(x, pad[0]), to_dev(g, pad[2])
     y = empty_like_dev(x.shape, dtype, pad[1])
@@ -74,7 +80,18 @@ def test_rmsnorm_fwd_clustered_rows(cols, dtype, pad):
     compare("rms rstd (clustered)", host(rstd), rrstd, *TOL_F32_OUT)
 
 
-def test_rmsnorm_rejects_rows_beyond_its_kernels():
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rmsnorm_rows_beyond_a_cluster(dtype):
+    """Rows beyond a cluster of 8 row groups (300000 columns): the column-block
+    kernels take them, forward and backward, against the oracle."""
+    x, g, dy = case(5, 300000, dtype, 1300)
+    check_rms(x, g, dy, 1e-5, dtype)
+
+
+def test_rmsnorm_rejects_rows_beyond_its_kernels(monkeypatch):
+    """With the column-block kernels off, rows beyond a cluster of row groups
+    are refused (and the workspace query answers 0)."""
+    monkeypatch.setenv("RR_LNC", "0")
     dev = torch.device("cuda", 0)
     x = torch.zeros(2, 300000, device=dev)          # beyond a cluster of 8 row groups
     g = torch.ones(300000, device=dev)

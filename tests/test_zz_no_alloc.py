@@ -80,11 +80,13 @@ def test_noalloc_matches_workspace_variant_twice(rows, cols, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_noalloc_longest_supported_rows(dtype):
-    """The longest rows the LayerNorm backward holds (found through the
-    workspace size query, which returns 0 for rows no kernel holds): the
+def test_noalloc_longest_supported_rows(dtype, monkeypatch):
+    """The longest rows the LayerNorm backward holds without the column-block
+    kernels (which take rows of any length; RR_LNC=0 here), found through the
+    workspace size query, which returns 0 for rows no kernel holds: the
     scratch then carries the fewest column partials.  One column beyond, both
     entry points refuse the shape with the same status."""
+    monkeypatch.setenv("RR_LNC", "0")
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     lo, hi = 65537, 1 << 20            # supported / not (one partial is 8 MiB at 2^20)
     assert rr.rr_layernorm_bwd_workspace_size(3, lo, tdt) > 0
@@ -116,3 +118,12 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     st = lib.rr_layernorm_bwd_noalloc(*fake, rows, cols, 0, ctypes.c_void_p(0))
     assert st == 4                        # RR_ERR_WORKSPACE_TOO_SMALL
     assert b"8 MiB" in lib.rr_last_error_detail()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_noalloc_column_block_rows(dtype):
+    """Rows the column-block kernels take (255 x 65537, the sweep's longest):
+    the no-allocation entry point fits their column partials and row records
+    in its scratch (with fewer row groups where needed); both entry points
+    agree with the oracle."""
+    _check_twice(255, 65537, dtype, 7)
