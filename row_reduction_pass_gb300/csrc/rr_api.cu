@@ -760,14 +760,16 @@ rr_status lnx_plan(OpKind op, rr_dtype dt, int64_t rows, int64_t cols, Plan* pl,
 // Column-block LayerNorm / RMSNorm kernels for very long rows (rr_lnc.cuh):
 // statistics, then outputs, in separate launches over (class, column block,
 // row group) items, so every SM streams from the first microsecond instead of
-// waiting on a row per block or cluster (bf16 255 x 65537: see the design
-// notes for the numbers).  Taken for rows of at least kLncMinBytes when no
-// tier is forced; RR_LNC=0 turns them off, RR_LNC_MIN (bytes) moves the
-// threshold (tuning aids).  Items: as many row groups per class as keep the
+// waiting on a row per block or cluster.  Taken when no tier is forced for
+// rows of at least 64 KB, and for the LayerNorm backward from 8 KB (bf16 4097
+// columns 55.1 -> 49.5 us, fp32 63.1 -> 55.4 us; the forwards and the RMSNorm
+// backward lost there to the phase-class kernels: bf16 LayerNorm forward 38.4
+// against 26.6 us); RR_LNC=0 turns them off, RR_LNC_MIN (bytes) sets one
+// threshold for all (tuning aids).  Items: as many row groups per class as keep the
 // blocks within one wave (5 blocks per SM: registers, 32 KB copy rings), so each
 // block streams as many rows as it can; each backward row group adds a
 // column-partial row for the column reduce to read.
-constexpr int64_t kLncMinBytes = 64 * 1024;
+constexpr int64_t kLncMinBytes = 64 * 1024, kLncMinBytesLnBwd = 8192;
 
 const rr::LncKernels& lnc_kernels(rr_dtype dt);
 
@@ -784,7 +786,7 @@ rr_status lnc_plan(bool bwd, bool rms, rr_dtype dt, int64_t rows, int64_t cols, 
   if (const char* f = std::getenv("RR_LNC"); f != nullptr && f[0] == '0')
     return fail(RR_ERR_INVALID_ARG, "column-block kernels off");
   const int E = dt == RR_BF16 ? 2 : 4, W = 16 / E;
-  int64_t min_bytes = kLncMinBytes;
+  int64_t min_bytes = bwd && !rms ? kLncMinBytesLnBwd : kLncMinBytes;
   if (const char* f = std::getenv("RR_LNC_MIN")) min_bytes = std::max<int64_t>(16, std::atoll(f));
   if (cols * E < min_bytes || rows < 1) return fail(RR_ERR_INVALID_ARG, "rows too short");
   int sms = 0;
@@ -808,8 +810,11 @@ rr_status lnc_plan(bool bwd, bool rms, rr_dtype dt, int64_t rows, int64_t cols, 
     while (b) { const int64_t t = a % b; a = b; b = t; }
     P = 16 / a;
   }
-  const int64_t cb = 32 * rr::kLncWarps * (bwd ? rr::kLncCplBwd : rr::kLncCplFwd);
-  const int64_t nb = cdiv(cdiv(cols + W - 1, W), cb);
+  // column blocks of at most cbmax chunks, all of a row's blocks equal
+  const int64_t cbmax = 32 * rr::kLncWarps * (bwd ? rr::kLncCplBwd : rr::kLncCplFwd);
+  const int64_t nch_max = cdiv(cols + W - 1, W);
+  const int64_t nb = cdiv(nch_max, cbmax);
+  const int64_t cb = cdiv(nch_max, nb);
   const int64_t per_class = cdiv(rows, P);
   const int64_t slots = 5 * (int64_t)sms;
   int64_t ng = std::min<int64_t>(per_class, std::max<int64_t>(1, slots / (P * nb)));
@@ -822,7 +827,7 @@ rr_status lnc_plan(bool bwd, bool rms, rr_dtype dt, int64_t rows, int64_t cols, 
     const size_t ws = bwd ? ((part + 15) & ~size_t(15)) + rec : 0;
     if (ng > 1 && bwd && (P * g2 > max_partials || ws > ws_limit)) continue;
     if (P * nb * g2 > INT32_MAX) return fail(RR_ERR_INVALID_ARG, "too many column blocks");
-    lp->geo = rr::LncGeo{rows, cols, (int32_t)P, (int32_t)nb, (int32_t)g2, (int32_t)rg,
+    lp->geo = rr::LncGeo{rows, cols, (int32_t)P, (int32_t)nb, (int32_t)g2, (int32_t)rg, (int32_t)cb,
                          (int64_t)(((part + 15) & ~size_t(15)) / sizeof(float))};
     lp->items = P * nb * g2;
     lp->partials = P * g2;

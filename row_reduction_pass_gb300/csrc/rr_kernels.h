@@ -95,6 +95,7 @@ struct LncGeo {
   int32_t nb;       // column blocks of kCB chunks
   int32_t ng;       // row groups per class
   int32_t rg;       // rows per group (of its class)
+  int32_t cb;       // chunks per column block (<= 32 * kLncWarps * CPL)
   int64_t rec_off;  // backward: floats from the workspace to the (S1, S2) records
 };
 constexpr int kLncWarps = 4;    // warps per block (128 threads)

@@ -8,11 +8,11 @@
 // start at the same offset phi within their first aligned 16-byte chunk), so
 // chunk k of a row of class c is an aligned 16-byte block whose lane e is
 // column k * W + e - phi.  A work item is (class, column block b, row group):
-// chunks [b * CB, b * CB + CB) of the rows of the class in the group.  Warp w
-// of the block takes chunks b * CB + 32 * CPL * w + lane + 32 * j (j < CPL) of
-// each of the item's rows in turn: the warps stream different columns of the
-// same rows, and no thread ever waits for another block -- the launches order
-// the phases.  Rows of a few hundred thousand bytes then keep every SM busy
+// chunks [b * CB, b * CB + CB) of the rows of the class in the group, CB at
+// most 128 CPL and chosen so the blocks of a row are equal.  Thread t of the
+// block takes chunks b * CB + t + 128 j (j < CPL) of each of the item's rows in
+// turn: the threads stream different columns of the same rows, and no thread
+// ever waits for another block -- the launches order the phases.  Rows of a few hundred thousand bytes then keep every SM busy
 // (a row per block or per cluster leaves most SMs idle or waiting), and the
 // second launch reads its inputs again from L2, where the first left them.
 //
@@ -50,9 +50,11 @@
 namespace rr {
 
 constexpr int kLncThreads = 32 * kLncWarps;
+constexpr int kLncStride = 16 * kLncThreads;  // bytes between a thread's chunks j, j + 1
 
 // A block's work item and its view of the rows: rows r0 + i P (i < nr) of
-// the class; this lane's chunks k0 + 32 j (j < CPL) of each.
+// the class; this thread's chunks k0 + 128 j (j < CPL, within the block) of
+// each.
 template <int W, int CPL>
 struct LncItem {
   int cls, b, grp;
@@ -60,7 +62,7 @@ struct LncItem {
   int64_t r0;       // first row of the item
   int nr;           // its rows
   int64_t rstep;    // bytes from one of its rows to the next (P rows)
-  int64_t off0;     // bytes from a row's start to this lane's chunk j = 0
+  int64_t off0;     // bytes from a row's start to this thread's chunk j = 0
   int lo[CPL], hi[CPL];  // valid lanes [lo, hi) of chunk j (empty outside the row)
 
   __device__ __forceinline__ void init(const LncGeo& g, const char* base, int E) {
@@ -79,25 +81,27 @@ struct LncItem {
     r0 = cls + (int64_t)g.P * first;
     nr = static_cast<int>(first < in_class ? (in_class - first < g.rg ? in_class - first : g.rg) : 0);
     rstep = (int64_t)g.P * rowb;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t k0 = (int64_t)b * (32 * CPL * kLncWarps) + 32 * CPL * warp + lane;
+    const int64_t k0 = (int64_t)b * g.cb + threadIdx.x;
     off0 = k0 * 16 - (int64_t)phi * E;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
-      const int64_t k = k0 + 32 * j;
+      const int64_t k = k0 + kLncThreads * j;
       lo[j] = k == 0 ? phi : 0;
       hi[j] = k == nch - 1 ? tail : W;
-      if (k >= nch) lo[j] = hi[j] = 0;
+      if (k >= nch || (int)threadIdx.x + kLncThreads * j >= g.cb) lo[j] = hi[j] = 0;
     }
   }
-  // This lane's chunk 0 in row i of the item (chunk j is 512 j bytes on).
+  // This thread's chunk 0 in row i of the item (chunk j is kLncStride j bytes
+  // on).
   __device__ __forceinline__ const char* at_row(const char* base, int i, const LncGeo& g,
                                                 int64_t rowb) const {
     return base + (r0 + (int64_t)i * g.P) * rowb + off0;
   }
   __device__ __forceinline__ bool has(int j) const { return hi[j] > lo[j]; }
   // Column of lane 0 of chunk j (negative for the lanes before the row).
-  __device__ __forceinline__ int64_t col0(int j, int E) const { return (off0 + 512 * j) / E; }
+  __device__ __forceinline__ int64_t col0(int j, int E) const {
+    return (off0 + (int64_t)kLncStride * j) / E;
+  }
 };
 
 // The W values src[col0, col0 + W) of a [cols] vector as fp32, 0 outside
@@ -184,18 +188,18 @@ __device__ __forceinline__ uint64_t lnc_policy_evict_last() {
 
 // A block's ring of kLncDepth row stages in dynamic shared memory: stage
 // i mod depth holds the block's chunks of row i of the item for T tensors,
-// brought by one 1-D bulk copy (TMA) per tensor that thread 0 issues depth - 1
-// rows ahead, completing on the stage's mbarrier; every thread waits for the
-// stage's phase (bounded) and reads its own chunks.  Thread 0 refills a stage
-// only after a block barrier that follows every thread's last read of it.
-// Bulk copies keep ~56 KB per block in flight without per-thread request
-// slots (per-thread 16-byte copies capped these kernels at ~2.4 TB/s).
-// Reads: this thread's chunk j of the stage is local chunk 32 CPL warp + lane
-// + 32 j.  K1 kernels (whose data the next launch reads again) mark the lines
-// evict-last in L2, K2 kernels evict-first.
+// brought by one 1-D bulk copy (TMA) per tensor that thread 0 issues two rows
+// (a pair) ahead, completing on the stage's mbarrier; every thread waits for
+// the stage's phase (bounded) and reads its own chunks.  Thread 0 refills a
+// stage only after a block barrier that follows every thread's last read of
+// it.  Bulk copies keep the rows in flight without per-thread request slots
+// (per-thread 16-byte copies capped these kernels at ~2.4 TB/s).  Reads: this
+// thread's chunk j of the stage is local chunk t + 128 j.  K1 kernels (whose
+// data the next launch reads again) mark the lines evict-last in L2, K2
+// kernels evict-first.
 template <int T, int CPL>
 struct LncBulk {
-  static constexpr int kCB = 32 * CPL * kLncWarps;  // chunks of a block's row
+  static constexpr int kCB = kLncThreads * CPL;  // chunks of a stage (a block has at most these)
   uint4* ring;
   uint64_t* bars;
   uint64_t policy;
@@ -214,19 +218,19 @@ struct LncBulk {
     const int64_t rowb = g.cols * E;
     const int64_t phi_b = (int64_t)it.phi * E;
     const int64_t nch = (phi_b + rowb + 15) / 16;
-    const int64_t kb = (int64_t)it.b * kCB;
-    const int64_t n = nch - kb < kCB ? nch - kb : kCB;
+    const int64_t kb = (int64_t)it.b * g.cb;
+    const int64_t n = nch - kb < g.cb ? nch - kb : g.cb;
     bytes = n > 0 ? static_cast<uint32_t>(n) * 16 : 0u;
 #pragma unroll
     for (int t = 0; t < T; ++t) nxt[t] = base[t] + it.r0 * rowb - phi_b + kb * 16;
     issued = 0;
-    local = 32 * CPL * (threadIdx.x >> 5) + (threadIdx.x & 31);
+    local = threadIdx.x;
   }
   __device__ __forceinline__ uint4* stage(int i, int t) const {
     return ring + ((i & (kLncDepth - 1)) * T + t) * kCB;
   }
   __device__ __forceinline__ const uint4& at(int i, int t, int j) const {
-    return stage(i, t)[local + 32 * j];
+    return stage(i, t)[local + kLncThreads * j];
   }
   // Thread 0: the next row's copies (none past the item's rows).
   __device__ __forceinline__ void issue(int nr, int64_t rstep) {
@@ -493,8 +497,8 @@ __global__ void __launch_bounds__(kLncThreads, 5) lnc_norm_kernel(const LnFwdPar
           }
         }
       }
-      if constexpr (M) lnc_store<DT, W>(out + 512 * j, it.lo[j], it.hi[j], y);
-      else st_chunk_stream(out + 512 * j, chunk_pack<DT>(y));
+      if constexpr (M) lnc_store<DT, W>(out + kLncStride * j, it.lo[j], it.hi[j], y);
+      else st_chunk_stream(out + kLncStride * j, chunk_pack<DT>(y));
     }
   };
   char* out = const_cast<char*>(it.at_row(p.y, 0, g, rowb));
@@ -697,8 +701,8 @@ __global__ void __launch_bounds__(kLncThreads, 6) lnc_bwd_dx_kernel(const LnBwdP
           mul2(o[e], o[e + 1], t0, t1b, rstd, rstd);
         }
       }
-      if constexpr (M) lnc_store<DT, W>(out + 512 * j, it.lo[j], it.hi[j], o);
-      else st_chunk_stream(out + 512 * j, chunk_pack<DT>(o));
+      if constexpr (M) lnc_store<DT, W>(out + kLncStride * j, it.lo[j], it.hi[j], o);
+      else st_chunk_stream(out + kLncStride * j, chunk_pack<DT>(o));
     }
   };
   char* out = const_cast<char*>(it.at_row(p.dx, 0, g, rowb));

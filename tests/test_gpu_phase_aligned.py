@@ -155,7 +155,7 @@ def test_xent_custom_ignore_index_and_all_rows_ignored():
 # LayerNorm / RMSNorm on the same phase counts, bases and cluster splits
 LN_SHAPES = [("bf16", 4097, 40), ("bf16", 4102, 11), ("f32", 2050, 13), ("f32", 2052, 4),
              ("bf16", 65537, 4), ("f32", 40001, 3), ("bf16", 32771, 21), ("bf16", 32768, 6),
-             ("f32", 16387, 9)]
+             ("f32", 16387, 9), ("f32", 16389, 1), ("bf16", 32772, 2)]
 
 
 # routed (default: the column-block kernels for rows of 64 KB and more), the
