@@ -56,11 +56,11 @@
  *     faster.  RR_SMX=0 (softmax family) and RR_LNX=0 (LayerNorm / RMSNorm)
  *     turn them off, RR_LNP=0/1 and RR_SMB=1 choose among their variants (tests
  *     and tuning; read at every call).  LayerNorm / RMSNorm rows of at least
- *     64 KB with no forced tier run on column-block kernels (row statistics in
- *     one launch, the outputs in the next; the forward keeps its per-block
- *     statistics in y until it writes y, so it takes them only when y does not
- *     overlap x); RR_LNC=0 turns those off and RR_LNC_MIN (bytes) moves their
- *     threshold.  Results agree within the tolerances of the operation
+ *     64 KB (LayerNorm backward: 8 KB) with no forced tier run on column-block
+ *     kernels (row statistics in one launch, the outputs in the next; the
+ *     forward keeps its per-block statistics in y until it writes y, so it
+ *     takes them only when y does not overlap x); RR_LNC=0 turns those off and
+ *     RR_LNC_MIN (bytes) sets their threshold.  Results agree within the tolerances of the operation
  *     whichever kernel runs; they are not bit-identical across kernels.
  */
 #ifndef RR_H
