@@ -816,7 +816,10 @@ rr_status lnc_plan(bool bwd, bool rms, rr_dtype dt, int64_t rows, int64_t cols, 
   const int64_t nb = cdiv(nch_max, cbmax);
   const int64_t cb = cdiv(nch_max, nb);
   const int64_t per_class = cdiv(rows, P);
-  const int64_t slots = 5 * (int64_t)sms;
+  // RR_LNC_SLOTS: blocks per SM the item count aims at (tuning aid)
+  int64_t per_sm = 5;
+  if (const char* f = std::getenv("RR_LNC_SLOTS")) per_sm = std::max(1, std::atoi(f));
+  const int64_t slots = per_sm * (int64_t)sms;
   int64_t ng = std::min<int64_t>(per_class, std::max<int64_t>(1, slots / (P * nb)));
   for (;; --ng) {
     const int64_t rg = cdiv(per_class, ng);
