@@ -60,8 +60,16 @@
  *     kernels (row statistics in one launch, the outputs in the next; the
  *     forward keeps its per-block statistics in y until it writes y, so it
  *     takes them only when y does not overlap x); RR_LNC=0 turns those off and
- *     RR_LNC_MIN (bytes) sets their threshold.  Results agree within the tolerances of the operation
- *     whichever kernel runs; they are not bit-identical across kernels.
+ *     RR_LNC_MIN (bytes) sets their threshold.  Rows of one column with no
+ *     forced tier run on elementwise kernels (a one-element row is its own
+ *     maximum, sum and moments); RR_ONE=0 turns those off.  Results agree
+ *     within the tolerances of the operation whichever kernel runs; they are
+ *     not bit-identical across kernels.
+ *   - Softmax family range: the exponentials are taken as
+ *     2^(x log2 e - fl(m log2 e)) times 2^(-r), r the rounding residual of
+ *     fl(m log2 e) (m the row maximum).  For |m| >= 2^30 that residual can
+ *     leave the float32 exponent range, and the row's outputs can then be NaN;
+ *     finite logits below 2^30 in magnitude are always in range.
  */
 #ifndef RR_H
 #define RR_H

@@ -1004,6 +1004,72 @@ rr_status span_launch(const P& p, rr_dtype dt, int mode, int64_t rows, int64_t c
   return span_launch(p, sp, stream);
 }
 
+// Rows of one column (rr_one.cuh): elementwise kernels over tiles of
+// kOneThreads x (16 / E) rows; as many blocks as are resident on the SMs at
+// once (each takes further tiles in turn), at most max_grid (the norm backward
+// writes one column partial per block).  Taken when no tier is forced; RR_ONE=0
+// turns it off (tuning aid).
+struct OnePlan {
+  const void* fn = nullptr;
+  int64_t grid = 0;
+};
+
+static const rr::OneKernels& one_kernels(rr_dtype dt) {
+  static const rr::OneKernels f32 = rr::one_kernels_f32();
+  static const rr::OneKernels bf16 = rr::one_kernels_bf16();
+  return dt == RR_BF16 ? bf16 : f32;
+}
+
+static bool one_eligible(int64_t rows, int64_t cols) {
+  if (cols != 1 || rows <= 0 || forced_tier() != -1) return false;
+  const char* f = std::getenv("RR_ONE");
+  return f == nullptr || f[0] != '0';
+}
+
+static rr_status one_plan(const void* fn, rr_dtype dt, int64_t rows, int64_t max_grid,
+                          OnePlan* op) {
+  if (max_grid < 1) return RR_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo* di = nullptr;
+  rr_status st = device_info(&di);
+  if (st != RR_OK) return st;
+  const int T = rr::kOneThreads;
+  int& occ = di->occ[{fn, (long long)T << 32}];
+  if (occ == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, T, 0);
+    if (e != cudaSuccess || occ <= 0)
+      return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+  }
+  const int64_t E = dt == RR_BF16 ? 2 : 4;
+  int64_t grid = cdiv(rows, T * (16 / E));
+  const int64_t resident = (int64_t)di->sms * occ;
+  if (grid > resident) grid = resident;
+  if (grid > max_grid) grid = max_grid;
+  op->fn = fn;
+  op->grid = grid;
+  return RR_OK;
+}
+
+template <class P>
+rr_status one_launch(const P& p, const OnePlan& op, int64_t rows, cudaStream_t stream) {
+  P pc = p;
+  int64_t n = rows;
+  void* args[] = {&pc, &n};
+  cudaError_t e =
+      cudaLaunchKernel(op.fn, dim3((unsigned)op.grid), dim3(rr::kOneThreads), args, 0, stream);
+  if (e != cudaSuccess) return fail(RR_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return RR_OK;
+}
+
+template <class P>
+rr_status one_run(const P& p, const void* fn, rr_dtype dt, int64_t rows, cudaStream_t stream) {
+  OnePlan op;
+  rr_status st = one_plan(fn, dt, rows, INT64_MAX, &op);
+  if (st != RR_OK) return st;
+  if ((st = one_launch(p, op, rows, stream)) != RR_OK) return st;
+  return ok();
+}
+
 template <class P>
 rr_status launch(const Plan& pl, const P& params, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -1101,6 +1167,8 @@ static rr_status softmax_fwd_impl(const void* x, void* y, int64_t rows, int64_t 
                       err, cols, 0, log};
   const int ft = forced_tier();
   if (ft == -2) return bad_tier();
+  if (one_eligible(rows, cols))
+    return one_run(p, one_kernels(dtype).fwd[log ? 1 : 0], dtype, rows, stream);
   if (ft <= 0 && aligned(x, 16) && aligned(y, 16)) {
     st = span_launch(p, dtype, log ? 1 : 0, rows, cols, false, stream);
     if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
@@ -1154,6 +1222,8 @@ static rr_status softmax_bwd_impl(const void* y, const void* dy, void* dx, int64
                          static_cast<char*>(dx), err, cols, log};
   const int ft = forced_tier();
   if (ft == -2) return bad_tier();
+  if (one_eligible(rows, cols))
+    return one_run(p, one_kernels(dtype).bwd[log ? 1 : 0], dtype, rows, stream);
   if (ft <= 0 && same && a == 0) {
     st = span_launch(p, dtype, log ? 4 : 3, rows, cols, false, stream);
     if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
@@ -1211,6 +1281,7 @@ rr_status rr_softmax_xent_fwd_bwd(const void* logits, const int32_t* labels, flo
                       bad_label_count, err, cols, ignore_index};
   const int ft = forced_tier();
   if (ft == -2) return bad_tier();
+  if (one_eligible(rows, cols)) return one_run(p, one_kernels(dtype).fwd[2], dtype, rows, stream);
   if (ft <= 0 && aligned(logits, 16) && aligned(dlogits, 16)) {
     st = span_launch(p, dtype, 2, rows, cols, aligned(labels, 16), stream);
     if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
@@ -1259,6 +1330,8 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
     rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma),
                       static_cast<const char*>(beta), static_cast<char*>(y), mean, rstd, err, cols,
                       eps, static_cast<float>(1.0 / static_cast<double>(cols))};
+    if (one_eligible(rows, cols))
+      return one_run(p, one_kernels(dtype).norm_fwd[0], dtype, rows, stream);
     if (ft <= 0 && aligned(x, 16) && aligned(y, 16)) {
       st = span_launch(p, dtype, 5, rows, cols, false, stream);
       if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
@@ -1329,6 +1402,8 @@ rr_status rr_rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
     rr::LnFwdParams p{static_cast<const char*>(x), static_cast<const char*>(gamma), nullptr,
                       static_cast<char*>(y), nullptr, rstd, err, cols, eps,
                       static_cast<float>(1.0 / static_cast<double>(cols))};
+    if (one_eligible(rows, cols))
+      return one_run(p, one_kernels(dtype).norm_fwd[1], dtype, rows, stream);
     if (ft <= 0 && aligned(x, 16) && aligned(y, 16)) {
       st = span_launch(p, dtype, 6, rows, cols, false, stream);
       if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
@@ -1423,6 +1498,12 @@ static size_t norm_bwd_workspace_size(bool rms, int64_t rows, int64_t cols, rr_d
     LncPlan lp;
     if (lnc_plan(true, rms, dtype, rows, cols, &lp) == RR_OK && lp.ws_bytes > best) best = lp.ws_bytes;
   }
+  OnePlan op;  // rows of one column: one partial per block
+  if (one_eligible(rows, cols) &&
+      one_plan(one_kernels(dtype).norm_bwd[rms], dtype, rows, INT64_MAX, &op) == RR_OK) {
+    const size_t ws = (size_t)op.grid * (rms ? 1 : 2) * sizeof(float);
+    if (ws > best) best = ws;
+  }
   SpanPlan sp;  // short rows with 16-byte aligned tensors: one partial per span block
   if (forced_tier() <= 0 && span_plan(dtype, rms ? 8 : 7, rows, cols, false, INT64_MAX, &sp) == RR_OK) {
     const size_t ws = (size_t)sp.grid * (rms ? 1 : 2) * (size_t)cols * sizeof(float);
@@ -1514,12 +1595,24 @@ static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* 
     SpanPlan sp;
     st = RR_ERR_INVALID_ARG;
     const int ft = forced_tier();
-    if (ft <= 0 && aligned(dy, 16) && aligned(x, 16) && aligned(dx, 16)) {
+    // rows of one column: elementwise, one partial per block
+    OnePlan op;
+    const bool one = one_eligible(rows, cols);
+    if (one &&
+        (st = one_plan(one_kernels(dtype).norm_bwd[rms], dtype, rows, max_partials, &op)) != RR_OK)
+      return st;
+    if (!one && ft <= 0 && aligned(dy, 16) && aligned(x, 16) && aligned(dx, 16)) {
       const bool stats_al = aligned(rstd, 16) && (rms || aligned(mean, 16));
       st = span_plan(dtype, rms ? 8 : 7, rows, cols, stats_al, max_partials, &sp);
       if (st != RR_OK && st != RR_ERR_INVALID_ARG) return st;
     }
-    if (st == RR_OK) {
+    if (one) {
+      need = (size_t)op.grid * planes * sizeof(float);
+      if (workspace_bytes < need)
+        return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+      if ((st = one_launch(p, op, rows, stream)) != RR_OK) return st;
+      pl.partials = op.grid;
+    } else if (st == RR_OK) {
       need = (size_t)sp.grid * planes * (size_t)cols * sizeof(float);
       if (workspace_bytes < need)
         return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);

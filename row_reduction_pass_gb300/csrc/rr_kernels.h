@@ -117,6 +117,20 @@ struct LncKernels {
 LncKernels lnc_kernels_f32();
 LncKernels lnc_kernels_bf16();
 
+// Rows of one column (rr_one.cuh), elementwise: fwd [mode] 0 softmax,
+// 1 log-softmax, 2 cross-entropy; bwd [log]; norm_fwd / norm_bwd [rms].
+// Blocks of kOneThreads threads; the norm backward writes one partial
+// (planes floats) per block.
+constexpr int kOneThreads = 256;
+struct OneKernels {
+  const void* fwd[3];
+  const void* bwd[2];
+  const void* norm_fwd[2];
+  const void* norm_bwd[2];
+};
+OneKernels one_kernels_f32();
+OneKernels one_kernels_bf16();
+
 // Short-row span kernels (rr_span.cuh): [dtype][mode], mode 0 softmax,
 // 1 log-softmax, 2 cross-entropy, 3 softmax backward, 4 log-softmax backward,
 // 5 LayerNorm forward, 6 RMSNorm forward, 7 LayerNorm backward, 8 RMSNorm
