@@ -100,6 +100,9 @@ struct RowGeo {
   __device__ __forceinline__ bool has(int q) const { return q < nq; }
   __device__ __forceinline__ int col(int q, int e) const { return colbase + chunk(q) * W + e; }
   __device__ __forceinline__ bool full(int q) const { return q >= qlo && q < qhi; }
+  // Every chunk this thread owns is full (rows without a ragged head or tail):
+  // loads and stores can skip the per-chunk checks.
+  __device__ __forceinline__ bool all_full() const { return qlo == 0 && qhi >= nq; }
   __device__ __forceinline__ bool valid(int q, int e) const {
     const int j = col(q, e);
     return j >= c0 && j < c1;
@@ -188,6 +191,19 @@ __device__ __forceinline__ void load_direct_mem(RowRegs<DT, W, NT, NQ>& r, int t
                                             const RowGeo<DT, W>& g, const char* g0,
                                             float fill) {
   constexpr int E = DType<DT>::E;
+  // rows without a ragged head or tail: no per-chunk checks (variants of
+  // several chunks per thread; in the two-chunk ones, which also hold the next
+  // row, the second copy of the loop costs registers)
+  if constexpr (W > 1 && NQ > 2) {
+    if (g.all_full()) {
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (!g.has(q)) break;
+        r.v[t][q] = ld_chunk_stream(g0 + g.off(q));
+      }
+      return;
+    }
+  }
 #pragma unroll
   for (int q = 0; q < NQ; ++q) {
     if (!g.has(q)) break;
@@ -217,6 +233,16 @@ __device__ __forceinline__ void load_staged_mem(RowRegs<DT, W, NT, NQ>& r, int t
                                             const unsigned char* sbuf, float fill) {
   constexpr int E = DType<DT>::E;
   const uint64_t a = reinterpret_cast<uint64_t>(g0);
+  if constexpr (W > 1) {
+    if (g.all_full()) {
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (!g.has(q)) break;
+        r.v[t][q] = *reinterpret_cast<const uint4*>(sbuf + g.off(q));
+      }
+      return;
+    }
+  }
 #pragma unroll
   for (int q = 0; q < NQ; ++q) {
     if (!g.has(q)) break;

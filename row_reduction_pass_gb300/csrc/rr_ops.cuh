@@ -343,6 +343,7 @@ struct OpSoftmaxXent {
     char* y0 = p.y + (r * p.cols + g.c0) * E - g.head_bytes;
     const bool masked = (s.m == -INFINITY);
     int ql = -1, el = 0;  // where this thread holds the label column, if it does
+    float xl = 0.f;       // and the logit there
     if (p.labels != nullptr) {
       const int32_t label = mt.label;
       const bool in_range = label >= 0 && (int64_t)label < geo.cols;
@@ -354,7 +355,6 @@ struct OpSoftmaxXent {
       } else if (!in_range) {
         if (leader) p.loss[r] = __int_as_float(0x7fc00000);
       } else if (ql >= 0) {
-        float xl = 0.f;
 #pragma unroll
         for (int q = 0; q < NQ; ++q)
 #pragma unroll
@@ -372,13 +372,13 @@ struct OpSoftmaxXent {
       }
       return;
     }
+    // Rows without a ragged head or tail (every chunk full) take loops with
+    // no per-chunk checks; the label's element is then rewritten after its
+    // chunk (same thread, same address: the later store wins).
     if (p.log) {
       // z_j = (x_j - m) - ln d: x - m first, so z keeps its relative accuracy
       const float lnd = logf(s.d);
-#pragma unroll
-      for (int q = 0; q < NQ; ++q) {
-        if (!g.has(q)) break;
-        float f[W];
+      auto logs = [&](int q, float* f) {
         if constexpr (W > 1) {
 #pragma unroll
           for (int e = 0; e < W; e += 2) {
@@ -388,6 +388,24 @@ struct OpSoftmaxXent {
         } else {
           f[0] = (x.get(0, q, 0) - s.m) - lnd;
         }
+      };
+      if constexpr (W > 1) {
+        if (g.all_full()) {
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) {
+            if (!g.has(q)) break;
+            float f[W];
+            logs(q, f);
+            st_chunk_stream(y0 + g.off(q), chunk_pack<DT>(f));
+          }
+          return;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (!g.has(q)) break;
+        float f[W];
+        logs(q, f);
         g.store_chunk(y0, q, f);
       }
       return;
@@ -396,10 +414,7 @@ struct OpSoftmaxXent {
     const float mL = s.m * kLog2e;
     const float rr = fmaf(s.m, kLog2e, -mL);
     const float inv = ex2(-rr) / s.d;
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-      if (!g.has(q)) break;
-      float f[W];
+    auto probs = [&](int q, float* f) {
       if constexpr (W > 1) {
 #pragma unroll
         for (int e = 0; e < W; e += 2) {
@@ -410,6 +425,26 @@ struct OpSoftmaxXent {
       } else {
         f[0] = ex2(fmaf(x.get(0, q, 0), kLog2e, -mL)) * inv;
       }
+    };
+    if constexpr (W > 1) {
+      if (g.all_full()) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          if (!g.has(q)) break;
+          float f[W];
+          probs(q, f);
+          st_chunk_stream(y0 + g.off(q), chunk_pack<DT>(f));
+        }
+        if (ql >= 0)
+          st_elem<DT>(y0 + g.off(ql) + el * E, ex2(fmaf(xl, kLog2e, -mL)) * inv - 1.0f);
+        return;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (!g.has(q)) break;
+      float f[W];
+      probs(q, f);
       if (q == ql) {
 #pragma unroll
         for (int e = 0; e < W; ++e)
@@ -498,10 +533,7 @@ struct OpSoftmaxBwd {
     S = rd.cluster(S, MergeSum1());
     if (!active) return;
     char* dx0 = p.dx + (r * p.cols + g.c0) * E - g.head_bytes;
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-      if (!g.has(q)) break;
-      float f[W];
+    auto grads = [&](int q, float* f) {
       if constexpr (W > 1) {
 #pragma unroll
         for (int e = 0; e < W; e += 2) {
@@ -518,6 +550,27 @@ struct OpSoftmaxBwd {
         f[0] = p.log ? fmaf(ex2(v.get(0, q, 0) * kLog2e), -S.s, v.get(1, q, 0))
                      : v.get(0, q, 0) * (v.get(1, q, 0) - S.s);
       }
+    };
+    // rows without a ragged head or tail: no per-chunk checks on the stores
+    // (variants of several chunks per thread; in the two-chunk ones the second
+    // copy of the loop costs registers)
+    if constexpr (W > 1 && NQ > 2) {
+      if (g.all_full()) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          if (!g.has(q)) break;
+          float f[W];
+          grads(q, f);
+          st_chunk_stream(dx0 + g.off(q), chunk_pack<DT>(f));
+        }
+        return;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (!g.has(q)) break;
+      float f[W];
+      grads(q, f);
       g.store_chunk(dx0, q, f);
     }
   }
