@@ -766,10 +766,11 @@ def run_sweep(args):
         # take longer at the measured copy bandwidth than the two products at
         # the measured bf16 rate, so the line reports both and the fraction of
         # the larger floor (the roofline time) that the kernel reaches.
+        # Two more lines at 32 heads x 4096 queries, where the products
+        # outweigh the tensors' traffic and the tensor-core rate is the bound.
         tpk, tsrc = bf16_peak()
         hpk, hsrc = hbm_peak()
-        for d_head in (64, 128):
-            bh, seq = 128, 512
+        for bh, seq, d_head in ((128, 512, 64), (128, 512, 128), (32, 4096, 64), (32, 4096, 128)):
             q, k, v = (tdev(a) for a in synth.attn_inputs(bh, seq, d_head, 31 + d_head))
             o = torch.empty_like(q)
             lse = torch.empty((bh, seq), device=dev)

@@ -71,6 +71,13 @@ def test_attention_several_query_tiles_per_pipeline(d):
     run_attention(64, 1024, d, 77 + d, False, heads_checked=[0, 21, 42, 63])
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_attention_long_causal_sequence(d):
+    # 4 heads x 2048 queries, causal: 32 key tiles on the longest query rows
+    # (the compute-bound regime the tensor-core timing lines use)
+    run_attention(4, 2048, d, 91 + d, True, heads_checked=[0, 3])
+
+
 def test_attention_lse_optional_and_empty():
     q, k, v = (dev_bf16(a) for a in synth.attn_inputs(2, 64, 64, 5))
     o = torch.empty_like(q)
