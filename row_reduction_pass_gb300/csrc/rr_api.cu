@@ -908,13 +908,16 @@ static int forced_tier() {
 static rr_status bad_tier() { return fail(RR_ERR_INVALID_ARG, "RR_FORCE_TIER must be 0..3 or T0..T3"); }
 static rr_status no_span(int64_t cols) {
   return fail(RR_ERR_INVALID_ARG,
-              "tier 0 (spans) takes 16-byte aligned tensors with rows of at most 128 bytes "
-              "(64 for the norm backward), not %lld columns", (long long)cols);
+              "tier 0 (spans) takes 16-byte aligned tensors with short rows whose byte length "
+              "is not a multiple of 16 (up to 448 bytes; 224 for the softmax backward, 64 for "
+              "the norm backward, fewer columns for some operations), not %lld columns",
+              (long long)cols);
 }
 
-// Short misaligned rows (byte length not a multiple of 16, up to 128 bytes, 64
-// for the norm backward; 16-byte aligned row tensors): the span kernels
-// (rr_span.cuh), one warp per span of 32 x rpl rows of ~3 KB.  mode 0
+// Short misaligned rows (byte length not a multiple of 16, up to 448 bytes by
+// operation, see span_plan; 16-byte aligned row tensors): the span kernels
+// (rr_span.cuh), one warp per span of 32 x rpl rows of ~3 KB (at least 32
+// rows).  mode 0
 // softmax, 1 log-softmax, 2 cross-entropy, 3 softmax backward, 4 log-softmax
 // backward, 5 LayerNorm forward, 6 RMSNorm forward, 7 LayerNorm backward,
 // 8 RMSNorm backward.  aux_aligned: the labels (mode 2) or the row statistics
@@ -930,8 +933,7 @@ struct SpanPlan {
 static rr_status span_plan(rr_dtype dt, int mode, int64_t rows, int64_t cols, bool aux_aligned,
                            int64_t max_grid, SpanPlan* sp) {
   const int E = dt == RR_BF16 ? 2 : 4;
-  // Rows whose byte length is not a multiple of 16, up to 128 bytes (64 for
-  // the norm backward, whose spans hold two tensors).  Rows of whole 16-byte
+  // Rows whose byte length is not a multiple of 16.  Rows of whole 16-byte
   // chunks go to the row-group / direct kernels, which read them as chunks.
   // In the spans a lane per row puts the lanes a multiple of 16 bytes apart:
   // 8- to 32-way shared-memory bank conflicts at 32..128-byte rows (256-byte
@@ -939,9 +941,37 @@ static rr_status span_plan(rr_dtype dt, int mode, int64_t rows, int64_t cols, bo
   // at staggered columns the row groups measured faster (bf16 64 columns:
   // cross-entropy 20.7 us against 27.5, softmax backward 12.5 against 29.9).
   // Odd multiples of 4 bytes are conflict-free, 8 mod 16 two-way.
-  // RR_SPAN_MAX_BYTES overrides the 128-byte limit (tuning aid).
-  int64_t lim = mode >= 7 ? 64 : 128;
-  if (const char* f = std::getenv("RR_SPAN_MAX_BYTES"); f != nullptr && mode < 7) lim = std::atoll(f);
+  // Length limits, from timings of each operation on 2^24-element tensors
+  // (cold L2) against the row-group / engine kernels for rows of 132 to 404
+  // bytes (fp32 33..101 columns, bf16 65..199):
+  //  - softmax / log-softmax: up to 448 bytes and 160 columns (fp32 33
+  //    columns: log-softmax 46.0 -> 19.4 us; bf16 197 columns lost, 29.4 ->
+  //    30.0 us);
+  //  - cross-entropy: up to 448 bytes and 200 columns (fp32 33: 63.8 -> 22.6
+  //    us, bf16 197: 36.9 -> 30.3 us);
+  //  - softmax / log-softmax backward (two tensors per span): up to 224 bytes
+  //    (fp32 33: 49.2 -> 29.6 us; even beyond);
+  //  - LayerNorm / RMSNorm forward: up to 448 bytes, bf16 up to 128 columns
+  //    (fp32 97: 41.5 -> 33.7 us; bf16 131 lost, 32.6 -> 34.9, and 197 lost,
+  //    29.3 -> 38.6: a lane's serial pass over that many columns with one
+  //    block of spans per SM);
+  //  - LayerNorm / RMSNorm backward: up to 64 bytes (two tensors, and the
+  //    column partials' second pass).
+  // RR_SPAN_MAX_BYTES replaces these limits by one byte limit for the
+  // operations but the norm backward (tuning aid).
+  int64_t lim = 64, cmax = INT64_MAX;
+  switch (mode) {
+    case 0: case 1: lim = 448; cmax = 160; break;
+    case 2: lim = 448; cmax = 200; break;
+    case 3: case 4: lim = 224; break;
+    case 5: case 6: lim = 448; cmax = E == 2 ? 128 : INT64_MAX; break;
+    default: break;
+  }
+  if (const char* f = std::getenv("RR_SPAN_MAX_BYTES"); f != nullptr && mode < 7) {
+    lim = std::atoll(f);
+    cmax = INT64_MAX;
+  }
+  if (cols > cmax) return RR_ERR_INVALID_ARG;
   const int64_t rb = cols * E;
   if (rb > lim || rb % 16 == 0 || rows <= 0 || max_grid < 1) return RR_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);

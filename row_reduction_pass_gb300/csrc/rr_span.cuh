@@ -1,7 +1,7 @@
 // rr_span.cuh -- short rows as contiguous spans of rows per warp: softmax,
 // log-softmax and cross-entropy, the softmax / log-softmax backward, and the
 // LayerNorm / RMSNorm forward and backward, for rows whose byte length is not
-// a multiple of 16 (up to 128 bytes; 64 for the norm backward).
+// a multiple of 16 (up to 448 bytes by operation; 64 for the norm backward).
 //
 // With rows this short a row-group kernel moves only a few bytes per thread
 // per row, far too little in flight to cover DRAM latency, and a misaligned row

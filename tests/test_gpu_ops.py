@@ -5,9 +5,11 @@ bases (element mode), in-place outputs, masked and ignored rows."""
 import numpy as np
 import pytest
 
+import oracle
 from row_reduction_pass_gb300 import synth
 
-from parity import check_ln, check_norm_bwd, check_softmax, check_xent
+from parity import (check_ln, check_log_softmax, check_norm_bwd, check_rms, check_softmax,
+                    check_softmax_bwd, check_xent, store)
 
 pytestmark = pytest.mark.gpu
 
@@ -129,3 +131,31 @@ def test_layernorm_bwd_short_rows(dtype, cols, rows, layout):
     x, g, b, dy = ln_case(rows, cols, dtype, 700 + cols + rows)
     check_norm_bwd(x, g, b, dy, dtype, stat_pad=1 if layout == "stats_misaligned" else 0,
                    inplace={"dx_over_dy": "dy", "dx_over_x": "x"}.get(layout))
+
+
+# Rows of 130..448 bytes that are not whole 16-byte chunks: the span kernels
+# take the softmax family, its backward (up to 224 bytes) and the norm forward
+# (bf16 up to 128 columns), with one row per lane (32 rows per span); around
+# the limits in bytes and columns on both sides.
+SPAN_LONG = [("f32", c) for c in (33, 35, 50, 63, 101, 111, 113)] + \
+            [("bf16", c) for c in (65, 99, 111, 127, 131, 150, 161, 199, 201)]
+
+
+@pytest.mark.parametrize("dtype,cols", SPAN_LONG)
+@pytest.mark.parametrize("rows", [1, 33, 5003, 70001])
+def test_span_rows_up_to_448_bytes(dtype, cols, rows):
+    """Several spans per warp (70001 rows), a ragged last span, one row; every
+    operation routed as without a forced tier, against the oracle."""
+    x, lab = logits(rows, cols, dtype, 900 + cols + rows)
+    lab[1::50] = cols + 3
+    check_softmax(x, dtype)
+    check_log_softmax(x, dtype)
+    check_xent(x, lab, dtype)
+    check_xent(x, lab, dtype, inplace=True)
+    y = store(oracle.softmax(x), dtype)
+    dy = store(np.random.default_rng(cols + rows).standard_normal((rows, cols)), dtype)
+    check_softmax_bwd(y, dy, dtype)
+    check_softmax_bwd(store(oracle.log_softmax(x), dtype), dy, dtype, log=True, inplace="dy")
+    xl, g, b, dyl = ln_case(rows, cols, dtype, 950 + cols + rows)
+    check_ln(xl, g, b, dyl, 1e-5, dtype)
+    check_rms(xl, g, dyl, 1e-5, dtype)

@@ -42,9 +42,19 @@ def tier(t):
 def holds(op: str, t: int, cols: int, e: int) -> bool:
     """Whether forced tier t takes rows of `cols` elements of e bytes (16-byte
     aligned tensors) for operation `op`."""
-    if t == 0:  # rows of a byte length not a multiple of 16, up to 128 (norm backward 64)
+    if t == 0:  # rows of a byte length not a multiple of 16, with a limit per operation
         rb = cols * e
-        return rb <= (64 if op in ("ln_bwd", "rms_bwd") else 128) and rb % 16 != 0
+        if rb % 16 == 0:
+            return False
+        if op in ("softmax", "log_softmax"):
+            return rb <= 448 and cols <= 160
+        if op == "xent":
+            return rb <= 448 and cols <= 200
+        if op in ("softmax_bwd", "log_softmax_bwd"):
+            return rb <= 224
+        if op in ("ln_fwd", "rms_fwd"):
+            return rb <= 448 and (e == 4 or cols <= 128)
+        return rb <= 64  # norm backward
     if t == 1:
         return True  # every row length used here fits one row group
     if t == 2:
