@@ -191,10 +191,11 @@ __device__ __forceinline__ void load_direct_mem(RowRegs<DT, W, NT, NQ>& r, int t
                                             const RowGeo<DT, W>& g, const char* g0,
                                             float fill) {
   constexpr int E = DType<DT>::E;
-  // rows without a ragged head or tail: no per-chunk checks (variants of
-  // several chunks per thread; in the two-chunk ones, which also hold the next
-  // row, the second copy of the loop costs registers)
-  if constexpr (W > 1 && NQ > 2) {
+  // rows without a ragged head or tail: no per-chunk checks (one-tensor
+  // operations, or several chunks per thread; in the two-chunk two-tensor
+  // ones, which also hold the next row, the second copy of the loop cost
+  // registers and spilled)
+  if constexpr (W > 1 && (NQ > 2 || NT == 1)) {
     if (g.all_full()) {
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {
