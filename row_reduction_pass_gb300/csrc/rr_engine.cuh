@@ -477,6 +477,11 @@ __global__ void __launch_bounds__(MAXT, STAGED ? 1 : 1024 / MAXT)
     if constexpr (kPre) {
       if (my_first < geo.rows && !Op::skip(m_cur)) Op::load_direct(cur, g_cur, p, geo, my_first, c0);
     }
+    // two rows per trip for one-tensor operations, so the next row's
+    // registers become the current ones by renaming, not by copies (the
+    // two-tensor backward spilled when unrolled)
+    constexpr int kRowUnroll = NT == 1 ? 2 : 1;
+#pragma unroll kRowUnroll
     for (int64_t i = 0;; ++i) {
       const int64_t wr = warp_first + i * step;
       if (wr >= geo.rows) break;
