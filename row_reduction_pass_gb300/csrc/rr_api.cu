@@ -1070,8 +1070,9 @@ static rr_status one_plan(const void* fn, rr_dtype dt, int64_t rows, int64_t max
     if (e != cudaSuccess || occ <= 0)
       return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
   }
-  const int64_t E = dt == RR_BF16 ? 2 : 4;
-  int64_t grid = cdiv(rows, T * (16 / E));
+  // tiles of kOneThreads x U rows, U = 16 / E (the norm backward: 4); a
+  // block without a tile just exits (the norm backward's partial is then 0)
+  int64_t grid = cdiv(rows, T * 4);
   const int64_t resident = (int64_t)di->sms * occ;
   if (grid > resident) grid = resident;
   if (grid > max_grid) grid = max_grid;

@@ -5,7 +5,8 @@
 // (sec. 3.2, sec. 2.2) becomes elementwise; the general kernels' per-row
 // machinery (row geometry, staging, merges over lanes) cost ~190 thread
 // instructions for such a row.  A block takes tiles of kOneThreads x U rows
-// (U = 16 bytes / element size), tiles b, b + grid, ...; thread t of a tile
+// (U = 16 bytes / element size; 4 in the norm backward, which reads four
+// tensors a row), tiles b, b + grid, ...; thread t of a tile
 // takes rows t, t + kOneThreads, ..., its U loads of each tensor issued
 // together, so every warp access covers consecutive rows.  Masked rows,
 // labels out of range, ignored rows and non-finite values come out as in the
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(kOneThreads) one_norm_bwd_kernel(const LnBwdPa
   constexpr int E = DType<DT>::E;
   constexpr int kPlanes = RMS ? 1 : 2;
   __shared__ float red[kOneThreads / 32][2];
-  constexpr int U = 16 / E;
+  constexpr int U = 4;  // rows a thread takes per tile (four tensors in flight per row)
   const float gm = ld_elem<DT>(p.gamma);
   float ag = 0.f, ab = 0.f;  // this thread's sums of dy xhat, dy (its rows in order)
   RR_ONE_TILES(U) {
