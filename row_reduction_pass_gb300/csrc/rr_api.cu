@@ -1056,8 +1056,7 @@ static bool one_eligible(int64_t rows, int64_t cols) {
   return f == nullptr || f[0] != '0';
 }
 
-static rr_status one_plan(const void* fn, rr_dtype dt, int64_t rows, int64_t max_grid,
-                          OnePlan* op) {
+static rr_status one_plan(const void* fn, int64_t rows, int64_t max_grid, OnePlan* op) {
   if (max_grid < 1) return RR_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
   DevInfo* di = nullptr;
@@ -1093,9 +1092,9 @@ rr_status one_launch(const P& p, const OnePlan& op, int64_t rows, cudaStream_t s
 }
 
 template <class P>
-rr_status one_run(const P& p, const void* fn, rr_dtype dt, int64_t rows, cudaStream_t stream) {
+rr_status one_run(const P& p, const void* fn, int64_t rows, cudaStream_t stream) {
   OnePlan op;
-  rr_status st = one_plan(fn, dt, rows, INT64_MAX, &op);
+  rr_status st = one_plan(fn, rows, INT64_MAX, &op);
   if (st != RR_OK) return st;
   if ((st = one_launch(p, op, rows, stream)) != RR_OK) return st;
   return ok();
@@ -1199,7 +1198,7 @@ static rr_status softmax_fwd_impl(const void* x, void* y, int64_t rows, int64_t 
   const int ft = forced_tier();
   if (ft == -2) return bad_tier();
   if (one_eligible(rows, cols))
-    return one_run(p, one_kernels(dtype).fwd[log ? 1 : 0], dtype, rows, stream);
+    return one_run(p, one_kernels(dtype).fwd[log ? 1 : 0], rows, stream);
   if (ft <= 0 && aligned(x, 16) && aligned(y, 16)) {
     st = span_launch(p, dtype, log ? 1 : 0, rows, cols, false, stream);
     if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
@@ -1254,7 +1253,7 @@ static rr_status softmax_bwd_impl(const void* y, const void* dy, void* dx, int64
   const int ft = forced_tier();
   if (ft == -2) return bad_tier();
   if (one_eligible(rows, cols))
-    return one_run(p, one_kernels(dtype).bwd[log ? 1 : 0], dtype, rows, stream);
+    return one_run(p, one_kernels(dtype).bwd[log ? 1 : 0], rows, stream);
   if (ft <= 0 && same && a == 0) {
     st = span_launch(p, dtype, log ? 4 : 3, rows, cols, false, stream);
     if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
@@ -1309,10 +1308,10 @@ rr_status rr_softmax_xent_fwd_bwd(const void* logits, const int32_t* labels, flo
   int* err = device_error_word();
   if (!err) return RR_ERR_CUDA;
   rr::SoftmaxParams p{static_cast<const char*>(logits), static_cast<char*>(dlogits), labels, loss,
-                      bad_label_count, err, cols, ignore_index};
+                      bad_label_count, err, cols, ignore_index, 0};
   const int ft = forced_tier();
   if (ft == -2) return bad_tier();
-  if (one_eligible(rows, cols)) return one_run(p, one_kernels(dtype).fwd[2], dtype, rows, stream);
+  if (one_eligible(rows, cols)) return one_run(p, one_kernels(dtype).fwd[2], rows, stream);
   if (ft <= 0 && aligned(logits, 16) && aligned(dlogits, 16)) {
     st = span_launch(p, dtype, 2, rows, cols, aligned(labels, 16), stream);
     if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
@@ -1362,7 +1361,7 @@ rr_status rr_layernorm_fwd(const void* x, const void* gamma, const void* beta, v
                       static_cast<const char*>(beta), static_cast<char*>(y), mean, rstd, err, cols,
                       eps, static_cast<float>(1.0 / static_cast<double>(cols))};
     if (one_eligible(rows, cols))
-      return one_run(p, one_kernels(dtype).norm_fwd[0], dtype, rows, stream);
+      return one_run(p, one_kernels(dtype).norm_fwd[0], rows, stream);
     if (ft <= 0 && aligned(x, 16) && aligned(y, 16)) {
       st = span_launch(p, dtype, 5, rows, cols, false, stream);
       if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
@@ -1434,7 +1433,7 @@ rr_status rr_rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
                       static_cast<char*>(y), nullptr, rstd, err, cols, eps,
                       static_cast<float>(1.0 / static_cast<double>(cols))};
     if (one_eligible(rows, cols))
-      return one_run(p, one_kernels(dtype).norm_fwd[1], dtype, rows, stream);
+      return one_run(p, one_kernels(dtype).norm_fwd[1], rows, stream);
     if (ft <= 0 && aligned(x, 16) && aligned(y, 16)) {
       st = span_launch(p, dtype, 6, rows, cols, false, stream);
       if (st != RR_ERR_INVALID_ARG) return st == RR_OK ? ok() : st;
@@ -1531,7 +1530,7 @@ static size_t norm_bwd_workspace_size(bool rms, int64_t rows, int64_t cols, rr_d
   }
   OnePlan op;  // rows of one column: one partial per block
   if (one_eligible(rows, cols) &&
-      one_plan(one_kernels(dtype).norm_bwd[rms], dtype, rows, INT64_MAX, &op) == RR_OK) {
+      one_plan(one_kernels(dtype).norm_bwd[rms], rows, INT64_MAX, &op) == RR_OK) {
     const size_t ws = (size_t)op.grid * (rms ? 1 : 2) * sizeof(float);
     if (ws > best) best = ws;
   }
@@ -1630,7 +1629,7 @@ static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* 
     OnePlan op;
     const bool one = one_eligible(rows, cols);
     if (one &&
-        (st = one_plan(one_kernels(dtype).norm_bwd[rms], dtype, rows, max_partials, &op)) != RR_OK)
+        (st = one_plan(one_kernels(dtype).norm_bwd[rms], rows, max_partials, &op)) != RR_OK)
       return st;
     if (!one && ft <= 0 && aligned(dy, 16) && aligned(x, 16) && aligned(dx, 16)) {
       const bool stats_al = aligned(rstd, 16) && (rms || aligned(mean, 16));
