@@ -1100,6 +1100,92 @@ rr_status one_run(const P& p, const void* fn, int64_t rows, cudaStream_t stream)
   return ok();
 }
 
+// LayerNorm / RMSNorm backward of short misaligned rows (rr_lns.cuh): byte
+// length 65..1009 and not a multiple of 16 (shorter ones go to the spans; at
+// most 64 chunks a row, whatever its offset),
+// dy, x and dx at the same address modulo 16 (x's is hb0).  The variant is
+// the narrowest that holds the longest chunk span of a row: two rows per warp
+// up to 16 chunks, then one row per warp with one or two (fp32 only) chunks a
+// lane.  As
+// many blocks as are resident, at most max_partials (one column partial each).
+// RR_LNS=0 turns these kernels off; RR_LNS_V=0..2 forces a variant (tuning
+// aids).
+struct LnsPlan {
+  const void* fn = nullptr;
+  int64_t grid = 0;
+  size_t smem = 0;
+  rr::LnsGeo geo{};
+};
+
+static const rr::LnsKernels& lns_kernels(rr_dtype dt) {
+  static const rr::LnsKernels f32 = rr::lns_kernels_f32();
+  static const rr::LnsKernels bf16 = rr::lns_kernels_bf16();
+  return dt == RR_BF16 ? bf16 : f32;
+}
+
+static rr_status lns_plan(bool rms, rr_dtype dt, int64_t rows, int64_t cols, int hb0,
+                          int64_t max_partials, LnsPlan* lp) {
+  if (const char* f = std::getenv("RR_LNS"); f != nullptr && f[0] == '0')
+    return RR_ERR_INVALID_ARG;
+  const int64_t E = dt == RR_BF16 ? 2 : 4;
+  const int64_t rb = cols * E;
+  if (rb % 16 == 0 || rb <= 64 || rb > 1024 || rows < 1 || max_partials < 1)
+    return RR_ERR_INVALID_ARG;
+  int64_t a = 16, b = rb % 16;
+  while (b) {
+    const int64_t t = a % b;
+    a = b;
+    b = t;
+  }
+  const int64_t P = 16 / a;  // 2, 4 or 8 for 2- and 4-byte elements: divides kLnsWarps
+  const int64_t nch_max = (rb + 15 + 15) / 16;  // chunks a row touches at worst
+  if (nch_max > 64) return RR_ERR_INVALID_ARG;
+  int v = nch_max <= 16 ? 0 : nch_max <= 32 ? 1 : 2;
+  // Taken where at least 3/4 of the variant's chunk slots hold a chunk: with
+  // fewer, the per-row reductions and statistics loads are shared by too few
+  // elements and the row-group kernels were faster (2^24-element timings:
+  // fp32 97 columns, 26 of 32 slots, LayerNorm backward 77.9 -> 53.7 us,
+  // fp32 250 columns 58.4 -> 53.6 us, bf16 97 columns 61.5 -> 49.2 us; fp32 31
+  // columns, 9 of 16 slots, 73.6 -> 81.2 us; fp32 127 columns, 33 of 64,
+  // 60.2 -> 73.8 us).  bf16 rows of more than 32 chunks are left out: the
+  // two-chunk variant needs 170 registers there (bf16 500 columns 37.0 ->
+  // 62.8 us) and is not built.
+  const int64_t cap = v == 0 ? 16 : v == 1 ? 32 : 64;
+  bool take = 4 * nch_max >= 3 * cap && !(dt == RR_BF16 && v == 2);
+  if (const char* f = std::getenv("RR_LNS_V"); f != nullptr && f[0] >= '0' && f[0] <= '2') {
+    const int fv = f[0] - '0';
+    if (nch_max <= (fv == 0 ? 16 : fv == 1 ? 32 : 64) && !(dt == RR_BF16 && fv == 2)) {
+      v = fv;
+      take = true;
+    }
+  }
+  if (!take) return RR_ERR_INVALID_ARG;
+  const void* fn = lns_kernels(dt).bwd[rms ? 1 : 0][v];
+  const size_t smem = (size_t)rr::kLnsWarps * (rms ? 1 : 2) * (size_t)cols * sizeof(float);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo* di = nullptr;
+  rr_status st = device_info(&di);
+  if (st != RR_OK) return st;
+  if ((int64_t)smem > di->smem_optin) return RR_ERR_INVALID_ARG;
+  if ((st = set_smem(di, fn, smem)) != RR_OK) return st;
+  const int T = 32 * rr::kLnsWarps;
+  int& occ = di->occ[{fn, ((long long)T << 32) | (long long)smem}];
+  if (occ == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, T, smem);
+    if (e != cudaSuccess || occ <= 0)
+      return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+  }
+  const int64_t rpw = v == 0 ? 2 : 1;  // rows a warp holds at once
+  int64_t grid = cdiv(rows, rpw * rr::kLnsWarps);
+  if (grid > (int64_t)di->sms * occ) grid = (int64_t)di->sms * occ;
+  if (grid > max_partials) grid = max_partials;
+  lp->fn = fn;
+  lp->grid = grid;
+  lp->smem = smem;
+  lp->geo = rr::LnsGeo{rows, (int32_t)cols, (int32_t)P, hb0, (int32_t)rb};
+  return RR_OK;
+}
+
 template <class P>
 rr_status launch(const Plan& pl, const P& params, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -1528,6 +1614,11 @@ static size_t norm_bwd_workspace_size(bool rms, int64_t rows, int64_t cols, rr_d
     LncPlan lp;
     if (lnc_plan(true, rms, dtype, rows, cols, &lp) == RR_OK && lp.ws_bytes > best) best = lp.ws_bytes;
   }
+  LnsPlan sp2;  // short misaligned rows by phase class: one partial per block
+  if (forced_tier() < 0 && lns_plan(rms, dtype, rows, cols, 0, INT64_MAX, &sp2) == RR_OK) {
+    const size_t ws = (size_t)sp2.grid * (rms ? 1 : 2) * (size_t)cols * sizeof(float);
+    if (ws > best) best = ws;
+  }
   OnePlan op;  // rows of one column: one partial per block
   if (one_eligible(rows, cols) &&
       one_plan(one_kernels(dtype).norm_bwd[rms], rows, INT64_MAX, &op) == RR_OK) {
@@ -1652,15 +1743,32 @@ static rr_status norm_bwd(bool rms, const void* dy, const void* x, const float* 
       const uintptr_t a16 = reinterpret_cast<uintptr_t>(x) & 15;
       const bool same16 = a16 == (reinterpret_cast<uintptr_t>(dy) & 15) &&
                           a16 == (reinterpret_cast<uintptr_t>(dx) & 15);
+      // short misaligned rows: phase-class warps (one partial per block)
+      LnsPlan sp2;
+      st = RR_ERR_INVALID_ARG;
+      if (same16 && ft < 0) {
+        st = lns_plan(rms, dtype, rows, cols, (int)a16, max_partials, &sp2);
+        if (st != RR_OK && st != RR_ERR_INVALID_ARG) return st;
+      }
       // the longest rows: column-block kernels, where their partials and
       // records fit the workspace
       LncPlan lp;
-      st = RR_ERR_INVALID_ARG;
-      if (same16 && ft < 0) {
+      const bool lns = st == RR_OK;
+      if (!lns && same16 && ft < 0) {
         st = lnc_plan(true, rms, dtype, rows, cols, &lp, max_partials, workspace_bytes);
         if (st != RR_OK && st != RR_ERR_INVALID_ARG) return st;
       }
-      if (st == RR_OK) {
+      if (lns) {
+        need = (size_t)sp2.grid * planes * (size_t)cols * sizeof(float);
+        if (workspace_bytes < need)
+          return fail(RR_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+        rr::LnsGeo g = sp2.geo;
+        void* args[] = {&p, &g};
+        cudaError_t e = cudaLaunchKernel(sp2.fn, dim3((unsigned)sp2.grid),
+                                         dim3(32 * rr::kLnsWarps), args, sp2.smem, stream);
+        if (e != cudaSuccess) return fail(RR_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+        pl.partials = sp2.grid;
+      } else if (st == RR_OK) {
         const rr::LncKernels& k = lnc_kernels(dtype);
         rr::LncGeo g = lp.geo;
         void* args[] = {&p, &g};

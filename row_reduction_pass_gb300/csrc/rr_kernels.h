@@ -117,6 +117,26 @@ struct LncKernels {
 LncKernels lnc_kernels_f32();
 LncKernels lnc_kernels_bf16();
 
+// LayerNorm / RMSNorm backward of short misaligned rows by phase class
+// (rr_lns.cuh): bwd[rms][v], v = 0 two rows per warp (16 lanes, one chunk
+// each: rows of at most 16 chunks), 1 one row per warp (32 chunks), 2 one row
+// per warp with two chunks a lane (64 chunks; fp32 only, null for bf16).
+// Blocks of kLnsWarps warps,
+// one column partial ([planes][cols] floats) per block.
+constexpr int kLnsWarps = 8;
+struct LnsGeo {
+  int64_t rows;
+  int32_t cols;
+  int32_t P;    // phase classes (divides kLnsWarps)
+  int32_t hb0;  // byte of row 0 within its 16-byte block (x, dy and dx alike)
+  int32_t rb;   // bytes per row
+};
+struct LnsKernels {
+  const void* bwd[2][3];
+};
+LnsKernels lns_kernels_f32();
+LnsKernels lns_kernels_bf16();
+
 // Rows of one column (rr_one.cuh), elementwise: fwd [mode] 0 softmax,
 // 1 log-softmax, 2 cross-entropy; bwd [log]; norm_fwd / norm_bwd [rms].
 // Blocks of kOneThreads threads; the norm backward writes one partial

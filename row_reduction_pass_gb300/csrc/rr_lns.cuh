@@ -1,0 +1,205 @@
+// rr_lns.cuh -- LayerNorm / RMSNorm backward of short rows whose byte length
+// is not a multiple of 16 (65 bytes to 1 KB), by phase class.
+//
+// The backward of "Engineering a CUDA Machine Learning Framework from
+// Scratch", sec. 2.2 (pre-derived analytic gradients), per row:
+//   xhat = (x - mean) rstd (RMSNorm: x rstd),  g = dy gamma,
+//   S1 = sum g,  S2 = sum g xhat,
+//   dx = rstd (g - S1 / C - xhat S2 / C)      (RMSNorm: without S1),
+// and over rows, per column: dgamma = sum dy xhat, dbeta = sum dy.
+//
+// A row of rb bytes starts at byte h = (base + r rb) mod 16 of its first
+// 16-byte block, and h repeats every P = 16 / gcd(16, rb mod 16) rows (x, dy
+// and dx share their address modulo 16).  A warp takes the rows of one phase
+// class only, so its lanes own fixed aligned 16-byte chunks of every row it
+// sees -- chunk j holds columns W j - h / E .. W j - h / E + W - 1 -- and
+// their column partials stay in registers, with gamma read once per launch.
+// SUB lanes hold a row (SUB = 16: a warp takes two rows at a time), NQ chunks
+// each.  Full chunks are single 16-byte loads and stores; the head and tail
+// chunk of a row move element by element (nothing outside the row is read).
+// Columns outside the row hold dy = 0 and xhat = 0 and add nothing.  A row
+// with rstd = 0 (masked by the forward) gets dx = 0 and adds nothing.  At the
+// end each block adds its warps' column partials in a fixed order (warp 0..7)
+// into its row of the workspace, [gridDim.x][planes][cols] floats, which
+// col_reduce_kernel sums: the result does not depend on timing.
+#pragma once
+
+#include "rr_kernels.h"
+#include "rr_ops.cuh"
+
+namespace rr {
+
+template <int DT, bool RMS, int SUB, int NQ>
+__global__ void __launch_bounds__(32 * kLnsWarps)
+    lns_bwd_kernel(const LnBwdParams p, const LnsGeo geo) {
+  constexpr int E = DType<DT>::E;
+  constexpr int W = 16 / E;
+  constexpr int kPlanes = RMS ? 1 : 2;
+  constexpr int RPW = 32 / SUB;  // rows a warp holds at once
+  extern __shared__ __align__(16) float lns_part[];  // [warps][planes][cols]
+  const int C = geo.cols;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sl = lane % SUB, sr = lane / SUB;
+  const int64_t gw = (int64_t)blockIdx.x * kLnsWarps + warp;
+  const int P = geo.P;
+  const int cls = (int)(gw % P);            // P divides kLnsWarps
+  const int64_t wi = gw / P;                // this warp among its class's warps
+  const int64_t wpc = (int64_t)gridDim.x * kLnsWarps / P;
+  const int h = (int)(((int64_t)geo.hb0 + (int64_t)cls * geo.rb) & 15);  // head bytes
+  const int hc = h / E;                     // elements of chunk 0 before column 0
+  const int nch = (h + geo.rb + 15) / 16;   // chunks a row touches
+  const int64_t nrows = geo.rows > cls ? (geo.rows - cls + P - 1) / P : 0;  // rows of the class
+
+  // this lane's chunks: column of element e of chunk q, whole-chunk flags,
+  // gamma there (0 outside the row), and the column partials
+  bool has[NQ], full[NQ];
+  float gm[NQ][W], ag[NQ][W], ab[NQ][W];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const int j = sl + SUB * q;
+    has[q] = j < nch;
+    full[q] = has[q] && 16 * j >= h && 16 * j + 16 <= h + geo.rb;
+#pragma unroll
+    for (int e = 0; e < W; ++e) {
+      const int col = W * j + e - hc;
+      gm[q][e] = (has[q] && col >= 0 && col < C) ? ld_elem_cached<DT>(p.gamma + (int64_t)col * E)
+                                                  : 0.f;
+      ag[q][e] = 0.f;
+      ab[q][e] = 0.f;
+    }
+  }
+
+  for (int64_t t0 = wi * RPW; t0 < nrows; t0 += wpc * RPW) {
+    const int64_t t = t0 + sr;
+    const bool act = t < nrows;
+    const int64_t r = cls + (int64_t)P * t;
+    float rs = 0.f, mu = 0.f;
+    if (act) {
+      rs = __ldg(p.rstd + r);
+      if constexpr (!RMS) mu = __ldg(p.mean + r);
+    }
+    const bool live = act && rs != 0.f;
+    const int64_t rowoff = r * (int64_t)geo.rb - h;  // byte of chunk 0 from each tensor's base
+    float xh[NQ][W], dv[NQ][W];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const int j = sl + SUB * q;
+      float xv[W], dyv[W];
+#pragma unroll
+      for (int e = 0; e < W; ++e) {
+        xv[e] = mu;
+        dyv[e] = 0.f;
+      }
+      if (live && has[q]) {
+        const int64_t off = rowoff + 16 * (int64_t)j;
+        if (full[q]) {
+          const uint4 cx = ld_chunk_stream(p.x + off);
+          const uint4 cd = ld_chunk_stream(p.dy + off);
+#pragma unroll
+          for (int e = 0; e < W; ++e) {
+            xv[e] = chunk_get<DT>(cx, e);
+            dyv[e] = chunk_get<DT>(cd, e);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < W; ++e) {
+            const int col = W * j + e - hc;
+            if (col >= 0 && col < C) {
+              xv[e] = ld_elem<DT>(p.x + off + e * E);
+              dyv[e] = ld_elem<DT>(p.dy + off + e * E);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < W; ++e) {
+        xh[q][e] = RMS ? xv[e] * rs : (xv[e] - mu) * rs;
+        dv[q][e] = dyv[e];
+        const float g = __fmul_rn(dyv[e], gm[q][e]);
+        if constexpr (!RMS) s1 += g;
+        s2 = fmaf(g, xh[q][e], s2);
+      }
+    }
+    // the row's sums over its SUB lanes (every lane ends with the same bits)
+#pragma unroll
+    for (int o = SUB / 2; o >= 1; o >>= 1) {
+      if constexpr (!RMS) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    }
+    if (!act) continue;
+    const float a = RMS ? 0.f : s1 * p.inv_cols;
+    const float b = s2 * p.inv_cols;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (!has[q]) continue;
+      const int j = sl + SUB * q;
+      float f[W];
+#pragma unroll
+      for (int e = 0; e < W; ++e) {
+        const float g = __fmul_rn(dv[q][e], gm[q][e]);
+        f[e] = live ? fmaf(xh[q][e], -b, g - a) * rs : 0.f;
+        ag[q][e] = fmaf(dv[q][e], xh[q][e], ag[q][e]);
+        if constexpr (!RMS) ab[q][e] += dv[q][e];
+      }
+      const int64_t off = rowoff + 16 * (int64_t)j;
+      if (full[q]) {
+        st_chunk_stream(p.dx + off, chunk_pack<DT>(f));
+      } else {
+#pragma unroll
+        for (int e = 0; e < W; ++e) {
+          const int col = W * j + e - hc;
+          if (col >= 0 && col < C) st_elem<DT>(p.dx + off + e * E, f[e]);
+        }
+      }
+    }
+  }
+
+  // the warp's column partials: rows of the two half-warps added (SUB = 16),
+  // then each column written once into the warp's shared-memory row
+  float* mine = lns_part + (size_t)warp * kPlanes * C;
+  for (int i = lane; i < kPlanes * C; i += 32) mine[i] = 0.f;
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+#pragma unroll
+    for (int e = 0; e < W; ++e) {
+      if constexpr (RPW == 2) {
+        const float og = __shfl_xor_sync(0xffffffffu, ag[q][e], 16);
+        const float ob = __shfl_xor_sync(0xffffffffu, ab[q][e], 16);
+        ag[q][e] = sr == 0 ? ag[q][e] + og : og + ag[q][e];
+        ab[q][e] = sr == 0 ? ab[q][e] + ob : ob + ab[q][e];
+      }
+      const int col = W * (sl + SUB * q) + e - hc;
+      if (sr == 0 && has[q] && col >= 0 && col < C) {
+        mine[col] = ag[q][e];
+        if constexpr (!RMS) mine[C + col] = ab[q][e];
+      }
+    }
+  }
+  __syncthreads();
+  float* out = p.ws + (int64_t)blockIdx.x * kPlanes * C;
+  for (int i = threadIdx.x; i < kPlanes * C; i += blockDim.x) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kLnsWarps; ++w) s += lns_part[(size_t)w * kPlanes * C + i];
+    out[i] = s;
+  }
+}
+
+// bf16 has no two-chunk variant (170 registers; slower than the row groups).
+template <int DT>
+LnsKernels make_lns_set() {
+  LnsKernels k{};
+  k.bwd[0][0] = (const void*)lns_bwd_kernel<DT, false, 16, 1>;
+  k.bwd[0][1] = (const void*)lns_bwd_kernel<DT, false, 32, 1>;
+  k.bwd[1][0] = (const void*)lns_bwd_kernel<DT, true, 16, 1>;
+  k.bwd[1][1] = (const void*)lns_bwd_kernel<DT, true, 32, 1>;
+  if constexpr (DT == kF32) {
+    k.bwd[0][2] = (const void*)lns_bwd_kernel<DT, false, 32, 2>;
+    k.bwd[1][2] = (const void*)lns_bwd_kernel<DT, true, 32, 2>;
+  }
+  return k;
+}
+
+}  // namespace rr
