@@ -1141,17 +1141,18 @@ static rr_status lns_plan(bool rms, rr_dtype dt, int64_t rows, int64_t cols, int
   const int64_t nch_max = (rb + 15 + 15) / 16;  // chunks a row touches at worst
   if (nch_max > 64) return RR_ERR_INVALID_ARG;
   int v = nch_max <= 16 ? 0 : nch_max <= 32 ? 1 : 2;
-  // Taken where at least 3/4 of the variant's chunk slots hold a chunk: with
-  // fewer, the per-row reductions and statistics loads are shared by too few
-  // elements and the row-group kernels were faster (2^24-element timings:
-  // fp32 97 columns, 26 of 32 slots, LayerNorm backward 77.9 -> 53.7 us,
-  // fp32 250 columns 58.4 -> 53.6 us, bf16 97 columns 61.5 -> 49.2 us; fp32 31
-  // columns, 9 of 16 slots, 73.6 -> 81.2 us; fp32 127 columns, 33 of 64,
-  // 60.2 -> 73.8 us).  bf16 rows of more than 32 chunks are left out: the
-  // two-chunk variant needs 170 registers there (bf16 500 columns 37.0 ->
-  // 62.8 us) and is not built.
+  // Measured on 2^24-element tensors against the row-group kernels: fp32 rows
+  // won at every length tried (17 columns 128.0 -> 118.5 us, 45: 91.6 -> 51.3,
+  // 97: 76.1 -> 45.6, 127: 60.6 -> 57.1, 250: 58.6 -> 35.5; LayerNorm), so
+  // fp32 takes every row that fits.  bf16 rows won where at least 3/4 of the
+  // variant's chunk slots hold a chunk (97 columns, 14 of 16: 61.3 -> 51.8
+  // us) and lost below (33 columns 85.7 -> 126.9 us, 59: 54.2 -> 79.1, 123,
+  // 17 of 32: 52.2 -> 89.1): a bf16 chunk is eight columns, so the per-lane
+  // arrays and the element-wise head and tail chunks cost twice as much.
+  // bf16 rows of more than 32 chunks are left out: a two-chunk variant needs
+  // ~170 registers there (500 columns 37.0 -> 62.8 us) and is not built.
   const int64_t cap = v == 0 ? 16 : v == 1 ? 32 : 64;
-  bool take = 4 * nch_max >= 3 * cap && !(dt == RR_BF16 && v == 2);
+  bool take = dt == RR_F32 || (4 * nch_max >= 3 * cap && v < 2);
   if (const char* f = std::getenv("RR_LNS_V"); f != nullptr && f[0] >= '0' && f[0] <= '2') {
     const int fv = f[0] - '0';
     if (nch_max <= (fv == 0 ? 16 : fv == 1 ? 32 : 64) && !(dt == RR_BF16 && fv == 2)) {

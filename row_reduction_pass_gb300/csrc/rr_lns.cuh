@@ -15,7 +15,7 @@
 // sees -- chunk j holds columns W j - h / E .. W j - h / E + W - 1 -- and
 // their column partials stay in registers, with gamma read once per launch.
 // SUB lanes hold a row (SUB = 16: a warp takes two rows at a time), NQ chunks
-// each.  Full chunks are single 16-byte loads and stores; the head and tail
+// each, and the next row's chunks while they compute one.  Full chunks are single 16-byte loads and stores; the head and tail
 // chunk of a row move element by element (nothing outside the row is read).
 // Columns outside the row hold dy = 0 and xhat = 0 and add nothing.  A row
 // with rstd = 0 (masked by the forward) gets dx = 0 and adds nothing.  At the
@@ -69,54 +69,73 @@ __global__ void __launch_bounds__(32 * kLnsWarps)
     }
   }
 
+  // A row's raw chunks (and statistics) in registers; the next row's are
+  // loaded before the current one is processed (register double buffer), so
+  // each warp keeps a row's loads in flight while it computes.
+  struct Raw {
+    uint4 x[NQ], dy[NQ];
+    float rs, mu;
+  };
+  auto fetch = [&](int64_t t, Raw& v) {
+    v.rs = 0.f;
+    v.mu = 0.f;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      v.x[q] = make_uint4(0, 0, 0, 0);
+      v.dy[q] = make_uint4(0, 0, 0, 0);
+    }
+    if (t >= nrows) return;
+    const int64_t r = cls + (int64_t)P * t;
+    v.rs = __ldg(p.rstd + r);
+    if constexpr (!RMS) v.mu = __ldg(p.mean + r);
+    const int64_t rowoff = r * (int64_t)geo.rb - h;  // byte of chunk 0 from each tensor's base
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (!has[q]) continue;
+      const int j = sl + SUB * q;
+      const int64_t off = rowoff + 16 * (int64_t)j;
+      if (full[q]) {
+        v.x[q] = ld_chunk_stream(p.x + off);
+        v.dy[q] = ld_chunk_stream(p.dy + off);
+      } else {
+#pragma unroll
+        for (int e = 0; e < W; ++e) {
+          const int col = W * j + e - hc;
+          if (col >= 0 && col < C) {
+            chunk_set_bits<DT>(v.x[q], e, ld_elem_bits<DT>(p.x + off + e * E));
+            chunk_set_bits<DT>(v.dy[q], e, ld_elem_bits<DT>(p.dy + off + e * E));
+          }
+        }
+      }
+    }
+  };
+
+  Raw cur;
+  fetch(wi * RPW + sr, cur);
   for (int64_t t0 = wi * RPW; t0 < nrows; t0 += wpc * RPW) {
     const int64_t t = t0 + sr;
+    Raw nxt;
+    fetch(t + wpc * RPW, nxt);
     const bool act = t < nrows;
     const int64_t r = cls + (int64_t)P * t;
-    float rs = 0.f, mu = 0.f;
-    if (act) {
-      rs = __ldg(p.rstd + r);
-      if constexpr (!RMS) mu = __ldg(p.mean + r);
-    }
+    const float rs = cur.rs, mu = cur.mu;
     const bool live = act && rs != 0.f;
-    const int64_t rowoff = r * (int64_t)geo.rb - h;  // byte of chunk 0 from each tensor's base
+    const int64_t rowoff = r * (int64_t)geo.rb - h;
     float xh[NQ][W], dv[NQ][W];
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
       const int j = sl + SUB * q;
-      float xv[W], dyv[W];
 #pragma unroll
       for (int e = 0; e < W; ++e) {
-        xv[e] = mu;
-        dyv[e] = 0.f;
-      }
-      if (live && has[q]) {
-        const int64_t off = rowoff + 16 * (int64_t)j;
-        if (full[q]) {
-          const uint4 cx = ld_chunk_stream(p.x + off);
-          const uint4 cd = ld_chunk_stream(p.dy + off);
-#pragma unroll
-          for (int e = 0; e < W; ++e) {
-            xv[e] = chunk_get<DT>(cx, e);
-            dyv[e] = chunk_get<DT>(cd, e);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < W; ++e) {
-            const int col = W * j + e - hc;
-            if (col >= 0 && col < C) {
-              xv[e] = ld_elem<DT>(p.x + off + e * E);
-              dyv[e] = ld_elem<DT>(p.dy + off + e * E);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < W; ++e) {
-        xh[q][e] = RMS ? xv[e] * rs : (xv[e] - mu) * rs;
-        dv[q][e] = dyv[e];
-        const float g = __fmul_rn(dyv[e], gm[q][e]);
+        const int col = W * j + e - hc;
+        // columns outside the row: x = mean (xhat = 0), dy = 0
+        const bool in = live && has[q] && col >= 0 && col < C;
+        const float xv = in ? chunk_get<DT>(cur.x[q], e) : mu;
+        const float dyv = in ? chunk_get<DT>(cur.dy[q], e) : 0.f;
+        xh[q][e] = RMS ? xv * rs : (xv - mu) * rs;
+        dv[q][e] = dyv;
+        const float g = __fmul_rn(dyv, gm[q][e]);
         if constexpr (!RMS) s1 += g;
         s2 = fmaf(g, xh[q][e], s2);
       }
@@ -127,6 +146,7 @@ __global__ void __launch_bounds__(32 * kLnsWarps)
       if constexpr (!RMS) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
       s2 += __shfl_xor_sync(0xffffffffu, s2, o);
     }
+    cur = nxt;
     if (!act) continue;
     const float a = RMS ? 0.f : s1 * p.inv_cols;
     const float b = s2 * p.inv_cols;
