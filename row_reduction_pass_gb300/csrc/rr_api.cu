@@ -1104,11 +1104,11 @@ rr_status one_run(const P& p, const void* fn, int64_t rows, cudaStream_t stream)
 // length 65..1009 and not a multiple of 16 (shorter ones go to the spans; at
 // most 64 chunks a row, whatever its offset),
 // dy, x and dx at the same address modulo 16 (x's is hb0).  The variant is
-// the narrowest that holds the longest chunk span of a row: two rows per warp
-// up to 16 chunks, then one row per warp with one or two (fp32 only) chunks a
-// lane.  As
+// the narrowest that holds the longest chunk span of a row: four rows per warp
+// up to 8 chunks, two up to 16, then one row per warp with one or two (fp32
+// only) chunks a lane.  As
 // many blocks as are resident, at most max_partials (one column partial each).
-// RR_LNS=0 turns these kernels off; RR_LNS_V=0..2 forces a variant (tuning
+// RR_LNS=0 turns these kernels off; RR_LNS_V=0..3 forces a variant (tuning
 // aids).
 struct LnsPlan {
   const void* fn = nullptr;
@@ -1140,7 +1140,9 @@ static rr_status lns_plan(bool rms, rr_dtype dt, int64_t rows, int64_t cols, int
   const int64_t P = 16 / a;  // 2, 4 or 8 for 2- and 4-byte elements: divides kLnsWarps
   const int64_t nch_max = (rb + 15 + 15) / 16;  // chunks a row touches at worst
   if (nch_max > 64) return RR_ERR_INVALID_ARG;
-  int v = nch_max <= 16 ? 0 : nch_max <= 32 ? 1 : 2;
+  static constexpr int64_t kCap[4] = {8, 16, 32, 64};  // chunks a row each variant holds
+  static constexpr int64_t kRpw[4] = {4, 2, 1, 1};      // rows a warp holds at once
+  int v = nch_max <= 8 ? 0 : nch_max <= 16 ? 1 : nch_max <= 32 ? 2 : 3;
   // Measured on 2^24-element tensors against the row-group kernels: fp32 rows
   // won at every length tried (17 columns 128.0 -> 118.5 us, 45: 91.6 -> 51.3,
   // 97: 76.1 -> 45.6, 127: 60.6 -> 57.1, 250: 58.6 -> 35.5; LayerNorm), so
@@ -1151,11 +1153,10 @@ static rr_status lns_plan(bool rms, rr_dtype dt, int64_t rows, int64_t cols, int
   // arrays and the element-wise head and tail chunks cost twice as much.
   // bf16 rows of more than 32 chunks are left out: a two-chunk variant needs
   // ~170 registers there (500 columns 37.0 -> 62.8 us) and is not built.
-  const int64_t cap = v == 0 ? 16 : v == 1 ? 32 : 64;
-  bool take = dt == RR_F32 || (4 * nch_max >= 3 * cap && v < 2);
-  if (const char* f = std::getenv("RR_LNS_V"); f != nullptr && f[0] >= '0' && f[0] <= '2') {
+  bool take = dt == RR_F32 || (4 * nch_max >= 3 * kCap[v] && v < 3);
+  if (const char* f = std::getenv("RR_LNS_V"); f != nullptr && f[0] >= '0' && f[0] <= '3') {
     const int fv = f[0] - '0';
-    if (nch_max <= (fv == 0 ? 16 : fv == 1 ? 32 : 64) && !(dt == RR_BF16 && fv == 2)) {
+    if (nch_max <= kCap[fv] && !(dt == RR_BF16 && fv >= 3)) {
       v = fv;
       take = true;
     }
@@ -1176,7 +1177,7 @@ static rr_status lns_plan(bool rms, rr_dtype dt, int64_t rows, int64_t cols, int
     if (e != cudaSuccess || occ <= 0)
       return fail(RR_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
   }
-  const int64_t rpw = v == 0 ? 2 : 1;  // rows a warp holds at once
+  const int64_t rpw = kRpw[v];
   int64_t grid = cdiv(rows, rpw * rr::kLnsWarps);
   if (grid > (int64_t)di->sms * occ) grid = (int64_t)di->sms * occ;
   if (grid > max_partials) grid = max_partials;

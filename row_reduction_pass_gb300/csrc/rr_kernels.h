@@ -118,11 +118,10 @@ LncKernels lnc_kernels_f32();
 LncKernels lnc_kernels_bf16();
 
 // LayerNorm / RMSNorm backward of short misaligned rows by phase class
-// (rr_lns.cuh): bwd[rms][v], v = 0 two rows per warp (16 lanes, one chunk
-// each: rows of at most 16 chunks), 1 one row per warp (32 chunks), 2 one row
-// per warp with two chunks a lane (64 chunks; fp32 only, null for bf16).
-// Blocks of kLnsWarps warps,
-// one column partial ([planes][cols] floats) per block.
+// (rr_lns.cuh): bwd[rms][v], v = (lanes a row, chunks a lane): 0 (8, 1),
+// 1 (16, 1), 2 (32, 1), and fp32 only (null for bf16) 3 (32, 2); a row of up
+// to lanes x chunks 16-byte chunks, 32 / lanes rows a warp.  Blocks of
+// kLnsWarps warps, one column partial ([planes][cols] floats) per block.
 constexpr int kLnsWarps = 8;
 struct LnsGeo {
   int64_t rows;
@@ -132,7 +131,7 @@ struct LnsGeo {
   int32_t rb;   // bytes per row
 };
 struct LnsKernels {
-  const void* bwd[2][3];
+  const void* bwd[2][4];
 };
 LnsKernels lns_kernels_f32();
 LnsKernels lns_kernels_bf16();

@@ -14,7 +14,7 @@
 // class only, so its lanes own fixed aligned 16-byte chunks of every row it
 // sees -- chunk j holds columns W j - h / E .. W j - h / E + W - 1 -- and
 // their column partials stay in registers, with gamma read once per launch.
-// SUB lanes hold a row (SUB = 16: a warp takes two rows at a time), NQ chunks
+// SUB lanes hold a row (SUB = 8 or 16: a warp takes 4 or 2 rows at a time), NQ chunks
 // each, and the next row's chunks while they compute one.  Full chunks are single 16-byte loads and stores; the head and tail
 // chunk of a row move element by element (nothing outside the row is read).
 // Columns outside the row hold dy = 0 and xhat = 0 and add nothing.  A row
@@ -175,8 +175,8 @@ __global__ void __launch_bounds__(32 * kLnsWarps)
     }
   }
 
-  // the warp's column partials: rows of the two half-warps added (SUB = 16),
-  // then each column written once into the warp's shared-memory row
+  // the warp's column partials: the rows it held side by side added (SUB <
+  // 32), then each column written once into the warp's shared-memory row
   float* mine = lns_part + (size_t)warp * kPlanes * C;
   for (int i = lane; i < kPlanes * C; i += 32) mine[i] = 0.f;
   __syncwarp();
@@ -184,11 +184,13 @@ __global__ void __launch_bounds__(32 * kLnsWarps)
   for (int q = 0; q < NQ; ++q) {
 #pragma unroll
     for (int e = 0; e < W; ++e) {
-      if constexpr (RPW == 2) {
-        const float og = __shfl_xor_sync(0xffffffffu, ag[q][e], 16);
-        const float ob = __shfl_xor_sync(0xffffffffu, ab[q][e], 16);
-        ag[q][e] = sr == 0 ? ag[q][e] + og : og + ag[q][e];
-        ab[q][e] = sr == 0 ? ab[q][e] + ob : ob + ab[q][e];
+#pragma unroll
+      for (int o = 16; o >= SUB; o >>= 1) {  // the warp's rows, lower lanes first
+        const float og = __shfl_xor_sync(0xffffffffu, ag[q][e], o);
+        const float ob = __shfl_xor_sync(0xffffffffu, ab[q][e], o);
+        const bool lo = (lane & o) == 0;
+        ag[q][e] = lo ? ag[q][e] + og : og + ag[q][e];
+        ab[q][e] = lo ? ab[q][e] + ob : ob + ab[q][e];
       }
       const int col = W * (sl + SUB * q) + e - hc;
       if (sr == 0 && has[q] && col >= 0 && col < C) {
@@ -207,17 +209,23 @@ __global__ void __launch_bounds__(32 * kLnsWarps)
   }
 }
 
-// bf16 has no two-chunk variant (170 registers; slower than the row groups).
+// Variants (SUB lanes a row, NQ chunks a lane): 0 (8, 1), 1 (16, 1), 2 (32, 1)
+// and, fp32 only, 3 (32, 2).  Two chunks a lane at 8 or 16 lanes a row were
+// slower for the LayerNorm (fp32 31 columns 69.0 against 75.4 us), and
+// two-chunk bf16 variants need ~170 registers and were slower than the row
+// groups.
 template <int DT>
 LnsKernels make_lns_set() {
   LnsKernels k{};
-  k.bwd[0][0] = (const void*)lns_bwd_kernel<DT, false, 16, 1>;
-  k.bwd[0][1] = (const void*)lns_bwd_kernel<DT, false, 32, 1>;
-  k.bwd[1][0] = (const void*)lns_bwd_kernel<DT, true, 16, 1>;
-  k.bwd[1][1] = (const void*)lns_bwd_kernel<DT, true, 32, 1>;
+  k.bwd[0][0] = (const void*)lns_bwd_kernel<DT, false, 8, 1>;
+  k.bwd[0][1] = (const void*)lns_bwd_kernel<DT, false, 16, 1>;
+  k.bwd[0][2] = (const void*)lns_bwd_kernel<DT, false, 32, 1>;
+  k.bwd[1][0] = (const void*)lns_bwd_kernel<DT, true, 8, 1>;
+  k.bwd[1][1] = (const void*)lns_bwd_kernel<DT, true, 16, 1>;
+  k.bwd[1][2] = (const void*)lns_bwd_kernel<DT, true, 32, 1>;
   if constexpr (DT == kF32) {
-    k.bwd[0][2] = (const void*)lns_bwd_kernel<DT, false, 32, 2>;
-    k.bwd[1][2] = (const void*)lns_bwd_kernel<DT, true, 32, 2>;
+    k.bwd[0][3] = (const void*)lns_bwd_kernel<DT, false, 32, 2>;
+    k.bwd[1][3] = (const void*)lns_bwd_kernel<DT, true, 32, 2>;
   }
   return k;
 }
