@@ -121,25 +121,38 @@ __global__ void __launch_bounds__(32 * kLnsWarps)
     const float rs = cur.rs, mu = cur.mu;
     const bool live = act && rs != 0.f;
     const int64_t rowoff = r * (int64_t)geo.rb - h;
+    // element pairs in packed f32x2 arithmetic; g = dy gamma stays a scalar
+    // round-to-nearest product
     float xh[NQ][W], dv[NQ][W];
-    float s1 = 0.f, s2 = 0.f;
+    float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
       const int j = sl + SUB * q;
+      float xv[W];
 #pragma unroll
       for (int e = 0; e < W; ++e) {
         const int col = W * j + e - hc;
         // columns outside the row: x = mean (xhat = 0), dy = 0
         const bool in = live && has[q] && col >= 0 && col < C;
-        const float xv = in ? chunk_get<DT>(cur.x[q], e) : mu;
-        const float dyv = in ? chunk_get<DT>(cur.dy[q], e) : 0.f;
-        xh[q][e] = RMS ? xv * rs : (xv - mu) * rs;
-        dv[q][e] = dyv;
-        const float g = __fmul_rn(dyv, gm[q][e]);
-        if constexpr (!RMS) s1 += g;
-        s2 = fmaf(g, xh[q][e], s2);
+        xv[e] = in ? chunk_get<DT>(cur.x[q], e) : mu;
+        dv[q][e] = in ? chunk_get<DT>(cur.dy[q], e) : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < W; e += 2) {
+        if constexpr (RMS) {
+          mul2(xh[q][e], xh[q][e + 1], xv[e], xv[e + 1], rs, rs);
+        } else {
+          float t0, t1;
+          add2(t0, t1, xv[e], xv[e + 1], -mu, -mu);
+          mul2(xh[q][e], xh[q][e + 1], t0, t1, rs, rs);
+        }
+        const float g0 = __fmul_rn(dv[q][e], gm[q][e]);
+        const float g1 = __fmul_rn(dv[q][e + 1], gm[q][e + 1]);
+        if constexpr (!RMS) add2(s1a, s1b, s1a, s1b, g0, g1);
+        fma2(s2a, s2b, g0, g1, xh[q][e], xh[q][e + 1], s2a, s2b);
       }
     }
+    float s1 = s1a + s1b, s2 = s2a + s2b;
     // the row's sums over its SUB lanes (every lane ends with the same bits)
 #pragma unroll
     for (int o = SUB / 2; o >= 1; o >>= 1) {
@@ -156,11 +169,17 @@ __global__ void __launch_bounds__(32 * kLnsWarps)
       const int j = sl + SUB * q;
       float f[W];
 #pragma unroll
-      for (int e = 0; e < W; ++e) {
-        const float g = __fmul_rn(dv[q][e], gm[q][e]);
-        f[e] = live ? fmaf(xh[q][e], -b, g - a) * rs : 0.f;
-        ag[q][e] = fmaf(dv[q][e], xh[q][e], ag[q][e]);
-        if constexpr (!RMS) ab[q][e] += dv[q][e];
+      for (int e = 0; e < W; e += 2) {
+        const float g0 = __fmul_rn(dv[q][e], gm[q][e]);
+        const float g1 = __fmul_rn(dv[q][e + 1], gm[q][e + 1]);
+        float t0, t1;
+        add2(t0, t1, g0, g1, -a, -a);
+        fma2(t0, t1, xh[q][e], xh[q][e + 1], -b, -b, t0, t1);
+        mul2(f[e], f[e + 1], t0, t1, rs, rs);
+        if (!live) f[e] = f[e + 1] = 0.f;  // a masked row: dx = 0
+        fma2(ag[q][e], ag[q][e + 1], dv[q][e], dv[q][e + 1], xh[q][e], xh[q][e + 1], ag[q][e],
+             ag[q][e + 1]);
+        if constexpr (!RMS) add2(ab[q][e], ab[q][e + 1], ab[q][e], ab[q][e + 1], dv[q][e], dv[q][e + 1]);
       }
       const int64_t off = rowoff + 16 * (int64_t)j;
       if (full[q]) {
