@@ -641,11 +641,14 @@ def run_profile_case(args):
         fn = lambda: rr.rr_softmax_xent_fwd_bwd(x, lab, loss, x)  # noqa: E731
     elif args.profile == "attention":
         # causal attention, 8 batches x 16 heads x 512 queries; --profile-rows
-        # gives the head dimension (64 by default)
+        # gives the head dimension (64 by default), --profile-seq the queries
+        # (4096: 32 heads, the tensor-bound sweep shape)
         d_head = args.profile_rows or 64
-        q, k, v = (bf16(a) for a in synth.attn_inputs(128, 512, d_head, 31 + d_head))
+        seq = args.profile_seq or 512
+        heads = 128 if seq == 512 else max(1, (32 * 4096) // seq)
+        q, k, v = (bf16(a) for a in synth.attn_inputs(heads, seq, d_head, 31 + d_head))
         o = torch.empty_like(q)
-        lse = torch.empty((128, 512), device=dev)
+        lse = torch.empty((heads, seq), device=dev)
         fn = lambda: rr.rr_attention_fwd(q, k, v, o, lse, causal=True)  # noqa: E731
     elif args.profile == "softmax":
         sm = synth.make("softmax_bf16_causal_65536x512")
@@ -908,6 +911,7 @@ def main():
                     default=None,
                     help="run only this kernel (for ncu captures of one kernel)")
     ap.add_argument("--profile-rows", type=int, default=0)
+    ap.add_argument("--profile-seq", type=int, default=0, help="queries for --profile attention")
     ap.add_argument("--profile-workload", default="", help="LayerNorm workload name for --profile")
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload and sweep case separately (one JSON line each)")
