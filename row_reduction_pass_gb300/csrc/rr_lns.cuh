@@ -14,10 +14,13 @@
 // class only, so its lanes own fixed aligned 16-byte chunks of every row it
 // sees -- chunk j holds columns W j - h / E .. W j - h / E + W - 1 -- and
 // their column partials stay in registers, with gamma read once per launch.
-// SUB lanes hold a row (SUB = 8 or 16: a warp takes 4 or 2 rows at a time), NQ chunks
-// each, and the next row's chunks while they compute one.  Full chunks are single 16-byte loads and stores; the head and tail
-// chunk of a row move element by element (nothing outside the row is read).
-// Columns outside the row hold dy = 0 and xhat = 0 and add nothing.  A row
+// SUB lanes hold a row (SUB = 8, 16 or 32: a warp takes 4, 2 or 1 rows at a
+// time), NQ chunks each, and the next row's chunks while they compute one.
+// Full chunks are single 16-byte loads and stores; the head and tail chunk of
+// a row move element by element (nothing outside the row is read or written).
+// Element pairs use packed f32x2 arithmetic, but g = dy gamma stays a scalar
+// round-to-nearest product.  Columns outside the row hold dy = 0 and
+// xhat = 0 and add nothing.  A row
 // with rstd = 0 (masked by the forward) gets dx = 0 and adds nothing.  At the
 // end each block adds its warps' column partials in a fixed order (warp 0..7)
 // into its row of the workspace, [gridDim.x][planes][cols] floats, which
@@ -179,7 +182,8 @@ __global__ void __launch_bounds__(32 * kLnsWarps)
         if (!live) f[e] = f[e + 1] = 0.f;  // a masked row: dx = 0
         fma2(ag[q][e], ag[q][e + 1], dv[q][e], dv[q][e + 1], xh[q][e], xh[q][e + 1], ag[q][e],
              ag[q][e + 1]);
-        if constexpr (!RMS) add2(ab[q][e], ab[q][e + 1], ab[q][e], ab[q][e + 1], dv[q][e], dv[q][e + 1]);
+        if constexpr (!RMS)
+          add2(ab[q][e], ab[q][e + 1], ab[q][e], ab[q][e + 1], dv[q][e], dv[q][e + 1]);
       }
       const int64_t off = rowoff + 16 * (int64_t)j;
       if (full[q]) {
