@@ -909,8 +909,9 @@ static rr_status bad_tier() { return fail(RR_ERR_INVALID_ARG, "RR_FORCE_TIER mus
 static rr_status no_span(int64_t cols) {
   return fail(RR_ERR_INVALID_ARG,
               "tier 0 (spans) takes 16-byte aligned tensors with short rows whose byte length "
-              "is not a multiple of 16 (up to 448 bytes; 224 for the softmax backward, 64 for "
-              "the norm backward, fewer columns for some operations), not %lld columns",
+              "is not a multiple of 16 (up to 448 bytes; 224 for the softmax backward, 64 "
+              "(bf16 96) for the norm backward, fewer columns for some operations), not %lld "
+              "columns",
               (long long)cols);
 }
 
@@ -955,11 +956,16 @@ static rr_status span_plan(rr_dtype dt, int mode, int64_t rows, int64_t cols, bo
   //    (fp32 97: 41.5 -> 33.7 us; bf16 131 lost, 32.6 -> 34.9, and 197 lost,
   //    29.3 -> 38.6: a lane's serial pass over that many columns with one
   //    block of spans per SM);
-  //  - LayerNorm / RMSNorm backward: up to 64 bytes (two tensors, and the
-  //    column partials' second pass).
+  //  - LayerNorm / RMSNorm backward: up to 64 bytes, bf16 96 (two tensors,
+  //    and the column partials' second pass).
   // RR_SPAN_MAX_BYTES replaces these limits by one byte limit for the
   // operations but the norm backward (tuning aid).
-  int64_t lim = 64, cmax = INT64_MAX;
+  // the norm backward: 64 bytes, bf16 96 (at most 48 columns, two column
+  // slots a lane beyond 32; against the phase-class kernel bf16 33 columns
+  // 69.7 -> 51.2 us, 47 columns 55.0 against 54.4 us, 63 columns lost, 53.1
+  // against 66.6 us; fp32 25 and 31 columns were faster there too, 43.0 /
+  // 65.8 against 58.4 / 80.3 us)
+  int64_t lim = E == 2 ? 96 : 64, cmax = INT64_MAX;
   switch (mode) {
     case 0: case 1: lim = 448; cmax = 160; break;
     case 2: lim = 448; cmax = 200; break;

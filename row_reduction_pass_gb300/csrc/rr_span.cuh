@@ -359,15 +359,16 @@ __global__ void __launch_bounds__(32 * kSpanWarps)
   cp_async_wait<0>();
 }
 
-// LayerNorm (RMS = false) or RMSNorm backward of short rows (C x element size
-// <= 64 bytes, so C <= 32; with longer rows two tensors' spans leave room for
-// one block per SM and the row-group kernels are faster).  Per stage a warp
+// LayerNorm (RMS = false) or RMSNorm backward of short rows (at most 64 bytes,
+// bf16 96 bytes, so C <= 48; the column pass holds up to 64 columns; with
+// longer rows two tensors' spans leave room for one block per SM and the
+// other kernels are faster).  Per stage a warp
 // copies spans of dy and x and the span's row statistics (mean, rstd: by
 // cp.async when they are 16-byte aligned, else loaded into the same buffer).
 // Two passes over the staged span:
 //  - columns: the column partials sum dy*xhat (and sum dy) in registers, lane
-//    l taking column l % C of rows l / C, l / C + 32 / C, ...: consecutive
-//    lanes read consecutive elements;
+//    l taking column l % C of rows l / C, l / C + 32 / C, ... (C > 32: columns
+//    l and l + 32 of every row): consecutive lanes read consecutive elements;
 //  - rows: lane l takes rows l, l + 32, ...: S1 = sum g, S2 = sum g*xhat with
 //    g = dy*gamma, and dx = rstd*((g - S1/C) - xhat*S2/C), written over dy in
 //    shared memory and stored out as 16-byte blocks.
@@ -397,12 +398,17 @@ __global__ void __launch_bounds__(32 * kSpanWarps, 3)
   for (int j = threadIdx.x; j < C; j += blockDim.x) sg[j] = ld_elem_cached<DT>(p.gamma + (int64_t)j * E);
   __syncthreads();
 
-  // column pass geometry: nph row phases of C lanes
-  const int nph = 32 / C;
-  const int ph = lane / C;
-  const int j0 = lane % C;
+  // column pass geometry: for C <= 32, nph row phases of C lanes (lane l takes
+  // column l % C of rows l / C, l / C + nph, ...); for 32 < C <= 64 one phase,
+  // lane l taking columns l and l + 32 of every row
+  const bool wide = C > 32;
+  const int nph = wide ? 1 : 32 / C;
+  const int ph = wide ? 0 : lane / C;
+  const int j0 = wide ? lane : lane % C;
+  const int j1 = lane + 32;
   const bool on = ph < nph;
-  float ag = 0.f, ab = 0.f;
+  const bool on1 = wide && j1 < C;
+  float ag = 0.f, ab = 0.f, ag1 = 0.f, ab1 = 0.f;
 
   const int64_t total = geo.rows * (int64_t)C * E;
   auto span_bytes = [&](int64_t s) -> int64_t {
@@ -468,6 +474,13 @@ __global__ void __launch_bounds__(32 * kSpanWarps, 3)
         const float xh = RMS ? xv * rs : (xv - mu) * rs;
         ag = fmaf(dyv, xh, ag);
         if (!RMS) ab += dyv;
+        if (on1) {
+          const float dy1 = span_ld<DT>(gbuf, i * C + j1);
+          const float x1 = span_ld<DT>(xbuf, i * C + j1);
+          const float xh1 = RMS ? x1 * rs : (x1 - mu) * rs;
+          ag1 = fmaf(dy1, xh1, ag1);
+          if (!RMS) ab1 += dy1;
+        }
       }
     __syncwarp();
     for (int k = 0; k < geo.rpl; ++k) {
@@ -508,18 +521,23 @@ __global__ void __launch_bounds__(32 * kSpanWarps, 3)
   }
   cp_async_wait<0>();
   __syncthreads();
-  // the lanes' partials, [warps][planes][32] floats over the (now idle) span
-  // buffers: slot lane holds column j0 of phase ph
+  // the lanes' partials, [warps][planes][64] floats over the (now idle) span
+  // buffers: slot lane holds column j0 of phase ph, slot 32 + lane (wide
+  // rows) column lane + 32
   float* red = reinterpret_cast<float*>(smem);
-  red[(warp * kPlanes) * 32 + lane] = ag;
-  if (!RMS) red[(warp * kPlanes + 1) * 32 + lane] = ab;
+  red[(warp * kPlanes) * 64 + lane] = ag;
+  red[(warp * kPlanes) * 64 + 32 + lane] = ag1;
+  if (!RMS) {
+    red[(warp * kPlanes + 1) * 64 + lane] = ab;
+    red[(warp * kPlanes + 1) * 64 + 32 + lane] = ab1;
+  }
   __syncthreads();
   float* out = p.ws + (int64_t)blockIdx.x * kPlanes * C;
   for (int idx = threadIdx.x; idx < kPlanes * C; idx += blockDim.x) {
     const int pl = idx / C, j = idx % C;
     float t = 0.f;
     for (int w = 0; w < kSpanWarps; ++w)
-      for (int q = 0; q < nph; ++q) t += red[(w * kPlanes + pl) * 32 + q * C + j];
+      for (int q = 0; q < nph; ++q) t += red[(w * kPlanes + pl) * 64 + q * C + j];
     out[idx] = t;
   }
 }

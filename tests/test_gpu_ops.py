@@ -114,16 +114,19 @@ def test_layernorm_eps_zero_and_large():
     check_ln(x, g, b, dy, 10.0, "f32")
 
 
-SHORT = [("f32", c) for c in (1, 3, 17, 31, 32)] + [("bf16", c) for c in (1, 5, 32, 33, 47, 64)]
+SHORT = [("f32", c) for c in (1, 3, 17, 31, 32)] + \
+        [("bf16", c) for c in (1, 5, 32, 33, 47, 63, 64)]
 
 
 @pytest.mark.parametrize("dtype,cols", SHORT)
 @pytest.mark.parametrize("rows", [1, 37, 4099, 60001, 1000003])
 @pytest.mark.parametrize("layout", ["plain", "stats_misaligned", "dx_over_dy", "dx_over_x"])
 def test_layernorm_bwd_short_rows(dtype, cols, rows, layout):
-    """Rows of at most 128 bytes: spans of rows per warp (a million rows: several
-    spans per warp through both stages), ragged last span, statistics staged
-    with the span (16-byte aligned) or loaded, dx in place."""
+    """Short rows: spans of rows per warp up to 64 bytes, bf16 96 (a million
+    rows: several spans per warp through both stages; bf16 rows of 33..47
+    columns hold two column slots a lane), the phase-class kernel beyond,
+    ragged last span, statistics staged with the span (16-byte aligned) or
+    loaded, dx in place."""
     if rows * cols > 400000 and layout != "plain":
         pytest.skip("large shapes run in the plain layout only")
     if rows > 100000 and cols > 5:

@@ -54,7 +54,7 @@ def holds(op: str, t: int, cols: int, e: int) -> bool:
             return rb <= 224
         if op in ("ln_fwd", "rms_fwd"):
             return rb <= 448 and (e == 4 or cols <= 128)
-        return rb <= 64  # norm backward
+        return rb <= (96 if e == 2 else 64)  # norm backward
     if t == 1:
         return True  # every row length used here fits one row group
     if t == 2:
