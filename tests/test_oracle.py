@@ -303,3 +303,41 @@ def test_brute_force_tiny_against_torch():
         np.testing.assert_allclose(dx, xt.grad.numpy(), rtol=1e-8, atol=1e-10)
         np.testing.assert_allclose(dg, gt.grad.numpy(), rtol=1e-9, atol=1e-11)
         np.testing.assert_allclose(db, bt.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------- rows of one column ----
+
+def test_one_column_closed_forms():
+    """A one-element row is its own maximum, sum and moments: softmax 1,
+    log-softmax 0, cross-entropy loss 0 and dlogits 0 at the label (1 for a
+    label out of range, whose loss is NaN), a -inf or NaN row masked to 0, +inf
+    giving NaN; LayerNorm mean = x, rstd = 1 / sqrt(eps), y = beta; RMSNorm
+    rstd = 1 / sqrt(x^2 + eps); the backward's dx = rstd (g - g - xhat g xhat)
+    = 0 for LayerNorm.  These are the values the elementwise kernels write."""
+    x = f32([[2.5], [-7.0], [0.0], [1e8], [-np.inf], [np.nan], [np.inf]])
+    live = slice(0, 4)
+    y = oracle.softmax(x)
+    z = oracle.log_softmax(x)
+    assert np.all(y[live] == 1.0) and np.all(z[live] == 0.0)
+    assert np.all(y[4:6] == 0.0) and np.all(z[4:6] == 0.0)
+    assert np.isnan(y[6, 0]) and np.isnan(z[6, 0])
+    lab = np.array([0, 0, 3, -100, 0, 0, 0], np.int32)
+    loss, dl, bad = oracle.xent(x, lab)
+    assert loss[0] == 0.0 and loss[1] == 0.0 and dl[0, 0] == 0.0 and dl[1, 0] == 0.0
+    assert np.isnan(loss[2]) and dl[2, 0] == 1.0 and bad == 1
+    assert loss[3] == 0.0 and dl[3, 0] == 0.0          # ignored
+    assert loss[4] == 0.0 and loss[5] == 0.0           # masked rows
+    assert np.isnan(loss[6]) and np.isnan(dl[6, 0])    # +inf
+    xs = f32([[2.5], [-7.0], [0.25]])
+    g, b = f32([1.5]), f32([-0.25])
+    yl, mean, rstd = oracle.ln_fwd(xs, g, b, 1e-5)
+    assert np.allclose(mean, xs[:, 0], rtol=0, atol=0)
+    assert np.allclose(rstd, 1.0 / math.sqrt(1e-5), rtol=1e-12)
+    assert np.allclose(yl, -0.25, rtol=0, atol=1e-12)
+    yr, rr_ = oracle.rms_fwd(xs, g, 1e-5)
+    assert np.allclose(rr_, 1.0 / np.sqrt(xs[:, 0].astype(np.float64) ** 2 + 1e-5), rtol=1e-12)
+    assert np.allclose(yr[:, 0], xs[:, 0] * rr_ * 1.5, rtol=1e-12)
+    dy = f32([[0.5], [-1.0], [2.0]])
+    dx, dg, db, _, _ = oracle.ln_bwd(dy, xs, mean, rstd, g)
+    assert np.allclose(dx, 0.0, atol=1e-12)
+    assert np.allclose(db, dy.sum(), rtol=1e-12) and np.allclose(dg, 0.0, atol=1e-12)
